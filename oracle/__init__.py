@@ -1,0 +1,210 @@
+"""fp64 CPU oracle for cartridge attention (TEST INFRASTRUCTURE ONLY).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path never routes through it.
+
+The arithmetic lives in ``cart_oracle.c`` (plain loops in fp64, OpenMP over
+independent (batch, head) problems); this module only compiles it with gcc and
+marshals numpy arrays into it.  See that file's header for what is computed
+and which passage of the Cartridges guide each part follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cart_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libcart_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libcart_oracle.so`` (gcc, -O2,
+    OpenMP when available; never -ffast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Geom(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("n", ctypes.c_int), ("Hq", ctypes.c_int),
+                ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("p", ctypes.c_int),
+                ("frozen_prefix", ctypes.c_int), ("scale", ctypes.c_double),
+                ("theta", ctypes.c_double)]
+
+
+_D = ctypes.POINTER(ctypes.c_double)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            L.cart_oracle_fwd.restype = ctypes.c_int
+            L.cart_oracle_fwd.argtypes = [ctypes.POINTER(_Geom)] + [_D] * 7 + [ctypes.c_int] * 4
+            L.cart_oracle_bwd.restype = ctypes.c_int
+            L.cart_oracle_bwd.argtypes = [ctypes.POINTER(_Geom)] + [_D] * 11 + [ctypes.c_int] * 2
+            L.cart_oracle_decode.restype = ctypes.c_int
+            L.cart_oracle_decode.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_double] * 2
+                                             + [_D] * 7 + [ctypes.c_int,
+                                                           ctypes.POINTER(ctypes.c_int), _D])
+            L.cart_oracle_rope.restype = None
+            L.cart_oracle_rope.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_double, ctypes.c_double, ctypes.c_int]
+            L.cart_oracle_write_to_cache.restype = None
+            L.cart_oracle_write_to_cache.argtypes = [
+                ctypes.POINTER(ctypes.c_float), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.POINTER(ctypes.c_uint16), ctypes.c_longlong, ctypes.c_int]
+            L.cart_oracle_num_threads.restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def num_threads() -> int:
+    return int(lib().cart_oracle_num_threads())
+
+
+def _f64(x) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta) -> _Geom:
+    return _Geom(B, n, Hq, Hkv, d, p, frozen_prefix, float(scale), float(theta))
+
+
+def fwd(q, k, v, kc, vc, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
+        heads=None, rows=None):
+    """Forward of cartridge attention.
+
+    q ``[B, n, Hq, d]``, k/v ``[B, n, Hkv, d]``, kc/vc ``[p, Hkv, d]`` (any
+    float arrays; read as fp64).  Returns ``(o [B, n, Hq, d], lse [B, Hq, n])``.
+    ``heads=(lo, hi)`` / ``rows=(lo, hi)`` restrict which outputs are computed
+    (the rest are NaN)."""
+    q, k, v, kc, vc = (_f64(t) for t in (q, k, v, kc, vc))
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if p is None:
+        p = kc.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if kc.size == 0:
+        kc = np.zeros((1, Hkv, d))
+        vc = np.zeros((1, Hkv, d))
+    o = np.full((B, n, Hq, d), np.nan)
+    lse = np.full((B, Hq, n), np.nan)
+    h_lo, h_hi = heads if heads is not None else (0, Hq)
+    i_lo, i_hi = rows if rows is not None else (0, n)
+    # the forward does not depend on which rows are frozen
+    g = _geom(B, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta)
+    rc = lib().cart_oracle_fwd(ctypes.byref(g), _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
+                               _ptr(vc), _ptr(o), _ptr(lse), h_lo, h_hi, i_lo, i_hi)
+    if rc != 0:
+        raise ValueError(f"cart_oracle_fwd failed ({rc})")
+    return o, lse
+
+
+def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
+        kv_heads=None):
+    """Gradients of ``sum(dout * o)``: returns ``dq, dk, dv, dkc, dvc`` (fp64),
+    dkc/dvc summed over the batch with rows ``< frozen_prefix`` exactly 0.
+    ``kv_heads=(lo, hi)`` restricts the work to those kv heads and the query
+    heads reading them (other entries are NaN)."""
+    q, k, v, kc, vc, dout = (_f64(t) for t in (q, k, v, kc, vc, dout))
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if p is None:
+        p = kc.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    pc = max(p, 1)
+    if kc.size == 0:
+        kc = np.zeros((1, Hkv, d))
+        vc = np.zeros((1, Hkv, d))
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    dkc = np.full((pc, Hkv, d), np.nan)
+    dvc = np.full((pc, Hkv, d), np.nan)
+    lo, hi = kv_heads if kv_heads is not None else (0, Hkv)
+    g = _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta)
+    rc = lib().cart_oracle_bwd(ctypes.byref(g), _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
+                               _ptr(vc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(dkc), _ptr(dvc), lo, hi)
+    if rc != 0:
+        raise ValueError(f"cart_oracle_bwd failed ({rc})")
+    return dq, dk, dv, dkc[:p], dvc[:p]
+
+
+def decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6):
+    """One decode step behind a shared cartridge.  Returns
+    ``(o [B, Hq, d], k_cache', v_cache')`` where the caches have the new
+    token's rotated key / value written at row ``lens[b]``."""
+    q, k_new, v_new, kc, vc = (_f64(t) for t in (q, k_new, v_new, kc, vc))
+    kcache = _f64(k_cache).copy()
+    vcache = _f64(v_cache).copy()
+    B, Hq, d = q.shape
+    Hkv = k_new.shape[1]
+    p = kc.shape[0]
+    rows = kcache.shape[1]
+    lens = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if kc.size == 0:
+        kc = np.zeros((1, Hkv, d))
+        vc = np.zeros((1, Hkv, d))
+    o = np.full((B, Hq, d), np.nan)
+    rc = lib().cart_oracle_decode(B, Hq, Hkv, d, p, float(scale), float(theta), _ptr(q),
+                                  _ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(kcache),
+                                  _ptr(vcache), rows,
+                                  lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _ptr(o))
+    if rc != 0:
+        raise ValueError(f"cart_oracle_decode failed ({rc})")
+    return o, kcache, vcache
+
+
+def rope(x, pos0, *, theta=1.0e6, inverse=False):
+    """Rotate ``x [rows, H, d]`` row r at position ``pos0 + r``."""
+    x = _f64(x)
+    rows, H, d = x.shape
+    out = np.empty_like(x)
+    lib().cart_oracle_rope(_ptr(x), _ptr(out), rows, H, d, float(pos0), float(theta),
+                           1 if inverse else 0)
+    return out
+
+
+def write_to_cache(src_f32, dst_u16, dst_row0=0):
+    """f32 ``[p, Hkv, d]`` -> bf16 bit patterns written into ``dst_u16``
+    (``[rows, Hkv, d]`` uint16, modified in place) from row ``dst_row0``."""
+    src = np.ascontiguousarray(np.asarray(src_f32, dtype=np.float32))
+    p, Hkv, d = src.shape
+    assert dst_u16.dtype == np.uint16 and dst_u16.flags.c_contiguous
+    assert dst_u16.shape[1:] == (Hkv, d) and dst_row0 + p <= dst_u16.shape[0]
+    lib().cart_oracle_write_to_cache(src.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), p,
+                                     Hkv, d,
+                                     dst_u16.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                     Hkv * d, dst_row0)
+    return dst_u16
