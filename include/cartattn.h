@@ -1,0 +1,165 @@
+/*
+ * cartattn.h -- C ABI of the GB300 (sm_103a) cartridge-attention library.
+ *
+ * A cartridge is a trained KV prefix: per layer a [p, kv_head, d] pair of
+ * key/value rows living in KV-cache row space.  Cartridge keys are already
+ * rotated (RoPE) at positions 0..p-1 and are never rotated again; the real
+ * tokens that follow sit at RoPE positions p, p+1, ...  The first
+ * `frozen_prefix` rows (1 by default: the attention sink) are frozen
+ * constants; the remaining rows are trainable leaves.
+ * (Cartridges guide, section "Semantics", parameterization bullet.)
+ *
+ * Attention runs over concat(sink, trainable rows, real-token K/V) along the
+ * sequence with the end-aligned causal mask, source_offset = kv_seq - q_seq:
+ * every query sees every cartridge row and is causal over the real tokens.
+ * Query head h reads kv head h / (Hq / Hkv).
+ * (Cartridges guide, "Semantics", attention bullet.)
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, row-major, innermost last,
+ *     16-byte aligned, owned by the caller.  The library never frees them.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     validate their arguments synchronously on the host, then enqueue work
+ *     asynchronously on `stream`; nothing is written when validation fails.
+ *   - RoPE is the rotate-half form: element j pairs with j + d/2 at angle
+ *     position * theta^(-2j/d); angles are reduced in fp64 on the device.
+ *   - Return value: CART_OK (0) or a negative cart_status.
+ *   - The library holds no per-call state.  It caches, per process, only the
+ *     CUDA driver entry point used to build TMA descriptors.
+ */
+#ifndef CARTATTN_H_
+#define CARTATTN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define CART_API __attribute__((visibility("default")))
+#else
+#define CART_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cart_status {
+  CART_OK = 0,
+  CART_ERR_GEOMETRY = -1,   /* bad sizes: Hq % Hkv, d not 64/128, p < frozen_prefix, n < 1 ... */
+  CART_ERR_POINTER = -2,    /* NULL or not 16-byte aligned */
+  CART_ERR_DTYPE = -3,      /* dtype not supported for this argument */
+  CART_ERR_WORKSPACE = -4,  /* workspace NULL or smaller than the *_workspace_size() answer */
+  CART_ERR_CUDA = -5,       /* a CUDA runtime / driver call failed (launch, attribute, TMA map) */
+  CART_ERR_DEVICE = -6,     /* current device is not a compute capability 10.3 GPU */
+  CART_ERR_TIMEOUT = -7     /* a kernel gave up waiting (see cart_device_status) */
+} cart_status;
+
+typedef enum cart_dtype { CART_BF16 = 0, CART_F32 = 1 } cart_dtype;
+
+/* Geometry of one training-shape call.
+ *   B      independent sequences sharing ONE cartridge (the packed group)
+ *   n      real tokens per sequence (q_seq); kv_seq = p + n
+ *   Hq     query heads;  Hkv  kv heads;  Hq % Hkv == 0
+ *   d      head dimension, 64 or 128
+ *   p      cartridge rows INCLUDING the frozen sink rows (p >= 0)
+ *   frozen_prefix  leading cartridge rows whose gradient is exactly 0
+ *   scale  softmax scale (normally 1/sqrt(d))
+ *   rope_theta     RoPE base (1e6 for the Qwen3 family)            */
+typedef struct cart_geom {
+  int B, n, Hq, Hkv, d, p, frozen_prefix;
+  float scale;
+  double rope_theta;
+} cart_geom;
+
+/* ------------------------------------------------------------------------
+ * cart_write_to_cache -- write the whole cartridge into a cache, converting
+ * f32 leaf rows to the cache dtype (round to nearest even for bf16).
+ * (Cartridges guide, "Semantics", serving bullet: the prefix is written into
+ * an empty KV cache, converted to the cache dtype, and the cache advances to
+ * p.  The same conversion produces the bf16 shadow the attention kernels
+ * read once per optimizer step.)
+ *   kc, vc        [p, Hkv, d] f32 (device)
+ *   k_dst, v_dst  destination rows; row r of the cartridge goes to row
+ *                 dst_row0 + r, rows are row_stride_elems elements apart
+ *                 (row_stride_elems >= Hkv*d, a multiple of 8)
+ *   dst_dtype     CART_BF16 or CART_F32
+ * Either pair member may be NULL to skip it (not both).                   */
+CART_API int cart_write_to_cache(const float* kc, const float* vc, int p, int Hkv, int d, void* k_dst,
+                        void* v_dst, long long row_stride_elems, int dst_row0,
+                        cart_dtype dst_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cart_attn_fwd -- training forward.
+ *   q   [B, n, Hq, d]  in_dtype, NOT rotated (rotated in the library at p+i)
+ *   k,v [B, n, Hkv, d] in_dtype, k NOT rotated
+ *   kc, vc [p, Hkv, d] cart_dtype (bf16 shadow or f32 leaves), already in
+ *          attended space (never rotated)
+ *   o   [B, n, Hq, d]  in_dtype (output)
+ *   lse [B, Hq, n]     f32 (output): natural-log log-sum-exp of the scaled
+ *                      logits of each query row; the backward consumes it.
+ * Arithmetic: bf16 tensor-core products with f32 accumulation; f32 inputs
+ * are rounded to bf16 on load.  Workspace: cart_attn_fwd_workspace_size().  */
+CART_API size_t cart_attn_fwd_workspace_size(const cart_geom* g, cart_dtype in_dtype,
+                                    cart_dtype cart_dtype);
+CART_API int cart_attn_fwd(const cart_geom* g, cart_dtype in_dtype, cart_dtype cart_dtype,
+                  const void* q, const void* k, const void* v, const void* kc, const void* vc,
+                  void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cart_attn_bwd -- training backward through the concat into the cartridge.
+ * (Cartridges guide, "Semantics": the backward routes gradients through the
+ * concat into the trainable rows; row 0 is the frozen attention sink.)
+ *   q,k,v,kc,vc,o,lse  as given to / returned by cart_attn_fwd
+ *   dout [B, n, Hq, d] in_dtype: gradient of the loss w.r.t. o
+ *   dq [B, n, Hq, d], dk, dv [B, n, Hkv, d]  in_dtype outputs, gradients
+ *        w.r.t. the UN-rotated inputs q and k (the transpose rotation at
+ *        position p+i is applied) and v
+ *   dkc, dvc [p, Hkv, d] f32 outputs: gradient w.r.t. the cartridge rows,
+ *        summed over the batch and over the query heads of each group.
+ *        accumulate == 0 overwrites, 1 adds to the existing contents.  Rows
+ *        < frozen_prefix are set to exactly 0.0 in both modes.
+ * Workspace: cart_attn_bwd_workspace_size().                              */
+CART_API size_t cart_attn_bwd_workspace_size(const cart_geom* g, cart_dtype in_dtype,
+                                    cart_dtype cart_dtype);
+CART_API int cart_attn_bwd(const cart_geom* g, cart_dtype in_dtype, cart_dtype cart_dtype,
+                  const void* q, const void* k, const void* v, const void* kc, const void* vc,
+                  const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                  void* dv, float* dkc, float* dvc, int accumulate, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cart_attn_decode -- one q_seq = 1 decode step for B conversations behind
+ * ONE shared cartridge.  (Cartridges guide, "Semantics", serving bullet: a
+ * normal decode continues at position p with the training-time layout.)
+ *   q      [B, Hq, d]  bf16, new token's query, NOT rotated
+ *   k_new, v_new [B, Hkv, d] bf16, new token's key (NOT rotated) and value
+ *   kc, vc [p, Hkv, d] bf16 shared cartridge (e.g. from cart_write_to_cache)
+ *   k_cache, v_cache [B, cache_rows, Hkv, d] bf16 private caches; rows
+ *          0..len[b]-1 hold already-rotated keys at positions p..p+len[b]-1
+ *   priv_len [B] int32 (device): len[b], 0 <= len[b] < cache_rows (entries
+ *          outside that range are clamped into it)
+ *   o      [B, Hq, d] bf16 (output)
+ * The new token sits at position p + len[b]: its rotated key and its value
+ * are written to private row len[b], then it attends to the p cartridge rows
+ * and private rows 0..len[b].  The caller advances len afterwards.
+ * Workspace: cart_attn_decode_workspace_size().                           */
+CART_API size_t cart_attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int p, int cache_rows);
+CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double rope_theta,
+                     const void* q, const void* k_new, const void* v_new, const void* kc,
+                     const void* vc, void* k_cache, void* v_cache, int cache_rows,
+                     const int* priv_len, void* o, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Human-readable name of a cart_status value (static string). */
+CART_API const char* cart_status_string(int status);
+
+/* Reads (and with clear != 0 resets) the device status word that kernels set
+ * when a bounded wait gives up.  Synchronizes the current device.  Writes the
+ * bits to *bits_out (may be NULL); returns CART_OK, CART_ERR_TIMEOUT when any
+ * bit is set, or CART_ERR_CUDA. */
+CART_API int cart_device_status(unsigned* bits_out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CARTATTN_H_ */

@@ -62,7 +62,7 @@ def lib():
             L.cart_oracle_fwd.restype = ctypes.c_int
             L.cart_oracle_fwd.argtypes = [ctypes.POINTER(_Geom)] + [_D] * 7 + [ctypes.c_int] * 4
             L.cart_oracle_bwd.restype = ctypes.c_int
-            L.cart_oracle_bwd.argtypes = [ctypes.POINTER(_Geom)] + [_D] * 11 + [ctypes.c_int] * 2
+            L.cart_oracle_bwd.argtypes = [ctypes.POINTER(_Geom)] + [_D] * 11 + [ctypes.c_int] * 4
             L.cart_oracle_decode.restype = ctypes.c_int
             L.cart_oracle_decode.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_double] * 2
                                              + [_D] * 7 + [ctypes.c_int,
@@ -128,11 +128,13 @@ def fwd(q, k, v, kc, vc, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
 
 
 def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
-        kv_heads=None):
+        kv_heads=None, rows=None):
     """Gradients of ``sum(dout * o)``: returns ``dq, dk, dv, dkc, dvc`` (fp64),
     dkc/dvc summed over the batch with rows ``< frozen_prefix`` exactly 0.
     ``kv_heads=(lo, hi)`` restricts the work to those kv heads and the query
-    heads reading them (other entries are NaN)."""
+    heads reading them (other entries are NaN).  ``rows=(lo, hi)`` counts only
+    those query rows of the loss: dq outside them is NaN and dk/dv/dkc/dvc
+    hold those rows' contributions (exact for keys no other row sees)."""
     q, k, v, kc, vc, dout = (_f64(t) for t in (q, k, v, kc, vc, dout))
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
@@ -150,10 +152,11 @@ def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0
     dkc = np.full((pc, Hkv, d), np.nan)
     dvc = np.full((pc, Hkv, d), np.nan)
     lo, hi = kv_heads if kv_heads is not None else (0, Hkv)
+    i_lo, i_hi = rows if rows is not None else (0, n)
     g = _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta)
     rc = lib().cart_oracle_bwd(ctypes.byref(g), _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
                                _ptr(vc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                               _ptr(dkc), _ptr(dvc), lo, hi)
+                               _ptr(dkc), _ptr(dvc), lo, hi, i_lo, i_hi)
     if rc != 0:
         raise ValueError(f"cart_oracle_bwd failed ({rc})")
     return dq, dk, dv, dkc[:p], dvc[:p]

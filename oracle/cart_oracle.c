@@ -164,14 +164,17 @@ int cart_oracle_fwd(const cart_ogeom* g, const double* q, const double* k,
 /* ---- backward ------------------------------------------------------------ */
 
 /* Gradients of sum(dout * o) for kv heads [kh_lo, kh_hi) and the query heads
- * that read them.  dq/dk/dv entries of other heads are untouched; dkc/dvc rows
- * of the selected kv heads are overwritten (summed over the batch). */
+ * that read them, counting only the query rows [i_lo, i_hi) of the loss (the
+ * full gradient when the range is [0, n)).  dq of rows outside the range and
+ * entries of other heads are untouched; dk/dv/dkc/dvc of the selected kv
+ * heads are overwritten (cartridge rows summed over the batch). */
 int cart_oracle_bwd(const cart_ogeom* g, const double* q, const double* k,
                     const double* v, const double* kc, const double* vc,
                     const double* dout, double* dq, double* dk, double* dv,
-                    double* dkc, double* dvc, int kh_lo, int kh_hi) {
+                    double* dkc, double* dvc, int kh_lo, int kh_hi, int i_lo, int i_hi) {
     if (!geom_ok(g)) return -1;
     if (kh_lo < 0 || kh_hi > g->Hkv || kh_lo > kh_hi) return -1;
+    if (i_lo < 0 || i_hi > g->n || i_lo > i_hi) return -1;
     const int B = g->B, n = g->n, Hq = g->Hq, Hkv = g->Hkv, d = g->d, p = g->p;
     const int G = Hq / Hkv, kv = p + n;
     const int nk = kh_hi - kh_lo;
@@ -196,7 +199,7 @@ int cart_oracle_bwd(const cart_ogeom* g, const double* q, const double* k,
         }
         build_kv(g, k, v, kc, vc, b, kh, kt, vt);
         for (int h = kh * G; h < (kh + 1) * G; ++h) {
-            for (int i = 0; i < n; ++i) {
+            for (int i = i_lo; i < i_hi; ++i) {
                 const double* qi = q + (((size_t)b * n + i) * Hq + h) * d;
                 const double* gi = dout + (((size_t)b * n + i) * Hq + h) * d;
                 rope_vec(qi, qt, d, (double)(p + i), g->theta, 0);

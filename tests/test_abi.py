@@ -1,0 +1,108 @@
+"""CPU-only checks of the C ABI boundary: the library builds for sm_103a,
+loads, exports every entry point declared in include/cartattn.h, and rejects
+bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from trained_kv_prefix_gb300 import build as cbuild
+from trained_kv_prefix_gb300 import cartattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return cartattn.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "cartattn.h")).read()
+    return sorted(set(re.findall(r"CART_API\s+[\w\s\*]+?\b(cart_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("cart_attn_fwd", "cart_attn_bwd", "cart_attn_decode", "cart_write_to_cache"):
+        assert required in names
+    assert set(names) == set(cartattn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.cart_status_string(0) == b"ok"
+    assert lib.cart_status_string(-1) == b"bad geometry"
+    assert lib.cart_status_string(-7) == b"a kernel gave up waiting"
+    assert lib.cart_status_string(123) == b"unknown status"
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Hq=6, Hkv=4),            # Hq % Hkv != 0
+    dict(d=96),                   # unsupported head dim
+    dict(frozen_prefix=5, p=4),   # frozen rows beyond the cartridge
+    dict(n=0),                    # no real tokens
+    dict(p=-1),
+])
+def test_workspace_query_rejects_bad_geometry(lib, bad):
+    kw = dict(B=1, n=8, Hq=4, Hkv=2, d=64, p=4, frozen_prefix=1)
+    kw.update(bad)
+    g = cartattn.geom(**kw)
+    assert cartattn.fwd_workspace_size(g, 0, 1) == 0
+    assert cartattn.bwd_workspace_size(g, 0, 1) == 0
+
+
+def test_workspace_sizes_are_positive_and_grow(lib):
+    g1 = cartattn.geom(1, 128, 4, 2, 128, 16)
+    g2 = cartattn.geom(2, 128, 4, 2, 128, 16)
+    a, b = cartattn.fwd_workspace_size(g1, 0, 1), cartattn.fwd_workspace_size(g2, 0, 1)
+    assert 0 < a < b
+    assert cartattn.bwd_workspace_size(g1, 0, 1) > a
+    assert cartattn.decode_workspace_size(64, 32, 8, 128, 4096, 1025) > 0
+    assert cartattn.decode_workspace_size(4, 12, 4, 128, 16, 8) == 0   # G = 3 unsupported
+
+
+def test_calls_validate_before_touching_the_device(lib):
+    g = cartattn.geom(1, 8, 4, 2, 64, 4)
+    null = ctypes.c_void_p(0)
+    # NULL inputs
+    rc = lib.cart_attn_fwd(ctypes.byref(g), 0, 1, null, null, null, null, null, null, null, null,
+                           0, null)
+    assert rc == -2
+    # misaligned pointer
+    odd = ctypes.c_void_p(0x1001)
+    rc = lib.cart_attn_fwd(ctypes.byref(g), 0, 1, odd, odd, odd, odd, odd, odd, odd, odd, 0, null)
+    assert rc == -2
+    # bad dtype
+    al = ctypes.c_void_p(0x1000)
+    rc = lib.cart_attn_fwd(ctypes.byref(g), 7, 1, al, al, al, al, al, al, al, al, 1 << 30, null)
+    assert rc == -3
+    # workspace too small
+    rc = lib.cart_attn_fwd(ctypes.byref(g), 0, 1, al, al, al, al, al, al, al, al, 16, null)
+    assert rc == -4
+    # cache write: stride smaller than a row
+    rc = lib.cart_write_to_cache(al, al, 4, 2, 64, al, al, 64, 0, 0, null)
+    assert rc == -1
+    # decode: unsupported group size
+    rc = lib.cart_attn_decode(2, 6, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al, al, 8, al, al,
+                              al, 1 << 20, null)
+    assert rc == -1
+
+
+def test_no_gpu_here_means_a_cuda_or_device_error(lib):
+    """With valid arguments but no usable sm_103 device the call fails loudly
+    instead of computing anything elsewhere."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    g = cartattn.geom(1, 8, 4, 2, 64, 4)
+    al = ctypes.c_void_p(0x1000)
+    ws = cartattn.fwd_workspace_size(g, 0, 1)
+    rc = lib.cart_attn_fwd(ctypes.byref(g), 0, 1, al, al, al, al, al, al, al, al, ws, None)
+    assert rc in (-5, -6)

@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+seeded inputs.  Small geometries span several 128-row tiles with ragged tails
+and cover the degenerate cases (p = 0, sink-only cartridge, n = 1, MHA,
+G = 8, f32 inputs); the full workloads are checked on sampled outputs or
+properties that hold at any size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import gpu_helpers as gh
+from trained_kv_prefix_gb300 import cartattn, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _shape(name, B, n, Hq, Hkv, d, p, dtype="bf16", cart="f32", frozen=1, seed=100, do_std=1.0):
+    return synth.TrainShape(name, B=B, n=n, Hq=Hq, Hkv=Hkv, d=d, p=p, frozen_prefix=frozen,
+                            dtype=dtype, cart_dtype=cart, seed=seed, qkv_std=0.5, do_std=do_std)
+
+
+SMALL = [
+    synth.TINY,
+    _shape("p0", 2, 200, 8, 2, 128, 0, frozen=0, seed=101),
+    _shape("sink_only", 1, 130, 4, 2, 128, 1, seed=102),
+    _shape("mha_ragged_p", 2, 70, 2, 2, 128, 130, seed=103),
+    _shape("g8_d64", 1, 257, 8, 1, 64, 300, seed=104),
+    _shape("n1", 3, 1, 4, 2, 128, 256, seed=105),
+    _shape("multi_tile", 1, 384, 8, 2, 128, 513, seed=106),
+    _shape("bf16_cart", 2, 160, 4, 1, 128, 200, cart="bf16", seed=107),
+    _shape("f32_d128", 1, 150, 4, 2, 128, 140, dtype="f32", seed=108),
+    _shape("frozen3", 1, 100, 4, 2, 64, 40, frozen=3, seed=109),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from trained_kv_prefix_gb300 import build
+    build.build()
+    cartattn.device_status(clear=True)
+
+
+@pytest.mark.parametrize("s", SMALL, ids=[s.name for s in SMALL])
+def test_train_parity_small(s):
+    inp = synth.train_inputs(s)
+    got = gh.run_train_gpu(s, inp)
+    ref = gh.oracle_train(s, inp)
+    gh.check_fwd(got, ref)
+    gh.check_grads(got, ref, s.frozen_prefix)
+
+
+def test_bwd_accumulate_mode():
+    s = _shape("acc", 1, 96, 4, 2, 64, 70, seed=110)
+    inp = synth.train_inputs(s)
+    rng = np.random.default_rng(5)
+    dkc0 = torch.from_numpy(rng.standard_normal((s.p, s.Hkv, s.d))).float()
+    dvc0 = torch.from_numpy(rng.standard_normal((s.p, s.Hkv, s.d))).float()
+    got = gh.run_train_gpu(s, inp, accumulate=True, dkc0=dkc0, dvc0=dvc0)
+    ref = gh.oracle_train(s, inp)
+    ref["dkc"] = ref["dkc"] + dkc0.double().numpy()
+    ref["dvc"] = ref["dvc"] + dvc0.double().numpy()
+    ref["dkc"][: s.frozen_prefix] = 0.0
+    ref["dvc"][: s.frozen_prefix] = 0.0
+    gh.check_grads(got, ref, s.frozen_prefix, names=("dkc", "dvc"))
+
+
+def test_backward_is_deterministic():
+    s = _shape("det", 2, 200, 8, 2, 128, 300, seed=111)
+    inp = synth.train_inputs(s)
+    a = gh.run_train_gpu(s, inp)
+    b = gh.run_train_gpu(s, inp)
+    for k in ("o", "lse", "dq", "dk", "dv", "dkc", "dvc"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+def test_cache_write_bitwise():
+    rng = np.random.default_rng(7)
+    p, Hkv, d = 300, 4, 128
+    kc = torch.from_numpy((rng.standard_normal((p, Hkv, d)) * 3).astype(np.float32))
+    vc = torch.from_numpy((rng.standard_normal((p, Hkv, d)) * 1e-3).astype(np.float32))
+    rows = 320
+    kd = torch.zeros((rows, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros((rows, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    cartattn.cart_write_to_cache(kc.cuda(), vc.cuda(), kd, vd, dst_row0=7)
+    torch.cuda.synchronize()
+    for src, dst in ((kc, kd), (vc, vd)):
+        want = np.zeros((rows, Hkv, d), dtype=np.uint16)
+        oracle.write_to_cache(src.numpy(), want, dst_row0=7)
+        got = dst.cpu().view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(got, want)
+
+
+def test_cache_write_f32_destination():
+    rng = np.random.default_rng(8)
+    kc = torch.from_numpy(rng.standard_normal((33, 2, 64)).astype(np.float32))
+    kd = torch.zeros((40, 2, 64), dtype=torch.float32, device="cuda")
+    vd = torch.zeros((40, 2, 64), dtype=torch.float32, device="cuda")
+    cartattn.cart_write_to_cache(kc.cuda(), kc.cuda(), kd, vd, dst_row0=5)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(kd.cpu().numpy()[5:38], kc.numpy())
+    assert (kd.cpu().numpy()[:5] == 0).all() and (kd.cpu().numpy()[38:] == 0).all()
+
+
+# ------------------------------------------------------------- decode ----
+def _decode_case(name, B, Hq, Hkv, d, p, max_private, lens=(), seed=200):
+    return synth.DecodeShape(name, B=B, Hq=Hq, Hkv=Hkv, d=d, p=p, max_private=max_private,
+                             seed=seed, fixed_len=tuple(lens))
+
+
+DECODE_SMALL = [
+    _decode_case("ragged", 3, 4, 2, 64, 16, 39, lens=(0, 17, 39)),
+    _decode_case("p0", 2, 8, 2, 128, 0, 200, lens=(0, 130)),
+    _decode_case("g8_p300", 4, 8, 1, 128, 300, 300, lens=(0, 1, 127, 300)),
+    _decode_case("g1_big", 5, 4, 4, 128, 1000, 600, lens=(600, 0, 128, 129, 255)),
+]
+
+
+def _run_decode(s, inp):
+    g = {k: v.cuda() for k, v in inp.items()}
+    o = cartattn.cart_attn_decode(g["q"], g["k_new"], g["v_new"], g["kc"], g["vc"], g["k_cache"],
+                                  g["v_cache"], g["lens"], theta=s.theta)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    return synth.f64(o), g["k_cache"].cpu(), g["v_cache"].cpu()
+
+
+def _check_decode(s, inp, o, kcache, vcache):
+    a = {k: synth.f64(v) for k, v in inp.items() if k != "lens"}
+    lens = inp["lens"].numpy()
+    o_ref, kref, vref = oracle.decode(a["q"], a["k_new"], a["v_new"], a["kc"], a["vc"],
+                                      a["k_cache"], a["v_cache"], lens, theta=s.theta)
+    assert gh.max_abs(o, o_ref) <= gh.FWD_MAXABS, gh.max_abs(o, o_ref)
+    assert gh.rel_l2(o, o_ref) <= gh.FWD_RELL2, gh.rel_l2(o, o_ref)
+    kc_new = synth.f64(kcache)
+    vc_new = synth.f64(vcache)
+    for b in range(s.B):
+        L = int(lens[b])
+        # rows other than the appended one are untouched
+        mask = np.ones(s.cache_rows, bool)
+        mask[L] = False
+        np.testing.assert_array_equal(kc_new[b][mask], a["k_cache"][b][mask])
+        np.testing.assert_array_equal(vc_new[b][mask], a["v_cache"][b][mask])
+        np.testing.assert_array_equal(vc_new[b, L], a["v_new"][b])
+        # the appended key is the rotated new key, rounded once to bf16
+        np.testing.assert_allclose(kc_new[b, L], kref[b, L], rtol=2 ** -8, atol=1e-6)
+
+
+@pytest.mark.parametrize("s", DECODE_SMALL, ids=[s.name for s in DECODE_SMALL])
+def test_decode_parity_small(s):
+    inp = synth.decode_inputs(s)
+    o, kc, vc = _run_decode(s, inp)
+    _check_decode(s, inp, o, kc, vc)
+
+
+def test_decode_serving_workload():
+    """64 conversations behind one p = 4096 cartridge, 0..1024 private rows."""
+    s = synth.DECODE
+    inp = synth.decode_inputs(s)
+    o, kc, vc = _run_decode(s, inp)
+    _check_decode(s, inp, o, kc, vc)
+
+
+# ------------------------------------------------ full-size workloads ----
+def test_equivalence_gate_bf16():
+    """Cartridge = rotated bf16 K/V of 512 prefix tokens; the 256 continuation
+    queries behind it match (a) the oracle on the same stored inputs and
+    (b) causal attention over all 768 tokens (the zero-step gate)."""
+    s = synth.EQUIV
+    p, n = s.p, s.n
+    kraw, vraw, rng = synth.token_kv(p + n, s.Hkv, s.d, seed=s.seed, std=s.qkv_std)
+    qcont = synth.token_q(rng, n, s.Hq, s.d, std=s.qkv_std)
+    inp = dict(q=synth.to_storage(qcont[None], "bf16"), k=synth.to_storage(kraw[None, p:], "bf16"),
+               v=synth.to_storage(vraw[None, p:], "bf16"),
+               kc=synth.to_storage(oracle.rope(kraw[:p], 0, theta=s.theta), "bf16"),
+               vc=synth.to_storage(vraw[:p], "bf16"),
+               do=synth.to_storage(np.zeros((1, n, s.Hq, s.d)), "bf16"))
+    got = gh.run_train_gpu(s, inp, bwd=False)
+    ref = gh.oracle_train(s, inp, bwd=False)
+    gh.check_fwd(got, ref)
+    # the prefill reference: every token real, positions 0..767, stored values
+    kfull = synth.f64(synth.to_storage(kraw, "bf16"))[None]
+    vfull = synth.f64(synth.to_storage(vraw, "bf16"))[None]
+    qfull = np.zeros((1, p + n, s.Hq, s.d))
+    qfull[0, p:] = synth.f64(inp["q"])[0]
+    empty = np.zeros((0, s.Hkv, s.d))
+    o_full, _ = oracle.fwd(qfull, kfull, vfull, empty, empty, theta=s.theta, rows=(p, p + n))
+    assert gh.max_abs(got["o"][0], o_full[0, p:]) <= gh.FWD_MAXABS
+    assert gh.rel_l2(got["o"][0], o_full[0, p:]) <= gh.FWD_RELL2
+
+
+def test_selfstudy_workload_one_group():
+    """B=4, Hq=32, Hkv=8, d=128, p=2048, n=1024: every output of kv-head
+    group 0 (query heads 0-3) against the oracle, cartridge gradient included."""
+    s = synth.SELFSTUDY
+    inp = synth.train_inputs(s)
+    got = gh.run_train_gpu(s, inp)
+    G = s.Hq // s.Hkv
+    ref = gh.oracle_train(s, inp, heads=(0, G), kv_heads=(0, 1))
+    gh.check_fwd(got, ref, sl=(slice(None), slice(None), slice(0, G)),
+                 lse_sl=(slice(None), slice(0, G)))
+    gh.check_grads(got, ref, s.frozen_prefix,
+                   sls=dict(dq=(slice(None), slice(None), slice(0, G)),
+                            dk=(slice(None), slice(None), slice(0, 1)),
+                            dv=(slice(None), slice(None), slice(0, 1)),
+                            dkc=(slice(None), slice(0, 1)), dvc=(slice(None), slice(0, 1))))
+
+
+def test_longctx_workload_sampled():
+    """B=1, Hq=64, Hkv=8, d=128, p=8192, n=4096.  Forward rows and the last
+    query tile's gradients of kv group 3 against the oracle; the keys of the
+    last real tile are seen only by that tile's queries, so their dK/dV are
+    exact there.  Cartridge gradients via properties that hold at any size."""
+    s = synth.LONGCTX
+    inp = synth.train_inputs(s)
+    got = gh.run_train_gpu(s, inp)
+    G = s.Hq // s.Hkv
+    g0 = 3
+    lo, hi = s.n - 128, s.n
+    ref = gh.oracle_train(s, inp, heads=(g0 * G, g0 * G + G), rows=(lo, hi),
+                          kv_heads=(g0, g0 + 1), bwd_rows=(lo, hi))
+    hs = slice(g0 * G, g0 * G + G)
+    gh.check_fwd(got, ref, sl=(slice(None), slice(lo, hi), hs), lse_sl=(slice(None), hs, slice(lo, hi)))
+    gh.check_grads(got, ref, s.frozen_prefix, names=("dq", "dk", "dv"),
+                   sls=dict(dq=(slice(None), slice(lo, hi), hs),
+                            dk=(slice(None), slice(lo, hi), slice(g0, g0 + 1)),
+                            dv=(slice(None), slice(lo, hi), slice(g0, g0 + 1))))
+    # frozen sink row exactly zero; the other rows do not depend on the freeze
+    assert (got["dkc"][0] == 0).all() and (got["dvc"][0] == 0).all()
+    unfrozen = gh.run_train_gpu(s, inp, frozen_prefix=0)
+    np.testing.assert_array_equal(unfrozen["dkc"][1:], got["dkc"][1:])
+    np.testing.assert_array_equal(unfrozen["dvc"][1:], got["dvc"][1:])
+    assert np.abs(unfrozen["dvc"][0]).max() > 0
+    # value gradients over every attended row sum to the summed upstream
+    # gradient of the group (softmax weights sum to one)
+    do = synth.f64(inp["do"])
+    for g in range(s.Hkv):
+        lhs = unfrozen["dvc"][:, g].sum(0) + got["dv"][:, :, g].sum((0, 1))
+        rhs = do[:, :, g * G:(g + 1) * G].sum((0, 1, 2))
+        assert gh.rel_l2(lhs, rhs) <= gh.GRAD_RELL2
+    # key gradients (rotated into the attended space) sum to zero
+    for g in (0, 5):
+        dk_att = oracle.rope(got["dk"][0, :, g:g + 1], s.p, theta=s.theta)[:, 0]
+        lhs = unfrozen["dkc"][:, g].sum(0) + dk_att.sum(0)
+        scale = np.abs(unfrozen["dkc"][:, g]).sum(0).max() + np.abs(dk_att).sum(0).max()
+        assert np.abs(lhs).max() <= 1e-2 * scale

@@ -262,6 +262,20 @@ def test_bwd_kv_head_restriction():
     np.testing.assert_array_equal(part[3][:, 1], full[3][:, 1])
 
 
+def test_bwd_row_partition_sums_to_full():
+    """The loss is a sum over query rows, so per-row-range gradients add up
+    to the full gradient (and dq of each row comes from its own range)."""
+    P = _problem(43, 2, 9, 4, 2, 8, 5)
+    full = oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"])
+    parts = [oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"], rows=r)
+             for r in ((0, 4), (4, 9))]
+    np.testing.assert_array_equal(parts[0][0][:, :4], full[0][:, :4])
+    np.testing.assert_array_equal(parts[1][0][:, 4:], full[0][:, 4:])
+    assert np.isnan(parts[0][0][:, 4:]).all()
+    for t in (1, 2, 3, 4):
+        np.testing.assert_allclose(parts[0][t] + parts[1][t], full[t], rtol=0, atol=1e-13)
+
+
 # -------------------------------------------------------------- decode ----
 def test_decode_is_last_row_of_forward():
     """Decoding behind the cartridge equals the training-time forward of the

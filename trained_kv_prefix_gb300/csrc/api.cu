@@ -1,0 +1,503 @@
+// api.cu -- the C ABI (include/cartattn.h): host-side validation, workspace
+// carving, TMA descriptor construction and kernel launches.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace cart {
+
+__device__ uint32_t g_device_status;
+
+uint32_t* device_status_ptr() {
+  // One address per device; looked up with that device current.
+  static uint32_t* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t*>(p);
+  }
+  return cache[dev];
+}
+
+namespace {
+
+// ------------------------------------------------------------ utilities ----
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4D bf16 map with a 64 x 1 x rows x 1 box, 128-byte swizzle.  dims innermost
+// first; strides in bytes for dims 1..3.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t d3, uint64_t s1, uint64_t s2, uint64_t s3, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {d0, d1, d2, d3};
+  cuuint64_t strides[3] = {s1, s2, s3};
+  cuuint32_t box[4] = {64, 1, box_rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [blocks, rows, H, d] bf16 tensor as (d, H, rows, blocks).
+bool make_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, int H, int d,
+                   uint32_t box_rows) {
+  const uint64_t e = 2;
+  return make_map(m, base, d, H, rows, blocks, d * e, static_cast<uint64_t>(H) * d * e,
+                  static_cast<uint64_t>(rows) * H * d * e, box_rows);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CART_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return CART_ERR_CUDA;
+  if (major != 10 || minor != 3) return CART_ERR_DEVICE;
+  return CART_OK;
+}
+
+int check_geom(const cart_geom* g) {
+  if (!g) return CART_ERR_POINTER;
+  if (g->B < 1 || g->n < 1 || g->Hq < 1 || g->Hkv < 1 || g->Hq % g->Hkv != 0) return CART_ERR_GEOMETRY;
+  if (g->d != 64 && g->d != 128) return CART_ERR_GEOMETRY;
+  if (g->p < 0 || g->frozen_prefix < 0 || g->frozen_prefix > g->p) return CART_ERR_GEOMETRY;
+  if (!(std::isfinite(g->scale)) || !(g->rope_theta > 0.0) || !std::isfinite(g->rope_theta))
+    return CART_ERR_GEOMETRY;
+  if (g->B > 65535 || g->Hq > 65535 || (g->n + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
+  return CART_OK;
+}
+
+bool dtype_ok(cart_dtype t) { return t == CART_BF16 || t == CART_F32; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace carving shared by the size query and the call.
+struct TrainWs {
+  size_t table = 0, qr = 0, kr = 0, vb = 0, kcb = 0, vcb = 0, dob = 0, dvec = 0, total = 0;
+};
+
+TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
+  TrainWs w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t e16 = 2;
+  const size_t rows_q = static_cast<size_t>(g->B) * g->n * g->Hq * g->d;
+  const size_t rows_k = static_cast<size_t>(g->B) * g->n * g->Hkv * g->d;
+  const size_t cart = static_cast<size_t>(g->p) * g->Hkv * g->d;
+  w.table = take(static_cast<size_t>(g->n) * (g->d / 2) * sizeof(float2));
+  w.qr = take(rows_q * e16);
+  w.kr = take(rows_k * e16);
+  w.vb = (in == CART_F32) ? take(rows_k * e16) : SIZE_MAX;
+  w.kcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
+  w.vcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
+  if (bwd) {
+    w.dob = (in == CART_F32) ? take(rows_q * e16) : SIZE_MAX;
+    w.dvec = take(static_cast<size_t>(g->B) * g->Hq * g->n * sizeof(float));
+  }
+  w.total = off;
+  return w;
+}
+
+#define CART_CUDA(x)                                  \
+  do {                                                \
+    if ((x) != cudaSuccess) return CART_ERR_CUDA;     \
+  } while (0)
+
+// Shared front half of fwd and bwd: rope table, rotated Q/K, bf16 V and
+// cartridge, and the TMA maps over them.
+struct TrainPrep {
+  const float2* table;
+  const void* qr;
+  const void* kr;
+  const void* vb;
+  const void* kcb;
+  const void* vcb;
+  CUtensorMap mQ, mQ64, mK, mV, mKc, mVc;
+};
+
+int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
+               const void* v, const void* kc, const void* vc, uint8_t* ws, const TrainWs& w,
+               cudaStream_t st, TrainPrep* out) {
+  const bool f32 = in == CART_F32;
+  float2* table = reinterpret_cast<float2*>(ws + w.table);
+  __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(ws + w.qr);
+  __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(ws + w.kr);
+  CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, make_rope_freqs(g->d, g->rope_theta), st));
+  CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, st));
+  CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, st));
+  const void* vb = v;
+  if (f32) {
+    __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.vb);
+    CART_CUDA(launch_rope_rows(v, true, t, table, g->B, g->n, g->Hkv, g->d, false, st));
+    vb = t;
+  }
+  const void* kcb = kc;
+  const void* vcb = vc;
+  if (cd == CART_F32 && g->p > 0) {
+    __nv_bfloat16* tk = reinterpret_cast<__nv_bfloat16*>(ws + w.kcb);
+    __nv_bfloat16* tv = reinterpret_cast<__nv_bfloat16*>(ws + w.vcb);
+    const int row = g->Hkv * g->d;
+    CART_CUDA(launch_write_to_cache(static_cast<const float*>(kc), g->p, row, tk, row, 0, true, st));
+    CART_CUDA(launch_write_to_cache(static_cast<const float*>(vc), g->p, row, tv, row, 0, true, st));
+    kcb = tk;
+    vcb = tv;
+  }
+  out->table = table;
+  out->qr = qr;
+  out->kr = kr;
+  out->vb = vb;
+  out->kcb = kcb;
+  out->vcb = vcb;
+  bool ok = make_rows_map(&out->mQ, qr, g->B, g->n, g->Hq, g->d, 128) &&
+            make_rows_map(&out->mQ64, qr, g->B, g->n, g->Hq, g->d, 64) &&
+            make_rows_map(&out->mK, kr, g->B, g->n, g->Hkv, g->d, 128) &&
+            make_rows_map(&out->mV, vb, g->B, g->n, g->Hkv, g->d, 128);
+  if (g->p > 0)
+    ok = ok && make_rows_map(&out->mKc, kcb, 1, g->p, g->Hkv, g->d, 128) &&
+         make_rows_map(&out->mVc, vcb, 1, g->p, g->Hkv, g->d, 128);
+  else  // never loaded when there are no cartridge tiles
+    ok = ok && make_rows_map(&out->mKc, kr, 1, 1, g->Hkv, g->d, 128) &&
+         make_rows_map(&out->mVc, kr, 1, 1, g->Hkv, g->d, 128);
+  return ok ? CART_OK : CART_ERR_CUDA;
+}
+
+int train_common_checks(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
+                        const void* k, const void* v, const void* kc, const void* vc) {
+  int rc = check_geom(g);
+  if (rc) return rc;
+  if (!dtype_ok(in) || !dtype_ok(cd)) return CART_ERR_DTYPE;
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return CART_ERR_POINTER;
+  if (g->p > 0 && (!kc || !vc || !aligned16(kc) || !aligned16(vc))) return CART_ERR_POINTER;
+  return CART_OK;
+}
+
+}  // namespace
+}  // namespace cart
+
+using namespace cart;
+
+extern "C" {
+
+const char* cart_status_string(int s) {
+  switch (s) {
+    case CART_OK: return "ok";
+    case CART_ERR_GEOMETRY: return "bad geometry";
+    case CART_ERR_POINTER: return "null or misaligned pointer";
+    case CART_ERR_DTYPE: return "unsupported dtype";
+    case CART_ERR_WORKSPACE: return "workspace too small";
+    case CART_ERR_CUDA: return "CUDA error";
+    case CART_ERR_DEVICE: return "device is not sm_103";
+    case CART_ERR_TIMEOUT: return "a kernel gave up waiting";
+    default: return "unknown status";
+  }
+}
+
+int cart_device_status(unsigned* bits_out, int clear) {
+  uint32_t* p = device_status_ptr();
+  if (!p) return CART_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CART_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return CART_ERR_CUDA;
+  if (clear && cudaMemset(p, 0, sizeof v) != cudaSuccess) return CART_ERR_CUDA;
+  if (bits_out) *bits_out = v;
+  return v ? CART_ERR_TIMEOUT : CART_OK;
+}
+
+int cart_write_to_cache(const float* kc, const float* vc, int p, int Hkv, int d, void* k_dst,
+                        void* v_dst, long long row_stride_elems, int dst_row0,
+                        cart_dtype dst_dtype, void* stream) {
+  if (p < 0 || Hkv < 1 || d < 8 || d % 8 != 0 || dst_row0 < 0) return CART_ERR_GEOMETRY;
+  const long long row = static_cast<long long>(Hkv) * d;
+  if (row_stride_elems < row || row_stride_elems % 8 != 0) return CART_ERR_GEOMETRY;
+  if (!dtype_ok(dst_dtype)) return CART_ERR_DTYPE;
+  if ((!kc || !k_dst) && (!vc || !v_dst)) return CART_ERR_POINTER;
+  if ((kc && !aligned16(kc)) || (vc && !aligned16(vc)) || (k_dst && !aligned16(k_dst)) ||
+      (v_dst && !aligned16(v_dst)))
+    return CART_ERR_POINTER;
+  int rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dst_dtype == CART_BF16;
+  if (kc && k_dst)
+    CART_CUDA(launch_write_to_cache(kc, p, static_cast<int>(row), k_dst, row_stride_elems,
+                                    dst_row0, bf16, st));
+  if (vc && v_dst)
+    CART_CUDA(launch_write_to_cache(vc, p, static_cast<int>(row), v_dst, row_stride_elems,
+                                    dst_row0, bf16, st));
+  return CART_OK;
+}
+
+size_t cart_attn_fwd_workspace_size(const cart_geom* g, cart_dtype in, cart_dtype cd) {
+  if (check_geom(g) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
+  return train_ws(g, in, cd, false).total;
+}
+
+int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
+                  const void* v, const void* kc, const void* vc, void* o, float* lse,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = train_common_checks(g, in, cd, q, k, v, kc, vc);
+  if (rc) return rc;
+  if (!o || !lse || !aligned16(o) || !aligned16(lse)) return CART_ERR_POINTER;
+  const TrainWs w = train_ws(g, in, cd, false);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TrainPrep tp;
+  rc = train_prep(g, in, cd, q, k, v, kc, vc, static_cast<uint8_t*>(workspace), w, st, &tp);
+  if (rc) return rc;
+  FwdLaunch l{};
+  l.mQ = &tp.mQ;
+  l.mKc = &tp.mKc;
+  l.mVc = &tp.mVc;
+  l.mK = &tp.mK;
+  l.mV = &tp.mV;
+  l.d = g->d;
+  l.n_rows = g->n;
+  l.n_qblocks = g->B;
+  l.Hq_map = g->Hq;
+  l.G = g->Hq / g->Hkv;
+  l.p = g->p;
+  l.n_real = g->n;
+  l.cart_tiles_per_split = 0;
+  l.n_splits = 1;
+  l.scale_log2 = g->scale * 1.4426950408889634f;
+  l.out = o;
+  l.out_f32 = in == CART_F32;
+  l.lse = lse;
+  l.decode = false;
+  CART_CUDA(launch_fwd(l, st));
+  return CART_OK;
+}
+
+size_t cart_attn_bwd_workspace_size(const cart_geom* g, cart_dtype in, cart_dtype cd) {
+  if (check_geom(g) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
+  return train_ws(g, in, cd, true).total;
+}
+
+int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
+                  const void* v, const void* kc, const void* vc, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* dkc, float* dvc,
+                  int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = train_common_checks(g, in, cd, q, k, v, kc, vc);
+  if (rc) return rc;
+  if (!o || !lse || !dout || !dq || !dk || !dv || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return CART_ERR_POINTER;
+  if (g->p > 0 && (!dkc || !dvc || !aligned16(dkc) || !aligned16(dvc))) return CART_ERR_POINTER;
+  if (accumulate != 0 && accumulate != 1) return CART_ERR_GEOMETRY;
+  const TrainWs w = train_ws(g, in, cd, true);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  TrainPrep tp;
+  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp);
+  if (rc) return rc;
+  const bool f32 = in == CART_F32;
+  const void* dob = dout;
+  if (f32) {
+    __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.dob);
+    CART_CUDA(launch_rope_rows(dout, true, t, tp.table, g->B, g->n, g->Hq, g->d, false, st));
+    dob = t;
+  }
+  float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
+  CART_CUDA(launch_bwd_dot(o, dout, f32, Dvec, g->B, g->n, g->Hq, g->d, st));
+  CUtensorMap mdO, mdO64;
+  if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128) ||
+      !make_rows_map(&mdO64, dob, g->B, g->n, g->Hq, g->d, 64))
+    return CART_ERR_CUDA;
+  BwdLaunch l{};
+  l.mQ = &tp.mQ;
+  l.mdO = &mdO;
+  l.mQ64 = &tp.mQ64;
+  l.mdO64 = &mdO64;
+  l.mKc = &tp.mKc;
+  l.mVc = &tp.mVc;
+  l.mK = &tp.mK;
+  l.mV = &tp.mV;
+  l.B = g->B;
+  l.n = g->n;
+  l.Hq = g->Hq;
+  l.Hkv = g->Hkv;
+  l.d = g->d;
+  l.p = g->p;
+  l.frozen_prefix = g->frozen_prefix;
+  l.scale = g->scale;
+  l.lse = lse;
+  l.Dvec = Dvec;
+  l.dq = dq;
+  l.dk = dk;
+  l.dv = dv;
+  l.out_f32 = f32;
+  l.dkc = dkc;
+  l.dvc = dvc;
+  l.accumulate = accumulate;
+  l.table = tp.table;
+  CART_CUDA(launch_bwd(l, st, st));
+  return CART_OK;
+}
+
+// ------------------------------------------------------------------ decode --
+namespace {
+constexpr int kDecodeChunk = 128;
+
+struct DecodeWs {
+  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, total = 0;
+  int splits = 0, tiles_per_split = 0;
+};
+
+DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
+  DecodeWs w;
+  const int n_ct = (p + 127) / 128;
+  const int R = B * (Hq / Hkv);
+  const int qtiles = (R + 127) / 128;
+  if (n_ct > 0) {
+    // aim for about one CTA per SM for the cartridge part
+    const long long units = static_cast<long long>(n_ct) * Hkv * qtiles;
+    int per = static_cast<int>((units + 147) / 148);
+    if (per < 1) per = 1;
+    w.tiles_per_split = per;
+    w.splits = (n_ct + per - 1) / per;
+  }
+  const int chunks = (rows + kDecodeChunk - 1) / kDecodeChunk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  w.q_rot = take(static_cast<size_t>(B) * Hq * d * 2);
+  w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
+  w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
+  w.priv_part = take(static_cast<size_t>(B) * Hq * chunks * d * 4);
+  w.priv_ml = take(static_cast<size_t>(B) * Hq * chunks * 2 * 4);
+  w.total = off;
+  return w;
+}
+
+int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta, int rows) {
+  if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || p < 0 || rows < 1)
+    return CART_ERR_GEOMETRY;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return CART_ERR_GEOMETRY;
+  if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
+  if (!std::isfinite(scale) || !(theta > 0.0) || !std::isfinite(theta)) return CART_ERR_GEOMETRY;
+  if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
+  if ((rows + kDecodeChunk - 1) / kDecodeChunk > 65535 * 16) return CART_ERR_GEOMETRY;
+  return CART_OK;
+}
+}  // namespace
+
+size_t cart_attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int p, int cache_rows) {
+  if (check_decode(B, Hq, Hkv, d, p, 1.f, 1.0, cache_rows)) return 0;
+  return decode_ws(B, Hq, Hkv, d, p, cache_rows).total;
+}
+
+int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double rope_theta,
+                     const void* q, const void* k_new, const void* v_new, const void* kc,
+                     const void* vc, void* k_cache, void* v_cache, int cache_rows,
+                     const int* priv_len, void* o, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  int rc = check_decode(B, Hq, Hkv, d, p, scale, rope_theta, cache_rows);
+  if (rc) return rc;
+  const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return CART_ERR_POINTER;
+  if (!priv_len || (reinterpret_cast<uintptr_t>(priv_len) & 3u)) return CART_ERR_POINTER;
+  if (p > 0 && (!kc || !vc || !aligned16(kc) || !aligned16(vc))) return CART_ERR_POINTER;
+  const DecodeWs w = decode_ws(B, Hq, Hkv, d, p, cache_rows);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int G = Hq / Hkv, R = B * G;
+  DecodeLaunch a{};
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.p = p;
+  a.rows = cache_rows;
+  a.scale = scale;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.kc = static_cast<const __nv_bfloat16*>(kc);
+  a.vc = static_cast<const __nv_bfloat16*>(vc);
+  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  a.len = priv_len;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.q_rot = reinterpret_cast<__nv_bfloat16*>(ws + w.q_rot);
+  a.n_cart_splits = w.splits;
+  a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
+  a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
+  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
+  a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
+  a.chunk = kDecodeChunk;
+  CART_CUDA(launch_decode_prep(a, make_rope_freqs(d, rope_theta), st));
+  if (p > 0) {
+    CUtensorMap mQ, mKc, mVc;
+    if (!make_rows_map(&mQ, a.q_rot, 1, R, Hkv, d, 128) ||
+        !make_rows_map(&mKc, kc, 1, p, Hkv, d, 128) || !make_rows_map(&mVc, vc, 1, p, Hkv, d, 128))
+      return CART_ERR_CUDA;
+    FwdLaunch l{};
+    l.mQ = &mQ;
+    l.mKc = &mKc;
+    l.mVc = &mVc;
+    l.mK = &mKc;  // no real-token tiles in this mode
+    l.mV = &mVc;
+    l.d = d;
+    l.n_rows = R;
+    l.n_qblocks = 1;
+    l.Hq_map = Hkv;
+    l.G = 1;
+    l.p = p;
+    l.n_real = 0;
+    l.cart_tiles_per_split = w.tiles_per_split;
+    l.n_splits = w.splits;
+    l.scale_log2 = scale * 1.4426950408889634f;
+    l.out = const_cast<float*>(a.cart_part);
+    l.out_f32 = true;
+    l.lse = const_cast<float*>(a.cart_lse);
+    l.decode = true;
+    CART_CUDA(launch_fwd(l, st));
+  }
+  CART_CUDA(launch_decode_private(a, st));
+  CART_CUDA(launch_decode_combine(a, st));
+  return CART_OK;
+}
+
+}  // extern "C"

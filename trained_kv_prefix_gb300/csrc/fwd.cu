@@ -1,0 +1,445 @@
+// fwd.cu -- tcgen05 forward of cartridge attention (sm_103a).
+//
+// One CTA owns a 128-row query tile of one (sequence, head) and walks the key
+// tiles of concat(cartridge rows, real tokens): first every cartridge tile
+// (all visible), then the real-token tiles up to the diagonal (end-aligned
+// causal mask: key j of the real part is visible from query i iff j <= i).
+// (Cartridges guide, "Semantics", attention bullet.)
+//
+// Roles (192 threads):
+//   warps 0-3  softmax warpgroup: thread t owns query row t (TMEM lane t).
+//              Reads S from TMEM, masks, keeps the running max / sum in
+//              f32 (log2 domain), rescales O in TMEM when the max grows by
+//              more than 2^8, writes P (bf16) to shared memory in the
+//              128-byte-swizzled K-major layout, and finally normalises O.
+//   warp 4     TMA producer: Q tile once, then K/V tiles into a 2-stage ring.
+//   warp 5     MMA issuer (one thread): S = Q K^T and O += P V on tcgen05,
+//              accumulators in TMEM (S: 128 columns, O: d columns).
+//
+// The same kernel also computes split-KV partials of the decode step over a
+// shared cartridge (rows of all conversations of one kv head batched into the
+// M dimension); then it writes O normalised by its own sum (f32) and the
+// log2-domain log-sum-exp per row.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace cart {
+namespace {
+
+struct FwdParams {
+  int n_rows, Hq_map, G, p, n_real, cart_tiles_per_split, n_qtiles;
+  float scale_log2;
+  void* out;
+  float* lse;
+  int out_f32;
+  int decode;
+  uint32_t* status;
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = kTile * D * 2;      // one Q, K or V tile (bf16)
+  static constexpr int kStages = 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kP = kV + kStages * kTileBytes;
+  static constexpr int kPBytes = kTile * kTile * 2;
+  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kBytes = kBar + 128;             // barriers + TMEM slot
+  static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-B alignment
+};
+
+enum FwdBar { kQFull = 0, kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull, kSFree, kPFull,
+              kODone, kDrain, kNumBars };
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k) {
+  // 16-element K step inside a 64-element (128 B) swizzle atom column;
+  // atom columns of a 128-row tile are 16 KB apart.
+  return sdesc_sw128(base + static_cast<uint32_t>(k >> 2) * 16384u +
+                         static_cast<uint32_t>(k & 3) * 32u,
+                     16u, 1024u);
+}
+
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int k) {
+  // 16 rows along K = two 8-row groups (1024 B each); 64-wide N blocks 16 KB apart.
+  return sdesc_sw128(base + static_cast<uint32_t>(k) * 2048u, 16384u, 1024u);
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
+               const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
+               const __grid_constant__ CUtensorMap mV, const FwdParams a) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kNumBars * 8);
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item ----
+  int head, qb, qt, kvh, split;
+  if (!a.decode) {
+    head = blockIdx.x;
+    qb = blockIdx.y;
+    qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);  // heaviest tiles first
+    kvh = head / a.G;
+    split = 0;
+  } else {
+    head = blockIdx.x;
+    qb = 0;
+    qt = blockIdx.y;
+    kvh = head;
+    split = blockIdx.z;
+  }
+  const int q0 = qt * kTile;
+  const int n_ct_all = (a.p + kTile - 1) / kTile;
+  int ct_lo = 0, ct_hi = n_ct_all, n_rt = 0;
+  if (a.decode) {
+    ct_lo = split * a.cart_tiles_per_split;
+    ct_hi = min(ct_lo + a.cart_tiles_per_split, n_ct_all);
+  } else {
+    n_rt = min(qt + 1, (a.n_real + kTile - 1) / kTile);
+  }
+  const int n_ct = max(ct_hi - ct_lo, 0);
+  const int T = n_ct + n_rt;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bars[kQFull], 1);
+    mbar_init(&bars[kKVFull0], 1);
+    mbar_init(&bars[kKVFull1], 1);
+    mbar_init(&bars[kKVEmpty0], 1);
+    mbar_init(&bars[kKVEmpty1], 1);
+    mbar_init(&bars[kSFull], 1);
+    mbar_init(&bars[kSFree], 128);
+    mbar_init(&bars[kPFull], 128);
+    mbar_init(&bars[kODone], 1);
+    mbar_init(&bars[kDrain], 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;
+  const uint32_t tO = tmem + 128;
+  volatile int* abort_p = &abort_flag;
+
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sP = smem + L::kP;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mKc);
+      tma_prefetch_desc(&mVc);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      mbar_arrive_expect_tx(&bars[kQFull], L::kTileBytes);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h)
+        tma_load_4d(sQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, q0, qb);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < T; ++t) {
+        const int s = t & 1;
+        if (t >= 2) {
+          ok = mbar_wait(&bars[kKVEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutTma);
+          if (!ok) break;
+        }
+        uint8_t* sK = smem + L::kK + s * L::kTileBytes;
+        uint8_t* sV = smem + L::kV + s * L::kTileBytes;
+        mbar_arrive_expect_tx(&bars[kKVFull0 + s], 2 * L::kTileBytes);
+        if (t < n_ct) {
+          const int row0 = (ct_lo + t) * kTile;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_4d(sK + h * 16384, &mKc, &bars[kKVFull0 + s], h * 64, kvh, row0, 0);
+            tma_load_4d(sV + h * 16384, &mVc, &bars[kKVFull0 + s], h * 64, kvh, row0, 0);
+          }
+        } else {
+          const int row0 = (t - n_ct) * kTile;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_4d(sK + h * 16384, &mK, &bars[kKVFull0 + s], h * 64, kvh, row0, qb);
+            tma_load_4d(sV + h * 16384, &mV, &bars[kKVFull0 + s], h * 64, kvh, row0, qb);
+          }
+        }
+        issued = t + 1;
+      }
+      if (!ok) {
+        // Give the copies already in flight a bounded chance to land before
+        // the CTA releases its shared memory.
+        int dummy = 0;
+        mbar_wait(&bars[kQFull], 0, &dummy, nullptr, 0);
+        for (int t = max(issued - 2, 0); t < issued; ++t)
+          mbar_wait(&bars[kKVFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA --
+    if (lane == 0 && T > 0) {
+      const uint32_t idS = idesc_bf16(128, 128, false, false);
+      const uint32_t idPV = idesc_bf16(128, D, false, true);
+      const uint32_t q_base = smem_u32(sQ);
+      const uint32_t p_base = smem_u32(sP);
+      bool ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutMma);
+      auto issue_pv = [&](int t) {
+        const int sp = t & 1;
+        const uint32_t v_base = smem_u32(smem + L::kV + sp * L::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_bf16_ss(tO, kmajor_desc(p_base, k), mnmajor_desc(v_base, k), idPV,
+                       (t > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bars[kODone]);
+        umma_commit(&bars[kKVEmpty0 + sp]);
+      };
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t & 1;
+        ok = mbar_wait(&bars[kKVFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        if (!ok) break;
+        if (t > 0) {
+          ok = mbar_wait(&bars[kSFree], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(smem + L::kK + s * L::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_bf16_ss(tS, kmajor_desc(q_base, k), kmajor_desc(k_base, k), idS, k > 0 ? 1u : 0u);
+        umma_commit(&bars[kSFull]);
+        if (t > 0) {
+          ok = mbar_wait(&bars[kPFull], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t - 1);
+        }
+      }
+      if (ok) {
+        ok = mbar_wait(&bars[kPFull], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(T - 1);
+        }
+      }
+      // Drain: every MMA issued above completes before the CTA tears down.
+      umma_commit(&bars[kDrain]);
+      int dummy = 0;
+      mbar_wait(&bars[kDrain], 0, &dummy, nullptr, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax --
+    const int row = threadIdx.x;  // 0..127 == TMEM lane
+    const int i = q0 + row;       // query row within its block
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = T > 0;
+    for (int t = 0; t < T && ok; ++t) {
+      ok = mbar_wait(&bars[kSFull], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(tS + lane_off + 0, r0);
+      tmem_ld32(tS + lane_off + 32, r1);
+      tmem_ld32(tS + lane_off + 64, r2);
+      tmem_ld32(tS + lane_off + 96, r3);
+      tmem_ld_wait();
+      tmem_reg_fence(r0);
+      tmem_reg_fence(r1);
+      tmem_reg_fence(r2);
+      tmem_reg_fence(r3);
+      tc_fence_before();
+      mbar_arrive(&bars[kSFree]);
+
+      // number of leading visible columns of this tile for this row
+      int valid;
+      if (t < n_ct) {
+        valid = min(kTile, a.p - (ct_lo + t) * kTile);
+      } else {
+        const int col0 = (t - n_ct) * kTile;
+        valid = min(i, a.n_real - 1) - col0 + 1;
+        valid = max(0, min(valid, kTile));
+      }
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        s[c] = __uint_as_float(r0[c]);
+        s[32 + c] = __uint_as_float(r1[c]);
+        s[64 + c] = __uint_as_float(r2[c]);
+        s[96 + c] = __uint_as_float(r3[c]);
+      }
+      float rmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float x = (c < valid) ? s[c] * a.scale_log2 : -INFINITY;
+        s[c] = x;
+        rmax = fmaxf(rmax, x);
+      }
+      // Lazy rescaling: keep the stale max unless the new one exceeds it by
+      // more than 8 (P values then stay below 2^8, safe in bf16 / f32).
+      float alpha = 1.f;
+      bool rescale = false;
+      if (rmax > m + 8.f) {
+        alpha = exp2_approx(m - rmax);  // exp2(-inf) = 0 on the first tile
+        m = rmax;
+        rescale = t > 0;
+      }
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = exp2_approx(s[2 * c] - m);
+        const float p1 = exp2_approx(s[2 * c + 1] - m);
+        rs += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      if (t > 0) {
+        ok = mbar_wait(&bars[kODone], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int blk = 0; blk < D / 32; ++blk) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + blk * 32, o);
+            tmem_ld_wait();
+            tmem_reg_fence(o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tO + lane_off + blk * 32, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      l = l * alpha + rs;
+      // P row -> swizzled K-major tile: keys 0..63 in the first 16 KB atom
+      // column, 64..127 in the second.
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        uint4 v = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        *reinterpret_cast<uint4*>(sP + (c16 >> 3) * 16384 + sw128_offset(row, c16 & 7)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[kPFull]);
+    }
+    // ------------------------------------------------------------ epilogue --
+    if (ok) {
+      ok = mbar_wait(&bars[kODone], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool row_ok = i < a.n_rows;
+#pragma unroll
+      for (int blk = 0; blk < D / 32; ++blk) {
+        uint32_t o[32];
+        tmem_ld32(tO + lane_off + blk * 32, o);
+        tmem_ld_wait();
+        tmem_reg_fence(o);
+        if (row_ok) {
+          if (a.decode || a.out_f32) {
+            float* dst;
+            if (a.decode)
+              dst = static_cast<float*>(a.out) +
+                    ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i) * D;
+            else
+              dst = static_cast<float*>(a.out) +
+                    ((static_cast<long long>(qb) * a.n_rows + i) * a.Hq_map + head) * D;
+            float4* d4 = reinterpret_cast<float4*>(dst + blk * 32);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              d4[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l,
+                                  __uint_as_float(o[4 * c + 1]) * inv_l,
+                                  __uint_as_float(o[4 * c + 2]) * inv_l,
+                                  __uint_as_float(o[4 * c + 3]) * inv_l);
+          } else {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                                 ((static_cast<long long>(qb) * a.n_rows + i) * a.Hq_map + head) * D;
+            uint4* d4 = reinterpret_cast<uint4*>(dst + blk * 32);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              d4[c] = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[8 * c]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l));
+          }
+        }
+      }
+      if (row_ok) {
+        const float lse2 = m + __log2f(l);
+        if (a.decode)
+          a.lse[(static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i] = lse2;
+        else
+          a.lse[(static_cast<long long>(qb) * a.Hq_map + head) * a.n_rows + i] =
+              lse2 * 0.69314718055994531f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 256);
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
+  using L = FwdSmem<D>;
+  static_assert(L::kAlloc <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::kAlloc);
+  if (e != cudaSuccess) return e;
+  FwdParams p{};
+  p.n_rows = a.n_rows;
+  p.Hq_map = a.Hq_map;
+  p.G = a.G;
+  p.p = a.p;
+  p.n_real = a.n_real;
+  p.cart_tiles_per_split = a.cart_tiles_per_split;
+  p.n_qtiles = (a.n_rows + kTile - 1) / kTile;
+  p.scale_log2 = a.scale_log2;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.out_f32 = a.out_f32 ? 1 : 0;
+  p.decode = a.decode ? 1 : 0;
+  p.status = device_status_ptr();
+  dim3 grid;
+  if (!a.decode)
+    grid = dim3(a.Hq_map, a.n_qblocks, p.n_qtiles);
+  else
+    grid = dim3(a.Hq_map, p.n_qtiles, a.n_splits);
+  fwd_kernel<D><<<grid, 192, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
+  if (a.d == 128) return launch_fwd_d<128>(a, st);
+  if (a.d == 64) return launch_fwd_d<64>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cart

@@ -1,0 +1,121 @@
+// internal.cuh -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/cartattn.h"
+
+namespace cart {
+
+constexpr int kTile = 128;          // query rows / key rows per tcgen05 tile
+constexpr int kMaxHeadDim = 128;
+
+// Device status word (bits from ptx.cuh); one per device.
+uint32_t* device_status_ptr();
+
+// fp64 inverse frequencies theta^(-2j/d), j < d/2, passed by value.
+struct RopeFreqs {
+  double inv_freq[kMaxHeadDim / 2];
+};
+RopeFreqs make_rope_freqs(int d, double theta);
+
+// ----------------------------------------------------------------- misc ----
+// f32 -> bf16 / f32 row copy into a strided destination.
+cudaError_t launch_write_to_cache(const float* src, int p, int row_elems, void* dst,
+                                  long long row_stride, int dst_row0, bool dst_bf16,
+                                  cudaStream_t st);
+
+// cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2].
+cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
+                              cudaStream_t st);
+
+// Rotate rows of x [B, n, H, d] (bf16 or f32) at positions pos0 + i using the
+// table (row i of the table = position pos0 + i) and write bf16 to out (same
+// layout).  With rotate == false this is a plain convert/copy.
+cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, const float2* table,
+                             int B, int n, int H, int d, bool rotate, cudaStream_t st);
+
+// D[b, h, i] = sum_c dO[b,i,h,c] * O[b,i,h,c] (f32).
+cudaError_t launch_bwd_dot(const void* o, const void* dout, bool f32, float* Dvec, int B,
+                           int n, int Hq, int d, cudaStream_t st);
+
+// ------------------------------------------------------------- forward ----
+struct FwdLaunch {
+  const CUtensorMap* mQ;   // 4D (d, Hq_map, rows, blocks) bf16, 64x1x128x1 box, SW128
+  const CUtensorMap* mKc;  // 4D (d, Hkv, p, 1)
+  const CUtensorMap* mVc;
+  const CUtensorMap* mK;   // 4D (d, Hkv, n, B) rotated real keys
+  const CUtensorMap* mV;   // 4D (d, Hkv, n, B)
+  int d;
+  int n_rows;              // query rows per query block (n, or B*G for decode)
+  int n_qblocks;           // query blocks: B for training, 1 for decode
+  int Hq_map;              // heads in the query map
+  int G;                   // query heads per kv head (1 for decode: rows carry the group)
+  int p;                   // cartridge rows
+  int n_real;              // real key rows (0 for decode)
+  int cart_tiles_per_split;// decode: cartridge tiles per split (0 = all)
+  int n_splits;            // decode: number of splits
+  float scale_log2;        // scale * log2(e)
+  void* out;               // training: o [B, n, Hq, d]; decode: f32 partial [S, Hkv, R, d]
+  bool out_f32;
+  float* lse;              // training: [B, Hq, n]; decode: [S, Hkv, R]
+  bool decode;
+};
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
+
+// ------------------------------------------------------------ backward ----
+struct BwdLaunch {
+  const CUtensorMap* mQ;    // 4D (d, Hq, n, B) rotated queries (bf16), 128-row box
+  const CUtensorMap* mdO;   // 4D (d, Hq, n, B) dO (bf16), 128-row box
+  const CUtensorMap* mQ64;  // same tensors, 64-row box
+  const CUtensorMap* mdO64;
+  const CUtensorMap* mKc;   // 4D (d, Hkv, p, 1)
+  const CUtensorMap* mVc;
+  const CUtensorMap* mK;    // 4D (d, Hkv, n, B) rotated real keys
+  const CUtensorMap* mV;
+  int B, n, Hq, Hkv, d, p, frozen_prefix;
+  float scale;
+  const float* lse;         // [B, Hq, n] natural log
+  const float* Dvec;        // [B, Hq, n]
+  void* dq;                 // [B, n, Hq, d] output dtype
+  void* dk;                 // [B, n, Hkv, d]
+  void* dv;
+  bool out_f32;
+  float* dkc;               // [p, Hkv, d]
+  float* dvc;
+  int accumulate;
+  const float2* table;      // rope table for positions p .. p+n-1
+};
+// dK/dV kernel on st_dkdv, dQ kernel on st_dq (the two are independent).
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st_dkdv, cudaStream_t st_dq);
+
+// -------------------------------------------------------------- decode ----
+struct DecodeLaunch {
+  int B, Hq, Hkv, d, p, rows;
+  float scale;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const __nv_bfloat16* kc;
+  const __nv_bfloat16* vc;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  const int* len;
+  __nv_bfloat16* o;
+  __nv_bfloat16* q_rot;     // [B*G, Hkv, d]: row r = b*G + hh of kv head g
+  int n_cart_splits;
+  const float* cart_part;   // [S, Hkv, R, d]
+  const float* cart_lse;    // [S, Hkv, R]
+  float* priv_part;         // [B, Hkv, chunks, G, d]
+  float* priv_ml;           // [B, Hkv, chunks, G, 2]
+  int chunk;                // private keys per CTA
+};
+cudaError_t launch_decode_prep(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
+cudaError_t launch_decode_private(const DecodeLaunch& a, cudaStream_t st);
+cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t st);
+
+}  // namespace cart

@@ -1,0 +1,250 @@
+// misc.cu -- bandwidth-bound helper kernels of the cartridge-attention path:
+//   * the cartridge cache write (f32 leaves -> cache dtype), which also makes
+//     the bf16 shadow the tensor-core kernels read;
+//   * the RoPE cos/sin table for a run of positions (fp64 angle reduction);
+//   * rotation of real-token Q/K rows at positions p + i into bf16;
+//   * the backward's per-row D = rowsum(dO * O).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace cart {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(long long work, int per_block = kThreads) {
+  long long g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > 152 * 64) g = 152 * 64;  // grid-stride loops cover the rest
+  return static_cast<int>(g);
+}
+
+// ---------------------------------------------------------- cache write ----
+// One thread converts 8 consecutive values of one cartridge row.
+__global__ void write_to_cache_kernel(const float* __restrict__ src, int p, int row_elems,
+                                      void* __restrict__ dst, long long row_stride, int dst_row0,
+                                      int dst_bf16) {
+  const int vec_per_row = row_elems / 8;
+  const long long total = static_cast<long long>(p) * vec_per_row;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(t / vec_per_row);
+    const int c = static_cast<int>(t % vec_per_row) * 8;
+    const float4* s =
+        reinterpret_cast<const float4*>(src + static_cast<long long>(r) * row_elems + c);
+    const float4 a = __ldg(s), b = __ldg(s + 1);
+    const long long off = static_cast<long long>(dst_row0 + r) * row_stride + c;
+    if (dst_bf16) {
+      uint4 o;
+      o.x = pack_bf16x2(a.x, a.y);
+      o.y = pack_bf16x2(a.z, a.w);
+      o.z = pack_bf16x2(b.x, b.y);
+      o.w = pack_bf16x2(b.z, b.w);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + off) = o;
+    } else {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dst) + off);
+      d[0] = a;
+      d[1] = b;
+    }
+  }
+}
+
+// ----------------------------------------------------------- rope table ----
+// table[i * (d/2) + j] = (cos, sin) of (pos0 + i) * inv_freq[j].  The angle
+// is formed and reduced modulo 2*pi in fp64 (two-part 2*pi); the reduced
+// angle is split into an f32 head and tail so that cos/sin of the head plus
+// a first-order tail correction keep the table accurate to ~1e-7.
+__global__ void rope_table_kernel(float2* __restrict__ table, int pos0, int npos, int half,
+                                  const RopeFreqs f) {
+  const long long total = static_cast<long long>(npos) * half;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(t / half), j = static_cast<int>(t % half);
+    const double ang = static_cast<double>(pos0 + i) * f.inv_freq[j];
+    const double kTwoPiHi = 6.283185307179586232;   // nearest double to 2*pi
+    const double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+    const double k = rint(ang * 0.15915494309189535);
+    double r = fma(-k, kTwoPiHi, ang);
+    r = fma(-k, kTwoPiLo, r);
+    const float rh = static_cast<float>(r);
+    const float rl = static_cast<float>(r - static_cast<double>(rh));
+    float s, c;
+    sincosf(rh, &s, &c);
+    table[t] = make_float2(c - s * rl, s + c * rl);
+  }
+}
+
+// ----------------------------------------------------------- rope rows ----
+// x [B, n, H, d] -> out bf16 same layout.  One thread owns 8 consecutive
+// pair indices j..j+7 of one row: elements j.. and j+d/2.. .
+template <bool kF32>
+__global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __restrict__ out,
+                                 const float2* __restrict__ table, int B, int n, int H, int d,
+                                 int rotate) {
+  const int half = d / 2;
+  const int chunks = half / 8;
+  const long long total = static_cast<long long>(B) * n * H * chunks;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = t / chunks;  // (b * n + i) * H + h
+    const int j0 = static_cast<int>(t % chunks) * 8;
+    const int i = static_cast<int>((row / H) % n);
+    float x0[8], x1[8];
+    if (kF32) {
+      const float* x = static_cast<const float*>(xv) + row * d;
+      const float4* a = reinterpret_cast<const float4*>(x + j0);
+      const float4* b = reinterpret_cast<const float4*>(x + j0 + half);
+      float4 a0 = __ldg(a), a1 = __ldg(a + 1), b0 = __ldg(b), b1 = __ldg(b + 1);
+      x0[0] = a0.x; x0[1] = a0.y; x0[2] = a0.z; x0[3] = a0.w;
+      x0[4] = a1.x; x0[5] = a1.y; x0[6] = a1.z; x0[7] = a1.w;
+      x1[0] = b0.x; x1[1] = b0.y; x1[2] = b0.z; x1[3] = b0.w;
+      x1[4] = b1.x; x1[5] = b1.y; x1[6] = b1.z; x1[7] = b1.w;
+    } else {
+      const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(xv) + row * d;
+      uint4 a = __ldg(reinterpret_cast<const uint4*>(x + j0));
+      uint4 b = __ldg(reinterpret_cast<const uint4*>(x + j0 + half));
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 fa = __bfloat1622float2(pa[e]);
+        float2 fb = __bfloat1622float2(pb[e]);
+        x0[2 * e] = fa.x; x0[2 * e + 1] = fa.y;
+        x1[2 * e] = fb.x; x1[2 * e + 1] = fb.y;
+      }
+    }
+    float y0[8], y1[8];
+    if (rotate) {
+      const float2* tb = table + static_cast<long long>(i) * half + j0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 cs = __ldg(tb + e);
+        y0[e] = x0[e] * cs.x - x1[e] * cs.y;
+        y1[e] = x1[e] * cs.x + x0[e] * cs.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { y0[e] = x0[e]; y1[e] = x1[e]; }
+    }
+    uint4 o0, o1;
+    o0.x = pack_bf16x2(y0[0], y0[1]); o0.y = pack_bf16x2(y0[2], y0[3]);
+    o0.z = pack_bf16x2(y0[4], y0[5]); o0.w = pack_bf16x2(y0[6], y0[7]);
+    o1.x = pack_bf16x2(y1[0], y1[1]); o1.y = pack_bf16x2(y1[2], y1[3]);
+    o1.z = pack_bf16x2(y1[4], y1[5]); o1.w = pack_bf16x2(y1[6], y1[7]);
+    __nv_bfloat16* orow = out + row * d;
+    *reinterpret_cast<uint4*>(orow + j0) = o0;
+    *reinterpret_cast<uint4*>(orow + j0 + half) = o1;
+  }
+}
+
+// ------------------------------------------------------------- bwd dot ----
+// Dvec[b, h, i] = sum_c dO[b,i,h,c] * O[b,i,h,c]; 8 lanes per row, 4 rows
+// per warp; the loop trip count is uniform across the warp.
+template <bool kF32>
+__global__ void bwd_dot_kernel(const void* __restrict__ ov, const void* __restrict__ dov,
+                               float* __restrict__ Dvec, int B, int n, int Hq, int d) {
+  const long long rows = static_cast<long long>(B) * n * Hq;
+  const int lane8 = threadIdx.x & 7;
+  const int group = (threadIdx.x & 31) >> 3;
+  const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long base = warp_id * 4; base < rows; base += warps * 4) {
+    const long long row = base + group;
+    float acc = 0.f;
+    if (row < rows) {
+      for (int c = lane8 * 8; c < d; c += 64) {
+        if (kF32) {
+          const float4* o =
+              reinterpret_cast<const float4*>(static_cast<const float*>(ov) + row * d + c);
+          const float4* g =
+              reinterpret_cast<const float4*>(static_cast<const float*>(dov) + row * d + c);
+          float4 o0 = __ldg(o), o1 = __ldg(o + 1), g0 = __ldg(g), g1 = __ldg(g + 1);
+          acc += o0.x * g0.x + o0.y * g0.y + o0.z * g0.z + o0.w * g0.w;
+          acc += o1.x * g1.x + o1.y * g1.y + o1.z * g1.z + o1.w * g1.w;
+        } else {
+          uint4 o = __ldg(reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(ov) + row * d + c));
+          uint4 g = __ldg(reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(dov) + row * d + c));
+          const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&o);
+          const __nv_bfloat162* pg = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 fo = __bfloat1622float2(po[e]);
+            float2 fg = __bfloat1622float2(pg[e]);
+            acc += fo.x * fg.x + fo.y * fg.y;
+          }
+        }
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (lane8 == 0 && row < rows) {
+      const int h = static_cast<int>(row % Hq);
+      const long long bi = row / Hq;
+      const int i = static_cast<int>(bi % n);
+      const int b = static_cast<int>(bi / n);
+      Dvec[(static_cast<long long>(b) * Hq + h) * n + i] = acc;
+    }
+  }
+}
+
+}  // namespace
+
+RopeFreqs make_rope_freqs(int d, double theta) {
+  RopeFreqs f{};
+  for (int j = 0; j < d / 2 && j < kMaxHeadDim / 2; ++j)
+    f.inv_freq[j] = std::pow(theta, -2.0 * static_cast<double>(j) / static_cast<double>(d));
+  return f;
+}
+
+cudaError_t launch_write_to_cache(const float* src, int p, int row_elems, void* dst,
+                                  long long row_stride, int dst_row0, bool dst_bf16,
+                                  cudaStream_t st) {
+  if (p <= 0) return cudaSuccess;
+  const long long work = static_cast<long long>(p) * (row_elems / 8);
+  write_to_cache_kernel<<<grid_for(work), kThreads, 0, st>>>(src, p, row_elems, dst, row_stride,
+                                                             dst_row0, dst_bf16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
+                              cudaStream_t st) {
+  if (npos <= 0) return cudaSuccess;
+  const long long work = static_cast<long long>(npos) * (d / 2);
+  rope_table_kernel<<<grid_for(work), kThreads, 0, st>>>(table, pos0, npos, d / 2, f);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, const float2* table,
+                             int B, int n, int H, int d, bool rotate, cudaStream_t st) {
+  const long long work = static_cast<long long>(B) * n * H * (d / 16);
+  if (work <= 0) return cudaSuccess;
+  if (x_f32)
+    rope_rows_kernel<true><<<grid_for(work), kThreads, 0, st>>>(x, out, table, B, n, H, d,
+                                                                rotate ? 1 : 0);
+  else
+    rope_rows_kernel<false><<<grid_for(work), kThreads, 0, st>>>(x, out, table, B, n, H, d,
+                                                                 rotate ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dot(const void* o, const void* dout, bool f32, float* Dvec, int B, int n,
+                           int Hq, int d, cudaStream_t st) {
+  const long long rows = static_cast<long long>(B) * n * Hq;
+  if (rows <= 0) return cudaSuccess;
+  const int grid = grid_for(rows * 8);  // 8 threads per row
+  if (f32)
+    bwd_dot_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, Dvec, B, n, Hq, d);
+  else
+    bwd_dot_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, Dvec, B, n, Hq, d);
+  return cudaGetLastError();
+}
+
+}  // namespace cart
