@@ -1,0 +1,531 @@
+#!/usr/bin/env python
+"""Benchmark of the cartridge-attention hot path on GB300.
+
+One step = one pass over every step of the path on synthetic data:
+  a1  cartridge write: f32 leaf rows -> bf16 shadow        (cart_write_to_cache)
+  a2-a4  training forward (RoPE at p+i, end-aligned mask)  (cart_attn_fwd)
+  a5-a8  training backward into the cartridge rows          (cart_attn_bwd)
+         [N > 1: all-reduce(SUM) of the cartridge gradients]
+  a9  one decode step of 64 conversations behind a shared cartridge
+                                                            (cart_attn_decode)
+Workloads: self-study training B=4, Hq=32, Hkv=8, d=128, p=2048 (row 0
+frozen), n=1024, bf16 Q/K/V with f32 cartridge leaves; serving decode B=64,
+p=4096 shared, private lengths ~U{0..1024}.  `--workload longctx` swaps the
+training part for B=1, Hq=64, p=8192, n=4096.
+
+`value` is the training fwd+bwd throughput in algorithmic TFLOP/s (4*d FLOPs
+per visible (query, key) pair forward, 2.5x that backward), summed over
+ranks; the decode throughput (algorithmic HBM GB/s, the shared cartridge
+counted once) is reported under "decode".  L2 is flushed (256 MiB write)
+between timed steps, outside the timed events.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "cartridge-attn fwd+bwd TFLOP/s and decode HBM GB/s (% of GB300 roofline)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("selfstudy", "longctx"), default="selfstudy")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ peaks ----
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_src_sha(name: str) -> str:
+    csrc = os.path.join(ROOT, "trained_kv_prefix_gb300", "csrc")
+    files = {"bwd_dkdv": "bwd.cu", "bwd_dq": "bwd.cu", "fwd": "fwd.cu",
+             "decode_cartridge": "fwd.cu", "decode_private": "decode.cu",
+             "decode_combine": "decode.cu"}
+    f = files.get(name)
+    if f is None:
+        return ""
+    h = hashlib.sha256()
+    for part in (f, "ptx.cuh"):
+        with open(os.path.join(csrc, part), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, when it was taken
+    on the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_src_sha(kernel)
+    pat = re.compile(r"^\|\s*" + re.escape(kernel) + r"\s*\|\s*" + re.escape(workload) +
+                     r"\s*\|\s*(\d+)\s*\|\s*([0-9a-f]+)\s*\|")
+    with open(path) as f:
+        for line in f:
+            m = pat.match(line.strip())
+            if m and m.group(2) == sha:
+                return int(m.group(1))
+    return None
+
+
+# ----------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[0]), smax=float(parts[1]), power=float(parts[2]),
+                                 hw=parts[4], hwt=parts[5], swt=parts[6], swp=parts[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows), "samples": len(rows),
+                "samples_under_load": len(load), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- accounting ----
+def decode_bytes(s, lens) -> int:
+    """Algorithmic HBM bytes of one decode step: the shared cartridge once,
+    each conversation's private rows 0..L_b (K and V), q / k_new / v_new / o,
+    and the appended row."""
+    import numpy as np
+    row = s.Hkv * s.d * 2
+    L = np.asarray(lens, dtype=np.int64)
+    cart = 2 * s.p * row
+    priv = 2 * int((L + 1).sum()) * row
+    io = s.B * (2 * s.Hq * s.d * 2 + 2 * s.Hkv * s.d * 2) + 2 * s.B * row + s.B * 4
+    return cart + priv + io
+
+
+def kernel_work(name, ts, ds, lens):
+    """(amount, unit) of algorithmic work one launch of `name` performs."""
+    pairs = ts.B * ts.Hq * ts.pairs_per_head()
+    if name == "fwd":
+        return 4.0 * ts.d * pairs, "flop"
+    if name == "bwd_dkdv":   # S^T, dP^T, dV, dK: 4 of the 5 algorithmic GEMMs
+        return 8.0 * ts.d * pairs, "flop"
+    if name == "bwd_dq":     # dQ (the S and dP it recomputes are not counted)
+        return 2.0 * ts.d * pairs, "flop"
+    row = ds.Hkv * ds.d * 2
+    if name == "decode_cartridge":
+        return 2.0 * ds.p * row, "byte"
+    if name == "decode_private":
+        import numpy as np
+        return 2.0 * int((np.asarray(lens, np.int64) + 1).sum()) * row, "byte"
+    return None, None
+
+
+# ------------------------------------------------------------- reference ----
+def oracle_sample_flops(ts, heads, rows):
+    pairs = 0
+    for i in range(rows[0], rows[1]):
+        pairs += ts.p + i + 1
+    pairs *= ts.B * heads
+    return 4.0 * ts.d * pairs * 3.5   # fwd + bwd (2.5x)
+
+
+def run_oracle_sample(ts, inp64, kv_heads, rows):
+    import oracle
+    G = ts.Hq // ts.Hkv
+    oracle.fwd(inp64["q"], inp64["k"], inp64["v"], inp64["kc"], inp64["vc"], theta=ts.theta,
+               heads=(kv_heads[0] * G, kv_heads[1] * G), rows=rows)
+    oracle.bwd(inp64["q"], inp64["k"], inp64["v"], inp64["kc"], inp64["vc"], inp64["do"],
+               theta=ts.theta, kv_heads=kv_heads, rows=rows)
+
+
+def cpu_baseline(ts, target_s=15.0):
+    """The oracle as it stands, timed on this host's cores on a bounded sample
+    (query rows at the end of the sequence, half of the kv groups, every
+    sequence), sized for roughly `target_s` seconds."""
+    import oracle
+    from trained_kv_prefix_gb300 import synth
+    inp = synth.train_inputs(ts)
+    a = {k: synth.f64(v) for k, v in inp.items()}
+    kvh = (0, max(1, ts.Hkv // 2))
+    heads = (kvh[1] - kvh[0]) * (ts.Hq // ts.Hkv)
+    probe = (ts.n - 16, ts.n)
+    t0 = time.perf_counter()
+    run_oracle_sample(ts, a, kvh, probe)
+    dt = time.perf_counter() - t0
+    per_row = max(dt / 16, 1e-6)
+    nrows = int(max(16, min(ts.n, target_s / per_row)))
+    rows = (ts.n - nrows, ts.n)
+    t0 = time.perf_counter()
+    run_oracle_sample(ts, a, kvh, rows)
+    dt = time.perf_counter() - t0
+    flops = oracle_sample_flops(ts, heads, rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": (f"{ts.name} fwd+bwd, fp64 oracle, all {ts.B} sequences, kv groups "
+                       f"{kvh[0]}..{kvh[1] - 1} ({heads} query heads), query rows "
+                       f"{rows[0]}..{rows[1] - 1} of {ts.n}; algorithmic FLOPs of the sample")}
+
+
+def reference_arm(args, ts):
+    import oracle
+    from trained_kv_prefix_gb300 import dist as cdist, synth
+    rank, world, _ = cdist.env_rank_world()
+    if rank != 0:
+        return
+    oracle.build()
+    inp = synth.train_inputs(ts)
+    a = {k: synth.f64(v) for k, v in inp.items()}
+    kvh = (0, max(1, ts.Hkv // 2))
+    heads = (kvh[1] - kvh[0]) * (ts.Hq // ts.Hkv)
+    # size one step so that warmup + steps stay within ~150 s of CPU time
+    t0 = time.perf_counter()
+    run_oracle_sample(ts, a, kvh, (ts.n - 8, ts.n))
+    per_row = max((time.perf_counter() - t0) / 8, 1e-6)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nrows = int(max(1, min(ts.n, budget / per_row)))
+    rows = (ts.n - nrows, ts.n)
+    for _ in range(args.warmup):
+        run_oracle_sample(ts, a, kvh, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_sample(ts, a, kvh, rows)
+    dt = time.perf_counter() - t0
+    flops = oracle_sample_flops(ts, heads, rows) * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{ts.name} fwd+bwd, fp64 oracle, all {ts.B} sequences, {heads} query heads, "
+              f"query rows {rows[0]}..{rows[1] - 1} per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(ts), "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_name(ts):
+    return (f"{ts.name}-train B={ts.B} Hq={ts.Hq} Hkv={ts.Hkv} d={ts.d} p={ts.p} "
+            f"(row 0 frozen) n={ts.n} bf16/f32-leaves + serving-decode B=64 Hq=32 Hkv=8 d=128 "
+            f"p=4096 L~U{{0..1024}}")
+
+
+# ------------------------------------------------------------------ ours ----
+def main():
+    args = parse_args()
+    from trained_kv_prefix_gb300 import synth
+    ts = synth.SELFSTUDY if args.workload == "selfstudy" else synth.LONGCTX
+    if args.impl == "reference":
+        reference_arm(args, ts)
+        return
+
+    import numpy as np
+    import torch
+    from trained_kv_prefix_gb300 import build as cbuild
+    from trained_kv_prefix_gb300 import cartattn
+    from trained_kv_prefix_gb300 import dist as cdist
+
+    rank, world, local = cdist.env_rank_world()
+    has_pg = cdist.init_from_env("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        cbuild.build()
+    cdist.barrier(dev)
+    cartattn.lib()
+    peaks, peaks_src = load_peaks()
+    ds = synth.DECODE
+
+    # ---- inputs (per-rank seeds: every rank trains on its own sequences)
+    tin = {k: v.to(dev) for k, v in synth.train_inputs(ts, seed=ts.seed + 1000 * rank).items()}
+    din = {k: v.to(dev) for k, v in synth.decode_inputs(ds, seed=ds.seed + 1000 * rank).items()}
+    lens = din["lens"].cpu().numpy()
+    kcb = torch.empty(tin["kc"].shape, dtype=torch.bfloat16, device=dev)
+    vcb = torch.empty_like(kcb)
+    o = torch.empty_like(tin["q"])
+    lse = torch.empty((ts.B, ts.Hq, ts.n), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(tin["q"]), torch.empty_like(tin["k"]), torch.empty_like(tin["v"])
+    dkc = torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev)
+    dvc = torch.empty_like(dkc)
+    od = torch.empty_like(din["q"])
+    g = cartattn.geom(ts.B, ts.n, ts.Hq, ts.Hkv, ts.d, ts.p, ts.frozen_prefix, None, ts.theta)
+    ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(cartattn.bwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(cartattn.decode_workspace_size(ds.B, ds.Hq, ds.Hkv, ds.d, ds.p,
+                                                      ds.cache_rows), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def train_part():
+        cartattn.cart_write_to_cache(tin["kc"], tin["vc"], kcb, vcb)
+        cartattn.cart_attn_fwd(tin["q"], tin["k"], tin["v"], kcb, vcb, frozen_prefix=ts.frozen_prefix,
+                               theta=ts.theta, o=o, lse=lse, workspace=ws_f)
+        cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], kcb, vcb, o, lse, tin["do"],
+                               frozen_prefix=ts.frozen_prefix, theta=ts.theta, dq=dq, dk=dk, dv=dv,
+                               dkc=dkc, dvc=dvc, workspace=ws_b)
+        cdist.allreduce_cartridge_grads(dkc, dvc)
+
+    def decode_part():
+        cartattn.cart_attn_decode(din["q"], din["k_new"], din["v_new"], din["kc"], din["vc"],
+                                  din["k_cache"], din["v_cache"], din["lens"], theta=ds.theta,
+                                  o=od, workspace=ws_d)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        train_part()
+        decode_part()
+    torch.cuda.synchronize(dev)
+    assert cartattn.device_status() == 0
+
+    # ---- timed region
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    cdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    cartattn.trace_enable(True)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            evs[i][0].record(stream)
+            train_part()
+            evs[i][1].record(stream)
+            decode_part()
+            evs[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    cartattn.trace_enable(False)
+    cdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    status = cartattn.device_status()
+    train_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    trace = cartattn.trace_read(True)
+    n_launch = len(trace)
+    train_ms, dec_ms = cdist.max_over_ranks([train_ms, dec_ms], dev)
+
+    flops_step = ts.fwd_flops() + ts.bwd_flops()
+    value = world * flops_step * K / (train_ms * 1e-3) / 1e12
+    dbytes = decode_bytes(ds, lens)
+    dec_gbs = world * dbytes * K / (dec_ms * 1e-3) / 1e9
+
+    # ---- per-kernel device times from the trace (events on the launch stream)
+    per = {}
+    for name, ms in trace:
+        t = per.setdefault(name, [0, 0.0])
+        t[0] += 1
+        t[1] += ms
+    total_ms = sum(v[1] for v in per.values()) or 1.0
+    kernels = []
+    for name, (cnt, ms) in sorted(per.items(), key=lambda kv: -kv[1][1]):
+        amt, unit = kernel_work(name, ts, ds, lens)
+        ent = {"name": name, "launches": cnt, "total_ms": round(ms, 4),
+               "share": round(ms / total_ms, 4), "avg_us": round(ms / cnt * 1e3, 2)}
+        if amt is not None:
+            avg_s = ms / cnt * 1e-3
+            if unit == "flop":
+                ent.update(achieved=amt / avg_s / 1e12, unit="TFLOP/s",
+                           frac=amt / avg_s / 1e12 / peaks["bf16_tflops"])
+            else:
+                ent.update(achieved=amt / avg_s / 1e9, unit="GB/s",
+                           frac=amt / avg_s / 1e9 / peaks["hbm_gbs"])
+        kernels.append(ent)
+
+    def roofline_for(name):
+        ent = next((k for k in kernels if k["name"] == name), None)
+        if ent is None or "achieved" not in ent:
+            return None
+        tensor = ent["unit"] == "TFLOP/s"
+        amt, _ = kernel_work(name, ts, ds, lens)
+        rf = {"kernel": name, "bound": "tensor" if tensor else "hbm",
+              "achieved": ent["achieved"],
+              "peak": peaks["bf16_tflops"] if tensor else peaks["hbm_gbs"],
+              "unit": ent["unit"], "frac": ent["frac"],
+              "traffic": ncu_traffic(name, ts.name if tensor else ds.name),
+              "work_per_launch": amt, "work_unit": "FLOP" if tensor else "byte",
+              "peak_source": f"{peaks_src} (MEASURED_PEAKS.json bf16 burst)" if tensor
+              else f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs)"}
+        if tensor:
+            rf["frac_of_sustained"] = ent["achieved"] / peaks["bf16_tflops_sustained"]
+        return rf
+
+    train_kernels = [k for k in kernels if k["name"] in ("fwd", "bwd_dkdv", "bwd_dq")]
+    dominant = train_kernels[0]["name"] if train_kernels else kernels[0]["name"]
+    dec_kernels = [k for k in kernels if k["name"].startswith("decode")]
+    dec_dom = dec_kernels[0]["name"] if dec_kernels else None
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    dec_e2e = None
+    if args.e2e_steps > 0:
+        host = {k: v.cpu().pin_memory() for k, v in synth.train_inputs(
+            ts, seed=ts.seed + 1000 * rank).items()}
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        outs_h = {"dq": torch.empty_like(dq, device="cpu").pin_memory(),
+                  "dk": torch.empty_like(dk, device="cpu").pin_memory(),
+                  "dv": torch.empty_like(dv, device="cpu").pin_memory(),
+                  "dkc": torch.empty_like(dkc, device="cpu").pin_memory(),
+                  "dvc": torch.empty_like(dvc, device="cpu").pin_memory()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+
+        def e2e_step():
+            for k2, v in host.items():
+                dev_in[k2].copy_(v, non_blocking=True)
+            cartattn.cart_write_to_cache(dev_in["kc"], dev_in["vc"], kcb, vcb)
+            cartattn.cart_attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], kcb, vcb,
+                                   frozen_prefix=ts.frozen_prefix, theta=ts.theta, o=o, lse=lse,
+                                   workspace=ws_f)
+            cartattn.cart_attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], kcb, vcb, o, lse,
+                                   dev_in["do"], frozen_prefix=ts.frozen_prefix, theta=ts.theta,
+                                   dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc, workspace=ws_b)
+            cdist.allreduce_cartridge_grads(dkc, dvc)
+            for k2, t in (("dq", dq), ("dk", dk), ("dv", dv), ("dkc", dkc), ("dvc", dvc)):
+                outs_h[k2].copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        cdist.barrier(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = cdist.max_over_ranks([e0.elapsed_time(e1)], dev)[0]
+        e2e = {"value": world * flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.e2e_steps}
+        # decode end to end: the new token's q/k/v and lengths in, o out
+        dhost = {k: din[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "lens")}
+        od_h = torch.empty_like(od, device="cpu").pin_memory()
+
+        def dec_e2e_step():
+            for k2, v in dhost.items():
+                din[k2].copy_(v, non_blocking=True)
+            decode_part()
+            od_h.copy_(od, non_blocking=True)
+
+        dec_e2e_step()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            flush.zero_()
+            dec_e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dflush = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dflush[0].record(stream)
+        for _ in range(args.e2e_steps):
+            flush.zero_()
+        dflush[1].record(stream)
+        torch.cuda.synchronize(dev)
+        d_ms = max(e0.elapsed_time(e1) - dflush[0].elapsed_time(dflush[1]), 1e-6)
+        d_ms = cdist.max_over_ranks([d_ms], dev)[0]
+        dec_e2e = {"value": world * dbytes * args.e2e_steps / (d_ms * 1e-3) / 1e9, "unit": "GB/s",
+                   "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in dhost.values()),
+                   "d2h_bytes_per_step": od_h.numel() * od_h.element_size()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(ts)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": (train_ms + dec_ms) / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_name(ts), "global_batch": ts.B * world,
+                       "seq_len": ts.n, "cartridge_rows": ts.p,
+                       "decode_conversations": ds.B * world, "parallelism": f"dp{world}",
+                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "train_ms_per_step": train_ms / K, "decode_ms_per_step": dec_ms / K,
+                       "wall_s": round(wall, 3)},
+            "roofline": roofline_for(dominant),
+            "decode": {"metric": "decode HBM GB/s (shared cartridge counted once)",
+                       "value": dec_gbs, "unit": "GB/s", "bytes_per_step": dbytes,
+                       "frac": dec_gbs / world / peaks["hbm_gbs"],
+                       "roofline": roofline_for(dec_dom) if dec_dom else None, "e2e": dec_e2e},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,
+            "clocks": clk.summary(), "kernels": kernels, "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if has_pg:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

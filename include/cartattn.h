@@ -158,6 +158,20 @@ CART_API const char* cart_status_string(int status);
  * bit is set, or CART_ERR_CUDA. */
 CART_API int cart_device_status(unsigned* bits_out, int clear);
 
+/* ------------------------------------------------------------------------
+ * Launch tracing (off by default).  cart_trace_enable(1) clears the trace
+ * and starts recording: every later kernel launch of the library is
+ * bracketed by two CUDA events recorded on the launching stream.
+ * cart_trace_enable(0) stops recording and keeps what was recorded.
+ * cart_trace_count() returns the number of recorded launches (at most
+ * 65536).  cart_trace_get(i, ...) copies the kernel's name (NUL-terminated,
+ * truncated to name_len) and, if ms != NULL, waits for launch i to finish
+ * and writes its device time in milliseconds.  Not meant for use while a
+ * stream is being captured into a CUDA graph. */
+CART_API int cart_trace_enable(int on);
+CART_API int cart_trace_count(void);
+CART_API int cart_trace_get(int i, char* name, int name_len, float* ms);
+
 #ifdef __cplusplus
 }
 #endif

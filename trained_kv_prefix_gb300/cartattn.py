@@ -74,8 +74,12 @@ def lib():
             L.cart_status_string.argtypes = [i]
             L.cart_status_string.restype = ctypes.c_char_p
             L.cart_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+            L.cart_trace_enable.argtypes = [i]
+            L.cart_trace_count.argtypes = []
+            L.cart_trace_get.argtypes = [i, ctypes.c_char_p, i, ctypes.POINTER(ctypes.c_float)]
             for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd",
-                         "cart_attn_decode", "cart_device_status"):
+                         "cart_attn_decode", "cart_device_status", "cart_trace_enable",
+                         "cart_trace_count", "cart_trace_get"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -83,7 +87,8 @@ def lib():
 
 EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd",
            "cart_attn_bwd_workspace_size", "cart_attn_bwd", "cart_attn_decode_workspace_size",
-           "cart_attn_decode", "cart_status_string", "cart_device_status")
+           "cart_attn_decode", "cart_status_string", "cart_device_status", "cart_trace_enable",
+           "cart_trace_count", "cart_trace_get")
 
 
 def _check(fn: str, rc: int):
@@ -231,3 +236,22 @@ def device_status(clear: bool = True) -> int:
     if rc not in (0, -7):
         raise CartError("cart_device_status", rc)
     return int(bits.value)
+
+
+def trace_enable(on: bool = True):
+    """Start (clearing earlier records) or stop recording per-launch events."""
+    lib().cart_trace_enable(1 if on else 0)
+
+
+def trace_read(with_times: bool = True):
+    """List of (kernel name, device ms or None) for the recorded launches."""
+    L = lib()
+    out = []
+    buf = ctypes.create_string_buffer(32)
+    for i in range(L.cart_trace_count()):
+        ms = ctypes.c_float(-1.0)
+        rc = L.cart_trace_get(i, buf, 32, ctypes.byref(ms) if with_times else None)
+        if rc != 0 and with_times:
+            raise CartError("cart_trace_get", rc)
+        out.append((buf.value.decode(), float(ms.value) if with_times else None))
+    return out

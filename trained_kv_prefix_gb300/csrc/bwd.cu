@@ -773,11 +773,14 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
                            DqSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_blocks = p.n_ct * p.Hkv + p.n_rt * p.Hkv * p.B;
-  if (n_blocks > 0)
+  if (n_blocks > 0) {
+    TraceScope tr("bwd_dkdv", st_dkdv);
     dkdv_kernel<D><<<n_blocks, 192, DkdvSmem<D>::kAlloc, st_dkdv>>>(
         *l.mQ64, *l.mdO64, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  TraceScope tr("bwd_dq", st_dq);
   dq_kernel<D><<<dim3(p.Hq, p.B, p.n_qtiles), 192, DqSmem<D>::kAlloc, st_dq>>>(
       *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
   return cudaGetLastError();

@@ -280,6 +280,7 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, cudaStream_t st) {
   constexpr int CH = 128;
   const dim3 grid((a.rows + CH - 1) / CH, a.Hkv, a.B);
   const float scale_log2 = a.scale * 1.4426950408889634f;
+  TraceScope tr("decode_private", st);
   decode_private_kernel<D, G, CH><<<grid, 128, 0, st>>>(a, scale_log2);
   return cudaGetLastError();
 }
@@ -287,6 +288,7 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_decode_prep(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
+  TraceScope tr("decode_prep", st);
   decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
   return cudaGetLastError();
 }
@@ -313,6 +315,7 @@ cudaError_t launch_decode_private(const DecodeLaunch& a, cudaStream_t st) {
 }
 
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t st) {
+  TraceScope tr("decode_combine", st);
   decode_combine_kernel<128><<<a.B * a.Hq, a.d, 0, st>>>(a);
   return cudaGetLastError();
 }

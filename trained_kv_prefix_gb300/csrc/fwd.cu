@@ -430,6 +430,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
     grid = dim3(a.Hq_map, a.n_qblocks, p.n_qtiles);
   else
     grid = dim3(a.Hq_map, p.n_qtiles, a.n_splits);
+  TraceScope tr(a.decode ? "decode_cartridge" : "fwd", st);
   fwd_kernel<D><<<grid, 192, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
   return cudaGetLastError();
 }

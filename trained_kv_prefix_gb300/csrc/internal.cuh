@@ -17,6 +17,19 @@ constexpr int kMaxHeadDim = 128;
 // Device status word (bits from ptx.cuh); one per device.
 uint32_t* device_status_ptr();
 
+// Launch tracing (trace.cu): brackets a launch with events on its stream
+// while tracing is enabled.
+int trace_begin(const char* name, cudaStream_t st);
+void trace_end(int slot, cudaStream_t st);
+struct TraceScope {
+  int slot;
+  cudaStream_t st;
+  TraceScope(const char* name, cudaStream_t s) : slot(trace_begin(name, s)), st(s) {}
+  ~TraceScope() { trace_end(slot, st); }
+  TraceScope(const TraceScope&) = delete;
+  TraceScope& operator=(const TraceScope&) = delete;
+};
+
 // fp64 inverse frequencies theta^(-2j/d), j < d/2, passed by value.
 struct RopeFreqs {
   double inv_freq[kMaxHeadDim / 2];

@@ -209,6 +209,7 @@ cudaError_t launch_write_to_cache(const float* src, int p, int row_elems, void* 
                                   cudaStream_t st) {
   if (p <= 0) return cudaSuccess;
   const long long work = static_cast<long long>(p) * (row_elems / 8);
+  TraceScope tr("write_to_cache", st);
   write_to_cache_kernel<<<grid_for(work), kThreads, 0, st>>>(src, p, row_elems, dst, row_stride,
                                                              dst_row0, dst_bf16 ? 1 : 0);
   return cudaGetLastError();
@@ -218,6 +219,7 @@ cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const Ro
                               cudaStream_t st) {
   if (npos <= 0) return cudaSuccess;
   const long long work = static_cast<long long>(npos) * (d / 2);
+  TraceScope tr("rope_table", st);
   rope_table_kernel<<<grid_for(work), kThreads, 0, st>>>(table, pos0, npos, d / 2, f);
   return cudaGetLastError();
 }
@@ -226,6 +228,7 @@ cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, cons
                              int B, int n, int H, int d, bool rotate, cudaStream_t st) {
   const long long work = static_cast<long long>(B) * n * H * (d / 16);
   if (work <= 0) return cudaSuccess;
+  TraceScope tr(rotate ? "rope_rows" : "to_bf16", st);
   if (x_f32)
     rope_rows_kernel<true><<<grid_for(work), kThreads, 0, st>>>(x, out, table, B, n, H, d,
                                                                 rotate ? 1 : 0);
@@ -240,6 +243,7 @@ cudaError_t launch_bwd_dot(const void* o, const void* dout, bool f32, float* Dve
   const long long rows = static_cast<long long>(B) * n * Hq;
   if (rows <= 0) return cudaSuccess;
   const int grid = grid_for(rows * 8);  // 8 threads per row
+  TraceScope tr("bwd_dot", st);
   if (f32)
     bwd_dot_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, Dvec, B, n, Hq, d);
   else
