@@ -149,6 +149,34 @@ CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale,
                      const int* priv_len, void* o, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* ------------------------------------------------------------------------
+ * cart_attn_decode_noalloc -- the decode step of cart_attn_decode for
+ * callers that cannot allocate device memory: a serving loop running under a
+ * fixed device-memory budget planned at start-up (a cudaMalloc on the decode
+ * path would synchronize the device and stall the other streams), or a plain
+ * C host that links only this library and has no device allocator to carve a
+ * workspace from.  The paper has no counterpart; this is a library service.
+ *   Arguments, layouts and results are those of cart_attn_decode, without
+ *   the workspace: the scratch is a static device array of
+ *   CART_DECODE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the
+ *   library holds until the process exits.  (The 64-conversation, p = 4096,
+ *   1025-row serving shape needs about 18.5 MB.)
+ *   Returns CART_ERR_WORKSPACE, without touching the device, when the
+ *   problem needs more scratch than that; otherwise as cart_attn_decode.
+ *   Calls no cudaMalloc / cudaFree or allocating library routine.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  All calls share the one array: calls whose work can
+ *   overlap on the GPU (other streams, or other host threads without
+ *   ordering) race on it and must be serialised by the caller.  Nothing in
+ *   the array needs clearing between calls.                               */
+#define CART_DECODE_NOALLOC_SCRATCH_BYTES (24u << 20)
+CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, int p, float scale,
+                                      double rope_theta, const void* q, const void* k_new,
+                                      const void* v_new, const void* kc, const void* vc,
+                                      void* k_cache, void* v_cache, int cache_rows,
+                                      const int* priv_len, void* o, void* stream);
+
 /* Human-readable name of a cart_status value (static string). */
 CART_API const char* cart_status_string(int status);
 

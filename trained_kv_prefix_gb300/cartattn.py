@@ -88,7 +88,7 @@ def lib():
 EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd",
            "cart_attn_bwd_workspace_size", "cart_attn_bwd", "cart_attn_decode_workspace_size",
            "cart_attn_decode", "cart_status_string", "cart_device_status", "cart_trace_enable",
-           "cart_trace_count", "cart_trace_get")
+           "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc")
 
 
 def _check(fn: str, rc: int):
