@@ -50,19 +50,6 @@ struct BwdParams {
   uint32_t* status;
 };
 
-// K-major operand descriptor: `k` is the 16-element K step; atom columns
-// (64 elements of K) are `atom_stride` bytes apart (= rows * 128 B).
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int k, uint32_t atom_stride) {
-  return sdesc_sw128(base + static_cast<uint32_t>(k >> 2) * atom_stride +
-                         static_cast<uint32_t>(k & 3) * 32u,
-                     16u, 1024u);
-}
-// MN-major operand descriptor: `k` steps 16 rows along K (2 x 1024 B groups);
-// 64-wide M/N blocks are `block_stride` bytes apart.
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int k, uint32_t block_stride) {
-  return sdesc_sw128(base + static_cast<uint32_t>(k) * 2048u, block_stride, 1024u);
-}
-
 __device__ __forceinline__ void store_row_out(void* base, long long off, const float* x, int n,
                                               bool f32) {
   if (f32) {
@@ -79,24 +66,32 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 }
 
 // =========================================================== dK / dV ======
+// Threads: warps 0-3 and 4-7 are two P^T / dS^T warpgroups that take
+// alternate 64-query steps (thread t of a group owns key row t = TMEM lane
+// t), warp 8 is the TMA producer, warp 9 issues the MMAs.
+// TMEM (512 columns): step buffer x in {0,1} holds S^T at columns x*64 and
+// dP^T at 128 + x*64 (64 f32 columns each); the warpgroup overwrites their
+// first 32 columns with P^T and dS^T packed as bf16 pairs, which the dV and
+// dK MMAs then read as their A operand straight from TMEM.  dV accumulates
+// at 256, dK at 384.
+constexpr int kDkdvThreads = 320;
+
 template <int D>
 struct DkdvSmem {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 3;
   static constexpr int kKV = kTile * D * 2;        // resident K or V tile
   static constexpr int kQT = 64 * D * 2;           // 64-row Q or dO tile
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKV;
   static constexpr int kStage0 = kV + kKV;         // stage s: Q at +0, dO at +kQT
-  static constexpr int kPT = kStage0 + kStages * 2 * kQT;
-  static constexpr int kDST = kPT + kTile * 64 * 2;
-  static constexpr int kVec = kDST + kTile * 64 * 2;  // stage s: lse2[64], D[64]
+  static constexpr int kVec = kStage0 + kStages * 2 * kQT;  // stage s: lse2[64], D[64]
   static constexpr int kBar = kVec + kStages * 512;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-enum DkdvBar { kResFull = 0, kQdoFull0, kQdoFull1, kQdoEmpty0, kQdoEmpty1, kStFull0, kStFull1,
-               kStFree0, kStFree1, kDsFull, kDsFree, kAccDone, kDkdvDrain, kDkdvBars };
+enum DkdvBar { kResFull = 0, kQdoFull0, kQdoEmpty0 = kQdoFull0 + 3, kStFull0 = kQdoEmpty0 + 3,
+               kDsFull0 = kStFull0 + 2, kAccDone = kDsFull0 + 2, kDkdvDrain, kDkdvBars };
 
 struct DkdvItem {
   int b, hh, qt;
@@ -120,13 +115,29 @@ __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& a, bool cart, int
   return it;
 }
 
+__device__ __forceinline__ void write_cart_row(float* dst, const float* x, int n, bool frozen,
+                                               int accumulate) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  for (int c = 0; c < n / 4; ++c) {
+    float4 v = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+    if (frozen) {
+      v = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (accumulate) {
+      const float4 o = d4[c];
+      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+    }
+    d4[c] = v;
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap mQ64, const __grid_constant__ CUtensorMap mdO64,
                 const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const BwdParams a) {
   using L = DkdvSmem<D>;
+  constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -156,21 +167,19 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars[kResFull], 1);
-    mbar_init(&bars[kQdoFull0], 32);
-    mbar_init(&bars[kQdoFull1], 32);
-    mbar_init(&bars[kQdoEmpty0], 1);
-    mbar_init(&bars[kQdoEmpty1], 1);
-    mbar_init(&bars[kStFull0], 1);
-    mbar_init(&bars[kStFull1], 1);
-    mbar_init(&bars[kStFree0], 128);
-    mbar_init(&bars[kStFree1], 128);
-    mbar_init(&bars[kDsFull], 128);
-    mbar_init(&bars[kDsFree], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars[kQdoFull0 + s], 32);
+      mbar_init(&bars[kQdoEmpty0 + s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[kStFull0 + x], 1);
+      mbar_init(&bars[kDsFull0 + x], 128);
+    }
     mbar_init(&bars[kAccDone], 1);
     mbar_init(&bars[kDkdvDrain], 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -182,11 +191,9 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_p = &abort_flag;
   uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
-  uint8_t* sPT = smem + L::kPT;
-  uint8_t* sDST = smem + L::kDST;
   float* vec = reinterpret_cast<float*>(smem + L::kVec);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer --
     bool ok = U > 0;
     if (ok && lane == 0) {
@@ -206,9 +213,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     int issued = 0;
     for (int u = 0; u < U && ok; ++u) {
-      const int s = u % L::kStages;
-      if (u >= L::kStages) {
-        ok = mbar_wait(&bars[kQdoEmpty0 + s], ((u / L::kStages) - 1) & 1, abort_p, a.status,
+      const int s = u % S;
+      if (u >= S) {
+        ok = mbar_wait(&bars[kQdoEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
                        kDevErrTimeoutTma);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(192, 1)
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
       const int h = g * a.G + it.hh;
       float* lse2 = vec + s * 128;
-      float* dv = lse2 + 64;
+      float* dvv = lse2 + 64;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int c = lane + 32 * r;
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(192, 1)
           dd = __ldg(a.Dvec + idx);
         }
         lse2[c] = l2;
-        dv[c] = dd;
+        dvv[c] = dd;
       }
       if (lane == 0) {
         uint8_t* sQ = smem + L::kStage0 + s * 2 * L::kQT;
@@ -248,64 +255,69 @@ __global__ void __launch_bounds__(192, 1)
     if (!ok && lane == 0 && U > 0) {
       int dummy = 0;
       mbar_wait(&bars[kResFull], 0, &dummy, nullptr, 0);
-      for (int u = max(issued - L::kStages, 0); u < issued; ++u)
-        mbar_wait(&bars[kQdoFull0 + u % L::kStages], (u / L::kStages) & 1, &dummy, nullptr, 0);
+      for (int u = max(issued - S, 0); u < issued; ++u)
+        mbar_wait(&bars[kQdoFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA --
     if (lane == 0 && U > 0) {
       const uint32_t idST = idesc_bf16(128, 64, false, false);
       const uint32_t idACC = idesc_bf16(128, D, false, true);
-      const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
-      const uint32_t pt_base = smem_u32(sPT), dst_base = smem_u32(sDST);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16u, 1024u);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16u, 1024u);
+      const uint64_t dQk0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16u, 1024u);    // K-major
+      const uint64_t dQm0 = sdesc_sw128(smem_u32(smem + L::kStage0), 8192u, 1024u);  // MN-major
+      constexpr uint32_t kStageBytes = 2 * L::kQT;
       bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma);
+      // dV += P^T dO and dK += dS^T Q for step u: A from TMEM (buffer u&1),
+      // B = the step's dO / Q tile as MN-major operands (64 rows = 4 K steps).
       auto issue_acc = [&](int u) {
-        const int s = u % L::kStages;
-        const uint32_t q_base = smem_u32(smem + L::kStage0 + s * 2 * L::kQT);
-        const uint32_t do_base = q_base + L::kQT;
+        const int s = u % S, x = u & 1;
+        const uint32_t so = s * kStageBytes;
+        const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kQT);
+        const uint32_t pt = tST0 + x * 64, dst = tDP0 + x * 64;
+        const uint32_t first = u > 0 ? 1u : 0u;
+        umma_bf16_ts(tDV, pt, ddo, idACC, first);
+        umma_bf16_ts(tDK, dst, dq, idACC, first);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // 64 queries = 4 K steps
-          umma_bf16_ss(tDV, kdesc(pt_base, k, 16384u), mndesc(do_base, k, 8192u), idACC,
-                       (u > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_bf16_ss(tDK, kdesc(dst_base, k, 16384u), mndesc(q_base, k, 8192u), idACC,
-                       (u > 0 || k > 0) ? 1u : 0u);
-        umma_commit(&bars[kDsFree]);
+        for (int k = 1; k < 4; ++k) {
+          umma_bf16_ts(tDV, pt + k * 8, desc_add(ddo, k * 2048), idACC, 1u);
+          umma_bf16_ts(tDK, dst + k * 8, desc_add(dq, k * 2048), idACC, 1u);
+        }
         umma_commit(&bars[kQdoEmpty0 + s]);
       };
       for (int u = 0; u < U && ok; ++u) {
-        const int s = u % L::kStages, x = u & 1;
-        ok = mbar_wait(&bars[kQdoFull0 + s], (u / L::kStages) & 1, abort_p, a.status,
-                       kDevErrTimeoutMma);
+        const int s = u % S, x = u & 1;
+        ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status, kDevErrTimeoutMma);
         if (!ok) break;
-        if (u >= 2) {
-          ok = mbar_wait(&bars[kStFree0 + x], ((u >> 1) - 1) & 1, abort_p, a.status,
-                         kDevErrTimeoutMma);
-          if (!ok) break;
-        }
         tc_fence_after();
-        const uint32_t q_base = smem_u32(smem + L::kStage0 + s * 2 * L::kQT);
-        const uint32_t do_base = q_base + L::kQT;
+        // buffer x was last read by the dV/dK MMAs of step u-2, issued before
+        // this point: the tensor pipe runs one CTA's MMAs in issue order.
+        const uint32_t so = s * kStageBytes;
+        const uint64_t dq = desc_add(dQk0, so), ddo = desc_add(dQk0, so + L::kQT);
+        const uint32_t tst = tST0 + x * 64, tdp = tDP0 + x * 64;
+        umma_bf16_ss(tst, dK0, dq, idST, 0u);
+        umma_bf16_ss(tdp, dV0, ddo, idST, 0u);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16_ss(tST0 + x * 64, kdesc(k_base, k, 16384u), kdesc(q_base, k, 8192u), idST,
-                       k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16_ss(tDP0 + x * 64, kdesc(v_base, k, 16384u), kdesc(do_base, k, 8192u), idST,
-                       k > 0 ? 1u : 0u);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t offa = (k >> 2) * 16384 + (k & 3) * 32;
+          const uint32_t offb = (k >> 2) * 8192 + (k & 3) * 32;
+          umma_bf16_ss(tst, desc_add(dK0, offa), desc_add(dq, offb), idST, 1u);
+          umma_bf16_ss(tdp, desc_add(dV0, offa), desc_add(ddo, offb), idST, 1u);
+        }
         umma_commit(&bars[kStFull0 + x]);
         if (u > 0) {
-          ok = mbar_wait(&bars[kDsFull], (u - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+          ok = mbar_wait(&bars[kDsFull0 + (x ^ 1)], ((u - 1) >> 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           issue_acc(u - 1);
         }
       }
       if (ok) {
-        ok = mbar_wait(&bars[kDsFull], (U - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kDsFull0 + ((U - 1) & 1)], ((U - 1) >> 1) & 1, abort_p, a.status,
+                       kDevErrTimeoutMma);
         if (ok) {
           tc_fence_after();
           issue_acc(U - 1);
@@ -318,75 +330,71 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ P^T / dS^T warpgroup --
-    const int row = threadIdx.x;  // key row within the tile == TMEM lane
+    // ------------------------------------------- P^T / dS^T warpgroups 0, 1 --
+    const int wg = warp >> 2;
+    const int row = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const int j = tile * kTile + row;
     const bool key_ok = cart ? (j < a.p) : (j < a.n);
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    bool ok = U > 0;
-    for (int u = 0; u < U && ok; ++u) {
-      const int s = u % L::kStages, x = u & 1;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tst = tST0 + wg * 64 + lane_off, tdp = tDP0 + wg * 64 + lane_off;
+    bool ok = U > wg;
+    for (int u = wg; u < U && ok; u += 2) {
+      const int s = u % S;
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
-      ok = mbar_wait(&bars[kStFull0 + x], (u >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      // acquire the lse / D vectors the producer lanes published with kQdoFull
-      // (already complete: the MMAs behind kStFull waited for it)
-      ok = mbar_wait(&bars[kQdoFull0 + s], (u / L::kStages) & 1, abort_p, a.status,
-                     kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kStFull0 + wg], (u >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      // acquire the lse / D vectors the producer lanes published with
+      // kQdoFull (already complete: the MMAs behind kStFull waited for it)
+      if (ok) ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status,
+                             kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s0[32], s1[32], d0[32], d1[32];
-      tmem_ld32(tST0 + x * 64 + lane_off, s0);
-      tmem_ld32(tST0 + x * 64 + lane_off + 32, s1);
-      tmem_ld32(tDP0 + x * 64 + lane_off, d0);
-      tmem_ld32(tDP0 + x * 64 + lane_off + 32, d1);
-      tmem_ld_wait();
-      tmem_reg_fence(s0);
-      tmem_reg_fence(s1);
-      tmem_reg_fence(d0);
-      tmem_reg_fence(d1);
-      tc_fence_before();
-      mbar_arrive(&bars[kStFree0 + x]);
-      const float* lse2 = vec + s * 128;
-      const float* dvv = lse2 + 64;
-      // query q = qt*64 + c sees key j: cartridge always; real iff j <= q
-      int qlim = cart ? 64 : (j - it.qt * 64);  // columns c < qlim are masked for real keys
+      // columns c < qlim are invisible: none for a cartridge key, those with
+      // query < key for a real key, all for rows past the end of the keys
+      const int qlim = !key_ok ? 64 : (cart ? 0 : j - it.qt * 64);
+      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 128);
+      const float4* dv4 = reinterpret_cast<const float4*>(vec + s * 128 + 64);
       uint32_t pk[32], dk[32];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float pv[2], dsv[2];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tst + half * 32, sr);
+        tmem_ld32(tdp + half * 32, dr);
+        tmem_ld_wait();
+        tmem_reg_fence(sr);
+        tmem_reg_fence(dr);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int cc = c + e;
-          const float sv = __uint_as_float(cc < 32 ? s0[cc] : s1[cc - 32]);
-          const float dp = __uint_as_float(cc < 32 ? d0[cc] : d1[cc - 32]);
-          const bool vis = key_ok && (cart || cc >= qlim);
-          const float pe = vis ? exp2_approx(sv * a.scale_log2 - lse2[cc]) : 0.f;
-          pv[e] = pe;
-          dsv[e] = pe * (dp - dvv[cc]);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = lse4[half * 8 + c4];
+          const float4 d4 = dv4[half * 8 + c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dsv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = half * 32 + c4 * 4 + e;
+            const float x = fmaf(__uint_as_float(sr[c4 * 4 + e]), a.scale_log2, -lv[e]);
+            const float pe = (cc >= qlim) ? exp2_approx(x) : 0.f;
+            pv[e] = pe;
+            dsv[e] = pe * (__uint_as_float(dr[c4 * 4 + e]) - dd[e]);
+          }
+          pk[half * 16 + c4 * 2] = pack_bf16x2(pv[0], pv[1]);
+          pk[half * 16 + c4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk[half * 16 + c4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
+          dk[half * 16 + c4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
-        pk[c / 2] = pack_bf16x2(pv[0], pv[1]);
-        dk[c / 2] = pack_bf16x2(dsv[0], dsv[1]);
       }
-      if (u > 0) {
-        ok = mbar_wait(&bars[kDsFree], (u - 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16) {
-        *reinterpret_cast<uint4*>(sPT + sw128_offset(row, c16)) =
-            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-        *reinterpret_cast<uint4*>(sDST + sw128_offset(row, c16)) =
-            make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
-      }
-      fence_proxy_async_smem();
+      // P^T and dS^T over the first 32 columns of S^T and dP^T (both were
+      // read above by this thread's own lane)
+      tmem_st32(tst, pk);
+      tmem_st32(tdp, dk);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[kDsFull]);
+      mbar_arrive(&bars[kDsFull0 + wg]);
     }
     // ------------------------------------------------------------ epilogue --
+    // warpgroup 0 writes dV, warpgroup 1 writes dK
+    ok = ok || U <= wg;
     if (ok) {
       ok = mbar_wait(&bars[kAccDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
@@ -394,61 +402,25 @@ __global__ void __launch_bounds__(192, 1)
     if (ok) {
       tc_fence_after();
       float kv[D];
-      // dV row
+      const uint32_t src = (wg == 0 ? tDV : tDK) + lane_off;
+      const float mul = wg == 0 ? 1.f : a.scale;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tDV + lane_off + c * 32, r);
+        tmem_ld32(src + c * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) kv[c * 32 + e] = __uint_as_float(r[e]);
+        for (int e = 0; e < 32; ++e) kv[c * 32 + e] = __uint_as_float(r[e]) * mul;
       }
       if (key_ok) {
+        const bool frozen = j < a.frozen_prefix;
         if (cart) {
-          float* dst = a.dvc + (static_cast<long long>(j) * a.Hkv + g) * D;
-          float4* d4 = reinterpret_cast<float4*>(dst);
-          const bool frozen = j < a.frozen_prefix;
-          for (int c = 0; c < D / 4; ++c) {
-            float4 v = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
-            if (frozen) {
-              v = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else if (a.accumulate) {
-              const float4 o = d4[c];
-              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-            }
-            d4[c] = v;
-          }
-        } else {
+          float* dst = (wg == 0 ? a.dvc : a.dkc) + (static_cast<long long>(j) * a.Hkv + g) * D;
+          write_cart_row(dst, kv, D, frozen, a.accumulate);
+        } else if (wg == 0) {
           store_row_out(a.dv, ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D, kv, D,
                         a.out_f32 != 0);
-        }
-      }
-      // dK row (scaled), rotated back for real keys
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tDK + lane_off + c * 32, r);
-        tmem_ld_wait();
-        tmem_reg_fence(r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) kv[c * 32 + e] = __uint_as_float(r[e]) * a.scale;
-      }
-      if (key_ok) {
-        if (cart) {
-          float* dst = a.dkc + (static_cast<long long>(j) * a.Hkv + g) * D;
-          float4* d4 = reinterpret_cast<float4*>(dst);
-          const bool frozen = j < a.frozen_prefix;
-          for (int c = 0; c < D / 4; ++c) {
-            float4 v = make_float4(kv[4 * c], kv[4 * c + 1], kv[4 * c + 2], kv[4 * c + 3]);
-            if (frozen) {
-              v = make_float4(0.f, 0.f, 0.f, 0.f);
-            } else if (a.accumulate) {
-              const float4 o = d4[c];
-              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-            }
-            d4[c] = v;
-          }
         } else {
           const float2* tb = a.table + static_cast<long long>(j) * (D / 2);
 #pragma unroll
@@ -468,7 +440,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 // ================================================================ dQ ======
@@ -588,15 +560,21 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && T > 0) {
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idDQ = idesc_bf16(128, D, false, true);
-      const uint32_t q_base = smem_u32(sQ), do_base = smem_u32(sdO), ds_base = smem_u32(sDS);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
+      const uint64_t dO0 = sdesc_sw128(smem_u32(sdO), 16u, 1024u);
+      const uint64_t dS0 = sdesc_sw128(smem_u32(sDS), 16u, 1024u);
+      const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);      // K-major
+      const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kK), 16384u, 1024u);   // MN-major
+      const uint64_t dVk0 = sdesc_sw128(smem_u32(smem + L::kV), 16u, 1024u);
       bool ok = mbar_wait(&bars[kQdFull], 0, abort_p, a.status, kDevErrTimeoutMma);
       auto issue_dq = [&](int t) {
         const int sp = t & 1;
-        const uint32_t k_base = smem_u32(smem + L::kK + sp * L::kT);
+        const uint64_t dkm = desc_add(dKm0, sp * L::kT);
+        umma_bf16_ss(tDQ, dS0, dkm, idDQ, t > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          umma_bf16_ss(tDQ, kdesc(ds_base, k, 16384u), mndesc(k_base, k, 16384u), idDQ,
-                       (t > 0 || k > 0) ? 1u : 0u);
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ss(tDQ, desc_add(dS0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(dkm, k * 2048),
+                       idDQ, 1u);
         umma_commit(&bars[kDqDone]);
         umma_commit(&bars[kKvEmpty0 + sp]);
       };
@@ -609,16 +587,15 @@ __global__ void __launch_bounds__(192, 1)
           if (!ok) break;
         }
         tc_fence_after();
-        const uint32_t k_base = smem_u32(smem + L::kK + s * L::kT);
-        const uint32_t v_base = smem_u32(smem + L::kV + s * L::kT);
+        const uint64_t dk = desc_add(dKk0, s * L::kT), dv = desc_add(dVk0, s * L::kT);
+        umma_bf16_ss(tS, dQ0, dk, idS, 0u);
+        umma_bf16_ss(tDP, dO0, dv, idS, 0u);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16_ss(tS, kdesc(q_base, k, 16384u), kdesc(k_base, k, 16384u), idS,
-                       k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16_ss(tDP, kdesc(do_base, k, 16384u), kdesc(v_base, k, 16384u), idS,
-                       k > 0 ? 1u : 0u);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          umma_bf16_ss(tS, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
+          umma_bf16_ss(tDP, desc_add(dO0, off), desc_add(dv, off), idS, 1u);
+        }
         umma_commit(&bars[kSdFull]);
         if (t > 0) {
           ok = mbar_wait(&bars[kDsdFull], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
@@ -775,7 +752,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   const int n_blocks = p.n_ct * p.Hkv + p.n_rt * p.Hkv * p.B;
   if (n_blocks > 0) {
     TraceScope tr("bwd_dkdv", st_dkdv);
-    dkdv_kernel<D><<<n_blocks, 192, DkdvSmem<D>::kAlloc, st_dkdv>>>(
+    dkdv_kernel<D><<<n_blocks, kDkdvThreads, DkdvSmem<D>::kAlloc, st_dkdv>>>(
         *l.mQ64, *l.mdO64, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
   }
   e = cudaGetLastError();

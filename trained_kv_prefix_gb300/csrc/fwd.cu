@@ -57,19 +57,6 @@ struct FwdSmem {
 enum FwdBar { kQFull = 0, kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull, kSFree, kPFull,
               kODone, kDrain, kNumBars };
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k) {
-  // 16-element K step inside a 64-element (128 B) swizzle atom column;
-  // atom columns of a 128-row tile are 16 KB apart.
-  return sdesc_sw128(base + static_cast<uint32_t>(k >> 2) * 16384u +
-                         static_cast<uint32_t>(k & 3) * 32u,
-                     16u, 1024u);
-}
-
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int k) {
-  // 16 rows along K = two 8-row groups (1024 B each); 64-wide N blocks 16 KB apart.
-  return sdesc_sw128(base + static_cast<uint32_t>(k) * 2048u, 16384u, 1024u);
-}
-
 template <int D>
 __global__ void __launch_bounds__(192, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
@@ -197,16 +184,26 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && T > 0) {
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idPV = idesc_bf16(128, D, false, true);
-      const uint32_t q_base = smem_u32(sQ);
-      const uint32_t p_base = smem_u32(sP);
+      // Base descriptors, computed once; each MMA below adds a compile-time
+      // byte offset (16-element K step inside a 64-element atom column, atom
+      // columns 16 KB apart; MN-major V steps 16 rows = 2048 B).
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
+      const uint64_t dP0 = sdesc_sw128(smem_u32(sP), 16u, 1024u);
+      // stage 1 descriptors = stage 0 + one tile (selected, not indexed, so
+      // that nothing lands in local memory)
+      const uint64_t dKs0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);
+      const uint64_t dVs0 = sdesc_sw128(smem_u32(smem + L::kV), 16384u, 1024u);
+      const uint64_t dKs1 = desc_add(dKs0, L::kTileBytes);
+      const uint64_t dVs1 = desc_add(dVs0, L::kTileBytes);
       bool ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutMma);
       auto issue_pv = [&](int t) {
         const int sp = t & 1;
-        const uint32_t v_base = smem_u32(smem + L::kV + sp * L::kTileBytes);
+        const uint64_t dv = sp ? dVs1 : dVs0;
+        umma_bf16_ss(tO, dP0, dv, idPV, t > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          umma_bf16_ss(tO, kmajor_desc(p_base, k), mnmajor_desc(v_base, k), idPV,
-                       (t > 0 || k > 0) ? 1u : 0u);
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ss(tO, desc_add(dP0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(dv, k * 2048),
+                       idPV, 1u);
         umma_commit(&bars[kODone]);
         umma_commit(&bars[kKVEmpty0 + sp]);
       };
@@ -219,10 +216,13 @@ __global__ void __launch_bounds__(192, 1)
           if (!ok) break;
         }
         tc_fence_after();
-        const uint32_t k_base = smem_u32(smem + L::kK + s * L::kTileBytes);
+        const uint64_t dk = s ? dKs1 : dKs0;
+        umma_bf16_ss(tS, dQ0, dk, idS, 0u);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_bf16_ss(tS, kmajor_desc(q_base, k), kmajor_desc(k_base, k), idS, k > 0 ? 1u : 0u);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          umma_bf16_ss(tS, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
+        }
         umma_commit(&bars[kSFull]);
         if (t > 0) {
           ok = mbar_wait(&bars[kPFull], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);

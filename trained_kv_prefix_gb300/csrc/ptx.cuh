@@ -150,6 +150,18 @@ __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]: A is M x K with row m in TMEM lane m
+// and 16-bit elements packed two per 32-bit column (the lower index in the
+// low half); one K step of 16 spans 8 columns.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every previously issued tcgen05 op of this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -225,6 +237,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Advance a shared-memory descriptor by a byte offset: the start address
+// lives in the low 14 bits as addr >> 4 and shared addresses stay below
+// 256 KB, so a plain add never carries out of the field.  With a
+// compile-time offset this is one add, which keeps the MMA-issuing thread's
+// instruction chain short.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_offset) {
+  return desc + static_cast<uint64_t>(byte_offset >> 4);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulation.
