@@ -444,30 +444,41 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 }
 
 // ================================================================ dQ ======
+// One CTA per 128-row query tile.  Keys stream in 96-row steps (N = 96):
+// S = Q K^T and dP = dO V^T go to double-buffered TMEM (S at x*96, dP at
+// 192 + x*96), two warpgroups take alternate steps and overwrite the first
+// 48 columns of S with dS = P (dP - D) packed as bf16 pairs, and
+// dQ += dS K reads dS from TMEM (A operand) with K as an MN-major operand;
+// dQ accumulates at column 384.  Threads: warps 0-7 the two warpgroups
+// (thread = query row = TMEM lane), warp 8 TMA, warp 9 MMA.
+constexpr int kDqThreads = 320;
+constexpr int kDqKeys = 96;
+
 template <int D>
 struct DqSmem {
-  static constexpr int kStages = 2;
-  static constexpr int kT = kTile * D * 2;
+  static constexpr int kStages = 3;
+  static constexpr int kQT = kTile * D * 2;      // 128-row Q or dO tile
+  static constexpr int kKT = kDqKeys * D * 2;    // 96-row K or V tile
   static constexpr int kQ = 0;
-  static constexpr int kdO = kQ + kT;
-  static constexpr int kK = kdO + kT;
-  static constexpr int kV = kK + kStages * kT;
-  static constexpr int kDS = kV + kStages * kT;
-  static constexpr int kBar = kDS + kTile * kTile * 2;
-  static constexpr int kBytes = kBar + 128;
+  static constexpr int kdO = kQ + kQT;
+  static constexpr int kStage0 = kdO + kQT;      // stage s: K at +0, V at +kKT
+  static constexpr int kBar = kStage0 + kStages * 2 * kKT;
+  static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-enum DqBar { kQdFull = 0, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSdFull, kSdFree, kDsdFull,
-             kDqDone, kDqDrain, kDqBars };
+enum DqBar { kQdFull = 0, kKvFull0, kKvEmpty0 = kKvFull0 + 3, kSdFull0 = kKvEmpty0 + 3,
+             kDsdFull0 = kSdFull0 + 2, kDqDone = kDsdFull0 + 2, kDqDrain, kDqBars };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
-              const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
-              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+              const __grid_constant__ CUtensorMap mKc96, const __grid_constant__ CUtensorMap mVc96,
+              const __grid_constant__ CUtensorMap mK96, const __grid_constant__ CUtensorMap mV96,
               const BwdParams a) {
   using L = DqSmem<D>;
+  constexpr int S = L::kStages;
+  constexpr int NK = kDqKeys;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -480,25 +491,27 @@ __global__ void __launch_bounds__(192, 1)
   const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);
   const int kvh = h / a.G;
   const int q0 = qt * kTile;
-  const int n_ct = a.n_ct;
-  const int n_rt = min(qt + 1, a.n_rt);
+  const int n_ct = (a.p + NK - 1) / NK;
+  const int last_q = min(q0 + kTile, a.n) - 1;          // last real query of the tile
+  const int n_rt = last_q / NK + 1;                      // real key steps up to the diagonal
   const int T = n_ct + n_rt;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars[kQdFull], 1);
-    mbar_init(&bars[kKvFull0], 1);
-    mbar_init(&bars[kKvFull1], 1);
-    mbar_init(&bars[kKvEmpty0], 1);
-    mbar_init(&bars[kKvEmpty1], 1);
-    mbar_init(&bars[kSdFull], 1);
-    mbar_init(&bars[kSdFree], 128);
-    mbar_init(&bars[kDsdFull], 128);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars[kKvFull0 + s], 1);
+      mbar_init(&bars[kKvEmpty0 + s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[kSdFull0 + x], 1);
+      mbar_init(&bars[kDsdFull0 + x], 128);
+    }
     mbar_init(&bars[kDqDone], 1);
     mbar_init(&bars[kDqDrain], 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -506,17 +519,16 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 256;
+  const uint32_t tS0 = tmem, tDP0 = tmem + 192, tDQ = tmem + 384;
   volatile int* abort_p = &abort_flag;
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sdO = smem + L::kdO;
-  uint8_t* sDS = smem + L::kDS;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
-      mbar_arrive_expect_tx(&bars[kQdFull], 2 * L::kT);
+      mbar_arrive_expect_tx(&bars[kQdFull], 2 * L::kQT);
 #pragma unroll
       for (int hc = 0; hc < D / 64; ++hc) {
         tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdFull], hc * 64, h, q0, b);
@@ -525,25 +537,25 @@ __global__ void __launch_bounds__(192, 1)
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < T; ++t) {
-        const int s = t & 1;
-        if (t >= 2) {
-          ok = mbar_wait(&bars[kKvEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
+        const int s = t % S;
+        if (t >= S) {
+          ok = mbar_wait(&bars[kKvEmpty0 + s], ((t / S) - 1) & 1, abort_p, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
-        uint8_t* sK = smem + L::kK + s * L::kT;
-        uint8_t* sV = smem + L::kV + s * L::kT;
-        mbar_arrive_expect_tx(&bars[kKvFull0 + s], 2 * L::kT);
+        uint8_t* sK = smem + L::kStage0 + s * 2 * L::kKT;
+        uint8_t* sV = sK + L::kKT;
+        mbar_arrive_expect_tx(&bars[kKvFull0 + s], 2 * L::kKT);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc) {
           if (t < n_ct) {
-            tma_load_4d(sK + hc * 16384, &mKc, &bars[kKvFull0 + s], hc * 64, kvh, t * kTile, 0);
-            tma_load_4d(sV + hc * 16384, &mVc, &bars[kKvFull0 + s], hc * 64, kvh, t * kTile, 0);
+            tma_load_4d(sK + hc * (NK * 128), &mKc96, &bars[kKvFull0 + s], hc * 64, kvh, t * NK, 0);
+            tma_load_4d(sV + hc * (NK * 128), &mVc96, &bars[kKvFull0 + s], hc * 64, kvh, t * NK, 0);
           } else {
-            tma_load_4d(sK + hc * 16384, &mK, &bars[kKvFull0 + s], hc * 64, kvh,
-                        (t - n_ct) * kTile, b);
-            tma_load_4d(sV + hc * 16384, &mV, &bars[kKvFull0 + s], hc * 64, kvh,
-                        (t - n_ct) * kTile, b);
+            tma_load_4d(sK + hc * (NK * 128), &mK96, &bars[kKvFull0 + s], hc * 64, kvh,
+                        (t - n_ct) * NK, b);
+            tma_load_4d(sV + hc * (NK * 128), &mV96, &bars[kKvFull0 + s], hc * 64, kvh,
+                        (t - n_ct) * NK, b);
           }
         }
         issued = t + 1;
@@ -551,64 +563,65 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) {
         int dummy = 0;
         mbar_wait(&bars[kQdFull], 0, &dummy, nullptr, 0);
-        for (int t = max(issued - 2, 0); t < issued; ++t)
-          mbar_wait(&bars[kKvFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
+        for (int t = max(issued - S, 0); t < issued; ++t)
+          mbar_wait(&bars[kKvFull0 + t % S], (t / S) & 1, &dummy, nullptr, 0);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0 && T > 0) {
-      const uint32_t idS = idesc_bf16(128, 128, false, false);
+      const uint32_t idS = idesc_bf16(128, NK, false, false);
       const uint32_t idDQ = idesc_bf16(128, D, false, true);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
       const uint64_t dO0 = sdesc_sw128(smem_u32(sdO), 16u, 1024u);
-      const uint64_t dS0 = sdesc_sw128(smem_u32(sDS), 16u, 1024u);
-      const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);      // K-major
-      const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kK), 16384u, 1024u);   // MN-major
-      const uint64_t dVk0 = sdesc_sw128(smem_u32(smem + L::kV), 16u, 1024u);
+      const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16u, 1024u);           // K-major
+      const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kStage0), NK * 128u, 1024u);     // MN-major
+      constexpr uint32_t kStageBytes = 2 * L::kKT;
       bool ok = mbar_wait(&bars[kQdFull], 0, abort_p, a.status, kDevErrTimeoutMma);
       auto issue_dq = [&](int t) {
-        const int sp = t & 1;
-        const uint64_t dkm = desc_add(dKm0, sp * L::kT);
-        umma_bf16_ss(tDQ, dS0, dkm, idDQ, t > 0 ? 1u : 0u);
+        const int s = t % S, x = t & 1;
+        const uint64_t dkm = desc_add(dKm0, s * kStageBytes);
+        const uint32_t ds = tS0 + x * NK;
+        umma_bf16_ts(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ss(tDQ, desc_add(dS0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(dkm, k * 2048),
-                       idDQ, 1u);
-        umma_commit(&bars[kDqDone]);
-        umma_commit(&bars[kKvEmpty0 + sp]);
+        for (int k = 1; k < NK / 16; ++k)
+          umma_bf16_ts(tDQ, ds + k * 8, desc_add(dkm, k * 2048), idDQ, 1u);
+        umma_commit(&bars[kKvEmpty0 + s]);
       };
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t & 1;
-        ok = mbar_wait(&bars[kKvFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        const int s = t % S, x = t & 1;
+        ok = mbar_wait(&bars[kKvFull0 + s], (t / S) & 1, abort_p, a.status, kDevErrTimeoutMma);
         if (!ok) break;
-        if (t > 0) {
-          ok = mbar_wait(&bars[kSdFree], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
-          if (!ok) break;
-        }
         tc_fence_after();
-        const uint64_t dk = desc_add(dKk0, s * L::kT), dv = desc_add(dVk0, s * L::kT);
-        umma_bf16_ss(tS, dQ0, dk, idS, 0u);
-        umma_bf16_ss(tDP, dO0, dv, idS, 0u);
+        // buffer x was last read by the dQ MMA of step t-2, issued earlier
+        const uint64_t dk = desc_add(dKk0, s * kStageBytes);
+        const uint64_t dv = desc_add(dk, L::kKT);
+        const uint32_t ts = tS0 + x * NK, tdp = tDP0 + x * NK;
+        umma_bf16_ss(ts, dQ0, dk, idS, 0u);
+        umma_bf16_ss(tdp, dO0, dv, idS, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss(tS, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
-          umma_bf16_ss(tDP, desc_add(dO0, off), desc_add(dv, off), idS, 1u);
+          const uint32_t offa = (k >> 2) * 16384 + (k & 3) * 32;
+          const uint32_t offb = (k >> 2) * (NK * 128) + (k & 3) * 32;
+          umma_bf16_ss(ts, desc_add(dQ0, offa), desc_add(dk, offb), idS, 1u);
+          umma_bf16_ss(tdp, desc_add(dO0, offa), desc_add(dv, offb), idS, 1u);
         }
-        umma_commit(&bars[kSdFull]);
+        umma_commit(&bars[kSdFull0 + x]);
         if (t > 0) {
-          ok = mbar_wait(&bars[kDsdFull], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+          ok = mbar_wait(&bars[kDsdFull0 + (x ^ 1)], ((t - 1) >> 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           issue_dq(t - 1);
         }
       }
       if (ok) {
-        ok = mbar_wait(&bars[kDsdFull], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kDsdFull0 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, abort_p, a.status,
+                       kDevErrTimeoutMma);
         if (ok) {
           tc_fence_after();
           issue_dq(T - 1);
+          umma_commit(&bars[kDqDone]);
         }
       }
       umma_commit(&bars[kDqDrain]);
@@ -617,34 +630,36 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    const int row = threadIdx.x;
+    const int wg = warp >> 2;
+    const int row = threadIdx.x & 127;
     const int i = q0 + row;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tS0 + wg * NK + lane_off, tdp = tDP0 + wg * NK + lane_off;
     float lse2 = INFINITY, Di = 0.f;
     if (i < a.n) {
       const long long idx = (static_cast<long long>(b) * a.Hq + h) * a.n + i;
       lse2 = __ldg(a.lse + idx) * kLog2e;
       Di = __ldg(a.Dvec + idx);
     }
-    bool ok = T > 0;
-    for (int t = 0; t < T && ok; ++t) {
-      ok = mbar_wait(&bars[kSdFull], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+    bool ok = T > wg;
+    for (int t = wg; t < T && ok; t += 2) {
+      ok = mbar_wait(&bars[kSdFull0 + wg], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       int valid;
       if (t < n_ct) {
-        valid = min(kTile, a.p - t * kTile);
+        valid = min(NK, a.p - t * NK);
       } else {
-        const int col0 = (t - n_ct) * kTile;
-        valid = max(0, min(min(i, a.n - 1) - col0 + 1, kTile));
+        const int col0 = (t - n_ct) * NK;
+        valid = max(0, min(min(i, a.n - 1) - col0 + 1, NK));
       }
-      uint32_t pk[64];
+      uint32_t pk[NK / 2];
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
+      for (int blk = 0; blk < NK / 32; ++blk) {
         uint32_t sr[32], dr[32];
-        tmem_ld32(tS + lane_off + blk * 32, sr);
-        tmem_ld32(tDP + lane_off + blk * 32, dr);
+        tmem_ld32(ts + blk * 32, sr);
+        tmem_ld32(tdp + blk * 32, dr);
         tmem_ld_wait();
         tmem_reg_fence(sr);
         tmem_reg_fence(dr);
@@ -654,56 +669,58 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int cc = blk * 32 + c + e;
-            const float pe = (cc < valid)
-                                 ? exp2_approx(__uint_as_float(sr[c + e]) * a.scale_log2 - lse2)
-                                 : 0.f;
+            const float x = fmaf(__uint_as_float(sr[c + e]), a.scale_log2, -lse2);
+            const float pe = (cc < valid) ? exp2_approx(x) : 0.f;
             ds[e] = pe * (__uint_as_float(dr[c + e]) - Di);
           }
           pk[blk * 16 + c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
       }
+      tmem_st32(ts, pk);
+      tmem_st16(ts + 32, pk + 32);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[kSdFree]);
-      if (t > 0) {
-        ok = mbar_wait(&bars[kDqDone], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16)
-        *reinterpret_cast<uint4*>(sDS + (c16 >> 3) * 16384 + sw128_offset(row, c16 & 7)) =
-            make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars[kDsdFull]);
+      mbar_arrive(&bars[kDsdFull0 + wg]);
     }
+    ok = ok || T <= wg;
     if (ok) {
-      ok = mbar_wait(&bars[kDqDone], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = mbar_wait(&bars[kDqDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      float x[D];
+      // warpgroup wg finishes the rotation pairs j in [wg*D/4, wg*D/4 + D/4)
+      // and their partners j + D/2
+      constexpr int Q = D / 4;
+      float lo[Q], hi[Q];
+      const uint32_t base = tDQ + lane_off + wg * Q;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tDQ + lane_off + c * 32, r);
+      for (int c = 0; c < Q / 16; ++c) {
+        // columns [wg*Q + 16c, +16) and their partners D/2 further on
+        uint32_t r[16];
+        tmem_ld16(base + c * 16, r);
         tmem_ld_wait();
-        tmem_reg_fence(r);
+        tmem_reg_fence16(r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]) * a.scale;
+        for (int e = 0; e < 16; ++e) lo[c * 16 + e] = __uint_as_float(r[e]) * a.scale;
+        tmem_ld16(base + D / 2 + c * 16, r);
+        tmem_ld_wait();
+        tmem_reg_fence16(r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) hi[c * 16 + e] = __uint_as_float(r[e]) * a.scale;
       }
       if (i < a.n) {
-        const float2* tb = a.table + static_cast<long long>(i) * (D / 2);
+        const float2* tb = a.table + static_cast<long long>(i) * (D / 2) + wg * Q;
 #pragma unroll
-        for (int e = 0; e < D / 2; ++e) {
+        for (int e = 0; e < Q; ++e) {
           const float2 cs = __ldg(tb + e);
-          const float x0 = x[e], x1 = x[e + D / 2];
-          x[e] = x0 * cs.x + x1 * cs.y;
-          x[e + D / 2] = x1 * cs.x - x0 * cs.y;
+          const float x0 = lo[e], x1 = hi[e];
+          lo[e] = x0 * cs.x + x1 * cs.y;
+          hi[e] = x1 * cs.x - x0 * cs.y;
         }
-        store_row_out(a.dq, ((static_cast<long long>(b) * a.n + i) * a.Hq + h) * D, x, D,
-                      a.out_f32 != 0);
+        const long long off = ((static_cast<long long>(b) * a.n + i) * a.Hq + h) * D;
+        store_row_out(a.dq, off + wg * Q, lo, Q, a.out_f32 != 0);
+        store_row_out(a.dq, off + D / 2 + wg * Q, hi, Q, a.out_f32 != 0);
       }
     }
   }
@@ -711,7 +728,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 template <int D>
@@ -758,8 +775,8 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   TraceScope tr("bwd_dq", st_dq);
-  dq_kernel<D><<<dim3(p.Hq, p.B, p.n_qtiles), 192, DqSmem<D>::kAlloc, st_dq>>>(
-      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
+  dq_kernel<D><<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
+      *l.mQ, *l.mdO, *l.mKc96, *l.mVc96, *l.mK96, *l.mV96, p);
   return cudaGetLastError();
 }
 
