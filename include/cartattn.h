@@ -24,8 +24,12 @@
  *   - RoPE is the rotate-half form: element j pairs with j + d/2 at angle
  *     position * theta^(-2j/d); angles are reduced in fp64 on the device.
  *   - Return value: CART_OK (0) or a negative cart_status.
- *   - The library holds no per-call state.  It caches, per process, only the
- *     CUDA driver entry point used to build TMA descriptors.
+ *   - The library holds no per-call state.  It caches, per process, the
+ *     CUDA driver entry point used to build TMA descriptors and, per device,
+ *     one helper stream with two events on which cart_attn_bwd runs its dQ
+ *     kernel concurrently with its dK/dV kernel (forked from and joined back
+ *     into the caller's stream).  Calls on one device from several host
+ *     threads at once must therefore be serialised by the caller.
  */
 #ifndef CARTATTN_H_
 #define CARTATTN_H_

@@ -71,6 +71,33 @@ bool make_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, int H
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A second stream per device on which the backward's dQ kernel runs
+// concurrently with the dK/dV kernel (they read the same inputs and write
+// disjoint outputs).  Forked from and joined back into the caller's stream
+// with two events, so the caller sees one ordered call.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+  static SideStream ss[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  SideStream& x = ss[dev];
+  if (!x.s) {
+    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
+      x.s = nullptr;
+      return nullptr;
+    }
+  }
+  return &x;
+}
+
 int check_device() {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CART_ERR_CUDA;
@@ -378,7 +405,18 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.dvc = dvc;
   l.accumulate = accumulate;
   l.table = tp.table;
-  CART_CUDA(launch_bwd(l, st, st));
+  SideStream* side = side_stream();
+  if (!side) {
+    CART_CUDA(launch_bwd(l, st, st));
+    return CART_OK;
+  }
+  CART_CUDA(cudaEventRecord(side->fork, st));
+  CART_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+  const cudaError_t e = launch_bwd(l, st, side->s);
+  // join even when a launch failed, so the side stream never runs ahead
+  CART_CUDA(cudaEventRecord(side->join, side->s));
+  CART_CUDA(cudaStreamWaitEvent(st, side->join, 0));
+  CART_CUDA(e);
   return CART_OK;
 }
 

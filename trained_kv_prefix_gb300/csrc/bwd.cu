@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -66,14 +68,16 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 }
 
 // =========================================================== dK / dV ======
-// Threads: warps 0-3 and 4-7 are two P^T / dS^T warpgroups that take
-// alternate 64-query steps (thread t of a group owns key row t = TMEM lane
-// t), warp 8 is the TMA producer, warp 9 issues the MMAs.
+// Threads: warps 0-3 and 4-7 are two P^T / dS^T warpgroups that share every
+// 64-query step, warpgroup w taking queries [32w, 32w + 32) (thread t of a
+// group owns key row t = TMEM lane t); warp 8 is the TMA producer, warp 9
+// issues the MMAs.
 // TMEM (512 columns): step buffer x in {0,1} holds S^T at columns x*64 and
-// dP^T at 128 + x*64 (64 f32 columns each); the warpgroup overwrites their
-// first 32 columns with P^T and dS^T packed as bf16 pairs, which the dV and
-// dK MMAs then read as their A operand straight from TMEM.  dV accumulates
-// at 256, dK at 384.
+// dP^T at 128 + x*64 (64 f32 columns each).  Warpgroup w overwrites the
+// first 16 columns of its own 32-column half with its P^T and dS^T packed
+// as bf16 pairs, which the dV and dK MMAs read as their A operand straight
+// from TMEM (K step k of 16 queries lives at column (k/2)*32 + (k%2)*8).
+// dV accumulates at 256, dK at 384.
 constexpr int kDkdvThreads = 320;
 
 template <int D>
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kStFull0 + x], 1);
-      mbar_init(&bars[kDsFull0 + x], 128);
+      mbar_init(&bars[kDsFull0 + x], 256);
     }
     mbar_init(&bars[kAccDone], 1);
     mbar_init(&bars[kDkdvDrain], 1);
@@ -282,8 +286,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         umma_bf16_ts(tDK, dst, dq, idACC, first);
 #pragma unroll
         for (int k = 1; k < 4; ++k) {
-          umma_bf16_ts(tDV, pt + k * 8, desc_add(ddo, k * 2048), idACC, 1u);
-          umma_bf16_ts(tDK, dst + k * 8, desc_add(dq, k * 2048), idACC, 1u);
+          const uint32_t ac = (k >> 1) * 32 + (k & 1) * 8;
+          umma_bf16_ts(tDV, pt + ac, desc_add(ddo, k * 2048), idACC, 1u);
+          umma_bf16_ts(tDK, dst + ac, desc_add(dq, k * 2048), idACC, 1u);
         }
         umma_commit(&bars[kQdoEmpty0 + s]);
       };
@@ -336,12 +341,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const int j = tile * kTile + row;
     const bool key_ok = cart ? (j < a.p) : (j < a.n);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tst = tST0 + wg * 64 + lane_off, tdp = tDP0 + wg * 64 + lane_off;
-    bool ok = U > wg;
-    for (int u = wg; u < U && ok; u += 2) {
-      const int s = u % S;
+    bool ok = true;
+    for (int u = 0; u < U && ok; ++u) {
+      const int s = u % S, x = u & 1;
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
-      ok = mbar_wait(&bars[kStFull0 + wg], (u >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kStFull0 + x], (u >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       // acquire the lse / D vectors the producer lanes published with
       // kQdoFull (already complete: the MMAs behind kStFull waited for it)
       if (ok) ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status,
@@ -349,52 +353,57 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // columns c < qlim are invisible: none for a cartridge key, those with
-      // query < key for a real key, all for rows past the end of the keys
-      const int qlim = !key_ok ? 64 : (cart ? 0 : j - it.qt * 64);
-      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 128);
-      const float4* dv4 = reinterpret_cast<const float4*>(vec + s * 128 + 64);
-      uint32_t pk[32], dk[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tst + half * 32, sr);
-        tmem_ld32(tdp + half * 32, dr);
-        tmem_ld_wait();
-        tmem_reg_fence(sr);
-        tmem_reg_fence(dr);
+      const uint32_t tst = tST0 + x * 64 + wg * 32 + lane_off;
+      const uint32_t tdp = tDP0 + x * 64 + wg * 32 + lane_off;
+      // this group's columns c (query it.qt*64 + wg*32 + c) are invisible for
+      // c < qlim: none for a cartridge key, query < key for a real key, all
+      // for rows past the end of the keys
+      const int qlim = !key_ok ? 32 : (cart ? 0 : j - it.qt * 64 - wg * 32);
+      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 128 + wg * 32);
+      const float4* dv4 = reinterpret_cast<const float4*>(vec + s * 128 + 64 + wg * 32);
+      uint32_t sr[32], dr[32], pk[16], dk[16];
+      tmem_ld32(tst, sr);
+      tmem_ld32(tdp, dr);
+      tmem_ld_wait();
+      tmem_reg_fence(sr);
+      tmem_reg_fence(dr);
+      auto compute = [&](auto masked) {
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = lse4[half * 8 + c4];
-          const float4 d4 = dv4[half * 8 + c4];
+          const float4 l4 = lse4[c4];
+          const float4 d4 = dv4[c4];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
           float pv[4], dsv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int cc = half * 32 + c4 * 4 + e;
-            const float x = fmaf(__uint_as_float(sr[c4 * 4 + e]), a.scale_log2, -lv[e]);
-            const float pe = (cc >= qlim) ? exp2_approx(x) : 0.f;
+            const int cc = c4 * 4 + e;
+            const float xv = fmaf(__uint_as_float(sr[cc]), a.scale_log2, -lv[e]);
+            float pe = exp2_approx(xv);
+            if (decltype(masked)::value) pe = (cc >= qlim) ? pe : 0.f;
             pv[e] = pe;
-            dsv[e] = pe * (__uint_as_float(dr[c4 * 4 + e]) - dd[e]);
+            dsv[e] = pe * (__uint_as_float(dr[cc]) - dd[e]);
           }
-          pk[half * 16 + c4 * 2] = pack_bf16x2(pv[0], pv[1]);
-          pk[half * 16 + c4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk[half * 16 + c4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
-          dk[half * 16 + c4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          pk[c4 * 2] = pack_bf16x2(pv[0], pv[1]);
+          pk[c4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk[c4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
+          dk[c4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
-      }
-      // P^T and dS^T over the first 32 columns of S^T and dP^T (both were
-      // read above by this thread's own lane)
-      tmem_st32(tst, pk);
-      tmem_st32(tdp, dk);
+      };
+      if (__any_sync(0xffffffffu, qlim > 0))
+        compute(std::true_type{});
+      else
+        compute(std::false_type{});
+      // P^T and dS^T over the first 16 columns of this group's halves of
+      // S^T and dP^T (read above by this thread's own lane)
+      tmem_st16(tst, pk);
+      tmem_st16(tdp, dk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[kDsFull0 + wg]);
+      mbar_arrive(&bars[kDsFull0 + x]);
     }
     // ------------------------------------------------------------ epilogue --
     // warpgroup 0 writes dV, warpgroup 1 writes dK
-    ok = ok || U <= wg;
     if (ok) {
       ok = mbar_wait(&bars[kAccDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
@@ -446,11 +455,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 // ================================================================ dQ ======
 // One CTA per 128-row query tile.  Keys stream in 96-row steps (N = 96):
 // S = Q K^T and dP = dO V^T go to double-buffered TMEM (S at x*96, dP at
-// 192 + x*96), two warpgroups take alternate steps and overwrite the first
-// 48 columns of S with dS = P (dP - D) packed as bf16 pairs, and
-// dQ += dS K reads dS from TMEM (A operand) with K as an MN-major operand;
-// dQ accumulates at column 384.  Threads: warps 0-7 the two warpgroups
-// (thread = query row = TMEM lane), warp 8 TMA, warp 9 MMA.
+// 192 + x*96).  Both warpgroups work on every step, warpgroup w on keys
+// [48w, 48w + 48): it overwrites the first 24 columns of its half of S with
+// dS = P (dP - D) packed as bf16 pairs, and dQ += dS K reads dS from TMEM
+// (A operand; K step k of 16 keys at column (k/3)*48 + (k%3)*8) with K as
+// an MN-major operand.  dQ accumulates at column 384.  Threads: warps 0-7
+// the two warpgroups (thread = query row = TMEM lane), warp 8 TMA, warp 9
+// MMA.
 constexpr int kDqThreads = 320;
 constexpr int kDqKeys = 96;
 
@@ -505,7 +516,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kSdFull0 + x], 1);
-      mbar_init(&bars[kDsdFull0 + x], 128);
+      mbar_init(&bars[kDsdFull0 + x], 256);
     }
     mbar_init(&bars[kDqDone], 1);
     mbar_init(&bars[kDqDrain], 1);
@@ -585,7 +596,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         umma_bf16_ts(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < NK / 16; ++k)
-          umma_bf16_ts(tDQ, ds + k * 8, desc_add(dkm, k * 2048), idDQ, 1u);
+          umma_bf16_ts(tDQ, ds + (k / 3) * 48 + (k % 3) * 8, desc_add(dkm, k * 2048), idDQ, 1u);
         umma_commit(&bars[kKvEmpty0 + s]);
       };
       for (int t = 0; t < T && ok; ++t) {
@@ -634,55 +645,71 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row = threadIdx.x & 127;
     const int i = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t ts = tS0 + wg * NK + lane_off, tdp = tDP0 + wg * NK + lane_off;
     float lse2 = INFINITY, Di = 0.f;
     if (i < a.n) {
       const long long idx = (static_cast<long long>(b) * a.Hq + h) * a.n + i;
       lse2 = __ldg(a.lse + idx) * kLog2e;
       Di = __ldg(a.Dvec + idx);
     }
-    bool ok = T > wg;
-    for (int t = wg; t < T && ok; t += 2) {
-      ok = mbar_wait(&bars[kSdFull0 + wg], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+    constexpr int NH = NK / 2;  // keys per warpgroup and step
+    bool ok = T > 0;
+    for (int t = 0; t < T && ok; ++t) {
+      const int x = t & 1;
+      ok = mbar_wait(&bars[kSdFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // this group's key columns c (key step*96 + wg*48 + c) are visible for
+      // c < valid
       int valid;
       if (t < n_ct) {
-        valid = min(NK, a.p - t * NK);
+        valid = min(NH, a.p - t * NK - wg * NH);
       } else {
-        const int col0 = (t - n_ct) * NK;
-        valid = max(0, min(min(i, a.n - 1) - col0 + 1, NK));
+        const int col0 = (t - n_ct) * NK + wg * NH;
+        valid = min(min(i, a.n - 1) - col0 + 1, NH);
       }
-      uint32_t pk[NK / 2];
+      const uint32_t ts = tS0 + x * NK + wg * NH + lane_off;
+      const uint32_t tdp = tDP0 + x * NK + wg * NH + lane_off;
+      uint32_t sa[32], da[32], sb[16], db[16];
+      tmem_ld32(ts, sa);
+      tmem_ld16(ts + 32, sb);
+      tmem_ld32(tdp, da);
+      tmem_ld16(tdp + 32, db);
+      tmem_ld_wait();
+      tmem_reg_fence(sa);
+      tmem_reg_fence16(sb);
+      tmem_reg_fence(da);
+      tmem_reg_fence16(db);
+      uint32_t pk[32];  // 24 used; the rest pads the 32-column store
+      auto compute = [&](auto masked) {
 #pragma unroll
-      for (int blk = 0; blk < NK / 32; ++blk) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(ts + blk * 32, sr);
-        tmem_ld32(tdp + blk * 32, dr);
-        tmem_ld_wait();
-        tmem_reg_fence(sr);
-        tmem_reg_fence(dr);
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
+        for (int c = 0; c < NH; c += 2) {
           float ds[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int cc = blk * 32 + c + e;
-            const float x = fmaf(__uint_as_float(sr[c + e]), a.scale_log2, -lse2);
-            const float pe = (cc < valid) ? exp2_approx(x) : 0.f;
-            ds[e] = pe * (__uint_as_float(dr[c + e]) - Di);
+            const int cc = c + e;
+            const uint32_t sv = cc < 32 ? sa[cc] : sb[cc - 32];
+            const uint32_t dv = cc < 32 ? da[cc] : db[cc - 32];
+            float pe = exp2_approx(fmaf(__uint_as_float(sv), a.scale_log2, -lse2));
+            if (decltype(masked)::value) pe = (cc < valid) ? pe : 0.f;
+            ds[e] = pe * (__uint_as_float(dv) - Di);
           }
-          pk[blk * 16 + c / 2] = pack_bf16x2(ds[0], ds[1]);
+          pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
-      }
+      };
+      if (__any_sync(0xffffffffu, valid < NH))
+        compute(std::true_type{});
+      else
+        compute(std::false_type{});
+#pragma unroll
+      for (int c = NH / 2; c < 32; ++c) pk[c] = 0u;
+      // 32-column store at the start of this group's 48 S columns: 24 packed
+      // dS columns plus 8 padding columns, all inside the group's own half
       tmem_st32(ts, pk);
-      tmem_st16(ts + 32, pk + 32);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[kDsdFull0 + wg]);
+      mbar_arrive(&bars[kDsdFull0 + x]);
     }
-    ok = ok || T <= wg;
     if (ok) {
       ok = mbar_wait(&bars[kDqDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
