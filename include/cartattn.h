@@ -140,7 +140,7 @@ CART_API int cart_attn_bwd(const cart_geom* g, cart_dtype in_dtype, cart_dtype c
  *   k_cache, v_cache [B, cache_rows, Hkv, d] bf16 private caches; rows
  *          0..len[b]-1 hold already-rotated keys at positions p..p+len[b]-1
  *   priv_len [B] int32 (device): len[b], 0 <= len[b] < cache_rows (entries
- *          outside that range are clamped into it)
+ *          outside that range are clamped into it); cache_rows <= 32768
  *   o      [B, Hq, d] bf16 (output)
  * The new token sits at position p + len[b]: its rotated key and its value
  * are written to private row len[b], then it attends to the p cartridge rows

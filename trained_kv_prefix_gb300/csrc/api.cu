@@ -69,6 +69,15 @@ bool make_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, int H
                   static_cast<uint64_t>(rows) * H * d * e, box_rows);
 }
 
+}  // namespace
+
+bool make_bf16_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, int H, int d,
+                        unsigned box_rows) {
+  return make_rows_map(m, base, blocks, rows, H, d, box_rows);
+}
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // A second stream per device on which the backward's dQ kernel runs
@@ -466,7 +475,7 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
   if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
   if (!std::isfinite(scale) || !(theta > 0.0) || !std::isfinite(theta)) return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
-  if ((rows + kDecodeChunk - 1) / kDecodeChunk > 65535 * 16) return CART_ERR_GEOMETRY;
+  if ((rows + kDecodeChunk - 1) / kDecodeChunk > 256) return CART_ERR_GEOMETRY;  // <= 32767 rows
   return CART_OK;
 }
 }  // namespace
@@ -519,8 +528,23 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
   a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
   a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
   a.chunk = kDecodeChunk;
-  CART_CUDA(launch_decode_prep(a, make_rope_freqs(d, rope_theta), st));
+  const RopeFreqs freqs = make_rope_freqs(d, rope_theta);
+  // The cartridge split pass (tensor cores, with the query rotation it
+  // needs) and the private pass (HBM) are independent: the former runs on the
+  // helper stream.
+  SideStream* side = p > 0 ? side_stream() : nullptr;
+  cudaStream_t st_cart = side ? side->s : st;
+  if (side) {
+    CART_CUDA(cudaEventRecord(side->fork, st));
+    CART_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+  }
   if (p > 0) {
+    const cudaError_t e0 = launch_decode_prep(a, freqs, st_cart);
+    if (e0 != cudaSuccess && side) {
+      cudaEventRecord(side->join, side->s);
+      cudaStreamWaitEvent(st, side->join, 0);
+    }
+    CART_CUDA(e0);
     CUtensorMap mQ, mKc, mVc;
     if (!make_rows_map(&mQ, a.q_rot, 1, R, Hkv, d, 128) ||
         !make_rows_map(&mKc, kc, 1, p, Hkv, d, 128) || !make_rows_map(&mVc, vc, 1, p, Hkv, d, 128))
@@ -545,9 +569,19 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
     l.out_f32 = true;
     l.lse = const_cast<float*>(a.cart_lse);
     l.decode = true;
-    CART_CUDA(launch_fwd(l, st));
+    const cudaError_t e = launch_fwd(l, st_cart);
+    if (e != cudaSuccess && side) {  // keep the helper stream joined
+      cudaEventRecord(side->join, side->s);
+      cudaStreamWaitEvent(st, side->join, 0);
+    }
+    CART_CUDA(e);
   }
-  CART_CUDA(launch_decode_private(a, st));
+  const cudaError_t ep = launch_decode_private(a, freqs, st);
+  if (side) {
+    CART_CUDA(cudaEventRecord(side->join, side->s));
+    CART_CUDA(cudaStreamWaitEvent(st, side->join, 0));
+  }
+  CART_CUDA(ep);
   CART_CUDA(launch_decode_combine(a, st));
   return CART_OK;
 }

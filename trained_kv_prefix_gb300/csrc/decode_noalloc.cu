@@ -137,6 +137,7 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   if (!std::isfinite(scale) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
     return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
+  if ((cache_rows + kNoallocChunk - 1) / kNoallocChunk > 256) return CART_ERR_GEOMETRY;
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* ptr : ptrs)
     if (!ptr || !al16(ptr)) return CART_ERR_POINTER;
@@ -181,8 +182,9 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
   a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
   a.chunk = kNoallocChunk;
-  if (launch_decode_prep(a, make_rope_freqs(d, rope_theta), st) != cudaSuccess) return CART_ERR_CUDA;
+  const RopeFreqs freqs = make_rope_freqs(d, rope_theta);
   if (p > 0) {
+    if (launch_decode_prep(a, freqs, st) != cudaSuccess) return CART_ERR_CUDA;
     CUtensorMap mQ, mKc, mVc;
     if (!rows_map(&mQ, a.q_rot, B * G, Hkv, d) || !rows_map(&mKc, kc, p, Hkv, d) ||
         !rows_map(&mVc, vc, p, Hkv, d))
@@ -209,7 +211,7 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
     l.decode = true;
     if (launch_fwd(l, st) != cudaSuccess) return CART_ERR_CUDA;
   }
-  if (launch_decode_private(a, st) != cudaSuccess) return CART_ERR_CUDA;
+  if (launch_decode_private(a, freqs, st) != cudaSuccess) return CART_ERR_CUDA;
   if (launch_decode_combine(a, st) != cudaSuccess) return CART_ERR_CUDA;
   return CART_OK;
 }

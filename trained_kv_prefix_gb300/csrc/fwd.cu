@@ -6,20 +6,20 @@
 // causal mask: key j of the real part is visible from query i iff j <= i).
 // (Cartridges guide, "Semantics", attention bullet.)
 //
-// Roles (192 threads):
-//   warps 0-3  softmax warpgroup: thread t owns query row t (TMEM lane t).
-//              Reads S from TMEM, masks, keeps the running max / sum in
-//              f32 (log2 domain), rescales O in TMEM when the max grows by
-//              more than 2^8, writes P (bf16) to shared memory in the
-//              128-byte-swizzled K-major layout, and finally normalises O.
-//   warp 4     TMA producer: Q tile once, then K/V tiles into a 2-stage ring.
-//   warp 5     MMA issuer (one thread): S = Q K^T and O += P V on tcgen05,
-//              accumulators in TMEM (S: 128 columns, O: d columns).
+// Roles (320 threads):
+//   warps 0-7  two softmax warpgroups.  Thread t of a group owns query row t
+//              (TMEM lane t); warpgroup w handles key columns [64w, 64w+64)
+//              of every 128-key tile.  The row maximum is exchanged between
+//              the two groups through shared memory; each keeps its own
+//              partial row sum and rescales its own half of O in TMEM when
+//              the maximum grows by more than 2^8 (lazy rescaling, log2
+//              domain).  P (bf16 pairs) is written back into TMEM over the
+//              group's own S columns.
+//   warp 8     TMA producer: Q tile once, then K/V tiles into a 2-stage ring.
+//   warp 9     MMA issuer (one thread): S = Q K^T into a double-buffered S
+//              (columns 0-127 / 128-255) and O += P V with P read from TMEM
+//              as the A operand (columns 256.. hold O).
 //
-// The same kernel also computes split-KV partials of the decode step over a
-// shared cartridge (rows of all conversations of one kv head batched into the
-// M dimension); then it writes O normalised by its own sum (f32) and the
-// log2-domain log-sum-exp per row.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,6 +40,8 @@ struct FwdParams {
   uint32_t* status;
 };
 
+constexpr int kFwdThreads = 320;
+
 template <int D>
 struct FwdSmem {
   static constexpr int kTileBytes = kTile * D * 2;      // one Q, K or V tile (bf16)
@@ -47,18 +49,21 @@ struct FwdSmem {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;
-  static constexpr int kPBytes = kTile * kTile * 2;
-  static constexpr int kBar = kP + kPBytes;
+  // row maxima [2 tile buffers][2 groups][128] then row sums [2 groups][128], f32
+  static constexpr int kRed = kV + kStages * kTileBytes;
+  static constexpr int kBar = kRed + 3 * 256 * 4;
   static constexpr int kBytes = kBar + 128;             // barriers + TMEM slot
   static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-B alignment
 };
 
-enum FwdBar { kQFull = 0, kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull, kSFree, kPFull,
-              kODone, kDrain, kNumBars };
+// kRedFull0/1: both softmax groups published a tile's row maxima; kLFull:
+// both published their row sums.  (mbarriers rather than a named barrier, so
+// that every wait stays bounded.)
+enum FwdBar { kQFull = 0, kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull0, kSFull1, kPFull0,
+              kPFull1, kODone, kRedFull0, kRedFull1, kLFull, kDrain, kNumBars };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdParams a) {
@@ -68,6 +73,7 @@ __global__ void __launch_bounds__(192, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kNumBars * 8);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -102,33 +108,32 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
-    mbar_init(&bars[kKVFull0], 1);
-    mbar_init(&bars[kKVFull1], 1);
-    mbar_init(&bars[kKVEmpty0], 1);
-    mbar_init(&bars[kKVEmpty1], 1);
-    mbar_init(&bars[kSFull], 1);
-    mbar_init(&bars[kSFree], 128);
-    mbar_init(&bars[kPFull], 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kKVFull0 + s], 1);
+      mbar_init(&bars[kKVEmpty0 + s], 1);
+      mbar_init(&bars[kSFull0 + s], 1);
+      mbar_init(&bars[kPFull0 + s], 256);
+      mbar_init(&bars[kRedFull0 + s], 256);
+    }
+    mbar_init(&bars[kLFull], 256);
     mbar_init(&bars[kODone], 1);
     mbar_init(&bars[kDrain], 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, 256);
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + 128;
+  const uint32_t tS0 = tmem;        // S buffers at columns 0 and 128
+  const uint32_t tO = tmem + 256;
   volatile int* abort_p = &abort_flag;
-
   uint8_t* sQ = smem + L::kQ;
-  uint8_t* sP = smem + L::kP;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer --
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&mQ);
@@ -179,31 +184,29 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA --
     if (lane == 0 && T > 0) {
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idPV = idesc_bf16(128, D, false, true);
-      // Base descriptors, computed once; each MMA below adds a compile-time
-      // byte offset (16-element K step inside a 64-element atom column, atom
-      // columns 16 KB apart; MN-major V steps 16 rows = 2048 B).
+      // Base descriptors, computed once; each MMA adds a compile-time offset.
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
-      const uint64_t dP0 = sdesc_sw128(smem_u32(sP), 16u, 1024u);
-      // stage 1 descriptors = stage 0 + one tile (selected, not indexed, so
-      // that nothing lands in local memory)
       const uint64_t dKs0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);
       const uint64_t dVs0 = sdesc_sw128(smem_u32(smem + L::kV), 16384u, 1024u);
       const uint64_t dKs1 = desc_add(dKs0, L::kTileBytes);
       const uint64_t dVs1 = desc_add(dVs0, L::kTileBytes);
       bool ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutMma);
+      // O += P V for tile t: P from TMEM buffer t&1 (K step k of 16 keys at
+      // column (k/4)*64 + (k%4)*8: warpgroup w packed keys 64w.. at 64w),
+      // V MN-major (16 rows = 2048 B per K step).
       auto issue_pv = [&](int t) {
         const int sp = t & 1;
         const uint64_t dv = sp ? dVs1 : dVs0;
-        umma_bf16_ss(tO, dP0, dv, idPV, t > 0 ? 1u : 0u);
+        const uint32_t tp = tS0 + sp * 128;
+        umma_bf16_ts(tO, tp, dv, idPV, t > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ss(tO, desc_add(dP0, (k >> 2) * 16384 + (k & 3) * 32), desc_add(dv, k * 2048),
-                       idPV, 1u);
+          umma_bf16_ts(tO, tp + (k >> 2) * 64 + (k & 3) * 8, desc_add(dv, k * 2048), idPV, 1u);
         umma_commit(&bars[kODone]);
         umma_commit(&bars[kKVEmpty0 + sp]);
       };
@@ -211,28 +214,29 @@ __global__ void __launch_bounds__(192, 1)
         const int s = t & 1;
         ok = mbar_wait(&bars[kKVFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
         if (!ok) break;
-        if (t > 0) {
-          ok = mbar_wait(&bars[kSFree], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
-          if (!ok) break;
-        }
         tc_fence_after();
+        // S buffer s last held P of tile t-2, read by the PV MMA issued
+        // before this point (one CTA's MMAs run in issue order).
         const uint64_t dk = s ? dKs1 : dKs0;
-        umma_bf16_ss(tS, dQ0, dk, idS, 0u);
+        const uint32_t ts = tS0 + s * 128;
+        umma_bf16_ss(ts, dQ0, dk, idS, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss(tS, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
+          umma_bf16_ss(ts, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
         }
-        umma_commit(&bars[kSFull]);
+        umma_commit(&bars[kSFull0 + s]);
         if (t > 0) {
-          ok = mbar_wait(&bars[kPFull], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+          ok = mbar_wait(&bars[kPFull0 + (s ^ 1)], ((t - 1) >> 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           issue_pv(t - 1);
         }
       }
       if (ok) {
-        ok = mbar_wait(&bars[kPFull], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kPFull0 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, abort_p, a.status,
+                       kDevErrTimeoutMma);
         if (ok) {
           tc_fence_after();
           issue_pv(T - 1);
@@ -246,53 +250,65 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax --
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int i = q0 + row;       // query row within its block
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int wg = warp >> 2;
+    const int row = threadIdx.x & 127;  // == TMEM lane
+    const int i = q0 + row;             // query row within its block
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float m = -INFINITY, l = 0.f;
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
-      ok = mbar_wait(&bars[kSFull], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      const int x = t & 1;
+      ok = mbar_wait(&bars[kSFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tS + lane_off + 0, r0);
-      tmem_ld32(tS + lane_off + 32, r1);
-      tmem_ld32(tS + lane_off + 64, r2);
-      tmem_ld32(tS + lane_off + 96, r3);
+      const uint32_t ts = tS0 + x * 128 + wg * 64 + lane_off;
+      uint32_t r0[32], r1[32];
+      tmem_ld32(ts, r0);
+      tmem_ld32(ts + 32, r1);
       tmem_ld_wait();
       tmem_reg_fence(r0);
       tmem_reg_fence(r1);
-      tmem_reg_fence(r2);
-      tmem_reg_fence(r3);
-      tc_fence_before();
-      mbar_arrive(&bars[kSFree]);
-
-      // number of leading visible columns of this tile for this row
+      // number of visible columns of this group's 64 (leading columns)
       int valid;
       if (t < n_ct) {
-        valid = min(kTile, a.p - (ct_lo + t) * kTile);
+        valid = a.p - (ct_lo + t) * kTile - wg * 64;
       } else {
-        const int col0 = (t - n_ct) * kTile;
+        const int col0 = (t - n_ct) * kTile + wg * 64;
         valid = min(i, a.n_real - 1) - col0 + 1;
-        valid = max(0, min(valid, kTile));
       }
-      float s[128];
+      valid = max(0, min(valid, 64));
+      float s[64];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(r0[c]);
-        s[32 + c] = __uint_as_float(r1[c]);
-        s[64 + c] = __uint_as_float(r2[c]);
-        s[96 + c] = __uint_as_float(r3[c]);
+        s[c] = __uint_as_float(r0[c]) * a.scale_log2;
+        s[32 + c] = __uint_as_float(r1[c]) * a.scale_log2;
       }
-      float rmax = -INFINITY;
+      if (__any_sync(0xffffffffu, valid < 64)) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float x = (c < valid) ? s[c] * a.scale_log2 : -INFINITY;
-        s[c] = x;
-        rmax = fmaxf(rmax, x);
+        for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
       }
+      // row maximum of this group's columns (4 independent chains), then of
+      // the whole tile through shared memory
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 64; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      float rmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      // Slot reuse is safe: the other group read this buffer two tiles ago,
+      // before it arrived on the other buffer's barrier, which this group has
+      // waited for since.
+      float* redt = red + x * 256;
+      redt[wg * 128 + row] = rmax;
+      mbar_arrive(&bars[kRedFull0 + x]);
+      ok = mbar_wait(&bars[kRedFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      rmax = fmaxf(rmax, redt[(wg ^ 1) * 128 + row]);
       // Lazy rescaling: keep the stale max unless the new one exceeds it by
       // more than 8 (P values then stay below 2^8, safe in bf16 / f32).
       float alpha = 1.f;
@@ -302,59 +318,66 @@ __global__ void __launch_bounds__(192, 1)
         m = rmax;
         rescale = t > 0;
       }
-      float rs = 0.f;
-      uint32_t pk[64];
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float p0 = exp2_approx(s[2 * c] - m);
         const float p1 = exp2_approx(s[2 * c + 1] - m);
-        rs += p0 + p1;
+        rs0 += p0;
+        rs1 += p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
+      // P over the first 32 columns of this group's S half (already read)
+      tmem_st32(ts, pk);
+      l = l * alpha + (rs0 + rs1);
       if (t > 0) {
         ok = mbar_wait(&bars[kODone], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
+          // this group's half of the O columns
 #pragma unroll
-          for (int blk = 0; blk < D / 32; ++blk) {
+          for (int blk = 0; blk < D / 64; ++blk) {
             uint32_t o[32];
-            tmem_ld32(tO + lane_off + blk * 32, o);
+            const uint32_t addr = tO + lane_off + wg * (D / 2) + blk * 32;
+            tmem_ld32(addr, o);
             tmem_ld_wait();
             tmem_reg_fence(o);
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(tO + lane_off + blk * 32, o);
+            tmem_st32(addr, o);
           }
-          tmem_st_wait();
         }
       }
-      l = l * alpha + rs;
-      // P row -> swizzled K-major tile: keys 0..63 in the first 16 KB atom
-      // column, 64..127 in the second.
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        uint4 v = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-        *reinterpret_cast<uint4*>(sP + (c16 >> 3) * 16384 + sw128_offset(row, c16 & 7)) = v;
-      }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[kPFull]);
+      mbar_arrive(&bars[kPFull0 + x]);
     }
     // ------------------------------------------------------------ epilogue --
     if (ok) {
       ok = mbar_wait(&bars[kODone], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
     }
+    // combine the two groups' row sums (own smem slots, own barrier)
+    float l_all = l;
+    if (ok) {
+      red[512 + wg * 128 + row] = l;
+      mbar_arrive(&bars[kLFull]);
+      ok = mbar_wait(&bars[kLFull], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) l_all = l + red[512 + (wg ^ 1) * 128 + row];
+    }
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / l_all;
       const bool row_ok = i < a.n_rows;
 #pragma unroll
-      for (int blk = 0; blk < D / 32; ++blk) {
+      for (int blk = 0; blk < D / 64; ++blk) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + blk * 32, o);
+        const int col = wg * (D / 2) + blk * 32;
+        tmem_ld32(tO + lane_off + col, o);
         tmem_ld_wait();
         tmem_reg_fence(o);
         if (row_ok) {
@@ -366,7 +389,7 @@ __global__ void __launch_bounds__(192, 1)
             else
               dst = static_cast<float*>(a.out) +
                     ((static_cast<long long>(qb) * a.n_rows + i) * a.Hq_map + head) * D;
-            float4* d4 = reinterpret_cast<float4*>(dst + blk * 32);
+            float4* d4 = reinterpret_cast<float4*>(dst + col);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               d4[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l,
@@ -376,7 +399,7 @@ __global__ void __launch_bounds__(192, 1)
           } else {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
                                  ((static_cast<long long>(qb) * a.n_rows + i) * a.Hq_map + head) * D;
-            uint4* d4 = reinterpret_cast<uint4*>(dst + blk * 32);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
               d4[c] = make_uint4(
@@ -387,8 +410,8 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      if (row_ok) {
-        const float lse2 = m + __log2f(l);
+      if (row_ok && wg == 0) {
+        const float lse2 = m + __log2f(l_all);
         if (a.decode)
           a.lse[(static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i] = lse2;
         else
@@ -401,7 +424,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 256);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 template <int D>
@@ -431,7 +454,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   else
     grid = dim3(a.Hq_map, p.n_qtiles, a.n_splits);
   TraceScope tr(a.decode ? "decode_cartridge" : "fwd", st);
-  fwd_kernel<D><<<grid, 192, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
+  fwd_kernel<D><<<grid, kFwdThreads, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
   return cudaGetLastError();
 }
 

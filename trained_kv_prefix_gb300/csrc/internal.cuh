@@ -30,6 +30,11 @@ struct TraceScope {
   TraceScope& operator=(const TraceScope&) = delete;
 };
 
+// 4D bf16 TMA map over a [blocks, rows, H, d] tensor as (d, H, rows, blocks)
+// with a 64 x 1 x box_rows x 1 box and 128-byte swizzle (api.cu).
+bool make_bf16_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, int H, int d,
+                        unsigned box_rows);
+
 // fp64 inverse frequencies theta^(-2j/d), j < d/2, passed by value.
 struct RopeFreqs {
   double inv_freq[kMaxHeadDim / 2];
@@ -131,8 +136,10 @@ struct DecodeLaunch {
   float* priv_ml;           // [B, Hkv, chunks, G, 2]
   int chunk;                // private keys per CTA
 };
+// Rotated queries [B*G, Hkv, d] for the cartridge pass.
 cudaError_t launch_decode_prep(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
-cudaError_t launch_decode_private(const DecodeLaunch& a, cudaStream_t st);
+// The private pass also rotates the queries and appends the new token's row.
+cudaError_t launch_decode_private(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t st);
 
 }  // namespace cart
