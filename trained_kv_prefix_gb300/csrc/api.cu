@@ -431,10 +431,10 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
 
 // ------------------------------------------------------------------ decode --
 namespace {
-constexpr int kDecodeChunk = 128;
 
 struct DecodeWs {
-  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, total = 0;
+  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, counters = 0,
+         total = 0;
   int splits = 0, tiles_per_split = 0;
 };
 
@@ -463,6 +463,7 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
   w.priv_part = take(static_cast<size_t>(B) * Hq * chunks * d * 4);
   w.priv_ml = take(static_cast<size_t>(B) * Hq * chunks * 2 * 4);
+  w.counters = take(static_cast<size_t>(B) * Hkv * 4);
   w.total = off;
   return w;
 }
@@ -475,7 +476,7 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
   if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
   if (!std::isfinite(scale) || !(theta > 0.0) || !std::isfinite(theta)) return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
-  if ((rows + kDecodeChunk - 1) / kDecodeChunk > 256) return CART_ERR_GEOMETRY;  // <= 32767 rows
+  if ((rows + kDecodeChunk - 1) / kDecodeChunk > 256) return CART_ERR_GEOMETRY;  // <= 32768 rows
   return CART_OK;
 }
 }  // namespace
@@ -501,9 +502,7 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int G = Hq / Hkv, R = B * G;
   DecodeLaunch a{};
   a.B = B;
   a.Hq = Hq;
@@ -523,66 +522,14 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
   a.o = static_cast<__nv_bfloat16*>(o);
   a.q_rot = reinterpret_cast<__nv_bfloat16*>(ws + w.q_rot);
   a.n_cart_splits = w.splits;
+  a.cart_tiles_per_split = w.tiles_per_split;
   a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
   a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
   a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
   a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
+  a.counters = reinterpret_cast<int*>(ws + w.counters);
   a.chunk = kDecodeChunk;
-  const RopeFreqs freqs = make_rope_freqs(d, rope_theta);
-  // The cartridge split pass (tensor cores, with the query rotation it
-  // needs) and the private pass (HBM) are independent: the former runs on the
-  // helper stream.
-  SideStream* side = p > 0 ? side_stream() : nullptr;
-  cudaStream_t st_cart = side ? side->s : st;
-  if (side) {
-    CART_CUDA(cudaEventRecord(side->fork, st));
-    CART_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-  }
-  if (p > 0) {
-    const cudaError_t e0 = launch_decode_prep(a, freqs, st_cart);
-    if (e0 != cudaSuccess && side) {
-      cudaEventRecord(side->join, side->s);
-      cudaStreamWaitEvent(st, side->join, 0);
-    }
-    CART_CUDA(e0);
-    CUtensorMap mQ, mKc, mVc;
-    if (!make_rows_map(&mQ, a.q_rot, 1, R, Hkv, d, 128) ||
-        !make_rows_map(&mKc, kc, 1, p, Hkv, d, 128) || !make_rows_map(&mVc, vc, 1, p, Hkv, d, 128))
-      return CART_ERR_CUDA;
-    FwdLaunch l{};
-    l.mQ = &mQ;
-    l.mKc = &mKc;
-    l.mVc = &mVc;
-    l.mK = &mKc;  // no real-token tiles in this mode
-    l.mV = &mVc;
-    l.d = d;
-    l.n_rows = R;
-    l.n_qblocks = 1;
-    l.Hq_map = Hkv;
-    l.G = 1;
-    l.p = p;
-    l.n_real = 0;
-    l.cart_tiles_per_split = w.tiles_per_split;
-    l.n_splits = w.splits;
-    l.scale_log2 = scale * 1.4426950408889634f;
-    l.out = const_cast<float*>(a.cart_part);
-    l.out_f32 = true;
-    l.lse = const_cast<float*>(a.cart_lse);
-    l.decode = true;
-    const cudaError_t e = launch_fwd(l, st_cart);
-    if (e != cudaSuccess && side) {  // keep the helper stream joined
-      cudaEventRecord(side->join, side->s);
-      cudaStreamWaitEvent(st, side->join, 0);
-    }
-    CART_CUDA(e);
-  }
-  const cudaError_t ep = launch_decode_private(a, freqs, st);
-  if (side) {
-    CART_CUDA(cudaEventRecord(side->join, side->s));
-    CART_CUDA(cudaStreamWaitEvent(st, side->join, 0));
-  }
-  CART_CUDA(ep);
-  CART_CUDA(launch_decode_combine(a, st));
+  CART_CUDA(launch_decode(a, make_rope_freqs(d, rope_theta), static_cast<cudaStream_t>(stream)));
   return CART_OK;
 }
 

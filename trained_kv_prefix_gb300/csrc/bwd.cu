@@ -787,11 +787,9 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.accumulate = l.accumulate;
   p.table = l.table;
   p.status = device_status_ptr();
-  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DkdvSmem<D>::kAlloc);
+  cudaError_t e = set_smem_once<dkdv_kernel<D>>(DkdvSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           DqSmem<D>::kAlloc);
+  e = set_smem_once<dq_kernel<D>>(DqSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_blocks = p.n_ct * p.Hkv + p.n_rt * p.Hkv * p.B;
   if (n_blocks > 0) {

@@ -7,13 +7,15 @@
 //             reduction once per conversation) and lays the rotated queries
 //             out per kv head as [B*G rows, Hkv, d], so that the cartridge
 //             part runs as ONE tensor-core problem per kv head (rows of all
-//             conversations batched into M) -- see fwd.cu.  It and the
-//             cartridge pass run on a second stream, next to the private pass.
+//             conversations batched into M) -- see fwd.cu; zeroes the
+//             arrival counters.
 //   private   split-KV over each conversation's own rows 0..len[b]: TMA-staged
 //             chunks, mma.sync for the two small products, the new token's
-//             rotation and append fused in.  Bound by HBM.
-//   combine   merges the cartridge splits and the private chunks of every
-//             (conversation, head) with their log-sum-exps.
+//             rotation and append fused in.  Bound by HBM.  Launched as the
+//             programmatic dependent of the cartridge pass, so the two run
+//             together; the last CTA of each (conversation, kv head) waits
+//             for the cartridge grid and merges all parts with their
+//             log-sum-exps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,6 +60,8 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const 
     cs[threadIdx.x] = make_float2(c - s * rl, s + c * rl);
   }
   __syncthreads();
+  if (threadIdx.x < a.Hkv) a.counters[b * a.Hkv + threadIdx.x] = 0;
+  if (a.p == 0) return;
   const int chunks = half / 8;  // 8 pair indices per task
   const int tasks = a.Hq * chunks;
   for (int t = threadIdx.x; t < tasks; t += blockDim.x) {
@@ -83,8 +87,99 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const 
   }
 }
 
+constexpr int kPrivCH = kDecodeChunk;
+constexpr int kPrivBox = 32;
+constexpr int kPrivMT = kPrivCH / 64;  // m16 key tiles per warp
+
+// ------------------------------------------------------------- combine ----
+// One warp merges the parts of one (conversation b, query head h); lane owns
+// d/32 dims.  All log-sum-exps are in the log2 domain.  Part p < S is
+// cartridge split p (normalised output, lse); part S + c is private chunk c
+// (unnormalised acc against m, sum l).  Partials written by other CTAs are
+// read through L2 (ld.global.cg).
+__device__ __forceinline__ void combine_head_warp(const DecodeLaunch& a, int b, int h, int lane) {
+  const int G = a.Hq / a.Hkv, g = h / G, hh = h % G;
+  const int d = a.d;
+  const int R = a.B * G, r = b * G + hh;
+  const int L = clamp_len(a.len, b, a.rows);
+  const int n_chunks = (a.rows + kPrivCH - 1) / kPrivCH;
+  const int S = a.n_cart_splits;
+  const int np = S + L / kPrivCH + 1;
+  const long long pbase = ((static_cast<long long>(b) * a.Hkv + g) * n_chunks) * G + hh;
+  auto part_lw = [&](int p, float* scale_m, float* lsum) {
+    if (p < S) {
+      *scale_m = __ldcg(a.cart_lse + (static_cast<long long>(p) * a.Hkv + g) * R + r);
+      *lsum = 1.f;
+      return *scale_m;
+    }
+    const long long pi = pbase + static_cast<long long>(p - S) * G;
+    *scale_m = __ldcg(a.priv_ml + pi * 2);
+    *lsum = __ldcg(a.priv_ml + pi * 2 + 1);
+    return *scale_m + __log2f(*lsum);
+  };
+  float M = -INFINITY;
+  for (int p = lane; p < np; p += 32) {
+    float sm, ls;
+    M = fmaxf(M, part_lw(p, &sm, &ls));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float num[4] = {0.f, 0.f, 0.f, 0.f};
+  float den = 0.f;
+  const int per_lane = d / 32;  // 4 or 2
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    float w = 0.f, dn = 0.f;
+    if (p0 + lane < np) {
+      float sm, ls;
+      part_lw(p0 + lane, &sm, &ls);
+      w = exp2_approx(sm - M);   // scales the stored row
+      dn = w * ls;
+    }
+    const int cnt = min(32, np - p0);
+    // eight parts per round: all eight rows are requested before any is used
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int p = p0 + j0 + u;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 + u < cnt) {
+          const float* src = p < S
+              ? a.cart_part + ((static_cast<long long>(p) * a.Hkv + g) * R + r) * d
+              : a.priv_part + (pbase + static_cast<long long>(p - S) * G) * d;
+          if (per_lane == 4) {
+            v[u] = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+          } else {
+            const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src) + lane);
+            v[u] = make_float4(t2.x, t2.y, 0.f, 0.f);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = min(j0 + u, 31);
+        const float wj = (j0 + u < cnt) ? __shfl_sync(0xffffffffu, w, j) : 0.f;
+        const float dj = __shfl_sync(0xffffffffu, dn, j);
+        if (j0 + u < cnt) den += dj;
+        num[0] = fmaf(wj, v[u].x, num[0]);
+        num[1] = fmaf(wj, v[u].y, num[1]);
+        num[2] = fmaf(wj, v[u].z, num[2]);
+        num[3] = fmaf(wj, v[u].w, num[3]);
+      }
+    }
+  }
+  const float inv = 1.f / den;
+  __nv_bfloat16* out = a.o + (static_cast<long long>(b) * a.Hq + h) * d + lane * per_lane;
+  if (per_lane == 4) {
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(num[0] * inv, num[1] * inv),
+                                                pack_bf16x2(num[2] * inv, num[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(num[0] * inv, num[1] * inv);
+  }
+}
+
 // ------------------------------------------------------------- private ----
-// grid: (chunks, Hkv, B); block: 128 threads (4 warps).  Keys of the chunk:
+// grid: (Hkv, chunks, B); block: 128 threads (4 warps).  Keys of the chunk:
 // private rows [c*CH, min((c+1)*CH, len+1)).
 //   * TMA stages the chunk's K and V rows in shared memory (128-byte
 //     swizzle, 32-row boxes, only as many boxes as the chunk has rows).
@@ -99,16 +194,14 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const 
 //     ldmatrix.trans (warp w owns output dims 32w..32w+31).
 // Output per query head: unnormalised acc[d] against the chunk's own max m
 // (log2 domain) and its sum l.
-constexpr int kPrivCH = 128;
-constexpr int kPrivBox = 32;
 
 template <int D>
 struct PrivSmem {
   static constexpr int kHalf = kPrivCH * 128;          // 64 dims x 128 rows (bf16)
   static constexpr int kK = 0;
   static constexpr int kV = kK + (D / 64) * kHalf;
-  static constexpr int kP = kV + (D / 64) * kHalf;     // bf16 [8 queries][136]
-  static constexpr int kPStride = 136;                 // elements per P row (272 B)
+  static constexpr int kP = kV + (D / 64) * kHalf;     // bf16 [8 queries][CH + 8]
+  static constexpr int kPStride = kPrivCH + 8;         // padded row: conflict-free B loads
   static constexpr int kCS = kP + 8 * kPStride * 2;    // float2 [D/2]
   static constexpr int kRed = kCS + (D / 2) * 8;       // f32 [2][4 warps][8]
   static constexpr int kBar = kRed + 2 * 4 * 8 * 4;
@@ -171,7 +264,9 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
   __shared__ int abort_flag;
 
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // kv head fastest: the CTAs reading the interleaved head slices of the
+  // same cache rows run together (DRAM row locality)
+  const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
   const int Lb = clamp_len(a.len, b, a.rows);
   const int k0 = c * CH;
   if (k0 > Lb) return;  // whole chunk beyond this conversation's rows
@@ -281,15 +376,16 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   }
   __syncthreads();
 
-  // ---- S^T = K Q^T for this warp's 32 keys (two m16 tiles)
-  float sacc[2][4];
+  // ---- S^T = K Q^T for this warp's keys (MT m16 tiles)
+  constexpr int MT = kPrivMT;
+  float sacc[MT][4];
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt) {
+  for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) sacc[mt][e] = 0.f;
     // lane -> row address: matrices (rows 0-7,k lo), (rows 8-15,k lo),
     // (rows 0-7,k hi), (rows 8-15,k hi)
-    const int row = warp * 32 + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int row = warp * 16 * MT + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       uint32_t af[4];
@@ -303,10 +399,10 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   for (int qq = 0; qq < 2; ++qq) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int key = warp * 32 + mt * 16 + g8 + 8 * hf;
+        const int key = warp * 16 * MT + mt * 16 + g8 + 8 * hf;
         float sv = sacc[mt][2 * hf + qq] * scale_log2;
         sv = key < kn ? sv : -INFINITY;
         sacc[mt][2 * hf + qq] = sv;
@@ -328,10 +424,10 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
     mq[qq] = fmaxf(fmaxf(sred[q], sred[8 + q]), fmaxf(sred[16 + q], sred[24 + q]));
     float sum = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int key = warp * 32 + mt * 16 + g8 + 8 * hf;
+        const int key = warp * 16 * MT + mt * 16 + g8 + 8 * hf;
         const float pv = exp2_approx(sacc[mt][2 * hf + qq] - mq[qq]);  // 0 for masked keys
         sum += pv;
         sP[q * L::kPStride + key] = __float2bfloat16_rn(pv);
@@ -392,150 +488,107 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
         if (q < G) a.priv_part[(part_idx + q) * D + 16 * dt + g8 + 8 * hf] = oacc[2 * hf + qq];
       }
   }
-}
 
-// ------------------------------------------------------------- combine ----
-// One warp per (conversation, query head); lane owns d/32 dims.  All
-// log-sum-exps are in the log2 domain.  Part p < S is cartridge split p
-// (normalised output, lse); part S + c is private chunk c (unnormalised acc
-// against m, sum l).
-__global__ void __launch_bounds__(256) decode_combine_kernel(DecodeLaunch a) {
-  const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (warp_global >= a.B * a.Hq) return;
-  const int b = warp_global / a.Hq, h = warp_global % a.Hq;
-  const int G = a.Hq / a.Hkv, g = h / G, hh = h % G;
-  const int d = a.d;
-  const int R = a.B * G, r = b * G + hh;
-  const int L = clamp_len(a.len, b, a.rows);
-  const int n_chunks = (a.rows + kPrivCH - 1) / kPrivCH;
-  const int S = a.n_cart_splits;
-  const int np = S + L / kPrivCH + 1;
-  const long long pbase = ((static_cast<long long>(b) * a.Hkv + g) * n_chunks) * G + hh;
-  auto part_lw = [&](int p, float* scale_m, float* lsum) {
-    if (p < S) {
-      *scale_m = a.cart_lse[(static_cast<long long>(p) * a.Hkv + g) * R + r];
-      *lsum = 1.f;
-      return *scale_m;
-    }
-    const long long pi = pbase + static_cast<long long>(p - S) * G;
-    *scale_m = a.priv_ml[pi * 2];
-    *lsum = a.priv_ml[pi * 2 + 1];
-    return *scale_m + __log2f(*lsum);
-  };
-  float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) {
-    float sm, ls;
-    M = fmaxf(M, part_lw(p, &sm, &ls));
+  // ---- the last private CTA of (b, g) merges every part of its G heads
+  __shared__ int s_last;
+  __threadfence();  // this CTA's partials are visible before it is counted
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(a.counters + b * a.Hkv + g, 1);
+    s_last = prev == Lb / CH;  // used chunks of this conversation = Lb/CH + 1
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float num[4] = {0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-  const int per_lane = d / 32;  // 4 or 2
-  for (int p0 = 0; p0 < np; p0 += 32) {
-    float w = 0.f, dn = 0.f;
-    if (p0 + lane < np) {
-      float sm, ls;
-      part_lw(p0 + lane, &sm, &ls);
-      w = exp2_approx(sm - M);   // scales the stored row
-      dn = w * ls;
-    }
-    const int cnt = min(32, np - p0);
-    // eight parts per round: all eight rows are requested before any is used
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int p = p0 + j0 + u;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j0 + u < cnt) {
-          const float* src = p < S
-              ? a.cart_part + ((static_cast<long long>(p) * a.Hkv + g) * R + r) * d
-              : a.priv_part + (pbase + static_cast<long long>(p - S) * G) * d;
-          if (per_lane == 4) {
-            v[u] = __ldg(reinterpret_cast<const float4*>(src) + lane);
-          } else {
-            const float2 t2 = __ldg(reinterpret_cast<const float2*>(src) + lane);
-            v[u] = make_float4(t2.x, t2.y, 0.f, 0.f);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = min(j0 + u, 31);
-        const float wj = (j0 + u < cnt) ? __shfl_sync(0xffffffffu, w, j) : 0.f;
-        const float dj = __shfl_sync(0xffffffffu, dn, j);
-        if (j0 + u < cnt) den += dj;
-        num[0] = fmaf(wj, v[u].x, num[0]);
-        num[1] = fmaf(wj, v[u].y, num[1]);
-        num[2] = fmaf(wj, v[u].z, num[2]);
-        num[3] = fmaf(wj, v[u].w, num[3]);
-      }
-    }
-  }
-  const float inv = 1.f / den;
-  __nv_bfloat16* out = a.o + (static_cast<long long>(b) * a.Hq + h) * d + lane * per_lane;
-  if (per_lane == 4) {
-    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(num[0] * inv, num[1] * inv),
-                                                pack_bf16x2(num[2] * inv, num[3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(num[0] * inv, num[1] * inv);
-  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // the cartridge partials come from the grid this one depends on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int hh = warp; hh < G; hh += 4) combine_head_warp(a, b, g * G + hh, lane);
+  if (tid == 0) a.counters[b * a.Hkv + g] = 0;
 }
 
 template <int D, int G>
 cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, const CUtensorMap& mK,
-                              const CUtensorMap& mV, cudaStream_t st) {
+                              const CUtensorMap& mV, bool dependent, cudaStream_t st) {
   using L = PrivSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(decode_private_kernel<D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  cudaError_t e = set_smem_once<decode_private_kernel<D, G>>(L::kAlloc);
   if (e != cudaSuccess) return e;
-  const dim3 grid((a.rows + kPrivCH - 1) / kPrivCH, a.Hkv, a.B);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hkv, (a.rows + kPrivCH - 1) / kPrivCH, a.B);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
   const float scale_log2 = a.scale * 1.4426950408889634f;
   TraceScope tr("decode_private", st);
-  decode_private_kernel<D, G><<<grid, 128, L::kAlloc, st>>>(mK, mV, a, f, scale_log2,
-                                                            device_status_ptr());
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, mK, mV, a, f, scale_log2,
+                            device_status_ptr());
 }
 
 }  // namespace
 
-cudaError_t launch_decode_prep(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
-  TraceScope tr("decode_prep", st);
-  decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_decode_private(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
   const int G = a.Hq / a.Hkv;
   if (a.chunk != kPrivCH) return cudaErrorInvalidValue;
+  {
+    TraceScope tr("decode_prep", st);
+    decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.p > 0) {
+    CUtensorMap mQ, mKc, mVc;
+    if (!make_bf16_rows_map(&mQ, a.q_rot, 1, a.B * G, a.Hkv, a.d, 128) ||
+        !make_bf16_rows_map(&mKc, a.kc, 1, a.p, a.Hkv, a.d, 128) ||
+        !make_bf16_rows_map(&mVc, a.vc, 1, a.p, a.Hkv, a.d, 128))
+      return cudaErrorInvalidValue;
+    FwdLaunch l{};
+    l.mQ = &mQ;
+    l.mKc = &mKc;
+    l.mVc = &mVc;
+    l.mK = &mKc;  // no real-token tiles in decode mode
+    l.mV = &mVc;
+    l.d = a.d;
+    l.n_rows = a.B * G;
+    l.n_qblocks = 1;
+    l.Hq_map = a.Hkv;
+    l.G = 1;
+    l.p = a.p;
+    l.n_real = 0;
+    l.cart_tiles_per_split = a.cart_tiles_per_split;
+    l.n_splits = a.n_cart_splits;
+    l.scale_log2 = a.scale * 1.4426950408889634f;
+    l.out = const_cast<float*>(a.cart_part);
+    l.out_f32 = true;
+    l.lse = const_cast<float*>(a.cart_lse);
+    l.decode = true;
+    e = launch_fwd(l, st);
+    if (e != cudaSuccess) return e;
+  }
   CUtensorMap mK, mV;
   if (!make_bf16_rows_map(&mK, a.k_cache, a.B, a.rows, a.Hkv, a.d, kPrivBox) ||
       !make_bf16_rows_map(&mV, a.v_cache, a.B, a.rows, a.Hkv, a.d, kPrivBox))
     return cudaErrorInvalidValue;
+  const bool dep = a.p > 0;
   if (a.d == 128) {
     switch (G) {
-      case 1: return launch_private_dg<128, 1>(a, f, mK, mV, st);
-      case 2: return launch_private_dg<128, 2>(a, f, mK, mV, st);
-      case 4: return launch_private_dg<128, 4>(a, f, mK, mV, st);
-      case 8: return launch_private_dg<128, 8>(a, f, mK, mV, st);
+      case 1: return launch_private_dg<128, 1>(a, f, mK, mV, dep, st);
+      case 2: return launch_private_dg<128, 2>(a, f, mK, mV, dep, st);
+      case 4: return launch_private_dg<128, 4>(a, f, mK, mV, dep, st);
+      case 8: return launch_private_dg<128, 8>(a, f, mK, mV, dep, st);
     }
   } else if (a.d == 64) {
     switch (G) {
-      case 1: return launch_private_dg<64, 1>(a, f, mK, mV, st);
-      case 2: return launch_private_dg<64, 2>(a, f, mK, mV, st);
-      case 4: return launch_private_dg<64, 4>(a, f, mK, mV, st);
-      case 8: return launch_private_dg<64, 8>(a, f, mK, mV, st);
+      case 1: return launch_private_dg<64, 1>(a, f, mK, mV, dep, st);
+      case 2: return launch_private_dg<64, 2>(a, f, mK, mV, dep, st);
+      case 4: return launch_private_dg<64, 4>(a, f, mK, mV, dep, st);
+      case 8: return launch_private_dg<64, 8>(a, f, mK, mV, dep, st);
     }
   }
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t st) {
-  TraceScope tr("decode_combine", st);
-  decode_combine_kernel<<<(a.B * a.Hq + 7) / 8, 256, 0, st>>>(a);
-  return cudaGetLastError();
 }
 
 }  // namespace cart

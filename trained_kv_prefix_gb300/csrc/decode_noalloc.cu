@@ -16,8 +16,10 @@
 // that device current) and caches it; that first call should come before any
 // stream capture.  All calls share the one array: calls whose work overlaps
 // on the GPU (different streams, or different host threads without ordering)
-// race on it.  Every scratch word a call reads is written earlier in the
-// same call, so nothing needs to be cleared between calls.
+// race on it.  The only words that must start at zero (the per-conversation
+// arrival counters) are cleared at the start of every call by its first
+// kernel; every other scratch word a call reads is written earlier in the
+// same call.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,10 +36,11 @@ static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[CART_DEC
 namespace cart {
 namespace {
 
-constexpr int kNoallocChunk = 128;  // private keys per CTA, as in cart_attn_decode
+constexpr int kNoallocChunk = kDecodeChunk;  // private keys per CTA
 
 struct NoallocLayout {
-  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, total = 0;
+  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, counters = 0,
+         total = 0;
   int splits = 0, tiles_per_split = 0;
 };
 
@@ -67,6 +70,7 @@ NoallocLayout layout(int B, int Hq, int Hkv, int d, int p, int rows) {
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
   w.priv_part = take(static_cast<size_t>(B) * Hq * chunks * d * 4);
   w.priv_ml = take(static_cast<size_t>(B) * Hq * chunks * 2 * 4);
+  w.counters = take(static_cast<size_t>(B) * Hkv * 4);
   w.total = off;
   return w;
 }
@@ -92,30 +96,6 @@ int scratch_address(void** out) {
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool rows_map(CUtensorMap* m, const void* base, int rows, int H, int d) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  if (!fn) return false;
-  const uint64_t e = 2;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(rows), 1};
-  cuuint64_t strides[3] = {d * e, static_cast<uint64_t>(H) * d * e,
-                           static_cast<uint64_t>(rows) * H * d * e};
-  cuuint32_t box[4] = {64, 1, 128, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 }  // namespace
 }  // namespace cart
@@ -177,41 +157,13 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   a.o = static_cast<__nv_bfloat16*>(o);
   a.q_rot = reinterpret_cast<__nv_bfloat16*>(ws + w.q_rot);
   a.n_cart_splits = w.splits;
+  a.cart_tiles_per_split = w.tiles_per_split;
   a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
   a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
   a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
   a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
+  a.counters = reinterpret_cast<int*>(ws + w.counters);
   a.chunk = kNoallocChunk;
-  const RopeFreqs freqs = make_rope_freqs(d, rope_theta);
-  if (p > 0) {
-    if (launch_decode_prep(a, freqs, st) != cudaSuccess) return CART_ERR_CUDA;
-    CUtensorMap mQ, mKc, mVc;
-    if (!rows_map(&mQ, a.q_rot, B * G, Hkv, d) || !rows_map(&mKc, kc, p, Hkv, d) ||
-        !rows_map(&mVc, vc, p, Hkv, d))
-      return CART_ERR_CUDA;
-    FwdLaunch l{};
-    l.mQ = &mQ;
-    l.mKc = &mKc;
-    l.mVc = &mVc;
-    l.mK = &mKc;  // no real-token tiles in decode mode
-    l.mV = &mVc;
-    l.d = d;
-    l.n_rows = B * G;
-    l.n_qblocks = 1;
-    l.Hq_map = Hkv;
-    l.G = 1;
-    l.p = p;
-    l.n_real = 0;
-    l.cart_tiles_per_split = w.tiles_per_split;
-    l.n_splits = w.splits;
-    l.scale_log2 = scale * 1.4426950408889634f;
-    l.out = const_cast<float*>(a.cart_part);
-    l.out_f32 = true;
-    l.lse = const_cast<float*>(a.cart_lse);
-    l.decode = true;
-    if (launch_fwd(l, st) != cudaSuccess) return CART_ERR_CUDA;
-  }
-  if (launch_decode_private(a, freqs, st) != cudaSuccess) return CART_ERR_CUDA;
-  if (launch_decode_combine(a, st) != cudaSuccess) return CART_ERR_CUDA;
+  if (launch_decode(a, make_rope_freqs(d, rope_theta), st) != cudaSuccess) return CART_ERR_CUDA;
   return CART_OK;
 }

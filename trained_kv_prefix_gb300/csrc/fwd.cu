@@ -42,10 +42,12 @@ struct FwdParams {
 
 constexpr int kFwdThreads = 320;
 
-template <int D>
+// NS = K/V stages in shared memory: 2 for training; 1 in decode mode, where
+// the cartridge pass runs next to the private pass and leaves it room.
+template <int D, int NS>
 struct FwdSmem {
   static constexpr int kTileBytes = kTile * D * 2;      // one Q, K or V tile (bf16)
-  static constexpr int kStages = 2;
+  static constexpr int kStages = NS;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
@@ -62,12 +64,12 @@ struct FwdSmem {
 enum FwdBar { kQFull = 0, kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull0, kSFull1, kPFull0,
               kPFull1, kODone, kRedFull0, kRedFull1, kLFull, kDrain, kNumBars };
 
-template <int D>
+template <int D, int NS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdParams a) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -106,6 +108,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int T = n_ct + n_rt;
 
   if (threadIdx.x == 0) {
+    // decode mode: let the dependent private pass start right away (it only
+    // waits for this grid where it reads the cartridge partials)
+    if (a.decode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
     for (int s = 0; s < 2; ++s) {
@@ -148,9 +153,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < T; ++t) {
-        const int s = t & 1;
-        if (t >= 2) {
-          ok = mbar_wait(&bars[kKVEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
+        const int s = t % NS;
+        if (t >= NS) {
+          ok = mbar_wait(&bars[kKVEmpty0 + s], ((t / NS) - 1) & 1, abort_p, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
@@ -179,8 +184,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // the CTA releases its shared memory.
         int dummy = 0;
         mbar_wait(&bars[kQFull], 0, &dummy, nullptr, 0);
-        for (int t = max(issued - 2, 0); t < issued; ++t)
-          mbar_wait(&bars[kKVFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
+        for (int t = max(issued - NS, 0); t < issued; ++t)
+          mbar_wait(&bars[kKVFull0 + t % NS], (t / NS) & 1, &dummy, nullptr, 0);
       }
     }
     __syncwarp();
@@ -200,9 +205,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // column (k/4)*64 + (k%4)*8: warpgroup w packed keys 64w.. at 64w),
       // V MN-major (16 rows = 2048 B per K step).
       auto issue_pv = [&](int t) {
-        const int sp = t & 1;
+        const int sp = t % NS;           // smem stage of V
         const uint64_t dv = sp ? dVs1 : dVs0;
-        const uint32_t tp = tS0 + sp * 128;
+        const uint32_t tp = tS0 + (t & 1) * 128;  // TMEM buffer holding P
         umma_bf16_ts(tO, tp, dv, idPV, t > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
@@ -211,13 +216,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         umma_commit(&bars[kKVEmpty0 + sp]);
       };
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t & 1;
-        ok = mbar_wait(&bars[kKVFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        const int ks = t % NS, s = t & 1;
+        ok = mbar_wait(&bars[kKVFull0 + ks], (t / NS) & 1, abort_p, a.status, kDevErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         // S buffer s last held P of tile t-2, read by the PV MMA issued
         // before this point (one CTA's MMAs run in issue order).
-        const uint64_t dk = s ? dKs1 : dKs0;
+        const uint64_t dk = ks ? dKs1 : dKs0;
         const uint32_t ts = tS0 + s * 128;
         umma_bf16_ss(ts, dQ0, dk, idS, 0u);
 #pragma unroll
@@ -226,7 +231,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           umma_bf16_ss(ts, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
         }
         umma_commit(&bars[kSFull0 + s]);
-        if (t > 0) {
+        if constexpr (NS == 1) {
+          // one K/V slot: PV(t) must free it before tile t+1 can load
+          ok = mbar_wait(&bars[kPFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t);
+        } else if (t > 0) {
           ok = mbar_wait(&bars[kPFull0 + (s ^ 1)], ((t - 1) >> 1) & 1, abort_p, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
@@ -234,7 +245,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           issue_pv(t - 1);
         }
       }
-      if (ok) {
+      if (NS > 1 && ok) {
         ok = mbar_wait(&bars[kPFull0 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, abort_p, a.status,
                        kDevErrTimeoutMma);
         if (ok) {
@@ -427,12 +438,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int D, int NS>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, NS>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kAlloc);
+  cudaError_t e = set_smem_once<fwd_kernel<D, NS>>(L::kAlloc);
   if (e != cudaSuccess) return e;
   FwdParams p{};
   p.n_rows = a.n_rows;
@@ -454,15 +464,20 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   else
     grid = dim3(a.Hq_map, p.n_qtiles, a.n_splits);
   TraceScope tr(a.decode ? "decode_cartridge" : "fwd", st);
-  fwd_kernel<D><<<grid, kFwdThreads, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
+  fwd_kernel<D, NS><<<grid, kFwdThreads, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
-  if (a.d == 128) return launch_fwd_d<128>(a, st);
-  if (a.d == 64) return launch_fwd_d<64>(a, st);
+  if (a.decode) {
+    if (a.d == 128) return launch_fwd_d<128, 1>(a, st);
+    if (a.d == 64) return launch_fwd_d<64, 1>(a, st);
+  } else {
+    if (a.d == 128) return launch_fwd_d<128, 2>(a, st);
+    if (a.d == 64) return launch_fwd_d<64, 2>(a, st);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -13,6 +15,21 @@ namespace cart {
 
 constexpr int kTile = 128;          // query rows / key rows per tcgen05 tile
 constexpr int kMaxHeadDim = 128;
+
+// Raises a kernel's dynamic shared-memory limit once per device (the call is
+// comparatively slow and the setting persists for the process).
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit);
+  return e;
+}
 
 // Device status word (bits from ptx.cuh); one per device.
 uint32_t* device_status_ptr();
@@ -134,12 +151,16 @@ struct DecodeLaunch {
   const float* cart_lse;    // [S, Hkv, R]
   float* priv_part;         // [B, Hkv, chunks, G, d]
   float* priv_ml;           // [B, Hkv, chunks, G, 2]
+  int* counters;            // [B, Hkv] arrivals of private chunks (zeroed by prep)
   int chunk;                // private keys per CTA
+  int cart_tiles_per_split; // cartridge tiles per split CTA
 };
-// Rotated queries [B*G, Hkv, d] for the cartridge pass.
-cudaError_t launch_decode_prep(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
-// The private pass also rotates the queries and appends the new token's row.
-cudaError_t launch_decode_private(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
-cudaError_t launch_decode_combine(const DecodeLaunch& a, cudaStream_t st);
+// The whole decode step on one stream: prep (rotated queries for the
+// cartridge pass, counters := 0), the cartridge split pass (fwd kernel in
+// decode mode), then the private pass launched as its programmatic dependent
+// (it overlaps the cartridge pass; the last private CTA of every
+// (conversation, kv head) waits for the cartridge grid and combines).
+constexpr int kDecodeChunk = 128;  // private keys per CTA
+cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
 }  // namespace cart
