@@ -88,7 +88,6 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const 
 }
 
 constexpr int kPrivCH = kDecodeChunk;
-constexpr int kPrivBox = 32;
 constexpr int kPrivMT = kPrivCH / 64;  // m16 key tiles per warp
 
 // ------------------------------------------------------------- combine ----
@@ -181,8 +180,8 @@ __device__ __forceinline__ void combine_head_warp(const DecodeLaunch& a, int b, 
 // ------------------------------------------------------------- private ----
 // grid: (Hkv, chunks, B); block: 128 threads (4 warps).  Keys of the chunk:
 // private rows [c*CH, min((c+1)*CH, len+1)).
-//   * TMA stages the chunk's K and V rows in shared memory (128-byte
-//     swizzle, 32-row boxes, only as many boxes as the chunk has rows).
+//   * 16-byte cp.async copies stage the chunk's K and V rows in shared memory
+//     (128-byte swizzled layout, only the 16-row groups the chunk covers).
 //   * Meanwhile the block rotates the group's G queries at position p+len
 //     (one fp64-reduced cos/sin per frequency, shared through shared memory)
 //     straight into mma.sync B fragments (queries padded to 8 columns).
@@ -204,8 +203,7 @@ struct PrivSmem {
   static constexpr int kPStride = kPrivCH + 8;         // padded row: conflict-free B loads
   static constexpr int kCS = kP + 8 * kPStride * 2;    // float2 [D/2]
   static constexpr int kRed = kCS + (D / 2) * 8;       // f32 [2][4 warps][8]
-  static constexpr int kBar = kRed + 2 * 4 * 8 * 4;
-  static constexpr int kBytes = kBar + 16;
+  static constexpr int kBytes = kRed + 2 * 4 * 8 * 4;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -249,9 +247,8 @@ __device__ __forceinline__ float2 rope_cs(const RopeFreqs& f, int j, int pos) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(128) decode_private_kernel(
-    const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
-    DecodeLaunch a, const RopeFreqs f, float scale_log2, uint32_t* status) {
+__global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, const RopeFreqs f,
+                                                             float scale_log2) {
   using L = PrivSmem<D>;
   constexpr int CH = kPrivCH;
   constexpr int HALF = D / 2;
@@ -261,8 +258,6 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(smem + L::kP);
   float2* scs = reinterpret_cast<float2*>(smem + L::kCS);
   float* sred = reinterpret_cast<float*>(smem + L::kRed);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  __shared__ int abort_flag;
 
   // kv head fastest: the CTAs reading the interleaved head slices of the
   // same cache rows run together (DRAM row locality)
@@ -273,25 +268,30 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   const int kn = min(CH, Lb + 1 - k0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, tig = lane & 3;
-  const int nbox = (kn + kPrivBox - 1) / kPrivBox;
   const int pos = a.p + Lb;
   const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
 
-  if (tid == 0) {
-    abort_flag = 0;
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, 2u * nbox * (D / 64) * (kPrivBox * 128));
-    for (int j = 0; j < nbox; ++j)
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        const int off = h * L::kHalf + j * kPrivBox * 128;
-        tma_load_4d(smem + L::kK + off, &mK, bar, h * 64, g, k0 + j * kPrivBox, b);
-        tma_load_4d(smem + L::kV + off, &mV, bar, h * 64, g, k0 + j * kPrivBox, b);
-      }
+  // Stage the chunk's rows 0..16*ceil(kn/16) of K and V with 16-byte
+  // cp.async copies into the 128-byte-swizzled layout (rows >= kn of the last
+  // 16-row group are zero-filled, so P = 0 never meets stale data).
+  const int kgroups = (kn + 15) / 16;
+  {
+    constexpr int kPieces = D / 8;  // 16-byte pieces per row
+    const long long rstride = static_cast<long long>(a.Hkv) * D;
+    const __nv_bfloat16* kg = a.k_cache + (static_cast<long long>(b) * a.rows + k0) * rstride + g * D;
+    const __nv_bfloat16* vg = a.v_cache + (static_cast<long long>(b) * a.rows + k0) * rstride + g * D;
+    const uint32_t sKb = smem_u32(smem + L::kK), sVb = smem_u32(smem + L::kV);
+    for (int t = tid; t < kgroups * 16 * kPieces; t += 128) {
+      const int rr = t / kPieces, dc = t % kPieces;
+      const uint32_t so = tile_chunk(0, rr, dc);
+      const int src_bytes = rr < kn ? 16 : 0;
+      const long long go = static_cast<long long>(min(rr, kn - 1)) * rstride + dc * 8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sKb + so),
+                   "l"(kg + go), "r"(src_bytes) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sVb + so),
+                   "l"(vg + go), "r"(src_bytes) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
   if (tid < HALF) scs[tid] = rope_cs(f, tid, pos);
   __syncthreads();
@@ -337,9 +337,8 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
       bq[k][1] = pack_bf16x2(qv[k][2], qv[k][3]);
     }
   }
-  bool ok = mbar_wait(bar, 0, &abort_flag, status, kDevErrTimeoutTma);
-  ok = __syncthreads_and(ok);
-  if (!ok) return;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
 
   // ---- the new token: rotated key and value into the cache row len and
   // into this block's shared copy (its chunk holds that row)
@@ -366,15 +365,6 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
     }
     __syncthreads();
   }
-
-  // Rows >= kn of the chunk are never loaded (or hold rows past len): zero
-  // V over the rest of the last 16-key group so that P = 0 times V stays 0.
-  const int kgroups = (kn + 15) / 16;
-  for (int t = tid; t < (kgroups * 16 - kn) * (D / 8); t += 128) {
-    const int rr = kn + t / (D / 8), dc = t % (D / 8);
-    *reinterpret_cast<uint4*>(smem + L::kV + tile_chunk(0, rr, dc)) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();
 
   // ---- S^T = K Q^T for this warp's keys (MT m16 tiles)
   constexpr int MT = kPrivMT;
@@ -507,8 +497,8 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
 }
 
 template <int D, int G>
-cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, const CUtensorMap& mK,
-                              const CUtensorMap& mV, bool dependent, cudaStream_t st) {
+cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool dependent,
+                              cudaStream_t st) {
   using L = PrivSmem<D>;
   cudaError_t e = set_smem_once<decode_private_kernel<D, G>>(L::kAlloc);
   if (e != cudaSuccess) return e;
@@ -524,8 +514,7 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, const C
   cfg.numAttrs = dependent ? 1 : 0;
   const float scale_log2 = a.scale * 1.4426950408889634f;
   TraceScope tr("decode_private", st);
-  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, mK, mV, a, f, scale_log2,
-                            device_status_ptr());
+  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, a, f, scale_log2);
 }
 
 }  // namespace
@@ -568,24 +557,20 @@ cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_
     e = launch_fwd(l, st);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap mK, mV;
-  if (!make_bf16_rows_map(&mK, a.k_cache, a.B, a.rows, a.Hkv, a.d, kPrivBox) ||
-      !make_bf16_rows_map(&mV, a.v_cache, a.B, a.rows, a.Hkv, a.d, kPrivBox))
-    return cudaErrorInvalidValue;
   const bool dep = a.p > 0;
   if (a.d == 128) {
     switch (G) {
-      case 1: return launch_private_dg<128, 1>(a, f, mK, mV, dep, st);
-      case 2: return launch_private_dg<128, 2>(a, f, mK, mV, dep, st);
-      case 4: return launch_private_dg<128, 4>(a, f, mK, mV, dep, st);
-      case 8: return launch_private_dg<128, 8>(a, f, mK, mV, dep, st);
+      case 1: return launch_private_dg<128, 1>(a, f, dep, st);
+      case 2: return launch_private_dg<128, 2>(a, f, dep, st);
+      case 4: return launch_private_dg<128, 4>(a, f, dep, st);
+      case 8: return launch_private_dg<128, 8>(a, f, dep, st);
     }
   } else if (a.d == 64) {
     switch (G) {
-      case 1: return launch_private_dg<64, 1>(a, f, mK, mV, dep, st);
-      case 2: return launch_private_dg<64, 2>(a, f, mK, mV, dep, st);
-      case 4: return launch_private_dg<64, 4>(a, f, mK, mV, dep, st);
-      case 8: return launch_private_dg<64, 8>(a, f, mK, mV, dep, st);
+      case 1: return launch_private_dg<64, 1>(a, f, dep, st);
+      case 2: return launch_private_dg<64, 2>(a, f, dep, st);
+      case 4: return launch_private_dg<64, 4>(a, f, dep, st);
+      case 8: return launch_private_dg<64, 8>(a, f, dep, st);
     }
   }
   return cudaErrorInvalidValue;
