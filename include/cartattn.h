@@ -66,7 +66,7 @@ typedef enum cart_dtype { CART_BF16 = 0, CART_F32 = 1 } cart_dtype;
  *   d      head dimension, 64 or 128
  *   p      cartridge rows INCLUDING the frozen sink rows (p >= 0)
  *   frozen_prefix  leading cartridge rows whose gradient is exactly 0
- *   scale  softmax scale (normally 1/sqrt(d))
+ *   scale  softmax scale (normally 1/sqrt(d)); finite and > 0
  *   rope_theta     RoPE base (1e6 for the Qwen3 family)            */
 typedef struct cart_geom {
   int B, n, Hq, Hkv, d, p, frozen_prefix;

@@ -122,7 +122,8 @@ int check_geom(const cart_geom* g) {
   if (g->B < 1 || g->n < 1 || g->Hq < 1 || g->Hkv < 1 || g->Hq % g->Hkv != 0) return CART_ERR_GEOMETRY;
   if (g->d != 64 && g->d != 128) return CART_ERR_GEOMETRY;
   if (g->p < 0 || g->frozen_prefix < 0 || g->frozen_prefix > g->p) return CART_ERR_GEOMETRY;
-  if (!(std::isfinite(g->scale)) || !(g->rope_theta > 0.0) || !std::isfinite(g->rope_theta))
+  if (!(std::isfinite(g->scale)) || !(g->scale > 0.f) || !(g->rope_theta > 0.0) ||
+      !std::isfinite(g->rope_theta))
     return CART_ERR_GEOMETRY;
   if (g->B > 65535 || g->Hq > 65535 || (g->n + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
   return CART_OK;
@@ -172,7 +173,8 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
 // cartridge, and the TMA maps over them.
 struct TrainPrep {
   const float2* table;
-  const void* qr;
+  bool q_in_kernel;
+  const void* qr;  // rotated bf16 queries, or q itself when q_in_kernel
   const void* kr;
   const void* vb;
   const void* kcb;
@@ -180,15 +182,21 @@ struct TrainPrep {
   CUtensorMap mQ, mQ64, mK, mV, mKc, mVc;
 };
 
+// With q_in_kernel (bf16 queries only) Q is left unrotated: mQ maps q itself
+// and the forward kernel rotates each tile in shared memory.
 int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
                const void* v, const void* kc, const void* vc, uint8_t* ws, const TrainWs& w,
-               cudaStream_t st, TrainPrep* out) {
+               cudaStream_t st, TrainPrep* out, bool q_in_kernel = false) {
   const bool f32 = in == CART_F32;
+  if (f32) q_in_kernel = false;
   float2* table = reinterpret_cast<float2*>(ws + w.table);
   __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(ws + w.qr);
   __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(ws + w.kr);
   CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, make_rope_freqs(g->d, g->rope_theta), st));
-  CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, st));
+  if (q_in_kernel)
+    qr = static_cast<__nv_bfloat16*>(const_cast<void*>(q));
+  else
+    CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, st));
   CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, st));
   const void* vb = v;
   if (f32) {
@@ -208,6 +216,7 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
     vcb = tv;
   }
   out->table = table;
+  out->q_in_kernel = q_in_kernel;
   out->qr = qr;
   out->kr = kr;
   out->vb = vb;
@@ -309,7 +318,8 @@ int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TrainPrep tp;
-  rc = train_prep(g, in, cd, q, k, v, kc, vc, static_cast<uint8_t*>(workspace), w, st, &tp);
+  rc = train_prep(g, in, cd, q, k, v, kc, vc, static_cast<uint8_t*>(workspace), w, st, &tp,
+                  /*q_in_kernel=*/true);
   if (rc) return rc;
   FwdLaunch l{};
   l.mQ = &tp.mQ;
@@ -331,6 +341,8 @@ int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.out_f32 = in == CART_F32;
   l.lse = lse;
   l.decode = false;
+  l.rotate_q = tp.q_in_kernel;
+  l.table = tp.table;
   CART_CUDA(launch_fwd(l, st));
   return CART_OK;
 }
@@ -442,10 +454,10 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
   DecodeWs w;
   const int n_ct = (p + 127) / 128;
   const int R = B * (Hq / Hkv);
-  const int qtiles = (R + 127) / 128;
+  const int qpairs = ((R + 127) / 128 + 1) / 2;  // the cartridge pass takes two row tiles per CTA
   if (n_ct > 0) {
     // aim for about one CTA per SM for the cartridge part
-    const long long units = static_cast<long long>(n_ct) * Hkv * qtiles;
+    const long long units = static_cast<long long>(n_ct) * Hkv * qpairs;
     int per = static_cast<int>((units + 147) / 148);
     if (per < 1) per = 1;
     w.tiles_per_split = per;
@@ -474,7 +486,8 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return CART_ERR_GEOMETRY;
   if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
-  if (!std::isfinite(scale) || !(theta > 0.0) || !std::isfinite(theta)) return CART_ERR_GEOMETRY;
+  if (!std::isfinite(scale) || !(scale > 0.f) || !(theta > 0.0) || !std::isfinite(theta))
+    return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
   if ((rows + kDecodeChunk - 1) / kDecodeChunk > 256) return CART_ERR_GEOMETRY;  // <= 32768 rows
   return CART_OK;

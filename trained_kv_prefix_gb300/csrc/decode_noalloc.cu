@@ -50,9 +50,9 @@ NoallocLayout layout(int B, int Hq, int Hkv, int d, int p, int rows) {
   NoallocLayout w;
   const int n_ct = (p + 127) / 128;
   const int R = B * (Hq / Hkv);
-  const int qtiles = (R + 127) / 128;
+  const int qpairs = ((R + 127) / 128 + 1) / 2;  // the cartridge pass takes two row tiles per CTA
   if (n_ct > 0) {
-    const long long units = static_cast<long long>(n_ct) * Hkv * qtiles;
+    const long long units = static_cast<long long>(n_ct) * Hkv * qpairs;
     int per = static_cast<int>((units + 147) / 148);
     if (per < 1) per = 1;
     w.tiles_per_split = per;
@@ -114,7 +114,7 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return CART_ERR_GEOMETRY;
   if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
-  if (!std::isfinite(scale) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
+  if (!std::isfinite(scale) || !(scale > 0.f) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
     return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
   if ((cache_rows + kNoallocChunk - 1) / kNoallocChunk > 256) return CART_ERR_GEOMETRY;

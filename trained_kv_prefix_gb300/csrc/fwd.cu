@@ -1,25 +1,33 @@
 // fwd.cu -- tcgen05 forward of cartridge attention (sm_103a).
 //
-// One CTA owns a 128-row query tile of one (sequence, head) and walks the key
-// tiles of concat(cartridge rows, real tokens): first every cartridge tile
-// (all visible), then the real-token tiles up to the diagonal (end-aligned
-// causal mask: key j of the real part is visible from query i iff j <= i).
-// (Cartridges guide, "Semantics", attention bullet.)
+// One CTA owns two 128-row query tiles, A and B, that see the same keys:
+// consecutive row tiles of one (sequence, head) in training, the two halves
+// of a kv head's stacked decode rows in decode mode.  Both walk the key tiles
+// of concat(cartridge rows, real tokens) -- first every cartridge tile (all
+// visible), then the real-token tiles up to their diagonal (end-aligned
+// causal mask: real key j is visible from query i iff j <= i; Cartridges
+// guide, "Semantics", attention bullet) -- so every K/V tile is staged once
+// for both.  The two tiles are independent softmax streams: while one
+// warpgroup turns its S into P, the tensor pipe runs the other tile's
+// products, and the exp work of one tile overlaps the MMAs of the other.
 //
 // Roles (320 threads):
-//   warps 0-7  two softmax warpgroups.  Thread t of a group owns query row t
-//              (TMEM lane t); warpgroup w handles key columns [64w, 64w+64)
-//              of every 128-key tile.  The row maximum is exchanged between
-//              the two groups through shared memory; each keeps its own
-//              partial row sum and rescales its own half of O in TMEM when
-//              the maximum grows by more than 2^8 (lazy rescaling, log2
-//              domain).  P (bf16 pairs) is written back into TMEM over the
-//              group's own S columns.
-//   warp 8     TMA producer: Q tile once, then K/V tiles into a 2-stage ring.
-//   warp 9     MMA issuer (one thread): S = Q K^T into a double-buffered S
-//              (columns 0-127 / 128-255) and O += P V with P read from TMEM
-//              as the A operand (columns 256.. hold O).
-//
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B.  Thread t owns
+//              row t of its tile (TMEM lane t) and reads the whole 128-key S
+//              row, so row maxima and sums need no exchange.  O is rescaled
+//              in TMEM only when the running maximum grows by more than 2^8
+//              (lazy rescaling, log2 domain).  P (bf16 pairs) goes back into
+//              TMEM over the first 64 columns of the tile's S.
+//              With rotate_q the group first applies RoPE to its Q tile in
+//              shared memory (real-token queries at positions p + i).
+//   warp 8     TMA producer: both Q tiles once, then K and V tiles into two
+//              separate 2-stage rings.
+//   warp 9     MMA issuer (one thread).  Per key tile t:
+//                PV_A(t), S_A(t+1) = Q_A K(t+1)^T, PV_B(t), S_B(t+1).
+//              One CTA's MMAs run in issue order, so the commit that
+//              publishes S_X(t+1) also certifies that PV_X(t) has finished
+//              reading P_X(t) and writing O_X.
+// TMEM (512 columns): S_A 0-127, S_B 128-255, O_A at 256, O_B at 384.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,81 +39,131 @@ namespace cart {
 namespace {
 
 struct FwdParams {
-  int n_rows, Hq_map, G, p, n_real, cart_tiles_per_split, n_qtiles;
+  int n_rows, Hq_map, G, n_qblocks, p, n_real, cart_tiles_per_split, n_qtiles, n_pairs;
   float scale_log2;
   void* out;
   float* lse;
   int out_f32;
   int decode;
+  int rotate_q;
+  const float2* table;  // rotate_q: cos/sin rows for positions p .. p + n_rows - 1
   uint32_t* status;
 };
 
 constexpr int kFwdThreads = 320;
 
-// NS = K/V stages in shared memory: 2 for training; 1 in decode mode, where
-// the cartridge pass runs next to the private pass and leaves it room.
-template <int D, int NS>
+template <int D>
 struct FwdSmem {
-  static constexpr int kTileBytes = kTile * D * 2;      // one Q, K or V tile (bf16)
-  static constexpr int kStages = NS;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  // row maxima [2 tile buffers][2 groups][128] then row sums [2 groups][128], f32
-  static constexpr int kRed = kV + kStages * kTileBytes;
-  static constexpr int kBar = kRed + 3 * 256 * 4;
-  static constexpr int kBytes = kBar + 128;             // barriers + TMEM slot
-  static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-B alignment
+  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row Q, K or V tile (bf16)
+  static constexpr int kQ = 0;                      // Q_A, Q_B
+  static constexpr int kK = kQ + 2 * kTileBytes;    // K ring, 2 stages
+  static constexpr int kV = kK + 2 * kTileBytes;    // V ring, 2 stages
+  static constexpr int kBar = kV + 2 * kTileBytes;
+  static constexpr int kBytes = kBar + 256;         // barriers + TMEM slot
+  static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-B alignment
 };
 
-// kRedFull0/1: both softmax groups published a tile's row maxima; kLFull:
-// both published their row sums.  (mbarriers rather than a named barrier, so
-// that every wait stays bounded.)
-enum FwdBar { kQFull = 0, kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull0, kSFull1, kPFull0,
-              kPFull1, kODone, kRedFull0, kRedFull1, kLFull, kDrain, kNumBars };
+enum FwdBar {
+  kQFull = 0,  // TMA: both Q tiles landed
+  kQReady0,    // softmax group x: its Q tile is final (rotated if asked); 128 arrivals
+  kQReady1,
+  kKFull0,
+  kKFull1,
+  kKEmpty0,
+  kKEmpty1,
+  kVFull0,
+  kVFull1,
+  kVEmpty0,
+  kVEmpty1,
+  kSFull0,  // S of tile x is in TMEM (MMA commit)
+  kSFull1,
+  kPFull0,  // P of tile x is in TMEM (128 arrivals)
+  kPFull1,
+  kODone0,  // the last PV of tile x has completed
+  kODone1,
+  kDrain,
+  kNumBars
+};
+static_assert(kNumBars * 8 + 4 <= 256, "barrier area");
 
-template <int D, int NS>
+// RoPE of one Q row held in a 128-byte-swizzled tile, in place.  Rotate-half
+// pairs (c, c + D/2): for D = 128 chunk j of the first 64-wide block pairs
+// with chunk j of the second block; for D = 64 chunk j pairs with chunk j + 4.
+template <int D>
+__device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, const float2* tb) {
+#pragma unroll
+  for (int j = 0; j < D / 16; ++j) {
+    const uint32_t o0 = sw128_offset(row, j);
+    const uint32_t o1 = D == 128 ? 16384u + sw128_offset(row, j) : sw128_offset(row, j + 4);
+    const uint4 a = *reinterpret_cast<const uint4*>(sQ + o0);
+    const uint4 b = *reinterpret_cast<const uint4*>(sQ + o1);
+    const uint32_t pa[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t pb[4] = {b.x, b.y, b.z, b.w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = bf16x2_to_float2(pa[e]);
+      const float2 fb = bf16x2_to_float2(pb[e]);
+      const float2 c0 = __ldg(tb + 8 * j + 2 * e);
+      const float2 c1 = __ldg(tb + 8 * j + 2 * e + 1);
+      float y0a, y1a, y0b, y1b;
+      rope_pair(fa.x, fb.x, c0, y0a, y1a);
+      rope_pair(fa.y, fb.y, c1, y0b, y1b);
+      ya[e] = pack_bf16x2(y0a, y0b);
+      yb[e] = pack_bf16x2(y1a, y1b);
+    }
+    *reinterpret_cast<uint4*>(sQ + o0) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(sQ + o1) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+  }
+}
+
+template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const FwdParams a) {
-  using L = FwdSmem<D, NS>;
+  using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kNumBars * 8);
-  float* red = reinterpret_cast<float*>(smem + L::kRed);
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item ----
-  int head, qb, qt, kvh, split;
+  // ---- work item (training: heaviest pairs first) ----
+  int head, qb, pair, kvh, split;
   if (!a.decode) {
-    head = blockIdx.x;
-    qb = blockIdx.y;
-    qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);  // heaviest tiles first
+    const int hb = a.Hq_map * a.n_qblocks;
+    pair = a.n_pairs - 1 - static_cast<int>(blockIdx.x) / hb;
+    const int rem = static_cast<int>(blockIdx.x) % hb;
+    head = rem % a.Hq_map;
+    qb = rem / a.Hq_map;
     kvh = head / a.G;
     split = 0;
   } else {
     head = blockIdx.x;
     qb = 0;
-    qt = blockIdx.y;
+    pair = blockIdx.y;
     kvh = head;
     split = blockIdx.z;
   }
-  const int q0 = qt * kTile;
+  const bool hasB = 2 * pair + 1 < a.n_qtiles;
   const int n_ct_all = (a.p + kTile - 1) / kTile;
-  int ct_lo = 0, ct_hi = n_ct_all, n_rt = 0;
+  int ct_lo = 0, ct_hi = n_ct_all, n_rt_A = 0, n_rt_B = 0;
   if (a.decode) {
     ct_lo = split * a.cart_tiles_per_split;
     ct_hi = min(ct_lo + a.cart_tiles_per_split, n_ct_all);
   } else {
-    n_rt = min(qt + 1, (a.n_real + kTile - 1) / kTile);
+    const int n_real_tiles = (a.n_real + kTile - 1) / kTile;
+    n_rt_A = min(2 * pair + 1, n_real_tiles);
+    n_rt_B = hasB ? min(2 * pair + 2, n_real_tiles) : 0;
   }
   const int n_ct = max(ct_hi - ct_lo, 0);
-  const int T = n_ct + n_rt;
+  const int T_A = n_ct + n_rt_A;
+  const int T_B = hasB ? n_ct + n_rt_B : 0;
+  const int T = max(T_A, T_B);
 
   if (threadIdx.x == 0) {
     // decode mode: let the dependent private pass start right away (it only
@@ -114,14 +172,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[kKVFull0 + s], 1);
-      mbar_init(&bars[kKVEmpty0 + s], 1);
+      mbar_init(&bars[kQReady0 + s], 128);
+      mbar_init(&bars[kKFull0 + s], 1);
+      mbar_init(&bars[kKEmpty0 + s], 1);
+      mbar_init(&bars[kVFull0 + s], 1);
+      mbar_init(&bars[kVEmpty0 + s], 1);
       mbar_init(&bars[kSFull0 + s], 1);
-      mbar_init(&bars[kPFull0 + s], 256);
-      mbar_init(&bars[kRedFull0 + s], 256);
+      mbar_init(&bars[kPFull0 + s], 128);
+      mbar_init(&bars[kODone0 + s], 1);
     }
-    mbar_init(&bars[kLFull], 256);
-    mbar_init(&bars[kODone], 1);
     mbar_init(&bars[kDrain], 1);
     fence_mbar_init();
   }
@@ -133,10 +192,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem;        // S buffers at columns 0 and 128
-  const uint32_t tO = tmem + 256;
   volatile int* abort_p = &abort_flag;
-  uint8_t* sQ = smem + L::kQ;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
@@ -146,46 +202,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mVc);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
-      mbar_arrive_expect_tx(&bars[kQFull], L::kTileBytes);
+      const int q0A = 2 * pair * kTile;
+      mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h)
-        tma_load_4d(sQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, q0, qb);
-      int issued = 0;
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, q0A, qb);
+        // tile B of a lone last tile reads rows past the end: zero fill
+        tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, head,
+                    q0A + kTile, qb);
+      }
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int t = 0; t < T; ++t) {
-        const int s = t % NS;
-        if (t >= NS) {
-          ok = mbar_wait(&bars[kKVEmpty0 + s], ((t / NS) - 1) & 1, abort_p, a.status,
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t & 1;
+        const bool cart = t < n_ct;
+        const int row0 = cart ? (ct_lo + t) * kTile : (t - n_ct) * kTile;
+        const CUtensorMap* mk = cart ? &mKc : &mK;
+        const CUtensorMap* mv = cart ? &mVc : &mV;
+        const int blk = cart ? 0 : qb;
+        if (t >= 2) {
+          ok = mbar_wait(&bars[kKEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
         uint8_t* sK = smem + L::kK + s * L::kTileBytes;
-        uint8_t* sV = smem + L::kV + s * L::kTileBytes;
-        mbar_arrive_expect_tx(&bars[kKVFull0 + s], 2 * L::kTileBytes);
-        if (t < n_ct) {
-          const int row0 = (ct_lo + t) * kTile;
+        mbar_arrive_expect_tx(&bars[kKFull0 + s], L::kTileBytes);
 #pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            tma_load_4d(sK + h * 16384, &mKc, &bars[kKVFull0 + s], h * 64, kvh, row0, 0);
-            tma_load_4d(sV + h * 16384, &mVc, &bars[kKVFull0 + s], h * 64, kvh, row0, 0);
-          }
-        } else {
-          const int row0 = (t - n_ct) * kTile;
-#pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            tma_load_4d(sK + h * 16384, &mK, &bars[kKVFull0 + s], h * 64, kvh, row0, qb);
-            tma_load_4d(sV + h * 16384, &mV, &bars[kKVFull0 + s], h * 64, kvh, row0, qb);
-          }
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_4d(sK + h * 16384, mk, &bars[kKFull0 + s], h * 64, kvh, row0, blk);
+        k_issued = t + 1;
+        if (t >= 2) {
+          ok = mbar_wait(&bars[kVEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutTma);
+          if (!ok) break;
         }
-        issued = t + 1;
+        uint8_t* sV = smem + L::kV + s * L::kTileBytes;
+        mbar_arrive_expect_tx(&bars[kVFull0 + s], L::kTileBytes);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_4d(sV + h * 16384, mv, &bars[kVFull0 + s], h * 64, kvh, row0, blk);
+        v_issued = t + 1;
       }
       if (!ok) {
         // Give the copies already in flight a bounded chance to land before
         // the CTA releases its shared memory.
         int dummy = 0;
         mbar_wait(&bars[kQFull], 0, &dummy, nullptr, 0);
-        for (int t = max(issued - NS, 0); t < issued; ++t)
-          mbar_wait(&bars[kKVFull0 + t % NS], (t / NS) & 1, &dummy, nullptr, 0);
+        for (int t = max(k_issued - 2, 0); t < k_issued; ++t)
+          mbar_wait(&bars[kKFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
+        for (int t = max(v_issued - 2, 0); t < v_issued; ++t)
+          mbar_wait(&bars[kVFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
       }
     }
     __syncwarp();
@@ -194,64 +260,81 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0 && T > 0) {
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idPV = idesc_bf16(128, D, false, true);
-      // Base descriptors, computed once; each MMA adds a compile-time offset.
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
-      const uint64_t dKs0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);
-      const uint64_t dVs0 = sdesc_sw128(smem_u32(smem + L::kV), 16384u, 1024u);
-      const uint64_t dKs1 = desc_add(dKs0, L::kTileBytes);
-      const uint64_t dVs1 = desc_add(dVs0, L::kTileBytes);
-      bool ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutMma);
-      // O += P V for tile t: P from TMEM buffer t&1 (K step k of 16 keys at
-      // column (k/4)*64 + (k%4)*8: warpgroup w packed keys 64w.. at 64w),
-      // V MN-major (16 rows = 2048 B per K step).
-      auto issue_pv = [&](int t) {
-        const int sp = t % NS;           // smem stage of V
-        const uint64_t dv = sp ? dVs1 : dVs0;
-        const uint32_t tp = tS0 + (t & 1) * 128;  // TMEM buffer holding P
-        umma_bf16_ts(tO, tp, dv, idPV, t > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(tO, tp + (k >> 2) * 64 + (k & 3) * 8, desc_add(dv, k * 2048), idPV, 1u);
-        umma_commit(&bars[kODone]);
-        umma_commit(&bars[kKVEmpty0 + sp]);
-      };
-      for (int t = 0; t < T && ok; ++t) {
-        const int ks = t % NS, s = t & 1;
-        ok = mbar_wait(&bars[kKVFull0 + ks], (t / NS) & 1, abort_p, a.status, kDevErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
-        // S buffer s last held P of tile t-2, read by the PV MMA issued
-        // before this point (one CTA's MMAs run in issue order).
-        const uint64_t dk = ks ? dKs1 : dKs0;
-        const uint32_t ts = tS0 + s * 128;
-        umma_bf16_ss(ts, dQ0, dk, idS, 0u);
+      // Base descriptors, computed once; each MMA adds an offset.
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + L::kQ), 16u, 1024u);
+      const uint64_t dQ1 = desc_add(dQ0, L::kTileBytes);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);
+      const uint64_t dK1 = desc_add(dK0, L::kTileBytes);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + L::kV), 16384u, 1024u);
+      const uint64_t dV1 = desc_add(dV0, L::kTileBytes);
+      // S_x = Q_x K(t)^T (K-major operands; K step k of 16 at byte offset
+      // (k/4)*16384 + (k%4)*32 within the two 64-wide blocks)
+      auto issue_qk = [&](int x, int t) {
+        const uint64_t dq = x ? dQ1 : dQ0;
+        const uint64_t dk = (t & 1) ? dK1 : dK0;
+        const uint32_t ts = tmem + x * 128;
+        umma_bf16_ss(ts, dq, dk, idS, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss(ts, desc_add(dQ0, off), desc_add(dk, off), idS, 1u);
+          umma_bf16_ss(ts, desc_add(dq, off), desc_add(dk, off), idS, 1u);
         }
-        umma_commit(&bars[kSFull0 + s]);
-        if constexpr (NS == 1) {
-          // one K/V slot: PV(t) must free it before tile t+1 can load
-          ok = mbar_wait(&bars[kPFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        umma_commit(&bars[kSFull0 + x]);
+      };
+      // O_x += P_x V(t): P from TMEM (K step k of 16 keys = 8 packed columns
+      // at 8k), V MN-major (16 rows = 2048 B per K step).
+      auto issue_pv = [&](int x, int t) {
+        const uint64_t dv = (t & 1) ? dV1 : dV0;
+        const uint32_t tp = tmem + x * 128;
+        const uint32_t to = tmem + 256 + x * 128;
+        umma_bf16_ts(to, tp, dv, idPV, t > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ts(to, tp + k * 8, desc_add(dv, k * 2048), idPV, 1u);
+      };
+      bool ok = mbar_wait(&bars[kQReady0], 0, abort_p, a.status, kDevErrTimeoutMma) &&
+                mbar_wait(&bars[kKFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+      }
+      if (ok && hasB) {
+        ok = mbar_wait(&bars[kQReady1], 0, abort_p, a.status, kDevErrTimeoutMma);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(1, 0);
+        }
+      }
+      if (ok) umma_commit(&bars[kKEmpty0]);
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t & 1;
+        ok = mbar_wait(&bars[kVFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        if (!ok) break;
+        const bool next = t + 1 < T;
+        if (t < T_A) {
+          ok = mbar_wait(&bars[kPFull0], t & 1, abort_p, a.status, kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t);
-        } else if (t > 0) {
-          ok = mbar_wait(&bars[kPFull0 + (s ^ 1)], ((t - 1) >> 1) & 1, abort_p, a.status,
+          issue_pv(0, t);
+          if (t == T_A - 1) umma_commit(&bars[kODone0]);
+        }
+        if (next) {
+          ok = mbar_wait(&bars[kKFull0 + (s ^ 1)], ((t + 1) >> 1) & 1, abort_p, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t - 1);
+          if (t + 1 < T_A) issue_qk(0, t + 1);
         }
-      }
-      if (NS > 1 && ok) {
-        ok = mbar_wait(&bars[kPFull0 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, abort_p, a.status,
-                       kDevErrTimeoutMma);
-        if (ok) {
+        if (t < T_B) {
+          ok = mbar_wait(&bars[kPFull1], t & 1, abort_p, a.status, kDevErrTimeoutMma);
+          if (!ok) break;
           tc_fence_after();
-          issue_pv(T - 1);
+          issue_pv(1, t);
+          if (t == T_B - 1) umma_commit(&bars[kODone1]);
+          if (t + 1 < T_B) issue_qk(1, t + 1);
         }
+        umma_commit(&bars[kVEmpty0 + s]);
+        if (next) umma_commit(&bars[kKEmpty0 + (s ^ 1)]);
       }
       // Drain: every MMA issued above completes before the CTA tears down.
       umma_commit(&bars[kDrain]);
@@ -261,65 +344,65 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax --
-    const int wg = warp >> 2;
+    const int x = warp >> 2;  // 0: tile A, 1: tile B
+    const int Tx = x ? T_B : T_A;
     const int row = threadIdx.x & 127;  // == TMEM lane
-    const int i = q0 + row;             // query row within its block
+    const int i = (2 * pair + x) * kTile + row;  // query row within its block
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + x * 128 + lane_off;
     float m = -INFINITY, l = 0.f;
-    bool ok = T > 0;
-    for (int t = 0; t < T && ok; ++t) {
-      const int x = t & 1;
-      ok = mbar_wait(&bars[kSFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+    bool ok = Tx > 0;
+    if (ok) {
+      if (a.rotate_q) {
+        ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && i < a.n_rows)
+          rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
+                          a.table + static_cast<long long>(i) * (D / 2));
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kQReady0 + x]);
+      } else {
+        // the MMA thread waits on kQReady only: forward the TMA completion
+        ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        mbar_arrive(&bars[kQReady0 + x]);
+      }
+    }
+    const int i_cap = min(i, a.n_real - 1);
+    for (int t = 0; t < Tx && ok; ++t) {
+      ok = mbar_wait(&bars[kSFull0 + x], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t ts = tS0 + x * 128 + wg * 64 + lane_off;
-      uint32_t r0[32], r1[32];
-      tmem_ld32(ts, r0);
-      tmem_ld32(ts + 32, r1);
+      uint32_t r[4][32];
+      tmem_ld32(tS, r[0]);
+      tmem_ld32(tS + 32, r[1]);
+      tmem_ld32(tS + 64, r[2]);
+      tmem_ld32(tS + 96, r[3]);
       tmem_ld_wait();
-      tmem_reg_fence(r0);
-      tmem_reg_fence(r1);
-      // number of visible columns of this group's 64 (leading columns)
-      int valid;
-      if (t < n_ct) {
-        valid = a.p - (ct_lo + t) * kTile - wg * 64;
-      } else {
-        const int col0 = (t - n_ct) * kTile + wg * 64;
-        valid = min(i, a.n_real - 1) - col0 + 1;
-      }
-      valid = max(0, min(valid, 64));
-      float s[64];
+      tmem_reg_fence(r[0]);
+      tmem_reg_fence(r[1]);
+      tmem_reg_fence(r[2]);
+      tmem_reg_fence(r[3]);
+      // number of visible keys of this tile (leading columns)
+      int valid = t < n_ct ? a.p - (ct_lo + t) * kTile : i_cap - (t - n_ct) * kTile + 1;
+      valid = max(0, min(valid, kTile));
+      if (__any_sync(0xffffffffu, valid < kTile)) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(r0[c]) * a.scale_log2;
-        s[32 + c] = __uint_as_float(r1[c]) * a.scale_log2;
+        for (int c = 0; c < kTile; ++c)
+          if (c >= valid) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      if (__any_sync(0xffffffffu, valid < 64)) {
+      // row maximum of the raw scores (scale_log2 > 0), 4 independent chains
+      float mx[4];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = c < valid ? s[c] : -INFINITY;
-      }
-      // row maximum of this group's columns (4 independent chains), then of
-      // the whole tile through shared memory
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      for (int q = 0; q < 4; ++q) {
+        float v = __uint_as_float(r[q][0]);
 #pragma unroll
-      for (int c = 4; c < 64; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 1; c < 32; ++c) v = fmaxf(v, __uint_as_float(r[q][c]));
+        mx[q] = v;
       }
-      float rmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      // Slot reuse is safe: the other group read this buffer two tiles ago,
-      // before it arrived on the other buffer's barrier, which this group has
-      // waited for since.
-      float* redt = red + x * 256;
-      redt[wg * 128 + row] = rmax;
-      mbar_arrive(&bars[kRedFull0 + x]);
-      ok = mbar_wait(&bars[kRedFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      rmax = fmaxf(rmax, redt[(wg ^ 1) * 128 + row]);
+      const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
       // Lazy rescaling: keep the stale max unless the new one exceeds it by
       // more than 8 (P values then stay below 2^8, safe in bf16 / f32).
       float alpha = 1.f;
@@ -329,37 +412,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m = rmax;
         rescale = t > 0;
       }
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pk[32];
+      const float neg_m = -m;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = exp2_approx(s[2 * c] - m);
-        const float p1 = exp2_approx(s[2 * c + 1] - m);
-        rs0 += p0;
-        rs1 += p1;
-        pk[c] = pack_bf16x2(p0, p1);
+      for (int q = 0; q < 4; q += 2) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = exp2_approx(fmaf(__uint_as_float(r[q][2 * c]), a.scale_log2, neg_m));
+          const float p1 =
+              exp2_approx(fmaf(__uint_as_float(r[q][2 * c + 1]), a.scale_log2, neg_m));
+          const float p2 =
+              exp2_approx(fmaf(__uint_as_float(r[q + 1][2 * c]), a.scale_log2, neg_m));
+          const float p3 =
+              exp2_approx(fmaf(__uint_as_float(r[q + 1][2 * c + 1]), a.scale_log2, neg_m));
+          rs[q] += p0;
+          rs[q + 1] += p1;
+          rs[(q + 2) & 3] += p2;
+          rs[(q + 3) & 3] += p3;
+          pk[c] = pack_bf16x2(p0, p1);
+          pk[16 + c] = pack_bf16x2(p2, p3);
+        }
+        // keys 32q .. 32q + 63 -> packed columns 16q .. 16q + 31
+        tmem_st32(tS + 16 * q, pk);
       }
-      // P over the first 32 columns of this group's S half (already read)
-      tmem_st32(ts, pk);
-      l = l * alpha + (rs0 + rs1);
-      if (t > 0) {
-        ok = mbar_wait(&bars[kODone], (t - 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-          // this group's half of the O columns
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      if (__any_sync(0xffffffffu, rescale)) {
+        // PV(t-1) has completed: the commit that published S(t) follows it.
 #pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk) {
-            uint32_t o[32];
-            const uint32_t addr = tO + lane_off + wg * (D / 2) + blk * 32;
-            tmem_ld32(addr, o);
-            tmem_ld_wait();
-            tmem_reg_fence(o);
+        for (int blk = 0; blk < D / 32; ++blk) {
+          uint32_t o[32];
+          tmem_ld32(tO + blk * 32, o);
+          tmem_ld_wait();
+          tmem_reg_fence(o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(addr, o);
-          }
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(tO + blk * 32, o);
         }
       }
       tmem_st_wait();
@@ -368,27 +456,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     // ------------------------------------------------------------ epilogue --
     if (ok) {
-      ok = mbar_wait(&bars[kODone], (T - 1) & 1, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = mbar_wait(&bars[kODone0 + x], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
-    }
-    // combine the two groups' row sums (own smem slots, own barrier)
-    float l_all = l;
-    if (ok) {
-      red[512 + wg * 128 + row] = l;
-      mbar_arrive(&bars[kLFull]);
-      ok = mbar_wait(&bars[kLFull], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) l_all = l + red[512 + (wg ^ 1) * 128 + row];
     }
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l_all;
+      const float inv_l = 1.f / l;
       const bool row_ok = i < a.n_rows;
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk) {
+      for (int blk = 0; blk < D / 32; ++blk) {
         uint32_t o[32];
-        const int col = wg * (D / 2) + blk * 32;
-        tmem_ld32(tO + lane_off + col, o);
+        const int col = blk * 32;
+        tmem_ld32(tO + col, o);
         tmem_ld_wait();
         tmem_reg_fence(o);
         if (row_ok) {
@@ -421,8 +500,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (row_ok && wg == 0) {
-        const float lse2 = m + __log2f(l_all);
+      if (row_ok) {
+        const float lse2 = m + __log2f(l);
         if (a.decode)
           a.lse[(static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i] = lse2;
         else
@@ -438,46 +517,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-template <int D, int NS>
+template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
-  using L = FwdSmem<D, NS>;
+  using L = FwdSmem<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  cudaError_t e = set_smem_once<fwd_kernel<D, NS>>(L::kAlloc);
+  cudaError_t e = set_smem_once<fwd_kernel<D>>(L::kAlloc);
   if (e != cudaSuccess) return e;
   FwdParams p{};
   p.n_rows = a.n_rows;
   p.Hq_map = a.Hq_map;
   p.G = a.G;
+  p.n_qblocks = a.n_qblocks;
   p.p = a.p;
   p.n_real = a.n_real;
   p.cart_tiles_per_split = a.cart_tiles_per_split;
   p.n_qtiles = (a.n_rows + kTile - 1) / kTile;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
   p.scale_log2 = a.scale_log2;
   p.out = a.out;
   p.lse = a.lse;
   p.out_f32 = a.out_f32 ? 1 : 0;
   p.decode = a.decode ? 1 : 0;
+  p.rotate_q = a.rotate_q ? 1 : 0;
+  p.table = a.table;
   p.status = device_status_ptr();
   dim3 grid;
   if (!a.decode)
-    grid = dim3(a.Hq_map, a.n_qblocks, p.n_qtiles);
+    grid = dim3(static_cast<unsigned>(p.n_pairs) * a.Hq_map * a.n_qblocks, 1, 1);
   else
-    grid = dim3(a.Hq_map, p.n_qtiles, a.n_splits);
+    grid = dim3(a.Hq_map, p.n_pairs, a.n_splits);
   TraceScope tr(a.decode ? "decode_cartridge" : "fwd", st);
-  fwd_kernel<D, NS><<<grid, kFwdThreads, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
+  fwd_kernel<D><<<grid, kFwdThreads, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
-  if (a.decode) {
-    if (a.d == 128) return launch_fwd_d<128, 1>(a, st);
-    if (a.d == 64) return launch_fwd_d<64, 1>(a, st);
-  } else {
-    if (a.d == 128) return launch_fwd_d<128, 2>(a, st);
-    if (a.d == 64) return launch_fwd_d<64, 2>(a, st);
-  }
+  if (a.rotate_q && (a.decode || !a.table)) return cudaErrorInvalidValue;
+  if (a.d == 128) return launch_fwd_d<128>(a, st);
+  if (a.d == 64) return launch_fwd_d<64>(a, st);
   return cudaErrorInvalidValue;
 }
 

@@ -99,7 +99,12 @@ struct FwdLaunch {
   bool out_f32;
   float* lse;              // training: [B, Hq, n]; decode: [S, Hkv, R]
   bool decode;
+  bool rotate_q;           // training: mQ holds unrotated bf16 queries; the kernel
+                           // applies RoPE in shared memory using `table`
+  const float2* table;     // rope table for positions p .. p+n-1 (rotate_q)
 };
+// Two 128-row query tiles per CTA (training: consecutive row tiles of one
+// (sequence, head); decode: rows 0-127 / 128-255 of a kv head's stacked rows).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 
 // ------------------------------------------------------------ backward ----

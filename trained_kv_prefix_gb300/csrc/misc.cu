@@ -123,9 +123,7 @@ __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __r
       const float2* tb = table + static_cast<long long>(i) * half + j0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float2 cs = __ldg(tb + e);
-        y0[e] = x0[e] * cs.x - x1[e] * cs.y;
-        y1[e] = x1[e] * cs.x + x0[e] * cs.y;
+        rope_pair(x0[e], x1[e], __ldg(tb + e), y0[e], y1[e]);
       }
     } else {
 #pragma unroll

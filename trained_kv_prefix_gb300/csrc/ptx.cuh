@@ -293,6 +293,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// One rotate-half RoPE pair (x0 at index j, x1 at j + d/2) by the angle whose
+// (cos, sin) is cs, with the rounding pinned (no contraction choices left to
+// the compiler) so that every kernel that rotates gets the same bits.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float2 cs, float& y0, float& y1) {
+  y0 = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y));
+  y1 = __fadd_rn(__fmul_rn(x1, cs.x), __fmul_rn(x0, cs.y));
+}
+
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
