@@ -135,7 +135,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspace carving shared by the size query and the call.
 struct TrainWs {
-  size_t table = 0, qr = 0, kr = 0, vb = 0, kcb = 0, vcb = 0, dob = 0, dvec = 0, total = 0;
+  size_t table = 0, qr = 0, kr = 0, vb = 0, kcb = 0, vcb = 0, dob = 0, dvec = 0, lse2 = 0,
+         total = 0;
+  int npad = 0;
 };
 
 TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
@@ -158,7 +160,9 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
   w.vcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
   if (bwd) {
     w.dob = (in == CART_F32) ? take(rows_q * e16) : SIZE_MAX;
-    w.dvec = take(static_cast<size_t>(g->B) * g->Hq * g->n * sizeof(float));
+    w.npad = (g->n + 127) / 128 * 128;
+    w.dvec = take(static_cast<size_t>(g->B) * g->Hq * w.npad * sizeof(float));
+    w.lse2 = take(static_cast<size_t>(g->B) * g->Hq * w.npad * sizeof(float));
   }
   w.total = off;
   return w;
@@ -380,7 +384,8 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
     dob = t;
   }
   float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
-  CART_CUDA(launch_bwd_dot(o, dout, f32, Dvec, g->B, g->n, g->Hq, g->d, st));
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
   CUtensorMap mdO, mdO64, mK96, mV96, mKc96, mVc96;
   if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128) ||
       !make_rows_map(&mdO64, dob, g->B, g->n, g->Hq, g->d, 64) ||
@@ -416,8 +421,9 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.p = g->p;
   l.frozen_prefix = g->frozen_prefix;
   l.scale = g->scale;
-  l.lse = lse;
+  l.lse2 = lse2;
   l.Dvec = Dvec;
+  l.npad = w.npad;
   l.dq = dq;
   l.dk = dk;
   l.dv = dv;

@@ -39,8 +39,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdParams {
   int B, n, Hq, Hkv, G, p, frozen_prefix, nq64, n_ct, n_rt, n_qtiles;
   float scale, scale_log2;
-  const float* lse;
-  const float* Dvec;
+  const float* lse2;  // [B, Hq, npad] log2-domain lse (+inf past n)
+  const float* Dvec;  // [B, Hq, npad] (0 past n)
+  int npad;
   void* dq;
   void* dk;
   void* dv;
@@ -80,9 +81,11 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 // dV accumulates at 256, dK at 384.
 constexpr int kDkdvThreads = 320;
 
+constexpr int kDkdvStages = 4;
+
 template <int D>
 struct DkdvSmem {
-  static constexpr int kStages = 3;
+  static constexpr int kStages = kDkdvStages;
   static constexpr int kKV = kTile * D * 2;        // resident K or V tile
   static constexpr int kQT = 64 * D * 2;           // 64-row Q or dO tile
   static constexpr int kK = 0;
@@ -94,7 +97,8 @@ struct DkdvSmem {
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-enum DkdvBar { kResFull = 0, kQdoFull0, kQdoEmpty0 = kQdoFull0 + 3, kStFull0 = kQdoEmpty0 + 3,
+enum DkdvBar { kResFull = 0, kQdoFull0, kQdoEmpty0 = kQdoFull0 + kDkdvStages,
+               kStFull0 = kQdoEmpty0 + kDkdvStages,
                kDsFull0 = kStFull0 + 2, kAccDone = kDsFull0 + 2, kDkdvDrain, kDkdvBars };
 
 struct DkdvItem {
@@ -172,7 +176,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     abort_flag = 0;
     mbar_init(&bars[kResFull], 1);
     for (int s = 0; s < S; ++s) {
-      mbar_init(&bars[kQdoFull0 + s], 32);
+      mbar_init(&bars[kQdoFull0 + s], 1);
       mbar_init(&bars[kQdoEmpty0 + s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -199,8 +203,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
-    bool ok = U > 0;
-    if (ok && lane == 0) {
+    // One lane: per step the Q and dO tiles (TMA) and the step's 64 entries
+    // of lse2 and D (plain bulk copies from the padded row vectors), all
+    // completing on the stage's full barrier.
+    if (lane == 0 && U > 0) {
       tma_prefetch_desc(&mQ64);
       tma_prefetch_desc(&mdO64);
       mbar_arrive_expect_tx(&bars[kResFull], 2 * L::kKV);
@@ -214,53 +220,38 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           tma_load_4d(sV + h * 16384, &mV, &bars[kResFull], h * 64, g, tile * kTile, b_real);
         }
       }
-    }
-    int issued = 0;
-    for (int u = 0; u < U && ok; ++u) {
-      const int s = u % S;
-      if (u >= S) {
-        ok = mbar_wait(&bars[kQdoEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
-                       kDevErrTimeoutTma);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
-      const int h = g * a.G + it.hh;
-      float* lse2 = vec + s * 128;
-      float* dvv = lse2 + 64;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int c = lane + 32 * r;
-        const int q = it.qt * 64 + c;
-        float l2 = INFINITY, dd = 0.f;
-        if (q < a.n) {
-          const long long idx = (static_cast<long long>(it.b) * a.Hq + h) * a.n + q;
-          l2 = __ldg(a.lse + idx) * kLog2e;
-          dd = __ldg(a.Dvec + idx);
+      int issued = 0;
+      bool ok = true;
+      for (int u = 0; u < U; ++u) {
+        const int s = u % S;
+        if (u >= S) {
+          ok = mbar_wait(&bars[kQdoEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutTma);
+          if (!ok) break;
         }
-        lse2[c] = l2;
-        dvv[c] = dd;
-      }
-      if (lane == 0) {
+        const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
+        const int h = g * a.G + it.hh;
         uint8_t* sQ = smem + L::kStage0 + s * 2 * L::kQT;
         uint8_t* sdO = sQ + L::kQT;
-        mbar_arrive_expect_tx(&bars[kQdoFull0 + s], 2 * L::kQT);
+        float* v = vec + s * 128;
+        const long long vo = (static_cast<long long>(it.b) * a.Hq + h) * a.npad + it.qt * 64;
+        mbar_arrive_expect_tx(&bars[kQdoFull0 + s], 2 * L::kQT + 512);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc) {
           tma_load_4d(sQ + hc * 8192, &mQ64, &bars[kQdoFull0 + s], hc * 64, h, it.qt * 64, it.b);
           tma_load_4d(sdO + hc * 8192, &mdO64, &bars[kQdoFull0 + s], hc * 64, h, it.qt * 64,
                       it.b);
         }
-      } else {
-        mbar_arrive(&bars[kQdoFull0 + s]);
+        bulk_load(v, a.lse2 + vo, 256, &bars[kQdoFull0 + s]);
+        bulk_load(v + 64, a.Dvec + vo, 256, &bars[kQdoFull0 + s]);
+        issued = u + 1;
       }
-      issued = u + 1;
-    }
-    if (!ok && lane == 0 && U > 0) {
-      int dummy = 0;
-      mbar_wait(&bars[kResFull], 0, &dummy, nullptr, 0);
-      for (int u = max(issued - S, 0); u < issued; ++u)
-        mbar_wait(&bars[kQdoFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
+      if (!ok) {
+        int dummy = 0;
+        mbar_wait(&bars[kResFull], 0, &dummy, nullptr, 0);
+        for (int u = max(issued - S, 0); u < issued; ++u)
+          mbar_wait(&bars[kQdoFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
+      }
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -346,8 +337,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int s = u % S, x = u & 1;
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
       ok = mbar_wait(&bars[kStFull0 + x], (u >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-      // acquire the lse / D vectors the producer lanes published with
-      // kQdoFull (already complete: the MMAs behind kStFull waited for it)
+      // the stage's lse2 / D vectors landed with kQdoFull (already complete:
+      // the MMAs behind kStFull waited for it); waiting makes them visible
       if (ok) ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status,
                              kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
@@ -645,12 +636,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row = threadIdx.x & 127;
     const int i = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float lse2 = INFINITY, Di = 0.f;
-    if (i < a.n) {
-      const long long idx = (static_cast<long long>(b) * a.Hq + h) * a.n + i;
-      lse2 = __ldg(a.lse + idx) * kLog2e;
-      Di = __ldg(a.Dvec + idx);
-    }
+    // padded vectors: rows past n read lse2 = +inf (P = 0) and D = 0
+    const long long vidx = (static_cast<long long>(b) * a.Hq + h) * a.npad + i;
+    const float lse2 = __ldg(a.lse2 + vidx);
+    const float Di = __ldg(a.Dvec + vidx);
     constexpr int NH = NK / 2;  // keys per warpgroup and step
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
@@ -776,8 +765,9 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.n_qtiles = p.n_rt;
   p.scale = l.scale;
   p.scale_log2 = l.scale * kLog2e;
-  p.lse = l.lse;
+  p.lse2 = l.lse2;
   p.Dvec = l.Dvec;
+  p.npad = l.npad;
   p.dq = l.dq;
   p.dk = l.dk;
   p.dv = l.dv;

@@ -74,9 +74,12 @@ cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const Ro
 cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, const float2* table,
                              int B, int n, int H, int d, bool rotate, cudaStream_t st);
 
-// D[b, h, i] = sum_c dO[b,i,h,c] * O[b,i,h,c] (f32).
-cudaError_t launch_bwd_dot(const void* o, const void* dout, bool f32, float* Dvec, int B,
-                           int n, int Hq, int d, cudaStream_t st);
+// Per-row vectors of the backward in [B, Hq, npad] layout (npad >= n):
+// Dvec = sum_c dO[b,i,h,c] * O[b,i,h,c], lse2 = lse * log2(e); padding rows
+// get D = 0 and lse2 = +inf (zero probability).
+cudaError_t launch_bwd_vec(const void* o, const void* dout, bool f32, const float* lse,
+                           float* Dvec, float* lse2, int B, int n, int npad, int Hq, int d,
+                           cudaStream_t st);
 
 // ------------------------------------------------------------- forward ----
 struct FwdLaunch {
@@ -123,8 +126,9 @@ struct BwdLaunch {
   const CUtensorMap* mV96;
   int B, n, Hq, Hkv, d, p, frozen_prefix;
   float scale;
-  const float* lse;         // [B, Hq, n] natural log
-  const float* Dvec;        // [B, Hq, n]
+  const float* lse2;        // [B, Hq, npad] log2-domain lse, +inf past n
+  const float* Dvec;        // [B, Hq, npad], 0 past n
+  int npad;                 // n rounded up to a multiple of 128
   void* dq;                 // [B, n, Hq, d] output dtype
   void* dk;                 // [B, n, Hkv, d]
   void* dv;

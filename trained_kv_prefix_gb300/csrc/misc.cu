@@ -3,7 +3,7 @@
 //     the bf16 shadow the tensor-core kernels read;
 //   * the RoPE cos/sin table for a run of positions (fp64 angle reduction);
 //   * rotation of real-token Q/K rows at positions p + i into bf16;
-//   * the backward's per-row D = rowsum(dO * O).
+//   * the backward's per-row D = rowsum(dO * O) and log2-domain lse.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -140,17 +140,24 @@ __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __r
   }
 }
 
-// ------------------------------------------------------------- bwd dot ----
-// Dvec[b, h, i] = sum_c dO[b,i,h,c] * O[b,i,h,c]; 8 lanes per row, 4 rows
-// per warp; the loop trip count is uniform across the warp.
+// ------------------------------------------------------------- bwd vec ----
+// Per query row of the backward, in [B, Hq, npad] layout (npad >= n, rows
+// n..npad-1 are padding that reads as "no probability mass"):
+//   Dvec[b, h, i] = sum_c dO[b,i,h,c] * O[b,i,h,c]   (0 for padding)
+//   lse2[b, h, i] = lse[b, h, i] * log2(e)           (+inf for padding)
+// 8 lanes per row, 4 rows per warp; the loop trip count is uniform across
+// the warp.
 template <bool kF32>
-__global__ void bwd_dot_kernel(const void* __restrict__ ov, const void* __restrict__ dov,
-                               float* __restrict__ Dvec, int B, int n, int Hq, int d) {
+__global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restrict__ dov,
+                               const float* __restrict__ lse, float* __restrict__ Dvec,
+                               float* __restrict__ lse2, int B, int n, int npad, int Hq, int d) {
   const long long rows = static_cast<long long>(B) * n * Hq;
   const int lane8 = threadIdx.x & 7;
   const int group = (threadIdx.x & 31) >> 3;
-  const long long warp_id = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
-  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long warp_id = tid >> 5;
+  const long long warps = nthreads >> 5;
   for (long long base = warp_id * 4; base < rows; base += warps * 4) {
     const long long row = base + group;
     float acc = 0.f;
@@ -188,8 +195,17 @@ __global__ void bwd_dot_kernel(const void* __restrict__ ov, const void* __restri
       const long long bi = row / Hq;
       const int i = static_cast<int>(bi % n);
       const int b = static_cast<int>(bi / n);
-      Dvec[(static_cast<long long>(b) * Hq + h) * n + i] = acc;
+      const long long bh = static_cast<long long>(b) * Hq + h;
+      Dvec[bh * npad + i] = acc;
+      lse2[bh * npad + i] = __ldg(lse + bh * n + i) * 1.4426950408889634f;
     }
+  }
+  const long long pad_rows = static_cast<long long>(B) * Hq * (npad - n);
+  for (long long t = tid; t < pad_rows; t += nthreads) {
+    const long long bh = t / (npad - n);
+    const int i = n + static_cast<int>(t % (npad - n));
+    Dvec[bh * npad + i] = 0.f;
+    lse2[bh * npad + i] = INFINITY;
   }
 }
 
@@ -236,16 +252,17 @@ cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dot(const void* o, const void* dout, bool f32, float* Dvec, int B, int n,
-                           int Hq, int d, cudaStream_t st) {
+cudaError_t launch_bwd_vec(const void* o, const void* dout, bool f32, const float* lse,
+                           float* Dvec, float* lse2, int B, int n, int npad, int Hq, int d,
+                           cudaStream_t st) {
   const long long rows = static_cast<long long>(B) * n * Hq;
-  if (rows <= 0) return cudaSuccess;
+  if (rows <= 0 || npad < n) return cudaSuccess;
   const int grid = grid_for(rows * 8);  // 8 threads per row
-  TraceScope tr("bwd_dot", st);
+  TraceScope tr("bwd_vec", st);
   if (f32)
-    bwd_dot_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, Dvec, B, n, Hq, d);
+    bwd_vec_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, lse, Dvec, lse2, B, n, npad, Hq, d);
   else
-    bwd_dot_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, Dvec, B, n, Hq, d);
+    bwd_vec_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, lse, Dvec, lse2, B, n, npad, Hq, d);
   return cudaGetLastError();
 }
 
