@@ -386,20 +386,10 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
   CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
-  CUtensorMap mdO, mdO64, mK96, mV96, mKc96, mVc96;
+  CUtensorMap mdO, mdO64;
   if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128) ||
-      !make_rows_map(&mdO64, dob, g->B, g->n, g->Hq, g->d, 64) ||
-      !make_rows_map(&mK96, tp.kr, g->B, g->n, g->Hkv, g->d, 96) ||
-      !make_rows_map(&mV96, tp.vb, g->B, g->n, g->Hkv, g->d, 96))
+      !make_rows_map(&mdO64, dob, g->B, g->n, g->Hq, g->d, 64))
     return CART_ERR_CUDA;
-  if (g->p > 0) {
-    if (!make_rows_map(&mKc96, tp.kcb, 1, g->p, g->Hkv, g->d, 96) ||
-        !make_rows_map(&mVc96, tp.vcb, 1, g->p, g->Hkv, g->d, 96))
-      return CART_ERR_CUDA;
-  } else {  // never loaded when there are no cartridge rows
-    mKc96 = mK96;
-    mVc96 = mV96;
-  }
   BwdLaunch l{};
   l.mQ = &tp.mQ;
   l.mdO = &mdO;
@@ -409,10 +399,6 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.mVc = &tp.mVc;
   l.mK = &tp.mK;
   l.mV = &tp.mV;
-  l.mKc96 = &mKc96;
-  l.mVc96 = &mVc96;
-  l.mK96 = &mK96;
-  l.mV96 = &mV96;
   l.B = g->B;
   l.n = g->n;
   l.Hq = g->Hq;

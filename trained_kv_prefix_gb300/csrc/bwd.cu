@@ -19,8 +19,8 @@
 //               P^T, dS^T (bf16, shared memory), dV += P^T dO, dK += dS^T Q.
 //               Epilogue: cartridge rows (f32, rows < frozen_prefix = 0) or
 //               real rows (dK rotated back by R(p+j)^T).
-//  dq_kernel    one CTA per 128-row query tile (like the forward): S = Q K^T,
-//               dP = dO V^T, dS = P (dP - D) -> shared memory, dQ += dS K;
+//  dq_kernel    one CTA per 128-row query tile: S = Q K^T, dP = dO V^T,
+//               dS = P (dP - D) -> TMEM, dQ += dS K over 128-key steps;
 //               epilogue rotates back by R(p+i)^T.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -444,43 +444,59 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 }
 
 // ================================================================ dQ ======
-// One CTA per 128-row query tile.  Keys stream in 96-row steps (N = 96):
-// S = Q K^T and dP = dO V^T go to double-buffered TMEM (S at x*96, dP at
-// 192 + x*96).  Both warpgroups work on every step, warpgroup w on keys
-// [48w, 48w + 48): it overwrites the first 24 columns of its half of S with
-// dS = P (dP - D) packed as bf16 pairs, and dQ += dS K reads dS from TMEM
-// (A operand; K step k of 16 keys at column (k/3)*48 + (k%3)*8) with K as
-// an MN-major operand.  dQ accumulates at column 384.  Threads: warps 0-7
-// the two warpgroups (thread = query row = TMEM lane), warp 8 TMA, warp 9
-// MMA.
+// One CTA per 128-row query tile (heaviest tiles first), Q and dO resident in
+// shared memory.  Keys stream in 128-row steps (every MMA has N = 128).
+// TMEM: S double buffered at x*128 (x = step & 1), dP at 256, dQ at 384.
+// Both warpgroups work on every step, warpgroup w on keys [64w, 64w + 64)
+// (thread = query row = TMEM lane).  A warpgroup reads its S and dP columns,
+// releases dP at once (so dP of the next step can be computed while it
+// works), then overwrites the first 32 of its 64 S columns with
+// dS = P (dP - D) packed as bf16 pairs; dQ += dS K reads dS from TMEM as its
+// A operand (K step k of 16 keys at column (k/4)*64 + (k%4)*8), K entering
+// as an MN-major operand.  MMA order per step t:
+//   S(t+1), dP(t+1) [after dP(t) is released], dQ(t) [after dS(t)].
+// K has a 3-stage ring (read by S and dQ), V a 2-stage ring (read by dP).
+// Threads: warps 0-7 the two warpgroups, warp 8 TMA, warp 9 MMA.
 constexpr int kDqThreads = 320;
-constexpr int kDqKeys = 96;
+constexpr int kDqKStages = 3;
+constexpr int kDqVStages = 2;
 
 template <int D>
 struct DqSmem {
-  static constexpr int kStages = 3;
-  static constexpr int kQT = kTile * D * 2;      // 128-row Q or dO tile
-  static constexpr int kKT = kDqKeys * D * 2;    // 96-row K or V tile
+  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile
   static constexpr int kQ = 0;
-  static constexpr int kdO = kQ + kQT;
-  static constexpr int kStage0 = kdO + kQT;      // stage s: K at +0, V at +kKT
-  static constexpr int kBar = kStage0 + kStages * 2 * kKT;
+  static constexpr int kdO = kQ + kTileBytes;
+  static constexpr int kK = kdO + kTileBytes;                 // K ring
+  static constexpr int kV = kK + kDqKStages * kTileBytes;     // V ring
+  static constexpr int kBar = kV + kDqVStages * kTileBytes;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-enum DqBar { kQdFull = 0, kKvFull0, kKvEmpty0 = kKvFull0 + 3, kSdFull0 = kKvEmpty0 + 3,
-             kDsdFull0 = kSdFull0 + 2, kDqDone = kDsdFull0 + 2, kDqDrain, kDqBars };
+enum DqBar {
+  kQdFull = 0,
+  kKFull0,
+  kKEmpty0 = kKFull0 + kDqKStages,
+  kVFull0 = kKEmpty0 + kDqKStages,
+  kVEmpty0 = kVFull0 + kDqVStages,
+  kSdFull0 = kVEmpty0 + kDqVStages,  // S of buffer x computed
+  kDpFull = kSdFull0 + 2,            // dP computed
+  kDpFree,                           // both groups read dP (256 arrivals)
+  kDsdFull0,                         // dS of buffer x written (256 arrivals)
+  kDqDone = kDsdFull0 + 2,
+  kDqDrain,
+  kDqBars
+};
+static_assert(kDqBars * 8 + 4 <= 256, "dq barrier area");
 
 template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
-              const __grid_constant__ CUtensorMap mKc96, const __grid_constant__ CUtensorMap mVc96,
-              const __grid_constant__ CUtensorMap mK96, const __grid_constant__ CUtensorMap mV96,
+              const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
+              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
               const BwdParams a) {
   using L = DqSmem<D>;
-  constexpr int S = L::kStages;
-  constexpr int NK = kDqKeys;
+  constexpr int SK = kDqKStages, SV = kDqVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -493,22 +509,28 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);
   const int kvh = h / a.G;
   const int q0 = qt * kTile;
-  const int n_ct = (a.p + NK - 1) / NK;
+  const int n_ct = (a.p + kTile - 1) / kTile;
   const int last_q = min(q0 + kTile, a.n) - 1;          // last real query of the tile
-  const int n_rt = last_q / NK + 1;                      // real key steps up to the diagonal
+  const int n_rt = last_q / kTile + 1;                   // real key steps up to the diagonal
   const int T = n_ct + n_rt;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bars[kQdFull], 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&bars[kKvFull0 + s], 1);
-      mbar_init(&bars[kKvEmpty0 + s], 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&bars[kKFull0 + s], 1);
+      mbar_init(&bars[kKEmpty0 + s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&bars[kVFull0 + s], 1);
+      mbar_init(&bars[kVEmpty0 + s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kSdFull0 + x], 1);
       mbar_init(&bars[kDsdFull0 + x], 256);
     }
+    mbar_init(&bars[kDpFull], 1);
+    mbar_init(&bars[kDpFree], 256);
     mbar_init(&bars[kDqDone], 1);
     mbar_init(&bars[kDqDrain], 1);
     fence_mbar_init();
@@ -521,7 +543,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tDP0 = tmem + 192, tDQ = tmem + 384;
+  const uint32_t tS0 = tmem, tDP = tmem + 256, tDQ = tmem + 384;
   volatile int* abort_p = &abort_flag;
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sdO = smem + L::kdO;
@@ -530,102 +552,120 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
-      mbar_arrive_expect_tx(&bars[kQdFull], 2 * L::kQT);
+      mbar_arrive_expect_tx(&bars[kQdFull], 2 * L::kTileBytes);
 #pragma unroll
       for (int hc = 0; hc < D / 64; ++hc) {
         tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdFull], hc * 64, h, q0, b);
         tma_load_4d(sdO + hc * 16384, &mdO, &bars[kQdFull], hc * 64, h, q0, b);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int t = 0; t < T; ++t) {
-        const int s = t % S;
-        if (t >= S) {
-          ok = mbar_wait(&bars[kKvEmpty0 + s], ((t / S) - 1) & 1, abort_p, a.status,
+      for (int t = 0; t < T && ok; ++t) {
+        const bool cart = t < n_ct;
+        const int row0 = cart ? t * kTile : (t - n_ct) * kTile;
+        const int blk = cart ? 0 : b;
+        const int sk = t % SK, sv = t % SV;
+        if (t >= SK) {
+          ok = mbar_wait(&bars[kKEmpty0 + sk], ((t / SK) - 1) & 1, abort_p, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
-        uint8_t* sK = smem + L::kStage0 + s * 2 * L::kKT;
-        uint8_t* sV = sK + L::kKT;
-        mbar_arrive_expect_tx(&bars[kKvFull0 + s], 2 * L::kKT);
+        uint8_t* sK = smem + L::kK + sk * L::kTileBytes;
+        mbar_arrive_expect_tx(&bars[kKFull0 + sk], L::kTileBytes);
 #pragma unroll
-        for (int hc = 0; hc < D / 64; ++hc) {
-          if (t < n_ct) {
-            tma_load_4d(sK + hc * (NK * 128), &mKc96, &bars[kKvFull0 + s], hc * 64, kvh, t * NK, 0);
-            tma_load_4d(sV + hc * (NK * 128), &mVc96, &bars[kKvFull0 + s], hc * 64, kvh, t * NK, 0);
-          } else {
-            tma_load_4d(sK + hc * (NK * 128), &mK96, &bars[kKvFull0 + s], hc * 64, kvh,
-                        (t - n_ct) * NK, b);
-            tma_load_4d(sV + hc * (NK * 128), &mV96, &bars[kKvFull0 + s], hc * 64, kvh,
-                        (t - n_ct) * NK, b);
-          }
+        for (int hc = 0; hc < D / 64; ++hc)
+          tma_load_4d(sK + hc * 16384, cart ? &mKc : &mK, &bars[kKFull0 + sk], hc * 64, kvh, row0,
+                      blk);
+        k_issued = t + 1;
+        if (t >= SV) {
+          ok = mbar_wait(&bars[kVEmpty0 + sv], ((t / SV) - 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutTma);
+          if (!ok) break;
         }
-        issued = t + 1;
+        uint8_t* sV = smem + L::kV + sv * L::kTileBytes;
+        mbar_arrive_expect_tx(&bars[kVFull0 + sv], L::kTileBytes);
+#pragma unroll
+        for (int hc = 0; hc < D / 64; ++hc)
+          tma_load_4d(sV + hc * 16384, cart ? &mVc : &mV, &bars[kVFull0 + sv], hc * 64, kvh, row0,
+                      blk);
+        v_issued = t + 1;
       }
       if (!ok) {
         int dummy = 0;
         mbar_wait(&bars[kQdFull], 0, &dummy, nullptr, 0);
-        for (int t = max(issued - S, 0); t < issued; ++t)
-          mbar_wait(&bars[kKvFull0 + t % S], (t / S) & 1, &dummy, nullptr, 0);
+        for (int t = max(k_issued - SK, 0); t < k_issued; ++t)
+          mbar_wait(&bars[kKFull0 + t % SK], (t / SK) & 1, &dummy, nullptr, 0);
+        for (int t = max(v_issued - SV, 0); t < v_issued; ++t)
+          mbar_wait(&bars[kVFull0 + t % SV], (t / SV) & 1, &dummy, nullptr, 0);
       }
     }
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && T > 0) {
-      const uint32_t idS = idesc_bf16(128, NK, false, false);
+      const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idDQ = idesc_bf16(128, D, false, true);
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
-      const uint64_t dO0 = sdesc_sw128(smem_u32(sdO), 16u, 1024u);
-      const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16u, 1024u);           // K-major
-      const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kStage0), NK * 128u, 1024u);     // MN-major
-      constexpr uint32_t kStageBytes = 2 * L::kKT;
-      bool ok = mbar_wait(&bars[kQdFull], 0, abort_p, a.status, kDevErrTimeoutMma);
-      auto issue_dq = [&](int t) {
-        const int s = t % S, x = t & 1;
-        const uint64_t dkm = desc_add(dKm0, s * kStageBytes);
-        const uint32_t ds = tS0 + x * NK;
-        umma_bf16_ts(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 1; k < NK / 16; ++k)
-          umma_bf16_ts(tDQ, ds + (k / 3) * 48 + (k % 3) * 8, desc_add(dkm, k * 2048), idDQ, 1u);
-        umma_commit(&bars[kKvEmpty0 + s]);
-      };
-      for (int t = 0; t < T && ok; ++t) {
-        const int s = t % S, x = t & 1;
-        ok = mbar_wait(&bars[kKvFull0 + s], (t / S) & 1, abort_p, a.status, kDevErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
-        // buffer x was last read by the dQ MMA of step t-2, issued earlier
-        const uint64_t dk = desc_add(dKk0, s * kStageBytes);
-        const uint64_t dv = desc_add(dk, L::kKT);
-        const uint32_t ts = tS0 + x * NK, tdp = tDP0 + x * NK;
-        umma_bf16_ss(ts, dQ0, dk, idS, 0u);
-        umma_bf16_ss(tdp, dO0, dv, idS, 0u);
+      const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
+      const uint64_t dOd = sdesc_sw128(smem_u32(sdO), 16u, 1024u);
+      const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);      // K-major
+      const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kK), 16384u, 1024u);   // MN-major
+      const uint64_t dVk0 = sdesc_sw128(smem_u32(smem + L::kV), 16u, 1024u);
+      // C (f32, TMEM) = A (128 rows) * B^T (128 rows), both K-major over d
+      auto issue_nt = [&](uint32_t c, uint64_t da, uint64_t db) {
+        umma_bf16_ss(c, da, db, idS, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
-          const uint32_t offa = (k >> 2) * 16384 + (k & 3) * 32;
-          const uint32_t offb = (k >> 2) * (NK * 128) + (k & 3) * 32;
-          umma_bf16_ss(ts, desc_add(dQ0, offa), desc_add(dk, offb), idS, 1u);
-          umma_bf16_ss(tdp, desc_add(dO0, offa), desc_add(dv, offb), idS, 1u);
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idS, 1u);
         }
-        umma_commit(&bars[kSdFull0 + x]);
-        if (t > 0) {
-          ok = mbar_wait(&bars[kDsdFull0 + (x ^ 1)], ((t - 1) >> 1) & 1, abort_p, a.status,
+      };
+      bool ok = mbar_wait(&bars[kQdFull], 0, abort_p, a.status, kDevErrTimeoutMma) &&
+                mbar_wait(&bars[kKFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_nt(tS0, dQd, dKk0);
+        umma_commit(&bars[kSdFull0]);
+        ok = mbar_wait(&bars[kVFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_nt(tDP, dOd, dVk0);
+        umma_commit(&bars[kDpFull]);
+        umma_commit(&bars[kVEmpty0]);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int x = t & 1;
+        if (t + 1 < T) {
+          const int sk = (t + 1) % SK, sv = (t + 1) % SV;
+          ok = mbar_wait(&bars[kKFull0 + sk], ((t + 1) / SK) & 1, abort_p, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          issue_dq(t - 1);
-        }
-      }
-      if (ok) {
-        ok = mbar_wait(&bars[kDsdFull0 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, abort_p, a.status,
-                       kDevErrTimeoutMma);
-        if (ok) {
+          // buffer x^1 last held dS(t-1), read by dQ(t-1) issued earlier
+          // (one CTA's MMAs run in issue order)
+          issue_nt(tS0 + (x ^ 1) * 128, dQd, desc_add(dKk0, sk * L::kTileBytes));
+          umma_commit(&bars[kSdFull0 + (x ^ 1)]);
+          ok = mbar_wait(&bars[kDpFree], t & 1, abort_p, a.status, kDevErrTimeoutMma) &&
+               mbar_wait(&bars[kVFull0 + sv], ((t + 1) / SV) & 1, abort_p, a.status,
+                         kDevErrTimeoutMma);
+          if (!ok) break;
           tc_fence_after();
-          issue_dq(T - 1);
-          umma_commit(&bars[kDqDone]);
+          issue_nt(tDP, dOd, desc_add(dVk0, sv * L::kTileBytes));
+          umma_commit(&bars[kDpFull]);
+          umma_commit(&bars[kVEmpty0 + sv]);
         }
+        ok = mbar_wait(&bars[kDsdFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        const int sk = t % SK;
+        const uint64_t dkm = desc_add(dKm0, sk * L::kTileBytes);
+        const uint32_t ds = tS0 + x * 128;
+        umma_bf16_ts(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ts(tDQ, ds + (k >> 2) * 64 + (k & 3) * 8, desc_add(dkm, k * 2048), idDQ, 1u);
+        umma_commit(&bars[kKEmpty0 + sk]);
       }
+      if (ok) umma_commit(&bars[kDqDone]);
       umma_commit(&bars[kDqDrain]);
       int dummy = 0;
       mbar_wait(&bars[kDqDrain], 0, &dummy, nullptr, 0);
@@ -640,39 +680,36 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const long long vidx = (static_cast<long long>(b) * a.Hq + h) * a.npad + i;
     const float lse2 = __ldg(a.lse2 + vidx);
     const float Di = __ldg(a.Dvec + vidx);
-    constexpr int NH = NK / 2;  // keys per warpgroup and step
+    const int i_cap = min(i, a.n - 1);
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
       const int x = t & 1;
-      ok = mbar_wait(&bars[kSdFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kSdFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax) &&
+           mbar_wait(&bars[kDpFull], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // this group's key columns c (key step*96 + wg*48 + c) are visible for
-      // c < valid
-      int valid;
-      if (t < n_ct) {
-        valid = min(NH, a.p - t * NK - wg * NH);
-      } else {
-        const int col0 = (t - n_ct) * NK + wg * NH;
-        valid = min(min(i, a.n - 1) - col0 + 1, NH);
-      }
-      const uint32_t ts = tS0 + x * NK + wg * NH + lane_off;
-      const uint32_t tdp = tDP0 + x * NK + wg * NH + lane_off;
-      uint32_t sa[32], da[32], sb[16], db[16];
+      // visible keys of this group's 64 (leading columns)
+      int valid = t < n_ct ? a.p - t * kTile - wg * 64 : i_cap - (t - n_ct) * kTile - wg * 64 + 1;
+      valid = max(0, min(valid, 64));
+      const uint32_t ts = tS0 + x * 128 + wg * 64 + lane_off;
+      const uint32_t tdp = tDP + wg * 64 + lane_off;
+      uint32_t sa[32], sb[32], da[32], db[32];
       tmem_ld32(ts, sa);
-      tmem_ld16(ts + 32, sb);
+      tmem_ld32(ts + 32, sb);
       tmem_ld32(tdp, da);
-      tmem_ld16(tdp + 32, db);
+      tmem_ld32(tdp + 32, db);
       tmem_ld_wait();
       tmem_reg_fence(sa);
-      tmem_reg_fence16(sb);
+      tmem_reg_fence(sb);
       tmem_reg_fence(da);
-      tmem_reg_fence16(db);
-      uint32_t pk[32];  // 24 used; the rest pads the 32-column store
+      tmem_reg_fence(db);
+      tc_fence_before();
+      mbar_arrive(&bars[kDpFree]);
+      uint32_t pk[32];
       auto compute = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < NH; c += 2) {
+        for (int c = 0; c < 64; c += 2) {
           float ds[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -686,14 +723,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
       };
-      if (__any_sync(0xffffffffu, valid < NH))
+      if (__any_sync(0xffffffffu, valid < 64))
         compute(std::true_type{});
       else
         compute(std::false_type{});
-#pragma unroll
-      for (int c = NH / 2; c < 32; ++c) pk[c] = 0u;
-      // 32-column store at the start of this group's 48 S columns: 24 packed
-      // dS columns plus 8 padding columns, all inside the group's own half
+      // dS over the first 32 of this group's S columns (already read)
       tmem_st32(ts, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -791,7 +825,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   if (e != cudaSuccess) return e;
   TraceScope tr("bwd_dq", st_dq);
   dq_kernel<D><<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
-      *l.mQ, *l.mdO, *l.mKc96, *l.mVc96, *l.mK96, *l.mV96, p);
+      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
   return cudaGetLastError();
 }
 

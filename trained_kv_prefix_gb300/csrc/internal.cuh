@@ -120,10 +120,6 @@ struct BwdLaunch {
   const CUtensorMap* mVc;
   const CUtensorMap* mK;    // 4D (d, Hkv, n, B) rotated real keys
   const CUtensorMap* mV;
-  const CUtensorMap* mKc96; // the same four tensors with a 96-row box (dQ kernel)
-  const CUtensorMap* mVc96;
-  const CUtensorMap* mK96;
-  const CUtensorMap* mV96;
   int B, n, Hq, Hkv, d, p, frozen_prefix;
   float scale;
   const float* lse2;        // [B, Hq, npad] log2-domain lse, +inf past n
