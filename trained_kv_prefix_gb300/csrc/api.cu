@@ -183,7 +183,7 @@ struct TrainPrep {
   const void* vb;
   const void* kcb;
   const void* vcb;
-  CUtensorMap mQ, mQ64, mK, mV, mKc, mVc;
+  CUtensorMap mQ, mK, mV, mKc, mVc;
 };
 
 // With q_in_kernel (bf16 queries only) Q is left unrotated: mQ maps q itself
@@ -227,7 +227,6 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
   out->kcb = kcb;
   out->vcb = vcb;
   bool ok = make_rows_map(&out->mQ, qr, g->B, g->n, g->Hq, g->d, 128) &&
-            make_rows_map(&out->mQ64, qr, g->B, g->n, g->Hq, g->d, 64) &&
             make_rows_map(&out->mK, kr, g->B, g->n, g->Hkv, g->d, 128) &&
             make_rows_map(&out->mV, vb, g->B, g->n, g->Hkv, g->d, 128);
   if (g->p > 0)
@@ -386,15 +385,11 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
   CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
-  CUtensorMap mdO, mdO64;
-  if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128) ||
-      !make_rows_map(&mdO64, dob, g->B, g->n, g->Hq, g->d, 64))
-    return CART_ERR_CUDA;
+  CUtensorMap mdO;
+  if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
   BwdLaunch l{};
   l.mQ = &tp.mQ;
   l.mdO = &mdO;
-  l.mQ64 = &tp.mQ64;
-  l.mdO64 = &mdO64;
   l.mKc = &tp.mKc;
   l.mVc = &tp.mVc;
   l.mK = &tp.mK;

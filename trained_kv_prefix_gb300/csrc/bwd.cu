@@ -11,7 +11,7 @@
 //
 //  dkdv_kernel  one CTA per 128-row key tile.  A cartridge tile is seen by
 //               every query of every sequence, so its CTA loops over all
-//               (sequence, head of the group, 64-row query tile) and sums the
+//               (sequence, head of the group, 128-row query tile) and sums the
 //               batch inside its TMEM accumulators: the cartridge gradient
 //               needs no cross-CTA reduction.  A real-token tile loops over
 //               the heads of the group and the query tiles at or after it.
@@ -37,7 +37,7 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
-  int B, n, Hq, Hkv, G, p, frozen_prefix, nq64, n_ct, n_rt, n_qtiles;
+  int B, n, Hq, Hkv, G, p, frozen_prefix, n_ct, n_rt, n_qtiles;
   float scale, scale_log2;
   const float* lse2;  // [B, Hq, npad] log2-domain lse (+inf past n)
   const float* Dvec;  // [B, Hq, npad] (0 past n)
@@ -69,56 +69,59 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 }
 
 // =========================================================== dK / dV ======
-// Threads: warps 0-3 and 4-7 are two P^T / dS^T warpgroups that share every
-// 64-query step, warpgroup w taking queries [32w, 32w + 32) (thread t of a
-// group owns key row t = TMEM lane t); warp 8 is the TMA producer, warp 9
-// issues the MMAs.
-// TMEM (512 columns): step buffer x in {0,1} holds S^T at columns x*64 and
-// dP^T at 128 + x*64 (64 f32 columns each).  Warpgroup w overwrites the
-// first 16 columns of its own 32-column half with its P^T and dS^T packed
-// as bf16 pairs, which the dV and dK MMAs read as their A operand straight
-// from TMEM (K step k of 16 queries lives at column (k/2)*32 + (k%2)*8).
-// dV accumulates at 256, dK at 384.
-constexpr int kDkdvThreads = 320;
-
-constexpr int kDkdvStages = 4;
+// Threads: warps 0-15 are four P^T / dS^T warpgroups that share every
+// 128-query step, warpgroup w taking queries [32w, 32w + 32) (thread t of a
+// group owns key row t = TMEM lane t); warp 16 is the TMA producer, warp 17
+// issues the MMAs.  Every MMA has N = 128.
+// TMEM (512 columns): S^T at 0, dP^T at 128 (f32), dV at 256, dK at 384.
+// Warpgroup w overwrites the first 16 columns of its 32-column slices of
+// S^T and dP^T with P^T and dS^T packed as bf16 pairs, which the dV and dK
+// MMAs read as their A operand straight from TMEM (K step k of 16 queries at
+// column (k/2)*32 + (k%2)*8).  P^T is formed while dP^T is still being
+// computed (S^T and dP^T have their own barriers).  The next step's S^T and
+// dP^T are issued after this step's dV / dK MMAs (one CTA's MMAs run in
+// issue order, so they overwrite P^T / dS^T only after those have read it).
+constexpr int kDkdvThreads = 576;
+constexpr int kDkdvStages = 2;
 
 template <int D>
 struct DkdvSmem {
   static constexpr int kStages = kDkdvStages;
-  static constexpr int kKV = kTile * D * 2;        // resident K or V tile
-  static constexpr int kQT = 64 * D * 2;           // 64-row Q or dO tile
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kKV;
-  static constexpr int kStage0 = kV + kKV;         // stage s: Q at +0, dO at +kQT
-  static constexpr int kVec = kStage0 + kStages * 2 * kQT;  // stage s: lse2[64], D[64]
-  static constexpr int kBar = kVec + kStages * 512;
+  static constexpr int kTileBytes = kTile * D * 2;     // 128-row bf16 tile
+  static constexpr int kK = 0;                          // resident K
+  static constexpr int kV = kK + kTileBytes;            // resident V
+  static constexpr int kStage0 = kV + kTileBytes;       // stage s: Q at +0, dO at +kTileBytes
+  static constexpr int kVec = kStage0 + kStages * 2 * kTileBytes;  // stage s: lse2[128], D[128]
+  static constexpr int kBar = kVec + kStages * 1024;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
 enum DkdvBar { kResFull = 0, kQdoFull0, kQdoEmpty0 = kQdoFull0 + kDkdvStages,
-               kStFull0 = kQdoEmpty0 + kDkdvStages,
-               kDsFull0 = kStFull0 + 2, kAccDone = kDsFull0 + 2, kDkdvDrain, kDkdvBars };
+               kStFull = kQdoEmpty0 + kDkdvStages, kDpTFull, kDsFull, kAccDone, kDkdvDrain,
+               kDkdvBars };
 
 struct DkdvItem {
   int b, hh, qt;
 };
 
+// Step u of a key tile: a cartridge tile sees every (sequence, head of the
+// group, 128-row query tile); real tile rt of a sequence sees the heads of
+// the group and query tiles rt.. (the causal diagonal and after).
 __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& a, bool cart, int b_real, int rt,
                                               int u) {
   DkdvItem it;
   if (cart) {
-    const int per_b = a.G * a.nq64;
+    const int per_b = a.G * a.n_qtiles;
     it.b = u / per_b;
     const int rem = u % per_b;
-    it.hh = rem / a.nq64;
-    it.qt = rem % a.nq64;
+    it.hh = rem / a.n_qtiles;
+    it.qt = rem % a.n_qtiles;
   } else {
-    const int nq = a.nq64 - 2 * rt;
+    const int nq = a.n_qtiles - rt;
     it.b = b_real;
     it.hh = u / nq;
-    it.qt = 2 * rt + u % nq;
+    it.qt = rt + u % nq;
   }
   return it;
 }
@@ -140,7 +143,7 @@ __device__ __forceinline__ void write_cart_row(float* dst, const float* x, int n
 
 template <int D>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
-    dkdv_kernel(const __grid_constant__ CUtensorMap mQ64, const __grid_constant__ CUtensorMap mdO64,
+    dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                 const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const BwdParams a) {
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     b_real = rem / a.Hkv;
     g = rem % a.Hkv;
   }
-  const int U = cart ? a.B * a.G * a.nq64 : a.G * max(a.nq64 - 2 * tile, 0);
+  const int U = cart ? a.B * a.G * a.n_qtiles : a.G * max(a.n_qtiles - tile, 0);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -179,15 +182,14 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       mbar_init(&bars[kQdoFull0 + s], 1);
       mbar_init(&bars[kQdoEmpty0 + s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars[kStFull0 + x], 1);
-      mbar_init(&bars[kDsFull0 + x], 256);
-    }
+    mbar_init(&bars[kStFull], 1);
+    mbar_init(&bars[kDpTFull], 1);
+    mbar_init(&bars[kDsFull], 512);
     mbar_init(&bars[kAccDone], 1);
     mbar_init(&bars[kDkdvDrain], 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -195,21 +197,21 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tST0 = tmem, tDP0 = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+  const uint32_t tST = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
   volatile int* abort_p = &abort_flag;
   uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
   float* vec = reinterpret_cast<float*>(smem + L::kVec);
 
-  if (warp == 8) {
+  if (warp == 16) {
     // ------------------------------------------------------------ producer --
-    // One lane: per step the Q and dO tiles (TMA) and the step's 64 entries
+    // One lane: per step the Q and dO tiles (TMA) and the step's 128 entries
     // of lse2 and D (plain bulk copies from the padded row vectors), all
     // completing on the stage's full barrier.
     if (lane == 0 && U > 0) {
-      tma_prefetch_desc(&mQ64);
-      tma_prefetch_desc(&mdO64);
-      mbar_arrive_expect_tx(&bars[kResFull], 2 * L::kKV);
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mdO);
+      mbar_arrive_expect_tx(&bars[kResFull], 2 * L::kTileBytes);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
         if (cart) {
@@ -231,19 +233,19 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
         const int h = g * a.G + it.hh;
-        uint8_t* sQ = smem + L::kStage0 + s * 2 * L::kQT;
-        uint8_t* sdO = sQ + L::kQT;
-        float* v = vec + s * 128;
-        const long long vo = (static_cast<long long>(it.b) * a.Hq + h) * a.npad + it.qt * 64;
-        mbar_arrive_expect_tx(&bars[kQdoFull0 + s], 2 * L::kQT + 512);
+        uint8_t* sQ = smem + L::kStage0 + s * 2 * L::kTileBytes;
+        uint8_t* sdO = sQ + L::kTileBytes;
+        float* v = vec + s * 256;
+        const long long vo = (static_cast<long long>(it.b) * a.Hq + h) * a.npad + it.qt * kTile;
+        mbar_arrive_expect_tx(&bars[kQdoFull0 + s], 2 * L::kTileBytes + 1024);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc) {
-          tma_load_4d(sQ + hc * 8192, &mQ64, &bars[kQdoFull0 + s], hc * 64, h, it.qt * 64, it.b);
-          tma_load_4d(sdO + hc * 8192, &mdO64, &bars[kQdoFull0 + s], hc * 64, h, it.qt * 64,
+          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdoFull0 + s], hc * 64, h, it.qt * kTile, it.b);
+          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kQdoFull0 + s], hc * 64, h, it.qt * kTile,
                       it.b);
         }
-        bulk_load(v, a.lse2 + vo, 256, &bars[kQdoFull0 + s]);
-        bulk_load(v + 64, a.Dvec + vo, 256, &bars[kQdoFull0 + s]);
+        bulk_load(v, a.lse2 + vo, 512, &bars[kQdoFull0 + s]);
+        bulk_load(v + 128, a.Dvec + vo, 512, &bars[kQdoFull0 + s]);
         issued = u + 1;
       }
       if (!ok) {
@@ -254,79 +256,61 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 17) {
     // ----------------------------------------------------------------- MMA --
     if (lane == 0 && U > 0) {
-      const uint32_t idST = idesc_bf16(128, 64, false, false);
+      const uint32_t idST = idesc_bf16(128, 128, false, false);
       const uint32_t idACC = idesc_bf16(128, D, false, true);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16u, 1024u);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16u, 1024u);
-      const uint64_t dQk0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16u, 1024u);    // K-major
-      const uint64_t dQm0 = sdesc_sw128(smem_u32(smem + L::kStage0), 8192u, 1024u);  // MN-major
-      constexpr uint32_t kStageBytes = 2 * L::kQT;
-      bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma);
-      // dV += P^T dO and dK += dS^T Q for step u: A from TMEM (buffer u&1),
-      // B = the step's dO / Q tile as MN-major operands (64 rows = 4 K steps).
-      auto issue_acc = [&](int u) {
-        const int s = u % S, x = u & 1;
-        const uint32_t so = s * kStageBytes;
-        const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kQT);
-        const uint32_t pt = tST0 + x * 64, dst = tDP0 + x * 64;
-        const uint32_t first = u > 0 ? 1u : 0u;
-        umma_bf16_ts(tDV, pt, ddo, idACC, first);
-        umma_bf16_ts(tDK, dst, dq, idACC, first);
+      const uint64_t dQk0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16u, 1024u);     // K-major
+      const uint64_t dQm0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16384u, 1024u);  // MN-major
+      constexpr uint32_t kStageBytes = 2 * L::kTileBytes;
+      // C (f32, TMEM) = A (128 rows) * B^T (128 rows), both K-major over d
+      auto issue_nt = [&](uint32_t c, uint64_t da, uint64_t db) {
+        umma_bf16_ss(c, da, db, idST, 0u);
 #pragma unroll
-        for (int k = 1; k < 4; ++k) {
-          const uint32_t ac = (k >> 1) * 32 + (k & 1) * 8;
-          umma_bf16_ts(tDV, pt + ac, desc_add(ddo, k * 2048), idACC, 1u);
-          umma_bf16_ts(tDK, dst + ac, desc_add(dq, k * 2048), idACC, 1u);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idST, 1u);
         }
-        umma_commit(&bars[kQdoEmpty0 + s]);
       };
+      bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma);
       for (int u = 0; u < U && ok; ++u) {
-        const int s = u % S, x = u & 1;
+        const int s = u % S;
         ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status, kDevErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
-        // buffer x was last read by the dV/dK MMAs of step u-2, issued before
-        // this point: the tensor pipe runs one CTA's MMAs in issue order.
         const uint32_t so = s * kStageBytes;
-        const uint64_t dq = desc_add(dQk0, so), ddo = desc_add(dQk0, so + L::kQT);
-        const uint32_t tst = tST0 + x * 64, tdp = tDP0 + x * 64;
-        umma_bf16_ss(tst, dK0, dq, idST, 0u);
-        umma_bf16_ss(tdp, dV0, ddo, idST, 0u);
+        issue_nt(tST, dK0, desc_add(dQk0, so));
+        umma_commit(&bars[kStFull]);
+        issue_nt(tDP, dV0, desc_add(dQk0, so + L::kTileBytes));
+        umma_commit(&bars[kDpTFull]);
+        ok = mbar_wait(&bars[kDsFull], u & 1, abort_p, a.status, kDevErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q: A from TMEM, B = the step's dO / Q
+        // tile as MN-major operands (16 rows = 2048 B per K step)
+        const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kTileBytes);
+        const uint32_t first = u > 0 ? 1u : 0u;
+        umma_bf16_ts(tDV, tST, ddo, idACC, first);
+        umma_bf16_ts(tDK, tDP, dq, idACC, first);
 #pragma unroll
-        for (int k = 1; k < D / 16; ++k) {
-          const uint32_t offa = (k >> 2) * 16384 + (k & 3) * 32;
-          const uint32_t offb = (k >> 2) * 8192 + (k & 3) * 32;
-          umma_bf16_ss(tst, desc_add(dK0, offa), desc_add(dq, offb), idST, 1u);
-          umma_bf16_ss(tdp, desc_add(dV0, offa), desc_add(ddo, offb), idST, 1u);
+        for (int k = 1; k < kTile / 16; ++k) {
+          const uint32_t ac = (k >> 1) * 32 + (k & 1) * 8;
+          umma_bf16_ts(tDV, tST + ac, desc_add(ddo, k * 2048), idACC, 1u);
+          umma_bf16_ts(tDK, tDP + ac, desc_add(dq, k * 2048), idACC, 1u);
         }
-        umma_commit(&bars[kStFull0 + x]);
-        if (u > 0) {
-          ok = mbar_wait(&bars[kDsFull0 + (x ^ 1)], ((u - 1) >> 1) & 1, abort_p, a.status,
-                         kDevErrTimeoutMma);
-          if (!ok) break;
-          tc_fence_after();
-          issue_acc(u - 1);
-        }
+        umma_commit(&bars[kQdoEmpty0 + s]);
       }
-      if (ok) {
-        ok = mbar_wait(&bars[kDsFull0 + ((U - 1) & 1)], ((U - 1) >> 1) & 1, abort_p, a.status,
-                       kDevErrTimeoutMma);
-        if (ok) {
-          tc_fence_after();
-          issue_acc(U - 1);
-          umma_commit(&bars[kAccDone]);
-        }
-      }
+      if (ok) umma_commit(&bars[kAccDone]);
       umma_commit(&bars[kDkdvDrain]);
       int dummy = 0;
       mbar_wait(&bars[kDkdvDrain], 0, &dummy, nullptr, 0);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------- P^T / dS^T warpgroups 0, 1 --
+    // ------------------------------------------- P^T / dS^T warpgroups 0-3 --
     const int wg = warp >> 2;
     const int row = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const int j = tile * kTile + row;
@@ -334,9 +318,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
-      const int s = u % S, x = u & 1;
+      const int s = u % S;
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
-      ok = mbar_wait(&bars[kStFull0 + x], (u >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kStFull], u & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
       // the stage's lse2 / D vectors landed with kQdoFull (already complete:
       // the MMAs behind kStFull waited for it); waiting makes them visible
       if (ok) ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status,
@@ -344,94 +328,129 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tst = tST0 + x * 64 + wg * 32 + lane_off;
-      const uint32_t tdp = tDP0 + x * 64 + wg * 32 + lane_off;
-      // this group's columns c (query it.qt*64 + wg*32 + c) are invisible for
-      // c < qlim: none for a cartridge key, query < key for a real key, all
-      // for rows past the end of the keys
-      const int qlim = !key_ok ? 32 : (cart ? 0 : j - it.qt * 64 - wg * 32);
-      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 128 + wg * 32);
-      const float4* dv4 = reinterpret_cast<const float4*>(vec + s * 128 + 64 + wg * 32);
-      uint32_t sr[32], dr[32], pk[16], dk[16];
-      tmem_ld32(tst, sr);
+      const uint32_t tst = tST + wg * 32 + lane_off;
+      const uint32_t tdp = tDP + wg * 32 + lane_off;
+      // this group's columns c (query it.qt*128 + wg*32 + c) are invisible
+      // for c < qlim: none for a cartridge key, query < key for a real key,
+      // all for rows past the end of the keys
+      const int qlim =
+          !key_ok ? 32 : (cart ? 0 : max(0, min(32, j - it.qt * kTile - wg * 32)));
+      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 256 + wg * 32);
+      const float4* dv4 = reinterpret_cast<const float4*>(vec + s * 256 + 128 + wg * 32);
+      uint32_t r[32];
+      tmem_ld32(tst, r);
+      tmem_ld_wait();
+      tmem_reg_fence(r);
+      // P^T (f32, kept in r) while dP^T is still being computed
+      const bool masked = __any_sync(0xffffffffu, qlim > 0);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l4 = lse4[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c4 * 4 + e;
+          float pe = exp2_approx(fmaf(__uint_as_float(r[cc]), a.scale_log2, -lv[e]));
+          if (masked) pe = (cc >= qlim) ? pe : 0.f;
+          r[cc] = __float_as_uint(pe);
+        }
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        pk[c] = pack_bf16x2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+      tmem_st16(tst, pk);
+      ok = mbar_wait(&bars[kDpTFull], u & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dr[32], pd[16];
       tmem_ld32(tdp, dr);
       tmem_ld_wait();
-      tmem_reg_fence(sr);
       tmem_reg_fence(dr);
-      auto compute = [&](auto masked) {
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = lse4[c4];
-          const float4 d4 = dv4[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 d4 = dv4[c4];
+        const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+        float ds[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = c4 * 4 + e;
-            const float xv = fmaf(__uint_as_float(sr[cc]), a.scale_log2, -lv[e]);
-            float pe = exp2_approx(xv);
-            if (decltype(masked)::value) pe = (cc >= qlim) ? pe : 0.f;
-            pv[e] = pe;
-            dsv[e] = pe * (__uint_as_float(dr[cc]) - dd[e]);
-          }
-          pk[c4 * 2] = pack_bf16x2(pv[0], pv[1]);
-          pk[c4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          dk[c4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
-          dk[c4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c4 * 4 + e;
+          ds[e] = __uint_as_float(r[cc]) * (__uint_as_float(dr[cc]) - dd[e]);
         }
-      };
-      if (__any_sync(0xffffffffu, qlim > 0))
-        compute(std::true_type{});
-      else
-        compute(std::false_type{});
-      // P^T and dS^T over the first 16 columns of this group's halves of
-      // S^T and dP^T (read above by this thread's own lane)
-      tmem_st16(tst, pk);
-      tmem_st16(tdp, dk);
+        pd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+        pd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
+      tmem_st16(tdp, pd);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars[kDsFull0 + x]);
+      mbar_arrive(&bars[kDsFull]);
     }
     // ------------------------------------------------------------ epilogue --
-    // warpgroup 0 writes dV, warpgroup 1 writes dK
+    // warpgroups 0 and 1 write the two halves of dV; 2 and 3 take the RoPE
+    // pairs [w2*D/4, (w2+1)*D/4) of dK with their partners D/2 further on
     if (ok) {
       ok = mbar_wait(&bars[kAccDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
-      float kv[D];
-      const uint32_t src = (wg == 0 ? tDV : tDK) + lane_off;
-      const float mul = wg == 0 ? 1.f : a.scale;
+      constexpr int HW = D / 2, QP = D / 4;
+      if (wg < 2) {
+        float x[HW];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(src + c * 32, r);
-        tmem_ld_wait();
-        tmem_reg_fence(r);
+        for (int c = 0; c < HW / 16; ++c) {
+          uint32_t rr[16];
+          tmem_ld16(tDV + lane_off + wg * HW + c * 16, rr);
+          tmem_ld_wait();
+          tmem_reg_fence16(rr);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) kv[c * 32 + e] = __uint_as_float(r[e]) * mul;
-      }
-      if (key_ok) {
-        const bool frozen = j < a.frozen_prefix;
-        if (cart) {
-          float* dst = (wg == 0 ? a.dvc : a.dkc) + (static_cast<long long>(j) * a.Hkv + g) * D;
-          write_cart_row(dst, kv, D, frozen, a.accumulate);
-        } else if (wg == 0) {
-          store_row_out(a.dv, ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D, kv, D,
-                        a.out_f32 != 0);
-        } else {
-          const float2* tb = a.table + static_cast<long long>(j) * (D / 2);
+          for (int e = 0; e < 16; ++e) x[c * 16 + e] = __uint_as_float(rr[e]);
+        }
+        if (key_ok) {
+          if (cart)
+            write_cart_row(a.dvc + (static_cast<long long>(j) * a.Hkv + g) * D + wg * HW, x, HW,
+                           j < a.frozen_prefix, a.accumulate);
+          else
+            store_row_out(a.dv, ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D + wg * HW,
+                          x, HW, a.out_f32 != 0);
+        }
+      } else {
+        const int w2 = wg - 2;
+        float lo[QP], hi[QP];
 #pragma unroll
-          for (int e = 0; e < D / 2; ++e) {
-            const float2 cs = __ldg(tb + e);
-            const float x0 = kv[e], x1 = kv[e + D / 2];
-            kv[e] = x0 * cs.x + x1 * cs.y;
-            kv[e + D / 2] = x1 * cs.x - x0 * cs.y;
+        for (int c = 0; c < QP / 16; ++c) {
+          uint32_t rr[16];
+          tmem_ld16(tDK + lane_off + w2 * QP + c * 16, rr);
+          tmem_ld_wait();
+          tmem_reg_fence16(rr);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) lo[c * 16 + e] = __uint_as_float(rr[e]) * a.scale;
+          tmem_ld16(tDK + lane_off + D / 2 + w2 * QP + c * 16, rr);
+          tmem_ld_wait();
+          tmem_reg_fence16(rr);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hi[c * 16 + e] = __uint_as_float(rr[e]) * a.scale;
+        }
+        if (key_ok) {
+          if (cart) {
+            float* dst = a.dkc + (static_cast<long long>(j) * a.Hkv + g) * D;
+            const bool frozen = j < a.frozen_prefix;
+            write_cart_row(dst + w2 * QP, lo, QP, frozen, a.accumulate);
+            write_cart_row(dst + D / 2 + w2 * QP, hi, QP, frozen, a.accumulate);
+          } else {
+            const float2* tb = a.table + static_cast<long long>(j) * (D / 2) + w2 * QP;
+#pragma unroll
+            for (int e = 0; e < QP; ++e) {
+              const float2 cs = __ldg(tb + e);
+              const float x0 = lo[e], x1 = hi[e];
+              lo[e] = x0 * cs.x + x1 * cs.y;
+              hi[e] = x1 * cs.x - x0 * cs.y;
+            }
+            const long long off = ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D;
+            store_row_out(a.dk, off + w2 * QP, lo, QP, a.out_f32 != 0);
+            store_row_out(a.dk, off + D / 2 + w2 * QP, hi, QP, a.out_f32 != 0);
           }
-          store_row_out(a.dk, ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D, kv, D,
-                        a.out_f32 != 0);
         }
       }
     }
@@ -440,7 +459,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (warp == 17) tmem_dealloc(tmem, 512);
 }
 
 // ================================================================ dQ ======
@@ -793,7 +812,6 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.G = l.Hq / l.Hkv;
   p.p = l.p;
   p.frozen_prefix = l.frozen_prefix;
-  p.nq64 = (l.n + 63) / 64;
   p.n_ct = (l.p + kTile - 1) / kTile;
   p.n_rt = (l.n + kTile - 1) / kTile;
   p.n_qtiles = p.n_rt;
@@ -819,7 +837,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   if (n_blocks > 0) {
     TraceScope tr("bwd_dkdv", st_dkdv);
     dkdv_kernel<D><<<n_blocks, kDkdvThreads, DkdvSmem<D>::kAlloc, st_dkdv>>>(
-        *l.mQ64, *l.mdO64, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
+        *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

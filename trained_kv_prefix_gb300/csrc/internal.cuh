@@ -114,8 +114,6 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 struct BwdLaunch {
   const CUtensorMap* mQ;    // 4D (d, Hq, n, B) rotated queries (bf16), 128-row box
   const CUtensorMap* mdO;   // 4D (d, Hq, n, B) dO (bf16), 128-row box
-  const CUtensorMap* mQ64;  // same tensors, 64-row box
-  const CUtensorMap* mdO64;
   const CUtensorMap* mKc;   // 4D (d, Hkv, p, 1)
   const CUtensorMap* mVc;
   const CUtensorMap* mK;    // 4D (d, Hkv, n, B) rotated real keys
