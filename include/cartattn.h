@@ -163,8 +163,8 @@ CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale,
  *   Arguments, layouts and results are those of cart_attn_decode, without
  *   the workspace: the scratch is a static device array of
  *   CART_DECODE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the
- *   library holds until the process exits.  (The 64-conversation, p = 4096,
- *   1025-row serving shape needs about 19 MiB.)
+ *   library holds until the process exits.  (The 64-conversation, p = 4096
+ *   serving shape needs about 5 MiB.)
  *   Returns CART_ERR_WORKSPACE, without touching the device, when the
  *   problem needs more scratch than that; otherwise as cart_attn_decode.
  *   Calls no cudaMalloc / cudaFree or allocating library routine.
@@ -172,9 +172,8 @@ CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale,
  *   that device current) and caches it; make that first call before any
  *   stream capture.  All calls share the one array: calls whose work can
  *   overlap on the GPU (other streams, or other host threads without
- *   ordering) race on it and must be serialised by the caller.  The call
- *   clears the few words that must start at zero (per-conversation arrival
- *   counters) itself, in its first kernel.                                */
+ *   ordering) race on it and must be serialised by the caller.  No scratch
+ *   word needs to start at zero: each call writes what it reads.          */
 #define CART_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
 CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, int p, float scale,
                                       double rope_theta, const void* q, const void* k_new,

@@ -83,10 +83,13 @@ def test_noalloc_matches_workspace_decode_twice_in_a_row(lib):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
-    s = synth.DecodeShape("huge", B=512, Hq=32, Hkv=8, d=128, p=4096, max_private=4096, seed=1,
-                          fixed_len=tuple([0] * 512))
+    # 4096 conversations x 32 heads x 128 dims of rotated bf16 queries alone
+    # fill the 32 MiB scratch
+    nb = 4096
+    s = synth.DecodeShape("huge", B=nb, Hq=32, Hkv=8, d=128, p=4096, max_private=64, seed=1,
+                          fixed_len=tuple([0] * nb))
     t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
-    lens = torch.zeros(512, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(nb, dtype=torch.int32, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = lib.cart_attn_decode_noalloc(s.B, s.Hq, s.Hkv, s.d, s.p, s.scale, s.theta, _p(t), _p(t),
                                       _p(t), _p(t), _p(t), _p(t), _p(t), s.cache_rows, _p(lens),

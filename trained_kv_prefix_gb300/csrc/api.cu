@@ -432,8 +432,7 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
 namespace {
 
 struct DecodeWs {
-  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, counters = 0,
-         total = 0;
+  size_t q_rot = 0, cart_part = 0, cart_lse = 0, total = 0;
   int splits = 0, tiles_per_split = 0;
 };
 
@@ -443,14 +442,13 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
   const int R = B * (Hq / Hkv);
   const int qpairs = ((R + 127) / 128 + 1) / 2;  // the cartridge pass takes two row tiles per CTA
   if (n_ct > 0) {
-    // aim for about one CTA per SM for the cartridge part
+    // about kDecodeCartCtas CTAs for the cartridge part
     const long long units = static_cast<long long>(n_ct) * Hkv * qpairs;
-    int per = static_cast<int>((units + 147) / 148);
+    int per = static_cast<int>((units + kDecodeCartCtas - 1) / kDecodeCartCtas);
     if (per < 1) per = 1;
     w.tiles_per_split = per;
     w.splits = (n_ct + per - 1) / per;
   }
-  const int chunks = (rows + kDecodeChunk - 1) / kDecodeChunk;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -460,9 +458,6 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
   w.q_rot = take(static_cast<size_t>(B) * Hq * d * 2);
   w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
-  w.priv_part = take(static_cast<size_t>(B) * Hq * chunks * d * 4);
-  w.priv_ml = take(static_cast<size_t>(B) * Hq * chunks * 2 * 4);
-  w.counters = take(static_cast<size_t>(B) * Hkv * 4);
   w.total = off;
   return w;
 }
@@ -476,7 +471,7 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
   if (!std::isfinite(scale) || !(scale > 0.f) || !(theta > 0.0) || !std::isfinite(theta))
     return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
-  if ((rows + kDecodeChunk - 1) / kDecodeChunk > 256) return CART_ERR_GEOMETRY;  // <= 32768 rows
+  if (rows > 32768) return CART_ERR_GEOMETRY;
   return CART_OK;
 }
 }  // namespace
@@ -525,10 +520,6 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
   a.cart_tiles_per_split = w.tiles_per_split;
   a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
   a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
-  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
-  a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
-  a.counters = reinterpret_cast<int*>(ws + w.counters);
-  a.chunk = kDecodeChunk;
   CART_CUDA(launch_decode(a, make_rope_freqs(d, rope_theta), static_cast<cudaStream_t>(stream)));
   return CART_OK;
 }

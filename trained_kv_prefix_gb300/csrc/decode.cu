@@ -7,15 +7,16 @@
 //             reduction once per conversation) and lays the rotated queries
 //             out per kv head as [B*G rows, Hkv, d], so that the cartridge
 //             part runs as ONE tensor-core problem per kv head (rows of all
-//             conversations batched into M) -- see fwd.cu; zeroes the
-//             arrival counters.
-//   private   split-KV over each conversation's own rows 0..len[b]: TMA-staged
-//             chunks, mma.sync for the two small products, the new token's
-//             rotation and append fused in.  Bound by HBM.  Launched as the
-//             programmatic dependent of the cartridge pass, so the two run
-//             together; the last CTA of each (conversation, kv head) waits
-//             for the cartridge grid and merges all parts with their
-//             log-sum-exps.
+//             conversations batched into M) -- see fwd.cu.
+//   cartridge the forward kernel in decode mode over the shared rows, split
+//             into a few key ranges, writing normalised partial outputs and
+//             log-sum-exps (programmatic dependent of prep).
+//   private   one CTA per (conversation, kv head) streams the conversation's
+//             own rows 0..len[b] (the new token's rotation and append fused
+//             in), then merges with the cartridge splits.  Bound by HBM.
+//             Launched as the programmatic dependent of the cartridge pass,
+//             so the two run side by side; it waits for the cartridge grid
+//             only for the final merge.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +45,9 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
 // Rotated queries for the cartridge pass, laid out per kv head as
 // [B*G rows, Hkv, d] (row r = b*G + hh).  grid: B blocks; block: 128 threads.
 __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const RopeFreqs f) {
+  // the cartridge pass may start its set-up now; it waits for this grid
+  // before it loads the rotated queries
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float2 cs[kMaxHeadDim / 2];
   const int b = blockIdx.x;
   const int L = clamp_len(a.len, b, a.rows);
@@ -60,7 +64,6 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const 
     cs[threadIdx.x] = make_float2(c - s * rl, s + c * rl);
   }
   __syncthreads();
-  if (threadIdx.x < a.Hkv) a.counters[b * a.Hkv + threadIdx.x] = 0;
   if (a.p == 0) return;
   const int chunks = half / 8;  // 8 pair indices per task
   const int tasks = a.Hq * chunks;
@@ -87,123 +90,41 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const 
   }
 }
 
-constexpr int kPrivCH = kDecodeChunk;
-constexpr int kPrivMT = kPrivCH / 64;  // m16 key tiles per warp
-
-// ------------------------------------------------------------- combine ----
-// One warp merges the parts of one (conversation b, query head h); lane owns
-// d/32 dims.  All log-sum-exps are in the log2 domain.  Part p < S is
-// cartridge split p (normalised output, lse); part S + c is private chunk c
-// (unnormalised acc against m, sum l).  Partials written by other CTAs are
-// read through L2 (ld.global.cg).
-__device__ __forceinline__ void combine_head_warp(const DecodeLaunch& a, int b, int h, int lane) {
-  const int G = a.Hq / a.Hkv, g = h / G, hh = h % G;
-  const int d = a.d;
-  const int R = a.B * G, r = b * G + hh;
-  const int L = clamp_len(a.len, b, a.rows);
-  const int n_chunks = (a.rows + kPrivCH - 1) / kPrivCH;
-  const int S = a.n_cart_splits;
-  const int np = S + L / kPrivCH + 1;
-  const long long pbase = ((static_cast<long long>(b) * a.Hkv + g) * n_chunks) * G + hh;
-  auto part_lw = [&](int p, float* scale_m, float* lsum) {
-    if (p < S) {
-      *scale_m = __ldcg(a.cart_lse + (static_cast<long long>(p) * a.Hkv + g) * R + r);
-      *lsum = 1.f;
-      return *scale_m;
-    }
-    const long long pi = pbase + static_cast<long long>(p - S) * G;
-    *scale_m = __ldcg(a.priv_ml + pi * 2);
-    *lsum = __ldcg(a.priv_ml + pi * 2 + 1);
-    return *scale_m + __log2f(*lsum);
-  };
-  float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) {
-    float sm, ls;
-    M = fmaxf(M, part_lw(p, &sm, &ls));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float num[4] = {0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-  const int per_lane = d / 32;  // 4 or 2
-  for (int p0 = 0; p0 < np; p0 += 32) {
-    float w = 0.f, dn = 0.f;
-    if (p0 + lane < np) {
-      float sm, ls;
-      part_lw(p0 + lane, &sm, &ls);
-      w = exp2_approx(sm - M);   // scales the stored row
-      dn = w * ls;
-    }
-    const int cnt = min(32, np - p0);
-    // eight parts per round: all eight rows are requested before any is used
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int p = p0 + j0 + u;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j0 + u < cnt) {
-          const float* src = p < S
-              ? a.cart_part + ((static_cast<long long>(p) * a.Hkv + g) * R + r) * d
-              : a.priv_part + (pbase + static_cast<long long>(p - S) * G) * d;
-          if (per_lane == 4) {
-            v[u] = __ldcg(reinterpret_cast<const float4*>(src) + lane);
-          } else {
-            const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src) + lane);
-            v[u] = make_float4(t2.x, t2.y, 0.f, 0.f);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = min(j0 + u, 31);
-        const float wj = (j0 + u < cnt) ? __shfl_sync(0xffffffffu, w, j) : 0.f;
-        const float dj = __shfl_sync(0xffffffffu, dn, j);
-        if (j0 + u < cnt) den += dj;
-        num[0] = fmaf(wj, v[u].x, num[0]);
-        num[1] = fmaf(wj, v[u].y, num[1]);
-        num[2] = fmaf(wj, v[u].z, num[2]);
-        num[3] = fmaf(wj, v[u].w, num[3]);
-      }
-    }
-  }
-  const float inv = 1.f / den;
-  __nv_bfloat16* out = a.o + (static_cast<long long>(b) * a.Hq + h) * d + lane * per_lane;
-  if (per_lane == 4) {
-    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(num[0] * inv, num[1] * inv),
-                                                pack_bf16x2(num[2] * inv, num[3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(num[0] * inv, num[1] * inv);
-  }
-}
-
 // ------------------------------------------------------------- private ----
-// grid: (Hkv, chunks, B); block: 128 threads (4 warps).  Keys of the chunk:
-// private rows [c*CH, min((c+1)*CH, len+1)).
-//   * 16-byte cp.async copies stage the chunk's K and V rows in shared memory
-//     (128-byte swizzled layout, only the 16-row groups the chunk covers).
-//   * Meanwhile the block rotates the group's G queries at position p+len
-//     (one fp64-reduced cos/sin per frequency, shared through shared memory)
+// grid: (Hkv, B); block: 128 threads (4 warps).  CTA (g, slot) owns kv head g
+// of the conversation with the slot-th longest private length (longest
+// first, so that the short ones fill in behind), and streams that
+// conversation's rows 0..len through a 2-stage ring of 64-row chunks:
+//   * 16-byte cp.async copies stage a chunk's K and V rows in shared memory
+//     (128-byte swizzled layout; only the 16-row groups the chunk covers,
+//     rows past len zero-filled) while the previous chunk is computed.
+//   * The block rotates the group's G queries at position p+len (one
+//     fp64-reduced cos/sin per frequency, shared through shared memory)
 //     straight into mma.sync B fragments (queries padded to 8 columns).
-//   * The block whose chunk holds row len rotates the new key, writes it and
-//     the new value into the cache and patches its shared-memory copy.
-//   * S^T = K Q^T with mma.sync m16n8k16 (keys as M: warp w owns keys
-//     32w..32w+31), softmax statistics per query across the block, P (bf16)
-//     through shared memory, O^T = V^T P^T with V^T fragments read by
-//     ldmatrix.trans (warp w owns output dims 32w..32w+31).
-// Output per query head: unnormalised acc[d] against the chunk's own max m
-// (log2 domain) and its sum l.
+//   * The new token's key is rotated, written with its value into cache row
+//     len, and patched into the shared copy of the last chunk.
+//   * Per chunk: S^T = K Q^T with mma.sync m16n8k16 (keys as M: warp w owns
+//     keys 16w..16w+15), online softmax per query across the block, P (bf16)
+//     through shared memory, O^T += V^T P^T with V^T fragments read by
+//     ldmatrix.trans (warp w owns output dims 32w..32w+31), O kept in
+//     registers and rescaled when a query's running maximum grows.
+//   * Finally the block merges its (O, m, l) with the cartridge splits of
+//     the same query rows (normalised outputs with log-sum-exps, waited for
+//     through the grid dependency) and writes o.
+constexpr int kPrivCH = kDecodeChunk;  // keys per chunk
+constexpr int kPrivStages = 2;
 
 template <int D>
 struct PrivSmem {
-  static constexpr int kHalf = kPrivCH * 128;          // 64 dims x 128 rows (bf16)
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + (D / 64) * kHalf;
-  static constexpr int kP = kV + (D / 64) * kHalf;     // bf16 [8 queries][CH + 8]
+  static constexpr int kHalf = kPrivCH * 128;          // 64 dims x CH rows (bf16)
+  static constexpr int kTile = (D / 64) * kHalf;       // one K or V chunk
+  static constexpr int kStage = 2 * kTile;             // K then V
+  static constexpr int kP = kPrivStages * kStage;      // bf16 [8 queries][CH + 8]
   static constexpr int kPStride = kPrivCH + 8;         // padded row: conflict-free B loads
   static constexpr int kCS = kP + 8 * kPStride * 2;    // float2 [D/2]
   static constexpr int kRed = kCS + (D / 2) * 8;       // f32 [2][4 warps][8]
-  static constexpr int kBytes = kRed + 2 * 4 * 8 * 4;
+  static constexpr int kSlot = kRed + 2 * 4 * 8 * 4;   // int: this CTA's conversation
+  static constexpr int kBytes = kSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -229,7 +150,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 }
 
 // Address of the 16-byte chunk holding dims [8*dc, 8*dc + 8) of row `row` in a
-// TMA-written tile (two 64-dim halves, 128-byte swizzle).
+// staged chunk (64-dim halves of CH rows, 128-byte swizzle).
 __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int row, int dc) {
   return base + (dc >> 3) * (kPrivCH * 128) + row * 128 + ((((dc & 7) ^ (row & 7))) << 4);
 }
@@ -252,47 +173,67 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
   using L = PrivSmem<D>;
   constexpr int CH = kPrivCH;
   constexpr int HALF = D / 2;
+  static_assert(CH == 64, "four warps own 16 keys each");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(smem + L::kP);
   float2* scs = reinterpret_cast<float2*>(smem + L::kCS);
   float* sred = reinterpret_cast<float*>(smem + L::kRed);
-
-  // kv head fastest: the CTAs reading the interleaved head slices of the
-  // same cache rows run together (DRAM row locality)
-  const int g = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-  const int Lb = clamp_len(a.len, b, a.rows);
-  const int k0 = c * CH;
-  if (k0 > Lb) return;  // whole chunk beyond this conversation's rows
-  const int kn = min(CH, Lb + 1 - k0);
+  int* sslot = reinterpret_cast<int*>(smem + L::kSlot);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, tig = lane & 3;
-  const int pos = a.p + Lb;
-  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+  const int g = blockIdx.x;
 
-  // Stage the chunk's rows 0..16*ceil(kn/16) of K and V with 16-byte
-  // cp.async copies into the 128-byte-swizzled layout (rows >= kn of the last
-  // 16-row group are zero-filled, so P = 0 never meets stale data).
-  const int kgroups = (kn + 15) / 16;
-  {
+  // ---- this CTA's conversation: the one whose rank (longest first, ties by
+  // index) is blockIdx.y; in plain order past 256 conversations, where the
+  // quadratic ranking would cost more than it saves
+  if (a.B > 256 && tid == 0) *sslot = static_cast<int>(blockIdx.y);
+  for (int bb = tid; bb < a.B && a.B <= 256; bb += 128) {
+    const int Lb = clamp_len(a.len, bb, a.rows);
+    int rank = 0;
+    for (int o = 0; o < a.B; ++o) {
+      const int Lo = clamp_len(a.len, o, a.rows);
+      rank += (Lo > Lb) || (Lo == Lb && o < bb);
+    }
+    if (rank == static_cast<int>(blockIdx.y)) *sslot = bb;
+  }
+  __syncthreads();
+  const int b = *sslot;
+  const int Lb = clamp_len(a.len, b, a.rows);
+  const int nk = Lb + 1;                 // private rows 0..len
+  const int nc = (nk + CH - 1) / CH;     // chunks
+  const int pos = a.p + Lb;
+  const long long rstride = static_cast<long long>(a.Hkv) * D;
+  const __nv_bfloat16* kg0 = a.k_cache + static_cast<long long>(b) * a.rows * rstride + g * D;
+  const __nv_bfloat16* vg0 = a.v_cache + static_cast<long long>(b) * a.rows * rstride + g * D;
+  const uint32_t sbase = smem_u32(smem);
+
+  // Stage chunk c into ring slot c % 2: rows 0..16*ceil(kn/16) of K and V
+  // with 16-byte cp.async copies, rows >= kn of the last 16-row group
+  // zero-filled (so P = 0 never meets stale data).
+  auto stage = [&](int c) {
     constexpr int kPieces = D / 8;  // 16-byte pieces per row
-    const long long rstride = static_cast<long long>(a.Hkv) * D;
-    const __nv_bfloat16* kg = a.k_cache + (static_cast<long long>(b) * a.rows + k0) * rstride + g * D;
-    const __nv_bfloat16* vg = a.v_cache + (static_cast<long long>(b) * a.rows + k0) * rstride + g * D;
-    const uint32_t sKb = smem_u32(smem + L::kK), sVb = smem_u32(smem + L::kV);
-    for (int t = tid; t < kgroups * 16 * kPieces; t += 128) {
+    const int k0 = c * CH;
+    const int kn = min(CH, nk - k0);
+    const int rows16 = (kn + 15) & ~15;
+    const uint32_t sK = sbase + (c % kPrivStages) * L::kStage, sV = sK + L::kTile;
+    const __nv_bfloat16* kg = kg0 + static_cast<long long>(k0) * rstride;
+    const __nv_bfloat16* vg = vg0 + static_cast<long long>(k0) * rstride;
+    for (int t = tid; t < rows16 * kPieces; t += 128) {
       const int rr = t / kPieces, dc = t % kPieces;
       const uint32_t so = tile_chunk(0, rr, dc);
       const int src_bytes = rr < kn ? 16 : 0;
       const long long go = static_cast<long long>(min(rr, kn - 1)) * rstride + dc * 8;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sKb + so),
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sK + so),
                    "l"(kg + go), "r"(src_bytes) : "memory");
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sVb + so),
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sV + so),
                    "l"(vg + go), "r"(src_bytes) : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-  }
+  };
+  stage(0);
+  if (nc > 1) stage(1);
   if (tid < HALF) scs[tid] = rope_cs(f, tid, pos);
   __syncthreads();
 
@@ -326,10 +267,10 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = 16 * k + 8 * (e >> 1) + 2 * tig + (e & 1);
-        const float2 cs = scs[j];
-        const float x0 = qv[k][e], x1 = qv[k + D / 32][e];
-        qv[k][e] = x0 * cs.x - x1 * cs.y;
-        qv[k + D / 32][e] = x1 * cs.x + x0 * cs.y;
+        float y0, y1;
+        rope_pair(qv[k][e], qv[k + D / 32][e], scs[j], y0, y1);
+        qv[k][e] = y0;
+        qv[k + D / 32][e] = y1;
       }
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
@@ -337,163 +278,195 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
       bq[k][1] = pack_bf16x2(qv[k][2], qv[k][3]);
     }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
 
-  // ---- the new token: rotated key and value into the cache row len and
-  // into this block's shared copy (its chunk holds that row)
-  if (Lb - k0 < CH) {
-    const int rr = Lb - k0;
-    const long long crow = ((static_cast<long long>(b) * a.rows + Lb) * a.Hkv + g) * D;
-    const long long nrow = (static_cast<long long>(b) * a.Hkv + g) * D;
-    for (int j = tid; j < HALF; j += 128) {
-      const float x0 = __bfloat162float(a.k_new[nrow + j]);
-      const float x1 = __bfloat162float(a.k_new[nrow + j + HALF]);
-      const float2 cs = scs[j];
-      const __nv_bfloat16 y0 = __float2bfloat16_rn(x0 * cs.x - x1 * cs.y);
-      const __nv_bfloat16 y1 = __float2bfloat16_rn(x1 * cs.x + x0 * cs.y);
-      a.k_cache[crow + j] = y0;
-      a.k_cache[crow + j + HALF] = y1;
-      const int j1 = j + HALF;
-      *reinterpret_cast<__nv_bfloat16*>(smem + L::kK + (tile_chunk(0, rr, j >> 3)) + (j & 7) * 2) = y0;
-      *reinterpret_cast<__nv_bfloat16*>(smem + L::kK + (tile_chunk(0, rr, j1 >> 3)) + (j1 & 7) * 2) = y1;
-    }
-    for (int j = tid; j < D; j += 128) {
-      const __nv_bfloat16 v = a.v_new[nrow + j];
-      a.v_cache[crow + j] = v;
-      *reinterpret_cast<__nv_bfloat16*>(smem + L::kV + (tile_chunk(0, rr, j >> 3)) + (j & 7) * 2) = v;
-    }
+  // running statistics of this thread's queries 2tig, 2tig+1, and its O^T
+  // fragments: dims 16*dt + g8 (+8) for the warp's dim tiles dt
+  constexpr int kTilesPerWarp = D / 64;  // 2 (D = 128) or 1 (D = 64)
+  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+  float oacc[kTilesPerWarp][4];
+#pragma unroll
+  for (int i = 0; i < kTilesPerWarp; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
+
+  for (int c = 0; c < nc; ++c) {
+    if (c + 1 < nc)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-  }
-
-  // ---- S^T = K Q^T for this warp's keys (MT m16 tiles)
-  constexpr int MT = kPrivMT;
-  float sacc[MT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sacc[mt][e] = 0.f;
-    // lane -> row address: matrices (rows 0-7,k lo), (rows 8-15,k lo),
-    // (rows 0-7,k hi), (rows 8-15,k hi)
-    const int row = warp * 16 * MT + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      uint32_t af[4];
-      ldsm_x4(tile_chunk(sK, row, 2 * k + (lane >> 4)), af);
-      mma_bf16_16816(sacc[mt], af, bq[k][0], bq[k][1]);
+    const int k0 = c * CH;
+    const int kn = min(CH, nk - k0);
+    uint8_t* sKp = smem + (c % kPrivStages) * L::kStage;
+    const uint32_t sK = smem_u32(sKp), sV = sK + L::kTile;
+    // ---- the new token (row len) lives in the last chunk: rotated key and
+    // value into the cache and into the shared copy
+    if (c == nc - 1) {
+      const int rr = Lb - k0;
+      const long long crow = ((static_cast<long long>(b) * a.rows + Lb) * a.Hkv + g) * D;
+      const long long nrow = (static_cast<long long>(b) * a.Hkv + g) * D;
+      for (int j = tid; j < HALF; j += 128) {
+        float y0, y1;
+        rope_pair(__bfloat162float(a.k_new[nrow + j]), __bfloat162float(a.k_new[nrow + j + HALF]),
+                  scs[j], y0, y1);
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
+        a.k_cache[crow + j] = h0;
+        a.k_cache[crow + j + HALF] = h1;
+        const int j1 = j + HALF;
+        *reinterpret_cast<__nv_bfloat16*>(sKp + tile_chunk(0, rr, j >> 3) + (j & 7) * 2) = h0;
+        *reinterpret_cast<__nv_bfloat16*>(sKp + tile_chunk(0, rr, j1 >> 3) + (j1 & 7) * 2) = h1;
+      }
+      for (int j = tid; j < D; j += 128) {
+        const __nv_bfloat16 v = a.v_new[nrow + j];
+        a.v_cache[crow + j] = v;
+        *reinterpret_cast<__nv_bfloat16*>(sKp + L::kTile + tile_chunk(0, rr, j >> 3) + (j & 7) * 2) =
+            v;
+      }
+      __syncthreads();
     }
-  }
-  // thread holds keys r0 = warp*32 + mt*16 + g8 (+8) and queries 2tig, 2tig+1
-  float mq[2], lq[2];
+
+    // ---- S^T = K Q^T for this warp's 16 keys
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      // lane -> row address: matrices (rows 0-7,k lo), (rows 8-15,k lo),
+      // (rows 0-7,k hi), (rows 8-15,k hi)
+      const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {
-    float mx = -INFINITY;
+      for (int k = 0; k < D / 16; ++k) {
+        uint32_t af[4];
+        ldsm_x4(tile_chunk(sK, row, 2 * k + (lane >> 4)), af);
+        mma_bf16_16816(sacc, af, bq[k][0], bq[k][1]);
+      }
+    }
+    // thread holds keys warp*16 + g8 (+8) and queries 2tig, 2tig+1
+    float red[2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int qq = 0; qq < 2; ++qq) {
+      float mx = -INFINITY;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int key = warp * 16 * MT + mt * 16 + g8 + 8 * hf;
-        float sv = sacc[mt][2 * hf + qq] * scale_log2;
+        const int key = warp * 16 + g8 + 8 * hf;
+        float sv = sacc[2 * hf + qq] * scale_log2;
         sv = key < kn ? sv : -INFINITY;
-        sacc[mt][2 * hf + qq] = sv;
+        sacc[2 * hf + qq] = sv;
         mx = fmaxf(mx, sv);
       }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    mq[qq] = mx;
-  }
-  if (g8 == 0) {
-    sred[warp * 8 + 2 * tig] = mq[0];
-    sred[warp * 8 + 2 * tig + 1] = mq[1];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {
-    const int q = 2 * tig + qq;
-    mq[qq] = fmaxf(fmaxf(sred[q], sred[8 + q]), fmaxf(sred[16 + q], sred[24 + q]));
-    float sum = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int key = warp * 16 * MT + mt * 16 + g8 + 8 * hf;
-        const float pv = exp2_approx(sacc[mt][2 * hf + qq] - mq[qq]);  // 0 for masked keys
-        sum += pv;
-        sP[q * L::kPStride + key] = __float2bfloat16_rn(pv);
-      }
-    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-    lq[qq] = sum;
-  }
-  if (g8 == 0) {
-    sred[32 + warp * 8 + 2 * tig] = lq[0];
-    sred[32 + warp * 8 + 2 * tig + 1] = lq[1];
-  }
-  __syncthreads();
-  const int n_chunks = (a.rows + CH - 1) / CH;
-  const long long part_idx = ((static_cast<long long>(b) * a.Hkv + g) * n_chunks + c) * G;
-  if (warp == 0 && g8 == 0) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      red[qq] = mx;
+    }
+    if (g8 == 0) {
+      sred[warp * 8 + 2 * tig] = red[0];
+      sred[warp * 8 + 2 * tig + 1] = red[1];
+    }
+    __syncthreads();
+    float alpha[2];
 #pragma unroll
     for (int qq = 0; qq < 2; ++qq) {
       const int q = 2 * tig + qq;
-      if (q < G) {
-        const float lsum = (sred[32 + q] + sred[40 + q]) + (sred[48 + q] + sred[56 + q]);
-        a.priv_ml[(part_idx + q) * 2 + 0] = mq[qq];
-        a.priv_ml[(part_idx + q) * 2 + 1] = lsum;
+      const float cm = fmaxf(fmaxf(sred[q], sred[8 + q]), fmaxf(sred[16 + q], sred[24 + q]));
+      const float mnew = fmaxf(mrun[qq], cm);  // finite: every chunk holds a key
+      alpha[qq] = exp2_approx(mrun[qq] - mnew);  // 0 on the first chunk
+      mrun[qq] = mnew;
+      float sum = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int key = warp * 16 + g8 + 8 * hf;
+        const float pv = exp2_approx(sacc[2 * hf + qq] - mnew);  // 0 for masked keys
+        sum += pv;
+        sP[q * L::kPStride + key] = __float2bfloat16_rn(pv);
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      red[qq] = sum;  // this warp's partial row sum
+    }
+    if (g8 == 0) {
+      sred[32 + warp * 8 + 2 * tig] = red[0];
+      sred[32 + warp * 8 + 2 * tig + 1] = red[1];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      const int q = 2 * tig + qq;
+      const float cs = (sred[32 + q] + sred[40 + q]) + (sred[48 + q] + sred[56 + q]);
+      lrun[qq] = lrun[qq] * alpha[qq] + cs;
+    }
+
+    // ---- O^T = alpha O^T + V^T P^T: warp w owns dims 16*dt.. for its tiles
+    const int kgroups = (kn + 15) / 16;
+#pragma unroll
+    for (int i = 0; i < kTilesPerWarp; ++i) {
+      const int dt = warp * kTilesPerWarp + i;
+      oacc[i][0] *= alpha[0];
+      oacc[i][1] *= alpha[1];
+      oacc[i][2] *= alpha[0];
+      oacc[i][3] *= alpha[1];
+      // lane -> stored row (key) and dim chunk for the transposed matrices:
+      // m0 (dims lo, keys lo), m1 (dims hi, keys lo), m2 (dims lo, keys hi),
+      // m3 (dims hi, keys hi)
+      const int dchunk = 2 * dt + ((lane >> 3) & 1);
+      const int krow = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+      for (int k = 0; k < CH / 16; ++k) {
+        if (k >= kgroups) break;  // uniform across the block
+        uint32_t af[4];
+        ldsm_x4_t(tile_chunk(sV, 16 * k + krow, dchunk), af);
+        const uint32_t b0 =
+            *reinterpret_cast<const uint32_t*>(sP + g8 * L::kPStride + 16 * k + 2 * tig);
+        const uint32_t b1 =
+            *reinterpret_cast<const uint32_t*>(sP + g8 * L::kPStride + 16 * k + 8 + 2 * tig);
+        mma_bf16_16816(oacc[i], af, b0, b1);
       }
     }
+    __syncthreads();  // the ring slot, P and the reduction slots are free again
+    if (c + 2 < nc) stage(c + 2);
   }
 
-  // ---- O^T = V^T P^T: warp w owns dims 32w..32w+31 (two m16 tiles)
-  constexpr int kDimTiles = D / 16;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int dt = warp * 2 + i;
-    if (dt >= kDimTiles) break;
-    float oacc[4] = {0.f, 0.f, 0.f, 0.f};
-    // lane -> stored row (key) and dim chunk for the transposed matrices:
-    // m0 (dims lo, keys lo), m1 (dims hi, keys lo), m2 (dims lo, keys hi),
-    // m3 (dims hi, keys hi)
-    const int dchunk = 2 * dt + ((lane >> 3) & 1);
-    const int krow = (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-    for (int k = 0; k < CH / 16; ++k) {
-      if (k >= kgroups) break;  // uniform across the block
-      uint32_t af[4];
-      ldsm_x4_t(tile_chunk(sV, 16 * k + krow, dchunk), af);
-      const uint32_t b0 =
-          *reinterpret_cast<const uint32_t*>(sP + g8 * L::kPStride + 16 * k + 2 * tig);
-      const uint32_t b1 =
-          *reinterpret_cast<const uint32_t*>(sP + g8 * L::kPStride + 16 * k + 8 + 2 * tig);
-      mma_bf16_16816(oacc, af, b0, b1);
-    }
-    // oacc: dims 16dt + g8 (+8), queries 2tig, 2tig+1
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int q = 2 * tig + qq;
-        if (q < G) a.priv_part[(part_idx + q) * D + 16 * dt + g8 + 8 * hf] = oacc[2 * hf + qq];
-      }
-  }
-
-  // ---- the last private CTA of (b, g) merges every part of its G heads
-  __shared__ int s_last;
-  __threadfence();  // this CTA's partials are visible before it is counted
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(a.counters + b * a.Hkv + g, 1);
-    s_last = prev == Lb / CH;  // used chunks of this conversation = Lb/CH + 1
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  // ---- merge with the cartridge splits of the same query rows, write o
+  const int S = a.n_cart_splits;
   // the cartridge partials come from the grid this one depends on
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int hh = warp; hh < G; hh += 4) combine_head_warp(a, b, g * G + hh, lane);
-  if (tid == 0) a.counters[b * a.Hkv + g] = 0;
+  if (S > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int R = a.B * G;
+#pragma unroll
+  for (int qq = 0; qq < 2; ++qq) {
+    const int q = 2 * tig + qq;
+    if (q >= G) continue;
+    const int r = b * G + q;
+    // log-sum-exps (log2): the private part m + log2(l), split s cart_lse[s]
+    float M = mrun[qq] + __log2f(lrun[qq]);
+    for (int sp = 0; sp < S; ++sp)
+      M = fmaxf(M, __ldcg(a.cart_lse + (static_cast<long long>(sp) * a.Hkv + g) * R + r));
+    const float wp = exp2_approx(mrun[qq] - M);
+    float den = wp * lrun[qq];
+    float num[kTilesPerWarp][2];
+#pragma unroll
+    for (int i = 0; i < kTilesPerWarp; ++i) {
+      num[i][0] = wp * oacc[i][qq];
+      num[i][1] = wp * oacc[i][2 + qq];
+    }
+    for (int sp = 0; sp < S; ++sp) {
+      const long long rb = (static_cast<long long>(sp) * a.Hkv + g) * R + r;
+      const float ws = exp2_approx(__ldcg(a.cart_lse + rb) - M);
+      den += ws;
+      const float* part = a.cart_part + rb * D;
+#pragma unroll
+      for (int i = 0; i < kTilesPerWarp; ++i) {
+        const int dt = warp * kTilesPerWarp + i;
+        num[i][0] = fmaf(ws, __ldcg(part + 16 * dt + g8), num[i][0]);
+        num[i][1] = fmaf(ws, __ldcg(part + 16 * dt + g8 + 8), num[i][1]);
+      }
+    }
+    const float inv = 1.f / den;
+    __nv_bfloat16* out = a.o + (static_cast<long long>(b) * a.Hq + g * G + q) * D;
+#pragma unroll
+    for (int i = 0; i < kTilesPerWarp; ++i) {
+      const int dt = warp * kTilesPerWarp + i;
+      out[16 * dt + g8] = __float2bfloat16_rn(num[i][0] * inv);
+      out[16 * dt + g8 + 8] = __float2bfloat16_rn(num[i][1] * inv);
+    }
+  }
 }
 
 template <int D, int G>
@@ -503,7 +476,7 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
   cudaError_t e = set_smem_once<decode_private_kernel<D, G>>(L::kAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hkv, (a.rows + kPrivCH - 1) / kPrivCH, a.B);
+  cfg.gridDim = dim3(a.Hkv, a.B, 1);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = st;
@@ -521,7 +494,6 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
 
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
   const int G = a.Hq / a.Hkv;
-  if (a.chunk != kPrivCH) return cudaErrorInvalidValue;
   {
     TraceScope tr("decode_prep", st);
     decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
@@ -554,6 +526,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_
     l.out_f32 = true;
     l.lse = const_cast<float*>(a.cart_lse);
     l.decode = true;
+    l.pdl = true;
     e = launch_fwd(l, st);
     if (e != cudaSuccess) return e;
   }

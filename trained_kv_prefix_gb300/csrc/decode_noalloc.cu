@@ -16,10 +16,8 @@
 // that device current) and caches it; that first call should come before any
 // stream capture.  All calls share the one array: calls whose work overlaps
 // on the GPU (different streams, or different host threads without ordering)
-// race on it.  The only words that must start at zero (the per-conversation
-// arrival counters) are cleared at the start of every call by its first
-// kernel; every other scratch word a call reads is written earlier in the
-// same call.
+// race on it.  No scratch word needs to start at zero: every word a call
+// reads is written earlier in the same call.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,11 +34,8 @@ static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[CART_DEC
 namespace cart {
 namespace {
 
-constexpr int kNoallocChunk = kDecodeChunk;  // private keys per CTA
-
 struct NoallocLayout {
-  size_t q_rot = 0, cart_part = 0, cart_lse = 0, priv_part = 0, priv_ml = 0, counters = 0,
-         total = 0;
+  size_t q_rot = 0, cart_part = 0, cart_lse = 0, total = 0;
   int splits = 0, tiles_per_split = 0;
 };
 
@@ -53,12 +48,11 @@ NoallocLayout layout(int B, int Hq, int Hkv, int d, int p, int rows) {
   const int qpairs = ((R + 127) / 128 + 1) / 2;  // the cartridge pass takes two row tiles per CTA
   if (n_ct > 0) {
     const long long units = static_cast<long long>(n_ct) * Hkv * qpairs;
-    int per = static_cast<int>((units + 147) / 148);
+    int per = static_cast<int>((units + kDecodeCartCtas - 1) / kDecodeCartCtas);
     if (per < 1) per = 1;
     w.tiles_per_split = per;
     w.splits = (n_ct + per - 1) / per;
   }
-  const int chunks = (rows + kNoallocChunk - 1) / kNoallocChunk;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -68,9 +62,6 @@ NoallocLayout layout(int B, int Hq, int Hkv, int d, int p, int rows) {
   w.q_rot = take(static_cast<size_t>(B) * Hq * d * 2);
   w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
-  w.priv_part = take(static_cast<size_t>(B) * Hq * chunks * d * 4);
-  w.priv_ml = take(static_cast<size_t>(B) * Hq * chunks * 2 * 4);
-  w.counters = take(static_cast<size_t>(B) * Hkv * 4);
   w.total = off;
   return w;
 }
@@ -117,7 +108,7 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   if (!std::isfinite(scale) || !(scale > 0.f) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
     return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
-  if ((cache_rows + kNoallocChunk - 1) / kNoallocChunk > 256) return CART_ERR_GEOMETRY;
+  if (cache_rows > 32768) return CART_ERR_GEOMETRY;
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* ptr : ptrs)
     if (!ptr || !al16(ptr)) return CART_ERR_POINTER;
@@ -160,10 +151,6 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   a.cart_tiles_per_split = w.tiles_per_split;
   a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
   a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
-  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
-  a.priv_ml = reinterpret_cast<float*>(ws + w.priv_ml);
-  a.counters = reinterpret_cast<int*>(ws + w.counters);
-  a.chunk = kNoallocChunk;
   if (launch_decode(a, make_rope_freqs(d, rope_theta), st) != cudaSuccess) return CART_ERR_CUDA;
   return CART_OK;
 }

@@ -203,6 +203,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
       const int q0A = 2 * pair * kTile;
+      // decode mode: the queries come from the kernel this one depends on
+      if (a.decode) asm volatile("griddepcontrol.wait;" ::: "memory");
       mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
@@ -547,8 +549,17 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   else
     grid = dim3(a.Hq_map, p.n_pairs, a.n_splits);
   TraceScope tr(a.decode ? "decode_cartridge" : "fwd", st);
-  fwd_kernel<D><<<grid, kFwdThreads, L::kAlloc, st>>>(*a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kFwdThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fwd_kernel<D>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
 }
 
 }  // namespace

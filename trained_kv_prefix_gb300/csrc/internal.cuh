@@ -105,6 +105,9 @@ struct FwdLaunch {
   bool rotate_q;           // training: mQ holds unrotated bf16 queries; the kernel
                            // applies RoPE in shared memory using `table`
   const float2* table;     // rope table for positions p .. p+n-1 (rotate_q)
+  bool pdl;                // decode: launched as the programmatic dependent of
+                           // the kernel that writes its queries (waits for it
+                           // before loading Q)
 };
 // Two 128-row query tiles per CTA (training: consecutive row tiles of one
 // (sequence, head); decode: rows 0-127 / 128-255 of a kv head's stacked rows).
@@ -152,18 +155,17 @@ struct DecodeLaunch {
   int n_cart_splits;
   const float* cart_part;   // [S, Hkv, R, d]
   const float* cart_lse;    // [S, Hkv, R]
-  float* priv_part;         // [B, Hkv, chunks, G, d]
-  float* priv_ml;           // [B, Hkv, chunks, G, 2]
-  int* counters;            // [B, Hkv] arrivals of private chunks (zeroed by prep)
-  int chunk;                // private keys per CTA
   int cart_tiles_per_split; // cartridge tiles per split CTA
 };
 // The whole decode step on one stream: prep (rotated queries for the
-// cartridge pass, counters := 0), the cartridge split pass (fwd kernel in
-// decode mode), then the private pass launched as its programmatic dependent
-// (it overlaps the cartridge pass; the last private CTA of every
-// (conversation, kv head) waits for the cartridge grid and combines).
-constexpr int kDecodeChunk = 128;  // private keys per CTA
+// cartridge pass), the cartridge split pass (fwd kernel in decode mode,
+// programmatic dependent of prep), then the private pass launched as its
+// programmatic dependent (one CTA per (conversation, kv head); it runs next
+// to the cartridge pass and waits for that grid only for its final merge).
+constexpr int kDecodeChunk = 64;   // private keys per pipeline stage
+// The cartridge pass gets about this many CTAs (one SM each), so that the
+// private pass runs next to it on the remaining SMs.
+constexpr int kDecodeCartCtas = 32;
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
 }  // namespace cart
