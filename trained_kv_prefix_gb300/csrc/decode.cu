@@ -486,7 +486,6 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  TraceScope tr("decode_private", st);
   return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, a, f, scale_log2);
 }
 
@@ -494,10 +493,10 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
 
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
   const int G = a.Hq / a.Hkv;
-  {
-    TraceScope tr("decode_prep", st);
-    decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
-  }
+  // one trace scope for the whole step: events between the chained kernels
+  // would end their overlap
+  TraceScope tr("decode", st);
+  decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.p > 0) {

@@ -35,7 +35,9 @@ cudaError_t set_smem_once(int bytes) {
 uint32_t* device_status_ptr();
 
 // Launch tracing (trace.cu): brackets a launch with events on its stream
-// while tracing is enabled.
+// while tracing is enabled (a null name records nothing: kernels chained by
+// programmatic dependent launch are traced as one scope, since an event
+// between them would end the overlap).
 int trace_begin(const char* name, cudaStream_t st);
 void trace_end(int slot, cudaStream_t st);
 struct TraceScope {

@@ -29,7 +29,7 @@ constexpr size_t kMaxRecs = 1 << 16;
 }  // namespace
 
 int trace_begin(const char* name, cudaStream_t st) {
-  if (!g_on.load(std::memory_order_relaxed)) return -1;
+  if (!name || !g_on.load(std::memory_order_relaxed)) return -1;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_used >= kMaxRecs) return -1;
   if (g_used == g_recs.size()) {
