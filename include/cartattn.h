@@ -140,7 +140,8 @@ CART_API int cart_attn_bwd(const cart_geom* g, cart_dtype in_dtype, cart_dtype c
  *   k_cache, v_cache [B, cache_rows, Hkv, d] bf16 private caches; rows
  *          0..len[b]-1 hold already-rotated keys at positions p..p+len[b]-1
  *   priv_len [B] int32 (device): len[b], 0 <= len[b] < cache_rows (entries
- *          outside that range are clamped into it); cache_rows <= 32768
+ *          outside that range are clamped into it); cache_rows <= 32768 and
+ *          p + cache_rows < 2^24
  *   o      [B, Hq, d] bf16 (output)
  * The new token sits at position p + len[b]: its rotated key and its value
  * are written to private row len[b], then it attends to the p cartridge rows
@@ -163,8 +164,8 @@ CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale,
  *   Arguments, layouts and results are those of cart_attn_decode, without
  *   the workspace: the scratch is a static device array of
  *   CART_DECODE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the
- *   library holds until the process exits.  (The 64-conversation, p = 4096
- *   serving shape needs about 5 MiB.)
+ *   library holds until the process exits.  (The 64-conversation, p = 4096,
+ *   1025-row serving shape needs about 10 MiB.)
  *   Returns CART_ERR_WORKSPACE, without touching the device, when the
  *   problem needs more scratch than that; otherwise as cart_attn_decode.
  *   Calls no cudaMalloc / cudaFree or allocating library routine.

@@ -76,6 +76,19 @@ bool make_bf16_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, 
   return make_rows_map(m, base, blocks, rows, H, d, box_rows);
 }
 
+bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
+                    const uint64_t (&strides)[3], const uint32_t (&box)[4]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t ss[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t bb[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dd, ss, bb, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -432,8 +445,8 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
 namespace {
 
 struct DecodeWs {
-  size_t q_rot = 0, cart_part = 0, cart_lse = 0, total = 0;
-  int splits = 0, tiles_per_split = 0;
+  size_t cart_part = 0, cart_lse = 0, priv_part = 0, priv_lse = 0, total = 0;
+  int splits = 0, tiles_per_split = 0, max_units = 0;
 };
 
 DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
@@ -455,9 +468,11 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
     off += align256(bytes);
     return o;
   };
-  w.q_rot = take(static_cast<size_t>(B) * Hq * d * 2);
+  w.max_units = (rows + kDecodeUnit - 1) / kDecodeUnit;
   w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
+  w.priv_part = take(static_cast<size_t>(B) * Hq * w.max_units * d * 4);
+  w.priv_lse = take(static_cast<size_t>(B) * Hq * w.max_units * 4);
   w.total = off;
   return w;
 }
@@ -472,6 +487,9 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
     return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
   if (rows > 32768) return CART_ERR_GEOMETRY;
+  // positions p + len must be exact in f32 (the query rotation of the
+  // cartridge pass reduces its angles in f32)
+  if (static_cast<long long>(p) + rows >= (1ll << 24)) return CART_ERR_GEOMETRY;
   return CART_OK;
 }
 }  // namespace
@@ -515,11 +533,13 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
   a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
   a.len = priv_len;
   a.o = static_cast<__nv_bfloat16*>(o);
-  a.q_rot = reinterpret_cast<__nv_bfloat16*>(ws + w.q_rot);
   a.n_cart_splits = w.splits;
   a.cart_tiles_per_split = w.tiles_per_split;
   a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
   a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
+  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
+  a.priv_lse = reinterpret_cast<float*>(ws + w.priv_lse);
+  a.max_units = w.max_units;
   CART_CUDA(launch_decode(a, make_rope_freqs(d, rope_theta), static_cast<cudaStream_t>(stream)));
   return CART_OK;
 }

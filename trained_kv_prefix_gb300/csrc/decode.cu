@@ -2,21 +2,20 @@
 // (Cartridges guide, "Semantics", serving bullet: decoding continues at
 // position p with the training-time layout.)
 //
-// Work split:
-//   prep      rotates every query at position p + len[b] (fp64 angle
-//             reduction once per conversation) and lays the rotated queries
-//             out per kv head as [B*G rows, Hkv, d], so that the cartridge
-//             part runs as ONE tensor-core problem per kv head (rows of all
-//             conversations batched into M) -- see fwd.cu.
-//   cartridge the forward kernel in decode mode over the shared rows, split
-//             into a few key ranges, writing normalised partial outputs and
-//             log-sum-exps (programmatic dependent of prep).
-//   private   one CTA per (conversation, kv head) streams the conversation's
-//             own rows 0..len[b] (the new token's rotation and append fused
-//             in), then merges with the cartridge splits.  Bound by HBM.
-//             Launched as the programmatic dependent of the cartridge pass,
-//             so the two run side by side; it waits for the cartridge grid
-//             only for the final merge.
+// Work split (three kernels chained by programmatic dependent launch):
+//   cartridge the forward kernel in decode mode (fwd.cu): the B*G query rows
+//             of each kv head, rotated in shared memory at p + len[b], run as
+//             ONE tensor-core problem per kv head against the shared rows,
+//             split into a few key ranges; writes normalised partial outputs
+//             and log-sum-exps.  Launched first, on a few SMs.
+//   private   fixed units of up to kDecodeUnit private rows of one
+//             (conversation, kv head) per CTA: cp.async-staged 64-row chunks,
+//             mma.sync for the two small products, online softmax, the new
+//             token's rotation and append fused in; writes normalised partial
+//             outputs and log-sum-exps.  Bound by HBM; fills the GPU next to
+//             the cartridge pass.
+//   merge     combines the cartridge and private parts of every
+//             (conversation, query head) with their log-sum-exps into o.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,86 +30,26 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
   return L < 0 ? 0 : (L >= rows ? rows - 1 : L);
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
-  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    float2 t = __bfloat1622float2(p[e]);
-    f[2 * e] = t.x;
-    f[2 * e + 1] = t.y;
-  }
-}
-
-// ---------------------------------------------------------------- prep ----
-// Rotated queries for the cartridge pass, laid out per kv head as
-// [B*G rows, Hkv, d] (row r = b*G + hh).  grid: B blocks; block: 128 threads.
-__global__ void __launch_bounds__(128) decode_prep_kernel(DecodeLaunch a, const RopeFreqs f) {
-  // the cartridge pass may start its set-up now; it waits for this grid
-  // before it loads the rotated queries
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float2 cs[kMaxHeadDim / 2];
-  const int b = blockIdx.x;
-  const int L = clamp_len(a.len, b, a.rows);
-  const int d = a.d, half = d / 2, G = a.Hq / a.Hkv;
-  if (threadIdx.x < half) {
-    const double ang = static_cast<double>(a.p + L) * f.inv_freq[threadIdx.x];
-    const double k = rint(ang * 0.15915494309189535);
-    double r = fma(-k, 6.283185307179586232, ang);
-    r = fma(-k, 2.4492935982947064e-16, r);
-    const float rh = static_cast<float>(r);
-    const float rl = static_cast<float>(r - static_cast<double>(rh));
-    float s, c;
-    sincosf(rh, &s, &c);
-    cs[threadIdx.x] = make_float2(c - s * rl, s + c * rl);
-  }
-  __syncthreads();
-  if (a.p == 0) return;
-  const int chunks = half / 8;  // 8 pair indices per task
-  const int tasks = a.Hq * chunks;
-  for (int t = threadIdx.x; t < tasks; t += blockDim.x) {
-    const int h = t / chunks, j0 = (t % chunks) * 8;
-    const int g = h / G, hh = h % G;
-    const __nv_bfloat16* src = a.q + (static_cast<long long>(b) * a.Hq + h) * d;
-    __nv_bfloat16* dst = a.q_rot + (static_cast<long long>(b * G + hh) * a.Hkv + g) * d;
-    float x0[8], x1[8], y0[8], y1[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src + j0)), x0);
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(src + j0 + half)), x1);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 c = cs[j0 + e];
-      y0[e] = x0[e] * c.x - x1[e] * c.y;
-      y1[e] = x1[e] * c.x + x0[e] * c.y;
-    }
-    *reinterpret_cast<uint4*>(dst + j0) =
-        make_uint4(pack_bf16x2(y0[0], y0[1]), pack_bf16x2(y0[2], y0[3]),
-                   pack_bf16x2(y0[4], y0[5]), pack_bf16x2(y0[6], y0[7]));
-    *reinterpret_cast<uint4*>(dst + j0 + half) =
-        make_uint4(pack_bf16x2(y1[0], y1[1]), pack_bf16x2(y1[2], y1[3]),
-                   pack_bf16x2(y1[4], y1[5]), pack_bf16x2(y1[6], y1[7]));
-  }
-}
 
 // ------------------------------------------------------------- private ----
-// grid: (Hkv, B); block: 128 threads (4 warps).  CTA (g, slot) owns kv head g
-// of the conversation with the slot-th longest private length (longest
-// first, so that the short ones fill in behind), and streams that
-// conversation's rows 0..len through a 2-stage ring of 64-row chunks:
+// grid: (Hkv, B, max_units); block: 128 threads (4 warps).  CTA (g, b, u)
+// owns private rows [u*U, min((u+1)*U, len+1)) of kv head g of conversation
+// b (U = kDecodeUnit; CTAs past the end of a conversation exit at once) and
+// streams them through a 2-stage ring of 64-row chunks:
 //   * 16-byte cp.async copies stage a chunk's K and V rows in shared memory
 //     (128-byte swizzled layout; only the 16-row groups the chunk covers,
-//     rows past len zero-filled) while the previous chunk is computed.
+//     rows past the end zero-filled) while the previous chunk is computed.
 //   * The block rotates the group's G queries at position p+len (one
 //     fp64-reduced cos/sin per frequency, shared through shared memory)
 //     straight into mma.sync B fragments (queries padded to 8 columns).
-//   * The new token's key is rotated, written with its value into cache row
-//     len, and patched into the shared copy of the last chunk.
+//   * The CTA whose unit holds row len writes the new token's rotated key
+//     and its value into that cache row and patches its shared copy.
 //   * Per chunk: S^T = K Q^T with mma.sync m16n8k16 (keys as M: warp w owns
 //     keys 16w..16w+15), online softmax per query across the block, P (bf16)
 //     through shared memory, O^T += V^T P^T with V^T fragments read by
-//     ldmatrix.trans (warp w owns output dims 32w..32w+31), O kept in
-//     registers and rescaled when a query's running maximum grows.
-//   * Finally the block merges its (O, m, l) with the cartridge splits of
-//     the same query rows (normalised outputs with log-sum-exps, waited for
-//     through the grid dependency) and writes o.
+//     ldmatrix.trans (warp w owns output dims 16*dt.. of its tiles), O kept
+//     in registers and rescaled when a query's running maximum grows.
+//   * Output: the unit's normalised O and its log2-domain log-sum-exp.
 constexpr int kPrivCH = kDecodeChunk;  // keys per chunk
 constexpr int kPrivStages = 2;
 
@@ -123,8 +62,7 @@ struct PrivSmem {
   static constexpr int kPStride = kPrivCH + 8;         // padded row: conflict-free B loads
   static constexpr int kCS = kP + 8 * kPStride * 2;    // float2 [D/2]
   static constexpr int kRed = kCS + (D / 2) * 8;       // f32 [2][4 warps][8]
-  static constexpr int kSlot = kRed + 2 * 4 * 8 * 4;   // int: this CTA's conversation
-  static constexpr int kBytes = kSlot + 16;
+  static constexpr int kBytes = kRed + 2 * 4 * 8 * 4;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -174,39 +112,29 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
   constexpr int CH = kPrivCH;
   constexpr int HALF = D / 2;
   static_assert(CH == 64, "four warps own 16 keys each");
+  const int g = blockIdx.x, b = blockIdx.y, u = blockIdx.z;
+  const int Lb = clamp_len(a.len, b, a.rows);
+  const int k_lo = u * kDecodeUnit;
+  if (k_lo > Lb) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return;  // past the end of this conversation's rows
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(smem + L::kP);
   float2* scs = reinterpret_cast<float2*>(smem + L::kCS);
   float* sred = reinterpret_cast<float*>(smem + L::kRed);
-  int* sslot = reinterpret_cast<int*>(smem + L::kSlot);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, tig = lane & 3;
-  const int g = blockIdx.x;
-
-  // ---- this CTA's conversation: the one whose rank (longest first, ties by
-  // index) is blockIdx.y; in plain order past 256 conversations, where the
-  // quadratic ranking would cost more than it saves
-  if (a.B > 256 && tid == 0) *sslot = static_cast<int>(blockIdx.y);
-  for (int bb = tid; bb < a.B && a.B <= 256; bb += 128) {
-    const int Lb = clamp_len(a.len, bb, a.rows);
-    int rank = 0;
-    for (int o = 0; o < a.B; ++o) {
-      const int Lo = clamp_len(a.len, o, a.rows);
-      rank += (Lo > Lb) || (Lo == Lb && o < bb);
-    }
-    if (rank == static_cast<int>(blockIdx.y)) *sslot = bb;
-  }
-  __syncthreads();
-  const int b = *sslot;
-  const int Lb = clamp_len(a.len, b, a.rows);
-  const int nk = Lb + 1;                 // private rows 0..len
-  const int nc = (nk + CH - 1) / CH;     // chunks
+  const int nk = min(kDecodeUnit, Lb + 1 - k_lo);  // keys of this unit
+  const int nc = (nk + CH - 1) / CH;               // chunks
   const int pos = a.p + Lb;
   const long long rstride = static_cast<long long>(a.Hkv) * D;
-  const __nv_bfloat16* kg0 = a.k_cache + static_cast<long long>(b) * a.rows * rstride + g * D;
-  const __nv_bfloat16* vg0 = a.v_cache + static_cast<long long>(b) * a.rows * rstride + g * D;
+  const __nv_bfloat16* kg0 =
+      a.k_cache + (static_cast<long long>(b) * a.rows + k_lo) * rstride + g * D;
+  const __nv_bfloat16* vg0 =
+      a.v_cache + (static_cast<long long>(b) * a.rows + k_lo) * rstride + g * D;
   const uint32_t sbase = smem_u32(smem);
 
   // Stage chunk c into ring slot c % 2: rows 0..16*ceil(kn/16) of K and V
@@ -299,10 +227,10 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
     const int kn = min(CH, nk - k0);
     uint8_t* sKp = smem + (c % kPrivStages) * L::kStage;
     const uint32_t sK = smem_u32(sKp), sV = sK + L::kTile;
-    // ---- the new token (row len) lives in the last chunk: rotated key and
-    // value into the cache and into the shared copy
-    if (c == nc - 1) {
-      const int rr = Lb - k0;
+    // ---- the new token (row len) in this chunk: rotated key and value into
+    // the cache and into the shared copy
+    const int rr = Lb - (k_lo + k0);
+    if (rr >= 0 && rr < kn) {
       const long long crow = ((static_cast<long long>(b) * a.rows + Lb) * a.Hkv + g) * D;
       const long long nrow = (static_cast<long long>(b) * a.Hkv + g) * D;
       for (int j = tid; j < HALF; j += 128) {
@@ -394,7 +322,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
       lrun[qq] = lrun[qq] * alpha[qq] + cs;
     }
 
-    // ---- O^T = alpha O^T + V^T P^T: warp w owns dims 16*dt.. for its tiles
+    // ---- O^T = alpha O^T + V^T P^T
     const int kgroups = (kn + 15) / 16;
 #pragma unroll
     for (int i = 0; i < kTilesPerWarp; ++i) {
@@ -424,49 +352,28 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
     if (c + 2 < nc) stage(c + 2);
   }
 
-  // ---- merge with the cartridge splits of the same query rows, write o
-  const int S = a.n_cart_splits;
-  // the cartridge partials come from the grid this one depends on
-  if (S > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int R = a.B * G;
+  // ---- the unit's normalised output and log-sum-exp (log2)
+  const long long pidx = ((static_cast<long long>(b) * a.Hkv + g) * a.max_units + u) * G;
 #pragma unroll
   for (int qq = 0; qq < 2; ++qq) {
     const int q = 2 * tig + qq;
     if (q >= G) continue;
-    const int r = b * G + q;
-    // log-sum-exps (log2): the private part m + log2(l), split s cart_lse[s]
-    float M = mrun[qq] + __log2f(lrun[qq]);
-    for (int sp = 0; sp < S; ++sp)
-      M = fmaxf(M, __ldcg(a.cart_lse + (static_cast<long long>(sp) * a.Hkv + g) * R + r));
-    const float wp = exp2_approx(mrun[qq] - M);
-    float den = wp * lrun[qq];
-    float num[kTilesPerWarp][2];
-#pragma unroll
-    for (int i = 0; i < kTilesPerWarp; ++i) {
-      num[i][0] = wp * oacc[i][qq];
-      num[i][1] = wp * oacc[i][2 + qq];
-    }
-    for (int sp = 0; sp < S; ++sp) {
-      const long long rb = (static_cast<long long>(sp) * a.Hkv + g) * R + r;
-      const float ws = exp2_approx(__ldcg(a.cart_lse + rb) - M);
-      den += ws;
-      const float* part = a.cart_part + rb * D;
-#pragma unroll
-      for (int i = 0; i < kTilesPerWarp; ++i) {
-        const int dt = warp * kTilesPerWarp + i;
-        num[i][0] = fmaf(ws, __ldcg(part + 16 * dt + g8), num[i][0]);
-        num[i][1] = fmaf(ws, __ldcg(part + 16 * dt + g8 + 8), num[i][1]);
-      }
-    }
-    const float inv = 1.f / den;
-    __nv_bfloat16* out = a.o + (static_cast<long long>(b) * a.Hq + g * G + q) * D;
+    const float inv = 1.f / lrun[qq];
+    float* out = a.priv_part + (pidx + q) * D;
 #pragma unroll
     for (int i = 0; i < kTilesPerWarp; ++i) {
       const int dt = warp * kTilesPerWarp + i;
-      out[16 * dt + g8] = __float2bfloat16_rn(num[i][0] * inv);
-      out[16 * dt + g8 + 8] = __float2bfloat16_rn(num[i][1] * inv);
+      out[16 * dt + g8] = oacc[i][qq] * inv;
+      out[16 * dt + g8 + 8] = oacc[i][2 + qq] * inv;
     }
+    if (warp == 0 && g8 == 0) a.priv_lse[pidx + q] = mrun[qq] + __log2f(lrun[qq]);
   }
+  // The merge kernel may launch once every CTA of this grid is here.  One CTA
+  // also waits for the cartridge grid this one depends on, so that this
+  // grid's completion, which the merge kernel waits for, implies both.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (a.n_cart_splits > 0 && g == 0 && b == 0 && u == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, int G>
@@ -476,7 +383,7 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
   cudaError_t e = set_smem_once<decode_private_kernel<D, G>>(L::kAlloc);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hkv, a.B, 1);
+  cfg.gridDim = dim3(a.Hkv, a.B, a.max_units);
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = st;
@@ -489,19 +396,122 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
   return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, a, f, scale_log2);
 }
 
+// --------------------------------------------------------------- merge ----
+// grid: (Hkv, B); block: G warps; warp hh merges query head g*G + hh of
+// conversation b: cartridge splits s < S (cart_part / cart_lse) and private
+// units u < ceil((len+1)/U) (priv_part / priv_lse), all normalised outputs
+// with log2-domain log-sum-exps: o = sum_i 2^(lse_i - M) o_i / sum_i
+// 2^(lse_i - M).  Lane owns d/32 dims; parts go in rounds of 32 (one log-sum-
+// exp per lane), their rows 16 at a time, so a round costs three dependent
+// L2 trips.  Runs as the programmatic dependent of the private pass.
+template <int D>
+__global__ void decode_merge_kernel(DecodeLaunch a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int G = a.Hq / a.Hkv;
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = a.B * G, r = b * G + hh;
+  const int Lb = clamp_len(a.len, b, a.rows);
+  const int S = a.n_cart_splits;
+  const int np = S + Lb / kDecodeUnit + 1;
+  const long long pbase = (static_cast<long long>(b) * a.Hkv + g) * a.max_units * G + hh;
+  auto part_row = [&](int pt) -> const float* {
+    return pt < S ? a.cart_part + ((static_cast<long long>(pt) * a.Hkv + g) * R + r) * D
+                  : a.priv_part + (pbase + static_cast<long long>(pt - S) * G) * D;
+  };
+  auto part_lse = [&](int pt) -> float {
+    return pt < S ? __ldcg(a.cart_lse + (static_cast<long long>(pt) * a.Hkv + g) * R + r)
+                  : __ldcg(a.priv_lse + pbase + static_cast<long long>(pt - S) * G);
+  };
+  constexpr int PL = D / 32;  // dims per lane: 4 or 2
+  float M = -INFINITY, lse0 = -INFINITY;
+  for (int p0 = 0; p0 < np; p0 += 32)
+    if (p0 + lane < np) {
+      const float v = part_lse(p0 + lane);
+      if (p0 == 0) lse0 = v;
+      M = fmaxf(M, v);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    const bool have = p0 + lane < np;
+    const float lse = p0 == 0 ? lse0 : (have ? part_lse(p0 + lane) : -INFINITY);
+    const float w = have ? exp2_approx(lse - M) : 0.f;
+    den += w;
+    const int cnt = min(32, np - p0);
+    for (int j0 = 0; j0 < cnt; j0 += 16) {
+      float4 v[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 + t < cnt) {
+          const float* src = part_row(p0 + j0 + t);
+          if (PL == 4) {
+            v[t] = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+          } else {
+            const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src) + lane);
+            v[t] = make_float4(t2.x, t2.y, 0.f, 0.f);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + t) & 31);
+        if (j0 + t < cnt) {
+          num[0] = fmaf(wj, v[t].x, num[0]);
+          num[1] = fmaf(wj, v[t].y, num[1]);
+          num[2] = fmaf(wj, v[t].z, num[2]);
+          num[3] = fmaf(wj, v[t].w, num[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float inv = 1.f / den;
+  __nv_bfloat16* out = a.o + (static_cast<long long>(b) * a.Hq + g * G + hh) * D + lane * PL;
+  if (PL == 4)
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16x2(num[0] * inv, num[1] * inv),
+                                                pack_bf16x2(num[2] * inv, num[3] * inv));
+  else
+    *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(num[0] * inv, num[1] * inv);
+}
+
+template <int D>
+cudaError_t launch_merge_d(const DecodeLaunch& a, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hkv, a.B, 1);
+  cfg.blockDim = dim3(32 * (a.Hq / a.Hkv), 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, a);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st) {
   const int G = a.Hq / a.Hkv;
+  if (a.max_units != (a.rows + kDecodeUnit - 1) / kDecodeUnit) return cudaErrorInvalidValue;
   // one trace scope for the whole step: events between the chained kernels
   // would end their overlap
   TraceScope tr("decode", st);
-  decode_prep_kernel<<<a.B, 128, 0, st>>>(a, f);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   if (a.p > 0) {
+    // raw queries [B, Hkv, G, d] as (d, G, Hkv, B): a (64, G, 1, 128/G) box
+    // is 128 rows r = b*G + hh of one kv head
     CUtensorMap mQ, mKc, mVc;
-    if (!make_bf16_rows_map(&mQ, a.q_rot, 1, a.B * G, a.Hkv, a.d, 128) ||
+    const uint64_t e2 = 2;
+    const uint64_t qdims[4] = {static_cast<uint64_t>(a.d), static_cast<uint64_t>(G),
+                               static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.B)};
+    const uint64_t qstr[3] = {a.d * e2, static_cast<uint64_t>(G) * a.d * e2,
+                              static_cast<uint64_t>(a.Hkv) * G * a.d * e2};
+    const uint32_t qbox[4] = {64, static_cast<uint32_t>(G), 1, static_cast<uint32_t>(kTile / G)};
+    if (!make_bf16_map4(&mQ, a.q, qdims, qstr, qbox) ||
         !make_bf16_rows_map(&mKc, a.kc, 1, a.p, a.Hkv, a.d, 128) ||
         !make_bf16_rows_map(&mVc, a.vc, 1, a.p, a.Hkv, a.d, 128))
       return cudaErrorInvalidValue;
@@ -525,27 +535,34 @@ cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_
     l.out_f32 = true;
     l.lse = const_cast<float*>(a.cart_lse);
     l.decode = true;
-    l.pdl = true;
+    l.pdl = false;
+    l.dec_len = a.len;
+    l.dec_B = a.B;
+    l.dec_G = G;
+    l.dec_rows = a.rows;
+    l.freqs = &f;
     e = launch_fwd(l, st);
     if (e != cudaSuccess) return e;
   }
   const bool dep = a.p > 0;
+  e = cudaErrorInvalidValue;
   if (a.d == 128) {
     switch (G) {
-      case 1: return launch_private_dg<128, 1>(a, f, dep, st);
-      case 2: return launch_private_dg<128, 2>(a, f, dep, st);
-      case 4: return launch_private_dg<128, 4>(a, f, dep, st);
-      case 8: return launch_private_dg<128, 8>(a, f, dep, st);
+      case 1: e = launch_private_dg<128, 1>(a, f, dep, st); break;
+      case 2: e = launch_private_dg<128, 2>(a, f, dep, st); break;
+      case 4: e = launch_private_dg<128, 4>(a, f, dep, st); break;
+      case 8: e = launch_private_dg<128, 8>(a, f, dep, st); break;
     }
   } else if (a.d == 64) {
     switch (G) {
-      case 1: return launch_private_dg<64, 1>(a, f, dep, st);
-      case 2: return launch_private_dg<64, 2>(a, f, dep, st);
-      case 4: return launch_private_dg<64, 4>(a, f, dep, st);
-      case 8: return launch_private_dg<64, 8>(a, f, dep, st);
+      case 1: e = launch_private_dg<64, 1>(a, f, dep, st); break;
+      case 2: e = launch_private_dg<64, 2>(a, f, dep, st); break;
+      case 4: e = launch_private_dg<64, 4>(a, f, dep, st); break;
+      case 8: e = launch_private_dg<64, 8>(a, f, dep, st); break;
     }
   }
-  return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  return a.d == 128 ? launch_merge_d<128>(a, st) : launch_merge_d<64>(a, st);
 }
 
 }  // namespace cart

@@ -35,8 +35,8 @@ namespace cart {
 namespace {
 
 struct NoallocLayout {
-  size_t q_rot = 0, cart_part = 0, cart_lse = 0, total = 0;
-  int splits = 0, tiles_per_split = 0;
+  size_t cart_part = 0, cart_lse = 0, priv_part = 0, priv_lse = 0, total = 0;
+  int splits = 0, tiles_per_split = 0, max_units = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -59,9 +59,11 @@ NoallocLayout layout(int B, int Hq, int Hkv, int d, int p, int rows) {
     off += up256(bytes);
     return o;
   };
-  w.q_rot = take(static_cast<size_t>(B) * Hq * d * 2);
+  w.max_units = (rows + kDecodeUnit - 1) / kDecodeUnit;
   w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
+  w.priv_part = take(static_cast<size_t>(B) * Hq * w.max_units * d * 4);
+  w.priv_lse = take(static_cast<size_t>(B) * Hq * w.max_units * 4);
   w.total = off;
   return w;
 }
@@ -109,6 +111,7 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
     return CART_ERR_GEOMETRY;
   if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
   if (cache_rows > 32768) return CART_ERR_GEOMETRY;
+  if (static_cast<long long>(p) + cache_rows >= (1ll << 24)) return CART_ERR_GEOMETRY;
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* ptr : ptrs)
     if (!ptr || !al16(ptr)) return CART_ERR_POINTER;
@@ -146,11 +149,13 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
   a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
   a.len = priv_len;
   a.o = static_cast<__nv_bfloat16*>(o);
-  a.q_rot = reinterpret_cast<__nv_bfloat16*>(ws + w.q_rot);
   a.n_cart_splits = w.splits;
   a.cart_tiles_per_split = w.tiles_per_split;
   a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
   a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
+  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
+  a.priv_lse = reinterpret_cast<float*>(ws + w.priv_lse);
+  a.max_units = w.max_units;
   if (launch_decode(a, make_rope_freqs(d, rope_theta), st) != cudaSuccess) return CART_ERR_CUDA;
   return CART_OK;
 }

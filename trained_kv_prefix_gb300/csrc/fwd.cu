@@ -19,7 +19,9 @@
 //              (lazy rescaling, log2 domain).  P (bf16 pairs) goes back into
 //              TMEM over the first 64 columns of the tile's S.
 //              With rotate_q the group first applies RoPE to its Q tile in
-//              shared memory (real-token queries at positions p + i).
+//              shared memory (real-token queries at positions p + i); in
+//              decode mode it rotates the raw queries of row (b, hh) at
+//              p + len[b].
 //   warp 8     TMA producer: both Q tiles once, then K and V tiles into two
 //              separate 2-stage rings.
 //   warp 9     MMA issuer (one thread).  Per key tile t:
@@ -48,6 +50,10 @@ struct FwdParams {
   int rotate_q;
   const float2* table;  // rotate_q: cos/sin rows for positions p .. p + n_rows - 1
   uint32_t* status;
+  // decode mode: raw query rows r = b*G + hh, rotated here at p + len[b]
+  const int* dec_len;
+  int dec_B, dec_G, dec_rows;
+  float2 turns[kMaxHeadDim / 2];
 };
 
 constexpr int kFwdThreads = 320;
@@ -86,11 +92,12 @@ enum FwdBar {
 };
 static_assert(kNumBars * 8 + 4 <= 256, "barrier area");
 
-// RoPE of one Q row held in a 128-byte-swizzled tile, in place.  Rotate-half
-// pairs (c, c + D/2): for D = 128 chunk j of the first 64-wide block pairs
-// with chunk j of the second block; for D = 64 chunk j pairs with chunk j + 4.
-template <int D>
-__device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, const float2* tb) {
+// RoPE of one Q row held in a 128-byte-swizzled tile, in place; cs(j) gives
+// (cos, sin) of pair j.  Rotate-half pairs (c, c + D/2): for D = 128 chunk j
+// of the first 64-wide block pairs with chunk j of the second block; for
+// D = 64 chunk j pairs with chunk j + 4.
+template <int D, class CS>
+__device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, CS cs) {
 #pragma unroll
   for (int j = 0; j < D / 16; ++j) {
     const uint32_t o0 = sw128_offset(row, j);
@@ -104,8 +111,8 @@ __device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, const fl
     for (int e = 0; e < 4; ++e) {
       const float2 fa = bf16x2_to_float2(pa[e]);
       const float2 fb = bf16x2_to_float2(pb[e]);
-      const float2 c0 = __ldg(tb + 8 * j + 2 * e);
-      const float2 c1 = __ldg(tb + 8 * j + 2 * e + 1);
+      const float2 c0 = cs(8 * j + 2 * e);
+      const float2 c1 = cs(8 * j + 2 * e + 1);
       float y0a, y1a, y0b, y1b;
       rope_pair(fa.x, fb.x, c0, y0a, y1a);
       rope_pair(fa.y, fb.y, c1, y0b, y1b);
@@ -166,8 +173,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int T = max(T_A, T_B);
 
   if (threadIdx.x == 0) {
-    // decode mode: let the dependent private pass start right away (it only
-    // waits for this grid where it reads the cartridge partials)
+    // decode mode: let the dependent private pass start right away (one of
+    // its CTAs waits for this grid before that grid completes)
     if (a.decode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
@@ -203,15 +210,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
       const int q0A = 2 * pair * kTile;
-      // decode mode: the queries come from the kernel this one depends on
-      if (a.decode) asm volatile("griddepcontrol.wait;" ::: "memory");
       mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
-        tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, q0A, qb);
         // tile B of a lone last tile reads rows past the end: zero fill
-        tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, head,
-                    q0A + kTile, qb);
+        if (a.decode) {  // (d, G, Hkv, B) map, 128/G conversations per box
+          tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, 0, kvh,
+                      q0A / a.dec_G);
+          tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, 0,
+                      kvh, (q0A + kTile) / a.dec_G);
+        } else {
+          tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, q0A, qb);
+          tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, head,
+                      q0A + kTile, qb);
+        }
       }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
@@ -359,9 +371,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (a.rotate_q) {
         ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
+        const float2* tb = a.table + static_cast<long long>(i) * (D / 2);
         if (ok && i < a.n_rows)
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
-                          a.table + static_cast<long long>(i) * (D / 2));
+                          [&](int j) { return __ldg(tb + j); });
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kQReady0 + x]);
+      } else if (a.decode) {
+        // row i = b*G + hh of this kv head: its query at position p + len[b]
+        ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        const int bconv = i / a.dec_G;
+        if (ok && bconv < a.dec_B) {
+          int len = __ldg(a.dec_len + bconv);
+          len = len < 0 ? 0 : (len >= a.dec_rows ? a.dec_rows - 1 : len);
+          const int pos = a.p + len;
+          rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
+                          [&](int j) { return rope_cs_turns(a.turns[j], pos); });
+        }
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
       } else {
@@ -543,6 +570,13 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   p.rotate_q = a.rotate_q ? 1 : 0;
   p.table = a.table;
   p.status = device_status_ptr();
+  if (a.decode) {
+    p.dec_len = a.dec_len;
+    p.dec_B = a.dec_B;
+    p.dec_G = a.dec_G;
+    p.dec_rows = a.dec_rows;
+    for (int j = 0; j < kMaxHeadDim / 2; ++j) p.turns[j] = a.freqs->turns[j];
+  }
   dim3 grid;
   if (!a.decode)
     grid = dim3(static_cast<unsigned>(p.n_pairs) * a.Hq_map * a.n_qblocks, 1, 1);
@@ -566,6 +600,8 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
   if (a.rotate_q && (a.decode || !a.table)) return cudaErrorInvalidValue;
+  if (a.decode && (!a.dec_len || !a.freqs || a.dec_G < 1 || kTile % a.dec_G != 0))
+    return cudaErrorInvalidValue;
   if (a.d == 128) return launch_fwd_d<128>(a, st);
   if (a.d == 64) return launch_fwd_d<64>(a, st);
   return cudaErrorInvalidValue;

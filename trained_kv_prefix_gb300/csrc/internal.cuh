@@ -54,11 +54,35 @@ struct TraceScope {
 bool make_bf16_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, int H, int d,
                         unsigned box_rows);
 
-// fp64 inverse frequencies theta^(-2j/d), j < d/2, passed by value.
+// fp64 inverse frequencies theta^(-2j/d), j < d/2, passed by value, and the
+// same frequencies in turns per position, inv_freq / (2 pi), as an f32
+// (hi, lo) pair for the all-f32 angle reduction below.
 struct RopeFreqs {
   double inv_freq[kMaxHeadDim / 2];
+  float2 turns[kMaxHeadDim / 2];
 };
 RopeFreqs make_rope_freqs(int d, double theta);
+
+// (cos, sin) of pos * inv_freq with an all-f32 argument reduction, for
+// kernels that need many angles (fp64 is slow on this part).  The angle in
+// turns is pos * (hi + lo): pos * hi is split exactly into its rounded value
+// and the fma remainder (pos < 2^24 is exact in f32), the whole turns are
+// dropped from the rounded value (exact for |x| < 2^23), and the fraction
+// goes to sincospif.  Absolute error about 3e-7.
+__device__ __forceinline__ float2 rope_cs_turns(float2 turns, int pos) {
+  const float pf = static_cast<float>(pos);
+  const float th = pf * turns.x;
+  const float te = fmaf(pf, turns.x, -th);
+  const float r = (th - rintf(th)) + (te + pf * turns.y);
+  float s, c;
+  sincospif(2.f * r, &s, &c);
+  return make_float2(c, s);
+}
+
+// 4D bf16 TMA map with an arbitrary box and 128-byte swizzle; dims innermost
+// first, strides in bytes for dims 1..3 (api.cu).
+bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
+                    const uint64_t (&strides)[3], const uint32_t (&box)[4]);
 
 // ----------------------------------------------------------------- misc ----
 // f32 -> bf16 / f32 row copy into a strided destination.
@@ -107,9 +131,14 @@ struct FwdLaunch {
   bool rotate_q;           // training: mQ holds unrotated bf16 queries; the kernel
                            // applies RoPE in shared memory using `table`
   const float2* table;     // rope table for positions p .. p+n-1 (rotate_q)
-  bool pdl;                // decode: launched as the programmatic dependent of
-                           // the kernel that writes its queries (waits for it
-                           // before loading Q)
+  // decode mode: mQ maps the raw queries [B, Hkv, G, d] as (d, G, Hkv, B)
+  // with a (64, G, 1, 128/G) box, so that a 128-row tile is rows b*G + hh;
+  // the kernel rotates row (b, hh) at position p + len[b] in shared memory.
+  const int* dec_len;
+  int dec_B, dec_G, dec_rows;
+  const RopeFreqs* freqs;  // host copy, read at launch
+  bool pdl;                // launch as the programmatic dependent of the
+                           // previous kernel on the stream
 };
 // Two 128-row query tiles per CTA (training: consecutive row tiles of one
 // (sequence, head); decode: rows 0-127 / 128-255 of a kv head's stacked rows).
@@ -153,21 +182,25 @@ struct DecodeLaunch {
   __nv_bfloat16* v_cache;
   const int* len;
   __nv_bfloat16* o;
-  __nv_bfloat16* q_rot;     // [B*G, Hkv, d]: row r = b*G + hh of kv head g
   int n_cart_splits;
   const float* cart_part;   // [S, Hkv, R, d]
   const float* cart_lse;    // [S, Hkv, R]
   int cart_tiles_per_split; // cartridge tiles per split CTA
+  float* priv_part;         // [B, Hkv, units, G, d] normalised private partials
+  float* priv_lse;          // [B, Hkv, units, G] their log2-domain lse
+  int max_units;            // ceil(rows / kDecodeUnit)
 };
-// The whole decode step on one stream: prep (rotated queries for the
-// cartridge pass), the cartridge split pass (fwd kernel in decode mode,
-// programmatic dependent of prep), then the private pass launched as its
-// programmatic dependent (one CTA per (conversation, kv head); it runs next
-// to the cartridge pass and waits for that grid only for its final merge).
-constexpr int kDecodeChunk = 64;   // private keys per pipeline stage
+// The whole decode step on one stream, three kernels chained by
+// programmatic dependent launch: the cartridge split pass (fwd kernel in
+// decode mode, which rotates the queries itself) starts first on a few SMs;
+// the private pass (fixed units of kDecodeUnit private rows per CTA) fills
+// the rest of the GPU next to it; the merge kernel combines every
+// (conversation, head)'s parts once both are done.
+constexpr int kDecodeChunk = 64;    // private rows per pipeline stage
+constexpr int kDecodeUnit = 256;    // private rows per CTA
 // The cartridge pass gets about this many CTAs (one SM each), so that the
 // private pass runs next to it on the remaining SMs.
-constexpr int kDecodeCartCtas = 32;
+constexpr int kDecodeCartCtas = 48;
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
 }  // namespace cart

@@ -213,8 +213,12 @@ __global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restri
 
 RopeFreqs make_rope_freqs(int d, double theta) {
   RopeFreqs f{};
-  for (int j = 0; j < d / 2 && j < kMaxHeadDim / 2; ++j)
+  for (int j = 0; j < d / 2 && j < kMaxHeadDim / 2; ++j) {
     f.inv_freq[j] = std::pow(theta, -2.0 * static_cast<double>(j) / static_cast<double>(d));
+    const double t = f.inv_freq[j] / 6.283185307179586476925;
+    const float hi = static_cast<float>(t);
+    f.turns[j] = make_float2(hi, static_cast<float>(t - static_cast<double>(hi)));
+  }
   return f;
 }
 
