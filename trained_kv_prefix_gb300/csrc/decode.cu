@@ -35,7 +35,7 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 // grid: (Hkv, B, max_units); block: 128 threads (4 warps).  CTA (g, b, u)
 // owns private rows [u*U, min((u+1)*U, len+1)) of kv head g of conversation
 // b (U = kDecodeUnit; CTAs past the end of a conversation exit at once) and
-// streams them through a 2-stage ring of 64-row chunks:
+// streams them through a kPrivStages-deep ring of 64-row chunks:
 //   * 16-byte cp.async copies stage a chunk's K and V rows in shared memory
 //     (128-byte swizzled layout; only the 16-row groups the chunk covers,
 //     rows past the end zero-filled) while the previous chunk is computed.
@@ -52,6 +52,7 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 //   * Output: the unit's normalised O and its log2-domain log-sum-exp.
 constexpr int kPrivCH = kDecodeChunk;  // keys per chunk
 constexpr int kPrivStages = 2;
+static_assert(kPrivStages >= 1 && kPrivStages <= 4, "cp.async.wait_group counts below");
 
 template <int D>
 struct PrivSmem {
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
       a.v_cache + (static_cast<long long>(b) * a.rows + k_lo) * rstride + g * D;
   const uint32_t sbase = smem_u32(smem);
 
-  // Stage chunk c into ring slot c % 2: rows 0..16*ceil(kn/16) of K and V
+  // Stage chunk c into ring slot c % kPrivStages: rows 0..16*ceil(kn/16) of K and V
   // with 16-byte cp.async copies, rows >= kn of the last 16-row group
   // zero-filled (so P = 0 never meets stale data).
   auto stage = [&](int c) {
@@ -160,8 +161,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  stage(0);
-  if (nc > 1) stage(1);
+  for (int c = 0; c < kPrivStages && c < nc; ++c) stage(c);
   if (tid < HALF) scs[tid] = rope_cs(f, tid, pos);
   __syncthreads();
 
@@ -218,7 +218,14 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
     for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
 
   for (int c = 0; c < nc; ++c) {
-    if (c + 1 < nc)
+    // chunk c has landed once at most (chunks staged after it) groups are
+    // still pending
+    const int younger = min(kPrivStages - 1, nc - 1 - c);
+    if (younger >= 3)
+      asm volatile("cp.async.wait_group 3;" ::: "memory");
+    else if (younger == 2)
+      asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else if (younger == 1)
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     else
       asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
       }
     }
     __syncthreads();  // the ring slot, P and the reduction slots are free again
-    if (c + 2 < nc) stage(c + 2);
+    if (c + kPrivStages < nc) stage(c + kPrivStages);
   }
 
   // ---- the unit's normalised output and log-sum-exp (log2)

@@ -492,42 +492,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool row_ok = i < a.n_rows;
+      const bool f32 = a.decode || a.out_f32;
+      // Each warp turns its 32 rows x 32 columns at a time around through a
+      // 4 KB slice of its tile's Q buffer (every MMA that read Q_x is done),
+      // so that global stores cover whole 32-byte sectors: 16-byte granule
+      // k of staged row r sits at r*128 + (k ^ (r & 7))*16.
+      uint8_t* stg = smem + L::kQ + x * L::kTileBytes + (warp & 3) * 4096;
+      const int gpr = f32 ? 8 : 4;  // 16-byte granules per row and 32 columns
+      const int row0 = (2 * pair + x) * kTile + (warp & 3) * 32;
 #pragma unroll
       for (int blk = 0; blk < D / 32; ++blk) {
         uint32_t o[32];
-        const int col = blk * 32;
-        tmem_ld32(tO + col, o);
+        tmem_ld32(tO + blk * 32, o);
         tmem_ld_wait();
         tmem_reg_fence(o);
-        if (row_ok) {
-          if (a.decode || a.out_f32) {
-            float* dst;
+        uint8_t* my = stg + lane * 128;
+        if (f32) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(my + ((k ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                            __uint_as_float(o[4 * k + 2]) * inv_l,
+                            __uint_as_float(o[4 * k + 3]) * inv_l);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(my + ((k ^ (lane & 7)) << 4)) = make_uint4(
+                pack_bf16x2(__uint_as_float(o[8 * k]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
+        }
+        __syncwarp();
+        for (int st = 0; st < gpr; ++st) {
+          const int gi = st * 32 + lane;
+          const int r = gi / gpr, k = gi % gpr;
+          const int grow = row0 + r;
+          if (grow < a.n_rows) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
+            long long off;  // element offset of the row
             if (a.decode)
-              dst = static_cast<float*>(a.out) +
-                    ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i) * D;
+              off = ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + grow) * D;
             else
-              dst = static_cast<float*>(a.out) +
-                    ((static_cast<long long>(qb) * a.n_rows + i) * a.Hq_map + head) * D;
-            float4* d4 = reinterpret_cast<float4*>(dst + col);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              d4[c] = make_float4(__uint_as_float(o[4 * c]) * inv_l,
-                                  __uint_as_float(o[4 * c + 1]) * inv_l,
-                                  __uint_as_float(o[4 * c + 2]) * inv_l,
-                                  __uint_as_float(o[4 * c + 3]) * inv_l);
-          } else {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                 ((static_cast<long long>(qb) * a.n_rows + i) * a.Hq_map + head) * D;
-            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              d4[c] = make_uint4(
-                  pack_bf16x2(__uint_as_float(o[8 * c]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l));
+              off = ((static_cast<long long>(qb) * a.n_rows + grow) * a.Hq_map + head) * D;
+            if (f32)
+              *reinterpret_cast<uint4*>(static_cast<float*>(a.out) + off + blk * 32 + k * 4) = v;
+            else
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off + blk * 32 + k * 8) =
+                  v;
           }
         }
+        __syncwarp();
       }
       if (row_ok) {
         const float lse2 = m + __log2f(l);
