@@ -68,13 +68,13 @@ def load_peaks():
 
 def kernel_src_sha(name: str) -> str:
     csrc = os.path.join(ROOT, "trained_kv_prefix_gb300", "csrc")
-    files = {"bwd_dkdv": "bwd.cu", "bwd_dq": "bwd.cu", "fwd": "fwd.cu",
-             "decode": "decode.cu"}
+    files = {"bwd_dkdv": ["bwd.cu"], "bwd_dq": ["bwd.cu"], "fwd": ["fwd.cu"],
+             "decode": ["decode.cu", "fwd.cu"]}
     f = files.get(name)
     if f is None:
         return ""
     h = hashlib.sha256()
-    for part in (f, "ptx.cuh"):
+    for part in f + ["ptx.cuh", "internal.cuh"]:
         with open(os.path.join(csrc, part), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
