@@ -275,17 +275,31 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idST, 1u);
         }
       };
-      bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma);
+      // Issue order per step u: dV(u), S^T(u+1), dK(u), dP^T(u+1).  S^T(u+1)
+      // overwrites the P^T(u) that dV(u) reads and dP^T(u+1) the dS^T(u)
+      // that dK(u) reads; one CTA's MMAs run in issue order, so each comes
+      // after its reader, and the warpgroups form P^T(u+1) while dK(u) and
+      // dP^T(u+1) run.
+      auto issue_st_dpt = [&](int u, bool st) {
+        const uint32_t so = (u % S) * kStageBytes;
+        if (st) {
+          issue_nt(tST, dK0, desc_add(dQk0, so));
+          umma_commit(&bars[kStFull]);
+        } else {
+          issue_nt(tDP, dV0, desc_add(dQk0, so + L::kTileBytes));
+          umma_commit(&bars[kDpTFull]);
+        }
+      };
+      bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma) &&
+                mbar_wait(&bars[kQdoFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      if (ok) {
+        tc_fence_after();
+        issue_st_dpt(0, true);
+        issue_st_dpt(0, false);
+      }
       for (int u = 0; u < U && ok; ++u) {
         const int s = u % S;
-        ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status, kDevErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
         const uint32_t so = s * kStageBytes;
-        issue_nt(tST, dK0, desc_add(dQk0, so));
-        umma_commit(&bars[kStFull]);
-        issue_nt(tDP, dV0, desc_add(dQk0, so + L::kTileBytes));
-        umma_commit(&bars[kDpTFull]);
         ok = mbar_wait(&bars[kDsFull], u & 1, abort_p, a.status, kDevErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
@@ -294,14 +308,23 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kTileBytes);
         const uint32_t first = u > 0 ? 1u : 0u;
         umma_bf16_ts(tDV, tST, ddo, idACC, first);
+#pragma unroll
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ts(tDV, tST + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC, 1u);
+        const bool next = u + 1 < U;
+        if (next) {
+          ok = mbar_wait(&bars[kQdoFull0 + (u + 1) % S], ((u + 1) / S) & 1, abort_p, a.status,
+                         kDevErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_st_dpt(u + 1, true);
+        }
         umma_bf16_ts(tDK, tDP, dq, idACC, first);
 #pragma unroll
-        for (int k = 1; k < kTile / 16; ++k) {
-          const uint32_t ac = (k >> 1) * 32 + (k & 1) * 8;
-          umma_bf16_ts(tDV, tST + ac, desc_add(ddo, k * 2048), idACC, 1u);
-          umma_bf16_ts(tDK, tDP + ac, desc_add(dq, k * 2048), idACC, 1u);
-        }
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ts(tDK, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC, 1u);
         umma_commit(&bars[kQdoEmpty0 + s]);
+        if (next) issue_st_dpt(u + 1, false);
       }
       if (ok) umma_commit(&bars[kAccDone]);
       umma_commit(&bars[kDkdvDrain]);
