@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       // all for rows past the end of the keys
       const int qlim =
           !key_ok ? 32 : (cart ? 0 : max(0, min(32, j - it.qt * kTile - wg * 32)));
-      const float4* lse4 = reinterpret_cast<const float4*>(vec + s * 256 + wg * 32);
-      const float4* dv4 = reinterpret_cast<const float4*>(vec + s * 256 + 128 + wg * 32);
+      const uint32_t lse_s = smem_u32(vec + s * 256 + wg * 32);
+      const uint32_t dv_s = smem_u32(vec + s * 256 + 128 + wg * 32);
       uint32_t r[32];
       tmem_ld32(tst, r);
       tmem_ld_wait();
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const bool masked = __any_sync(0xffffffffu, qlim > 0);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l4 = lse4[c4];
+        const float4 l4 = lds128(lse_s + c4 * 16);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_reg_fence(dr);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 d4 = dv4[c4];
+        const float4 d4 = lds128(dv_s + c4 * 16);
         const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
         float ds[4];
 #pragma unroll

@@ -68,6 +68,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with an explicit suspend-time hint: a thread whose phase has not
+// completed sleeps (instead of polling) until the phase completes or about
+// `ns` nanoseconds pass, leaving its issue slots to the other warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  `abort` is a
 // CTA-shared flag: once any role of the CTA has given up, the others stop
 // waiting too.  Returns false on timeout or abort (and then sets both flags).
@@ -76,14 +90,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs || it > (1u << 30)) {
-        *abort = 1;
-        if (status) atomicOr(status, err_bit);
-        return false;
-      }
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs || it > (1u << 30)) {
+      *abort = 1;
+      if (status) atomicOr(status, err_bit);
+      return false;
     }
   }
 }
@@ -110,6 +122,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
       "r"(c3)
       : "memory");
+}
+
+// 16-byte load from shared memory by shared-window address.
+__device__ __forceinline__ float4 lds128(uint32_t saddr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(saddr));
+  return v;
 }
 
 // Plain (untiled) bulk copy global -> shared completing on an mbarrier: both
