@@ -61,7 +61,7 @@ typedef enum cart_dtype { CART_BF16 = 0, CART_F32 = 1 } cart_dtype;
 
 /* Geometry of one training-shape call.
  *   B      independent sequences sharing ONE cartridge (the packed group)
- *   n      real tokens per sequence (q_seq); kv_seq = p + n
+ *   n      real tokens per sequence (q_seq); kv_seq = p + n < 2^24
  *   Hq     query heads;  Hkv  kv heads;  Hq % Hkv == 0
  *   d      head dimension, 64 or 128
  *   p      cartridge rows INCLUDING the frozen sink rows (p >= 0)

@@ -139,6 +139,8 @@ int check_geom(const cart_geom* g) {
       !std::isfinite(g->rope_theta))
     return CART_ERR_GEOMETRY;
   if (g->B > 65535 || g->Hq > 65535 || (g->n + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
+  // RoPE positions p + i are reduced in f32 and must be exact there
+  if (static_cast<long long>(g->p) + g->n >= (1ll << 24)) return CART_ERR_GEOMETRY;
   return CART_OK;
 }
 
@@ -199,22 +201,43 @@ struct TrainPrep {
   CUtensorMap mQ, mK, mV, mKc, mVc;
 };
 
+// The backward's per-row vectors, produced by the same prep launch for bf16
+// inputs (o == nullptr: none).
+struct PrepVec {
+  const void* o = nullptr;
+  const void* dout = nullptr;
+  const float* lse = nullptr;
+  float* Dvec = nullptr;
+  float* lse2 = nullptr;
+  int npad = 0;
+};
+
 // With q_in_kernel (bf16 queries only) Q is left unrotated: mQ maps q itself
-// and the forward kernel rotates each tile in shared memory.
+// and the forward kernel rotates each tile in shared memory.  bf16 inputs
+// take one fused launch (table, K, Q, backward vectors); f32 inputs take the
+// generic kernels and the caller computes the vectors.
 int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
                const void* v, const void* kc, const void* vc, uint8_t* ws, const TrainWs& w,
-               cudaStream_t st, TrainPrep* out, bool q_in_kernel = false) {
+               cudaStream_t st, TrainPrep* out, bool q_in_kernel = false,
+               const PrepVec& vec = PrepVec()) {
   const bool f32 = in == CART_F32;
   if (f32) q_in_kernel = false;
   float2* table = reinterpret_cast<float2*>(ws + w.table);
   __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(ws + w.qr);
   __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(ws + w.kr);
-  CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, make_rope_freqs(g->d, g->rope_theta), st));
-  if (q_in_kernel)
-    qr = static_cast<__nv_bfloat16*>(const_cast<void*>(q));
-  else
+  const RopeFreqs freqs = make_rope_freqs(g->d, g->rope_theta);
+  if (!f32) {
+    CART_CUDA(launch_train_prep(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+        q_in_kernel ? nullptr : qr, kr, table, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
+        static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
+        vec.lse, vec.Dvec, vec.lse2, vec.npad, st));
+    if (q_in_kernel) qr = static_cast<__nv_bfloat16*>(const_cast<void*>(q));
+  } else {
+    CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, freqs, st));
     CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, st));
-  CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, st));
+    CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, st));
+  }
   const void* vb = v;
   if (f32) {
     __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.vb);
@@ -227,8 +250,8 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
     __nv_bfloat16* tk = reinterpret_cast<__nv_bfloat16*>(ws + w.kcb);
     __nv_bfloat16* tv = reinterpret_cast<__nv_bfloat16*>(ws + w.vcb);
     const int row = g->Hkv * g->d;
-    CART_CUDA(launch_write_to_cache(static_cast<const float*>(kc), g->p, row, tk, row, 0, true, st));
-    CART_CUDA(launch_write_to_cache(static_cast<const float*>(vc), g->p, row, tv, row, 0, true, st));
+    CART_CUDA(launch_write_to_cache(static_cast<const float*>(kc), tk, static_cast<const float*>(vc),
+                                    tv, g->p, row, row, 0, true, st));
     kcb = tk;
     vcb = tv;
   }
@@ -308,12 +331,9 @@ int cart_write_to_cache(const float* kc, const float* vc, int p, int Hkv, int d,
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = dst_dtype == CART_BF16;
-  if (kc && k_dst)
-    CART_CUDA(launch_write_to_cache(kc, p, static_cast<int>(row), k_dst, row_stride_elems,
-                                    dst_row0, bf16, st));
-  if (vc && v_dst)
-    CART_CUDA(launch_write_to_cache(vc, p, static_cast<int>(row), v_dst, row_stride_elems,
-                                    dst_row0, bf16, st));
+  CART_CUDA(launch_write_to_cache(kc && k_dst ? kc : nullptr, kc && k_dst ? k_dst : nullptr,
+                                  vc && v_dst ? vc : nullptr, vc && v_dst ? v_dst : nullptr, p,
+                                  static_cast<int>(row), row_stride_elems, dst_row0, bf16, st));
   return CART_OK;
 }
 
@@ -386,18 +406,27 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   TrainPrep tp;
-  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp);
-  if (rc) return rc;
   const bool f32 = in == CART_F32;
+  float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  PrepVec vec;  // bf16: the per-row vectors come out of the same prep launch
+  if (!f32) {
+    vec.o = o;
+    vec.dout = dout;
+    vec.lse = lse;
+    vec.Dvec = Dvec;
+    vec.lse2 = lse2;
+    vec.npad = w.npad;
+  }
+  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp, false, vec);
+  if (rc) return rc;
   const void* dob = dout;
   if (f32) {
     __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.dob);
     CART_CUDA(launch_rope_rows(dout, true, t, tp.table, g->B, g->n, g->Hq, g->d, false, st));
     dob = t;
+    CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
   }
-  float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
   CUtensorMap mdO;
   if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
   BwdLaunch l{};

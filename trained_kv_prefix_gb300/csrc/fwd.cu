@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           len = len < 0 ? 0 : (len >= a.dec_rows ? a.dec_rows - 1 : len);
           const int pos = a.p + len;
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
-                          [&](int j) { return rope_cs_turns(a.turns[j], pos); });
+                          [&](int j) { return rope_cs_turns_fast(a.turns[j], pos); });
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);

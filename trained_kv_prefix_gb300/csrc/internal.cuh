@@ -68,15 +68,24 @@ RopeFreqs make_rope_freqs(int d, double theta);
 // turns is pos * (hi + lo): pos * hi is split exactly into its rounded value
 // and the fma remainder (pos < 2^24 is exact in f32), the whole turns are
 // dropped from the rounded value (exact for |x| < 2^23), and the remaining
-// fraction, an angle in [-pi, pi], goes to the hardware sine / cosine.
-// Absolute error about 5e-7.
-__device__ __forceinline__ float2 rope_cs_turns(float2 turns, int pos) {
+// fraction r in [-1/2, 1/2] is what is left to evaluate.
+__device__ __forceinline__ float rope_turn_fraction(float2 turns, int pos) {
   const float pf = static_cast<float>(pos);
   const float th = pf * turns.x;
   const float te = fmaf(pf, turns.x, -th);
-  const float r = (th - rintf(th)) + (te + pf * turns.y);
+  return (th - rintf(th)) + (te + pf * turns.y);
+}
+// ... with sincospif (error about 2e-7 in all): the training table.
+__device__ __forceinline__ float2 rope_cs_turns(float2 turns, int pos) {
   float s, c;
-  __sincosf(6.28318530717958648f * r, &s, &c);
+  sincospif(2.f * rope_turn_fraction(turns, pos), &s, &c);
+  return make_float2(c, s);
+}
+// ... with the hardware sine / cosine (error about 5e-7): the many per-row
+// angles of the decode cartridge pass.
+__device__ __forceinline__ float2 rope_cs_turns_fast(float2 turns, int pos) {
+  float s, c;
+  __sincosf(6.28318530717958648f * rope_turn_fraction(turns, pos), &s, &c);
   return make_float2(c, s);
 }
 
@@ -86,10 +95,21 @@ bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
                     const uint64_t (&strides)[3], const uint32_t (&box)[4]);
 
 // ----------------------------------------------------------------- misc ----
-// f32 -> bf16 / f32 row copy into a strided destination.
-cudaError_t launch_write_to_cache(const float* src, int p, int row_elems, void* dst,
-                                  long long row_stride, int dst_row0, bool dst_bf16,
-                                  cudaStream_t st);
+// f32 -> bf16 / f32 row copy into a strided destination, for one or two
+// tensors (K and V) in one launch; an absent pair is (nullptr, nullptr).
+cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* src1, void* dst1,
+                                  int p, int row_elems, long long row_stride, int dst_row0,
+                                  bool dst_bf16, cudaStream_t st);
+
+// bf16 training inputs, one launch: RoPE table rows for positions p..p+n-1,
+// K rotated into kr, Q into qr (if qr), and with o given the backward's
+// [B, Hq, npad] vectors D = rowsum(dO * O) and lse * log2(e) (padding rows
+// D = 0, lse2 = +inf).
+cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
+                              __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
+                              int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
+                              const __nv_bfloat16* dout, const float* lse, float* Dvec,
+                              float* lse2, int npad, cudaStream_t st);
 
 // cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2].
 cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,

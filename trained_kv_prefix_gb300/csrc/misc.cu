@@ -25,14 +25,22 @@ int grid_for(long long work, int per_block = kThreads) {
 }
 
 // ---------------------------------------------------------- cache write ----
-// One thread converts 8 consecutive values of one cartridge row.
-__global__ void write_to_cache_kernel(const float* __restrict__ src, int p, int row_elems,
-                                      void* __restrict__ dst, long long row_stride, int dst_row0,
+// One thread converts 8 consecutive values of one cartridge row; the second
+// tensor (src1 -> dst1, may be absent) continues the index range of the
+// first, so K and V go in one launch.
+__global__ void write_to_cache_kernel(const float* __restrict__ src0, void* __restrict__ dst0,
+                                      const float* __restrict__ src1, void* __restrict__ dst1,
+                                      int p, int row_elems, long long row_stride, int dst_row0,
                                       int dst_bf16) {
   const int vec_per_row = row_elems / 8;
-  const long long total = static_cast<long long>(p) * vec_per_row;
-  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const long long per = static_cast<long long>(p) * vec_per_row;
+  const long long total = src1 ? 2 * per : per;
+  for (long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t0 < total;
+       t0 += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const bool second = t0 >= per;
+    const long long t = second ? t0 - per : t0;
+    const float* src = second ? src1 : src0;
+    void* dst = second ? dst1 : dst0;
     const int r = static_cast<int>(t / vec_per_row);
     const int c = static_cast<int>(t % vec_per_row) * 8;
     const float4* s =
@@ -59,23 +67,27 @@ __global__ void write_to_cache_kernel(const float* __restrict__ src, int p, int 
 // is formed and reduced modulo 2*pi in fp64 (two-part 2*pi); the reduced
 // angle is split into an f32 head and tail so that cos/sin of the head plus
 // a first-order tail correction keep the table accurate to ~1e-7.
+__device__ __forceinline__ float2 rope_table_entry(double pos, double inv_freq) {
+  const double ang = pos * inv_freq;
+  const double kTwoPiHi = 6.283185307179586232;   // nearest double to 2*pi
+  const double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
+  const double k = rint(ang * 0.15915494309189535);
+  double r = fma(-k, kTwoPiHi, ang);
+  r = fma(-k, kTwoPiLo, r);
+  const float rh = static_cast<float>(r);
+  const float rl = static_cast<float>(r - static_cast<double>(rh));
+  float s, c;
+  sincosf(rh, &s, &c);
+  return make_float2(c - s * rl, s + c * rl);
+}
+
 __global__ void rope_table_kernel(float2* __restrict__ table, int pos0, int npos, int half,
                                   const RopeFreqs f) {
   const long long total = static_cast<long long>(npos) * half;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int i = static_cast<int>(t / half), j = static_cast<int>(t % half);
-    const double ang = static_cast<double>(pos0 + i) * f.inv_freq[j];
-    const double kTwoPiHi = 6.283185307179586232;   // nearest double to 2*pi
-    const double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
-    const double k = rint(ang * 0.15915494309189535);
-    double r = fma(-k, kTwoPiHi, ang);
-    r = fma(-k, kTwoPiLo, r);
-    const float rh = static_cast<float>(r);
-    const float rl = static_cast<float>(r - static_cast<double>(rh));
-    float s, c;
-    sincosf(rh, &s, &c);
-    table[t] = make_float2(c - s * rl, s + c * rl);
+    table[t] = rope_table_entry(static_cast<double>(pos0 + i), f.inv_freq[j]);
   }
 }
 
@@ -137,6 +149,119 @@ __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __r
     __nv_bfloat16* orow = out + row * d;
     *reinterpret_cast<uint4*>(orow + j0) = o0;
     *reinterpret_cast<uint4*>(orow + j0 + half) = o1;
+  }
+}
+
+// ------------------------------------------------------- training prep ----
+// Everything the training kernels need before they start, for bf16 inputs,
+// in one launch over blocks of ppc (1..kPrepPos) real-token positions i:
+//   * the RoPE table rows of positions p + i (all-f32 angle reduction, see
+//     rope_cs_turns; positions must stay below 2^24);
+//   * K rotated at p + i for every (sequence, kv head), and Q for every
+//     (sequence, head) when qr is given (the forward rotates Q itself);
+//   * with o given (backward): D = rowsum(dO * O) and lse * log2(e) in
+//     [B, Hq, npad], padding rows npad > i >= n set to D = 0, lse2 = +inf.
+constexpr int kPrepPos = 4;
+
+__device__ __forceinline__ void rotate_chunk8(const __nv_bfloat16* x, __nv_bfloat16* y,
+                                              const float2* cs, int half) {
+  // elements j0..j0+7 and their rotate-half partners j0+half.. ; cs = the
+  // 8 (cos, sin) of these pairs
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(x));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(x + half));
+  const uint32_t pa[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t pb[4] = {b.x, b.y, b.z, b.w};
+  uint32_t ya[4], yb[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 fa = bf16x2_to_float2(pa[e]), fb = bf16x2_to_float2(pb[e]);
+    float y0a, y1a, y0b, y1b;
+    rope_pair(fa.x, fb.x, cs[2 * e], y0a, y1a);
+    rope_pair(fa.y, fb.y, cs[2 * e + 1], y0b, y1b);
+    ya[e] = pack_bf16x2(y0a, y0b);
+    yb[e] = pack_bf16x2(y1a, y1b);
+  }
+  *reinterpret_cast<uint4*>(y) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+  *reinterpret_cast<uint4*>(y + half) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+}
+
+__global__ void __launch_bounds__(kThreads) train_prep_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+    __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr, float2* __restrict__ table,
+    const RopeFreqs f, int p, int B, int n, int Hq, int Hkv, int d,
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+    const float* __restrict__ lse, float* __restrict__ Dvec, float* __restrict__ lse2, int npad,
+    int ppc) {
+  __shared__ float2 cs[kPrepPos][kMaxHeadDim / 2];
+  const int half = d / 2, chunks = half / 8;
+  const int i0 = blockIdx.x * ppc;
+  const int np = max(0, min(ppc, n - i0));  // real positions in this block
+  for (int t = threadIdx.x; t < np * half; t += blockDim.x) {
+    const int pl = t / half, j = t % half;
+    const float2 v = rope_cs_turns(f.turns[j], p + i0 + pl);
+    cs[pl][j] = v;
+    table[static_cast<long long>(i0 + pl) * half + j] = v;
+  }
+  __syncthreads();
+  // rotations: task = ((pos, b), head, chunk)
+  auto rotate_all = [&](const __nv_bfloat16* x, __nv_bfloat16* y, int H) {
+    const int tasks = np * B * H * chunks;
+#pragma unroll 4
+    for (int t = threadIdx.x; t < tasks; t += blockDim.x) {
+      const int jc = t % chunks;
+      const int h = (t / chunks) % H;
+      const int pb = t / (chunks * H);
+      const int b = pb % B, pl = pb / B;
+      const long long row = (static_cast<long long>(b) * n + i0 + pl) * H + h;
+      rotate_chunk8(x + row * d + jc * 8, y + row * d + jc * 8, &cs[pl][jc * 8], half);
+    }
+  };
+  rotate_all(k, kr, Hkv);
+  if (qr) rotate_all(q, qr, Hq);
+  if (!o) return;
+  // D and lse2: 8 lanes per (b, i, h) row, 4 rows per warp (uniform trip count)
+  const int lane8 = threadIdx.x & 7;
+  const int rows = np * B * Hq;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int rows_pad = ((rows + 3) / 4) * 4;
+#pragma unroll 2
+  for (int base = warp * 4; base < rows_pad; base += nwarps * 4) {
+    const int rr = base + ((threadIdx.x & 31) >> 3);
+    float acc = 0.f;
+    int h = 0, b = 0, pl = 0;
+    if (rr < rows) {
+      h = rr % Hq;
+      b = (rr / Hq) % B;
+      pl = rr / (Hq * B);
+      const long long row = (static_cast<long long>(b) * n + i0 + pl) * Hq + h;
+      for (int c = lane8 * 8; c < d; c += 64) {
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + row * d + c));
+        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + row * d + c));
+        const uint32_t po[4] = {ov.x, ov.y, ov.z, ov.w};
+        const uint32_t pg[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fo = bf16x2_to_float2(po[e]), fg = bf16x2_to_float2(pg[e]);
+          acc += fo.x * fg.x + fo.y * fg.y;
+        }
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (lane8 == 0 && rr < rows) {
+      const long long bh = static_cast<long long>(b) * Hq + h;
+      Dvec[bh * npad + i0 + pl] = acc;
+      lse2[bh * npad + i0 + pl] = __ldg(lse + bh * n + i0 + pl) * 1.4426950408889634f;
+    }
+  }
+  // padding rows of this block's positions
+  const int pad_lo = max(i0, n), pad_hi = min(i0 + ppc, npad);
+  for (int t = threadIdx.x; t < B * Hq * max(0, pad_hi - pad_lo); t += blockDim.x) {
+    const int i = pad_lo + t % (pad_hi - pad_lo);
+    const long long bh = t / (pad_hi - pad_lo);
+    Dvec[bh * npad + i] = 0.f;
+    lse2[bh * npad + i] = INFINITY;
   }
 }
 
@@ -222,14 +347,36 @@ RopeFreqs make_rope_freqs(int d, double theta) {
   return f;
 }
 
-cudaError_t launch_write_to_cache(const float* src, int p, int row_elems, void* dst,
-                                  long long row_stride, int dst_row0, bool dst_bf16,
-                                  cudaStream_t st) {
+cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* src1, void* dst1,
+                                  int p, int row_elems, long long row_stride, int dst_row0,
+                                  bool dst_bf16, cudaStream_t st) {
   if (p <= 0) return cudaSuccess;
-  const long long work = static_cast<long long>(p) * (row_elems / 8);
+  if (!src0) {  // only the second tensor
+    src0 = src1;
+    dst0 = dst1;
+    src1 = nullptr;
+  }
+  if (!src0) return cudaSuccess;
+  const long long work = static_cast<long long>(p) * (row_elems / 8) * (src1 ? 2 : 1);
   TraceScope tr("write_to_cache", st);
-  write_to_cache_kernel<<<grid_for(work), kThreads, 0, st>>>(src, p, row_elems, dst, row_stride,
-                                                             dst_row0, dst_bf16 ? 1 : 0);
+  write_to_cache_kernel<<<grid_for(work), kThreads, 0, st>>>(
+      src0, dst0, src1, src1 ? dst1 : nullptr, p, row_elems, row_stride, dst_row0, dst_bf16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
+                              __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
+                              int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
+                              const __nv_bfloat16* dout, const float* lse, float* Dvec,
+                              float* lse2, int npad, cudaStream_t st) {
+  const int span = o ? max(n, npad) : n;
+  // positions per CTA: enough CTAs for about eight per SM, at most kPrepPos
+  const int ppc = max(1, min(kPrepPos, (span + 152 * 8 - 1) / (152 * 8)));
+  const int grid = (span + ppc - 1) / ppc;
+  if (grid <= 0) return cudaSuccess;
+  TraceScope tr(o ? "bwd_prep" : "fwd_prep", st);
+  train_prep_kernel<<<grid, kThreads, 0, st>>>(q, k, qr, kr, table, f, p, B, n, Hq, Hkv, d, o,
+                                                dout, lse, Dvec, lse2, npad, ppc);
   return cudaGetLastError();
 }
 
