@@ -379,6 +379,11 @@ int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.decode = false;
   l.rotate_q = tp.q_in_kernel;
   l.table = tp.table;
+  CUtensorMap mO32;
+  if (in == CART_BF16) {
+    if (!make_rows_map(&mO32, o, g->B, g->n, g->Hq, g->d, 32)) return CART_ERR_CUDA;
+    l.mO32 = &mO32;
+  }
   CART_CUDA(launch_fwd(l, st));
   return CART_OK;
 }

@@ -48,6 +48,7 @@ struct FwdParams {
   int out_f32;
   int decode;
   int rotate_q;
+  int tma_out;          // training bf16 output: warps store their rows with mO32
   const float2* table;  // rotate_q: cos/sin rows for positions p .. p + n_rows - 1
   uint32_t* status;
   // decode mode: raw query rows r = b*G + hh, rotated here at p + len[b]
@@ -92,35 +93,50 @@ enum FwdBar {
 };
 static_assert(kNumBars * 8 + 4 <= 256, "barrier area");
 
-// RoPE of one Q row held in a 128-byte-swizzled tile, in place; cs(j) gives
-// (cos, sin) of pair j.  Rotate-half pairs (c, c + D/2): for D = 128 chunk j
-// of the first 64-wide block pairs with chunk j of the second block; for
-// D = 64 chunk j pairs with chunk j + 4.
+// RoPE of one Q row held in a 128-byte-swizzled tile, in place.
+// cs(j0, c) fills c[0..31] with the (cos, sin) of pairs j0..j0+31.
+// Rotate-half pairs (c, c + D/2): for D = 128 chunk j of the first 64-wide
+// block pairs with chunk j of the second block; for D = 64 chunk j pairs
+// with chunk j + 4.  Work goes by 32 pairs: all their angles first, then all
+// loads of the row's chunks, then the rotations and stores, so that the
+// latencies of each batch overlap.
 template <int D, class CS>
 __device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, CS cs) {
+  const uint32_t base = smem_u32(sQ);
 #pragma unroll
-  for (int j = 0; j < D / 16; ++j) {
-    const uint32_t o0 = sw128_offset(row, j);
-    const uint32_t o1 = D == 128 ? 16384u + sw128_offset(row, j) : sw128_offset(row, j + 4);
-    const uint4 a = *reinterpret_cast<const uint4*>(sQ + o0);
-    const uint4 b = *reinterpret_cast<const uint4*>(sQ + o1);
-    const uint32_t pa[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t pb[4] = {b.x, b.y, b.z, b.w};
-    uint32_t ya[4], yb[4];
+  for (int half = 0; half < D / 64; ++half) {
+    float2 c[32];
+    cs(32 * half, c);
+    uint4 av[4], bv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 fa = bf16x2_to_float2(pa[e]);
-      const float2 fb = bf16x2_to_float2(pb[e]);
-      const float2 c0 = cs(8 * j + 2 * e);
-      const float2 c1 = cs(8 * j + 2 * e + 1);
-      float y0a, y1a, y0b, y1b;
-      rope_pair(fa.x, fb.x, c0, y0a, y1a);
-      rope_pair(fa.y, fb.y, c1, y0b, y1b);
-      ya[e] = pack_bf16x2(y0a, y0b);
-      yb[e] = pack_bf16x2(y1a, y1b);
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = 4 * half + jj;
+      const uint32_t o0 = sw128_offset(row, j);
+      const uint32_t o1 = D == 128 ? 16384u + sw128_offset(row, j) : sw128_offset(row, j + 4);
+      av[jj] = lds_u4(base + o0);
+      bv[jj] = lds_u4(base + o1);
     }
-    *reinterpret_cast<uint4*>(sQ + o0) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-    *reinterpret_cast<uint4*>(sQ + o1) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = 4 * half + jj;
+      const uint32_t o0 = sw128_offset(row, j);
+      const uint32_t o1 = D == 128 ? 16384u + sw128_offset(row, j) : sw128_offset(row, j + 4);
+      const uint32_t pa[4] = {av[jj].x, av[jj].y, av[jj].z, av[jj].w};
+      const uint32_t pb[4] = {bv[jj].x, bv[jj].y, bv[jj].z, bv[jj].w};
+      uint32_t ya[4], yb[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = bf16x2_to_float2(pa[e]);
+        const float2 fb = bf16x2_to_float2(pb[e]);
+        float y0a, y1a, y0b, y1b;
+        rope_pair(fa.x, fb.x, c[8 * jj + 2 * e], y0a, y1a);
+        rope_pair(fa.y, fb.y, c[8 * jj + 2 * e + 1], y0b, y1b);
+        ya[e] = pack_bf16x2(y0a, y0b);
+        yb[e] = pack_bf16x2(y1a, y1b);
+      }
+      sts_u4(base + o0, make_uint4(ya[0], ya[1], ya[2], ya[3]));
+      sts_u4(base + o1, make_uint4(yb[0], yb[1], yb[2], yb[3]));
+    }
   }
 }
 
@@ -128,7 +144,8 @@ template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
-               const __grid_constant__ CUtensorMap mV, const FwdParams a) {
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO32,
+               const FwdParams a) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -371,10 +388,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (a.rotate_q) {
         ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
-        const float2* tb = a.table + static_cast<long long>(i) * (D / 2);
+        const float4* tb = reinterpret_cast<const float4*>(a.table + static_cast<long long>(i) * (D / 2));
         if (ok && i < a.n_rows)
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
-                          [&](int j) { return __ldg(tb + j); });
+                          [&](int j0, float2* c) {
+                            float4 v[16];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) v[q] = __ldg(tb + j0 / 2 + q);
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                              c[2 * q] = make_float2(v[q].x, v[q].y);
+                              c[2 * q + 1] = make_float2(v[q].z, v[q].w);
+                            }
+                          });
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
       } else if (a.decode) {
@@ -387,7 +413,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           len = len < 0 ? 0 : (len >= a.dec_rows ? a.dec_rows - 1 : len);
           const int pos = a.p + len;
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
-                          [&](int j) { return rope_cs_turns_fast(a.turns[j], pos); });
+                          [&](int j0, float2* c) {
+#pragma unroll
+                            for (int q = 0; q < 32; ++q)
+                              c[q] = rope_cs_turns_fast(a.turns[j0 + q], pos);
+                          });
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
@@ -493,6 +523,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float inv_l = 1.f / l;
       const bool row_ok = i < a.n_rows;
       const bool f32 = a.decode || a.out_f32;
+      if (a.tma_out) {
+        // bf16 output by TMA: every thread writes its row into its tile's Q
+        // buffer (every MMA that read Q_x is done) in the 128-byte-swizzled
+        // layout of the output map's box, then lane 0 stores the warp's 32
+        // rows (rows past n are clipped by the map).
+        uint8_t* sO = smem + L::kQ + x * L::kTileBytes;
+        const uint32_t base = smem_u32(sO);
+        uint32_t ob[D / 32][32];
+#pragma unroll
+        for (int blk = 0; blk < D / 32; ++blk) tmem_ld32(tO + blk * 32, ob[blk]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int blk = 0; blk < D / 32; ++blk) {
+          tmem_reg_fence(ob[blk]);
+          // columns 32*blk.. = 64-wide block blk/2, 16-byte chunks 4*(blk%2)..
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t* o = ob[blk] + 8 * k;
+            sts_u4(base + (blk >> 1) * 16384 + sw128_offset(row, 4 * (blk & 1) + k),
+                   make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l),
+                              pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l),
+                              pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l),
+                              pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l)));
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int r0 = (2 * pair + x) * kTile + (warp & 3) * 32;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_store_4d(&mO32, sO + h * 16384 + (warp & 3) * 4096, h * 64, head, r0, qb);
+          bulk_commit_group();
+          bulk_wait_all();
+        }
+        __syncwarp();
+      } else {
       // Each warp turns its 32 rows x 32 columns at a time around through a
       // 4 KB slice of its tile's Q buffer (every MMA that read Q_x is done),
       // so that global stores cover whole 32-byte sectors: 16-byte granule
@@ -500,12 +567,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint8_t* stg = smem + L::kQ + x * L::kTileBytes + (warp & 3) * 4096;
       const int gpr = f32 ? 8 : 4;  // 16-byte granules per row and 32 columns
       const int row0 = (2 * pair + x) * kTile + (warp & 3) * 32;
+      // every column block of O in flight at once, one wait
+      uint32_t ob[D / 32][32];
+#pragma unroll
+      for (int blk = 0; blk < D / 32; ++blk) tmem_ld32(tO + blk * 32, ob[blk]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int blk = 0; blk < D / 32; ++blk) tmem_reg_fence(ob[blk]);
 #pragma unroll
       for (int blk = 0; blk < D / 32; ++blk) {
-        uint32_t o[32];
-        tmem_ld32(tO + blk * 32, o);
-        tmem_ld_wait();
-        tmem_reg_fence(o);
+        const uint32_t* o = ob[blk];
         uint8_t* my = stg + lane * 128;
         if (f32) {
 #pragma unroll
@@ -543,6 +614,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         __syncwarp();
+      }
       }
       if (row_ok) {
         const float lse2 = m + __log2f(l);
@@ -583,6 +655,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   p.out_f32 = a.out_f32 ? 1 : 0;
   p.decode = a.decode ? 1 : 0;
   p.rotate_q = a.rotate_q ? 1 : 0;
+  p.tma_out = (!a.decode && !a.out_f32 && a.mO32) ? 1 : 0;
   p.table = a.table;
   p.status = device_status_ptr();
   if (a.decode) {
@@ -608,7 +681,8 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fwd_kernel<D>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV, p);
+  return cudaLaunchKernelEx(&cfg, fwd_kernel<D>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
+                            p.tma_out ? *a.mO32 : *a.mQ, p);
 }
 
 }  // namespace

@@ -135,6 +135,8 @@ struct FwdLaunch {
   const CUtensorMap* mVc;
   const CUtensorMap* mK;   // 4D (d, Hkv, n, B) rotated real keys
   const CUtensorMap* mV;   // 4D (d, Hkv, n, B)
+  const CUtensorMap* mO32; // training, bf16 output: 4D (d, Hq, n, B) over o, 64x1x32x1 box
+                           // (each warp stores its 32 rows by TMA); else null
   int d;
   int n_rows;              // query rows per query block (n, or B*G for decode)
   int n_qblocks;           // query blocks: B for training, 1 for decode
