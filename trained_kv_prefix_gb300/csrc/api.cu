@@ -432,8 +432,9 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
     dob = t;
     CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
   }
-  CUtensorMap mdO;
+  CUtensorMap mdO, mdQ;
   if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
+  if (!f32 && !make_rows_map(&mdQ, dq, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
   BwdLaunch l{};
   l.mQ = &tp.mQ;
   l.mdO = &mdO;
@@ -441,6 +442,7 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.mVc = &tp.mVc;
   l.mK = &tp.mK;
   l.mV = &tp.mV;
+  l.mdQ = f32 ? nullptr : &mdQ;
   l.B = g->B;
   l.n = g->n;
   l.Hq = g->Hq;

@@ -51,6 +51,7 @@ struct BwdParams {
   int accumulate;
   const float2* table;
   uint32_t* status;
+  int tma_dq;  // bf16 dQ stored by TMA through mdQ
 };
 
 __device__ __forceinline__ void store_row_out(void* base, long long off, const float* x, int n,
@@ -527,6 +528,7 @@ enum DqBar {
   kDsdFull0,                         // dS of buffer x written (256 arrivals)
   kDqDone = kDsdFull0 + 2,
   kDqDrain,
+  kDqStaged,                         // both groups staged their dQ columns (256 arrivals)
   kDqBars
 };
 static_assert(kDqBars * 8 + 4 <= 256, "dq barrier area");
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
               const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
               const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
-              const BwdParams a) {
+              const __grid_constant__ CUtensorMap mdQ, const BwdParams a) {
   using L = DqSmem<D>;
   constexpr int SK = kDqKStages, SV = kDqVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -575,6 +577,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bars[kDpFree], 256);
     mbar_init(&bars[kDqDone], 1);
     mbar_init(&bars[kDqDrain], 1);
+    mbar_init(&bars[kDqStaged], 256);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -810,6 +813,36 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           lo[e] = x0 * cs.x + x1 * cs.y;
           hi[e] = x1 * cs.x - x0 * cs.y;
         }
+      }
+      if (a.tma_dq) {
+        // Stage the row's columns in the (spent) Q tile, in the swizzled
+        // layout of the dQ map's 128-row box, then one thread stores the
+        // tile; rows past n are clipped by the map.
+        const uint32_t base = smem_u32(sQ);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const float* v = part ? hi : lo;
+          const int col0 = (part ? D / 2 : 0) + wg * Q;
+#pragma unroll
+          for (int k = 0; k < Q / 8; ++k) {
+            const int col = col0 + 8 * k;
+            sts_u4(base + (col >> 6) * 16384 + sw128_offset(row, (col & 63) >> 3),
+                   make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                              pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                              pack_bf16x2(v[8 * k + 6], v[8 * k + 7])));
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kDqStaged]);
+        if (threadIdx.x == 0) {
+          if (mbar_wait(&bars[kDqStaged], 0, abort_p, a.status, kDevErrTimeoutEpilogue)) {
+#pragma unroll
+            for (int hc = 0; hc < D / 64; ++hc) tma_store_4d(&mdQ, sQ + hc * 16384, hc * 64, h, q0, b);
+            bulk_commit_group();
+            bulk_wait_all();
+          }
+        }
+      } else if (i < a.n) {
         const long long off = ((static_cast<long long>(b) * a.n + i) * a.Hq + h) * D;
         store_row_out(a.dq, off + wg * Q, lo, Q, a.out_f32 != 0);
         store_row_out(a.dq, off + D / 2 + wg * Q, hi, Q, a.out_f32 != 0);
@@ -865,8 +898,9 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   TraceScope tr("bwd_dq", st_dq);
+  p.tma_dq = (!l.out_f32 && l.mdQ) ? 1 : 0;
   dq_kernel<D><<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
-      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
+      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p.tma_dq ? *l.mdQ : *l.mQ, p);
   return cudaGetLastError();
 }
 

@@ -175,6 +175,7 @@ struct BwdLaunch {
   const CUtensorMap* mVc;
   const CUtensorMap* mK;    // 4D (d, Hkv, n, B) rotated real keys
   const CUtensorMap* mV;
+  const CUtensorMap* mdQ;   // bf16 output: 4D (d, Hq, n, B) over dq, 128-row box; else null
   int B, n, Hq, Hkv, d, p, frozen_prefix;
   float scale;
   const float* lse2;        // [B, Hq, npad] log2-domain lse, +inf past n
