@@ -150,7 +150,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspace carving shared by the size query and the call.
 struct TrainWs {
-  size_t table = 0, qr = 0, kr = 0, vb = 0, kcb = 0, vcb = 0, dob = 0, dvec = 0, lse2 = 0,
+  size_t table = 0, qr = 0, kr = 0, vb = 0, kcb = 0, vcb = 0, dob = 0, dvec = 0, nlse2 = 0,
          total = 0;
   int npad = 0;
 };
@@ -177,7 +177,7 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
     w.dob = (in == CART_F32) ? take(rows_q * e16) : SIZE_MAX;
     w.npad = (g->n + 127) / 128 * 128;
     w.dvec = take(static_cast<size_t>(g->B) * g->Hq * w.npad * sizeof(float));
-    w.lse2 = take(static_cast<size_t>(g->B) * g->Hq * w.npad * sizeof(float));
+    w.nlse2 = take(static_cast<size_t>(g->B) * g->Hq * w.npad * sizeof(float));
   }
   w.total = off;
   return w;
@@ -207,8 +207,8 @@ struct PrepVec {
   const void* o = nullptr;
   const void* dout = nullptr;
   const float* lse = nullptr;
-  float* Dvec = nullptr;
-  float* lse2 = nullptr;
+  float* nDvec = nullptr;
+  float* nlse2 = nullptr;
   int npad = 0;
 };
 
@@ -231,7 +231,7 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         q_in_kernel ? nullptr : qr, kr, table, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
         static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
-        vec.lse, vec.Dvec, vec.lse2, vec.npad, st));
+        vec.lse, vec.nDvec, vec.nlse2, vec.npad, st));
     if (q_in_kernel) qr = static_cast<__nv_bfloat16*>(const_cast<void*>(q));
   } else {
     CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, freqs, st));
@@ -412,15 +412,15 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   TrainPrep tp;
   const bool f32 = in == CART_F32;
-  float* Dvec = reinterpret_cast<float*>(ws + w.dvec);
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  float* nDvec = reinterpret_cast<float*>(ws + w.dvec);
+  float* nlse2 = reinterpret_cast<float*>(ws + w.nlse2);
   PrepVec vec;  // bf16: the per-row vectors come out of the same prep launch
   if (!f32) {
     vec.o = o;
     vec.dout = dout;
     vec.lse = lse;
-    vec.Dvec = Dvec;
-    vec.lse2 = lse2;
+    vec.nDvec = nDvec;
+    vec.nlse2 = nlse2;
     vec.npad = w.npad;
   }
   rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp, false, vec);
@@ -430,7 +430,8 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
     __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.dob);
     CART_CUDA(launch_rope_rows(dout, true, t, tp.table, g->B, g->n, g->Hq, g->d, false, st));
     dob = t;
-    CART_CUDA(launch_bwd_vec(o, dout, f32, lse, Dvec, lse2, g->B, g->n, w.npad, g->Hq, g->d, st));
+    CART_CUDA(launch_bwd_vec(o, dout, f32, lse, nDvec, nlse2, g->B, g->n, w.npad, g->Hq, g->d,
+                             st));
   }
   CUtensorMap mdO, mdQ;
   if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
@@ -451,8 +452,8 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.p = g->p;
   l.frozen_prefix = g->frozen_prefix;
   l.scale = g->scale;
-  l.lse2 = lse2;
-  l.Dvec = Dvec;
+  l.nlse2 = nlse2;
+  l.nDvec = nDvec;
   l.npad = w.npad;
   l.dq = dq;
   l.dk = dk;

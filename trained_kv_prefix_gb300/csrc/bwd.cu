@@ -39,8 +39,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdParams {
   int B, n, Hq, Hkv, G, p, frozen_prefix, n_ct, n_rt, n_qtiles;
   float scale, scale_log2;
-  const float* lse2;  // [B, Hq, npad] log2-domain lse (+inf past n)
-  const float* Dvec;  // [B, Hq, npad] (0 past n)
+  const float* nlse2;  // [B, Hq, npad] -lse * log2(e) (-inf past n)
+  const float* nDvec;  // [B, Hq, npad] -D (0 past n)
   int npad;
   void* dq;
   void* dk;
@@ -75,13 +75,20 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 // group owns key row t = TMEM lane t); warp 16 is the TMA producer, warp 17
 // issues the MMAs.  Every MMA has N = 128.
 // TMEM (512 columns): S^T at 0, dP^T at 128 (f32), dV at 256, dK at 384.
-// Warpgroup w overwrites the first 16 columns of its 32-column slices of
-// S^T and dP^T with P^T and dS^T packed as bf16 pairs, which the dV and dK
-// MMAs read as their A operand straight from TMEM (K step k of 16 queries at
-// column (k/2)*32 + (k%2)*8).  P^T is formed while dP^T is still being
-// computed (S^T and dP^T have their own barriers).  The next step's S^T and
-// dP^T are issued after this step's dV / dK MMAs (one CTA's MMAs run in
-// issue order, so they overwrite P^T / dS^T only after those have read it).
+// A warpgroup loads its 32 S^T columns and releases S^T at once, so that the
+// next step's S^T is computed while it works; it forms P^T in registers
+// (while dP^T is still being computed), then loads its dP^T columns and
+// overwrites that 32-column slice with P^T (first 16 columns) and dS^T
+// (last 16) packed as bf16 pairs.  dV and dK read them as their A operand
+// straight from TMEM (K step k of 16 queries at column 128 + (k/2)*32 +
+// (k%2)*8, plus 16 for dS^T).  MMA order per step u:
+//   S^T(u+1) [after S^T(u) is released], dK(u), dV(u) [after P^T / dS^T(u)],
+//   dP^T(u+1) -- which overwrites P^T / dS^T(u) after dK(u) and dV(u) have
+// read them (one CTA's MMAs run in issue order).
+// Q and dO have their own ring barriers: Q(u)'s slot is released by dK(u),
+// issued first so that the next Q tile's copy overlaps dV(u) and dP^T(u+1)
+// before S^T(u+2) needs it; dO(u)'s slot is released by dV(u).  The step's
+// -lse2 entries travel with Q, its -D entries with dO.
 constexpr int kDkdvThreads = 576;
 constexpr int kDkdvStages = 2;
 
@@ -92,15 +99,16 @@ struct DkdvSmem {
   static constexpr int kK = 0;                          // resident K
   static constexpr int kV = kK + kTileBytes;            // resident V
   static constexpr int kStage0 = kV + kTileBytes;       // stage s: Q at +0, dO at +kTileBytes
-  static constexpr int kVec = kStage0 + kStages * 2 * kTileBytes;  // stage s: lse2[128], D[128]
+  static constexpr int kVec = kStage0 + kStages * 2 * kTileBytes;  // stage s: -lse2, -D [128]
   static constexpr int kBar = kVec + kStages * 1024;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-enum DkdvBar { kResFull = 0, kQdoFull0, kQdoEmpty0 = kQdoFull0 + kDkdvStages,
-               kStFull = kQdoEmpty0 + kDkdvStages, kDpTFull, kDsFull, kAccDone, kDkdvDrain,
-               kDkdvBars };
+enum DkdvBar { kResFull = 0, kQFull0, kQEmpty0 = kQFull0 + kDkdvStages,
+               kDoFull0 = kQEmpty0 + kDkdvStages, kDoEmpty0 = kDoFull0 + kDkdvStages,
+               kStFull = kDoEmpty0 + kDkdvStages, kStFree, kDpTFull, kDsFull, kAccDone,
+               kDkdvDrain, kDkdvBars };
 
 struct DkdvItem {
   int b, hh, qt;
@@ -180,10 +188,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     abort_flag = 0;
     mbar_init(&bars[kResFull], 1);
     for (int s = 0; s < S; ++s) {
-      mbar_init(&bars[kQdoFull0 + s], 1);
-      mbar_init(&bars[kQdoEmpty0 + s], 1);
+      mbar_init(&bars[kQFull0 + s], 1);
+      mbar_init(&bars[kQEmpty0 + s], 1);
+      mbar_init(&bars[kDoFull0 + s], 1);
+      mbar_init(&bars[kDoEmpty0 + s], 1);
     }
     mbar_init(&bars[kStFull], 1);
+    mbar_init(&bars[kStFree], 512);
     mbar_init(&bars[kDpTFull], 1);
     mbar_init(&bars[kDsFull], 512);
     mbar_init(&bars[kAccDone], 1);
@@ -206,9 +217,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
   if (warp == 16) {
     // ------------------------------------------------------------ producer --
-    // One lane: per step the Q and dO tiles (TMA) and the step's 128 entries
-    // of lse2 and D (plain bulk copies from the padded row vectors), all
-    // completing on the stage's full barrier.
+    // One lane: per step the Q tile with the step's 128 entries of -lse2,
+    // then the dO tile with its 128 entries of -D (TMA for the tiles, plain
+    // bulk copies from the padded row vectors), each pair completing on its
+    // ring slot's full barrier.
     if (lane == 0 && U > 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
@@ -223,37 +235,48 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           tma_load_4d(sV + h * 16384, &mV, &bars[kResFull], h * 64, g, tile * kTile, b_real);
         }
       }
-      int issued = 0;
+      int issued_q = 0, issued_do = 0;
       bool ok = true;
       for (int u = 0; u < U; ++u) {
         const int s = u % S;
-        if (u >= S) {
-          ok = mbar_wait(&bars[kQdoEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
-                         kDevErrTimeoutTma);
-          if (!ok) break;
-        }
         const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
         const int h = g * a.G + it.hh;
         uint8_t* sQ = smem + L::kStage0 + s * 2 * L::kTileBytes;
         uint8_t* sdO = sQ + L::kTileBytes;
         float* v = vec + s * 256;
         const long long vo = (static_cast<long long>(it.b) * a.Hq + h) * a.npad + it.qt * kTile;
-        mbar_arrive_expect_tx(&bars[kQdoFull0 + s], 2 * L::kTileBytes + 1024);
-#pragma unroll
-        for (int hc = 0; hc < D / 64; ++hc) {
-          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdoFull0 + s], hc * 64, h, it.qt * kTile, it.b);
-          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kQdoFull0 + s], hc * 64, h, it.qt * kTile,
-                      it.b);
+        if (u >= S) {
+          ok = mbar_wait(&bars[kQEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutTma);
+          if (!ok) break;
         }
-        bulk_load(v, a.lse2 + vo, 512, &bars[kQdoFull0 + s]);
-        bulk_load(v + 128, a.Dvec + vo, 512, &bars[kQdoFull0 + s]);
-        issued = u + 1;
+        mbar_arrive_expect_tx(&bars[kQFull0 + s], L::kTileBytes + 512);
+#pragma unroll
+        for (int hc = 0; hc < D / 64; ++hc)
+          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQFull0 + s], hc * 64, h, it.qt * kTile, it.b);
+        bulk_load(v, a.nlse2 + vo, 512, &bars[kQFull0 + s]);
+        issued_q = u + 1;
+        if (u >= S) {
+          ok = mbar_wait(&bars[kDoEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
+                         kDevErrTimeoutTma);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&bars[kDoFull0 + s], L::kTileBytes + 512);
+#pragma unroll
+        for (int hc = 0; hc < D / 64; ++hc)
+          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kDoFull0 + s], hc * 64, h, it.qt * kTile,
+                      it.b);
+        bulk_load(v + 128, a.nDvec + vo, 512, &bars[kDoFull0 + s]);
+        issued_do = u + 1;
       }
       if (!ok) {
+        // let the copies in flight land before the CTA exits
         int dummy = 0;
         mbar_wait(&bars[kResFull], 0, &dummy, nullptr, 0);
-        for (int u = max(issued - S, 0); u < issued; ++u)
-          mbar_wait(&bars[kQdoFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
+        for (int u = max(issued_q - S, 0); u < issued_q; ++u)
+          mbar_wait(&bars[kQFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
+        for (int u = max(issued_do - S, 0); u < issued_do; ++u)
+          mbar_wait(&bars[kDoFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
       }
     }
     __syncwarp();
@@ -276,11 +299,6 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idST, 1u);
         }
       };
-      // Issue order per step u: dV(u), S^T(u+1), dK(u), dP^T(u+1).  S^T(u+1)
-      // overwrites the P^T(u) that dV(u) reads and dP^T(u+1) the dS^T(u)
-      // that dK(u) reads; one CTA's MMAs run in issue order, so each comes
-      // after its reader, and the warpgroups form P^T(u+1) while dK(u) and
-      // dP^T(u+1) run.
       auto issue_st_dpt = [&](int u, bool st) {
         const uint32_t so = (u % S) * kStageBytes;
         if (st) {
@@ -292,40 +310,51 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
       };
       bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma) &&
-                mbar_wait(&bars[kQdoFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+                mbar_wait(&bars[kQFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
       if (ok) {
         tc_fence_after();
         issue_st_dpt(0, true);
-        issue_st_dpt(0, false);
+        ok = mbar_wait(&bars[kDoFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+        tc_fence_after();
+        if (ok) issue_st_dpt(0, false);
       }
       for (int u = 0; u < U && ok; ++u) {
         const int s = u % S;
         const uint32_t so = s * kStageBytes;
-        ok = mbar_wait(&bars[kDsFull], u & 1, abort_p, a.status, kDevErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q: A from TMEM, B = the step's dO / Q
-        // tile as MN-major operands (16 rows = 2048 B per K step)
-        const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kTileBytes);
-        const uint32_t first = u > 0 ? 1u : 0u;
-        umma_bf16_ts(tDV, tST, ddo, idACC, first);
-#pragma unroll
-        for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(tDV, tST + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC, 1u);
         const bool next = u + 1 < U;
-        if (next) {
-          ok = mbar_wait(&bars[kQdoFull0 + (u + 1) % S], ((u + 1) / S) & 1, abort_p, a.status,
+        if (next) {  // S^T(u+1) as soon as the warpgroups hold S^T(u)
+          ok = mbar_wait(&bars[kStFree], u & 1, abort_p, a.status, kDevErrTimeoutMma) &&
+               mbar_wait(&bars[kQFull0 + (u + 1) % S], ((u + 1) / S) & 1, abort_p, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           issue_st_dpt(u + 1, true);
         }
-        umma_bf16_ts(tDK, tDP, dq, idACC, first);
+        ok = mbar_wait(&bars[kDsFull], u & 1, abort_p, a.status, kDevErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        // dK += dS^T Q, then dV += P^T dO: A from TMEM (over dP^T), B = the
+        // step's Q / dO tile as MN-major operands (16 rows = 2048 B per K step)
+        const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kTileBytes);
+        const uint32_t first = u > 0 ? 1u : 0u;
+        umma_bf16_ts(tDK, tDP + 16, dq, idACC, first);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(tDK, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC, 1u);
-        umma_commit(&bars[kQdoEmpty0 + s]);
-        if (next) issue_st_dpt(u + 1, false);
+          umma_bf16_ts(tDK, tDP + 16 + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC,
+                       1u);
+        umma_commit(&bars[kQEmpty0 + s]);
+        umma_bf16_ts(tDV, tDP, ddo, idACC, first);
+#pragma unroll
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ts(tDV, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC, 1u);
+        umma_commit(&bars[kDoEmpty0 + s]);
+        if (next) {
+          ok = mbar_wait(&bars[kDoFull0 + (u + 1) % S], ((u + 1) / S) & 1, abort_p, a.status,
+                         kDevErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_st_dpt(u + 1, false);
+        }
       }
       if (ok) umma_commit(&bars[kAccDone]);
       umma_commit(&bars[kDkdvDrain]);
@@ -345,9 +374,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int s = u % S;
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
       ok = mbar_wait(&bars[kStFull], u & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
-      // the stage's lse2 / D vectors landed with kQdoFull (already complete:
-      // the MMAs behind kStFull waited for it); waiting makes them visible
-      if (ok) ok = mbar_wait(&bars[kQdoFull0 + s], (u / S) & 1, abort_p, a.status,
+      // the step's -lse2 entries landed with Q (kQFull already complete: the
+      // MMAs behind kStFull waited for it); waiting makes them visible
+      if (ok) ok = mbar_wait(&bars[kQFull0 + s], (u / S) & 1, abort_p, a.status,
                              kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -365,26 +394,37 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_ld32(tst, r);
       tmem_ld_wait();
       tmem_reg_fence(r);
-      // P^T (f32, kept in r) while dP^T is still being computed
+      tc_fence_before();
+      mbar_arrive(&bars[kStFree]);  // S^T(u+1) may overwrite S^T(u) now
+      // P^T = 2^(S^T * scale * log2(e) - lse2) (f32, kept in p) while dP^T
+      // is still being computed; two queries per packed two-lane op
       const bool masked = __any_sync(0xffffffffu, qlim > 0);
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      float2 p[16];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l4 = lds128(lse_s + c4 * 16);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float4 l4 = lds128(lse_s + c4 * 16);  // -lse2 of 4 queries
+        const float2 x0 = __ffma2_rn(u2f2(r[4 * c4], r[4 * c4 + 1]), sc2, make_float2(l4.x, l4.y));
+        const float2 x1 =
+            __ffma2_rn(u2f2(r[4 * c4 + 2], r[4 * c4 + 3]), sc2, make_float2(l4.z, l4.w));
+        p[2 * c4] = make_float2(exp2_approx(x0.x), exp2_approx(x0.y));
+        p[2 * c4 + 1] = make_float2(exp2_approx(x1.x), exp2_approx(x1.y));
+      }
+      if (masked) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c4 * 4 + e;
-          float pe = exp2_approx(fmaf(__uint_as_float(r[cc]), a.scale_log2, -lv[e]));
-          if (masked) pe = (cc >= qlim) ? pe : 0.f;
-          r[cc] = __float_as_uint(pe);
+        for (int c = 0; c < 16; ++c) {
+          p[c].x = (2 * c >= qlim) ? p[c].x : 0.f;
+          p[c].y = (2 * c + 1 >= qlim) ? p[c].y : 0.f;
         }
       }
       uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        pk[c] = pack_bf16x2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
-      tmem_st16(tst, pk);
+      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[c].x, p[c].y);
       ok = mbar_wait(&bars[kDpTFull], u & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      // the step's -D entries landed with dO (kDoFull already complete: the
+      // MMAs behind kDpTFull waited for it); waiting makes them visible
+      if (ok) ok = mbar_wait(&bars[kDoFull0 + s], (u / S) & 1, abort_p, a.status,
+                             kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -392,20 +432,21 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_ld32(tdp, dr);
       tmem_ld_wait();
       tmem_reg_fence(dr);
+      // dS^T = P^T * (dP^T - D)
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 d4 = lds128(dv_s + c4 * 16);
-        const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-        float ds[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c4 * 4 + e;
-          ds[e] = __uint_as_float(r[cc]) * (__uint_as_float(dr[cc]) - dd[e]);
-        }
-        pd[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-        pd[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+        const float4 d4 = lds128(dv_s + c4 * 16);  // -D of 4 queries
+        const float2 ds0 =
+            __fmul2_rn(p[2 * c4], __fadd2_rn(u2f2(dr[4 * c4], dr[4 * c4 + 1]), make_float2(d4.x, d4.y)));
+        const float2 ds1 = __fmul2_rn(
+            p[2 * c4 + 1], __fadd2_rn(u2f2(dr[4 * c4 + 2], dr[4 * c4 + 3]), make_float2(d4.z, d4.w)));
+        pd[2 * c4] = pack_bf16x2(ds0.x, ds0.y);
+        pd[2 * c4 + 1] = pack_bf16x2(ds1.x, ds1.y);
       }
-      tmem_st16(tdp, pd);
+      // P^T over the first 16 and dS^T over the last 16 of this group's dP^T
+      // columns (already read)
+      tmem_st16(tdp, pk);
+      tmem_st16(tdp + 16, pd);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kDsFull]);
@@ -721,10 +762,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row = threadIdx.x & 127;
     const int i = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // padded vectors: rows past n read lse2 = +inf (P = 0) and D = 0
+    // padded vectors: rows past n read -lse2 = -inf (P = 0) and -D = 0
     const long long vidx = (static_cast<long long>(b) * a.Hq + h) * a.npad + i;
-    const float lse2 = __ldg(a.lse2 + vidx);
-    const float Di = __ldg(a.Dvec + vidx);
+    const float nl = __ldg(a.nlse2 + vidx), nd = __ldg(a.nDvec + vidx);
+    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+    const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
     const int i_cap = min(i, a.n - 1);
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
@@ -755,17 +797,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       auto compute = [&](auto masked) {
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = c + e;
-            const uint32_t sv = cc < 32 ? sa[cc] : sb[cc - 32];
-            const uint32_t dv = cc < 32 ? da[cc] : db[cc - 32];
-            float pe = exp2_approx(fmaf(__uint_as_float(sv), a.scale_log2, -lse2));
-            if (decltype(masked)::value) pe = (cc < valid) ? pe : 0.f;
-            ds[e] = pe * (__uint_as_float(dv) - Di);
+          // two keys per packed two-lane op: P = 2^(S*scale*log2(e) - lse2),
+          // dS = P * (dP - D)
+          const float2 sv = c < 32 ? u2f2(sa[c], sa[c + 1]) : u2f2(sb[c - 32], sb[c - 31]);
+          const float2 dv = c < 32 ? u2f2(da[c], da[c + 1]) : u2f2(db[c - 32], db[c - 31]);
+          const float2 x = __ffma2_rn(sv, sc2, nl2);
+          float2 pe = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+          if (decltype(masked)::value) {
+            pe.x = (c < valid) ? pe.x : 0.f;
+            pe.y = (c + 1 < valid) ? pe.y : 0.f;
           }
-          pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+          const float2 ds = __fmul2_rn(pe, __fadd2_rn(dv, nd2));
+          pk[c / 2] = pack_bf16x2(ds.x, ds.y);
         }
       };
       if (__any_sync(0xffffffffu, valid < 64))
@@ -873,8 +916,8 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.n_qtiles = p.n_rt;
   p.scale = l.scale;
   p.scale_log2 = l.scale * kLog2e;
-  p.lse2 = l.lse2;
-  p.Dvec = l.Dvec;
+  p.nlse2 = l.nlse2;
+  p.nDvec = l.nDvec;
   p.npad = l.npad;
   p.dq = l.dq;
   p.dk = l.dk;

@@ -103,13 +103,13 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
 
 // bf16 training inputs, one launch: RoPE table rows for positions p..p+n-1,
 // K rotated into kr, Q into qr (if qr), and with o given the backward's
-// [B, Hq, npad] vectors D = rowsum(dO * O) and lse * log2(e) (padding rows
-// D = 0, lse2 = +inf).
+// [B, Hq, npad] vectors -D = -rowsum(dO * O) and -lse * log2(e), stored
+// negated (padding rows 0 and -inf).
 cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
-                              const __nv_bfloat16* dout, const float* lse, float* Dvec,
-                              float* lse2, int npad, cudaStream_t st);
+                              const __nv_bfloat16* dout, const float* lse, float* nDvec,
+                              float* nlse2, int npad, cudaStream_t st);
 
 // cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2].
 cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
@@ -122,10 +122,10 @@ cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, cons
                              int B, int n, int H, int d, bool rotate, cudaStream_t st);
 
 // Per-row vectors of the backward in [B, Hq, npad] layout (npad >= n):
-// Dvec = sum_c dO[b,i,h,c] * O[b,i,h,c], lse2 = lse * log2(e); padding rows
-// get D = 0 and lse2 = +inf (zero probability).
+// nDvec = -sum_c dO[b,i,h,c] * O[b,i,h,c], nlse2 = -lse * log2(e); padding
+// rows get 0 and -inf (zero probability).
 cudaError_t launch_bwd_vec(const void* o, const void* dout, bool f32, const float* lse,
-                           float* Dvec, float* lse2, int B, int n, int npad, int Hq, int d,
+                           float* nDvec, float* nlse2, int B, int n, int npad, int Hq, int d,
                            cudaStream_t st);
 
 // ------------------------------------------------------------- forward ----
@@ -178,8 +178,8 @@ struct BwdLaunch {
   const CUtensorMap* mdQ;   // bf16 output: 4D (d, Hq, n, B) over dq, 128-row box; else null
   int B, n, Hq, Hkv, d, p, frozen_prefix;
   float scale;
-  const float* lse2;        // [B, Hq, npad] log2-domain lse, +inf past n
-  const float* Dvec;        // [B, Hq, npad], 0 past n
+  const float* nlse2;       // [B, Hq, npad] -lse * log2(e), -inf past n
+  const float* nDvec;       // [B, Hq, npad] -D, 0 past n
   int npad;                 // n rounded up to a multiple of 128
   void* dq;                 // [B, n, Hq, d] output dtype
   void* dk;                 // [B, n, Hkv, d]

@@ -159,8 +159,10 @@ __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __r
 //     rope_cs_turns; positions must stay below 2^24);
 //   * K rotated at p + i for every (sequence, kv head), and Q for every
 //     (sequence, head) when qr is given (the forward rotates Q itself);
-//   * with o given (backward): D = rowsum(dO * O) and lse * log2(e) in
-//     [B, Hq, npad], padding rows npad > i >= n set to D = 0, lse2 = +inf.
+//   * with o given (backward): the negated row vectors -D = -rowsum(dO * O)
+//     and -lse * log2(e) in [B, Hq, npad] (stored negated so that the
+//     backward kernels add them with packed two-lane arithmetic), padding
+//     rows npad > i >= n set to -D = 0 and -lse2 = -inf.
 constexpr int kPrepPos = 4;
 
 __device__ __forceinline__ void rotate_chunk8(const __nv_bfloat16* x, __nv_bfloat16* y,
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr, float2* __restrict__ table,
     const RopeFreqs f, int p, int B, int n, int Hq, int Hkv, int d,
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-    const float* __restrict__ lse, float* __restrict__ Dvec, float* __restrict__ lse2, int npad,
+    const float* __restrict__ lse, float* __restrict__ nDvec, float* __restrict__ nlse2, int npad,
     int ppc) {
   __shared__ float2 cs[kPrepPos][kMaxHeadDim / 2];
   const int half = d / 2, chunks = half / 8;
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
   rotate_all(k, kr, Hkv);
   if (qr) rotate_all(q, qr, Hq);
   if (!o) return;
-  // D and lse2: 8 lanes per (b, i, h) row, 4 rows per warp (uniform trip count)
+  // -D and -lse2: 8 lanes per (b, i, h) row, 4 rows per warp (uniform trip count)
   const int lane8 = threadIdx.x & 7;
   const int rows = np * B * Hq;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -251,8 +253,8 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     if (lane8 == 0 && rr < rows) {
       const long long bh = static_cast<long long>(b) * Hq + h;
-      Dvec[bh * npad + i0 + pl] = acc;
-      lse2[bh * npad + i0 + pl] = __ldg(lse + bh * n + i0 + pl) * 1.4426950408889634f;
+      nDvec[bh * npad + i0 + pl] = -acc;
+      nlse2[bh * npad + i0 + pl] = __ldg(lse + bh * n + i0 + pl) * -1.4426950408889634f;
     }
   }
   // padding rows of this block's positions
@@ -260,22 +262,22 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
   for (int t = threadIdx.x; t < B * Hq * max(0, pad_hi - pad_lo); t += blockDim.x) {
     const int i = pad_lo + t % (pad_hi - pad_lo);
     const long long bh = t / (pad_hi - pad_lo);
-    Dvec[bh * npad + i] = 0.f;
-    lse2[bh * npad + i] = INFINITY;
+    nDvec[bh * npad + i] = 0.f;
+    nlse2[bh * npad + i] = -INFINITY;
   }
 }
 
 // ------------------------------------------------------------- bwd vec ----
 // Per query row of the backward, in [B, Hq, npad] layout (npad >= n, rows
 // n..npad-1 are padding that reads as "no probability mass"):
-//   Dvec[b, h, i] = sum_c dO[b,i,h,c] * O[b,i,h,c]   (0 for padding)
-//   lse2[b, h, i] = lse[b, h, i] * log2(e)           (+inf for padding)
+//   nDvec[b, h, i] = -sum_c dO[b,i,h,c] * O[b,i,h,c]  (0 for padding)
+//   nlse2[b, h, i] = -lse[b, h, i] * log2(e)          (-inf for padding)
 // 8 lanes per row, 4 rows per warp; the loop trip count is uniform across
 // the warp.
 template <bool kF32>
 __global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restrict__ dov,
-                               const float* __restrict__ lse, float* __restrict__ Dvec,
-                               float* __restrict__ lse2, int B, int n, int npad, int Hq, int d) {
+                               const float* __restrict__ lse, float* __restrict__ nDvec,
+                               float* __restrict__ nlse2, int B, int n, int npad, int Hq, int d) {
   const long long rows = static_cast<long long>(B) * n * Hq;
   const int lane8 = threadIdx.x & 7;
   const int group = (threadIdx.x & 31) >> 3;
@@ -321,16 +323,16 @@ __global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restri
       const int i = static_cast<int>(bi % n);
       const int b = static_cast<int>(bi / n);
       const long long bh = static_cast<long long>(b) * Hq + h;
-      Dvec[bh * npad + i] = acc;
-      lse2[bh * npad + i] = __ldg(lse + bh * n + i) * 1.4426950408889634f;
+      nDvec[bh * npad + i] = -acc;
+      nlse2[bh * npad + i] = __ldg(lse + bh * n + i) * -1.4426950408889634f;
     }
   }
   const long long pad_rows = static_cast<long long>(B) * Hq * (npad - n);
   for (long long t = tid; t < pad_rows; t += nthreads) {
     const long long bh = t / (npad - n);
     const int i = n + static_cast<int>(t % (npad - n));
-    Dvec[bh * npad + i] = 0.f;
-    lse2[bh * npad + i] = INFINITY;
+    nDvec[bh * npad + i] = 0.f;
+    nlse2[bh * npad + i] = -INFINITY;
   }
 }
 
@@ -367,8 +369,8 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
 cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
-                              const __nv_bfloat16* dout, const float* lse, float* Dvec,
-                              float* lse2, int npad, cudaStream_t st) {
+                              const __nv_bfloat16* dout, const float* lse, float* nDvec,
+                              float* nlse2, int npad, cudaStream_t st) {
   const int span = o ? max(n, npad) : n;
   // positions per CTA: enough CTAs for about eight per SM, at most kPrepPos
   const int ppc = max(1, min(kPrepPos, (span + 152 * 8 - 1) / (152 * 8)));
@@ -376,7 +378,7 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(o ? "bwd_prep" : "fwd_prep", st);
   train_prep_kernel<<<grid, kThreads, 0, st>>>(q, k, qr, kr, table, f, p, B, n, Hq, Hkv, d, o,
-                                                dout, lse, Dvec, lse2, npad, ppc);
+                                                dout, lse, nDvec, nlse2, npad, ppc);
   return cudaGetLastError();
 }
 
@@ -404,16 +406,16 @@ cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, cons
 }
 
 cudaError_t launch_bwd_vec(const void* o, const void* dout, bool f32, const float* lse,
-                           float* Dvec, float* lse2, int B, int n, int npad, int Hq, int d,
+                           float* nDvec, float* nlse2, int B, int n, int npad, int Hq, int d,
                            cudaStream_t st) {
   const long long rows = static_cast<long long>(B) * n * Hq;
   if (rows <= 0 || npad < n) return cudaSuccess;
   const int grid = grid_for(rows * 8);  // 8 threads per row
   TraceScope tr("bwd_vec", st);
   if (f32)
-    bwd_vec_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, lse, Dvec, lse2, B, n, npad, Hq, d);
+    bwd_vec_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, lse, nDvec, nlse2, B, n, npad, Hq, d);
   else
-    bwd_vec_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, lse, Dvec, lse2, B, n, npad, Hq, d);
+    bwd_vec_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, lse, nDvec, nlse2, B, n, npad, Hq, d);
   return cudaGetLastError();
 }
 

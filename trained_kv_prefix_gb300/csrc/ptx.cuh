@@ -357,6 +357,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two f32 register images as a float2 (operand of the packed two-lane
+// __ffma2_rn / __fadd2_rn / __fmul2_rn, one instruction for both lanes).
+__device__ __forceinline__ float2 u2f2(uint32_t x, uint32_t y) {
+  return make_float2(__uint_as_float(x), __uint_as_float(y));
+}
+
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
