@@ -186,9 +186,12 @@ CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, int p, floa
 CART_API const char* cart_status_string(int status);
 
 /* Reads (and with clear != 0 resets) the device status word that kernels set
- * when a bounded wait gives up.  Synchronizes the current device.  Writes the
- * bits to *bits_out (may be NULL); returns CART_OK, CART_ERR_TIMEOUT when any
- * bit is set, or CART_ERR_CUDA. */
+ * when a bounded wait gives up (bit 0: a TMA copy, 1: an MMA, 2: the softmax
+ * warps, 3: the epilogue), when a work schedule is inconsistent (bit 4), or
+ * when the dynamic shared memory does not start 1024-byte aligned (bit 5;
+ * the kernel then does nothing).  Synchronizes the current device.  Writes
+ * the bits to *bits_out (may be NULL); returns CART_OK, CART_ERR_TIMEOUT when
+ * any bit is set, or CART_ERR_CUDA. */
 CART_API int cart_device_status(unsigned* bits_out, int clear);
 
 /* ------------------------------------------------------------------------

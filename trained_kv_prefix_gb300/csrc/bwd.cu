@@ -85,30 +85,36 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 //   S^T(u+1) [after S^T(u) is released], dK(u), dV(u) [after P^T / dS^T(u)],
 //   dP^T(u+1) -- which overwrites P^T / dS^T(u) after dK(u) and dV(u) have
 // read them (one CTA's MMAs run in issue order).
-// Q and dO have their own ring barriers: Q(u)'s slot is released by dK(u),
-// issued first so that the next Q tile's copy overlaps dV(u) and dP^T(u+1)
-// before S^T(u+2) needs it; dO(u)'s slot is released by dV(u).  The step's
-// -lse2 entries travel with Q, its -D entries with dO.
+// Q and dO have rings of their own: a Q slot is released by dK(u), a dO
+// slot by dV(u).  Q gets three slots, so a Q tile is copied while two full
+// steps of MMAs run; dO gets two (its first reader, dP^T, comes later in the
+// step).  The step's -lse2 entries travel with Q, its -D entries with dO.
+// The layout fills the 227 KB limit, so it relies on the dynamic shared
+// memory starting 1024-byte aligned (checked at entry; no static shared
+// variables).
 constexpr int kDkdvThreads = 576;
-constexpr int kDkdvStages = 2;
+constexpr int kDkdvQSlots = 3, kDkdvDoSlots = 2;
 
 template <int D>
 struct DkdvSmem {
-  static constexpr int kStages = kDkdvStages;
-  static constexpr int kTileBytes = kTile * D * 2;     // 128-row bf16 tile
-  static constexpr int kK = 0;                          // resident K
-  static constexpr int kV = kK + kTileBytes;            // resident V
-  static constexpr int kStage0 = kV + kTileBytes;       // stage s: Q at +0, dO at +kTileBytes
-  static constexpr int kVec = kStage0 + kStages * 2 * kTileBytes;  // stage s: -lse2, -D [128]
-  static constexpr int kBar = kVec + kStages * 1024;
+  static constexpr int kTileBytes = kTile * D * 2;           // 128-row bf16 tile
+  static constexpr int kK = 0;                                // resident K
+  static constexpr int kV = kK + kTileBytes;                  // resident V
+  static constexpr int kQ0 = kV + kTileBytes;                 // Q ring
+  static constexpr int kDo0 = kQ0 + kDkdvQSlots * kTileBytes;  // dO ring
+  static constexpr int kVecL = kDo0 + kDkdvDoSlots * kTileBytes;  // -lse2 [128] per Q slot
+  static constexpr int kVecD = kVecL + kDkdvQSlots * 512;         // -D [128] per dO slot
+  static constexpr int kBar = kVecD + kDkdvDoSlots * 512;
   static constexpr int kBytes = kBar + 256;
-  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr int kAlloc = kBytes;
+  static_assert(kAlloc <= 232448, "dK/dV shared memory above the 227 KB limit");
 };
 
-enum DkdvBar { kResFull = 0, kQFull0, kQEmpty0 = kQFull0 + kDkdvStages,
-               kDoFull0 = kQEmpty0 + kDkdvStages, kDoEmpty0 = kDoFull0 + kDkdvStages,
-               kStFull = kDoEmpty0 + kDkdvStages, kStFree, kDpTFull, kDsFull, kAccDone,
+enum DkdvBar { kResFull = 0, kQFull0, kQEmpty0 = kQFull0 + kDkdvQSlots,
+               kDoFull0 = kQEmpty0 + kDkdvQSlots, kDoEmpty0 = kDoFull0 + kDkdvDoSlots,
+               kStFull = kDoEmpty0 + kDkdvDoSlots, kStFree, kDpTFull, kDsFull, kAccDone,
                kDkdvDrain, kDkdvBars };
+static_assert(kDkdvBars * 8 + 16 <= 256, "dK/dV barrier area");
 
 struct DkdvItem {
   int b, hh, qt;
@@ -157,13 +163,16 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                 const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                 const BwdParams a) {
   using L = DkdvSmem<D>;
-  constexpr int S = L::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  constexpr int SQ = kDkdvQSlots, SD = kDkdvDoSlots;
+  extern __shared__ __align__(1024) uint8_t dkdv_smem[];
+  uint8_t* smem = dkdv_smem;
+  if (smem_u32(smem) & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, kDevErrSmemLayout);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDkdvBars * 8);
-  __shared__ int abort_flag;
+  int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDkdvBars * 8 + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item: cartridge tiles first (heaviest), then real tiles ----
@@ -185,11 +194,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   const int U = cart ? a.B * a.G * a.n_qtiles : a.G * max(a.n_qtiles - tile, 0);
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    *abort_flag = 0;
     mbar_init(&bars[kResFull], 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SQ; ++s) {
       mbar_init(&bars[kQFull0 + s], 1);
       mbar_init(&bars[kQEmpty0 + s], 1);
+    }
+    for (int s = 0; s < SD; ++s) {
       mbar_init(&bars[kDoFull0 + s], 1);
       mbar_init(&bars[kDoEmpty0 + s], 1);
     }
@@ -210,10 +221,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tST = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
-  volatile int* abort_p = &abort_flag;
+  const uint32_t abort_s = smem_u32(abort_flag);
   uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
-  float* vec = reinterpret_cast<float*>(smem + L::kVec);
+  float* vecL = reinterpret_cast<float*>(smem + L::kVecL);
+  float* vecD = reinterpret_cast<float*>(smem + L::kVecD);
 
   if (warp == 16) {
     // ------------------------------------------------------------ producer --
@@ -238,128 +250,130 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       int issued_q = 0, issued_do = 0;
       bool ok = true;
       for (int u = 0; u < U; ++u) {
-        const int s = u % S;
+        const int sq = u % SQ, sd = u % SD;
         const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
         const int h = g * a.G + it.hh;
-        uint8_t* sQ = smem + L::kStage0 + s * 2 * L::kTileBytes;
-        uint8_t* sdO = sQ + L::kTileBytes;
-        float* v = vec + s * 256;
+        uint8_t* sQ = smem + L::kQ0 + sq * L::kTileBytes;
+        uint8_t* sdO = smem + L::kDo0 + sd * L::kTileBytes;
         const long long vo = (static_cast<long long>(it.b) * a.Hq + h) * a.npad + it.qt * kTile;
-        if (u >= S) {
-          ok = mbar_wait(&bars[kQEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
+        if (u >= SQ) {
+          ok = mbar_wait(&bars[kQEmpty0 + sq], ((u / SQ) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
-        mbar_arrive_expect_tx(&bars[kQFull0 + s], L::kTileBytes + 512);
+        mbar_arrive_expect_tx(&bars[kQFull0 + sq], L::kTileBytes + 512);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc)
-          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQFull0 + s], hc * 64, h, it.qt * kTile, it.b);
-        bulk_load(v, a.nlse2 + vo, 512, &bars[kQFull0 + s]);
+          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQFull0 + sq], hc * 64, h, it.qt * kTile, it.b);
+        bulk_load(vecL + sq * 128, a.nlse2 + vo, 512, &bars[kQFull0 + sq]);
         issued_q = u + 1;
-        if (u >= S) {
-          ok = mbar_wait(&bars[kDoEmpty0 + s], ((u / S) - 1) & 1, abort_p, a.status,
+        if (u >= SD) {
+          ok = mbar_wait(&bars[kDoEmpty0 + sd], ((u / SD) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
-        mbar_arrive_expect_tx(&bars[kDoFull0 + s], L::kTileBytes + 512);
+        mbar_arrive_expect_tx(&bars[kDoFull0 + sd], L::kTileBytes + 512);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc)
-          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kDoFull0 + s], hc * 64, h, it.qt * kTile,
+          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kDoFull0 + sd], hc * 64, h, it.qt * kTile,
                       it.b);
-        bulk_load(v + 128, a.nDvec + vo, 512, &bars[kDoFull0 + s]);
+        bulk_load(vecD + sd * 128, a.nDvec + vo, 512, &bars[kDoFull0 + sd]);
         issued_do = u + 1;
       }
       if (!ok) {
         // let the copies in flight land before the CTA exits
-        int dummy = 0;
-        mbar_wait(&bars[kResFull], 0, &dummy, nullptr, 0);
-        for (int u = max(issued_q - S, 0); u < issued_q; ++u)
-          mbar_wait(&bars[kQFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
-        for (int u = max(issued_do - S, 0); u < issued_do; ++u)
-          mbar_wait(&bars[kDoFull0 + u % S], (u / S) & 1, &dummy, nullptr, 0);
+        mbar_wait(&bars[kResFull], 0, 0u, nullptr, 0);
+        for (int u = max(issued_q - SQ, 0); u < issued_q; ++u)
+          mbar_wait(&bars[kQFull0 + u % SQ], (u / SQ) & 1, 0u, nullptr, 0);
+        for (int u = max(issued_do - SD, 0); u < issued_do; ++u)
+          mbar_wait(&bars[kDoFull0 + u % SD], (u / SD) & 1, 0u, nullptr, 0);
       }
     }
     __syncwarp();
   } else if (warp == 17) {
     // ----------------------------------------------------------------- MMA --
-    if (lane == 0 && U > 0) {
+    // The whole warp runs this loop (warp-uniform descriptors); one elected
+    // lane issues each MMA and commit.
+    if (U > 0) {
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu,
+                          mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
+      };
       const uint32_t idST = idesc_bf16(128, 128, false, false);
       const uint32_t idACC = idesc_bf16(128, D, false, true);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16u, 1024u);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16u, 1024u);
-      const uint64_t dQk0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16u, 1024u);     // K-major
-      const uint64_t dQm0 = sdesc_sw128(smem_u32(smem + L::kStage0), 16384u, 1024u);  // MN-major
-      constexpr uint32_t kStageBytes = 2 * L::kTileBytes;
+      // Q and dO ring slots as K-major (S^T, dP^T) and MN-major (dK, dV)
+      const uint64_t dQk0 = sdesc_sw128(smem_u32(smem + L::kQ0), 16u, 1024u);
+      const uint64_t dQm0 = sdesc_sw128(smem_u32(smem + L::kQ0), 16384u, 1024u);
+      const uint64_t dOk0 = sdesc_sw128(smem_u32(smem + L::kDo0), 16u, 1024u);
+      const uint64_t dOm0 = sdesc_sw128(smem_u32(smem + L::kDo0), 16384u, 1024u);
       // C (f32, TMEM) = A (128 rows) * B^T (128 rows), both K-major over d
       auto issue_nt = [&](uint32_t c, uint64_t da, uint64_t db) {
-        umma_bf16_ss(c, da, db, idST, 0u);
+        umma_bf16_ss_w(c, da, db, idST, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idST, 1u);
+          umma_bf16_ss_w(c, desc_add(da, off), desc_add(db, off), idST, 1u);
         }
       };
       auto issue_st_dpt = [&](int u, bool st) {
-        const uint32_t so = (u % S) * kStageBytes;
         if (st) {
-          issue_nt(tST, dK0, desc_add(dQk0, so));
-          umma_commit(&bars[kStFull]);
+          issue_nt(tST, dK0, desc_add(dQk0, (u % SQ) * L::kTileBytes));
+          umma_commit_w(&bars[kStFull]);
         } else {
-          issue_nt(tDP, dV0, desc_add(dQk0, so + L::kTileBytes));
-          umma_commit(&bars[kDpTFull]);
+          issue_nt(tDP, dV0, desc_add(dOk0, (u % SD) * L::kTileBytes));
+          umma_commit_w(&bars[kDpTFull]);
         }
       };
-      bool ok = mbar_wait(&bars[kResFull], 0, abort_p, a.status, kDevErrTimeoutMma) &&
-                mbar_wait(&bars[kQFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      bool ok = wait(&bars[kResFull], 0) &&
+                wait(&bars[kQFull0], 0);
       if (ok) {
         tc_fence_after();
         issue_st_dpt(0, true);
-        ok = mbar_wait(&bars[kDoFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+        ok = wait(&bars[kDoFull0], 0);
         tc_fence_after();
         if (ok) issue_st_dpt(0, false);
       }
       for (int u = 0; u < U && ok; ++u) {
-        const int s = u % S;
-        const uint32_t so = s * kStageBytes;
+        const int sq = u % SQ, sd = u % SD;
         const bool next = u + 1 < U;
         if (next) {  // S^T(u+1) as soon as the warpgroups hold S^T(u)
-          ok = mbar_wait(&bars[kStFree], u & 1, abort_p, a.status, kDevErrTimeoutMma) &&
-               mbar_wait(&bars[kQFull0 + (u + 1) % S], ((u + 1) / S) & 1, abort_p, a.status,
-                         kDevErrTimeoutMma);
+          ok = wait(&bars[kStFree], u & 1) &&
+               wait(&bars[kQFull0 + (u + 1) % SQ], ((u + 1) / SQ) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_st_dpt(u + 1, true);
         }
-        ok = mbar_wait(&bars[kDsFull], u & 1, abort_p, a.status, kDevErrTimeoutMma);
+        ok = wait(&bars[kDsFull], u & 1);
         if (!ok) break;
         tc_fence_after();
         // dK += dS^T Q, then dV += P^T dO: A from TMEM (over dP^T), B = the
         // step's Q / dO tile as MN-major operands (16 rows = 2048 B per K step)
-        const uint64_t dq = desc_add(dQm0, so), ddo = desc_add(dQm0, so + L::kTileBytes);
+        const uint64_t dq = desc_add(dQm0, sq * L::kTileBytes);
+        const uint64_t ddo = desc_add(dOm0, sd * L::kTileBytes);
         const uint32_t first = u > 0 ? 1u : 0u;
-        umma_bf16_ts(tDK, tDP + 16, dq, idACC, first);
+        umma_bf16_ts_w(tDK, tDP + 16, dq, idACC, first);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(tDK, tDP + 16 + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC,
+          umma_bf16_ts_w(tDK, tDP + 16 + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC,
                        1u);
-        umma_commit(&bars[kQEmpty0 + s]);
-        umma_bf16_ts(tDV, tDP, ddo, idACC, first);
+        umma_commit_w(&bars[kQEmpty0 + sq]);
+        umma_bf16_ts_w(tDV, tDP, ddo, idACC, first);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(tDV, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC, 1u);
-        umma_commit(&bars[kDoEmpty0 + s]);
+          umma_bf16_ts_w(tDV, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC, 1u);
+        umma_commit_w(&bars[kDoEmpty0 + sd]);
         if (next) {
-          ok = mbar_wait(&bars[kDoFull0 + (u + 1) % S], ((u + 1) / S) & 1, abort_p, a.status,
-                         kDevErrTimeoutMma);
+          ok = wait(&bars[kDoFull0 + (u + 1) % SD], ((u + 1) / SD) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_st_dpt(u + 1, false);
         }
       }
-      if (ok) umma_commit(&bars[kAccDone]);
-      umma_commit(&bars[kDkdvDrain]);
-      int dummy = 0;
-      mbar_wait(&bars[kDkdvDrain], 0, &dummy, nullptr, 0);
+      if (ok) umma_commit_w(&bars[kAccDone]);
+      umma_commit_w(&bars[kDkdvDrain]);
+      mbar_wait(&bars[kDkdvDrain], 0, 0u, nullptr, 0);
     }
     __syncwarp();
   } else {
@@ -371,12 +385,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
     for (int u = 0; u < U && ok; ++u) {
-      const int s = u % S;
+      const int sq = u % SQ, sd = u % SD;
       const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
-      ok = mbar_wait(&bars[kStFull], u & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kStFull], u & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       // the step's -lse2 entries landed with Q (kQFull already complete: the
       // MMAs behind kStFull waited for it); waiting makes them visible
-      if (ok) ok = mbar_wait(&bars[kQFull0 + s], (u / S) & 1, abort_p, a.status,
+      if (ok) ok = mbar_wait(&bars[kQFull0 + sq], (u / SQ) & 1, abort_s, a.status,
                              kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -388,8 +402,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       // all for rows past the end of the keys
       const int qlim =
           !key_ok ? 32 : (cart ? 0 : max(0, min(32, j - it.qt * kTile - wg * 32)));
-      const uint32_t lse_s = smem_u32(vec + s * 256 + wg * 32);
-      const uint32_t dv_s = smem_u32(vec + s * 256 + 128 + wg * 32);
+      const uint32_t lse_s = smem_u32(vecL + sq * 128 + wg * 32);
+      const uint32_t dv_s = smem_u32(vecD + sd * 128 + wg * 32);
       uint32_t r[32];
       tmem_ld32(tst, r);
       tmem_ld_wait();
@@ -420,10 +434,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[c].x, p[c].y);
-      ok = mbar_wait(&bars[kDpTFull], u & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kDpTFull], u & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       // the step's -D entries landed with dO (kDoFull already complete: the
       // MMAs behind kDpTFull waited for it); waiting makes them visible
-      if (ok) ok = mbar_wait(&bars[kDoFull0 + s], (u / S) & 1, abort_p, a.status,
+      if (ok) ok = mbar_wait(&bars[kDoFull0 + sd], (u / SD) & 1, abort_s, a.status,
                              kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -455,7 +469,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     // warpgroups 0 and 1 write the two halves of dV; 2 and 3 take the RoPE
     // pairs [w2*D/4, (w2+1)*D/4) of dK with their partners D/2 further on
     if (ok) {
-      ok = mbar_wait(&bars[kAccDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = mbar_wait(&bars[kAccDone], 0, abort_s, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -554,7 +568,7 @@ struct DqSmem {
   static constexpr int kV = kK + kDqKStages * kTileBytes;     // V ring
   static constexpr int kBar = kV + kDqVStages * kTileBytes;
   static constexpr int kBytes = kBar + 256;
-  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr int kAlloc = kBytes;  // dynamic shared memory starts 1024-aligned
 };
 
 enum DqBar {
@@ -572,6 +586,7 @@ enum DqBar {
   kDqStaged,                         // both groups staged their dQ columns (256 arrivals)
   kDqBars
 };
+static_assert(kDqBars * 8 + 16 <= 256, "dQ barrier area");
 static_assert(kDqBars * 8 + 4 <= 256, "dq barrier area");
 
 template <int D>
@@ -582,12 +597,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
               const __grid_constant__ CUtensorMap mdQ, const BwdParams a) {
   using L = DqSmem<D>;
   constexpr int SK = kDqKStages, SV = kDqVStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t dq_smem[];
+  uint8_t* smem = dq_smem;
+  if (smem_u32(smem) & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, kDevErrSmemLayout);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDqBars * 8);
-  __shared__ int abort_flag;
+  int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDqBars * 8 + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int h = blockIdx.x, b = blockIdx.y;
@@ -600,7 +618,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int T = n_ct + n_rt;
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
+    *abort_flag = 0;
     mbar_init(&bars[kQdFull], 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(&bars[kKFull0 + s], 1);
@@ -630,7 +648,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS0 = tmem, tDP = tmem + 256, tDQ = tmem + 384;
-  volatile int* abort_p = &abort_flag;
+  const uint32_t abort_s = smem_u32(abort_flag);
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sdO = smem + L::kdO;
 
@@ -652,7 +670,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int blk = cart ? 0 : b;
         const int sk = t % SK, sv = t % SV;
         if (t >= SK) {
-          ok = mbar_wait(&bars[kKEmpty0 + sk], ((t / SK) - 1) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kKEmpty0 + sk], ((t / SK) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
@@ -664,7 +682,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                       blk);
         k_issued = t + 1;
         if (t >= SV) {
-          ok = mbar_wait(&bars[kVEmpty0 + sv], ((t / SV) - 1) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kVEmpty0 + sv], ((t / SV) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
@@ -677,12 +695,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         v_issued = t + 1;
       }
       if (!ok) {
-        int dummy = 0;
-        mbar_wait(&bars[kQdFull], 0, &dummy, nullptr, 0);
+        mbar_wait(&bars[kQdFull], 0, 0u, nullptr, 0);
         for (int t = max(k_issued - SK, 0); t < k_issued; ++t)
-          mbar_wait(&bars[kKFull0 + t % SK], (t / SK) & 1, &dummy, nullptr, 0);
+          mbar_wait(&bars[kKFull0 + t % SK], (t / SK) & 1, 0u, nullptr, 0);
         for (int t = max(v_issued - SV, 0); t < v_issued; ++t)
-          mbar_wait(&bars[kVFull0 + t % SV], (t / SV) & 1, &dummy, nullptr, 0);
+          mbar_wait(&bars[kVFull0 + t % SV], (t / SV) & 1, 0u, nullptr, 0);
       }
     }
     __syncwarp();
@@ -704,13 +721,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idS, 1u);
         }
       };
-      bool ok = mbar_wait(&bars[kQdFull], 0, abort_p, a.status, kDevErrTimeoutMma) &&
-                mbar_wait(&bars[kKFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      bool ok = mbar_wait(&bars[kQdFull], 0, abort_s, a.status, kDevErrTimeoutMma) &&
+                mbar_wait(&bars[kKFull0], 0, abort_s, a.status, kDevErrTimeoutMma);
       if (ok) {
         tc_fence_after();
         issue_nt(tS0, dQd, dKk0);
         umma_commit(&bars[kSdFull0]);
-        ok = mbar_wait(&bars[kVFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kVFull0], 0, abort_s, a.status, kDevErrTimeoutMma);
       }
       if (ok) {
         tc_fence_after();
@@ -722,7 +739,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int x = t & 1;
         if (t + 1 < T) {
           const int sk = (t + 1) % SK, sv = (t + 1) % SV;
-          ok = mbar_wait(&bars[kKFull0 + sk], ((t + 1) / SK) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kKFull0 + sk], ((t + 1) / SK) & 1, abort_s, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
@@ -730,8 +747,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           // (one CTA's MMAs run in issue order)
           issue_nt(tS0 + (x ^ 1) * 128, dQd, desc_add(dKk0, sk * L::kTileBytes));
           umma_commit(&bars[kSdFull0 + (x ^ 1)]);
-          ok = mbar_wait(&bars[kDpFree], t & 1, abort_p, a.status, kDevErrTimeoutMma) &&
-               mbar_wait(&bars[kVFull0 + sv], ((t + 1) / SV) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kDpFree], t & 1, abort_s, a.status, kDevErrTimeoutMma) &&
+               mbar_wait(&bars[kVFull0 + sv], ((t + 1) / SV) & 1, abort_s, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
@@ -739,7 +756,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           umma_commit(&bars[kDpFull]);
           umma_commit(&bars[kVEmpty0 + sv]);
         }
-        ok = mbar_wait(&bars[kDsdFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kDsdFull0 + x], (t >> 1) & 1, abort_s, a.status, kDevErrTimeoutMma);
         if (!ok) break;
         tc_fence_after();
         const int sk = t % SK;
@@ -753,8 +770,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       if (ok) umma_commit(&bars[kDqDone]);
       umma_commit(&bars[kDqDrain]);
-      int dummy = 0;
-      mbar_wait(&bars[kDqDrain], 0, &dummy, nullptr, 0);
+      mbar_wait(&bars[kDqDrain], 0, 0u, nullptr, 0);
     }
     __syncwarp();
   } else {
@@ -771,8 +787,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
       const int x = t & 1;
-      ok = mbar_wait(&bars[kSdFull0 + x], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutSoftmax) &&
-           mbar_wait(&bars[kDpFull], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kSdFull0 + x], (t >> 1) & 1, abort_s, a.status, kDevErrTimeoutSoftmax) &&
+           mbar_wait(&bars[kDpFull], t & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -822,7 +838,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_arrive(&bars[kDsdFull0 + x]);
     }
     if (ok) {
-      ok = mbar_wait(&bars[kDqDone], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = mbar_wait(&bars[kDqDone], 0, abort_s, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -878,7 +894,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&bars[kDqStaged]);
         if (threadIdx.x == 0) {
-          if (mbar_wait(&bars[kDqStaged], 0, abort_p, a.status, kDevErrTimeoutEpilogue)) {
+          if (mbar_wait(&bars[kDqStaged], 0, abort_s, a.status, kDevErrTimeoutEpilogue)) {
 #pragma unroll
             for (int hc = 0; hc < D / 64; ++hc) tma_store_4d(&mdQ, sQ + hc * 16384, hc * 64, h, q0, b);
             bulk_commit_group();

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  volatile int* abort_p = &abort_flag;
+  const uint32_t abort_s = smem_u32(&abort_flag);
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const CUtensorMap* mv = cart ? &mVc : &mV;
         const int blk = cart ? 0 : qb;
         if (t >= 2) {
-          ok = mbar_wait(&bars[kKEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kKEmpty0 + s], ((t >> 1) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_4d(sK + h * 16384, mk, &bars[kKFull0 + s], h * 64, kvh, row0, blk);
         k_issued = t + 1;
         if (t >= 2) {
-          ok = mbar_wait(&bars[kVEmpty0 + s], ((t >> 1) - 1) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kVEmpty0 + s], ((t >> 1) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
@@ -277,12 +277,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) {
         // Give the copies already in flight a bounded chance to land before
         // the CTA releases its shared memory.
-        int dummy = 0;
-        mbar_wait(&bars[kQFull], 0, &dummy, nullptr, 0);
+        mbar_wait(&bars[kQFull], 0, 0u, nullptr, 0);
         for (int t = max(k_issued - 2, 0); t < k_issued; ++t)
-          mbar_wait(&bars[kKFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
+          mbar_wait(&bars[kKFull0 + (t & 1)], (t >> 1) & 1, 0u, nullptr, 0);
         for (int t = max(v_issued - 2, 0); t < v_issued; ++t)
-          mbar_wait(&bars[kVFull0 + (t & 1)], (t >> 1) & 1, &dummy, nullptr, 0);
+          mbar_wait(&bars[kVFull0 + (t & 1)], (t >> 1) & 1, 0u, nullptr, 0);
       }
     }
     __syncwarp();
@@ -323,14 +322,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int k = 1; k < kTile / 16; ++k)
           umma_bf16_ts(to, tp + k * 8, desc_add(dv, k * 2048), idPV, 1u);
       };
-      bool ok = mbar_wait(&bars[kQReady0], 0, abort_p, a.status, kDevErrTimeoutMma) &&
-                mbar_wait(&bars[kKFull0], 0, abort_p, a.status, kDevErrTimeoutMma);
+      bool ok = mbar_wait(&bars[kQReady0], 0, abort_s, a.status, kDevErrTimeoutMma) &&
+                mbar_wait(&bars[kKFull0], 0, abort_s, a.status, kDevErrTimeoutMma);
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
       }
       if (ok && hasB) {
-        ok = mbar_wait(&bars[kQReady1], 0, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kQReady1], 0, abort_s, a.status, kDevErrTimeoutMma);
         if (ok) {
           tc_fence_after();
           issue_qk(1, 0);
@@ -339,25 +338,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (ok) umma_commit(&bars[kKEmpty0]);
       for (int t = 0; t < T && ok; ++t) {
         const int s = t & 1;
-        ok = mbar_wait(&bars[kVFull0 + s], (t >> 1) & 1, abort_p, a.status, kDevErrTimeoutMma);
+        ok = mbar_wait(&bars[kVFull0 + s], (t >> 1) & 1, abort_s, a.status, kDevErrTimeoutMma);
         if (!ok) break;
         const bool next = t + 1 < T;
         if (t < T_A) {
-          ok = mbar_wait(&bars[kPFull0], t & 1, abort_p, a.status, kDevErrTimeoutMma);
+          ok = mbar_wait(&bars[kPFull0], t & 1, abort_s, a.status, kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, t);
           if (t == T_A - 1) umma_commit(&bars[kODone0]);
         }
         if (next) {
-          ok = mbar_wait(&bars[kKFull0 + (s ^ 1)], ((t + 1) >> 1) & 1, abort_p, a.status,
+          ok = mbar_wait(&bars[kKFull0 + (s ^ 1)], ((t + 1) >> 1) & 1, abort_s, a.status,
                          kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           if (t + 1 < T_A) issue_qk(0, t + 1);
         }
         if (t < T_B) {
-          ok = mbar_wait(&bars[kPFull1], t & 1, abort_p, a.status, kDevErrTimeoutMma);
+          ok = mbar_wait(&bars[kPFull1], t & 1, abort_s, a.status, kDevErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, t);
@@ -369,8 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // Drain: every MMA issued above completes before the CTA tears down.
       umma_commit(&bars[kDrain]);
-      int dummy = 0;
-      mbar_wait(&bars[kDrain], 0, &dummy, nullptr, 0);
+      mbar_wait(&bars[kDrain], 0, 0u, nullptr, 0);
     }
     __syncwarp();
   } else {
@@ -386,7 +384,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = Tx > 0;
     if (ok) {
       if (a.rotate_q) {
-        ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         const float4* tb = reinterpret_cast<const float4*>(a.table + static_cast<long long>(i) * (D / 2));
         if (ok && i < a.n_rows)
@@ -405,7 +403,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(&bars[kQReady0 + x]);
       } else if (a.decode) {
         // row i = b*G + hh of this kv head: its query at position p + len[b]
-        ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         const int bconv = i / a.dec_G;
         if (ok && bconv < a.dec_B) {
@@ -423,14 +421,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(&bars[kQReady0 + x]);
       } else {
         // the MMA thread waits on kQReady only: forward the TMA completion
-        ok = mbar_wait(&bars[kQFull], 0, abort_p, a.status, kDevErrTimeoutSoftmax);
+        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         mbar_arrive(&bars[kQReady0 + x]);
       }
     }
     const int i_cap = min(i, a.n_real - 1);
     for (int t = 0; t < Tx && ok; ++t) {
-      ok = mbar_wait(&bars[kSFull0 + x], t & 1, abort_p, a.status, kDevErrTimeoutSoftmax);
+      ok = mbar_wait(&bars[kSFull0 + x], t & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -515,7 +513,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     // ------------------------------------------------------------ epilogue --
     if (ok) {
-      ok = mbar_wait(&bars[kODone0 + x], 0, abort_p, a.status, kDevErrTimeoutEpilogue);
+      ok = mbar_wait(&bars[kODone0 + x], 0, abort_s, a.status, kDevErrTimeoutEpilogue);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {

@@ -17,6 +17,7 @@ enum : uint32_t {
   kDevErrTimeoutSoftmax = 1u << 2,
   kDevErrTimeoutEpilogue = 1u << 3,
   kDevErrBadSchedule = 1u << 4,
+  kDevErrSmemLayout = 1u << 5,  // dynamic shared memory not 1024-byte aligned
 };
 
 // Longest legitimate wait inside one kernel is microseconds; give up after
@@ -82,18 +83,30 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.  `abort` is a
-// CTA-shared flag: once any role of the CTA has given up, the others stop
-// waiting too.  Returns false on timeout or abort (and then sets both flags).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+// Volatile 32-bit shared-memory access by shared-window address.
+__device__ __forceinline__ uint32_t ld_volatile_shared(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_volatile_shared(uint32_t saddr, uint32_t v) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+
+// Bounded wait for the phase with the given parity to complete.  `abort_s` is
+// the shared-window address of a CTA-shared abort word (0: none): once any
+// role of the CTA has given up, the others stop waiting too.  Returns false
+// on timeout or abort (a timeout also sets the abort word and `err_bit` in
+// the status word).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t abort_s,
                                           uint32_t* status, uint32_t err_bit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-    if (*abort) return false;
+    if (abort_s && ld_volatile_shared(abort_s)) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs || it > (1u << 30)) {
-      *abort = 1;
+      if (abort_s) st_volatile_shared(abort_s, 1u);
       if (status) atomicOr(status, err_bit);
       return false;
     }
@@ -223,6 +236,35 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective issue: the whole converged warp executes these with
+// warp-uniform operands and one elected lane (the lowest active one, the
+// same lane every time) issues the instruction.  Keeping the issuing loop
+// warp-uniform lets the descriptors live in uniform registers, so each MMA
+// issues without per-instruction register moves.
+__device__ __forceinline__ void umma_bf16_ss_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 
