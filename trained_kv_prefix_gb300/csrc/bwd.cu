@@ -384,24 +384,24 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const bool key_ok = cart ? (j < a.p) : (j < a.n);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
+    // ring slots, their phases and (real tiles) the query tile of step u,
+    // advanced incrementally: no integer division in the per-step path
+    int sq = 0, sd = 0, qt = tile;
+    uint32_t phq = 0, phd = 0;
     for (int u = 0; u < U && ok; ++u) {
-      const int sq = u % SQ, sd = u % SD;
-      const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
       ok = mbar_wait(&bars[kStFull], u & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       // the step's -lse2 entries landed with Q (kQFull already complete: the
       // MMAs behind kStFull waited for it); waiting makes them visible
-      if (ok) ok = mbar_wait(&bars[kQFull0 + sq], (u / SQ) & 1, abort_s, a.status,
-                             kDevErrTimeoutSoftmax);
+      if (ok) ok = mbar_wait(&bars[kQFull0 + sq], phq, abort_s, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tst = tST + wg * 32 + lane_off;
       const uint32_t tdp = tDP + wg * 32 + lane_off;
-      // this group's columns c (query it.qt*128 + wg*32 + c) are invisible
+      // this group's columns c (query qt*128 + wg*32 + c) are invisible
       // for c < qlim: none for a cartridge key, query < key for a real key,
       // all for rows past the end of the keys
-      const int qlim =
-          !key_ok ? 32 : (cart ? 0 : max(0, min(32, j - it.qt * kTile - wg * 32)));
+      const int qlim = !key_ok ? 32 : (cart ? 0 : max(0, min(32, j - qt * kTile - wg * 32)));
       const uint32_t lse_s = smem_u32(vecL + sq * 128 + wg * 32);
       const uint32_t dv_s = smem_u32(vecD + sd * 128 + wg * 32);
       uint32_t r[32];
@@ -437,8 +437,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       ok = mbar_wait(&bars[kDpTFull], u & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       // the step's -D entries landed with dO (kDoFull already complete: the
       // MMAs behind kDpTFull waited for it); waiting makes them visible
-      if (ok) ok = mbar_wait(&bars[kDoFull0 + sd], (u / SD) & 1, abort_s, a.status,
-                             kDevErrTimeoutSoftmax);
+      if (ok) ok = mbar_wait(&bars[kDoFull0 + sd], phd, abort_s, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -464,6 +463,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kDsFull]);
+      if (++sq == SQ) sq = 0, phq ^= 1u;
+      if (++sd == SD) sd = 0, phd ^= 1u;
+      if (++qt == a.n_qtiles) qt = tile;  // real tiles: query tiles tile..n_qtiles-1
     }
     // ------------------------------------------------------------ epilogue --
     // warpgroups 0 and 1 write the two halves of dV; 2 and 3 take the RoPE
@@ -704,7 +706,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     __syncwarp();
   } else if (warp == 9) {
-    if (lane == 0 && T > 0) {
+    // ----------------------------------------------------------------- MMA --
+    // The whole warp runs this loop (warp-uniform descriptors); one elected
+    // lane issues each MMA and commit.
+    if (T > 0) {
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu,
+                          mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
+      };
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idDQ = idesc_bf16(128, D, false, true);
       const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
@@ -714,62 +723,60 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const uint64_t dVk0 = sdesc_sw128(smem_u32(smem + L::kV), 16u, 1024u);
       // C (f32, TMEM) = A (128 rows) * B^T (128 rows), both K-major over d
       auto issue_nt = [&](uint32_t c, uint64_t da, uint64_t db) {
-        umma_bf16_ss(c, da, db, idS, 0u);
+        umma_bf16_ss_w(c, da, db, idS, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss(c, desc_add(da, off), desc_add(db, off), idS, 1u);
+          umma_bf16_ss_w(c, desc_add(da, off), desc_add(db, off), idS, 1u);
         }
       };
-      bool ok = mbar_wait(&bars[kQdFull], 0, abort_s, a.status, kDevErrTimeoutMma) &&
-                mbar_wait(&bars[kKFull0], 0, abort_s, a.status, kDevErrTimeoutMma);
+      bool ok = wait(&bars[kQdFull], 0) &&
+                wait(&bars[kKFull0], 0);
       if (ok) {
         tc_fence_after();
         issue_nt(tS0, dQd, dKk0);
-        umma_commit(&bars[kSdFull0]);
-        ok = mbar_wait(&bars[kVFull0], 0, abort_s, a.status, kDevErrTimeoutMma);
+        umma_commit_w(&bars[kSdFull0]);
+        ok = wait(&bars[kVFull0], 0);
       }
       if (ok) {
         tc_fence_after();
         issue_nt(tDP, dOd, dVk0);
-        umma_commit(&bars[kDpFull]);
-        umma_commit(&bars[kVEmpty0]);
+        umma_commit_w(&bars[kDpFull]);
+        umma_commit_w(&bars[kVEmpty0]);
       }
       for (int t = 0; t < T && ok; ++t) {
         const int x = t & 1;
         if (t + 1 < T) {
           const int sk = (t + 1) % SK, sv = (t + 1) % SV;
-          ok = mbar_wait(&bars[kKFull0 + sk], ((t + 1) / SK) & 1, abort_s, a.status,
-                         kDevErrTimeoutMma);
+          ok = wait(&bars[kKFull0 + sk], ((t + 1) / SK) & 1);
           if (!ok) break;
           tc_fence_after();
           // buffer x^1 last held dS(t-1), read by dQ(t-1) issued earlier
           // (one CTA's MMAs run in issue order)
           issue_nt(tS0 + (x ^ 1) * 128, dQd, desc_add(dKk0, sk * L::kTileBytes));
-          umma_commit(&bars[kSdFull0 + (x ^ 1)]);
-          ok = mbar_wait(&bars[kDpFree], t & 1, abort_s, a.status, kDevErrTimeoutMma) &&
-               mbar_wait(&bars[kVFull0 + sv], ((t + 1) / SV) & 1, abort_s, a.status,
-                         kDevErrTimeoutMma);
+          umma_commit_w(&bars[kSdFull0 + (x ^ 1)]);
+          ok = wait(&bars[kDpFree], t & 1) &&
+               wait(&bars[kVFull0 + sv], ((t + 1) / SV) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_nt(tDP, dOd, desc_add(dVk0, sv * L::kTileBytes));
-          umma_commit(&bars[kDpFull]);
-          umma_commit(&bars[kVEmpty0 + sv]);
+          umma_commit_w(&bars[kDpFull]);
+          umma_commit_w(&bars[kVEmpty0 + sv]);
         }
-        ok = mbar_wait(&bars[kDsdFull0 + x], (t >> 1) & 1, abort_s, a.status, kDevErrTimeoutMma);
+        ok = wait(&bars[kDsdFull0 + x], (t >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
         const int sk = t % SK;
         const uint64_t dkm = desc_add(dKm0, sk * L::kTileBytes);
         const uint32_t ds = tS0 + x * 128;
-        umma_bf16_ts(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
+        umma_bf16_ts_w(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(tDQ, ds + (k >> 2) * 64 + (k & 3) * 8, desc_add(dkm, k * 2048), idDQ, 1u);
-        umma_commit(&bars[kKEmpty0 + sk]);
+          umma_bf16_ts_w(tDQ, ds + (k >> 2) * 64 + (k & 3) * 8, desc_add(dkm, k * 2048), idDQ, 1u);
+        umma_commit_w(&bars[kKEmpty0 + sk]);
       }
-      if (ok) umma_commit(&bars[kDqDone]);
-      umma_commit(&bars[kDqDrain]);
+      if (ok) umma_commit_w(&bars[kDqDone]);
+      umma_commit_w(&bars[kDqDrain]);
       mbar_wait(&bars[kDqDrain], 0, 0u, nullptr, 0);
     }
     __syncwarp();

@@ -287,7 +287,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ----------------------------------------------------------------- MMA --
-    if (lane == 0 && T > 0) {
+    // The whole warp runs this loop (warp-uniform descriptors); one elected
+    // lane issues each MMA and commit.
+    if (T > 0) {
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu,
+                          mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
+      };
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idPV = idesc_bf16(128, D, false, true);
       // Base descriptors, computed once; each MMA adds an offset.
@@ -303,13 +309,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint64_t dq = x ? dQ1 : dQ0;
         const uint64_t dk = (t & 1) ? dK1 : dK0;
         const uint32_t ts = tmem + x * 128;
-        umma_bf16_ss(ts, dq, dk, idS, 0u);
+        umma_bf16_ss_w(ts, dq, dk, idS, 0u);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss(ts, desc_add(dq, off), desc_add(dk, off), idS, 1u);
+          umma_bf16_ss_w(ts, desc_add(dq, off), desc_add(dk, off), idS, 1u);
         }
-        umma_commit(&bars[kSFull0 + x]);
+        umma_commit_w(&bars[kSFull0 + x]);
       };
       // O_x += P_x V(t): P from TMEM (K step k of 16 keys = 8 packed columns
       // at 8k), V MN-major (16 rows = 2048 B per K step).
@@ -317,57 +323,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint64_t dv = (t & 1) ? dV1 : dV0;
         const uint32_t tp = tmem + x * 128;
         const uint32_t to = tmem + 256 + x * 128;
-        umma_bf16_ts(to, tp, dv, idPV, t > 0 ? 1u : 0u);
+        umma_bf16_ts_w(to, tp, dv, idPV, t > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts(to, tp + k * 8, desc_add(dv, k * 2048), idPV, 1u);
+          umma_bf16_ts_w(to, tp + k * 8, desc_add(dv, k * 2048), idPV, 1u);
       };
-      bool ok = mbar_wait(&bars[kQReady0], 0, abort_s, a.status, kDevErrTimeoutMma) &&
-                mbar_wait(&bars[kKFull0], 0, abort_s, a.status, kDevErrTimeoutMma);
+      bool ok = wait(&bars[kQReady0], 0) &&
+                wait(&bars[kKFull0], 0);
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
       }
       if (ok && hasB) {
-        ok = mbar_wait(&bars[kQReady1], 0, abort_s, a.status, kDevErrTimeoutMma);
+        ok = wait(&bars[kQReady1], 0);
         if (ok) {
           tc_fence_after();
           issue_qk(1, 0);
         }
       }
-      if (ok) umma_commit(&bars[kKEmpty0]);
+      if (ok) umma_commit_w(&bars[kKEmpty0]);
       for (int t = 0; t < T && ok; ++t) {
         const int s = t & 1;
-        ok = mbar_wait(&bars[kVFull0 + s], (t >> 1) & 1, abort_s, a.status, kDevErrTimeoutMma);
+        ok = wait(&bars[kVFull0 + s], (t >> 1) & 1);
         if (!ok) break;
         const bool next = t + 1 < T;
         if (t < T_A) {
-          ok = mbar_wait(&bars[kPFull0], t & 1, abort_s, a.status, kDevErrTimeoutMma);
+          ok = wait(&bars[kPFull0], t & 1);
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, t);
-          if (t == T_A - 1) umma_commit(&bars[kODone0]);
+          if (t == T_A - 1) umma_commit_w(&bars[kODone0]);
         }
         if (next) {
-          ok = mbar_wait(&bars[kKFull0 + (s ^ 1)], ((t + 1) >> 1) & 1, abort_s, a.status,
-                         kDevErrTimeoutMma);
+          ok = wait(&bars[kKFull0 + (s ^ 1)], ((t + 1) >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
           if (t + 1 < T_A) issue_qk(0, t + 1);
         }
         if (t < T_B) {
-          ok = mbar_wait(&bars[kPFull1], t & 1, abort_s, a.status, kDevErrTimeoutMma);
+          ok = wait(&bars[kPFull1], t & 1);
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, t);
-          if (t == T_B - 1) umma_commit(&bars[kODone1]);
+          if (t == T_B - 1) umma_commit_w(&bars[kODone1]);
           if (t + 1 < T_B) issue_qk(1, t + 1);
         }
-        umma_commit(&bars[kVEmpty0 + s]);
-        if (next) umma_commit(&bars[kKEmpty0 + (s ^ 1)]);
+        umma_commit_w(&bars[kVEmpty0 + s]);
+        if (next) umma_commit_w(&bars[kKEmpty0 + (s ^ 1)]);
       }
       // Drain: every MMA issued above completes before the CTA tears down.
-      umma_commit(&bars[kDrain]);
+      umma_commit_w(&bars[kDrain]);
       mbar_wait(&bars[kDrain], 0, 0u, nullptr, 0);
     }
     __syncwarp();
@@ -451,13 +456,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (c >= valid) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
       // row maximum of the raw scores (scale_log2 > 0), 4 independent chains
+      // of three-input maxima
       float mx[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        float v = __uint_as_float(r[q][0]);
+        float v = fmax3(__uint_as_float(r[q][0]), __uint_as_float(r[q][1]),
+                        __uint_as_float(r[q][2]));
 #pragma unroll
-        for (int c = 1; c < 32; ++c) v = fmaxf(v, __uint_as_float(r[q][c]));
-        mx[q] = v;
+        for (int c = 3; c < 31; c += 2)
+          v = fmax3(v, __uint_as_float(r[q][c]), __uint_as_float(r[q][c + 1]));
+        mx[q] = fmaxf(v, __uint_as_float(r[q][31]));
       }
       const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
       // Lazy rescaling: keep the stale max unless the new one exceeds it by
@@ -469,31 +477,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m = rmax;
         rescale = t > 0;
       }
-      const float neg_m = -m;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(S * scale * log2(e) - m), two keys per packed two-lane op
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      const float2 nm2 = make_float2(-m, -m);
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int q = 0; q < 4; q += 2) {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float p0 = exp2_approx(fmaf(__uint_as_float(r[q][2 * c]), a.scale_log2, neg_m));
-          const float p1 =
-              exp2_approx(fmaf(__uint_as_float(r[q][2 * c + 1]), a.scale_log2, neg_m));
-          const float p2 =
-              exp2_approx(fmaf(__uint_as_float(r[q + 1][2 * c]), a.scale_log2, neg_m));
-          const float p3 =
-              exp2_approx(fmaf(__uint_as_float(r[q + 1][2 * c + 1]), a.scale_log2, neg_m));
-          rs[q] += p0;
-          rs[q + 1] += p1;
-          rs[(q + 2) & 3] += p2;
-          rs[(q + 3) & 3] += p3;
-          pk[c] = pack_bf16x2(p0, p1);
-          pk[16 + c] = pack_bf16x2(p2, p3);
+          const float2 x0 = __ffma2_rn(u2f2(r[q][2 * c], r[q][2 * c + 1]), sc2, nm2);
+          const float2 x1 = __ffma2_rn(u2f2(r[q + 1][2 * c], r[q + 1][2 * c + 1]), sc2, nm2);
+          const float2 p01 = make_float2(exp2_approx(x0.x), exp2_approx(x0.y));
+          const float2 p23 = make_float2(exp2_approx(x1.x), exp2_approx(x1.y));
+          rs[(c & 1) * 2] = __fadd2_rn(rs[(c & 1) * 2], p01);
+          rs[(c & 1) * 2 + 1] = __fadd2_rn(rs[(c & 1) * 2 + 1], p23);
+          pk[c] = pack_bf16x2(p01.x, p01.y);
+          pk[16 + c] = pack_bf16x2(p23.x, p23.y);
         }
         // keys 32q .. 32q + 63 -> packed columns 16q .. 16q + 31
         tmem_st32(tS + 16 * q, pk);
       }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      const float2 rs01 = __fadd2_rn(rs[0], rs[1]), rs23 = __fadd2_rn(rs[2], rs[3]);
+      l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
       if (__any_sync(0xffffffffu, rescale)) {
         // PV(t-1) has completed: the commit that published S(t) follows it.
 #pragma unroll
@@ -502,8 +509,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_ld32(tO + blk * 32, o);
           tmem_ld_wait();
           tmem_reg_fence(o);
+          const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          for (int c = 0; c < 32; c += 2) {
+            const float2 v = __fmul2_rn(u2f2(o[c], o[c + 1]), al2);
+            o[c] = __float_as_uint(v.x);
+            o[c + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + blk * 32, o);
         }
       }
