@@ -75,16 +75,17 @@ __device__ __forceinline__ void store_row_out(void* base, long long off, const f
 // group owns key row t = TMEM lane t); warp 16 is the TMA producer, warp 17
 // issues the MMAs.  Every MMA has N = 128.
 // TMEM (512 columns): S^T at 0, dP^T at 128 (f32), dV at 256, dK at 384.
-// A warpgroup loads its 32 S^T columns and releases S^T at once, so that the
-// next step's S^T is computed while it works; it forms P^T in registers
-// (while dP^T is still being computed), then loads its dP^T columns and
-// overwrites that 32-column slice with P^T (first 16 columns) and dS^T
-// (last 16) packed as bf16 pairs.  dV and dK read them as their A operand
-// straight from TMEM (K step k of 16 queries at column 128 + (k/2)*32 +
-// (k%2)*8, plus 16 for dS^T).  MMA order per step u:
-//   S^T(u+1) [after S^T(u) is released], dK(u), dV(u) [after P^T / dS^T(u)],
-//   dP^T(u+1) -- which overwrites P^T / dS^T(u) after dK(u) and dV(u) have
-// read them (one CTA's MMAs run in issue order).
+// A warpgroup loads its 32 S^T columns, forms P^T and writes it packed as
+// bf16 pairs over the first 16 of them (P phase); it later loads its 32 dP^T
+// columns and writes dS^T the same way over the first 16 of those (dS
+// phase).  dV and dK read P^T / dS^T as their A operand straight from TMEM
+// (K step k of 16 queries at column (k/2)*32 + (k%2)*8 of the region).
+// MMA order per step u:
+//   dV(u) [after the P phase], S^T(u+1), dK(u) [after the dS phase], dP^T(u+1)
+// so that dV(u) and S^T(u+1) run during the dS phase and dK(u), dP^T(u+1)
+// during the next P phase; S^T(u+1) overwrites P^T(u) after dV(u) has read
+// it, dP^T(u+1) overwrites dS^T(u) after dK(u) (one CTA's MMAs run in issue
+// order).
 // Q and dO have rings of their own: a Q slot is released by dK(u), a dO
 // slot by dV(u).  Q gets three slots, so a Q tile is copied while two full
 // steps of MMAs run; dO gets two (its first reader, dP^T, comes later in the
@@ -112,7 +113,7 @@ struct DkdvSmem {
 
 enum DkdvBar { kResFull = 0, kQFull0, kQEmpty0 = kQFull0 + kDkdvQSlots,
                kDoFull0 = kQEmpty0 + kDkdvQSlots, kDoEmpty0 = kDoFull0 + kDkdvDoSlots,
-               kStFull = kDoEmpty0 + kDkdvDoSlots, kStFree, kDpTFull, kDsFull, kAccDone,
+               kStFull = kDoEmpty0 + kDkdvDoSlots, kPtFull, kDpTFull, kDsFull, kAccDone,
                kDkdvDrain, kDkdvBars };
 static_assert(kDkdvBars * 8 + 16 <= 256, "dK/dV barrier area");
 
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       mbar_init(&bars[kDoEmpty0 + s], 1);
     }
     mbar_init(&bars[kStFull], 1);
-    mbar_init(&bars[kStFree], 512);
+    mbar_init(&bars[kPtFull], 512);
     mbar_init(&bars[kDpTFull], 1);
     mbar_init(&bars[kDsFull], 512);
     mbar_init(&bars[kAccDone], 1);
@@ -317,12 +318,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           umma_bf16_ss_w(c, desc_add(da, off), desc_add(db, off), idST, 1u);
         }
       };
-      auto issue_st_dpt = [&](int u, bool st) {
+      // S^T = K Q^T from Q slot `slot`, or dP^T = V dO^T from dO slot `slot`
+      auto issue_st_dpt = [&](int slot, bool st) {
         if (st) {
-          issue_nt(tST, dK0, desc_add(dQk0, (u % SQ) * L::kTileBytes));
+          issue_nt(tST, dK0, desc_add(dQk0, slot * L::kTileBytes));
           umma_commit_w(&bars[kStFull]);
         } else {
-          issue_nt(tDP, dV0, desc_add(dOk0, (u % SD) * L::kTileBytes));
+          issue_nt(tDP, dV0, desc_add(dOk0, slot * L::kTileBytes));
           umma_commit_w(&bars[kDpTFull]);
         }
       };
@@ -335,41 +337,51 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         tc_fence_after();
         if (ok) issue_st_dpt(0, false);
       }
+      // ring slots and phases advance incrementally (no division per step)
+      int sq = 0, sd = 0, sq1 = 1 % SQ, sd1 = 1 % SD;
+      uint32_t ph1q = SQ == 1 ? 1u : 0u, ph1d = SD == 1 ? 1u : 0u;  // phases of slot u+1
       for (int u = 0; u < U && ok; ++u) {
-        const int sq = u % SQ, sd = u % SD;
         const bool next = u + 1 < U;
-        if (next) {  // S^T(u+1) as soon as the warpgroups hold S^T(u)
-          ok = wait(&bars[kStFree], u & 1) &&
-               wait(&bars[kQFull0 + (u + 1) % SQ], ((u + 1) / SQ) & 1);
+        const uint32_t first = u > 0 ? 1u : 0u;
+        // dV += P^T dO: A = P^T from TMEM (over S^T), B = the step's dO tile
+        // as an MN-major operand (16 rows = 2048 B per K step)
+        ok = wait(&bars[kPtFull], u & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ddo = desc_add(dOm0, sd * L::kTileBytes);
+        umma_bf16_ts_w(tDV, tST, ddo, idACC, first);
+#pragma unroll
+        for (int k = 1; k < kTile / 16; ++k)
+          umma_bf16_ts_w(tDV, tST + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC,
+                         1u);
+        umma_commit_w(&bars[kDoEmpty0 + sd]);
+        if (next) {  // S^T(u+1) over P^T(u), after dV(u) in issue order
+          ok = wait(&bars[kQFull0 + sq1], ph1q);
           if (!ok) break;
           tc_fence_after();
-          issue_st_dpt(u + 1, true);
+          issue_st_dpt(sq1, true);
         }
+        // dK += dS^T Q: A = dS^T from TMEM (over dP^T), B = the Q tile
         ok = wait(&bars[kDsFull], u & 1);
         if (!ok) break;
         tc_fence_after();
-        // dK += dS^T Q, then dV += P^T dO: A from TMEM (over dP^T), B = the
-        // step's Q / dO tile as MN-major operands (16 rows = 2048 B per K step)
         const uint64_t dq = desc_add(dQm0, sq * L::kTileBytes);
-        const uint64_t ddo = desc_add(dOm0, sd * L::kTileBytes);
-        const uint32_t first = u > 0 ? 1u : 0u;
-        umma_bf16_ts_w(tDK, tDP + 16, dq, idACC, first);
+        umma_bf16_ts_w(tDK, tDP, dq, idACC, first);
 #pragma unroll
         for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts_w(tDK, tDP + 16 + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC,
-                       1u);
+          umma_bf16_ts_w(tDK, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(dq, k * 2048), idACC,
+                         1u);
         umma_commit_w(&bars[kQEmpty0 + sq]);
-        umma_bf16_ts_w(tDV, tDP, ddo, idACC, first);
-#pragma unroll
-        for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts_w(tDV, tDP + (k >> 1) * 32 + (k & 1) * 8, desc_add(ddo, k * 2048), idACC, 1u);
-        umma_commit_w(&bars[kDoEmpty0 + sd]);
-        if (next) {
-          ok = wait(&bars[kDoFull0 + (u + 1) % SD], ((u + 1) / SD) & 1);
+        if (next) {  // dP^T(u+1) over dS^T(u), after dK(u) in issue order
+          ok = wait(&bars[kDoFull0 + sd1], ph1d);
           if (!ok) break;
           tc_fence_after();
-          issue_st_dpt(u + 1, false);
+          issue_st_dpt(sd1, false);
         }
+        sq = sq1;
+        sd = sd1;
+        if (++sq1 == SQ) sq1 = 0, ph1q ^= 1u;
+        if (++sd1 == SD) sd1 = 0, ph1d ^= 1u;
       }
       if (ok) umma_commit_w(&bars[kAccDone]);
       umma_commit_w(&bars[kDkdvDrain]);
@@ -408,10 +420,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_ld32(tst, r);
       tmem_ld_wait();
       tmem_reg_fence(r);
-      tc_fence_before();
-      mbar_arrive(&bars[kStFree]);  // S^T(u+1) may overwrite S^T(u) now
-      // P^T = 2^(S^T * scale * log2(e) - lse2) (f32, kept in p) while dP^T
-      // is still being computed; two queries per packed two-lane op
+      // P^T = 2^(S^T * scale * log2(e) - lse2) (f32, kept in p for dS^T)
+      // while dP^T is still being computed; two queries per packed op
       const bool masked = __any_sync(0xffffffffu, qlim > 0);
       const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
       float2 p[16];
@@ -431,9 +441,16 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           p[c].y = (2 * c + 1 >= qlim) ? p[c].y : 0.f;
         }
       }
-      uint32_t pk[16];
+      {
+        // P^T packed over the first 16 of this group's S^T columns (read)
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[c].x, p[c].y);
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[c].x, p[c].y);
+        tmem_st16(tst, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kPtFull]);
+      }
       ok = mbar_wait(&bars[kDpTFull], u & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       // the step's -D entries landed with dO (kDoFull already complete: the
       // MMAs behind kDpTFull waited for it); waiting makes them visible
@@ -456,10 +473,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         pd[2 * c4] = pack_bf16x2(ds0.x, ds0.y);
         pd[2 * c4 + 1] = pack_bf16x2(ds1.x, ds1.y);
       }
-      // P^T over the first 16 and dS^T over the last 16 of this group's dP^T
-      // columns (already read)
-      tmem_st16(tdp, pk);
-      tmem_st16(tdp + 16, pd);
+      // dS^T packed over the first 16 of this group's dP^T columns (read)
+      tmem_st16(tdp, pd);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kDsFull]);
