@@ -192,6 +192,7 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
 // cartridge, and the TMA maps over them.
 struct TrainPrep {
   const float2* table;
+  RopeFreqs freqs;
   bool q_in_kernel;
   const void* qr;  // rotated bf16 queries, or q itself when q_in_kernel
   const void* kr;
@@ -256,6 +257,7 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
     vcb = tv;
   }
   out->table = table;
+  out->freqs = freqs;
   out->q_in_kernel = q_in_kernel;
   out->qr = qr;
   out->kr = kr;
@@ -463,6 +465,7 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.dvc = dvc;
   l.accumulate = accumulate;
   l.table = tp.table;
+  l.freqs = &tp.freqs;
   SideStream* side = side_stream();
   if (!side) {
     CART_CUDA(launch_bwd(l, st, st));

@@ -52,6 +52,8 @@ struct BwdParams {
   const float2* table;
   uint32_t* status;
   int tma_dq;  // bf16 dQ stored by TMA through mdQ
+  // RoPE angle of pair c at position x, in turns: x * (turns[c].x + turns[c].y)
+  float2 turns[kMaxHeadDim / 2];
 };
 
 __device__ __forceinline__ void store_row_out(void* base, long long off, const float* x, int n,
@@ -535,10 +537,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             write_cart_row(dst + w2 * QP, lo, QP, frozen, a.accumulate);
             write_cart_row(dst + D / 2 + w2 * QP, hi, QP, frozen, a.accumulate);
           } else {
-            const float2* tb = a.table + static_cast<long long>(j) * (D / 2) + w2 * QP;
+            // inverse rotation at position p + j; (cos, sin) computed here:
+            // one row of table per thread would be gathered uncoalesced
 #pragma unroll
             for (int e = 0; e < QP; ++e) {
-              const float2 cs = __ldg(tb + e);
+              const float2 cs = rope_cs_turns_fast(a.turns[w2 * QP + e], a.p + j);
               const float x0 = lo[e], x1 = hi[e];
               lo[e] = x0 * cs.x + x1 * cs.y;
               hi[e] = x1 * cs.x - x0 * cs.y;
@@ -886,10 +889,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int e = 0; e < 16; ++e) hi[c * 16 + e] = __uint_as_float(r[e]) * a.scale;
       }
       if (i < a.n) {
-        const float2* tb = a.table + static_cast<long long>(i) * (D / 2) + wg * Q;
+        // inverse rotation at position p + i; (cos, sin) computed here: one
+        // row of table per thread would be gathered uncoalesced
 #pragma unroll
         for (int e = 0; e < Q; ++e) {
-          const float2 cs = __ldg(tb + e);
+          const float2 cs = rope_cs_turns_fast(a.turns[wg * Q + e], a.p + i);
           const float x0 = lo[e], x1 = hi[e];
           lo[e] = x0 * cs.x + x1 * cs.y;
           hi[e] = x1 * cs.x - x0 * cs.y;
@@ -965,6 +969,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.dvc = l.dvc;
   p.accumulate = l.accumulate;
   p.table = l.table;
+  for (int c = 0; c < D / 2; ++c) p.turns[c] = l.freqs->turns[c];
   p.status = device_status_ptr();
   cudaError_t e = set_smem_once<dkdv_kernel<D>>(DkdvSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;

@@ -189,6 +189,7 @@ struct BwdLaunch {
   float* dvc;
   int accumulate;
   const float2* table;      // rope table for positions p .. p+n-1
+  const RopeFreqs* freqs;   // rope angles (the epilogues' inverse rotation)
 };
 // dK/dV kernel on st_dkdv, dQ kernel on st_dq (the two are independent).
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st_dkdv, cudaStream_t st_dq);
