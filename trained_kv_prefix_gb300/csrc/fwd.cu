@@ -140,6 +140,66 @@ __device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, CS cs) {
   }
 }
 
+// Training-forward Q rotation by table rows, one warp per 32 rows of a
+// 128-row tile: the warp takes one row at a time and lane l holds RoPE pairs
+// [l*PPL, (l + 1)*PPL), so each table row is read coalesced (one thread per
+// row would gather a table row per lane) and each row's pair halves are
+// 128-byte shared-memory segments.  Same arithmetic as rope_pair on the
+// table's (cos, sin): the bits equal those of the prep kernel's rotation.
+template <int D>
+struct RopeRowsCoop {
+  static constexpr int PPL = D / 64;  // pairs per lane
+  float2 cs[32][PPL];
+  // (cos, sin) of rows i0 .. i0 + 31 (rows at or past n_rows are skipped)
+  __device__ __forceinline__ void load(const float2* table, int i0, int n_rows, int lane) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      if (i0 + r < n_rows) {
+        const float2* t = table + static_cast<long long>(i0 + r) * (D / 2) + lane * PPL;
+        if (PPL == 2) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(t));
+          cs[r][0] = make_float2(v.x, v.y);
+          cs[r][PPL - 1] = make_float2(v.z, v.w);
+        } else {
+          cs[r][0] = __ldg(t);
+        }
+      }
+    }
+  }
+  // rotate tile rows r0 .. r0 + 31 in place (SW128 layout, 64-column chunks
+  // 16 KB apart)
+  __device__ __forceinline__ void apply(uint8_t* sQ, int r0, int i0, int n_rows, int lane) const {
+    const uint32_t base = smem_u32(sQ);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      if (i0 + r >= n_rows) break;
+      const uint32_t row = static_cast<uint32_t>(r0 + r);
+      if (PPL == 2) {
+        // elements 2l, 2l+1 (chunk 0) and 64+2l, 64+2l+1 (chunk 1)
+        const uint32_t o = sw128_offset(row, static_cast<uint32_t>(lane) >> 2) + (lane & 3) * 4;
+        const float2 a = bf16x2_to_float2(lds_u32(base + o));
+        const float2 b = bf16x2_to_float2(lds_u32(base + 16384u + o));
+        float y0a, y1a, y0b, y1b;
+        rope_pair(a.x, b.x, cs[r][0], y0a, y1a);
+        rope_pair(a.y, b.y, cs[r][PPL - 1], y0b, y1b);
+        sts_u32(base + o, pack_bf16x2(y0a, y0b));
+        sts_u32(base + 16384u + o, pack_bf16x2(y1a, y1b));
+      } else {
+        // element l (16-byte chunk l/8) and l + 32 (chunk 4 + l/8)
+        const uint32_t oa = sw128_offset(row, static_cast<uint32_t>(lane) >> 3) + (lane & 7) * 2;
+        const uint32_t ob = sw128_offset(row, 4u + (static_cast<uint32_t>(lane) >> 3)) + (lane & 7) * 2;
+        const float xa = __uint_as_float(static_cast<uint32_t>(lds_u16(base + oa)) << 16);
+        const float xb = __uint_as_float(static_cast<uint32_t>(lds_u16(base + ob)) << 16);
+        float y0, y1;
+        rope_pair(xa, xb, cs[r][0], y0, y1);
+        const uint32_t pk = pack_bf16x2(y0, y1);
+        sts_u16(base + oa, static_cast<uint16_t>(pk & 0xFFFFu));
+        sts_u16(base + ob, static_cast<uint16_t>(pk >> 16));
+      }
+    }
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
@@ -389,21 +449,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     bool ok = Tx > 0;
     if (ok) {
       if (a.rotate_q) {
+        // this warp's 32 rows: table rows fetched while the Q tile lands
+        const int r0 = (warp & 3) * 32;
+        const int i0 = (2 * pair + x) * kTile + r0;
+        RopeRowsCoop<D> rr;
+        rr.load(a.table, i0, a.n_rows, lane);
         ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
-        const float4* tb = reinterpret_cast<const float4*>(a.table + static_cast<long long>(i) * (D / 2));
-        if (ok && i < a.n_rows)
-          rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
-                          [&](int j0, float2* c) {
-                            float4 v[16];
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) v[q] = __ldg(tb + j0 / 2 + q);
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                              c[2 * q] = make_float2(v[q].x, v[q].y);
-                              c[2 * q + 1] = make_float2(v[q].z, v[q].w);
-                            }
-                          });
+        if (ok) rr.apply(smem + L::kQ + x * L::kTileBytes, r0, i0, a.n_rows, lane);
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
       } else if (a.decode) {

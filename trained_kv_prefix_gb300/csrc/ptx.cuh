@@ -151,6 +151,24 @@ __device__ __forceinline__ void sts_u4(uint32_t saddr, uint4 v) {
                : "memory");
 }
 
+// 4- and 2-byte shared-memory accesses by shared-window address.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t lds_u16(uint32_t saddr) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(saddr));
+  return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t saddr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(saddr), "h"(v) : "memory");
+}
+
 // 16-byte load from shared memory by shared-window address.
 __device__ __forceinline__ float4 lds128(uint32_t saddr) {
   float4 v;
