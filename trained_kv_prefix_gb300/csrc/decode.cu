@@ -40,8 +40,9 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 //     (128-byte swizzled layout; only the 16-row groups the chunk covers,
 //     rows past the end zero-filled) while the previous chunk is computed.
 //   * The block rotates the group's G queries at position p+len (one
-//     fp64-reduced cos/sin per frequency, shared through shared memory)
-//     straight into mma.sync B fragments (queries padded to 8 columns).
+//     cos/sin per frequency from the all-f32 turn reduction and the hardware
+//     sine / cosine, shared through shared memory) straight into mma.sync B
+//     fragments (queries padded to 8 columns).
 //   * The CTA whose unit holds row len writes the new token's rotated key
 //     and its value into that cache row and patches its shared copy.
 //   * Per chunk: S^T = K Q^T with mma.sync m16n8k16 (keys as M: warp w owns
@@ -94,17 +95,6 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int row, int dc) {
   return base + (dc >> 3) * (kPrivCH * 128) + row * 128 + ((((dc & 7) ^ (row & 7))) << 4);
 }
 
-__device__ __forceinline__ float2 rope_cs(const RopeFreqs& f, int j, int pos) {
-  const double ang = static_cast<double>(pos) * f.inv_freq[j];
-  const double k = rint(ang * 0.15915494309189535);
-  double r = fma(-k, 6.283185307179586232, ang);
-  r = fma(-k, 2.4492935982947064e-16, r);
-  const float rh = static_cast<float>(r);
-  const float rl = static_cast<float>(r - static_cast<double>(rh));
-  float s, c;
-  sincosf(rh, &s, &c);
-  return make_float2(c - s * rl, s + c * rl);
-}
 
 template <int D, int G>
 __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, const RopeFreqs f,
@@ -162,7 +152,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
   for (int c = 0; c < kPrivStages && c < nc; ++c) stage(c);
-  if (tid < HALF) scs[tid] = rope_cs(f, tid, pos);
+  if (tid < HALF) scs[tid] = rope_cs_turns_fast(f.turns[tid], pos);
   __syncthreads();
 
   // ---- rotated queries as B fragments: bq[k][0] = q[g8][16k + 2tig, +1],
