@@ -36,9 +36,11 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 // owns private rows [u*U, min((u+1)*U, len+1)) of kv head g of conversation
 // b (U = kDecodeUnit; CTAs past the end of a conversation exit at once) and
 // streams them through a kPrivStages-deep ring of 64-row chunks:
-//   * 16-byte cp.async copies stage a chunk's K and V rows in shared memory
-//     (128-byte swizzled layout; only the 16-row groups the chunk covers,
-//     rows past the end zero-filled) while the previous chunk is computed.
+//   * Thread 0 stages a chunk's K and V rows in shared memory by TMA (one
+//     (64, 1, 64, 1) box per 64-dim half, 128-byte swizzled, completing on
+//     the slot's mbarrier) while the previous chunk is computed; staged V
+//     rows past the unit's end are zeroed after they land (the cache may
+//     hold anything there, and 0 * a non-finite value is not 0).
 //   * The block rotates the group's G queries at position p+len (one
 //     cos/sin per frequency from the all-f32 turn reduction and the hardware
 //     sine / cosine, shared through shared memory) straight into mma.sync B
@@ -53,7 +55,6 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 //   * Output: the unit's normalised O and its log2-domain log-sum-exp.
 constexpr int kPrivCH = kDecodeChunk;  // keys per chunk
 constexpr int kPrivStages = 2;
-static_assert(kPrivStages >= 1 && kPrivStages <= 4, "cp.async.wait_group counts below");
 
 template <int D>
 struct PrivSmem {
@@ -64,7 +65,8 @@ struct PrivSmem {
   static constexpr int kPStride = kPrivCH + 8;         // padded row: conflict-free B loads
   static constexpr int kCS = kP + 8 * kPStride * 2;    // float2 [D/2]
   static constexpr int kRed = kCS + (D / 2) * 8;       // f32 [2][4 warps][8]
-  static constexpr int kBytes = kRed + 2 * 4 * 8 * 4;
+  static constexpr int kBar = kRed + 2 * 4 * 8 * 4;    // full[kPrivStages], abort word
+  static constexpr int kBytes = kBar + kPrivStages * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -97,13 +99,27 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int row, int dc) {
 
 
 template <int D, int G>
-__global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, const RopeFreqs f,
-                                                             float scale_log2) {
+__global__ void __launch_bounds__(128) decode_private_kernel(
+    const __grid_constant__ CUtensorMap mKs, const __grid_constant__ CUtensorMap mVs,
+    DecodeLaunch a, const RopeFreqs f, float scale_log2) {
   using L = PrivSmem<D>;
   constexpr int CH = kPrivCH;
   constexpr int HALF = D / 2;
   static_assert(CH == 64, "four warps own 16 keys each");
   const int g = blockIdx.x, b = blockIdx.y, u = blockIdx.z;
+  // the query words first: their global latency overlaps the length load,
+  // the staging and the angles below
+  uint32_t qraw[D / 16][2];
+  {
+    const int g8q = (threadIdx.x & 31) >> 2, tigq = threadIdx.x & 3;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        a.q + (static_cast<long long>(b) * a.Hq + g * G + (g8q < G ? g8q : 0)) * D);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        qraw[k][hf] = g8q < G ? __ldg(qrow + 8 * k + 4 * hf + tigq) : 0u;
+  }
   const int Lb = clamp_len(a.len, b, a.rows);
   const int k_lo = u * kDecodeUnit;
   if (k_lo > Lb) {
@@ -121,35 +137,29 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
   const int nk = min(kDecodeUnit, Lb + 1 - k_lo);  // keys of this unit
   const int nc = (nk + CH - 1) / CH;               // chunks
   const int pos = a.p + Lb;
-  const long long rstride = static_cast<long long>(a.Hkv) * D;
-  const __nv_bfloat16* kg0 =
-      a.k_cache + (static_cast<long long>(b) * a.rows + k_lo) * rstride + g * D;
-  const __nv_bfloat16* vg0 =
-      a.v_cache + (static_cast<long long>(b) * a.rows + k_lo) * rstride + g * D;
-  const uint32_t sbase = smem_u32(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  int* abort_flag = reinterpret_cast<int*>(full + kPrivStages);
+  const uint32_t abort_s = smem_u32(abort_flag);
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s2 = 0; s2 < kPrivStages; ++s2) mbar_init(&full[s2], 1);
+    fence_mbar_init();
+  }
 
-  // Stage chunk c into ring slot c % kPrivStages: rows 0..16*ceil(kn/16) of K and V
-  // with 16-byte cp.async copies, rows >= kn of the last 16-row group
-  // zero-filled (so P = 0 never meets stale data).
+  // Stage chunk c into ring slot c % kPrivStages (thread 0): the K and V rows
+  // of the chunk by TMA, 64 rows per box (rows past the cache's end read as
+  // zero; rows past the unit's end are whatever the cache holds).
   auto stage = [&](int c) {
-    constexpr int kPieces = D / 8;  // 16-byte pieces per row
-    const int k0 = c * CH;
-    const int kn = min(CH, nk - k0);
-    const int rows16 = (kn + 15) & ~15;
-    const uint32_t sK = sbase + (c % kPrivStages) * L::kStage, sV = sK + L::kTile;
-    const __nv_bfloat16* kg = kg0 + static_cast<long long>(k0) * rstride;
-    const __nv_bfloat16* vg = vg0 + static_cast<long long>(k0) * rstride;
-    for (int t = tid; t < rows16 * kPieces; t += 128) {
-      const int rr = t / kPieces, dc = t % kPieces;
-      const uint32_t so = tile_chunk(0, rr, dc);
-      const int src_bytes = rr < kn ? 16 : 0;
-      const long long go = static_cast<long long>(min(rr, kn - 1)) * rstride + dc * 8;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sK + so),
-                   "l"(kg + go), "r"(src_bytes) : "memory");
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sV + so),
-                   "l"(vg + go), "r"(src_bytes) : "memory");
+    if (tid != 0) return;
+    const int sl = c % kPrivStages;
+    uint8_t* sK = smem + sl * L::kStage;
+    mbar_arrive_expect_tx(&full[sl], L::kStage);
+    const int row = k_lo + c * CH;
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_4d(sK + h * L::kHalf, &mKs, &full[sl], h * 64, g, row, b);
+      tma_load_4d(sK + L::kTile + h * L::kHalf, &mVs, &full[sl], h * 64, g, row, b);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   };
   for (int c = 0; c < kPrivStages && c < nc; ++c) stage(c);
   if (tid < HALF) scs[tid] = rope_cs_turns_fast(f.turns[tid], pos);
@@ -160,24 +170,14 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
   uint32_t bq[D / 16][2];
   {
     float qv[D / 16][4];
-    if (g8 < G) {
-      const __nv_bfloat16* qrow = a.q + (static_cast<long long>(b) * a.Hq + g * G + g8) * D;
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k)
+    for (int k = 0; k < D / 16; ++k)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const __nv_bfloat162 v =
-              *reinterpret_cast<const __nv_bfloat162*>(qrow + 16 * k + 8 * hf + 2 * tig);
-          const float2 fv = __bfloat1622float2(v);
-          qv[k][2 * hf] = fv.x;
-          qv[k][2 * hf + 1] = fv.y;
-        }
-    } else {
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qv[k][e] = 0.f;
-    }
+      for (int hf = 0; hf < 2; ++hf) {
+        const float2 fv = bf16x2_to_float2(qraw[k][hf]);  // zero for rows g8 >= G
+        qv[k][2 * hf] = fv.x;
+        qv[k][2 * hf + 1] = fv.y;
+      }
     // rotate-half: element j < D/2 pairs with j + D/2, i.e. K step k with
     // step k + D/32 and the same offsets
 #pragma unroll
@@ -208,22 +208,17 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
     for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
 
   for (int c = 0; c < nc; ++c) {
-    // chunk c has landed once at most (chunks staged after it) groups are
-    // still pending
-    const int younger = min(kPrivStages - 1, nc - 1 - c);
-    if (younger >= 3)
-      asm volatile("cp.async.wait_group 3;" ::: "memory");
-    else if (younger == 2)
-      asm volatile("cp.async.wait_group 2;" ::: "memory");
-    else if (younger == 1)
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
+    // chunk c has landed when its slot's phase completes
+    const bool ok = mbar_wait(&full[c % kPrivStages], (c / kPrivStages) & 1, abort_s, a.status,
+                              kDevErrTimeoutTma);
+    if (__syncthreads_or(!ok)) break;
     const int k0 = c * CH;
     const int kn = min(CH, nk - k0);
     uint8_t* sKp = smem + (c % kPrivStages) * L::kStage;
     const uint32_t sK = smem_u32(sKp), sV = sK + L::kTile;
+    // staged V rows past the unit's end, up to the next 16-row group: zero
+    for (int t = tid; t < (((kn + 15) & ~15) - kn) * (D / 8); t += 128)
+      sts_u4(tile_chunk(sV, kn + t / (D / 8), t % (D / 8)), make_uint4(0u, 0u, 0u, 0u));
     // ---- the new token (row len) in this chunk: rotated key and value into
     // the cache and into the shared copy
     const int rr = Lb - (k_lo + k0);
@@ -256,12 +251,18 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
       // lane -> row address: matrices (rows 0-7,k lo), (rows 8-15,k lo),
       // (rows 0-7,k hi), (rows 8-15,k hi)
       const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      // two independent accumulation chains over the d steps
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        uint32_t af[4];
+      for (int k = 0; k < D / 16; k += 2) {
+        uint32_t af[4], ag[4];
         ldsm_x4(tile_chunk(sK, row, 2 * k + (lane >> 4)), af);
+        ldsm_x4(tile_chunk(sK, row, 2 * k + 2 + (lane >> 4)), ag);
         mma_bf16_16816(sacc, af, bq[k][0], bq[k][1]);
+        mma_bf16_16816(s2, ag, bq[k + 1][0], bq[k + 1][1]);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[e] += s2[e];
     }
     // thread holds keys warp*16 + g8 (+8) and queries 2tig, 2tig+1
     float red[2];
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(DecodeLaunch a, con
         mma_bf16_16816(oacc[i], af, b0, b1);
       }
     }
+    fence_proxy_async_smem();  // generic writes to the slot before its next copy
     __syncthreads();  // the ring slot, P and the reduction slots are free again
     if (c + kPrivStages < nc) stage(c + kPrivStages);
   }
@@ -379,6 +381,19 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
   using L = PrivSmem<D>;
   cudaError_t e = set_smem_once<decode_private_kernel<D, G>>(L::kAlloc);
   if (e != cudaSuccess) return e;
+  // private caches [B, rows, Hkv, d] as (d, Hkv, rows, B), a (64, 1, CH, 1) box
+  CUtensorMap mKs, mVs;
+  const uint64_t e2 = 2;
+  const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hkv),
+                            static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.B)};
+  const uint64_t str[3] = {D * e2, static_cast<uint64_t>(a.Hkv) * D * e2,
+                           static_cast<uint64_t>(a.rows) * a.Hkv * D * e2};
+  const uint32_t box[4] = {64, 1, static_cast<uint32_t>(kPrivCH), 1};
+  if (!make_bf16_map4(&mKs, a.k_cache, dims, str, box) ||
+      !make_bf16_map4(&mVs, a.v_cache, dims, str, box))
+    return cudaErrorInvalidValue;
+  DecodeLaunch pa = a;
+  pa.status = device_status_ptr();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hkv, a.B, a.max_units);
   cfg.blockDim = dim3(128, 1, 1);
@@ -390,7 +405,7 @@ cudaError_t launch_private_dg(const DecodeLaunch& a, const RopeFreqs& f, bool de
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, a, f, scale_log2);
+  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, G>, mKs, mVs, pa, f, scale_log2);
 }
 
 // --------------------------------------------------------------- merge ----

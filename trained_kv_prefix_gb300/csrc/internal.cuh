@@ -214,6 +214,7 @@ struct DecodeLaunch {
   float* priv_part;         // [B, Hkv, units, G, d] normalised private partials
   float* priv_lse;          // [B, Hkv, units, G] their log2-domain lse
   int max_units;            // ceil(rows / kDecodeUnit)
+  uint32_t* status;         // device status word (set by the launcher)
 };
 // The whole decode step on one stream, three kernels chained by
 // programmatic dependent launch: the cartridge split pass (fwd kernel in
