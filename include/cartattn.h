@@ -131,6 +131,28 @@ CART_API int cart_attn_bwd(const cart_geom* g, cart_dtype in_dtype, cart_dtype c
                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * cart_attn_bwd_parts -- cart_attn_bwd for a cartridge composed of several
+ * independently trained parts concatenated along the rows, each with its
+ * own frozen sink row.  (Cartridges guide, composition: parts are simply
+ * concatenated, and every part keeps its sink.)
+ *   frozen_rows [n_frozen] host int32: cartridge rows whose gradient is set
+ *        to exactly 0.0 in both accumulate modes, in addition to the rows
+ *        < frozen_prefix (e.g. each part's first row); any order, repeats
+ *        allowed; 0 <= row < p; 0 <= n_frozen <= CART_MAX_FROZEN_ROWS.
+ *        The list is copied into the launch: the caller may reuse it after
+ *        the call returns.  frozen_rows may be NULL when n_frozen == 0.
+ *   Everything else is as in cart_attn_bwd, which equals this call with
+ *   n_frozen == 0.  Returns CART_ERR_GEOMETRY for a bad list.            */
+#define CART_MAX_FROZEN_ROWS 64
+CART_API int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in_dtype, cart_dtype cart_dtype,
+                                 const void* q, const void* k, const void* v, const void* kc,
+                                 const void* vc, const void* o, const float* lse,
+                                 const void* dout, void* dq, void* dk, void* dv, float* dkc,
+                                 float* dvc, const int* frozen_rows, int n_frozen,
+                                 int accumulate, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* ------------------------------------------------------------------------
  * cart_attn_decode -- one q_seq = 1 decode step for B conversations behind
  * ONE shared cartridge.  (Cartridges guide, "Semantics", serving bullet: a
  * normal decode continues at position p with the training-time layout.)

@@ -128,9 +128,12 @@ def fwd(q, k, v, kc, vc, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
 
 
 def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
-        kv_heads=None, rows=None):
+        kv_heads=None, rows=None, frozen_rows=()):
     """Gradients of ``sum(dout * o)``: returns ``dq, dk, dv, dkc, dvc`` (fp64),
     dkc/dvc summed over the batch with rows ``< frozen_prefix`` exactly 0.
+    ``frozen_rows`` lists further frozen cartridge rows (a composed
+    cartridge: parts concatenated along the rows, each keeping its own sink
+    row); a frozen row is a constant of the loss, so its gradient is 0.
     ``kv_heads=(lo, hi)`` restricts the work to those kv heads and the query
     heads reading them (other entries are NaN).  ``rows=(lo, hi)`` counts only
     those query rows of the loss: dq outside them is NaN and dk/dv/dkc/dvc
@@ -159,6 +162,11 @@ def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0
                                _ptr(dkc), _ptr(dvc), lo, hi, i_lo, i_hi)
     if rc != 0:
         raise ValueError(f"cart_oracle_bwd failed ({rc})")
+    for j in frozen_rows:
+        if not 0 <= j < p:
+            raise ValueError("frozen row outside the cartridge")
+        dkc[j] = 0.0
+        dvc[j] = 0.0
     return dq, dk, dv, dkc[:p], dvc[:p]
 
 

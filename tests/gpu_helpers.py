@@ -41,7 +41,7 @@ def to_gpu(d: dict) -> dict:
 
 
 def run_train_gpu(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=None, accumulate=False,
-                  dkc0=None, dvc0=None):
+                  dkc0=None, dvc0=None, frozen_rows=None):
     fp = s.frozen_prefix if frozen_prefix is None else frozen_prefix
     g = to_gpu(inp)
     o, lse = cartattn.cart_attn_fwd(g["q"], g["k"], g["v"], g["kc"], g["vc"], frozen_prefix=fp,
@@ -52,7 +52,7 @@ def run_train_gpu(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=Non
         dvc = dvc0.clone().cuda() if dvc0 is not None else None
         dq, dk, dv, dkc, dvc = cartattn.cart_attn_bwd(
             g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse, g["do"], frozen_prefix=fp,
-            theta=s.theta, accumulate=accumulate, dkc=dkc, dvc=dvc)
+            theta=s.theta, accumulate=accumulate, dkc=dkc, dvc=dvc, frozen_rows=frozen_rows)
         out.update(dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc)
     torch.cuda.synchronize()
     assert cartattn.device_status(clear=True) == 0, "a kernel reported a timeout"
@@ -60,7 +60,7 @@ def run_train_gpu(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=Non
 
 
 def oracle_train(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=None, heads=None,
-                 rows=None, kv_heads=None, bwd_rows=None):
+                 rows=None, kv_heads=None, bwd_rows=None, frozen_rows=()):
     fp = s.frozen_prefix if frozen_prefix is None else frozen_prefix
     a = {k: synth.f64(v) for k, v in inp.items()}
     o, lse = oracle.fwd(a["q"], a["k"], a["v"], a["kc"], a["vc"], frozen_prefix=fp,
@@ -69,7 +69,7 @@ def oracle_train(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=None
     if bwd:
         dq, dk, dv, dkc, dvc = oracle.bwd(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["do"],
                                           frozen_prefix=fp, theta=s.theta, kv_heads=kv_heads,
-                                          rows=bwd_rows)
+                                          rows=bwd_rows, frozen_rows=frozen_rows)
         ref.update(dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc)
     return ref
 

@@ -89,6 +89,14 @@ def test_calls_validate_before_touching_the_device(lib):
     # cache write: stride smaller than a row
     rc = lib.cart_write_to_cache(al, al, 4, 2, 64, al, al, 64, 0, 0, null)
     assert rc == -1
+    # composed-cartridge backward: a frozen row outside the cartridge, too many
+    # rows, or a missing list
+    rows = (ctypes.c_int * 65)(*([1] * 65))
+    bad = (ctypes.c_int * 1)(4)  # p = 4: rows are 0..3
+    for lst, cnt in ((bad, 1), (rows, 65), (None, 2)):
+        rc = lib.cart_attn_bwd_parts(ctypes.byref(g), 0, 1, al, al, al, al, al, al, al, al, al,
+                                     al, al, al, al, lst, cnt, 0, al, 1 << 30, null)
+        assert rc == -1
     # decode: unsupported group size
     rc = lib.cart_attn_decode(2, 6, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al, al, 8, al, al,
                               al, 1 << 20, null)

@@ -66,6 +66,34 @@ def test_bwd_accumulate_mode():
     gh.check_grads(got, ref, s.frozen_prefix, names=("dkc", "dvc"))
 
 
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_bwd_composed_cartridge_parts(accumulate):
+    """Three parts concatenated along the rows (rows 0, 130 and 300 are their
+    sinks; 130 and 300 sit inside tiles, 300 in the ragged last tile): the
+    listed sinks get exactly 0.0 in both modes, every other row matches the
+    oracle."""
+    s = _shape("parts", 2, 140, 8, 2, 128, 333, seed=112)
+    sinks = (130, 300)
+    inp = synth.train_inputs(s)
+    kw = {}
+    if accumulate:
+        rng = np.random.default_rng(6)
+        kw = dict(accumulate=True,
+                  dkc0=torch.from_numpy(rng.standard_normal((s.p, s.Hkv, s.d))).float(),
+                  dvc0=torch.from_numpy(rng.standard_normal((s.p, s.Hkv, s.d))).float())
+    got = gh.run_train_gpu(s, inp, frozen_rows=sinks, **kw)
+    ref = gh.oracle_train(s, inp, frozen_rows=sinks)
+    if accumulate:
+        ref["dkc"] = ref["dkc"] + kw["dkc0"].double().numpy()
+        ref["dvc"] = ref["dvc"] + kw["dvc0"].double().numpy()
+    frozen = [0, *sinks]
+    for nme in ("dkc", "dvc"):
+        assert (got[nme][frozen] == 0.0).all(), f"{nme}: a part's sink is not exactly zero"
+        ref[nme][frozen] = 0.0
+    gh.check_fwd(got, ref)
+    gh.check_grads(got, ref, 1)
+
+
 def test_backward_is_deterministic():
     s = _shape("det", 2, 200, 8, 2, 128, 300, seed=111)
     inp = synth.train_inputs(s)

@@ -186,6 +186,32 @@ def test_bwd_matches_autograd(shape, frozen):
     assert (got[3][:frozen] == 0).all() and (got[4][:frozen] == 0).all()
 
 
+def test_bwd_composed_parts_freeze_each_sink():
+    """A composed cartridge (two parts concatenated along the rows, each with
+    its own sink row) freezes both sinks: their gradients are exactly 0 and
+    every other row's gradient is that of the all-trainable problem
+    (autograd formulation), since freezing a leaf does not change the others'
+    gradients."""
+    shape = (2, 24, 4, 2, 64, 20)
+    P = _problem(77, *shape)
+    part_b = 9  # second part occupies rows 9..19; row 9 is its sink
+    got = oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"], frozen_prefix=1,
+                     theta=THETA, frozen_rows=(part_b,))
+    want = tf.cartridge_grads(*(_t(P[x]) for x in ("q", "k", "v", "kc", "vc", "do")),
+                              frozen_prefix=0, theta=THETA)
+    for name, a, b in zip(("dq", "dk", "dv", "dkc", "dvc"), got, want):
+        b = b.numpy().copy()
+        if name in ("dkc", "dvc"):
+            assert np.abs(b[part_b]).max() > 0  # the sink would otherwise get a gradient
+            b[0] = 0.0
+            b[part_b] = 0.0
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12, err_msg=name)
+    assert (got[3][[0, part_b]] == 0).all() and (got[4][[0, part_b]] == 0).all()
+    with pytest.raises(ValueError):
+        oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"], theta=THETA,
+                   frozen_rows=(20,))
+
+
 def test_bwd_finite_differences():
     """Central differences of the oracle's own forward (tiny geometry)."""
     B, n, Hq, Hkv, d, p = 1, 6, 4, 2, 8, 5

@@ -67,6 +67,9 @@ def lib():
             L.cart_attn_bwd_workspace_size.restype = sz
             L.cart_attn_bwd.argtypes = [G, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                         i, vp, sz, vp]
+            L.cart_attn_bwd_parts.argtypes = [G, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, vp, ctypes.POINTER(ctypes.c_int), i, i, vp,
+                                              sz, vp]
             L.cart_attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
             L.cart_attn_decode_workspace_size.restype = sz
             L.cart_attn_decode.argtypes = [i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp, vp, i, vp,
@@ -77,7 +80,7 @@ def lib():
             L.cart_trace_enable.argtypes = [i]
             L.cart_trace_count.argtypes = []
             L.cart_trace_get.argtypes = [i, ctypes.c_char_p, i, ctypes.POINTER(ctypes.c_float)]
-            for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd",
+            for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd", "cart_attn_bwd_parts",
                          "cart_attn_decode", "cart_device_status", "cart_trace_enable",
                          "cart_trace_count", "cart_trace_get"):
                 getattr(L, name).restype = ctypes.c_int
@@ -86,7 +89,8 @@ def lib():
 
 
 EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd",
-           "cart_attn_bwd_workspace_size", "cart_attn_bwd", "cart_attn_decode_workspace_size",
+           "cart_attn_bwd_workspace_size", "cart_attn_bwd", "cart_attn_bwd_parts",
+           "cart_attn_decode_workspace_size",
            "cart_attn_decode", "cart_status_string", "cart_device_status", "cart_trace_enable",
            "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc")
 
@@ -174,9 +178,10 @@ def cart_attn_fwd(q, k, v, kc, vc, *, frozen_prefix=1, scale=None, theta=1.0e6, 
 
 def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None, theta=1.0e6,
                   accumulate=False, dq=None, dk=None, dv=None, dkc=None, dvc=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, frozen_rows=None):
     """Backward.  Returns ``(dq, dk, dv, dkc, dvc)``; dkc/dvc are f32
-    ``[p, Hkv, d]`` summed over the batch, rows < frozen_prefix exactly 0."""
+    ``[p, Hkv, d]`` summed over the batch, rows < frozen_prefix and the rows
+    listed in ``frozen_rows`` (a composed cartridge's part sinks) exactly 0."""
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
     p = kc.shape[0]
@@ -192,11 +197,21 @@ def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None,
         dvc = (torch.zeros if accumulate else torch.empty)((max(p, 1), Hkv, d),
                                                            dtype=torch.float32, device=q.device)
     ws = _workspace(bwd_workspace_size(g, dt, cd), q.device, workspace)
-    rc = lib().cart_attn_bwd(ctypes.byref(g), dt, cd, _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
-                             _ptr(vc), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                             _ptr(dv), _ptr(dkc), _ptr(dvc), 1 if accumulate else 0, _ptr(ws),
-                             ws.numel(), _stream(stream, q.device))
-    _check("cart_attn_bwd", rc)
+    if frozen_rows is None:
+        rc = lib().cart_attn_bwd(ctypes.byref(g), dt, cd, _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
+                                 _ptr(vc), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(dkc), _ptr(dvc), 1 if accumulate else 0, _ptr(ws),
+                                 ws.numel(), _stream(stream, q.device))
+        _check("cart_attn_bwd", rc)
+    else:
+        rows = list(frozen_rows)
+        arr = (ctypes.c_int * max(len(rows), 1))(*rows)
+        rc = lib().cart_attn_bwd_parts(ctypes.byref(g), dt, cd, _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse), _ptr(dout),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkc), _ptr(dvc), arr,
+                                       len(rows), 1 if accumulate else 0, _ptr(ws), ws.numel(),
+                                       _stream(stream, q.device))
+        _check("cart_attn_bwd_parts", rc)
     return dq, dk, dv, dkc[:p], dvc[:p]
 
 

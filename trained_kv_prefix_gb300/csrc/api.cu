@@ -399,8 +399,21 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
                   const void* v, const void* kc, const void* vc, const void* o, const float* lse,
                   const void* dout, void* dq, void* dk, void* dv, float* dkc, float* dvc,
                   int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  return cart_attn_bwd_parts(g, in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
+                             nullptr, 0, accumulate, workspace, workspace_bytes, stream);
+}
+
+int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
+                        const void* k, const void* v, const void* kc, const void* vc,
+                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                        void* dv, float* dkc, float* dvc, const int* frozen_rows, int n_frozen,
+                        int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = train_common_checks(g, in, cd, q, k, v, kc, vc);
   if (rc) return rc;
+  if (n_frozen < 0 || n_frozen > CART_MAX_FROZEN_ROWS || (n_frozen > 0 && !frozen_rows))
+    return CART_ERR_GEOMETRY;
+  for (int i = 0; i < n_frozen; ++i)
+    if (frozen_rows[i] < 0 || frozen_rows[i] >= g->p) return CART_ERR_GEOMETRY;
   if (!o || !lse || !dout || !dq || !dk || !dv || !aligned16(o) || !aligned16(lse) ||
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return CART_ERR_POINTER;
@@ -453,6 +466,8 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.d = g->d;
   l.p = g->p;
   l.frozen_prefix = g->frozen_prefix;
+  l.n_frozen = n_frozen;
+  for (int i = 0; i < n_frozen; ++i) l.frozen_rows[i] = frozen_rows[i];
   l.scale = g->scale;
   l.nlse2 = nlse2;
   l.nDvec = nDvec;

@@ -17,7 +17,7 @@
 //               the heads of the group and the query tiles at or after it.
 //               Per step: S^T = K Q^T, dP^T = V dO^T (TMEM, double buffered),
 //               P^T, dS^T (bf16, shared memory), dV += P^T dO, dK += dS^T Q.
-//               Epilogue: cartridge rows (f32, rows < frozen_prefix = 0) or
+//               Epilogue: cartridge rows (f32, frozen rows = 0) or
 //               real rows (dK rotated back by R(p+j)^T).
 //  dq_kernel    one CTA per 128-row query tile: S = Q K^T, dP = dO V^T,
 //               dS = P (dP - D) -> TMEM, dQ += dS K over 128-key steps;
@@ -54,7 +54,17 @@ struct BwdParams {
   int tma_dq;  // bf16 dQ stored by TMA through mdQ
   // RoPE angle of pair c at position x, in turns: x * (turns[c].x + turns[c].y)
   float2 turns[kMaxHeadDim / 2];
+  // cartridge rows frozen besides those < frozen_prefix (composed parts' sinks)
+  int n_frozen;
+  int frozen_rows[CART_MAX_FROZEN_ROWS];
 };
+
+// Cartridge row j gets no gradient: below frozen_prefix, or listed.
+__device__ __forceinline__ bool row_frozen(const BwdParams& a, int j) {
+  bool f = j < a.frozen_prefix;
+  for (int i = 0; i < a.n_frozen; ++i) f |= a.frozen_rows[i] == j;
+  return f;
+}
 
 __device__ __forceinline__ void store_row_out(void* base, long long off, const float* x, int n,
                                               bool f32) {
@@ -508,7 +518,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (key_ok) {
           if (cart)
             write_cart_row(a.dvc + (static_cast<long long>(j) * a.Hkv + g) * D + wg * HW, x, HW,
-                           j < a.frozen_prefix, a.accumulate);
+                           row_frozen(a, j), a.accumulate);
           else
             store_row_out(a.dv, ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D + wg * HW,
                           x, HW, a.out_f32 != 0);
@@ -533,7 +543,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (key_ok) {
           if (cart) {
             float* dst = a.dkc + (static_cast<long long>(j) * a.Hkv + g) * D;
-            const bool frozen = j < a.frozen_prefix;
+            const bool frozen = row_frozen(a, j);
             write_cart_row(dst + w2 * QP, lo, QP, frozen, a.accumulate);
             write_cart_row(dst + D / 2 + w2 * QP, hi, QP, frozen, a.accumulate);
           } else {
@@ -953,6 +963,8 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.G = l.Hq / l.Hkv;
   p.p = l.p;
   p.frozen_prefix = l.frozen_prefix;
+  p.n_frozen = l.n_frozen;
+  for (int i = 0; i < l.n_frozen; ++i) p.frozen_rows[i] = l.frozen_rows[i];
   p.n_ct = (l.p + kTile - 1) / kTile;
   p.n_rt = (l.n + kTile - 1) / kTile;
   p.n_qtiles = p.n_rt;

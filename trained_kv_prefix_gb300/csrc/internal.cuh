@@ -177,6 +177,8 @@ struct BwdLaunch {
   const CUtensorMap* mV;
   const CUtensorMap* mdQ;   // bf16 output: 4D (d, Hq, n, B) over dq, 128-row box; else null
   int B, n, Hq, Hkv, d, p, frozen_prefix;
+  int n_frozen;                            // cartridge rows also frozen (parts' sinks)
+  int frozen_rows[CART_MAX_FROZEN_ROWS];
   float scale;
   const float* nlse2;       // [B, Hq, npad] -lse * log2(e), -inf past n
   const float* nDvec;       // [B, Hq, npad] -D, 0 past n
