@@ -177,6 +177,33 @@ CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale,
                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * cart_attn_decode_span -- span verify: `span` consecutive new tokens per
+ * conversation in one step (q_seq = span), behind the shared cartridge.
+ * (Cartridges guide, "Batched self-study (measured)", the --spec-b bullet:
+ * each stream's span of carried and drafted tokens attends to its own cache
+ * behind the prefix in one pass; the mask is the end-aligned causal one.)
+ *   q      [B, span, Hq, d] bf16, the span's queries, NOT rotated
+ *   k_new, v_new [B, span, Hkv, d] bf16, the span's keys (NOT rotated) and
+ *          values
+ *   o      [B, span, Hq, d] bf16 (output)
+ *   priv_len [B]: len[b], clamped into 0 <= len[b] <= cache_rows - span
+ *   Token t of conversation b sits at position p + len[b] + t: the span's
+ *   rotated keys and values are written to private rows len[b] .. len[b] +
+ *   span - 1, and query t attends to the p cartridge rows and private rows
+ *   0 .. len[b] + t.  Requires 1 <= span <= cache_rows and
+ *   (Hq / Hkv) * span <= 32.  Everything else is as in cart_attn_decode,
+ *   which equals this call with span == 1.
+ * Workspace: cart_attn_decode_span_workspace_size().                      */
+CART_API size_t cart_attn_decode_span_workspace_size(int B, int span, int Hq, int Hkv, int d,
+                                                     int p, int cache_rows);
+CART_API int cart_attn_decode_span(int B, int span, int Hq, int Hkv, int d, int p, float scale,
+                                   double rope_theta, const void* q, const void* k_new,
+                                   const void* v_new, const void* kc, const void* vc,
+                                   void* k_cache, void* v_cache, int cache_rows,
+                                   const int* priv_len, void* o, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * cart_attn_decode_noalloc -- the decode step of cart_attn_decode for
  * callers that cannot allocate device memory: a serving loop running under a
  * fixed device-memory budget planned at start-up (a cudaMalloc on the decode

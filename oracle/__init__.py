@@ -197,6 +197,26 @@ def decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta
     return o, kcache, vcache
 
 
+def decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6):
+    """Span verify (Cartridges guide, "Batched self-study (measured)", the
+    --spec-b bullet): ``span`` new tokens per conversation in one step
+    (q ``[B, span, Hq, d]``, k_new / v_new ``[B, span, Hkv, d]``).  Token t
+    sits at position p + lens[b] + t, its rotated key / value go to private
+    row lens[b] + t, and query t sees the cartridge and private rows
+    0 .. lens[b] + t -- the end-aligned causal mask over the span, i.e. the
+    span's single-token steps taken in order.  Returns
+    ``(o [B, span, Hq, d], k_cache', v_cache')``."""
+    q, k_new, v_new = _f64(q), _f64(k_new), _f64(v_new)
+    span = q.shape[1]
+    kcache, vcache = _f64(k_cache).copy(), _f64(v_cache).copy()
+    lens = np.asarray(lens, dtype=np.int64)
+    o = np.empty(q.shape)
+    for t in range(span):
+        o[:, t], kcache, vcache = decode(q[:, t], k_new[:, t], v_new[:, t], kc, vc, kcache,
+                                         vcache, lens + t, scale=scale, theta=theta)
+    return o, kcache, vcache
+
+
 def rope(x, pos0, *, theta=1.0e6, inverse=False):
     """Rotate ``x [rows, H, d]`` row r at position ``pos0 + r``."""
     x = _f64(x)

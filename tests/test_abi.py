@@ -66,6 +66,13 @@ def test_workspace_sizes_are_positive_and_grow(lib):
     assert cartattn.bwd_workspace_size(g1, 0, 1) > a
     assert cartattn.decode_workspace_size(64, 32, 8, 128, 4096, 1025) > 0
     assert cartattn.decode_workspace_size(4, 12, 4, 128, 16, 8) == 0   # G = 3 unsupported
+    # span verify: the span's columns grow the workspace; G * span > 32 or a
+    # span longer than the cache is refused
+    one = cartattn.decode_span_workspace_size(64, 1, 32, 8, 128, 4096, 1025)
+    assert one == cartattn.decode_workspace_size(64, 32, 8, 128, 4096, 1025)
+    assert cartattn.decode_span_workspace_size(64, 8, 32, 8, 128, 4096, 1025) > one
+    assert cartattn.decode_span_workspace_size(64, 9, 32, 8, 128, 4096, 1025) == 0
+    assert cartattn.decode_span_workspace_size(4, 9, 8, 2, 128, 16, 8) == 0
 
 
 def test_calls_validate_before_touching_the_device(lib):
@@ -101,6 +108,11 @@ def test_calls_validate_before_touching_the_device(lib):
     rc = lib.cart_attn_decode(2, 6, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al, al, 8, al, al,
                               al, 1 << 20, null)
     assert rc == -1
+    # span decode: span 0, span past the cache, too many query columns
+    for span, rows in ((0, 8), (9, 8), (5, 64)):
+        rc = lib.cart_attn_decode_span(2, span, 16, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al,
+                                       al, rows, al, al, al, 1 << 30, null)
+        assert rc == -1, (span, rows)
 
 
 def test_no_gpu_here_means_a_cuda_or_device_error(lib):

@@ -182,6 +182,60 @@ def test_decode_parity_small(s):
     _check_decode(s, inp, o, kc, vc)
 
 
+SPAN_CASES = [
+    # (case, span): G*span query columns from 4 to 32 (one to four groups of
+    # 8); lengths at 0, at the last slot that fits the span, and spans that
+    # cross 64-row chunks and 256-row units
+    (_decode_case("span2", 3, 4, 2, 64, 16, 39, lens=(0, 17, 37)), 2),
+    (_decode_case("span3_units", 4, 8, 2, 128, 300, 300, lens=(0, 62, 254, 297)), 3),
+    (_decode_case("span8_g4", 3, 8, 2, 128, 200, 520, lens=(250, 0, 513)), 8),
+    (_decode_case("span4_g8_p0", 2, 8, 1, 128, 0, 300, lens=(0, 129)), 4),
+    (_decode_case("span5_g1_d64", 5, 4, 4, 64, 130, 260, lens=(0, 60, 128, 251, 256)), 5),
+    (_decode_case("span6_g4", 2, 8, 2, 128, 64, 200, lens=(190, 3)), 6),
+]
+
+
+@pytest.mark.parametrize("case", SPAN_CASES, ids=[c[0].name for c in SPAN_CASES])
+def test_decode_span_parity(case):
+    s, span = case
+    inp = synth.decode_span_inputs(s, span)
+    g = {k: v.cuda() for k, v in inp.items()}
+    o = cartattn.cart_attn_decode_span(g["q"], g["k_new"], g["v_new"], g["kc"], g["vc"],
+                                       g["k_cache"], g["v_cache"], g["lens"], theta=s.theta)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    a = {k: synth.f64(v) for k, v in inp.items() if k != "lens"}
+    lens = inp["lens"].numpy()
+    o_ref, kref, vref = oracle.decode_span(a["q"], a["k_new"], a["v_new"], a["kc"], a["vc"],
+                                           a["k_cache"], a["v_cache"], lens, theta=s.theta)
+    o = synth.f64(o)
+    assert gh.max_abs(o, o_ref) <= gh.FWD_MAXABS, gh.max_abs(o, o_ref)
+    assert gh.rel_l2(o, o_ref) <= gh.FWD_RELL2, gh.rel_l2(o, o_ref)
+    kc_new, vc_new = synth.f64(g["k_cache"]), synth.f64(g["v_cache"])
+    for b in range(s.B):
+        L = int(lens[b])
+        mask = np.ones(s.cache_rows, bool)
+        mask[L:L + span] = False
+        np.testing.assert_array_equal(kc_new[b][mask], a["k_cache"][b][mask])
+        np.testing.assert_array_equal(vc_new[b][mask], a["v_cache"][b][mask])
+        np.testing.assert_array_equal(vc_new[b, L:L + span], a["v_new"][b])
+        np.testing.assert_allclose(kc_new[b, L:L + span], kref[b, L:L + span], rtol=2 ** -8,
+                                   atol=1e-6)
+
+
+def test_decode_span_one_equals_decode():
+    """span = 1 is the single-token step, bit for bit."""
+    s = DECODE_SMALL[3]
+    inp = synth.decode_inputs(s)
+    o1, _, _ = _run_decode(s, inp)
+    g = {k: v.cuda() for k, v in inp.items()}
+    o2 = cartattn.cart_attn_decode_span(g["q"][:, None], g["k_new"][:, None], g["v_new"][:, None],
+                                        g["kc"], g["vc"], g["k_cache"], g["v_cache"], g["lens"],
+                                        theta=s.theta)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(o1, synth.f64(o2[:, 0]))
+
+
 def test_decode_serving_workload():
     """64 conversations behind one p = 4096 cartridge, 0..1024 private rows."""
     s = synth.DECODE

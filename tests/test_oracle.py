@@ -337,6 +337,41 @@ def test_decode_is_last_row_of_forward():
         np.testing.assert_array_equal(kc2[b, L + 1:], 7.0)
 
 
+def test_decode_span_is_rows_of_forward():
+    """Span verify (several new tokens per conversation in one step) equals
+    the training-time forward of the same tokens: query t is row len + t of
+    a sequence whose first len rows are the already-cached tokens."""
+    B, Hq, Hkv, d, p, span = 3, 4, 2, 16, 9, 3
+    lens = np.array([0, 4, 2], dtype=np.int32)
+    rows = 8
+    rng = np.random.default_rng(51)
+    kc = rng.standard_normal((p, Hkv, d)) * 0.5
+    vc = rng.standard_normal((p, Hkv, d)) * 0.5
+    kraw = rng.standard_normal((B, rows, Hkv, d)) * 0.5
+    vraw = rng.standard_normal((B, rows, Hkv, d)) * 0.5
+    q = rng.standard_normal((B, span, Hq, d)) * 0.5
+    k_cache = np.full((B, rows, Hkv, d), 7.0)
+    v_cache = np.full((B, rows, Hkv, d), 7.0)
+    for b in range(B):
+        L = lens[b]
+        k_cache[b, :L] = oracle.rope(kraw[b, :L], p)
+        v_cache[b, :L] = vraw[b, :L]
+    k_new = np.stack([kraw[b, lens[b]:lens[b] + span] for b in range(B)])
+    v_new = np.stack([vraw[b, lens[b]:lens[b] + span] for b in range(B)])
+    o, kc2, vc2 = oracle.decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens)
+    for b in range(B):
+        L = int(lens[b])
+        qs = np.zeros((1, L + span, Hq, d))
+        qs[0, L:] = q[b]
+        of, _ = oracle.fwd(qs, kraw[None, b, :L + span], vraw[None, b, :L + span], kc, vc,
+                           rows=(L, L + span))
+        np.testing.assert_allclose(o[b], of[0, L:L + span], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(kc2[b, L:L + span], oracle.rope(kraw[b, L:L + span], p + L),
+                                   atol=1e-14)
+        np.testing.assert_array_equal(vc2[b, L:L + span], vraw[b, L:L + span])
+        np.testing.assert_array_equal(kc2[b, L + span:], 7.0)
+
+
 def test_decode_matches_sdpa_single_query():
     B, Hq, Hkv, d, p = 2, 4, 1, 8, 6
     lens = np.array([0, 3], dtype=np.int32)

@@ -74,6 +74,10 @@ def lib():
             L.cart_attn_decode_workspace_size.restype = sz
             L.cart_attn_decode.argtypes = [i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp, vp, i, vp,
                                            vp, vp, sz, vp]
+            L.cart_attn_decode_span_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.cart_attn_decode_span_workspace_size.restype = sz
+            L.cart_attn_decode_span.argtypes = [i, i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp,
+                                                vp, i, vp, vp, vp, sz, vp]
             L.cart_status_string.argtypes = [i]
             L.cart_status_string.restype = ctypes.c_char_p
             L.cart_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
@@ -81,7 +85,8 @@ def lib():
             L.cart_trace_count.argtypes = []
             L.cart_trace_get.argtypes = [i, ctypes.c_char_p, i, ctypes.POINTER(ctypes.c_float)]
             for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd", "cart_attn_bwd_parts",
-                         "cart_attn_decode", "cart_device_status", "cart_trace_enable",
+                         "cart_attn_decode", "cart_attn_decode_span", "cart_device_status",
+                         "cart_trace_enable",
                          "cart_trace_count", "cart_trace_get"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -92,7 +97,8 @@ EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd
            "cart_attn_bwd_workspace_size", "cart_attn_bwd", "cart_attn_bwd_parts",
            "cart_attn_decode_workspace_size",
            "cart_attn_decode", "cart_status_string", "cart_device_status", "cart_trace_enable",
-           "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc")
+           "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc",
+           "cart_attn_decode_span_workspace_size", "cart_attn_decode_span")
 
 
 def _check(fn: str, rc: int):
@@ -241,6 +247,35 @@ def cart_attn_decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=N
                                 _ptr(v_cache), rows, _ptr(lens), _ptr(o), _ptr(ws), ws.numel(),
                                 _stream(stream, q.device))
     _check("cart_attn_decode", rc)
+    return o
+
+
+def decode_span_workspace_size(B, span, Hq, Hkv, d, p, rows) -> int:
+    return int(lib().cart_attn_decode_span_workspace_size(B, span, Hq, Hkv, d, p, rows))
+
+
+def cart_attn_decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None,
+                          theta=1.0e6, o=None, workspace=None, stream=None):
+    """Span verify: ``span`` new tokens per conversation in one step.  q
+    ``[B, span, Hq, d]``, k_new/v_new ``[B, span, Hkv, d]`` (bf16, not
+    rotated); the caches receive the span's rows lens[b] .. lens[b]+span-1.
+    Returns o ``[B, span, Hq, d]`` bf16."""
+    B, span, Hq, d = q.shape
+    Hkv = k_new.shape[2]
+    p = kc.shape[0]
+    rows = k_cache.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if lens.dtype != torch.int32:
+        raise TypeError("lens must be int32")
+    if o is None:
+        o = torch.empty_like(q)
+    ws = _workspace(decode_span_workspace_size(B, span, Hq, Hkv, d, p, rows), q.device, workspace)
+    rc = lib().cart_attn_decode_span(B, span, Hq, Hkv, d, p, float(scale), float(theta), _ptr(q),
+                                     _ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc),
+                                     _ptr(k_cache), _ptr(v_cache), rows, _ptr(lens), _ptr(o),
+                                     _ptr(ws), ws.numel(), _stream(stream, q.device))
+    _check("cart_attn_decode_span", rc)
     return o
 
 

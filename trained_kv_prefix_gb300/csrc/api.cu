@@ -504,10 +504,10 @@ struct DecodeWs {
   int splits = 0, tiles_per_split = 0, max_units = 0;
 };
 
-DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
+DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows, int span = 1) {
   DecodeWs w;
   const int n_ct = (p + 127) / 128;
-  const int R = B * (Hq / Hkv);
+  const int R = B * span * (Hq / Hkv);
   const int qpairs = ((R + 127) / 128 + 1) / 2;  // the cartridge pass takes two row tiles per CTA
   if (n_ct > 0) {
     // about kDecodeCartCtas CTAs for the cartridge part
@@ -526,21 +526,24 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows) {
   w.max_units = (rows + kDecodeUnit - 1) / kDecodeUnit;
   w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
   w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
-  w.priv_part = take(static_cast<size_t>(B) * Hq * w.max_units * d * 4);
-  w.priv_lse = take(static_cast<size_t>(B) * Hq * w.max_units * 4);
+  w.priv_part = take(static_cast<size_t>(B) * span * Hq * w.max_units * d * 4);
+  w.priv_lse = take(static_cast<size_t>(B) * span * Hq * w.max_units * 4);
   w.total = off;
   return w;
 }
 
-int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta, int rows) {
+int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta, int rows,
+                 int span = 1) {
   if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || p < 0 || rows < 1)
     return CART_ERR_GEOMETRY;
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return CART_ERR_GEOMETRY;
+  if (span < 1 || span > rows || G * span > kDecodeMaxColumns) return CART_ERR_GEOMETRY;
+  if (static_cast<long long>(B) * span > 65535) return CART_ERR_GEOMETRY;
   if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
   if (!std::isfinite(scale) || !(scale > 0.f) || !(theta > 0.0) || !std::isfinite(theta))
     return CART_ERR_GEOMETRY;
-  if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
+  if ((static_cast<long long>(B) * span * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
   if (rows > 32768) return CART_ERR_GEOMETRY;
   // positions p + len must be exact in f32 (the query rotation of the
   // cartridge pass reduces its angles in f32)
@@ -550,8 +553,13 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
 }  // namespace
 
 size_t cart_attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int p, int cache_rows) {
-  if (check_decode(B, Hq, Hkv, d, p, 1.f, 1.0, cache_rows)) return 0;
-  return decode_ws(B, Hq, Hkv, d, p, cache_rows).total;
+  return cart_attn_decode_span_workspace_size(B, 1, Hq, Hkv, d, p, cache_rows);
+}
+
+size_t cart_attn_decode_span_workspace_size(int B, int span, int Hq, int Hkv, int d, int p,
+                                            int cache_rows) {
+  if (check_decode(B, Hq, Hkv, d, p, 1.f, 1.0, cache_rows, span)) return 0;
+  return decode_ws(B, Hq, Hkv, d, p, cache_rows, span).total;
 }
 
 int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double rope_theta,
@@ -559,19 +567,30 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
                      const void* vc, void* k_cache, void* v_cache, int cache_rows,
                      const int* priv_len, void* o, void* workspace, size_t workspace_bytes,
                      void* stream) {
-  int rc = check_decode(B, Hq, Hkv, d, p, scale, rope_theta, cache_rows);
+  return cart_attn_decode_span(B, 1, Hq, Hkv, d, p, scale, rope_theta, q, k_new, v_new, kc, vc,
+                               k_cache, v_cache, cache_rows, priv_len, o, workspace,
+                               workspace_bytes, stream);
+}
+
+int cart_attn_decode_span(int B, int span, int Hq, int Hkv, int d, int p, float scale,
+                          double rope_theta, const void* q, const void* k_new, const void* v_new,
+                          const void* kc, const void* vc, void* k_cache, void* v_cache,
+                          int cache_rows, const int* priv_len, void* o, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  int rc = check_decode(B, Hq, Hkv, d, p, scale, rope_theta, cache_rows, span);
   if (rc) return rc;
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* ptr : ptrs)
     if (!ptr || !aligned16(ptr)) return CART_ERR_POINTER;
   if (!priv_len || (reinterpret_cast<uintptr_t>(priv_len) & 3u)) return CART_ERR_POINTER;
   if (p > 0 && (!kc || !vc || !aligned16(kc) || !aligned16(vc))) return CART_ERR_POINTER;
-  const DecodeWs w = decode_ws(B, Hq, Hkv, d, p, cache_rows);
+  const DecodeWs w = decode_ws(B, Hq, Hkv, d, p, cache_rows, span);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeLaunch a{};
+  a.span = span;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;

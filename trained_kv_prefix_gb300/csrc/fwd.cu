@@ -54,6 +54,7 @@ struct FwdParams {
   // decode mode: raw query rows r = b*G + hh, rotated here at p + len[b]
   const int* dec_len;
   int dec_B, dec_G, dec_rows;
+  int dec_s;  // span: rows of one conversation's s queries are consecutive
   float2 turns[kMaxHeadDim / 2];
 };
 
@@ -460,14 +461,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
       } else if (a.decode) {
-        // row i = b*G + hh of this kv head: its query at position p + len[b]
+        // row i = (b*s + t)*G + hh of this kv head: query t of conversation
+        // b's span at position p + len[b] + t
         ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
-        const int bconv = i / a.dec_G;
-        if (ok && bconv < a.dec_B) {
-          int len = __ldg(a.dec_len + bconv);
-          len = len < 0 ? 0 : (len >= a.dec_rows ? a.dec_rows - 1 : len);
-          const int pos = a.p + len;
+        const int vb = i / a.dec_G;
+        if (ok && vb < a.dec_B) {
+          int len = __ldg(a.dec_len + vb / a.dec_s);
+          const int lmax = a.dec_rows - a.dec_s;
+          len = len < 0 ? 0 : (len > lmax ? lmax : len);
+          const int pos = a.p + len + vb % a.dec_s;
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
                           [&](int j0, float2* c) {
 #pragma unroll
@@ -726,6 +729,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
     p.dec_B = a.dec_B;
     p.dec_G = a.dec_G;
     p.dec_rows = a.dec_rows;
+    p.dec_s = a.dec_s;
     for (int j = 0; j < kMaxHeadDim / 2; ++j) p.turns[j] = a.freqs->turns[j];
   }
   dim3 grid;
@@ -752,7 +756,8 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
   if (a.rotate_q && (a.decode || !a.table)) return cudaErrorInvalidValue;
-  if (a.decode && (!a.dec_len || !a.freqs || a.dec_G < 1 || kTile % a.dec_G != 0))
+  if (a.decode && (!a.dec_len || !a.freqs || a.dec_G < 1 || kTile % a.dec_G != 0 ||
+                   a.dec_s < 1 || a.dec_B % a.dec_s != 0))
     return cudaErrorInvalidValue;
   if (a.d == 128) return launch_fwd_d<128>(a, st);
   if (a.d == 64) return launch_fwd_d<64>(a, st);

@@ -158,7 +158,8 @@ struct FwdLaunch {
   // with a (64, G, 1, 128/G) box, so that a 128-row tile is rows b*G + hh;
   // the kernel rotates row (b, hh) at position p + len[b] in shared memory.
   const int* dec_len;
-  int dec_B, dec_G, dec_rows;
+  int dec_B, dec_G, dec_rows;  // dec_B counts (conversation, span position) pairs
+  int dec_s = 1;               // span length
   const RopeFreqs* freqs;  // host copy, read at launch
   bool pdl;                // launch as the programmatic dependent of the
                            // previous kernel on the stream
@@ -210,13 +211,14 @@ struct DecodeLaunch {
   const int* len;
   __nv_bfloat16* o;
   int n_cart_splits;
-  const float* cart_part;   // [S, Hkv, R, d]
+  const float* cart_part;   // [S, Hkv, R, d], R = B*span*G rows (b*span + t)*G + hh
   const float* cart_lse;    // [S, Hkv, R]
   int cart_tiles_per_split; // cartridge tiles per split CTA
-  float* priv_part;         // [B, Hkv, units, G, d] normalised private partials
-  float* priv_lse;          // [B, Hkv, units, G] their log2-domain lse
+  float* priv_part;         // [B, Hkv, units, span*G, d] normalised private partials
+  float* priv_lse;          // [B, Hkv, units, span*G] their log2-domain lse
   int max_units;            // ceil(rows / kDecodeUnit)
   uint32_t* status;         // device status word (set by the launcher)
+  int span = 1;             // queries per conversation (q, k_new, v_new, o are [B, span, ...])
 };
 // The whole decode step on one stream, three kernels chained by
 // programmatic dependent launch: the cartridge split pass (fwd kernel in
@@ -226,6 +228,7 @@ struct DecodeLaunch {
 // (conversation, head)'s parts once both are done.
 constexpr int kDecodeChunk = 64;    // private rows per pipeline stage
 constexpr int kDecodeUnit = 256;    // private rows per CTA
+constexpr int kDecodeMaxColumns = 32;  // G * span: query columns of the private pass
 // The cartridge pass gets about this many CTAs (one SM each), so that the
 // private pass runs next to it on the remaining SMs.
 constexpr int kDecodeCartCtas = 48;

@@ -169,6 +169,28 @@ def decode_inputs(s: DecodeShape, seed: int | None = None) -> dict:
                 lens=torch.from_numpy(lens))
 
 
+def decode_span_inputs(s: DecodeShape, span: int, seed: int | None = None) -> dict:
+    """As decode_inputs for ``span`` new tokens per conversation: query
+    ``[B, span, Hq, d]``, new K/V ``[B, span, Hkv, d]``, lengths
+    ``L_b ~ U{0..rows - span}`` (or ``s.fixed_len``) so the span fits."""
+    rng = np.random.default_rng(s.seed if seed is None else seed)
+    if s.fixed_len:
+        lens = np.asarray(s.fixed_len, dtype=np.int32)
+        assert lens.shape == (s.B,) and (lens + span <= s.cache_rows).all()
+    else:
+        lens = rng.integers(0, s.cache_rows - span + 1, size=s.B).astype(np.int32)
+    kc = _draw(rng, (s.p, s.Hkv, s.d), s.std, "bf16")
+    vc = _draw(rng, (s.p, s.Hkv, s.d), s.std, "bf16")
+    k_cache = _draw(rng, (s.B, s.cache_rows, s.Hkv, s.d), s.std, "bf16")
+    v_cache = _draw(rng, (s.B, s.cache_rows, s.Hkv, s.d), s.std, "bf16")
+    q = _draw(rng, (s.B, span, s.Hq, s.d), s.std, "bf16")
+    k_new = _draw(rng, (s.B, span, s.Hkv, s.d), s.std, "bf16")
+    v_new = _draw(rng, (s.B, span, s.Hkv, s.d), s.std, "bf16")
+    return dict(q=q, k_new=k_new, v_new=v_new, kc=kc, vc=vc,
+                k_cache=k_cache, v_cache=v_cache,
+                lens=torch.from_numpy(lens))
+
+
 def f64(t: torch.Tensor) -> np.ndarray:
     """Exact widening of a stored tensor to an fp64 numpy array."""
     return t.detach().cpu().to(torch.float64).contiguous().numpy()
