@@ -170,6 +170,60 @@ def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0
     return dq, dk, dv, dkc[:p], dvc[:p]
 
 
+def _segments(cu_seqlens, total):
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    if cu.ndim != 1 or cu.size < 2 or cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must rise from 0 to the packed token count")
+    return [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:])]
+
+
+def fwd_packed(q, k, v, kc, vc, cu_seqlens, *, p=None, frozen_prefix=1, scale=None,
+               theta=1.0e6):
+    """Packed segments (Cartridges guide, "Deliberate divergences from the
+    reference", packing bullet; "Batched self-study (measured)", packed
+    training step): the group's sequences lie back to back along ONE token
+    axis, q ``[T, Hq, d]``, k/v ``[T, Hkv, d]``, segment s holding tokens
+    ``cu_seqlens[s] .. cu_seqlens[s+1] - 1``.  RoPE restarts per segment
+    (its token i sits at position p + i) and attention runs per segment
+    behind the one shared cartridge, so each segment is exactly a
+    single-sequence call of ``fwd``.  Returns ``(o [T, Hq, d], lse [Hq, T])``."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, Hq, d = q.shape
+    o = np.zeros((T, Hq, d))
+    lse = np.zeros((Hq, T))
+    for a, b in _segments(cu_seqlens, T):
+        if b == a:
+            continue
+        o_s, lse_s = fwd(q[None, a:b], k[None, a:b], v[None, a:b], kc, vc, p=p,
+                         frozen_prefix=frozen_prefix, scale=scale, theta=theta)
+        o[a:b] = o_s[0]
+        lse[:, a:b] = lse_s[0]
+    return o, lse
+
+
+def bwd_packed(q, k, v, kc, vc, dout, cu_seqlens, *, p=None, frozen_prefix=1, scale=None,
+               theta=1.0e6, frozen_rows=()):
+    """Gradients of ``sum(dout * o)`` for packed segments (layouts of
+    ``fwd_packed``): each segment's dq/dk/dv are those of its own
+    single-sequence problem, and the cartridge gradient is their sum over
+    the segments (one shared cartridge), frozen rows exactly 0."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    T = q.shape[0]
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    kc64 = _f64(kc)
+    dkc = np.zeros(kc64.shape)
+    dvc = np.zeros(kc64.shape)
+    for a, b in _segments(cu_seqlens, T):
+        if b == a:
+            continue
+        g = bwd(q[None, a:b], k[None, a:b], v[None, a:b], kc, vc, dout[None, a:b], p=p,
+                frozen_prefix=frozen_prefix, scale=scale, theta=theta, frozen_rows=frozen_rows)
+        dq[a:b], dk[a:b], dv[a:b] = g[0][0], g[1][0], g[2][0]
+        dkc += g[3]
+        dvc += g[4]
+    return dq, dk, dv, dkc, dvc
+
+
 def decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6):
     """One decode step behind a shared cartridge.  Returns
     ``(o [B, Hq, d], k_cache', v_cache')`` where the caches have the new

@@ -429,3 +429,59 @@ def test_write_to_cache_nan_stays_nan():
     back = torch.from_numpy(dst.view(np.int16)).view(torch.bfloat16).float().numpy()
     assert np.isnan(back[0, 0, 0]) and np.isnan(back[0, 0, 1])
     assert back[0, 0, 2] == 1.0 and back[0, 0, 3] == 2.0
+
+
+PACKED_CASES = [
+    # (cu_seqlens, Hq, Hkv, d, p): ragged segments, an empty one, a lone token
+    ((0, 5, 5, 12, 13, 20), 4, 2, 16, 6),
+    ((0, 9, 17), 6, 3, 8, 1),
+    ((0, 3, 11), 2, 2, 8, 0),
+]
+
+
+@pytest.mark.parametrize("case", PACKED_CASES)
+def test_packed_matches_block_diagonal_attention(case):
+    """Packed segments equal ONE attention over the packed tokens with a block
+    diagonal mask and RoPE restarting at p per segment (forward, lse and every
+    gradient, sink frozen)."""
+    cu, Hq, Hkv, d, p = case
+    T = cu[-1]
+    P = _problem(60 + T, 1, T, Hq, Hkv, d, max(p, 1))
+    q, k, v, do = P["q"][0], P["k"][0], P["v"][0], P["do"][0]
+    kc, vc = P["kc"][:p], P["vc"][:p]
+    fp = min(1, p)
+    o, lse = oracle.fwd_packed(q, k, v, kc, vc, cu, frozen_prefix=fp)
+    o_t, lse_t = tf.packed_attention(_t(q), _t(k), _t(v), _t(kc), _t(vc), cu)
+    np.testing.assert_allclose(o, o_t.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.numpy(), rtol=0, atol=1e-12)
+    g = oracle.bwd_packed(q, k, v, kc, vc, do, cu, frozen_prefix=fp)
+    g_t = tf.packed_grads(_t(q), _t(k), _t(v), _t(kc), _t(vc), _t(do), cu, frozen_prefix=fp)
+    for a, b in zip(g, g_t):
+        np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-11)
+    if p:
+        assert (g[3][0] == 0).all() and (g[4][0] == 0).all()
+
+
+def test_packed_equal_segments_are_a_batch():
+    """Equal-length segments are the batched call with B = segments."""
+    B, n, Hq, Hkv, d, p = 3, 6, 4, 2, 8, 5
+    P = _problem(70, B, n, Hq, Hkv, d, p)
+    cu = [i * n for i in range(B + 1)]
+    flat = {k2: P[k2].reshape(B * n, *P[k2].shape[2:]) for k2 in ("q", "k", "v", "do")}
+    o, lse = oracle.fwd_packed(flat["q"], flat["k"], flat["v"], P["kc"], P["vc"], cu)
+    o_b, lse_b = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"])
+    np.testing.assert_array_equal(o, o_b.reshape(B * n, Hq, d))
+    np.testing.assert_array_equal(lse, lse_b.transpose(1, 0, 2).reshape(Hq, B * n))
+    g = oracle.bwd_packed(flat["q"], flat["k"], flat["v"], P["kc"], P["vc"], flat["do"], cu)
+    g_b = oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"])
+    for a, b in zip(g[:3], g_b[:3]):
+        np.testing.assert_array_equal(a, b.reshape(a.shape))
+    np.testing.assert_allclose(g[3], g_b[3], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(g[4], g_b[4], rtol=0, atol=1e-13)
+
+
+def test_packed_rejects_bad_segment_tables():
+    P = _problem(71, 1, 6, 2, 1, 8, 3)
+    for cu in ((0, 7), (1, 6), (0, 4, 2, 6), (0,)):
+        with pytest.raises(ValueError):
+            oracle.fwd_packed(P["q"][0], P["k"][0], P["v"][0], P["kc"], P["vc"], cu)

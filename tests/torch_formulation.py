@@ -78,3 +78,56 @@ def cartridge_grads(q, k, v, kc, vc, dout, *, frozen_prefix=1, theta=1.0e6, scal
     dkc[frozen_prefix:] = kt.grad
     dvc[frozen_prefix:] = vt.grad
     return q.grad, k.grad, v.grad, dkc, dvc
+
+
+def packed_attention(q, k, v, kc, vc, cu_seqlens, *, theta=1.0e6, scale=None):
+    """Packed segments as ONE attention over the packed token axis: q
+    ``[T, Hq, d]``, k/v ``[T, Hkv, d]``, keys = the p cartridge rows then all
+    T tokens.  The mask is block diagonal over the segments: token i of
+    segment s sees every cartridge row and the tokens 0..i of segment s;
+    RoPE positions restart at p in every segment.  Returns (o ``[T, Hq, d]``,
+    lse ``[Hq, T]``)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    p = kc.shape[0]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    cu = [int(x) for x in cu_seqlens]
+    seg = torch.zeros(T, dtype=torch.long)
+    local = torch.zeros(T, dtype=torch.long)
+    for s, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        seg[a:b] = s
+        local[a:b] = torch.arange(b - a)
+    pos = p + local
+    qh = rope_complex(q.permute(1, 0, 2), pos, theta)                  # [Hq, T, d]
+    kh = rope_complex(k.permute(1, 0, 2), pos, theta)                  # [Hkv, T, d]
+    K = torch.cat([kc.permute(1, 0, 2), kh], dim=1).repeat_interleave(G, dim=0)
+    V = torch.cat([vc.permute(1, 0, 2), v.permute(1, 0, 2)], dim=1).repeat_interleave(G, dim=0)
+    same = seg[:, None] == seg[None, :]
+    causal = local[None, :] <= local[:, None]
+    mask = torch.cat([torch.ones(T, p, dtype=torch.bool), same & causal], dim=1)  # [T, p + T]
+    o = F.scaled_dot_product_attention(qh, K, V, attn_mask=mask, scale=scale)
+    logits = torch.matmul(qh, K.transpose(-1, -2)) * scale
+    lse = torch.logsumexp(logits.masked_fill(~mask, float("-inf")), dim=-1)
+    return o.permute(1, 0, 2), lse
+
+
+def packed_grads(q, k, v, kc, vc, dout, cu_seqlens, *, frozen_prefix=1, theta=1.0e6,
+                 scale=None):
+    """Autograd gradients of sum(dout * o) through ``packed_attention``, the
+    sink rows held constant (gradient reported as exactly 0)."""
+    q = q.clone().requires_grad_(True)
+    k = k.clone().requires_grad_(True)
+    v = v.clone().requires_grad_(True)
+    kt = kc[frozen_prefix:].clone().requires_grad_(True)
+    vt = vc[frozen_prefix:].clone().requires_grad_(True)
+    o, _ = packed_attention(q, k, v, torch.cat([kc[:frozen_prefix], kt]),
+                            torch.cat([vc[:frozen_prefix], vt]), cu_seqlens, theta=theta,
+                            scale=scale)
+    (o * dout).sum().backward()
+    dkc = torch.zeros_like(kc)
+    dvc = torch.zeros_like(vc)
+    dkc[frozen_prefix:] = kt.grad
+    dvc[frozen_prefix:] = vt.grad
+    return q.grad, k.grad, v.grad, dkc, dvc
