@@ -153,6 +153,46 @@ CART_API int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in_dtype, cart_d
                                  void* stream);
 
 /* ------------------------------------------------------------------------
+ * cart_attn_fwd_packed / cart_attn_bwd_packed -- training on packed
+ * segments: the group's sequences lie back to back along ONE token axis
+ * instead of in a [B, n] batch.  RoPE restarts in every segment (its token i
+ * sits at position p + i) and attention runs per segment behind the one
+ * shared cartridge, so each segment is exactly one sequence of
+ * cart_attn_fwd / cart_attn_bwd.  (Cartridges guide, "Deliberate
+ * divergences from the reference", packing bullet; "Batched self-study
+ * (measured)", packed training step.)
+ *   g->B   number of segments S;  g->n  the longest segment (an upper bound:
+ *          it sizes the launch grids and the RoPE table)
+ *   total  packed tokens T, 1 <= T <= S * n
+ *   cu_seqlens [S + 1] DEVICE int32, 4-byte aligned: 0 = cu[0] <= cu[1] <=
+ *          ... <= cu[S] = T, every segment cu[s+1] - cu[s] <= n (empty
+ *          segments allowed).  A table that breaks these rules sets device
+ *          status bit 6; the kernels clamp it so that every access stays
+ *          inside the tensors (the results are then undefined).
+ *   q, o, dout, dq [T, Hq, d]; k, v, dk, dv [T, Hkv, d] (dtypes as in the
+ *          unpacked calls); lse [Hq, T] f32 (natural log), written by the
+ *          forward and read by the backward.
+ *   dkc, dvc [p, Hkv, d] f32: summed over every segment; frozen rows as in
+ *          cart_attn_bwd_parts (frozen_rows may be NULL when n_frozen == 0).
+ * Workspace: the *_packed_workspace_size() answers (0 for bad sizes).     */
+CART_API size_t cart_attn_fwd_packed_workspace_size(const cart_geom* g, int total,
+                                                    cart_dtype in_dtype, cart_dtype cart_dtype);
+CART_API int cart_attn_fwd_packed(const cart_geom* g, int total, const int* cu_seqlens,
+                                  cart_dtype in_dtype, cart_dtype cart_dtype, const void* q,
+                                  const void* k, const void* v, const void* kc, const void* vc,
+                                  void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+CART_API size_t cart_attn_bwd_packed_workspace_size(const cart_geom* g, int total,
+                                                    cart_dtype in_dtype, cart_dtype cart_dtype);
+CART_API int cart_attn_bwd_packed(const cart_geom* g, int total, const int* cu_seqlens,
+                                  cart_dtype in_dtype, cart_dtype cart_dtype, const void* q,
+                                  const void* k, const void* v, const void* kc, const void* vc,
+                                  const void* o, const float* lse, const void* dout, void* dq,
+                                  void* dk, void* dv, float* dkc, float* dvc,
+                                  const int* frozen_rows, int n_frozen, int accumulate,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * cart_attn_decode -- one q_seq = 1 decode step for B conversations behind
  * ONE shared cartridge.  (Cartridges guide, "Semantics", serving bullet: a
  * normal decode continues at position p with the training-time layout.)
@@ -238,7 +278,8 @@ CART_API const char* cart_status_string(int status);
  * when a bounded wait gives up (bit 0: a TMA copy, 1: an MMA, 2: the softmax
  * warps, 3: the epilogue), when a work schedule is inconsistent (bit 4), or
  * when the dynamic shared memory does not start 1024-byte aligned (bit 5;
- * the kernel then does nothing).  Synchronizes the current device.  Writes
+ * the kernel then does nothing), or when a packed segment table breaks its
+ * rules (bit 6).  Synchronizes the current device.  Writes
  * the bits to *bits_out (may be NULL); returns CART_OK, CART_ERR_TIMEOUT when
  * any bit is set, or CART_ERR_CUDA. */
 CART_API int cart_device_status(unsigned* bits_out, int clear);

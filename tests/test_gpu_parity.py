@@ -94,6 +94,67 @@ def test_bwd_composed_cartridge_parts(accumulate):
     gh.check_grads(got, ref, 1)
 
 
+PACKED = [
+    # (shape: heads, d, p, dtypes; B and n unused), segment lengths, max_seqlen
+    (_shape("packed_ragged", 0, 0, 8, 2, 128, 300, seed=120), (130, 1, 0, 257, 64), 257),
+    (_shape("packed_g8_d64", 0, 0, 8, 1, 64, 129, seed=121), (200, 77, 128), 256),
+    (_shape("packed_p0", 0, 0, 4, 2, 128, 0, frozen=0, seed=122), (40, 300, 129), 300),
+    (_shape("packed_f32", 0, 0, 4, 2, 128, 140, dtype="f32", seed=123), (100, 33, 150), 150),
+    (_shape("packed_bf16_cart", 0, 0, 4, 1, 128, 200, cart="bf16", seed=124), (1, 384, 2), 384),
+]
+
+
+def _run_packed(s, inp, max_seqlen, **kw):
+    g = gh.to_gpu({k: v for k, v in inp.items() if k != "max_seqlen"})
+    o, lse = cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], g["cu"],
+                                           max_seqlen, frozen_prefix=s.frozen_prefix,
+                                           theta=s.theta)
+    dq, dk, dv, dkc, dvc = cartattn.cart_attn_bwd_packed(
+        g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse, g["do"], g["cu"], max_seqlen,
+        frozen_prefix=s.frozen_prefix, theta=s.theta, **kw)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    out = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc)
+    return {k: synth.f64(v) for k, v in out.items()}
+
+
+@pytest.mark.parametrize("case", PACKED, ids=[c[0].name for c in PACKED])
+def test_packed_parity(case):
+    """Packed segments (ragged, empty, one-token, exactly one tile, a bound
+    above the longest) against the oracle's per-segment definition."""
+    s, lens, max_seqlen = case
+    inp = synth.packed_inputs(s, lens)
+    got = _run_packed(s, inp, max_seqlen)
+    a = {k: synth.f64(v) for k, v in inp.items() if k not in ("cu", "max_seqlen")}
+    cu = inp["cu"].numpy()
+    o, lse = oracle.fwd_packed(a["q"], a["k"], a["v"], a["kc"], a["vc"], cu,
+                               frozen_prefix=s.frozen_prefix, theta=s.theta)
+    ref = dict(o=o, lse=lse)
+    ref.update(zip(("dq", "dk", "dv", "dkc", "dvc"),
+                   oracle.bwd_packed(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["do"], cu,
+                                     frozen_prefix=s.frozen_prefix, theta=s.theta)))
+    gh.check_fwd(got, ref)
+    gh.check_grads(got, ref, s.frozen_prefix)
+
+
+def test_packed_equal_segments_match_the_batch_bitwise():
+    """Equal-length packed segments run the same tiles as the [B, n] batch:
+    every output is bit for bit the batched call's (the ragged tails read the
+    next segment's rows instead of zeros, which the masks remove exactly)."""
+    s = _shape("packed_vs_batch", 3, 200, 8, 2, 128, 257, seed=125)
+    inp = synth.train_inputs(s)
+    batch = gh.run_train_gpu(s, inp)
+    T = s.B * s.n
+    flat = {k: inp[k].reshape(T, *inp[k].shape[2:]) for k in ("q", "k", "v", "do")}
+    flat.update(kc=inp["kc"], vc=inp["vc"], cu=torch.arange(0, T + 1, s.n, dtype=torch.int32))
+    got = _run_packed(s, flat, s.n)
+    for k in ("o", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(got[k], batch[k].reshape(T, *batch[k].shape[2:]), err_msg=k)
+    np.testing.assert_array_equal(got["lse"], batch["lse"].transpose(1, 0, 2).reshape(s.Hq, T))
+    np.testing.assert_array_equal(got["dkc"], batch["dkc"])
+    np.testing.assert_array_equal(got["dvc"], batch["dvc"])
+
+
 def test_backward_is_deterministic():
     s = _shape("det", 2, 200, 8, 2, 128, 300, seed=111)
     inp = synth.train_inputs(s)

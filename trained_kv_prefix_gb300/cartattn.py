@@ -78,6 +78,15 @@ def lib():
             L.cart_attn_decode_span_workspace_size.restype = sz
             L.cart_attn_decode_span.argtypes = [i, i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp,
                                                 vp, i, vp, vp, vp, sz, vp]
+            L.cart_attn_fwd_packed_workspace_size.argtypes = [G, i, i, i]
+            L.cart_attn_fwd_packed_workspace_size.restype = sz
+            L.cart_attn_fwd_packed.argtypes = [G, i, vp, i, i, vp, vp, vp, vp, vp, vp, vp, vp,
+                                               sz, vp]
+            L.cart_attn_bwd_packed_workspace_size.argtypes = [G, i, i, i]
+            L.cart_attn_bwd_packed_workspace_size.restype = sz
+            L.cart_attn_bwd_packed.argtypes = [G, i, vp, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                               vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int), i, i,
+                                               vp, sz, vp]
             L.cart_status_string.argtypes = [i]
             L.cart_status_string.restype = ctypes.c_char_p
             L.cart_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
@@ -85,6 +94,7 @@ def lib():
             L.cart_trace_count.argtypes = []
             L.cart_trace_get.argtypes = [i, ctypes.c_char_p, i, ctypes.POINTER(ctypes.c_float)]
             for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd", "cart_attn_bwd_parts",
+                         "cart_attn_fwd_packed", "cart_attn_bwd_packed",
                          "cart_attn_decode", "cart_attn_decode_span", "cart_device_status",
                          "cart_trace_enable",
                          "cart_trace_count", "cart_trace_get"):
@@ -98,7 +108,9 @@ EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd
            "cart_attn_decode_workspace_size",
            "cart_attn_decode", "cart_status_string", "cart_device_status", "cart_trace_enable",
            "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc",
-           "cart_attn_decode_span_workspace_size", "cart_attn_decode_span")
+           "cart_attn_decode_span_workspace_size", "cart_attn_decode_span",
+           "cart_attn_fwd_packed_workspace_size", "cart_attn_fwd_packed",
+           "cart_attn_bwd_packed_workspace_size", "cart_attn_bwd_packed")
 
 
 def _check(fn: str, rc: int):
@@ -218,6 +230,80 @@ def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None,
                                        len(rows), 1 if accumulate else 0, _ptr(ws), ws.numel(),
                                        _stream(stream, q.device))
         _check("cart_attn_bwd_parts", rc)
+    return dq, dk, dv, dkc[:p], dvc[:p]
+
+
+def fwd_packed_workspace_size(g: _Geom, total: int, in_dtype: int, cart_dtype: int) -> int:
+    return int(lib().cart_attn_fwd_packed_workspace_size(ctypes.byref(g), total, in_dtype,
+                                                         cart_dtype))
+
+
+def bwd_packed_workspace_size(g: _Geom, total: int, in_dtype: int, cart_dtype: int) -> int:
+    return int(lib().cart_attn_bwd_packed_workspace_size(ctypes.byref(g), total, in_dtype,
+                                                         cart_dtype))
+
+
+def _packing(cu_seqlens, max_seqlen, q):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != q.device:
+        raise TypeError("cu_seqlens must be int32 on the tensors' device")
+    return cu_seqlens.numel() - 1, int(max_seqlen), q.shape[0]
+
+
+def cart_attn_fwd_packed(q, k, v, kc, vc, cu_seqlens, max_seqlen, *, frozen_prefix=1,
+                         scale=None, theta=1.0e6, o=None, lse=None, workspace=None, stream=None):
+    """Training forward on packed segments.  q ``[T, Hq, d]``, k/v
+    ``[T, Hkv, d]`` (not rotated), segment s = tokens cu_seqlens[s] ..
+    cu_seqlens[s+1]-1 (int32 on the device), none longer than max_seqlen.
+    Returns ``(o [T, Hq, d], lse [Hq, T] f32)``."""
+    S, n, T = _packing(cu_seqlens, max_seqlen, q)
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    p = kc.shape[0]
+    g = geom(S, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta)
+    dt, cd = _dt(q), _dt(kc)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    ws = _workspace(fwd_packed_workspace_size(g, T, dt, cd), q.device, workspace)
+    rc = lib().cart_attn_fwd_packed(ctypes.byref(g), T, _ptr(cu_seqlens), dt, cd, _ptr(q),
+                                    _ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse),
+                                    _ptr(ws), ws.numel(), _stream(stream, q.device))
+    _check("cart_attn_fwd_packed", rc)
+    return o, lse
+
+
+def cart_attn_bwd_packed(q, k, v, kc, vc, o, lse, dout, cu_seqlens, max_seqlen, *,
+                         frozen_prefix=1, scale=None, theta=1.0e6, accumulate=False, dq=None,
+                         dk=None, dv=None, dkc=None, dvc=None, workspace=None, stream=None,
+                         frozen_rows=()):
+    """Backward on packed segments (layouts of cart_attn_fwd_packed).
+    Returns ``(dq, dk, dv, dkc, dvc)``; dkc/dvc f32 ``[p, Hkv, d]`` summed
+    over the segments, frozen rows exactly 0."""
+    S, n, T = _packing(cu_seqlens, max_seqlen, q)
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    p = kc.shape[0]
+    g = geom(S, n, Hq, Hkv, d, p, frozen_prefix, scale, theta)
+    dt, cd = _dt(q), _dt(kc)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dkc is None:
+        dkc = (torch.zeros if accumulate else torch.empty)((max(p, 1), Hkv, d),
+                                                           dtype=torch.float32, device=q.device)
+    if dvc is None:
+        dvc = (torch.zeros if accumulate else torch.empty)((max(p, 1), Hkv, d),
+                                                           dtype=torch.float32, device=q.device)
+    ws = _workspace(bwd_packed_workspace_size(g, T, dt, cd), q.device, workspace)
+    rows = list(frozen_rows)
+    arr = (ctypes.c_int * max(len(rows), 1))(*rows)
+    rc = lib().cart_attn_bwd_packed(ctypes.byref(g), T, _ptr(cu_seqlens), dt, cd, _ptr(q),
+                                    _ptr(k), _ptr(v), _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse),
+                                    _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkc),
+                                    _ptr(dvc), arr, len(rows), 1 if accumulate else 0, _ptr(ws),
+                                    ws.numel(), _stream(stream, q.device))
+    _check("cart_attn_bwd_packed", rc)
     return dq, dk, dv, dkc[:p], dvc[:p]
 
 

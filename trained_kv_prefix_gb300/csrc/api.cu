@@ -155,7 +155,19 @@ struct TrainWs {
   int npad = 0;
 };
 
-TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
+// Packed layout (see SeqRows): cu == nullptr for the fixed [B, n, ...] one.
+struct Packing {
+  const int* cu = nullptr;
+  int total = 0;
+};
+
+// Tokens on the training tensors' token axis.
+long long token_rows(const cart_geom* g, const Packing& pk) {
+  return pk.cu ? pk.total : static_cast<long long>(g->B) * g->n;
+}
+
+TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd,
+                 const Packing& pk = Packing()) {
   TrainWs w;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -164,8 +176,8 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
     return o;
   };
   const size_t e16 = 2;
-  const size_t rows_q = static_cast<size_t>(g->B) * g->n * g->Hq * g->d;
-  const size_t rows_k = static_cast<size_t>(g->B) * g->n * g->Hkv * g->d;
+  const size_t rows_q = static_cast<size_t>(token_rows(g, pk)) * g->Hq * g->d;
+  const size_t rows_k = static_cast<size_t>(token_rows(g, pk)) * g->Hkv * g->d;
   const size_t cart = static_cast<size_t>(g->p) * g->Hkv * g->d;
   w.table = take(static_cast<size_t>(g->n) * (g->d / 2) * sizeof(float2));
   w.qr = take(rows_q * e16);
@@ -181,6 +193,14 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd) {
   }
   w.total = off;
   return w;
+}
+
+// TMA map over a training tensor [B, n, H, d] (fixed) or [total, H, d]
+// (packed) as (d, H, n, B) or (d, H, total, 1).
+bool make_tokens_map(CUtensorMap* m, const void* base, const cart_geom* g, const Packing& pk,
+                     int H, uint32_t box_rows) {
+  return pk.cu ? make_rows_map(m, base, 1, pk.total, H, g->d, box_rows)
+               : make_rows_map(m, base, g->B, g->n, H, g->d, box_rows);
 }
 
 #define CART_CUDA(x)                                  \
@@ -219,8 +239,8 @@ struct PrepVec {
 // generic kernels and the caller computes the vectors.
 int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
                const void* v, const void* kc, const void* vc, uint8_t* ws, const TrainWs& w,
-               cudaStream_t st, TrainPrep* out, bool q_in_kernel = false,
-               const PrepVec& vec = PrepVec()) {
+               cudaStream_t st, TrainPrep* out, bool q_in_kernel, const PrepVec& vec,
+               const Packing& pk) {
   const bool f32 = in == CART_F32;
   if (f32) q_in_kernel = false;
   float2* table = reinterpret_cast<float2*>(ws + w.table);
@@ -232,17 +252,20 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         q_in_kernel ? nullptr : qr, kr, table, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
         static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
-        vec.lse, vec.nDvec, vec.nlse2, vec.npad, st));
+        vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, st));
     if (q_in_kernel) qr = static_cast<__nv_bfloat16*>(const_cast<void*>(q));
   } else {
     CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, freqs, st));
-    CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, st));
-    CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, st));
+    CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, pk.cu, pk.total,
+                               st));
+    CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, pk.cu, pk.total,
+                               st));
   }
   const void* vb = v;
   if (f32) {
     __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.vb);
-    CART_CUDA(launch_rope_rows(v, true, t, table, g->B, g->n, g->Hkv, g->d, false, st));
+    CART_CUDA(launch_rope_rows(v, true, t, table, g->B, g->n, g->Hkv, g->d, false, pk.cu, pk.total,
+                               st));
     vb = t;
   }
   const void* kcb = kc;
@@ -264,9 +287,9 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
   out->vb = vb;
   out->kcb = kcb;
   out->vcb = vcb;
-  bool ok = make_rows_map(&out->mQ, qr, g->B, g->n, g->Hq, g->d, 128) &&
-            make_rows_map(&out->mK, kr, g->B, g->n, g->Hkv, g->d, 128) &&
-            make_rows_map(&out->mV, vb, g->B, g->n, g->Hkv, g->d, 128);
+  bool ok = make_tokens_map(&out->mQ, qr, g, pk, g->Hq, 128) &&
+            make_tokens_map(&out->mK, kr, g, pk, g->Hkv, 128) &&
+            make_tokens_map(&out->mV, vb, g, pk, g->Hkv, 128);
   if (g->p > 0)
     ok = ok && make_rows_map(&out->mKc, kcb, 1, g->p, g->Hkv, g->d, 128) &&
          make_rows_map(&out->mVc, vcb, 1, g->p, g->Hkv, g->d, 128);
@@ -276,9 +299,22 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
   return ok ? CART_OK : CART_ERR_CUDA;
 }
 
+// Packed layout: at least one token, no more than B segments of n tokens
+// hold, a 4-byte aligned table (its contents are checked on the device).
+int check_packing(const cart_geom* g, const Packing& pk) {
+  if (!pk.cu) return CART_OK;
+  if (pk.total < 1 || static_cast<long long>(pk.total) > static_cast<long long>(g->B) * g->n)
+    return CART_ERR_GEOMETRY;
+  if (reinterpret_cast<uintptr_t>(pk.cu) & 3u) return CART_ERR_POINTER;
+  return CART_OK;
+}
+
 int train_common_checks(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
-                        const void* k, const void* v, const void* kc, const void* vc) {
+                        const void* k, const void* v, const void* kc, const void* vc,
+                        const Packing& pk) {
   int rc = check_geom(g);
+  if (rc) return rc;
+  rc = check_packing(g, pk);
   if (rc) return rc;
   if (!dtype_ok(in) || !dtype_ok(cd)) return CART_ERR_DTYPE;
   if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return CART_ERR_POINTER;
@@ -339,25 +375,20 @@ int cart_write_to_cache(const float* kc, const float* vc, int p, int Hkv, int d,
   return CART_OK;
 }
 
-size_t cart_attn_fwd_workspace_size(const cart_geom* g, cart_dtype in, cart_dtype cd) {
-  if (check_geom(g) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
-  return train_ws(g, in, cd, false).total;
-}
-
-int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
-                  const void* v, const void* kc, const void* vc, void* o, float* lse,
-                  void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = train_common_checks(g, in, cd, q, k, v, kc, vc);
+static int fwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_dtype cd,
+                    const void* q, const void* k, const void* v, const void* kc, const void* vc,
+                    void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = train_common_checks(g, in, cd, q, k, v, kc, vc, pk);
   if (rc) return rc;
   if (!o || !lse || !aligned16(o) || !aligned16(lse)) return CART_ERR_POINTER;
-  const TrainWs w = train_ws(g, in, cd, false);
+  const TrainWs w = train_ws(g, in, cd, false, pk);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TrainPrep tp;
   rc = train_prep(g, in, cd, q, k, v, kc, vc, static_cast<uint8_t*>(workspace), w, st, &tp,
-                  /*q_in_kernel=*/true);
+                  /*q_in_kernel=*/true, PrepVec(), pk);
   if (rc) return rc;
   FwdLaunch l{};
   l.mQ = &tp.mQ;
@@ -381,13 +412,47 @@ int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
   l.decode = false;
   l.rotate_q = tp.q_in_kernel;
   l.table = tp.table;
+  l.cu = pk.cu;
+  l.total = pk.total;
   CUtensorMap mO32;
   if (in == CART_BF16) {
-    if (!make_rows_map(&mO32, o, g->B, g->n, g->Hq, g->d, 32)) return CART_ERR_CUDA;
+    if (!make_tokens_map(&mO32, o, g, pk, g->Hq, 32)) return CART_ERR_CUDA;
     l.mO32 = &mO32;
   }
   CART_CUDA(launch_fwd(l, st));
   return CART_OK;
+}
+
+size_t cart_attn_fwd_workspace_size(const cart_geom* g, cart_dtype in, cart_dtype cd) {
+  if (check_geom(g) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
+  return train_ws(g, in, cd, false).total;
+}
+
+int cart_attn_fwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
+                  const void* v, const void* kc, const void* vc, void* o, float* lse,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(g, Packing(), in, cd, q, k, v, kc, vc, o, lse, workspace, workspace_bytes,
+                  stream);
+}
+
+size_t cart_attn_fwd_packed_workspace_size(const cart_geom* g, int total, cart_dtype in,
+                                           cart_dtype cd) {
+  Packing pk;
+  pk.cu = reinterpret_cast<const int*>(16);  // any non-null table: sizes only
+  pk.total = total;
+  if (check_geom(g) || check_packing(g, pk) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
+  return train_ws(g, in, cd, false, pk).total;
+}
+
+int cart_attn_fwd_packed(const cart_geom* g, int total, const int* cu_seqlens, cart_dtype in,
+                         cart_dtype cd, const void* q, const void* k, const void* v,
+                         const void* kc, const void* vc, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Packing pk;
+  pk.cu = cu_seqlens;
+  pk.total = total;
+  if (!cu_seqlens) return CART_ERR_POINTER;
+  return fwd_impl(g, pk, in, cd, q, k, v, kc, vc, o, lse, workspace, workspace_bytes, stream);
 }
 
 size_t cart_attn_bwd_workspace_size(const cart_geom* g, cart_dtype in, cart_dtype cd) {
@@ -395,20 +460,12 @@ size_t cart_attn_bwd_workspace_size(const cart_geom* g, cart_dtype in, cart_dtyp
   return train_ws(g, in, cd, true).total;
 }
 
-int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
-                  const void* v, const void* kc, const void* vc, const void* o, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, float* dkc, float* dvc,
-                  int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
-  return cart_attn_bwd_parts(g, in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
-                             nullptr, 0, accumulate, workspace, workspace_bytes, stream);
-}
-
-int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
-                        const void* k, const void* v, const void* kc, const void* vc,
-                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
-                        void* dv, float* dkc, float* dvc, const int* frozen_rows, int n_frozen,
-                        int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = train_common_checks(g, in, cd, q, k, v, kc, vc);
+static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_dtype cd,
+                    const void* q, const void* k, const void* v, const void* kc, const void* vc,
+                    const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                    void* dv, float* dkc, float* dvc, const int* frozen_rows, int n_frozen,
+                    int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = train_common_checks(g, in, cd, q, k, v, kc, vc, pk);
   if (rc) return rc;
   if (n_frozen < 0 || n_frozen > CART_MAX_FROZEN_ROWS || (n_frozen > 0 && !frozen_rows))
     return CART_ERR_GEOMETRY;
@@ -419,7 +476,7 @@ int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const 
     return CART_ERR_POINTER;
   if (g->p > 0 && (!dkc || !dvc || !aligned16(dkc) || !aligned16(dvc))) return CART_ERR_POINTER;
   if (accumulate != 0 && accumulate != 1) return CART_ERR_GEOMETRY;
-  const TrainWs w = train_ws(g, in, cd, true);
+  const TrainWs w = train_ws(g, in, cd, true, pk);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
@@ -438,19 +495,20 @@ int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const 
     vec.nlse2 = nlse2;
     vec.npad = w.npad;
   }
-  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp, false, vec);
+  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp, false, vec, pk);
   if (rc) return rc;
   const void* dob = dout;
   if (f32) {
     __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(ws + w.dob);
-    CART_CUDA(launch_rope_rows(dout, true, t, tp.table, g->B, g->n, g->Hq, g->d, false, st));
+    CART_CUDA(launch_rope_rows(dout, true, t, tp.table, g->B, g->n, g->Hq, g->d, false, pk.cu,
+                               pk.total, st));
     dob = t;
     CART_CUDA(launch_bwd_vec(o, dout, f32, lse, nDvec, nlse2, g->B, g->n, w.npad, g->Hq, g->d,
-                             st));
+                             pk.cu, pk.total, st));
   }
   CUtensorMap mdO, mdQ;
-  if (!make_rows_map(&mdO, dob, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
-  if (!f32 && !make_rows_map(&mdQ, dq, g->B, g->n, g->Hq, g->d, 128)) return CART_ERR_CUDA;
+  if (!make_tokens_map(&mdO, dob, g, pk, g->Hq, 128)) return CART_ERR_CUDA;
+  if (!f32 && !make_tokens_map(&mdQ, dq, g, pk, g->Hq, 128)) return CART_ERR_CUDA;
   BwdLaunch l{};
   l.mQ = &tp.mQ;
   l.mdO = &mdO;
@@ -481,6 +539,8 @@ int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const 
   l.accumulate = accumulate;
   l.table = tp.table;
   l.freqs = &tp.freqs;
+  l.cu = pk.cu;
+  l.total = pk.total;
   SideStream* side = side_stream();
   if (!side) {
     CART_CUDA(launch_bwd(l, st, st));
@@ -494,6 +554,47 @@ int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const 
   CART_CUDA(cudaStreamWaitEvent(st, side->join, 0));
   CART_CUDA(e);
   return CART_OK;
+}
+
+
+int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
+                  const void* v, const void* kc, const void* vc, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* dkc, float* dvc,
+                  int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(g, Packing(), in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
+                  nullptr, 0, accumulate, workspace, workspace_bytes, stream);
+}
+
+int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
+                        const void* k, const void* v, const void* kc, const void* vc,
+                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                        void* dv, float* dkc, float* dvc, const int* frozen_rows, int n_frozen,
+                        int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(g, Packing(), in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
+                  frozen_rows, n_frozen, accumulate, workspace, workspace_bytes, stream);
+}
+
+size_t cart_attn_bwd_packed_workspace_size(const cart_geom* g, int total, cart_dtype in,
+                                           cart_dtype cd) {
+  Packing pk;
+  pk.cu = reinterpret_cast<const int*>(16);  // any non-null table: sizes only
+  pk.total = total;
+  if (check_geom(g) || check_packing(g, pk) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
+  return train_ws(g, in, cd, true, pk).total;
+}
+
+int cart_attn_bwd_packed(const cart_geom* g, int total, const int* cu_seqlens, cart_dtype in,
+                         cart_dtype cd, const void* q, const void* k, const void* v,
+                         const void* kc, const void* vc, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, float* dkc, float* dvc,
+                         const int* frozen_rows, int n_frozen, int accumulate, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Packing pk;
+  pk.cu = cu_seqlens;
+  pk.total = total;
+  if (!cu_seqlens) return CART_ERR_POINTER;
+  return bwd_impl(g, pk, in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
+                  frozen_rows, n_frozen, accumulate, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ decode --

@@ -57,7 +57,15 @@ struct BwdParams {
   // cartridge rows frozen besides those < frozen_prefix (composed parts' sinks)
   int n_frozen;
   int frozen_rows[CART_MAX_FROZEN_ROWS];
+  // packed layout (SeqRows): segment table and packed token count
+  const int* cu;
+  int total;
 };
+
+// 128-row query tiles of sequence b (cu: the packed table, or null).
+__device__ __forceinline__ int seq_qtiles(const BwdParams& a, const int* cu, int b) {
+  return cu ? (seq_rows(cu, a.total, a.n, b).len + kTile - 1) / kTile : a.n_qtiles;
+}
 
 // Cartridge row j gets no gradient: below frozen_prefix, or listed.
 __device__ __forceinline__ bool row_frozen(const BwdParams& a, int j) {
@@ -129,30 +137,47 @@ enum DkdvBar { kResFull = 0, kQFull0, kQEmpty0 = kQFull0 + kDkdvQSlots,
                kDkdvDrain, kDkdvBars };
 static_assert(kDkdvBars * 8 + 16 <= 256, "dK/dV barrier area");
 
-struct DkdvItem {
+// The steps of a key tile in order: a cartridge tile sees every (sequence,
+// head of the group, 128-row query tile), sequence-major; real tile rt of a
+// sequence sees the heads of the group and query tiles rt.. (the causal
+// diagonal and after).  The query tile runs fastest, then the head.
+struct DkdvCursor {
   int b, hh, qt;
-};
-
-// Step u of a key tile: a cartridge tile sees every (sequence, head of the
-// group, 128-row query tile); real tile rt of a sequence sees the heads of
-// the group and query tiles rt.. (the causal diagonal and after).
-__device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& a, bool cart, int b_real, int rt,
-                                              int u) {
-  DkdvItem it;
-  if (cart) {
-    const int per_b = a.G * a.n_qtiles;
-    it.b = u / per_b;
-    const int rem = u % per_b;
-    it.hh = rem / a.n_qtiles;
-    it.qt = rem % a.n_qtiles;
-  } else {
-    const int nq = a.n_qtiles - rt;
-    it.b = b_real;
-    it.hh = u / nq;
-    it.qt = rt + u % nq;
+  int nq;         // query tiles of sequence b
+  int row0, blk;  // sequence b on the maps' token axis
+  __device__ __forceinline__ void load_seq(const BwdParams& a, const int* cu) {
+    const SeqRows r = seq_rows(cu, a.total, a.n, b);
+    nq = cu ? (r.len + kTile - 1) / kTile : a.n_qtiles;
+    row0 = r.row0;
+    blk = r.blk;
   }
-  return it;
-}
+  __device__ __forceinline__ void start(const BwdParams& a, const int* cu, bool cart, int b_real,
+                                        int rt) {
+    b = cart ? 0 : b_real;
+    hh = 0;
+    qt = cart ? 0 : rt;
+    load_seq(a, cu);
+    if (cart) skip_empty(a, cu);
+  }
+  // (cartridge tiles) move past sequences without tokens
+  __device__ __forceinline__ void skip_empty(const BwdParams& a, const int* cu) {
+    while (nq == 0 && b + 1 < a.B) {
+      ++b;
+      load_seq(a, cu);
+    }
+  }
+  __device__ __forceinline__ void next(const BwdParams& a, const int* cu, bool cart, int rt) {
+    if (++qt < nq) return;
+    qt = cart ? 0 : rt;
+    if (++hh < a.G || !cart) return;
+    hh = 0;
+    if (b + 1 < a.B) {
+      ++b;
+      load_seq(a, cu);
+      skip_empty(a, cu);
+    }
+  }
+};
 
 __device__ __forceinline__ void write_cart_row(float* dst, const float* x, int n, bool frozen,
                                                int accumulate) {
@@ -169,7 +194,7 @@ __device__ __forceinline__ void write_cart_row(float* dst, const float* x, int n
   }
 }
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                 const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
@@ -187,6 +212,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDkdvBars * 8);
   int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDkdvBars * 8 + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* const cu = kPacked ? a.cu : nullptr;  // packed segment table
 
   // ---- work item: cartridge tiles first (heaviest), then real tiles ----
   int blk = blockIdx.x;
@@ -204,7 +230,17 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     b_real = rem / a.Hkv;
     g = rem % a.Hkv;
   }
-  const int U = cart ? a.B * a.G * a.n_qtiles : a.G * max(a.n_qtiles - tile, 0);
+  int U;
+  if (!cu) {
+    U = cart ? a.B * a.G * a.n_qtiles : a.G * max(a.n_qtiles - tile, 0);
+  } else if (cart) {  // packed: every segment's query tiles
+    int tiles = 0;
+    for (int b = 0; b < a.B; ++b) tiles += seq_qtiles(a, cu, b);
+    U = a.G * tiles;
+  } else {
+    U = a.G * max(seq_qtiles(a, cu, b_real) - tile, 0);
+  }
+  if (U == 0) return;  // a packed segment shorter than the longest
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -256,15 +292,30 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           tma_load_4d(sK + h * 16384, &mKc, &bars[kResFull], h * 64, g, tile * kTile, 0);
           tma_load_4d(sV + h * 16384, &mVc, &bars[kResFull], h * 64, g, tile * kTile, 0);
         } else {
-          tma_load_4d(sK + h * 16384, &mK, &bars[kResFull], h * 64, g, tile * kTile, b_real);
-          tma_load_4d(sV + h * 16384, &mV, &bars[kResFull], h * 64, g, tile * kTile, b_real);
+          const SeqRows r = seq_rows(cu, a.total, a.n, b_real);
+          tma_load_4d(sK + h * 16384, &mK, &bars[kResFull], h * 64, g, r.row0 + tile * kTile,
+                      r.blk);
+          tma_load_4d(sV + h * 16384, &mV, &bars[kResFull], h * 64, g, r.row0 + tile * kTile,
+                      r.blk);
         }
       }
       int issued_q = 0, issued_do = 0;
       bool ok = true;
+      DkdvCursor it;
+      if (kPacked) it.start(a, cu, cart, b_real, tile);
       for (int u = 0; u < U; ++u) {
         const int sq = u % SQ, sd = u % SD;
-        const DkdvItem it = dkdv_item(a, cart, b_real, tile, u);
+        if (kPacked) {
+          if (u > 0) it.next(a, cu, cart, tile);
+        } else {  // fixed layout: every sequence has n_qtiles query tiles
+          const int nq = cart ? a.n_qtiles : a.n_qtiles - tile;
+          const int per_b = a.G * nq;
+          it.b = cart ? u / per_b : b_real;
+          it.hh = (u % per_b) / nq;
+          it.qt = (cart ? 0 : tile) + u % nq;
+          it.row0 = 0;
+          it.blk = it.b;
+        }
         const int h = g * a.G + it.hh;
         uint8_t* sQ = smem + L::kQ0 + sq * L::kTileBytes;
         uint8_t* sdO = smem + L::kDo0 + sd * L::kTileBytes;
@@ -277,7 +328,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         mbar_arrive_expect_tx(&bars[kQFull0 + sq], L::kTileBytes + 512);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc)
-          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQFull0 + sq], hc * 64, h, it.qt * kTile, it.b);
+          tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQFull0 + sq], hc * 64, h,
+                      it.row0 + it.qt * kTile, it.blk);
         bulk_load(vecL + sq * 128, a.nlse2 + vo, 512, &bars[kQFull0 + sq]);
         issued_q = u + 1;
         if (u >= SD) {
@@ -288,8 +340,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         mbar_arrive_expect_tx(&bars[kDoFull0 + sd], L::kTileBytes + 512);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc)
-          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kDoFull0 + sd], hc * 64, h, it.qt * kTile,
-                      it.b);
+          tma_load_4d(sdO + hc * 16384, &mdO, &bars[kDoFull0 + sd], hc * 64, h,
+                      it.row0 + it.qt * kTile, it.blk);
         bulk_load(vecD + sd * 128, a.nDvec + vo, 512, &bars[kDoFull0 + sd]);
         issued_do = u + 1;
       }
@@ -405,7 +457,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const int wg = warp >> 2;
     const int row = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const int j = tile * kTile + row;
-    const bool key_ok = cart ? (j < a.p) : (j < a.n);
+    // real tiles: the sequence's query tiles and tokens
+    const int nq_real = cart ? 0 : seq_qtiles(a, cu, b_real);
+    const bool key_ok = cart ? (j < a.p) : (j < (cu ? seq_rows(cu, a.total, a.n, b_real).len : a.n));
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
     // ring slots, their phases and (real tiles) the query tile of step u,
@@ -492,7 +546,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       mbar_arrive(&bars[kDsFull]);
       if (++sq == SQ) sq = 0, phq ^= 1u;
       if (++sd == SD) sd = 0, phd ^= 1u;
-      if (++qt == a.n_qtiles) qt = tile;  // real tiles: query tiles tile..n_qtiles-1
+      if (++qt == nq_real) qt = tile;  // real tiles: query tiles tile..nq_real-1
     }
     // ------------------------------------------------------------ epilogue --
     // warpgroups 0 and 1 write the two halves of dV; 2 and 3 take the RoPE
@@ -520,7 +574,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             write_cart_row(a.dvc + (static_cast<long long>(j) * a.Hkv + g) * D + wg * HW, x, HW,
                            row_frozen(a, j), a.accumulate);
           else
-            store_row_out(a.dv, ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D + wg * HW,
+            store_row_out(a.dv,
+                          ((static_cast<long long>(seq_rows(cu, a.total, a.n, b_real).g0) + j) *
+                               a.Hkv + g) * D + wg * HW,
                           x, HW, a.out_f32 != 0);
         }
       } else {
@@ -556,7 +612,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
               lo[e] = x0 * cs.x + x1 * cs.y;
               hi[e] = x1 * cs.x - x0 * cs.y;
             }
-            const long long off = ((static_cast<long long>(b_real) * a.n + j) * a.Hkv + g) * D;
+            const long long off =
+                ((static_cast<long long>(seq_rows(cu, a.total, a.n, b_real).g0) + j) * a.Hkv +
+                 g) * D;
             store_row_out(a.dk, off + w2 * QP, lo, QP, a.out_f32 != 0);
             store_row_out(a.dk, off + D / 2 + w2 * QP, hi, QP, a.out_f32 != 0);
           }
@@ -619,7 +677,7 @@ enum DqBar {
 static_assert(kDqBars * 8 + 16 <= 256, "dQ barrier area");
 static_assert(kDqBars * 8 + 4 <= 256, "dq barrier area");
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
               const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
@@ -637,13 +695,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDqBars * 8);
   int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDqBars * 8 + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* const cu = kPacked ? a.cu : nullptr;  // packed segment table
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);
+  const int seq_len = cu ? seq_rows(cu, a.total, a.n, b).len : a.n;
+  if (kPacked && qt * kTile >= seq_len) return;  // a segment shorter than the longest
   const int kvh = h / a.G;
   const int q0 = qt * kTile;
   const int n_ct = (a.p + kTile - 1) / kTile;
-  const int last_q = min(q0 + kTile, a.n) - 1;          // last real query of the tile
+  const int last_q = min(q0 + kTile, seq_len) - 1;      // last real query of the tile
   const int n_rt = last_q / kTile + 1;                   // real key steps up to the diagonal
   const int T = n_ct + n_rt;
 
@@ -686,18 +747,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
+      const SeqRows sr = seq_rows(cu, a.total, a.n, b);
       mbar_arrive_expect_tx(&bars[kQdFull], 2 * L::kTileBytes);
 #pragma unroll
       for (int hc = 0; hc < D / 64; ++hc) {
-        tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdFull], hc * 64, h, q0, b);
-        tma_load_4d(sdO + hc * 16384, &mdO, &bars[kQdFull], hc * 64, h, q0, b);
+        tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdFull], hc * 64, h, sr.row0 + q0, sr.blk);
+        tma_load_4d(sdO + hc * 16384, &mdO, &bars[kQdFull], hc * 64, h, sr.row0 + q0, sr.blk);
       }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int t = 0; t < T && ok; ++t) {
         const bool cart = t < n_ct;
-        const int row0 = cart ? t * kTile : (t - n_ct) * kTile;
-        const int blk = cart ? 0 : b;
+        const int row0 = cart ? t * kTile : sr.row0 + (t - n_ct) * kTile;
+        const int blk = cart ? 0 : sr.blk;
         const int sk = t % SK, sv = t % SV;
         if (t >= SK) {
           ok = mbar_wait(&bars[kKEmpty0 + sk], ((t / SK) - 1) & 1, abort_s, a.status,
@@ -818,7 +880,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float nl = __ldg(a.nlse2 + vidx), nd = __ldg(a.nDvec + vidx);
     const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
     const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
-    const int i_cap = min(i, a.n - 1);
+    const int i_cap = min(i, seq_len - 1);
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
       const int x = t & 1;
@@ -898,7 +960,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) hi[c * 16 + e] = __uint_as_float(r[e]) * a.scale;
       }
-      if (i < a.n) {
+      if (i < seq_len) {
         // inverse rotation at position p + i; (cos, sin) computed here: one
         // row of table per thread would be gathered uncoalesced
 #pragma unroll
@@ -909,7 +971,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           hi[e] = x1 * cs.x - x0 * cs.y;
         }
       }
-      if (a.tma_dq) {
+      const SeqRows sr = seq_rows(cu, a.total, a.n, b);
+      // a packed segment's last tile: a TMA store would run into the next
+      // segment, so its rows are stored one by one
+      if (a.tma_dq && (!cu || q0 + kTile <= seq_len || sr.row0 + seq_len == a.total)) {
         // Stage the row's columns in the (spent) Q tile, in the swizzled
         // layout of the dQ map's 128-row box, then one thread stores the
         // tile; rows past n are clipped by the map.
@@ -932,13 +997,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (threadIdx.x == 0) {
           if (mbar_wait(&bars[kDqStaged], 0, abort_s, a.status, kDevErrTimeoutEpilogue)) {
 #pragma unroll
-            for (int hc = 0; hc < D / 64; ++hc) tma_store_4d(&mdQ, sQ + hc * 16384, hc * 64, h, q0, b);
+            for (int hc = 0; hc < D / 64; ++hc)
+              tma_store_4d(&mdQ, sQ + hc * 16384, hc * 64, h, sr.row0 + q0, sr.blk);
             bulk_commit_group();
             bulk_wait_all();
           }
         }
-      } else if (i < a.n) {
-        const long long off = ((static_cast<long long>(b) * a.n + i) * a.Hq + h) * D;
+      } else if (i < seq_len) {
+        const long long off = ((static_cast<long long>(sr.g0) + i) * a.Hq + h) * D;
         store_row_out(a.dq, off + wg * Q, lo, Q, a.out_f32 != 0);
         store_row_out(a.dq, off + D / 2 + wg * Q, hi, Q, a.out_f32 != 0);
       }
@@ -981,23 +1047,30 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.dvc = l.dvc;
   p.accumulate = l.accumulate;
   p.table = l.table;
+  p.cu = l.cu;
+  p.total = l.total;
   for (int c = 0; c < D / 2; ++c) p.turns[c] = l.freqs->turns[c];
   p.status = device_status_ptr();
-  cudaError_t e = set_smem_once<dkdv_kernel<D>>(DkdvSmem<D>::kAlloc);
+  const bool packed = l.cu != nullptr;
+  cudaError_t e = packed ? set_smem_once<dkdv_kernel<D, true>>(DkdvSmem<D>::kAlloc)
+                         : set_smem_once<dkdv_kernel<D, false>>(DkdvSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  e = set_smem_once<dq_kernel<D>>(DqSmem<D>::kAlloc);
+  e = packed ? set_smem_once<dq_kernel<D, true>>(DqSmem<D>::kAlloc)
+             : set_smem_once<dq_kernel<D, false>>(DqSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_blocks = p.n_ct * p.Hkv + p.n_rt * p.Hkv * p.B;
   if (n_blocks > 0) {
     TraceScope tr("bwd_dkdv", st_dkdv);
-    dkdv_kernel<D><<<n_blocks, kDkdvThreads, DkdvSmem<D>::kAlloc, st_dkdv>>>(
-        *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
+    auto* kern = packed ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
+    kern<<<n_blocks, kDkdvThreads, DkdvSmem<D>::kAlloc, st_dkdv>>>(*l.mQ, *l.mdO, *l.mKc, *l.mVc,
+                                                                   *l.mK, *l.mV, p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   TraceScope tr("bwd_dq", st_dq);
   p.tma_dq = (!l.out_f32 && l.mdQ) ? 1 : 0;
-  dq_kernel<D><<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
+  auto* kern_dq = packed ? dq_kernel<D, true> : dq_kernel<D, false>;
+  kern_dq<<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
       *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p.tma_dq ? *l.mdQ : *l.mQ, p);
   return cudaGetLastError();
 }

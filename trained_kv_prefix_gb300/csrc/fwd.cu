@@ -55,6 +55,9 @@ struct FwdParams {
   const int* dec_len;
   int dec_B, dec_G, dec_rows;
   int dec_s;  // span: rows of one conversation's s queries are consecutive
+  // training, packed layout (SeqRows): segment table and packed token count
+  const int* cu;
+  int total;
   float2 turns[kMaxHeadDim / 2];
 };
 
@@ -201,7 +204,7 @@ struct RopeRowsCoop {
   }
 };
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
@@ -216,9 +219,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // packed training layout: the segment table (a constant null otherwise)
+  const int* const cu = kPacked ? a.cu : nullptr;
 
   // ---- work item (training: heaviest pairs first) ----
   int head, qb, pair, kvh, split;
+  // tokens of the query block's sequence (decode: the n_rows stacked rows);
+  // its place on the token axis is looked up again where it is used
+  int seq_len = a.n_rows;
   if (!a.decode) {
     const int hb = a.Hq_map * a.n_qblocks;
     pair = a.n_pairs - 1 - static_cast<int>(blockIdx.x) / hb;
@@ -227,6 +235,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     qb = rem / a.Hq_map;
     kvh = head / a.G;
     split = 0;
+    seq_len = seq_rows(cu, a.total, a.n_rows, qb).len;
   } else {
     head = blockIdx.x;
     qb = 0;
@@ -234,14 +243,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     kvh = head;
     split = blockIdx.z;
   }
-  const bool hasB = 2 * pair + 1 < a.n_qtiles;
+  const int n_qtiles = a.decode ? a.n_qtiles : (seq_len + kTile - 1) / kTile;
+  if (2 * pair >= n_qtiles) return;  // a packed segment shorter than the longest
+  const bool hasB = 2 * pair + 1 < n_qtiles;
   const int n_ct_all = (a.p + kTile - 1) / kTile;
   int ct_lo = 0, ct_hi = n_ct_all, n_rt_A = 0, n_rt_B = 0;
   if (a.decode) {
     ct_lo = split * a.cart_tiles_per_split;
     ct_hi = min(ct_lo + a.cart_tiles_per_split, n_ct_all);
   } else {
-    const int n_real_tiles = (a.n_real + kTile - 1) / kTile;
+    const int n_real_tiles = (seq_len + kTile - 1) / kTile;
     n_rt_A = min(2 * pair + 1, n_real_tiles);
     n_rt_B = hasB ? min(2 * pair + 2, n_real_tiles) : 0;
   }
@@ -288,6 +299,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
       const int q0A = 2 * pair * kTile;
+      const SeqRows sq = seq_rows(cu, a.total, a.n_rows, qb);  // training only
       mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
@@ -298,9 +310,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, 0,
                       kvh, (q0A + kTile) / a.dec_G);
         } else {
-          tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, q0A, qb);
+          tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, sq.row0 + q0A,
+                      sq.blk);
           tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, head,
-                      q0A + kTile, qb);
+                      sq.row0 + q0A + kTile, sq.blk);
         }
       }
       int k_issued = 0, v_issued = 0;
@@ -308,10 +321,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int t = 0; t < T && ok; ++t) {
         const int s = t & 1;
         const bool cart = t < n_ct;
-        const int row0 = cart ? (ct_lo + t) * kTile : (t - n_ct) * kTile;
+        const int row0 = cart ? (ct_lo + t) * kTile : sq.row0 + (t - n_ct) * kTile;
         const CUtensorMap* mk = cart ? &mKc : &mK;
         const CUtensorMap* mv = cart ? &mVc : &mV;
-        const int blk = cart ? 0 : qb;
+        const int blk = cart ? 0 : sq.blk;
         if (t >= 2) {
           ok = mbar_wait(&bars[kKEmpty0 + s], ((t >> 1) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
@@ -454,10 +467,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int r0 = (warp & 3) * 32;
         const int i0 = (2 * pair + x) * kTile + r0;
         RopeRowsCoop<D> rr;
-        rr.load(a.table, i0, a.n_rows, lane);
+        rr.load(a.table, i0, seq_len, lane);
         ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) rr.apply(smem + L::kQ + x * L::kTileBytes, r0, i0, a.n_rows, lane);
+        if (ok) rr.apply(smem + L::kQ + x * L::kTileBytes, r0, i0, seq_len, lane);
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
       } else if (a.decode) {
@@ -487,7 +500,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(&bars[kQReady0 + x]);
       }
     }
-    const int i_cap = min(i, a.n_real - 1);
+    const int i_cap = min(i, seq_len - 1);  // decode: no real keys, unused
     for (int t = 0; t < Tx && ok; ++t) {
       ok = mbar_wait(&bars[kSFull0 + x], t & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
@@ -587,9 +600,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const bool row_ok = i < a.n_rows;
+      const bool row_ok = i < seq_len;
       const bool f32 = a.decode || a.out_f32;
-      if (a.tma_out) {
+      const SeqRows sq = a.decode ? SeqRows{0, 0, 0, a.n_rows}
+                                  : seq_rows(cu, a.total, a.n_rows, qb);
+      // a packed segment's last rows: a TMA store of the warp's 32 rows would
+      // run into the next segment, so those warps store row by row
+      const int wr0 = (2 * pair + x) * kTile + (warp & 3) * 32;
+      const bool use_tma = a.tma_out && (!cu || wr0 + 32 <= sq.len ||
+                                         sq.row0 + sq.len == a.total);
+      if (use_tma) {
         // bf16 output by TMA: every thread writes its row into its tile's Q
         // buffer (every MMA that read Q_x is done) in the 128-byte-swizzled
         // layout of the output map's box, then lane 0 stores the warp's 32
@@ -617,10 +637,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int r0 = (2 * pair + x) * kTile + (warp & 3) * 32;
 #pragma unroll
           for (int h = 0; h < D / 64; ++h)
-            tma_store_4d(&mO32, sO + h * 16384 + (warp & 3) * 4096, h * 64, head, r0, qb);
+            tma_store_4d(&mO32, sO + h * 16384 + (warp & 3) * 4096, h * 64, head, sq.row0 + wr0,
+                         sq.blk);
           bulk_commit_group();
           bulk_wait_all();
         }
@@ -665,13 +685,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int gi = st * 32 + lane;
           const int r = gi / gpr, k = gi % gpr;
           const int grow = row0 + r;
-          if (grow < a.n_rows) {
+          if (grow < sq.len) {
             const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
             long long off;  // element offset of the row
             if (a.decode)
               off = ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + grow) * D;
             else
-              off = ((static_cast<long long>(qb) * a.n_rows + grow) * a.Hq_map + head) * D;
+              off = ((static_cast<long long>(sq.g0) + grow) * a.Hq_map + head) * D;
             if (f32)
               *reinterpret_cast<uint4*>(static_cast<float*>(a.out) + off + blk * 32 + k * 4) = v;
             else
@@ -687,7 +707,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (a.decode)
           a.lse[(static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i] = lse2;
         else
-          a.lse[(static_cast<long long>(qb) * a.Hq_map + head) * a.n_rows + i] =
+          a.lse[lse_index(cu, a.total, a.n_rows, a.Hq_map, qb, head, sq, i)] =
               lse2 * 0.69314718055994531f;
       }
     }
@@ -703,7 +723,9 @@ template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdSmem<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  cudaError_t e = set_smem_once<fwd_kernel<D>>(L::kAlloc);
+  const bool packed = !a.decode && a.cu;
+  cudaError_t e = packed ? set_smem_once<fwd_kernel<D, true>>(L::kAlloc)
+                         : set_smem_once<fwd_kernel<D, false>>(L::kAlloc);
   if (e != cudaSuccess) return e;
   FwdParams p{};
   p.n_rows = a.n_rows;
@@ -731,6 +753,9 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
     p.dec_rows = a.dec_rows;
     p.dec_s = a.dec_s;
     for (int j = 0; j < kMaxHeadDim / 2; ++j) p.turns[j] = a.freqs->turns[j];
+  } else {
+    p.cu = a.cu;
+    p.total = a.total;
   }
   dim3 grid;
   if (!a.decode)
@@ -748,7 +773,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fwd_kernel<D>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
+  return cudaLaunchKernelEx(&cfg, packed ? fwd_kernel<D, true> : fwd_kernel<D, false>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
                             p.tma_out ? *a.mO32 : *a.mQ, p);
 }
 

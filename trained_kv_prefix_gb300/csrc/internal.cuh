@@ -89,6 +89,47 @@ __device__ __forceinline__ float2 rope_cs_turns_fast(float2 turns, int pos) {
   return make_float2(c, s);
 }
 
+// Token axis of the training tensors.
+//   fixed layout (cu == nullptr): B sequences of n tokens, tensors
+//     [B, n, H, d], TMA maps (d, H, n, B);
+//   packed layout: B segments back to back on one axis of `total` tokens,
+//     segment b = tokens cu[b] .. cu[b+1] - 1 (at most n of them), tensors
+//     [total, H, d], TMA maps (d, H, total, 1).
+// In both, token i of sequence b sits at RoPE position p + i.
+struct SeqRows {
+  int row0;  // map row coordinate of the sequence's token 0
+  int blk;   // map block coordinate
+  int g0;    // flat token index of token 0 (plain addressing: (g0 + i) * H + h)
+  int len;   // tokens of the sequence
+};
+// A packed table is clamped so that every access stays inside the tensors
+// (a table that needed clamping is reported by the prep kernels).
+__device__ __forceinline__ SeqRows seq_rows(const int* cu, int total, int n, int b) {
+  SeqRows r;
+  if (!cu) {
+    r.row0 = 0;
+    r.blk = b;
+    r.g0 = b * n;
+    r.len = n;
+    return r;
+  }
+  int s0 = __ldg(cu + b), s1 = __ldg(cu + b + 1);
+  s0 = min(max(s0, 0), total);
+  s1 = min(max(s1, s0), min(total, s0 + n));
+  r.row0 = s0;
+  r.blk = 0;
+  r.g0 = s0;
+  r.len = s1 - s0;
+  return r;
+}
+// Index of (sequence b, head h, token i) in a forward log-sum-exp:
+// [B, Hq, n] for the fixed layout, [Hq, total] for the packed one.
+__device__ __forceinline__ long long lse_index(const int* cu, int total, int n, int Hq, int b,
+                                               int h, const SeqRows& r, int i) {
+  return cu ? static_cast<long long>(h) * total + r.g0 + i
+            : (static_cast<long long>(b) * Hq + h) * n + i;
+}
+
 // 4D bf16 TMA map with an arbitrary box and 128-byte swizzle; dims innermost
 // first, strides in bytes for dims 1..3 (api.cu).
 bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
@@ -105,11 +146,13 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
 // K rotated into kr, Q into qr (if qr), and with o given the backward's
 // [B, Hq, npad] vectors -D = -rowsum(dO * O) and -lse * log2(e), stored
 // negated (padding rows 0 and -inf).
+// cu / total: the packed layout (see SeqRows; cu == nullptr: fixed); the
+// packed table is checked here (status bit kDevErrSegments).
 cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
                               const __nv_bfloat16* dout, const float* lse, float* nDvec,
-                              float* nlse2, int npad, cudaStream_t st);
+                              float* nlse2, int npad, const int* cu, int total, cudaStream_t st);
 
 // cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2].
 cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
@@ -119,14 +162,15 @@ cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const Ro
 // table (row i of the table = position pos0 + i) and write bf16 to out (same
 // layout).  With rotate == false this is a plain convert/copy.
 cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, const float2* table,
-                             int B, int n, int H, int d, bool rotate, cudaStream_t st);
+                             int B, int n, int H, int d, bool rotate, const int* cu, int total,
+                             cudaStream_t st);
 
 // Per-row vectors of the backward in [B, Hq, npad] layout (npad >= n):
 // nDvec = -sum_c dO[b,i,h,c] * O[b,i,h,c], nlse2 = -lse * log2(e); padding
 // rows get 0 and -inf (zero probability).
 cudaError_t launch_bwd_vec(const void* o, const void* dout, bool f32, const float* lse,
                            float* nDvec, float* nlse2, int B, int n, int npad, int Hq, int d,
-                           cudaStream_t st);
+                           const int* cu, int total, cudaStream_t st);
 
 // ------------------------------------------------------------- forward ----
 struct FwdLaunch {
@@ -163,6 +207,10 @@ struct FwdLaunch {
   const RopeFreqs* freqs;  // host copy, read at launch
   bool pdl;                // launch as the programmatic dependent of the
                            // previous kernel on the stream
+  // training, packed layout (SeqRows): n_qblocks segments, n_rows = n_real
+  // = the longest; maps over (d, H, total, 1)
+  const int* cu = nullptr;
+  int total = 0;
 };
 // Two 128-row query tiles per CTA (training: consecutive row tiles of one
 // (sequence, head); decode: rows 0-127 / 128-255 of a kv head's stacked rows).
@@ -193,6 +241,10 @@ struct BwdLaunch {
   int accumulate;
   const float2* table;      // rope table for positions p .. p+n-1
   const RopeFreqs* freqs;   // rope angles (the epilogues' inverse rotation)
+  // packed layout (SeqRows): B segments of at most n tokens, maps over
+  // (d, H, total, 1); the row vectors stay [B, Hq, npad]
+  const int* cu = nullptr;
+  int total = 0;
 };
 // dK/dV kernel on st_dkdv, dQ kernel on st_dq (the two are independent).
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st_dkdv, cudaStream_t st_dq);

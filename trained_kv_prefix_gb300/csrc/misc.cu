@@ -94,18 +94,23 @@ __global__ void rope_table_kernel(float2* __restrict__ table, int pos0, int npos
 // ----------------------------------------------------------- rope rows ----
 // x [B, n, H, d] -> out bf16 same layout.  One thread owns 8 consecutive
 // pair indices j..j+7 of one row: elements j.. and j+d/2.. .
+// Packed layout (cu given): the same (b, i < n) index space, tokens past a
+// segment's end skipped, row (g0 + i) * H + h.
 template <bool kF32>
 __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __restrict__ out,
                                  const float2* __restrict__ table, int B, int n, int H, int d,
-                                 int rotate) {
+                                 int rotate, const int* __restrict__ cu, int ntok) {
   const int half = d / 2;
   const int chunks = half / 8;
   const long long total = static_cast<long long>(B) * n * H * chunks;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = t / chunks;  // (b * n + i) * H + h
+    const long long bih = t / chunks;  // (b * n + i) * H + h
     const int j0 = static_cast<int>(t % chunks) * 8;
-    const int i = static_cast<int>((row / H) % n);
+    const int i = static_cast<int>((bih / H) % n);
+    const SeqRows sr = seq_rows(cu, ntok, n, static_cast<int>(bih / (static_cast<long long>(H) * n)));
+    if (i >= sr.len) continue;
+    const long long row = (static_cast<long long>(sr.g0) + i) * H + bih % H;
     float x0[8], x1[8];
     if (kF32) {
       const float* x = static_cast<const float*>(xv) + row * d;
@@ -163,6 +168,9 @@ __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __r
 //     and -lse * log2(e) in [B, Hq, npad] (stored negated so that the
 //     backward kernels add them with packed two-lane arithmetic), padding
 //     rows npad > i >= n set to -D = 0 and -lse2 = -inf.
+// Packed layout (cu given, see SeqRows): sequence b is segment b, its token
+// i at flat row cu[b] + i; positions past a segment's end are padding of
+// the row vectors; block 0 also checks the segment table.
 constexpr int kPrepPos = 4;
 
 __device__ __forceinline__ void rotate_chunk8(const __nv_bfloat16* x, __nv_bfloat16* y,
@@ -187,15 +195,26 @@ __device__ __forceinline__ void rotate_chunk8(const __nv_bfloat16* x, __nv_bfloa
   *reinterpret_cast<uint4*>(y + half) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
+template <bool kPacked>
 __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr, float2* __restrict__ table,
     const RopeFreqs f, int p, int B, int n, int Hq, int Hkv, int d,
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, float* __restrict__ nDvec, float* __restrict__ nlse2, int npad,
-    int ppc) {
+    int ppc, const int* __restrict__ cu_arg, int ntok, uint32_t* status) {
+  const int* const cu = kPacked ? cu_arg : nullptr;
   __shared__ float2 cs[kPrepPos][kMaxHeadDim / 2];
   const int half = d / 2, chunks = half / 8;
+  if (cu && blockIdx.x == 0) {
+    // the packed table: rising from 0 to ntok, no segment longer than n
+    bool bad = threadIdx.x == 0 && (__ldg(cu) != 0 || __ldg(cu + B) != ntok);
+    for (int s = threadIdx.x; s < B; s += blockDim.x) {
+      const int len = __ldg(cu + s + 1) - __ldg(cu + s);
+      bad |= len < 0 || len > n;
+    }
+    if (bad && status) atomicOr(status, kDevErrSegments);
+  }
   const int i0 = blockIdx.x * ppc;
   const int np = max(0, min(ppc, n - i0));  // real positions in this block
   for (int t = threadIdx.x; t < np * half; t += blockDim.x) {
@@ -214,7 +233,9 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
       const int h = (t / chunks) % H;
       const int pb = t / (chunks * H);
       const int b = pb % B, pl = pb / B;
-      const long long row = (static_cast<long long>(b) * n + i0 + pl) * H + h;
+      const SeqRows sr = seq_rows(cu, ntok, n, b);
+      if (kPacked && i0 + pl >= sr.len) continue;  // past a segment's end
+      const long long row = (static_cast<long long>(sr.g0) + i0 + pl) * H + h;
       rotate_chunk8(x + row * d + jc * 8, y + row * d + jc * 8, &cs[pl][jc * 8], half);
     }
   };
@@ -231,11 +252,17 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     const int rr = base + ((threadIdx.x & 31) >> 3);
     float acc = 0.f;
     int h = 0, b = 0, pl = 0;
+    SeqRows sr{};
+    bool live = false;  // a token of its sequence (not past a packed segment's end)
     if (rr < rows) {
       h = rr % Hq;
       b = (rr / Hq) % B;
       pl = rr / (Hq * B);
-      const long long row = (static_cast<long long>(b) * n + i0 + pl) * Hq + h;
+      sr = seq_rows(cu, ntok, n, b);
+      live = !kPacked || i0 + pl < sr.len;
+    }
+    if (live) {
+      const long long row = (static_cast<long long>(sr.g0) + i0 + pl) * Hq + h;
       for (int c = lane8 * 8; c < d; c += 64) {
         const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + row * d + c));
         const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + row * d + c));
@@ -253,8 +280,10 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     if (lane8 == 0 && rr < rows) {
       const long long bh = static_cast<long long>(b) * Hq + h;
-      nDvec[bh * npad + i0 + pl] = -acc;
-      nlse2[bh * npad + i0 + pl] = __ldg(lse + bh * n + i0 + pl) * -1.4426950408889634f;
+      nDvec[bh * npad + i0 + pl] = live ? -acc : 0.f;
+      nlse2[bh * npad + i0 + pl] =
+          live ? __ldg(lse + lse_index(cu, ntok, n, Hq, b, h, sr, i0 + pl)) * -1.4426950408889634f
+               : -INFINITY;
     }
   }
   // padding rows of this block's positions
@@ -274,10 +303,13 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
 //   nlse2[b, h, i] = -lse[b, h, i] * log2(e)          (-inf for padding)
 // 8 lanes per row, 4 rows per warp; the loop trip count is uniform across
 // the warp.
+// Packed layout (cu given): the same (b, i < n, h) index space; tokens past
+// a segment's end are padding.
 template <bool kF32>
 __global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restrict__ dov,
                                const float* __restrict__ lse, float* __restrict__ nDvec,
-                               float* __restrict__ nlse2, int B, int n, int npad, int Hq, int d) {
+                               float* __restrict__ nlse2, int B, int n, int npad, int Hq, int d,
+                               const int* __restrict__ cu, int ntok) {
   const long long rows = static_cast<long long>(B) * n * Hq;
   const int lane8 = threadIdx.x & 7;
   const int group = (threadIdx.x & 31) >> 3;
@@ -286,9 +318,21 @@ __global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restri
   const long long warp_id = tid >> 5;
   const long long warps = nthreads >> 5;
   for (long long base = warp_id * 4; base < rows; base += warps * 4) {
-    const long long row = base + group;
+    const long long bih = base + group;  // (b * n + i) * Hq + h
     float acc = 0.f;
-    if (row < rows) {
+    int h = 0, i = 0, b = 0;
+    SeqRows sr{};
+    bool live = false;
+    long long row = 0;
+    if (bih < rows) {
+      h = static_cast<int>(bih % Hq);
+      i = static_cast<int>((bih / Hq) % n);
+      b = static_cast<int>(bih / (static_cast<long long>(Hq) * n));
+      sr = seq_rows(cu, ntok, n, b);
+      live = i < sr.len;
+      row = (static_cast<long long>(sr.g0) + i) * Hq + h;
+    }
+    if (live) {
       for (int c = lane8 * 8; c < d; c += 64) {
         if (kF32) {
           const float4* o =
@@ -317,14 +361,12 @@ __global__ void bwd_vec_kernel(const void* __restrict__ ov, const void* __restri
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    if (lane8 == 0 && row < rows) {
-      const int h = static_cast<int>(row % Hq);
-      const long long bi = row / Hq;
-      const int i = static_cast<int>(bi % n);
-      const int b = static_cast<int>(bi / n);
+    if (lane8 == 0 && bih < rows) {
       const long long bh = static_cast<long long>(b) * Hq + h;
-      nDvec[bh * npad + i] = -acc;
-      nlse2[bh * npad + i] = __ldg(lse + bh * n + i) * -1.4426950408889634f;
+      nDvec[bh * npad + i] = live ? -acc : 0.f;
+      nlse2[bh * npad + i] =
+          live ? __ldg(lse + lse_index(cu, ntok, n, Hq, b, h, sr, i)) * -1.4426950408889634f
+               : -INFINITY;
     }
   }
   const long long pad_rows = static_cast<long long>(B) * Hq * (npad - n);
@@ -370,15 +412,16 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
                               const __nv_bfloat16* dout, const float* lse, float* nDvec,
-                              float* nlse2, int npad, cudaStream_t st) {
+                              float* nlse2, int npad, const int* cu, int total, cudaStream_t st) {
   const int span = o ? max(n, npad) : n;
   // positions per CTA: enough CTAs for about eight per SM, at most kPrepPos
   const int ppc = max(1, min(kPrepPos, (span + 152 * 8 - 1) / (152 * 8)));
   const int grid = (span + ppc - 1) / ppc;
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(o ? "bwd_prep" : "fwd_prep", st);
-  train_prep_kernel<<<grid, kThreads, 0, st>>>(q, k, qr, kr, table, f, p, B, n, Hq, Hkv, d, o,
-                                                dout, lse, nDvec, nlse2, npad, ppc);
+  auto* kern = cu ? train_prep_kernel<true> : train_prep_kernel<false>;
+  kern<<<grid, kThreads, 0, st>>>(q, k, qr, kr, table, f, p, B, n, Hq, Hkv, d, o, dout, lse, nDvec,
+                                  nlse2, npad, ppc, cu, total, device_status_ptr());
   return cudaGetLastError();
 }
 
@@ -392,30 +435,33 @@ cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const Ro
 }
 
 cudaError_t launch_rope_rows(const void* x, bool x_f32, __nv_bfloat16* out, const float2* table,
-                             int B, int n, int H, int d, bool rotate, cudaStream_t st) {
+                             int B, int n, int H, int d, bool rotate, const int* cu, int total,
+                             cudaStream_t st) {
   const long long work = static_cast<long long>(B) * n * H * (d / 16);
   if (work <= 0) return cudaSuccess;
   TraceScope tr(rotate ? "rope_rows" : "to_bf16", st);
   if (x_f32)
     rope_rows_kernel<true><<<grid_for(work), kThreads, 0, st>>>(x, out, table, B, n, H, d,
-                                                                rotate ? 1 : 0);
+                                                                rotate ? 1 : 0, cu, total);
   else
     rope_rows_kernel<false><<<grid_for(work), kThreads, 0, st>>>(x, out, table, B, n, H, d,
-                                                                 rotate ? 1 : 0);
+                                                                 rotate ? 1 : 0, cu, total);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_vec(const void* o, const void* dout, bool f32, const float* lse,
                            float* nDvec, float* nlse2, int B, int n, int npad, int Hq, int d,
-                           cudaStream_t st) {
+                           const int* cu, int total, cudaStream_t st) {
   const long long rows = static_cast<long long>(B) * n * Hq;
   if (rows <= 0 || npad < n) return cudaSuccess;
   const int grid = grid_for(rows * 8);  // 8 threads per row
   TraceScope tr("bwd_vec", st);
   if (f32)
-    bwd_vec_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, lse, nDvec, nlse2, B, n, npad, Hq, d);
+    bwd_vec_kernel<true><<<grid, kThreads, 0, st>>>(o, dout, lse, nDvec, nlse2, B, n, npad, Hq, d,
+                                                    cu, total);
   else
-    bwd_vec_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, lse, nDvec, nlse2, B, n, npad, Hq, d);
+    bwd_vec_kernel<false><<<grid, kThreads, 0, st>>>(o, dout, lse, nDvec, nlse2, B, n, npad, Hq, d,
+                                                     cu, total);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,7 @@ enum : uint32_t {
   kDevErrTimeoutEpilogue = 1u << 3,
   kDevErrBadSchedule = 1u << 4,
   kDevErrSmemLayout = 1u << 5,  // dynamic shared memory not 1024-byte aligned
+  kDevErrSegments = 1u << 6,    // a packed segment table breaks its rules
 };
 
 // Longest legitimate wait inside one kernel is microseconds; give up after

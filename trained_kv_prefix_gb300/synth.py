@@ -128,6 +128,33 @@ def train_inputs(s: TrainShape, seed: int | None = None) -> dict:
     return dict(q=q, k=k, v=v, kc=kc, vc=vc, do=do)
 
 
+def packed_lengths(n_max: int, segments: int, seed: int) -> np.ndarray:
+    """Segment lengths of a packed group: conversations of uneven length,
+    ``U{1..n_max}`` (the longest set to n_max, so the grid bound is met)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, n_max + 1, size=segments)
+    lens[int(rng.integers(0, segments))] = n_max
+    return lens.astype(np.int32)
+
+
+def packed_inputs(s: TrainShape, lens, seed: int | None = None) -> dict:
+    """Packed segments of the given lengths (the shape's B and n are not
+    used): Q, dO ``[T, Hq, d]``, K, V ``[T, Hkv, d]``, cartridge ``[p, Hkv,
+    d]``, the int32 table ``cu_seqlens [S + 1]`` and ``max_seqlen``; values
+    drawn as in :func:`train_inputs`."""
+    lens = np.asarray(lens, dtype=np.int64)
+    T = int(lens.sum())
+    rng = np.random.default_rng(s.seed if seed is None else seed)
+    q = _draw(rng, (T, s.Hq, s.d), s.qkv_std, s.dtype)
+    k = _draw(rng, (T, s.Hkv, s.d), s.qkv_std, s.dtype)
+    v = _draw(rng, (T, s.Hkv, s.d), s.qkv_std, s.dtype)
+    kc = _draw(rng, (s.p, s.Hkv, s.d), s.qkv_std, s.cart_dtype)
+    vc = _draw(rng, (s.p, s.Hkv, s.d), s.qkv_std, s.cart_dtype)
+    do = _draw(rng, (T, s.Hq, s.d), s.do_std, s.dtype)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    return dict(q=q, k=k, v=v, kc=kc, vc=vc, do=do, cu=cu, max_seqlen=int(lens.max(initial=1)))
+
+
 def token_kv(total: int, Hkv: int, d: int, seed: int, std: float = 1.0):
     """Raw (un-rotated) per-token K and V for a sequence of ``total`` tokens,
     ``[total, Hkv, d]`` fp64 numpy arrays, plus queries for the same tokens at
