@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--workload", choices=("selfstudy", "longctx"), default="selfstudy")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--ext-steps", type=int, default=20,
+                    help="timed steps of the packed-training and span-decode lines (0: skip)")
     return ap.parse_args()
 
 
@@ -268,6 +270,90 @@ def reference_arm(args, ts):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def measure_extensions(args, ts, ds, dev, rank, peaks, flush):
+    """The packed-segment training step and the span-verify decode step,
+    each timed alone (CUDA events on the launch stream, L2 flushed outside
+    the events between steps).  Packed: ts's heads and cartridge, 8
+    segments of U{1..n} tokens (the longest n); work = 3.5 x 4d x Hq x the
+    visible pairs of every segment.  Span: the serving decode workload with
+    4 new tokens per conversation; bytes = the shared cartridge once + every
+    conversation's private rows 0..L+3 (K and V) + q/k/v/o of the span."""
+    import numpy as np
+    import torch
+    from trained_kv_prefix_gb300 import cartattn, synth
+
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, steps):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize(dev)
+        tot = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot / steps  # ms
+
+    out = {}
+    segs = 8
+    lens = synth.packed_lengths(ts.n, segs, seed=ts.seed + 1000 * rank)
+    pin = synth.packed_inputs(ts, lens, seed=ts.seed + 1000 * rank)
+    g = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in pin.items()}
+    kcb = g["kc"].to(torch.bfloat16)
+    vcb = g["vc"].to(torch.bfloat16)
+    n = g["max_seqlen"]
+    o, lse = cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], kcb, vcb, g["cu"], n,
+                                           frozen_prefix=ts.frozen_prefix, theta=ts.theta)
+
+    def packed_step():
+        cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], kcb, vcb, g["cu"], n,
+                                      frozen_prefix=ts.frozen_prefix, theta=ts.theta, o=o, lse=lse)
+        cartattn.cart_attn_bwd_packed(g["q"], g["k"], g["v"], kcb, vcb, o, lse, g["do"], g["cu"], n,
+                                      frozen_prefix=ts.frozen_prefix, theta=ts.theta)
+
+    L = lens.astype(np.float64)
+    flops = 3.5 * 4.0 * ts.d * ts.Hq * float((L * ts.p + L * (L + 1) / 2).sum())
+    ms = timed(packed_step, args.ext_steps)
+    tf = flops / (ms * 1e-3) / 1e12
+    out["packed_train"] = {
+        "metric": "packed-segment fwd+bwd TFLOP/s", "value": tf, "unit": "TFLOP/s",
+        "frac": tf / peaks["bf16_tflops"], "ms_per_step": ms,
+        "config": {"segments": segs, "tokens": int(L.sum()), "max_seqlen": n,
+                   "lengths": [int(x) for x in lens], "Hq": ts.Hq, "Hkv": ts.Hkv, "d": ts.d,
+                   "cartridge_rows": ts.p}}
+    span = 4
+    din = {k: v.to(dev) for k, v in synth.decode_span_inputs(ds, span, seed=ds.seed + 1000 * rank).items()}
+    ws = torch.empty(cartattn.decode_span_workspace_size(ds.B, span, ds.Hq, ds.Hkv, ds.d, ds.p,
+                                                         ds.cache_rows), dtype=torch.uint8,
+                     device=dev)
+    od = torch.empty_like(din["q"])
+
+    def span_step():
+        cartattn.cart_attn_decode_span(din["q"], din["k_new"], din["v_new"], din["kc"], din["vc"],
+                                       din["k_cache"], din["v_cache"], din["lens"], theta=ds.theta,
+                                       o=od, workspace=ws)
+
+    ms = timed(span_step, args.ext_steps)
+    Ls = din["lens"].cpu().numpy().astype(np.int64)
+    row = ds.Hkv * ds.d * 2
+    byts = 2 * ds.p * row + int((Ls + span).sum()) * 2 * row + ds.B * span * (
+        2 * ds.Hq * ds.d * 2 + 2 * row + 2 * row)
+    out["span_decode"] = {
+        "metric": "span-verify decode HBM GB/s", "value": byts / (ms * 1e-3) / 1e9, "unit": "GB/s",
+        "frac": byts / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "ms_per_step": ms,
+        "tokens_per_s": ds.B * span / (ms * 1e-3),
+        "config": {"conversations": ds.B, "span": span, "cartridge_rows": ds.p,
+                   "bytes_per_step": byts}}
+    assert cartattn.device_status() == 0
+    return out
 
 
 def workload_name(ts):
@@ -495,6 +581,8 @@ def main():
                    "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in dhost.values()),
                    "d2h_bytes_per_step": od_h.numel() * od_h.element_size()}
 
+    ext = measure_extensions(args, ts, ds, dev, rank, peaks, flush) if args.ext_steps > 0 else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(ts)
@@ -516,6 +604,7 @@ def main():
                        "value": dec_gbs, "unit": "GB/s", "bytes_per_step": dbytes,
                        "frac": dec_gbs / world / peaks["hbm_gbs"],
                        "roofline": roofline_for(dec_dom) if dec_dom else None, "e2e": dec_e2e},
+            "extensions": ext,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,
             "clocks": clk.summary(), "kernels": kernels, "device_status": status,
         }
