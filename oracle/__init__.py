@@ -47,7 +47,7 @@ class _Geom(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("n", ctypes.c_int), ("Hq", ctypes.c_int),
                 ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("p", ctypes.c_int),
                 ("frozen_prefix", ctypes.c_int), ("scale", ctypes.c_double),
-                ("theta", ctypes.c_double)]
+                ("theta", ctypes.c_double), ("window", ctypes.c_int)]
 
 
 _D = ctypes.POINTER(ctypes.c_double)
@@ -66,7 +66,8 @@ def lib():
             L.cart_oracle_decode.restype = ctypes.c_int
             L.cart_oracle_decode.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_double] * 2
                                              + [_D] * 7 + [ctypes.c_int,
-                                                           ctypes.POINTER(ctypes.c_int), _D])
+                                                           ctypes.POINTER(ctypes.c_int), _D,
+                                                           ctypes.c_int])
             L.cart_oracle_rope.restype = None
             L.cart_oracle_rope.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_double, ctypes.c_double, ctypes.c_int]
@@ -92,18 +93,21 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(_D)
 
 
-def _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta) -> _Geom:
-    return _Geom(B, n, Hq, Hkv, d, p, frozen_prefix, float(scale), float(theta))
+def _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta, window=0) -> _Geom:
+    return _Geom(B, n, Hq, Hkv, d, p, frozen_prefix, float(scale), float(theta), int(window))
 
 
 def fwd(q, k, v, kc, vc, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
-        heads=None, rows=None):
+        heads=None, rows=None, window=0):
     """Forward of cartridge attention.
 
     q ``[B, n, Hq, d]``, k/v ``[B, n, Hkv, d]``, kc/vc ``[p, Hkv, d]`` (any
     float arrays; read as fp64).  Returns ``(o [B, n, Hq, d], lse [B, Hq, n])``.
     ``heads=(lo, hi)`` / ``rows=(lo, hi)`` restrict which outputs are computed
-    (the rest are NaN)."""
+    (the rest are NaN).  ``window`` W > 0 is a sliding window (Cartridges
+    guide, "gemma4 (measured)": a cartridge is visible to a local-SWA query
+    exactly as a real prefix, within the window): the query at position P
+    sees keys at positions P - W + 1 .. P, cartridge row j at position j."""
     q, k, v, kc, vc = (_f64(t) for t in (q, k, v, kc, vc))
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
@@ -119,7 +123,7 @@ def fwd(q, k, v, kc, vc, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
     h_lo, h_hi = heads if heads is not None else (0, Hq)
     i_lo, i_hi = rows if rows is not None else (0, n)
     # the forward does not depend on which rows are frozen
-    g = _geom(B, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta)
+    g = _geom(B, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta, window)
     rc = lib().cart_oracle_fwd(ctypes.byref(g), _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
                                _ptr(vc), _ptr(o), _ptr(lse), h_lo, h_hi, i_lo, i_hi)
     if rc != 0:
@@ -128,7 +132,7 @@ def fwd(q, k, v, kc, vc, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
 
 
 def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0e6,
-        kv_heads=None, rows=None, frozen_rows=()):
+        kv_heads=None, rows=None, frozen_rows=(), window=0):
     """Gradients of ``sum(dout * o)``: returns ``dq, dk, dv, dkc, dvc`` (fp64),
     dkc/dvc summed over the batch with rows ``< frozen_prefix`` exactly 0.
     ``frozen_rows`` lists further frozen cartridge rows (a composed
@@ -156,7 +160,7 @@ def bwd(q, k, v, kc, vc, dout, *, p=None, frozen_prefix=1, scale=None, theta=1.0
     dvc = np.full((pc, Hkv, d), np.nan)
     lo, hi = kv_heads if kv_heads is not None else (0, Hkv)
     i_lo, i_hi = rows if rows is not None else (0, n)
-    g = _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta)
+    g = _geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta, window)
     rc = lib().cart_oracle_bwd(ctypes.byref(g), _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
                                _ptr(vc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                                _ptr(dkc), _ptr(dvc), lo, hi, i_lo, i_hi)
@@ -178,7 +182,7 @@ def _segments(cu_seqlens, total):
 
 
 def fwd_packed(q, k, v, kc, vc, cu_seqlens, *, p=None, frozen_prefix=1, scale=None,
-               theta=1.0e6):
+               theta=1.0e6, window=0):
     """Packed segments (Cartridges guide, "Deliberate divergences from the
     reference", packing bullet; "Batched self-study (measured)", packed
     training step): the group's sequences lie back to back along ONE token
@@ -195,14 +199,14 @@ def fwd_packed(q, k, v, kc, vc, cu_seqlens, *, p=None, frozen_prefix=1, scale=No
         if b == a:
             continue
         o_s, lse_s = fwd(q[None, a:b], k[None, a:b], v[None, a:b], kc, vc, p=p,
-                         frozen_prefix=frozen_prefix, scale=scale, theta=theta)
+                         frozen_prefix=frozen_prefix, scale=scale, theta=theta, window=window)
         o[a:b] = o_s[0]
         lse[:, a:b] = lse_s[0]
     return o, lse
 
 
 def bwd_packed(q, k, v, kc, vc, dout, cu_seqlens, *, p=None, frozen_prefix=1, scale=None,
-               theta=1.0e6, frozen_rows=()):
+               theta=1.0e6, frozen_rows=(), window=0):
     """Gradients of ``sum(dout * o)`` for packed segments (layouts of
     ``fwd_packed``): each segment's dq/dk/dv are those of its own
     single-sequence problem, and the cartridge gradient is their sum over
@@ -217,14 +221,16 @@ def bwd_packed(q, k, v, kc, vc, dout, cu_seqlens, *, p=None, frozen_prefix=1, sc
         if b == a:
             continue
         g = bwd(q[None, a:b], k[None, a:b], v[None, a:b], kc, vc, dout[None, a:b], p=p,
-                frozen_prefix=frozen_prefix, scale=scale, theta=theta, frozen_rows=frozen_rows)
+                frozen_prefix=frozen_prefix, scale=scale, theta=theta, frozen_rows=frozen_rows,
+                window=window)
         dq[a:b], dk[a:b], dv[a:b] = g[0][0], g[1][0], g[2][0]
         dkc += g[3]
         dvc += g[4]
     return dq, dk, dv, dkc, dvc
 
 
-def decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6):
+def decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6,
+           window=0):
     """One decode step behind a shared cartridge.  Returns
     ``(o [B, Hq, d], k_cache', v_cache')`` where the caches have the new
     token's rotated key / value written at row ``lens[b]``."""
@@ -245,13 +251,15 @@ def decode(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta
     rc = lib().cart_oracle_decode(B, Hq, Hkv, d, p, float(scale), float(theta), _ptr(q),
                                   _ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), _ptr(kcache),
                                   _ptr(vcache), rows,
-                                  lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _ptr(o))
+                                  lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _ptr(o),
+                                  int(window))
     if rc != 0:
         raise ValueError(f"cart_oracle_decode failed ({rc})")
     return o, kcache, vcache
 
 
-def decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6):
+def decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, theta=1.0e6,
+                window=0):
     """Span verify (Cartridges guide, "Batched self-study (measured)", the
     --spec-b bullet): ``span`` new tokens per conversation in one step
     (q ``[B, span, Hq, d]``, k_new / v_new ``[B, span, Hkv, d]``).  Token t
@@ -267,7 +275,8 @@ def decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None, 
     o = np.empty(q.shape)
     for t in range(span):
         o[:, t], kcache, vcache = decode(q[:, t], k_new[:, t], v_new[:, t], kc, vc, kcache,
-                                         vcache, lens + t, scale=scale, theta=theta)
+                                         vcache, lens + t, scale=scale, theta=theta,
+                                         window=window)
     return o, kcache, vcache
 
 

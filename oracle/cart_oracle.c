@@ -31,6 +31,12 @@
  *   - Decode: the private cache holds L_b already-rotated rows at positions
  *     p..p+L_b-1; the new token sits at position p+L_b, its key is rotated and
  *     appended at private row L_b, and it attends to p + L_b + 1 keys.
+ *   - Sliding window (Cartridges guide, "gemma4 (measured)": on a local-SWA
+ *     layer a served cartridge is visible exactly as a real prefix, within
+ *     the window, so the window may cut through the cartridge): with
+ *     window W > 0 a query at position P sees the keys at positions
+ *     P - W + 1 .. P (W keys counting itself); cartridge row j sits at
+ *     position j, so the sink gets no exemption.  W = 0: no window.
  *
  * Layouts (row-major, innermost last):
  *   q, o, dout, dq   [B, n, Hq, d]
@@ -54,7 +60,14 @@
 typedef struct {
     int B, n, Hq, Hkv, d, p, frozen_prefix;
     double scale, theta;
+    int window; /* sliding window in keys (0: none) */
 } cart_ogeom;
+
+/* First visible key (= key position) of the query at position pos. */
+static int first_key(int pos, int window) {
+    int lo = window > 0 ? pos - window + 1 : 0;
+    return lo > 0 ? lo : 0;
+}
 
 /* ---- RoPE (rotate-half) --------------------------------------------------- */
 
@@ -87,6 +100,7 @@ static int geom_ok(const cart_ogeom* g) {
     if (g->Hq % g->Hkv) return 0;
     if (g->p < 0 || g->frozen_prefix < 0 || g->frozen_prefix > g->p) return 0;
     if (g->p + g->n < 1) return 0;
+    if (g->window < 0) return 0;
     return 1;
 }
 
@@ -136,21 +150,24 @@ int cart_oracle_fwd(const cart_ogeom* g, const double* q, const double* k,
         for (int i = i_lo; i < i_hi; ++i) {
             const double* qi = q + (((size_t)b * n + i) * Hq + h) * d;
             rope_vec(qi, qt, d, (double)(p + i), g->theta, 0);
-            /* end-aligned causal mask: key j is visible iff j <= i + (kv - n) */
+            /* end-aligned causal mask: key j is visible iff j <= i + (kv - n)
+             * (key j sits at position j, query i at p + i = i + (kv - n)),
+             * and within the window: j >= p + i - W + 1 */
             int nvis = i + (kv - n) + 1;
+            int j0 = first_key(p + i, g->window);
             double m = -INFINITY;
-            for (int j = 0; j < nvis; ++j) {
+            for (int j = j0; j < nvis; ++j) {
                 double acc = 0.0;
                 for (int c = 0; c < d; ++c) acc += qt[c] * kt[(size_t)j * d + c];
                 s[j] = g->scale * acc;
                 if (s[j] > m) m = s[j];
             }
             double l = 0.0;
-            for (int j = 0; j < nvis; ++j) { s[j] = exp(s[j] - m); l += s[j]; }
+            for (int j = j0; j < nvis; ++j) { s[j] = exp(s[j] - m); l += s[j]; }
             /* o_i = sum_j softmax_j * v_j */
             double* oi = o + (((size_t)b * n + i) * Hq + h) * d;
             for (int c = 0; c < d; ++c) oi[c] = 0.0;
-            for (int j = 0; j < nvis; ++j) {
+            for (int j = j0; j < nvis; ++j) {
                 double w = s[j] / l;
                 for (int c = 0; c < d; ++c) oi[c] += w * vt[(size_t)j * d + c];
             }
@@ -204,28 +221,29 @@ int cart_oracle_bwd(const cart_ogeom* g, const double* q, const double* k,
                 const double* gi = dout + (((size_t)b * n + i) * Hq + h) * d;
                 rope_vec(qi, qt, d, (double)(p + i), g->theta, 0);
                 int nvis = i + (kv - n) + 1;
+                int j0 = first_key(p + i, g->window);
                 /* attention weights a_j = softmax_j(scale * qt . kt_j) */
                 double m = -INFINITY;
-                for (int j = 0; j < nvis; ++j) {
+                for (int j = j0; j < nvis; ++j) {
                     double acc = 0.0;
                     for (int c = 0; c < d; ++c) acc += qt[c] * kt[(size_t)j * d + c];
                     a[j] = g->scale * acc;
                     if (a[j] > m) m = a[j];
                 }
                 double l = 0.0;
-                for (int j = 0; j < nvis; ++j) { a[j] = exp(a[j] - m); l += a[j]; }
-                for (int j = 0; j < nvis; ++j) a[j] /= l;
+                for (int j = j0; j < nvis; ++j) { a[j] = exp(a[j] - m); l += a[j]; }
+                for (int j = j0; j < nvis; ++j) a[j] /= l;
                 /* d(loss)/d(a_j) = dout . vt_j ; softmax Jacobian:
                  * d(loss)/d(s_j) = a_j (dp_j - sum_k a_k dp_k) */
                 double Dsum = 0.0;
-                for (int j = 0; j < nvis; ++j) {
+                for (int j = j0; j < nvis; ++j) {
                     double acc = 0.0;
                     for (int c = 0; c < d; ++c) acc += gi[c] * vt[(size_t)j * d + c];
                     dp[j] = acc;
                     Dsum += a[j] * acc;
                 }
                 for (int c = 0; c < d; ++c) dqt[c] = 0.0;
-                for (int j = 0; j < nvis; ++j) {
+                for (int j = j0; j < nvis; ++j) {
                     double ds = a[j] * (dp[j] - Dsum);
                     for (int c = 0; c < d; ++c) {
                         dqt[c] += g->scale * ds * kt[(size_t)j * d + c];
@@ -278,8 +296,9 @@ int cart_oracle_bwd(const cart_ogeom* g, const double* q, const double* k,
 int cart_oracle_decode(int B, int Hq, int Hkv, int d, int p, double scale, double theta,
                        const double* q, const double* k_new, const double* v_new,
                        const double* kc, const double* vc, double* k_cache,
-                       double* v_cache, int rows, const int* len, double* o) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 2 || (d & 1) || p < 0 || rows < 1)
+                       double* v_cache, int rows, const int* len, double* o, int window) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 2 || (d & 1) || p < 0 || rows < 1 ||
+        window < 0)
         return -1;
     for (int b = 0; b < B; ++b)
         if (len[b] < 0 || len[b] >= rows) return -1;
@@ -297,12 +316,13 @@ int cart_oracle_decode(int B, int Hq, int Hkv, int d, int p, double scale, doubl
     for (int t = 0; t < B * Hq; ++t) {
         int b = t / Hq, h = t % Hq, kh = h / G;
         int nkey = p + len[b] + 1;
+        int j0 = first_key(p + len[b], window); /* keys j0 .. p + len[b] */
         double* qt = (double*)malloc(sizeof(double) * d);
         double* s = (double*)malloc(sizeof(double) * (size_t)nkey);
         if (!qt || !s) { failed = 1; free(qt); free(s); continue; }
         rope_vec(q + ((size_t)b * Hq + h) * d, qt, d, (double)(p + len[b]), theta, 0);
         double m = -INFINITY;
-        for (int j = 0; j < nkey; ++j) {
+        for (int j = j0; j < nkey; ++j) {
             const double* kj = j < p ? kc + ((size_t)j * Hkv + kh) * d
                                      : k_cache + (((size_t)b * rows + (j - p)) * Hkv + kh) * d;
             double acc = 0.0;
@@ -311,10 +331,10 @@ int cart_oracle_decode(int B, int Hq, int Hkv, int d, int p, double scale, doubl
             if (s[j] > m) m = s[j];
         }
         double l = 0.0;
-        for (int j = 0; j < nkey; ++j) l += exp(s[j] - m);
+        for (int j = j0; j < nkey; ++j) l += exp(s[j] - m);
         double* ob = o + ((size_t)b * Hq + h) * d;
         for (int c = 0; c < d; ++c) ob[c] = 0.0;
-        for (int j = 0; j < nkey; ++j) {
+        for (int j = j0; j < nkey; ++j) {
             const double* vj = j < p ? vc + ((size_t)j * Hkv + kh) * d
                                      : v_cache + (((size_t)b * rows + (j - p)) * Hkv + kh) * d;
             double w = exp(s[j] - m) / l;

@@ -485,3 +485,72 @@ def test_packed_rejects_bad_segment_tables():
     for cu in ((0, 7), (1, 6), (0, 4, 2, 6), (0,)):
         with pytest.raises(ValueError):
             oracle.fwd_packed(P["q"][0], P["k"][0], P["v"][0], P["kc"], P["vc"], cu)
+
+
+@pytest.mark.parametrize("window", [1, 3, 8, 13, 40])
+def test_window_matches_masked_sdpa(window):
+    """Sliding window (the W most recent keys, counting itself; cartridge row
+    j at position j): forward, lse and every gradient against masked SDPA
+    with autograd.  p = 9, n = 7: W = 1 sees only itself, W = 3 / 8 cut
+    through the cartridge (the sink among the cut rows), W = 13 cuts it for
+    the late queries only, W = 40 cuts nothing."""
+    B, n, Hq, Hkv, d, p = 2, 7, 4, 2, 8, 9
+    P = _problem(80 + window, B, n, Hq, Hkv, d, p)
+    o, lse = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], window=window)
+    o_t, lse_t = tf.cartridge_attention(_t(P["q"]), _t(P["k"]), _t(P["v"]), _t(P["kc"]),
+                                        _t(P["vc"]), window=window)
+    np.testing.assert_allclose(o, o_t.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.permute(0, 1, 2).numpy(), rtol=0, atol=1e-12)
+    g = oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"], window=window)
+    g_t = tf.cartridge_grads(_t(P["q"]), _t(P["k"]), _t(P["v"]), _t(P["kc"]), _t(P["vc"]),
+                             _t(P["do"]), window=window)
+    for a, b in zip(g, g_t):
+        np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-11)
+    if window <= 3:
+        # rows that no query's window reaches get no gradient at all
+        far = p + 0 - window  # query 0 at position p reaches back to p - W + 1
+        assert (g[3][1:max(far + 1, 1)] == 0).all() and (g[4][1:max(far + 1, 1)] == 0).all()
+
+
+def test_window_wider_than_the_sequence_is_no_window():
+    B, n, Hq, Hkv, d, p = 2, 6, 4, 2, 8, 5
+    P = _problem(90, B, n, Hq, Hkv, d, p)
+    a = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], window=p + n)
+    b = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"])
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    ga = oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"], window=p + n)
+    gb = oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"])
+    for x, y in zip(ga, gb):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("window", [1, 4, 11])
+def test_windowed_decode_span_is_rows_of_windowed_forward(window):
+    """Serving parity under a sliding window: the span's queries equal rows
+    len .. len + span - 1 of the windowed training forward."""
+    B, Hq, Hkv, d, p, span = 3, 4, 2, 16, 9, 2
+    lens = np.array([0, 5, 2], dtype=np.int32)
+    rows = 8
+    rng = np.random.default_rng(52 + window)
+    kc = rng.standard_normal((p, Hkv, d)) * 0.5
+    vc = rng.standard_normal((p, Hkv, d)) * 0.5
+    kraw = rng.standard_normal((B, rows, Hkv, d)) * 0.5
+    vraw = rng.standard_normal((B, rows, Hkv, d)) * 0.5
+    q = rng.standard_normal((B, span, Hq, d)) * 0.5
+    k_cache = np.full((B, rows, Hkv, d), 7.0)
+    v_cache = np.full((B, rows, Hkv, d), 7.0)
+    for b in range(B):
+        L = lens[b]
+        k_cache[b, :L] = oracle.rope(kraw[b, :L], p)
+        v_cache[b, :L] = vraw[b, :L]
+    k_new = np.stack([kraw[b, lens[b]:lens[b] + span] for b in range(B)])
+    v_new = np.stack([vraw[b, lens[b]:lens[b] + span] for b in range(B)])
+    o, _, _ = oracle.decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, window=window)
+    for b in range(B):
+        L = int(lens[b])
+        qs = np.zeros((1, L + span, Hq, d))
+        qs[0, L:] = q[b]
+        of, _ = oracle.fwd(qs, kraw[None, b, :L + span], vraw[None, b, :L + span], kc, vc,
+                           rows=(L, L + span), window=window)
+        np.testing.assert_allclose(o[b], of[0, L:], rtol=0, atol=1e-13)

@@ -30,13 +30,18 @@ def rope_complex(x: torch.Tensor, pos: torch.Tensor, theta: float) -> torch.Tens
     return torch.cat([z.real, z.imag], dim=-1)
 
 
-def end_aligned_mask(q_seq: int, kv_seq: int) -> torch.Tensor:
+def end_aligned_mask(q_seq: int, kv_seq: int, window: int = 0) -> torch.Tensor:
+    """Key j visible from query i; with a sliding window W > 0 also
+    i + (kv_seq - q_seq) - j < W (the W most recent keys, counting itself)."""
     i = torch.arange(q_seq)[:, None]
     j = torch.arange(kv_seq)[None, :]
-    return j <= i + (kv_seq - q_seq)
+    vis = j <= i + (kv_seq - q_seq)
+    if window > 0:
+        vis = vis & (i + (kv_seq - q_seq) - j < window)
+    return vis
 
 
-def cartridge_attention(q, k, v, kc, vc, *, theta=1.0e6, scale=None):
+def cartridge_attention(q, k, v, kc, vc, *, theta=1.0e6, scale=None, window=0):
     """All inputs torch fp64 in the oracle's layouts:
     q ``[B, n, Hq, d]``, k/v ``[B, n, Hkv, d]``, kc/vc ``[p, Hkv, d]``.
     Returns (o ``[B, n, Hq, d]``, lse ``[B, Hq, n]``)."""
@@ -54,14 +59,15 @@ def cartridge_attention(q, k, v, kc, vc, *, theta=1.0e6, scale=None):
     vcb = vc.permute(1, 0, 2).unsqueeze(0).expand(B, Hkv, p, d)
     K = torch.cat([kcb, kh], dim=2).repeat_interleave(G, dim=1)       # [B, Hq, kv, d]
     V = torch.cat([vcb, vh], dim=2).repeat_interleave(G, dim=1)
-    mask = end_aligned_mask(n, p + n)
+    mask = end_aligned_mask(n, p + n, window)
     o = F.scaled_dot_product_attention(qh, K, V, attn_mask=mask, scale=scale)
     logits = torch.matmul(qh, K.transpose(-1, -2)) * scale
     lse = torch.logsumexp(logits.masked_fill(~mask, float("-inf")), dim=-1)
     return o.permute(0, 2, 1, 3), lse
 
 
-def cartridge_grads(q, k, v, kc, vc, dout, *, frozen_prefix=1, theta=1.0e6, scale=None):
+def cartridge_grads(q, k, v, kc, vc, dout, *, frozen_prefix=1, theta=1.0e6, scale=None,
+                    window=0):
     """Autograd gradients of sum(dout * o).  Frozen rows are held constant (the
     sink rows are not leaves), so their gradient is reported as exactly 0."""
     q = q.clone().requires_grad_(True)
@@ -71,7 +77,7 @@ def cartridge_grads(q, k, v, kc, vc, dout, *, frozen_prefix=1, theta=1.0e6, scal
     vt = vc[frozen_prefix:].clone().requires_grad_(True)
     kcat = torch.cat([kc[:frozen_prefix], kt], dim=0)
     vcat = torch.cat([vc[:frozen_prefix], vt], dim=0)
-    o, _ = cartridge_attention(q, k, v, kcat, vcat, theta=theta, scale=scale)
+    o, _ = cartridge_attention(q, k, v, kcat, vcat, theta=theta, scale=scale, window=window)
     (o * dout).sum().backward()
     dkc = torch.zeros_like(kc)
     dvc = torch.zeros_like(vc)
