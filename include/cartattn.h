@@ -67,11 +67,18 @@ typedef enum cart_dtype { CART_BF16 = 0, CART_F32 = 1 } cart_dtype;
  *   p      cartridge rows INCLUDING the frozen sink rows (p >= 0)
  *   frozen_prefix  leading cartridge rows whose gradient is exactly 0
  *   scale  softmax scale (normally 1/sqrt(d)); finite and > 0
- *   rope_theta     RoPE base (1e6 for the Qwen3 family)            */
+ *   rope_theta     RoPE base (1e6 for the Qwen3 family)
+ *   window sliding window in keys, 0 = none: the query at position P sees
+ *          the keys at positions P - window + 1 .. P (cartridge row j sits
+ *          at position j, so the window may cut through the cartridge and
+ *          its sink).  (Cartridges guide, "gemma4 (measured)": on a local-SWA
+ *          layer a cartridge is visible exactly as a real prefix, within
+ *          the window.)                                                  */
 typedef struct cart_geom {
   int B, n, Hq, Hkv, d, p, frozen_prefix;
   float scale;
   double rope_theta;
+  int window;
 } cart_geom;
 
 /* ------------------------------------------------------------------------
@@ -233,10 +240,13 @@ CART_API int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale,
  *   0 .. len[b] + t.  Requires 1 <= span <= cache_rows and
  *   (Hq / Hkv) * span <= 32.  Everything else is as in cart_attn_decode,
  *   which equals this call with span == 1.
+ *   window  sliding window in keys (0: none), as in cart_geom: token t
+ *   sees the keys at positions p + len[b] + t - window + 1 .. p + len[b] + t.
  * Workspace: cart_attn_decode_span_workspace_size().                      */
 CART_API size_t cart_attn_decode_span_workspace_size(int B, int span, int Hq, int Hkv, int d,
                                                      int p, int cache_rows);
-CART_API int cart_attn_decode_span(int B, int span, int Hq, int Hkv, int d, int p, float scale,
+CART_API int cart_attn_decode_span(int B, int span, int window, int Hq, int Hkv, int d, int p,
+                                   float scale,
                                    double rope_theta, const void* q, const void* k_new,
                                    const void* v_new, const void* kc, const void* vc,
                                    void* k_cache, void* v_cache, int cache_rows,

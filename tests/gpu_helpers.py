@@ -41,18 +41,19 @@ def to_gpu(d: dict) -> dict:
 
 
 def run_train_gpu(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=None, accumulate=False,
-                  dkc0=None, dvc0=None, frozen_rows=None):
+                  dkc0=None, dvc0=None, frozen_rows=None, window=0):
     fp = s.frozen_prefix if frozen_prefix is None else frozen_prefix
     g = to_gpu(inp)
     o, lse = cartattn.cart_attn_fwd(g["q"], g["k"], g["v"], g["kc"], g["vc"], frozen_prefix=fp,
-                                    theta=s.theta)
+                                    theta=s.theta, window=window)
     out = dict(o=o, lse=lse)
     if bwd:
         dkc = dkc0.clone().cuda() if dkc0 is not None else None
         dvc = dvc0.clone().cuda() if dvc0 is not None else None
         dq, dk, dv, dkc, dvc = cartattn.cart_attn_bwd(
             g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse, g["do"], frozen_prefix=fp,
-            theta=s.theta, accumulate=accumulate, dkc=dkc, dvc=dvc, frozen_rows=frozen_rows)
+            theta=s.theta, accumulate=accumulate, dkc=dkc, dvc=dvc, frozen_rows=frozen_rows,
+            window=window)
         out.update(dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc)
     torch.cuda.synchronize()
     assert cartattn.device_status(clear=True) == 0, "a kernel reported a timeout"
@@ -60,16 +61,16 @@ def run_train_gpu(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=Non
 
 
 def oracle_train(s: synth.TrainShape, inp: dict, *, bwd=True, frozen_prefix=None, heads=None,
-                 rows=None, kv_heads=None, bwd_rows=None, frozen_rows=()):
+                 rows=None, kv_heads=None, bwd_rows=None, frozen_rows=(), window=0):
     fp = s.frozen_prefix if frozen_prefix is None else frozen_prefix
     a = {k: synth.f64(v) for k, v in inp.items()}
     o, lse = oracle.fwd(a["q"], a["k"], a["v"], a["kc"], a["vc"], frozen_prefix=fp,
-                        theta=s.theta, heads=heads, rows=rows)
+                        theta=s.theta, heads=heads, rows=rows, window=window)
     ref = dict(o=o, lse=lse)
     if bwd:
         dq, dk, dv, dkc, dvc = oracle.bwd(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["do"],
                                           frozen_prefix=fp, theta=s.theta, kv_heads=kv_heads,
-                                          rows=bwd_rows, frozen_rows=frozen_rows)
+                                          rows=bwd_rows, frozen_rows=frozen_rows, window=window)
         ref.update(dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc)
     return ref
 

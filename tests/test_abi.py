@@ -104,13 +104,20 @@ def test_calls_validate_before_touching_the_device(lib):
         rc = lib.cart_attn_bwd_parts(ctypes.byref(g), 0, 1, al, al, al, al, al, al, al, al, al,
                                      al, al, al, al, lst, cnt, 0, al, 1 << 30, null)
         assert rc == -1
+    # a negative sliding window
+    gw = cartattn.geom(1, 8, 4, 2, 64, 4, window=-1)
+    rc = lib.cart_attn_fwd(ctypes.byref(gw), 0, 1, al, al, al, al, al, al, al, al, 1 << 30, null)
+    assert rc == -1
+    rc = lib.cart_attn_decode_span(2, 1, -1, 16, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al,
+                                   al, 8, al, al, al, 1 << 30, null)
+    assert rc == -1
     # decode: unsupported group size
     rc = lib.cart_attn_decode(2, 6, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al, al, 8, al, al,
                               al, 1 << 20, null)
     assert rc == -1
     # span decode: span 0, span past the cache, too many query columns
     for span, rows in ((0, 8), (9, 8), (5, 64)):
-        rc = lib.cart_attn_decode_span(2, span, 16, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al,
+        rc = lib.cart_attn_decode_span(2, span, 0, 16, 2, 128, 16, 0.1, 1e6, al, al, al, al, al, al,
                                        al, rows, al, al, al, 1 << 30, null)
         assert rc == -1, (span, rows)
 

@@ -155,6 +155,65 @@ def test_packed_equal_segments_match_the_batch_bitwise():
     np.testing.assert_array_equal(got["dvc"], batch["dvc"])
 
 
+WINDOWS = [
+    # (shape, window): p = 333, n = 300 -> query positions 333..632
+    (_shape("win1", 1, 300, 8, 2, 128, 333, seed=130), 1),          # itself only
+    (_shape("win100", 2, 300, 8, 2, 128, 333, seed=131), 100),      # real keys only
+    (_shape("win450", 1, 300, 8, 2, 128, 333, seed=132), 450),      # cuts the cartridge
+    (_shape("win700_d64", 1, 300, 4, 1, 64, 333, seed=133), 700),   # cuts it for late rows
+    (_shape("win200_ragged", 2, 130, 4, 2, 128, 70, seed=134), 200),  # sink cut for late rows
+]
+
+
+@pytest.mark.parametrize("case", WINDOWS, ids=[c[0].name for c in WINDOWS])
+def test_window_parity(case):
+    """Sliding window over the concatenated sequence (cartridge row j at
+    position j): the window cuts through the cartridge and its sink; rows no
+    query reaches get exactly zero gradient."""
+    s, window = case
+    inp = synth.train_inputs(s)
+    got = gh.run_train_gpu(s, inp, window=window)
+    ref = gh.oracle_train(s, inp, window=window)
+    gh.check_fwd(got, ref)
+    gh.check_grads(got, ref, s.frozen_prefix)
+    unseen = max(0, s.p - window + 1)  # cartridge rows before the first query's window
+    for nme in ("dkc", "dvc"):
+        assert (got[nme][:unseen] == 0.0).all(), nme
+
+
+def test_window_wider_than_the_sequence_is_bitwise_no_window():
+    s = _shape("win_wide", 2, 200, 8, 2, 128, 257, seed=135)
+    inp = synth.train_inputs(s)
+    a = gh.run_train_gpu(s, inp)
+    b = gh.run_train_gpu(s, inp, window=s.p + s.n)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+def test_packed_window_parity():
+    s = _shape("packed_win", 0, 0, 8, 2, 128, 300, seed=136)
+    lens, window = (130, 1, 0, 257, 64), 180
+    inp = synth.packed_inputs(s, lens)
+    g = gh.to_gpu({k: v for k, v in inp.items() if k != "max_seqlen"})
+    o, lse = cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], g["cu"], 257,
+                                           window=window)
+    grads = cartattn.cart_attn_bwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse,
+                                          g["do"], g["cu"], 257, window=window)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    got = {k: synth.f64(v) for k, v in zip(("o", "lse", "dq", "dk", "dv", "dkc", "dvc"),
+                                           (o, lse, *grads))}
+    a = {k: synth.f64(v) for k, v in inp.items() if k not in ("cu", "max_seqlen")}
+    cu = inp["cu"].numpy()
+    ref = dict(zip(("o", "lse"), oracle.fwd_packed(a["q"], a["k"], a["v"], a["kc"], a["vc"], cu,
+                                                   window=window)))
+    ref.update(zip(("dq", "dk", "dv", "dkc", "dvc"),
+                   oracle.bwd_packed(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["do"], cu,
+                                     window=window)))
+    gh.check_fwd(got, ref)
+    gh.check_grads(got, ref, 1)
+
+
 def test_backward_is_deterministic():
     s = _shape("det", 2, 200, 8, 2, 128, 300, seed=111)
     inp = synth.train_inputs(s)
@@ -388,3 +447,33 @@ def test_longctx_workload_sampled():
         lhs = unfrozen["dkc"][:, g].sum(0) + dk_att.sum(0)
         scale = np.abs(unfrozen["dkc"][:, g]).sum(0).max() + np.abs(dk_att).sum(0).max()
         assert np.abs(lhs).max() <= 1e-2 * scale
+
+
+WINDOW_DECODE = [
+    # (case, span, window): windows inside the private rows, cutting the
+    # cartridge, reaching past several 256-row units, one key only
+    (_decode_case("wdec_priv", 3, 8, 2, 128, 300, 600, lens=(0, 255, 599)), 1, 100),
+    (_decode_case("wdec_cart", 4, 4, 2, 128, 400, 300, lens=(0, 17, 200, 300)), 1, 350),
+    (_decode_case("wdec_units", 2, 8, 1, 128, 130, 900, lens=(899, 520)), 1, 700),
+    (_decode_case("wdec_one", 2, 4, 4, 64, 64, 70, lens=(69, 3)), 1, 1),
+    (_decode_case("wdec_span", 3, 8, 2, 128, 300, 600, lens=(0, 250, 595)), 4, 260),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_DECODE, ids=[c[0].name for c in WINDOW_DECODE])
+def test_window_decode_parity(case):
+    s, span, window = case
+    inp = synth.decode_span_inputs(s, span)
+    g = {k: v.cuda() for k, v in inp.items()}
+    o = cartattn.cart_attn_decode_span(g["q"], g["k_new"], g["v_new"], g["kc"], g["vc"],
+                                       g["k_cache"], g["v_cache"], g["lens"], theta=s.theta,
+                                       window=window)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    a = {k: synth.f64(v) for k, v in inp.items() if k != "lens"}
+    o_ref, _, _ = oracle.decode_span(a["q"], a["k_new"], a["v_new"], a["kc"], a["vc"],
+                                     a["k_cache"], a["v_cache"], inp["lens"].numpy(),
+                                     theta=s.theta, window=window)
+    o = synth.f64(o)
+    assert gh.max_abs(o, o_ref) <= gh.FWD_MAXABS, gh.max_abs(o, o_ref)
+    assert gh.rel_l2(o, o_ref) <= gh.FWD_RELL2, gh.rel_l2(o, o_ref)

@@ -39,7 +39,7 @@ class _Geom(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("n", ctypes.c_int), ("Hq", ctypes.c_int),
                 ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("p", ctypes.c_int),
                 ("frozen_prefix", ctypes.c_int), ("scale", ctypes.c_float),
-                ("rope_theta", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("window", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -76,7 +76,7 @@ def lib():
                                            vp, vp, sz, vp]
             L.cart_attn_decode_span_workspace_size.argtypes = [i, i, i, i, i, i, i]
             L.cart_attn_decode_span_workspace_size.restype = sz
-            L.cart_attn_decode_span.argtypes = [i, i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp,
+            L.cart_attn_decode_span.argtypes = [i, i, i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp,
                                                 vp, i, vp, vp, vp, sz, vp]
             L.cart_attn_fwd_packed_workspace_size.argtypes = [G, i, i, i]
             L.cart_attn_fwd_packed_workspace_size.restype = sz
@@ -139,10 +139,12 @@ def _stream(stream, device) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def geom(B, n, Hq, Hkv, d, p, frozen_prefix=1, scale=None, theta=1.0e6) -> _Geom:
+def geom(B, n, Hq, Hkv, d, p, frozen_prefix=1, scale=None, theta=1.0e6, window=0) -> _Geom:
+    """Training geometry; ``window`` > 0 is a sliding window in keys (the
+    query at position P sees keys P - window + 1 .. P), 0 none."""
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    return _Geom(B, n, Hq, Hkv, d, p, frozen_prefix, float(scale), float(theta))
+    return _Geom(B, n, Hq, Hkv, d, p, frozen_prefix, float(scale), float(theta), int(window))
 
 
 def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
@@ -173,14 +175,14 @@ def bwd_workspace_size(g: _Geom, in_dtype: int, cart_dtype: int) -> int:
 
 
 def cart_attn_fwd(q, k, v, kc, vc, *, frozen_prefix=1, scale=None, theta=1.0e6, o=None, lse=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, window=0):
     """Training forward.  q ``[B, n, Hq, d]``, k/v ``[B, n, Hkv, d]`` (not
     rotated), kc/vc ``[p, Hkv, d]`` (bf16 shadow or f32 leaves).  Returns
     ``(o, lse)`` with o like q and lse ``[B, Hq, n]`` f32."""
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
     p = kc.shape[0]
-    g = geom(B, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta)
+    g = geom(B, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta, window)
     dt, cd = _dt(q), _dt(kc)
     if o is None:
         o = torch.empty_like(q)
@@ -196,14 +198,14 @@ def cart_attn_fwd(q, k, v, kc, vc, *, frozen_prefix=1, scale=None, theta=1.0e6, 
 
 def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None, theta=1.0e6,
                   accumulate=False, dq=None, dk=None, dv=None, dkc=None, dvc=None,
-                  workspace=None, stream=None, frozen_rows=None):
+                  workspace=None, stream=None, frozen_rows=None, window=0):
     """Backward.  Returns ``(dq, dk, dv, dkc, dvc)``; dkc/dvc are f32
     ``[p, Hkv, d]`` summed over the batch, rows < frozen_prefix and the rows
     listed in ``frozen_rows`` (a composed cartridge's part sinks) exactly 0."""
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
     p = kc.shape[0]
-    g = geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta)
+    g = geom(B, n, Hq, Hkv, d, p, frozen_prefix, scale, theta, window)
     dt, cd = _dt(q), _dt(kc)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -250,7 +252,8 @@ def _packing(cu_seqlens, max_seqlen, q):
 
 
 def cart_attn_fwd_packed(q, k, v, kc, vc, cu_seqlens, max_seqlen, *, frozen_prefix=1,
-                         scale=None, theta=1.0e6, o=None, lse=None, workspace=None, stream=None):
+                         scale=None, theta=1.0e6, o=None, lse=None, workspace=None, stream=None,
+                         window=0):
     """Training forward on packed segments.  q ``[T, Hq, d]``, k/v
     ``[T, Hkv, d]`` (not rotated), segment s = tokens cu_seqlens[s] ..
     cu_seqlens[s+1]-1 (int32 on the device), none longer than max_seqlen.
@@ -259,7 +262,7 @@ def cart_attn_fwd_packed(q, k, v, kc, vc, cu_seqlens, max_seqlen, *, frozen_pref
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
     p = kc.shape[0]
-    g = geom(S, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta)
+    g = geom(S, n, Hq, Hkv, d, p, min(frozen_prefix, p), scale, theta, window)
     dt, cd = _dt(q), _dt(kc)
     if o is None:
         o = torch.empty_like(q)
@@ -276,7 +279,7 @@ def cart_attn_fwd_packed(q, k, v, kc, vc, cu_seqlens, max_seqlen, *, frozen_pref
 def cart_attn_bwd_packed(q, k, v, kc, vc, o, lse, dout, cu_seqlens, max_seqlen, *,
                          frozen_prefix=1, scale=None, theta=1.0e6, accumulate=False, dq=None,
                          dk=None, dv=None, dkc=None, dvc=None, workspace=None, stream=None,
-                         frozen_rows=()):
+                         frozen_rows=(), window=0):
     """Backward on packed segments (layouts of cart_attn_fwd_packed).
     Returns ``(dq, dk, dv, dkc, dvc)``; dkc/dvc f32 ``[p, Hkv, d]`` summed
     over the segments, frozen rows exactly 0."""
@@ -284,7 +287,7 @@ def cart_attn_bwd_packed(q, k, v, kc, vc, o, lse, dout, cu_seqlens, max_seqlen, 
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
     p = kc.shape[0]
-    g = geom(S, n, Hq, Hkv, d, p, frozen_prefix, scale, theta)
+    g = geom(S, n, Hq, Hkv, d, p, frozen_prefix, scale, theta, window)
     dt, cd = _dt(q), _dt(kc)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -341,7 +344,7 @@ def decode_span_workspace_size(B, span, Hq, Hkv, d, p, rows) -> int:
 
 
 def cart_attn_decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, scale=None,
-                          theta=1.0e6, o=None, workspace=None, stream=None):
+                          theta=1.0e6, o=None, workspace=None, stream=None, window=0):
     """Span verify: ``span`` new tokens per conversation in one step.  q
     ``[B, span, Hq, d]``, k_new/v_new ``[B, span, Hkv, d]`` (bf16, not
     rotated); the caches receive the span's rows lens[b] .. lens[b]+span-1.
@@ -357,7 +360,8 @@ def cart_attn_decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, sc
     if o is None:
         o = torch.empty_like(q)
     ws = _workspace(decode_span_workspace_size(B, span, Hq, Hkv, d, p, rows), q.device, workspace)
-    rc = lib().cart_attn_decode_span(B, span, Hq, Hkv, d, p, float(scale), float(theta), _ptr(q),
+    rc = lib().cart_attn_decode_span(B, span, int(window), Hq, Hkv, d, p, float(scale),
+                                     float(theta), _ptr(q),
                                      _ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc),
                                      _ptr(k_cache), _ptr(v_cache), rows, _ptr(lens), _ptr(o),
                                      _ptr(ws), ws.numel(), _stream(stream, q.device))

@@ -135,6 +135,7 @@ int check_geom(const cart_geom* g) {
   if (g->B < 1 || g->n < 1 || g->Hq < 1 || g->Hkv < 1 || g->Hq % g->Hkv != 0) return CART_ERR_GEOMETRY;
   if (g->d != 64 && g->d != 128) return CART_ERR_GEOMETRY;
   if (g->p < 0 || g->frozen_prefix < 0 || g->frozen_prefix > g->p) return CART_ERR_GEOMETRY;
+  if (g->window < 0) return CART_ERR_GEOMETRY;
   if (!(std::isfinite(g->scale)) || !(g->scale > 0.f) || !(g->rope_theta > 0.0) ||
       !std::isfinite(g->rope_theta))
     return CART_ERR_GEOMETRY;
@@ -414,6 +415,7 @@ static int fwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   l.table = tp.table;
   l.cu = pk.cu;
   l.total = pk.total;
+  l.window = g->window;
   CUtensorMap mO32;
   if (in == CART_BF16) {
     if (!make_tokens_map(&mO32, o, g, pk, g->Hq, 32)) return CART_ERR_CUDA;
@@ -541,6 +543,7 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   l.freqs = &tp.freqs;
   l.cu = pk.cu;
   l.total = pk.total;
+  l.window = g->window;
   SideStream* side = side_stream();
   if (!side) {
     CART_CUDA(launch_bwd(l, st, st));
@@ -668,16 +671,17 @@ int cart_attn_decode(int B, int Hq, int Hkv, int d, int p, float scale, double r
                      const void* vc, void* k_cache, void* v_cache, int cache_rows,
                      const int* priv_len, void* o, void* workspace, size_t workspace_bytes,
                      void* stream) {
-  return cart_attn_decode_span(B, 1, Hq, Hkv, d, p, scale, rope_theta, q, k_new, v_new, kc, vc,
-                               k_cache, v_cache, cache_rows, priv_len, o, workspace,
+  return cart_attn_decode_span(B, 1, 0, Hq, Hkv, d, p, scale, rope_theta, q, k_new, v_new, kc,
+                               vc, k_cache, v_cache, cache_rows, priv_len, o, workspace,
                                workspace_bytes, stream);
 }
 
-int cart_attn_decode_span(int B, int span, int Hq, int Hkv, int d, int p, float scale,
+int cart_attn_decode_span(int B, int span, int window, int Hq, int Hkv, int d, int p, float scale,
                           double rope_theta, const void* q, const void* k_new, const void* v_new,
                           const void* kc, const void* vc, void* k_cache, void* v_cache,
                           int cache_rows, const int* priv_len, void* o, void* workspace,
                           size_t workspace_bytes, void* stream) {
+  if (window < 0) return CART_ERR_GEOMETRY;
   int rc = check_decode(B, Hq, Hkv, d, p, scale, rope_theta, cache_rows, span);
   if (rc) return rc;
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
@@ -692,6 +696,7 @@ int cart_attn_decode_span(int B, int span, int Hq, int Hkv, int d, int p, float 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeLaunch a{};
   a.span = span;
+  a.window = window;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;

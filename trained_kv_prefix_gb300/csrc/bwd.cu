@@ -60,7 +60,18 @@ struct BwdParams {
   // packed layout (SeqRows): segment table and packed token count
   const int* cu;
   int total;
+  // sliding window in keys (0: none): the query at position P sees keys at
+  // positions P - window + 1 .. P (cartridge row j at position j)
+  int window;
 };
+
+// Query tiles (of any sequence) that can see a key at position kmax or
+// before under the window: queries i <= kmax - p + window - 1.
+__device__ __forceinline__ int window_qtiles(const BwdParams& a, int window, int kmax) {
+  if (window <= 0) return 1 << 30;
+  const int i_max = kmax - a.p + window - 1;
+  return i_max < 0 ? 0 : i_max / kTile + 1;
+}
 
 // 128-row query tiles of sequence b (cu: the packed table, or null).
 __device__ __forceinline__ int seq_qtiles(const BwdParams& a, const int* cu, int b) {
@@ -135,7 +146,9 @@ enum DkdvBar { kResFull = 0, kQFull0, kQEmpty0 = kQFull0 + kDkdvQSlots,
                kDoFull0 = kQEmpty0 + kDkdvQSlots, kDoEmpty0 = kDoFull0 + kDkdvDoSlots,
                kStFull = kDoEmpty0 + kDkdvDoSlots, kPtFull, kDpTFull, kDsFull, kAccDone,
                kDkdvDrain, kDkdvBars };
-static_assert(kDkdvBars * 8 + 16 <= 256, "dK/dV barrier area");
+// barrier area: the barriers, the TMEM address, the abort word, and the
+// query tile of the step in each Q slot (read by the masks under a window)
+static_assert(kDkdvBars * 8 + 16 + 4 * kDkdvQSlots <= 256, "dK/dV barrier area");
 
 // The steps of a key tile in order: a cartridge tile sees every (sequence,
 // head of the group, 128-row query tile), sequence-major; real tile rt of a
@@ -143,16 +156,18 @@ static_assert(kDkdvBars * 8 + 16 <= 256, "dK/dV barrier area");
 // diagonal and after).  The query tile runs fastest, then the head.
 struct DkdvCursor {
   int b, hh, qt;
-  int nq;         // query tiles of sequence b
+  int nq;         // query tiles of sequence b that see the key tile
+  int qcap;       // query tiles the window lets see the key tile
   int row0, blk;  // sequence b on the maps' token axis
   __device__ __forceinline__ void load_seq(const BwdParams& a, const int* cu) {
     const SeqRows r = seq_rows(cu, a.total, a.n, b);
-    nq = cu ? (r.len + kTile - 1) / kTile : a.n_qtiles;
+    nq = min(cu ? (r.len + kTile - 1) / kTile : a.n_qtiles, qcap);
     row0 = r.row0;
     blk = r.blk;
   }
   __device__ __forceinline__ void start(const BwdParams& a, const int* cu, bool cart, int b_real,
-                                        int rt) {
+                                        int rt, int cap) {
+    qcap = cap;
     b = cart ? 0 : b_real;
     hh = 0;
     qt = cart ? 0 : rt;
@@ -194,7 +209,7 @@ __device__ __forceinline__ void write_cart_row(float* dst, const float* x, int n
   }
 }
 
-template <int D, bool kPacked>
+template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                 const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
@@ -211,8 +226,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDkdvBars * 8);
   int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDkdvBars * 8 + 8);
+  int* step_qt = reinterpret_cast<int*>(smem + L::kBar + kDkdvBars * 8 + 16);  // [SQ]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* const cu = kPacked ? a.cu : nullptr;  // packed segment table
+  const int* const cu = kGeneral ? a.cu : nullptr;  // packed segment table
+  const int window = kGeneral ? a.window : 0;
 
   // ---- work item: cartridge tiles first (heaviest), then real tiles ----
   int blk = blockIdx.x;
@@ -230,17 +247,35 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     b_real = rem / a.Hkv;
     g = rem % a.Hkv;
   }
+  // query tiles the window lets see this key tile (its last key position)
+  const int qcap = window_qtiles(
+      a, window, cart ? min(tile * kTile + kTile - 1, a.p - 1) : a.p + tile * kTile + kTile - 1);
   int U;
-  if (!cu) {
+  if (!kGeneral) {
     U = cart ? a.B * a.G * a.n_qtiles : a.G * max(a.n_qtiles - tile, 0);
-  } else if (cart) {  // packed: every segment's query tiles
+  } else if (cart) {  // every sequence's query tiles
     int tiles = 0;
-    for (int b = 0; b < a.B; ++b) tiles += seq_qtiles(a, cu, b);
+    for (int b = 0; b < a.B; ++b) tiles += min(seq_qtiles(a, cu, b), qcap);
     U = a.G * tiles;
   } else {
-    U = a.G * max(seq_qtiles(a, cu, b_real) - tile, 0);
+    U = a.G * max(min(seq_qtiles(a, cu, b_real), qcap) - tile, 0);
   }
-  if (U == 0) return;  // a packed segment shorter than the longest
+  if (kGeneral && U == 0) {
+    // no query sees the tile: a packed segment shorter than the longest, or
+    // cartridge rows before every query's window (gradient 0); the fixed
+    // layout without a window always has steps
+    if (cart) {
+      for (int e = threadIdx.x; e < kTile * (D / 4); e += blockDim.x) {
+        const int j = tile * kTile + e / (D / 4);
+        if (j >= a.p) continue;
+        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+        const long long off = (static_cast<long long>(j) * a.Hkv + g) * D + (e % (D / 4)) * 4;
+        write_cart_row(a.dkc + off, zero, 4, row_frozen(a, j), a.accumulate);
+        write_cart_row(a.dvc + off, zero, 4, row_frozen(a, j), a.accumulate);
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -302,10 +337,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       int issued_q = 0, issued_do = 0;
       bool ok = true;
       DkdvCursor it;
-      if (kPacked) it.start(a, cu, cart, b_real, tile);
+      if (kGeneral) it.start(a, cu, cart, b_real, tile, qcap);
       for (int u = 0; u < U; ++u) {
         const int sq = u % SQ, sd = u % SD;
-        if (kPacked) {
+        if (kGeneral) {
           if (u > 0) it.next(a, cu, cart, tile);
         } else {  // fixed layout: every sequence has n_qtiles query tiles
           const int nq = cart ? a.n_qtiles : a.n_qtiles - tile;
@@ -325,6 +360,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
+        if (kGeneral) step_qt[sq] = it.qt;  // published by the arrive below
         mbar_arrive_expect_tx(&bars[kQFull0 + sq], L::kTileBytes + 512);
 #pragma unroll
         for (int hc = 0; hc < D / 64; ++hc)
@@ -457,8 +493,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const int wg = warp >> 2;
     const int row = threadIdx.x & 127;  // key row within the tile == TMEM lane
     const int j = tile * kTile + row;
-    // real tiles: the sequence's query tiles and tokens
-    const int nq_real = cart ? 0 : seq_qtiles(a, cu, b_real);
+    // real tiles: the sequence's query tiles (those the window allows) and
+    // tokens; the last query that sees this key under the window
+    const int nq_real = cart ? 0 : min(seq_qtiles(a, cu, b_real), qcap);
+    const int i_hi = window > 0 ? (cart ? j : a.p + j) - a.p + window - 1 : 1 << 30;
     const bool key_ok = cart ? (j < a.p) : (j < (cu ? seq_rows(cu, a.total, a.n, b_real).len : a.n));
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
@@ -480,6 +518,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       // for c < qlim: none for a cartridge key, query < key for a real key,
       // all for rows past the end of the keys
       const int qlim = !key_ok ? 32 : (cart ? 0 : max(0, min(32, j - qt * kTile - wg * 32)));
+      // ... and for c >= qhi (past the key's window)
+      // (a cartridge tile's steps run over every sequence's query tiles: the
+      // producer leaves the step's tile next to its Q slot)
+      const int qt_u = (window > 0 && cart) ? *reinterpret_cast<volatile int*>(step_qt + sq) : qt;
+      const int qhi = window > 0 ? max(0, min(32, i_hi - qt_u * kTile - wg * 32 + 1)) : 32;
       const uint32_t lse_s = smem_u32(vecL + sq * 128 + wg * 32);
       const uint32_t dv_s = smem_u32(vecD + sd * 128 + wg * 32);
       uint32_t r[32];
@@ -488,7 +531,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       tmem_reg_fence(r);
       // P^T = 2^(S^T * scale * log2(e) - lse2) (f32, kept in p for dS^T)
       // while dP^T is still being computed; two queries per packed op
-      const bool masked = __any_sync(0xffffffffu, qlim > 0);
+      const bool masked = __any_sync(0xffffffffu, qlim > 0 || qhi < 32);
       const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
       float2 p[16];
 #pragma unroll
@@ -503,8 +546,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          p[c].x = (2 * c >= qlim) ? p[c].x : 0.f;
-          p[c].y = (2 * c + 1 >= qlim) ? p[c].y : 0.f;
+          p[c].x = (2 * c >= qlim && 2 * c < qhi) ? p[c].x : 0.f;
+          p[c].y = (2 * c + 1 >= qlim && 2 * c + 1 < qhi) ? p[c].y : 0.f;
         }
       }
       {
@@ -677,7 +720,7 @@ enum DqBar {
 static_assert(kDqBars * 8 + 16 <= 256, "dQ barrier area");
 static_assert(kDqBars * 8 + 4 <= 256, "dq barrier area");
 
-template <int D, bool kPacked>
+template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
               const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
@@ -695,18 +738,30 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDqBars * 8);
   int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDqBars * 8 + 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* const cu = kPacked ? a.cu : nullptr;  // packed segment table
+  const int* const cu = kGeneral ? a.cu : nullptr;  // packed segment table
+  const int window = kGeneral ? a.window : 0;
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);
   const int seq_len = cu ? seq_rows(cu, a.total, a.n, b).len : a.n;
-  if (kPacked && qt * kTile >= seq_len) return;  // a segment shorter than the longest
+  if (kGeneral && qt * kTile >= seq_len) return;  // a segment shorter than the longest
   const int kvh = h / a.G;
   const int q0 = qt * kTile;
-  const int n_ct = (a.p + kTile - 1) / kTile;
+  // key tiles: cartridge tiles [ct_lo, n_ct_all), real tiles [rt_lo, rt_hi)
+  const int n_ct_all = (a.p + kTile - 1) / kTile;
   const int last_q = min(q0 + kTile, seq_len) - 1;      // last real query of the tile
-  const int n_rt = last_q / kTile + 1;                   // real key steps up to the diagonal
-  const int T = n_ct + n_rt;
+  const int rt_hi = last_q / kTile + 1;                  // real key steps up to the diagonal
+  int ct_lo = 0, rt_lo = 0;
+  if (window > 0) {
+    // the first key any row of the tile sees: position p + q0 - window + 1
+    const int lo = a.p + q0 - window + 1;
+    if (lo > 0) {
+      ct_lo = min(lo / kTile, n_ct_all);
+      rt_lo = lo > a.p ? (lo - a.p) / kTile : 0;
+    }
+  }
+  const int n_ct = n_ct_all - ct_lo;
+  const int T = n_ct + rt_hi - rt_lo;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -758,7 +813,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       bool ok = true;
       for (int t = 0; t < T && ok; ++t) {
         const bool cart = t < n_ct;
-        const int row0 = cart ? t * kTile : sr.row0 + (t - n_ct) * kTile;
+        const int row0 = cart ? (ct_lo + t) * kTile : sr.row0 + (rt_lo + t - n_ct) * kTile;
         const int blk = cart ? 0 : sr.blk;
         const int sk = t % SK, sv = t % SV;
         if (t >= SK) {
@@ -890,8 +945,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // visible keys of this group's 64 (leading columns)
-      int valid = t < n_ct ? a.p - t * kTile - wg * 64 : i_cap - (t - n_ct) * kTile - wg * 64 + 1;
+      // (key positions of this group's 64 columns start at kpos0)
+      const int kpos0 =
+          (t < n_ct ? (ct_lo + t) * kTile : a.p + (rt_lo + t - n_ct) * kTile) + wg * 64;
+      int valid = t < n_ct ? a.p - kpos0 : i_cap - (kpos0 - a.p) + 1;
       valid = max(0, min(valid, 64));
+      // ... and the first one under the window
+      const int first = window > 0 ? max(0, min(a.p + i - window + 1 - kpos0, 64)) : 0;
       const uint32_t ts = tS0 + x * 128 + wg * 64 + lane_off;
       const uint32_t tdp = tDP + wg * 64 + lane_off;
       uint32_t sa[32], sb[32], da[32], db[32];
@@ -917,14 +977,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const float2 x = __ffma2_rn(sv, sc2, nl2);
           float2 pe = make_float2(exp2_approx(x.x), exp2_approx(x.y));
           if (decltype(masked)::value) {
-            pe.x = (c < valid) ? pe.x : 0.f;
-            pe.y = (c + 1 < valid) ? pe.y : 0.f;
+            pe.x = (c < valid && c >= first) ? pe.x : 0.f;
+            pe.y = (c + 1 < valid && c + 1 >= first) ? pe.y : 0.f;
           }
           const float2 ds = __fmul2_rn(pe, __fadd2_rn(dv, nd2));
           pk[c / 2] = pack_bf16x2(ds.x, ds.y);
         }
       };
-      if (__any_sync(0xffffffffu, valid < 64))
+      if (__any_sync(0xffffffffu, valid < 64 || first > 0))
         compute(std::true_type{});
       else
         compute(std::false_type{});
@@ -1049,19 +1109,20 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.table = l.table;
   p.cu = l.cu;
   p.total = l.total;
+  p.window = l.window;
   for (int c = 0; c < D / 2; ++c) p.turns[c] = l.freqs->turns[c];
   p.status = device_status_ptr();
-  const bool packed = l.cu != nullptr;
-  cudaError_t e = packed ? set_smem_once<dkdv_kernel<D, true>>(DkdvSmem<D>::kAlloc)
+  const bool general = l.cu != nullptr || l.window > 0;
+  cudaError_t e = general ? set_smem_once<dkdv_kernel<D, true>>(DkdvSmem<D>::kAlloc)
                          : set_smem_once<dkdv_kernel<D, false>>(DkdvSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  e = packed ? set_smem_once<dq_kernel<D, true>>(DqSmem<D>::kAlloc)
+  e = general ? set_smem_once<dq_kernel<D, true>>(DqSmem<D>::kAlloc)
              : set_smem_once<dq_kernel<D, false>>(DqSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_blocks = p.n_ct * p.Hkv + p.n_rt * p.Hkv * p.B;
   if (n_blocks > 0) {
     TraceScope tr("bwd_dkdv", st_dkdv);
-    auto* kern = packed ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
+    auto* kern = general ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
     kern<<<n_blocks, kDkdvThreads, DkdvSmem<D>::kAlloc, st_dkdv>>>(*l.mQ, *l.mdO, *l.mKc, *l.mVc,
                                                                    *l.mK, *l.mV, p);
   }
@@ -1069,7 +1130,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   if (e != cudaSuccess) return e;
   TraceScope tr("bwd_dq", st_dq);
   p.tma_dq = (!l.out_f32 && l.mdQ) ? 1 : 0;
-  auto* kern_dq = packed ? dq_kernel<D, true> : dq_kernel<D, false>;
+  auto* kern_dq = general ? dq_kernel<D, true> : dq_kernel<D, false>;
   kern_dq<<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
       *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p.tma_dq ? *l.mdQ : *l.mQ, p);
   return cudaGetLastError();

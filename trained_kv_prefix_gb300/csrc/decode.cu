@@ -152,9 +152,14 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   }
   const int Lb = clamp_len(a.len, b, a.rows - S + 1);  // new rows Lb .. Lb + S - 1
   const int k_lo = u * kDecodeUnit;
-  if (k_lo > Lb + S - 1) {
+  // sliding window: column t sees private rows Lb + t - window + 1 .. Lb + t;
+  // lo0 is the first row any column sees, u_lo its unit
+  const int W = a.window;
+  const int lo0 = W > 0 ? Lb - W + 1 : 0;
+  const int u_lo = lo0 > 0 ? lo0 / kDecodeUnit : 0;
+  if (k_lo > Lb + S - 1 || u < u_lo) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    return;  // past the end of this conversation's rows
+    return;  // past the end of this conversation's rows, or before its window
   }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -164,6 +169,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   float* sred = reinterpret_cast<float*>(smem + L::kRed);
   const int nk = min(kDecodeUnit, Lb + S - k_lo);  // keys of this unit
   const int nc = (nk + CH - 1) / CH;               // chunks
+  const int c0 = lo0 > k_lo ? (lo0 - k_lo) / CH : 0;  // first chunk in the window
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
   int* abort_flag = reinterpret_cast<int*>(full + kPrivStages);
   const uint32_t abort_s = smem_u32(abort_flag);
@@ -173,12 +179,12 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
     fence_mbar_init();
   }
 
-  // Stage chunk c into ring slot c % kPrivStages (thread 0): the K and V rows
-  // of the chunk by TMA, 64 rows per box (rows past the cache's end read as
-  // zero; rows past the unit's end are whatever the cache holds).
+  // Stage chunk c into ring slot (c - c0) % kPrivStages (thread 0): the K and
+  // V rows of the chunk by TMA, 64 rows per box (rows past the cache's end
+  // read as zero; rows past the unit's end are whatever the cache holds).
   auto stage = [&](int c) {
     if (tid != 0) return;
-    const int sl = c % kPrivStages;
+    const int sl = (c - c0) % kPrivStages;
     uint8_t* sK = smem + sl * L::kStage;
     mbar_arrive_expect_tx(&full[sl], L::kStage);
     const int row = k_lo + c * CH;
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
       tma_load_4d(sK + L::kTile + h * L::kHalf, &mVs, &full[sl], h * 64, g, row, b);
     }
   };
-  for (int c = 0; c < kPrivStages && c < nc; ++c) stage(c);
+  for (int c = c0; c < c0 + kPrivStages && c < nc; ++c) stage(c);
   // one position for every column when S = 1: its angles once, shared
   if (S == 1 && tid < HALF) scs[tid] = rope_cs_turns_fast(f.turns[tid], a.p + Lb);
   __syncthreads();
@@ -259,14 +265,15 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
       for (int e = 0; e < 4; ++e) oacc[i][j][e] = 0.f;
   }
 
-  for (int c = 0; c < nc; ++c) {
+  for (int c = c0; c < nc; ++c) {
     // chunk c has landed when its slot's phase completes
-    const bool ok = mbar_wait(&full[c % kPrivStages], (c / kPrivStages) & 1, abort_s, a.status,
+    const int cr = c - c0;
+    const bool ok = mbar_wait(&full[cr % kPrivStages], (cr / kPrivStages) & 1, abort_s, a.status,
                               kDevErrTimeoutTma);
     if (__syncthreads_or(!ok)) break;
     const int k0 = c * CH;
     const int kn = min(CH, nk - k0);
-    uint8_t* sKp = smem + (c % kPrivStages) * L::kStage;
+    uint8_t* sKp = smem + (cr % kPrivStages) * L::kStage;
     const uint32_t sK = smem_u32(sKp), sV = sK + L::kTile;
     // staged V rows past the unit's end, up to the next 16-row group: zero
     for (int t = tid; t < (((kn + 15) & ~15) - kn) * (D / 8); t += 128)
@@ -347,7 +354,10 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
         for (int hf = 0; hf < 2; ++hf) {
           const int key = warp * 16 + g8 + 8 * hf;
           float sv = sacc[j][2 * hf + qq] * scale_log2;
-          const bool vis = key < kn && (!kSpan || k_lo + k0 + key <= qlast[j][qq]);
+          // (the window: row >= the column's position - window + 1)
+          const int r = k_lo + k0 + key;
+          const bool vis = key < kn && (!kSpan || r <= qlast[j][qq]) &&
+                           (W <= 0 || r >= (kSpan ? qlast[j][qq] - W + 1 : lo0));
           sv = vis ? sv : -INFINITY;
           sacc[j][2 * hf + qq] = sv;
           mx = fmaxf(mx, sv);
@@ -515,16 +525,19 @@ __global__ void decode_merge_kernel(DecodeLaunch a) {
   const int R = a.B * QC, r = vb * G + hh;
   const int Lb = clamp_len(a.len, b, a.rows - a.span + 1);
   const int S = a.n_cart_splits;
-  const int np = S + (Lb + a.span - 1) / kDecodeUnit + 1;
+  // private units from the first one inside the sliding window (u_lo)
+  const int lo0 = a.window > 0 ? Lb - a.window + 1 : 0;
+  const int u_lo = lo0 > 0 ? lo0 / kDecodeUnit : 0;
+  const int np = S + (Lb + a.span - 1) / kDecodeUnit + 1 - u_lo;
   const long long pbase =
       (static_cast<long long>(b) * a.Hkv + g) * a.max_units * QC + t * G + hh;
   auto part_row = [&](int pt) -> const float* {
     return pt < S ? a.cart_part + ((static_cast<long long>(pt) * a.Hkv + g) * R + r) * D
-                  : a.priv_part + (pbase + static_cast<long long>(pt - S) * QC) * D;
+                  : a.priv_part + (pbase + static_cast<long long>(u_lo + pt - S) * QC) * D;
   };
   auto part_lse = [&](int pt) -> float {
     return pt < S ? __ldcg(a.cart_lse + (static_cast<long long>(pt) * a.Hkv + g) * R + r)
-                  : __ldcg(a.priv_lse + pbase + static_cast<long long>(pt - S) * QC);
+                  : __ldcg(a.priv_lse + pbase + static_cast<long long>(u_lo + pt - S) * QC);
   };
   constexpr int PL = D / 32;  // dims per lane: 4 or 2
   float M = -INFINITY, lse0 = -INFINITY;
@@ -646,6 +659,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_
     l.dec_G = G;
     l.dec_rows = a.rows;
     l.dec_s = a.span;
+    l.window = a.window;
     l.freqs = &f;
     e = launch_fwd(l, st);
     if (e != cudaSuccess) return e;

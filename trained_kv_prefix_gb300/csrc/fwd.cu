@@ -58,6 +58,9 @@ struct FwdParams {
   // training, packed layout (SeqRows): segment table and packed token count
   const int* cu;
   int total;
+  // sliding window in keys (0: none): the query at position P sees keys at
+  // positions P - window + 1 .. P (cartridge row j at position j)
+  int window;
   float2 turns[kMaxHeadDim / 2];
 };
 
@@ -204,7 +207,12 @@ struct RopeRowsCoop {
   }
 };
 
-template <int D, bool kPacked>
+enum FwdMode { kFwdTrain = 0, kFwdGeneral = 1, kFwdDecode = 2 };
+
+// kMode: kFwdTrain (training, fixed [B, n] layout, no window), kFwdGeneral
+// (training with packed segments and / or a sliding window) or kFwdDecode
+// (the decode cartridge pass); each mode compiles only its own code.
+template <int D, int kMode>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
@@ -220,14 +228,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // packed training layout: the segment table (a constant null otherwise)
-  const int* const cu = kPacked ? a.cu : nullptr;
+  constexpr bool kDecode = kMode == kFwdDecode;
+  const int* const cu = kMode == kFwdGeneral ? a.cu : nullptr;
+  const int window = kMode == kFwdTrain ? 0 : a.window;
 
   // ---- work item (training: heaviest pairs first) ----
   int head, qb, pair, kvh, split;
   // tokens of the query block's sequence (decode: the n_rows stacked rows);
   // its place on the token axis is looked up again where it is used
   int seq_len = a.n_rows;
-  if (!a.decode) {
+  if (!kDecode) {
     const int hb = a.Hq_map * a.n_qblocks;
     pair = a.n_pairs - 1 - static_cast<int>(blockIdx.x) / hb;
     const int rem = static_cast<int>(blockIdx.x) % hb;
@@ -243,28 +253,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     kvh = head;
     split = blockIdx.z;
   }
-  const int n_qtiles = a.decode ? a.n_qtiles : (seq_len + kTile - 1) / kTile;
+  const int n_qtiles = kDecode ? a.n_qtiles : (seq_len + kTile - 1) / kTile;
   if (2 * pair >= n_qtiles) return;  // a packed segment shorter than the longest
   const bool hasB = 2 * pair + 1 < n_qtiles;
   const int n_ct_all = (a.p + kTile - 1) / kTile;
-  int ct_lo = 0, ct_hi = n_ct_all, n_rt_A = 0, n_rt_B = 0;
-  if (a.decode) {
+  // key tiles: cartridge tiles [ct_lo, ct_hi), then real tiles [rt_lo, n_rt_x)
+  int ct_lo = 0, ct_hi = n_ct_all, rt_lo = 0, n_rt_A = 0, n_rt_B = 0;
+  if (kDecode) {
     ct_lo = split * a.cart_tiles_per_split;
     ct_hi = min(ct_lo + a.cart_tiles_per_split, n_ct_all);
   } else {
     const int n_real_tiles = (seq_len + kTile - 1) / kTile;
     n_rt_A = min(2 * pair + 1, n_real_tiles);
     n_rt_B = hasB ? min(2 * pair + 2, n_real_tiles) : 0;
+    if (window > 0) {
+      // the first key any row of tile A sees: position p + q0A - window + 1
+      const int lo = a.p + 2 * pair * kTile - window + 1;
+      if (lo > 0) {
+        ct_lo = min(lo / kTile, n_ct_all);
+        rt_lo = lo > a.p ? (lo - a.p) / kTile : 0;
+      }
+    }
   }
   const int n_ct = max(ct_hi - ct_lo, 0);
-  const int T_A = n_ct + n_rt_A;
-  const int T_B = hasB ? n_ct + n_rt_B : 0;
+  const int T_A = n_ct + n_rt_A - rt_lo;
+  const int T_B = hasB ? n_ct + n_rt_B - rt_lo : 0;
   const int T = max(T_A, T_B);
 
   if (threadIdx.x == 0) {
     // decode mode: let the dependent private pass start right away (one of
     // its CTAs waits for this grid before that grid completes)
-    if (a.decode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (kDecode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
     for (int s = 0; s < 2; ++s) {
@@ -304,7 +323,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
         // tile B of a lone last tile reads rows past the end: zero fill
-        if (a.decode) {  // (d, G, Hkv, B) map, 128/G conversations per box
+        if (kDecode) {  // (d, G, Hkv, B) map, 128/G conversations per box
           tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, 0, kvh,
                       q0A / a.dec_G);
           tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, 0,
@@ -321,7 +340,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int t = 0; t < T && ok; ++t) {
         const int s = t & 1;
         const bool cart = t < n_ct;
-        const int row0 = cart ? (ct_lo + t) * kTile : sq.row0 + (t - n_ct) * kTile;
+        const int row0 = cart ? (ct_lo + t) * kTile : sq.row0 + (rt_lo + t - n_ct) * kTile;
         const CUtensorMap* mk = cart ? &mKc : &mK;
         const CUtensorMap* mv = cart ? &mVc : &mV;
         const int blk = cart ? 0 : sq.blk;
@@ -461,6 +480,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + 256 + x * 128 + lane_off;
     float m = -INFINITY, l = 0.f;
     bool ok = Tx > 0;
+    // decode: position of the row's first visible key (window > 0)
+    int key_lo_dec = 0;
     if (ok) {
       if (a.rotate_q) {
         // this warp's 32 rows: table rows fetched while the Q tile lands
@@ -473,7 +494,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (ok) rr.apply(smem + L::kQ + x * L::kTileBytes, r0, i0, seq_len, lane);
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
-      } else if (a.decode) {
+      } else if (kDecode) {
         // row i = (b*s + t)*G + hh of this kv head: query t of conversation
         // b's span at position p + len[b] + t
         ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
@@ -484,6 +505,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int lmax = a.dec_rows - a.dec_s;
           len = len < 0 ? 0 : (len > lmax ? lmax : len);
           const int pos = a.p + len + vb % a.dec_s;
+          if (window > 0) key_lo_dec = pos - window + 1;
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
                           [&](int j0, float2* c) {
 #pragma unroll
@@ -517,12 +539,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tmem_reg_fence(r[2]);
       tmem_reg_fence(r[3]);
       // number of visible keys of this tile (leading columns)
-      int valid = t < n_ct ? a.p - (ct_lo + t) * kTile : i_cap - (t - n_ct) * kTile + 1;
+      // and the first one (sliding window); key positions of this tile start
+      // at kpos0
+      const int kpos0 = t < n_ct ? (ct_lo + t) * kTile : a.p + (rt_lo + t - n_ct) * kTile;
+      int valid = t < n_ct ? a.p - kpos0 : i_cap - (kpos0 - a.p) + 1;
       valid = max(0, min(valid, kTile));
-      if (__any_sync(0xffffffffu, valid < kTile)) {
+      int first = 0;
+      if (window > 0) {
+        const int key_lo = kDecode ? key_lo_dec : a.p + i - window + 1;
+        first = max(0, min(key_lo - kpos0, kTile));
+      }
+      if (__any_sync(0xffffffffu, valid < kTile || first > 0)) {
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
-          if (c >= valid) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          if (c >= valid || c < first) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
       // row maximum of the raw scores (scale_log2 > 0), 4 independent chains
       // of three-input maxima
@@ -548,7 +578,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // P = 2^(S * scale * log2(e) - m), two keys per packed two-lane op
       const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-      const float2 nm2 = make_float2(-m, -m);
+      // (a row that has seen no visible key yet keeps m = -inf: P = 0)
+      const float mr = (kMode != kFwdTrain && m == -INFINITY) ? 0.f : m;
+      const float2 nm2 = make_float2(-mr, -mr);
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                       make_float2(0.f, 0.f)};
 #pragma unroll
@@ -599,10 +631,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      // a decode split may hold none of a windowed row's keys: O = 0
+      const float inv_l = (kMode == kFwdTrain || l > 0.f) ? 1.f / l : 0.f;
       const bool row_ok = i < seq_len;
-      const bool f32 = a.decode || a.out_f32;
-      const SeqRows sq = a.decode ? SeqRows{0, 0, 0, a.n_rows}
+      const bool f32 = kDecode || a.out_f32;
+      const SeqRows sq = kDecode ? SeqRows{0, 0, 0, a.n_rows}
                                   : seq_rows(cu, a.total, a.n_rows, qb);
       // a packed segment's last rows: a TMA store of the warp's 32 rows would
       // run into the next segment, so those warps store row by row
@@ -688,7 +721,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (grow < sq.len) {
             const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
             long long off;  // element offset of the row
-            if (a.decode)
+            if (kDecode)
               off = ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + grow) * D;
             else
               off = ((static_cast<long long>(sq.g0) + grow) * a.Hq_map + head) * D;
@@ -704,7 +737,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (row_ok) {
         const float lse2 = m + __log2f(l);
-        if (a.decode)
+        if (kDecode)
           a.lse[(static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i] = lse2;
         else
           a.lse[lse_index(cu, a.total, a.n_rows, a.Hq_map, qb, head, sq, i)] =
@@ -723,9 +756,12 @@ template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdSmem<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  const bool packed = !a.decode && a.cu;
-  cudaError_t e = packed ? set_smem_once<fwd_kernel<D, true>>(L::kAlloc)
-                         : set_smem_once<fwd_kernel<D, false>>(L::kAlloc);
+  const bool general = !a.decode && (a.cu || a.window > 0);
+  auto* kern = a.decode ? fwd_kernel<D, kFwdDecode>
+                        : (general ? fwd_kernel<D, kFwdGeneral> : fwd_kernel<D, kFwdTrain>);
+  cudaError_t e = a.decode ? set_smem_once<fwd_kernel<D, kFwdDecode>>(L::kAlloc)
+                           : (general ? set_smem_once<fwd_kernel<D, kFwdGeneral>>(L::kAlloc)
+                                      : set_smem_once<fwd_kernel<D, kFwdTrain>>(L::kAlloc));
   if (e != cudaSuccess) return e;
   FwdParams p{};
   p.n_rows = a.n_rows;
@@ -757,6 +793,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
     p.cu = a.cu;
     p.total = a.total;
   }
+  p.window = a.window;
   dim3 grid;
   if (!a.decode)
     grid = dim3(static_cast<unsigned>(p.n_pairs) * a.Hq_map * a.n_qblocks, 1, 1);
@@ -773,7 +810,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, packed ? fwd_kernel<D, true> : fwd_kernel<D, false>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
+  return cudaLaunchKernelEx(&cfg, kern, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
                             p.tma_out ? *a.mO32 : *a.mQ, p);
 }
 

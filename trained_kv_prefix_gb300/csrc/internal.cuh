@@ -211,6 +211,7 @@ struct FwdLaunch {
   // = the longest; maps over (d, H, total, 1)
   const int* cu = nullptr;
   int total = 0;
+  int window = 0;          // sliding window in keys (0: none)
 };
 // Two 128-row query tiles per CTA (training: consecutive row tiles of one
 // (sequence, head); decode: rows 0-127 / 128-255 of a kv head's stacked rows).
@@ -245,6 +246,7 @@ struct BwdLaunch {
   // (d, H, total, 1); the row vectors stay [B, Hq, npad]
   const int* cu = nullptr;
   int total = 0;
+  int window = 0;           // sliding window in keys (0: none)
 };
 // dK/dV kernel on st_dkdv, dQ kernel on st_dq (the two are independent).
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st_dkdv, cudaStream_t st_dq);
@@ -271,6 +273,7 @@ struct DecodeLaunch {
   int max_units;            // ceil(rows / kDecodeUnit)
   uint32_t* status;         // device status word (set by the launcher)
   int span = 1;             // queries per conversation (q, k_new, v_new, o are [B, span, ...])
+  int window = 0;           // sliding window in keys (0: none)
 };
 // The whole decode step on one stream, three kernels chained by
 // programmatic dependent launch: the cartridge split pass (fwd kernel in
