@@ -41,10 +41,10 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 // grid: (Hkv, B, max_units); block: 128 threads (4 warps).  CTA (g, b, u)
 // owns private rows [u*U, min((u+1)*U, len+s)) of kv head g of conversation
 // b (U = kDecodeUnit; CTAs past the end of a conversation exit at once) and
-// streams them through a kPrivStages-deep ring of 64-row chunks:
+// streams them through a ring of 64-row chunk buffers (kPrivStagesFor):
 //   * Thread 0 stages a chunk's K and V rows in shared memory by TMA (one
 //     (64, 1, 64, 1) box per 64-dim half, 128-byte swizzled, completing on
-//     the slot's mbarrier) while the previous chunk is computed; staged V
+//     the slot's mbarrier) as soon as the slot is free; staged V
 //     rows past the unit's end are zeroed after they land (the cache may
 //     hold anything there, and 0 * a non-finite value is not 0).
 //   * The block rotates the s*G query columns c = t*G + hh (t the span
@@ -63,10 +63,17 @@ __device__ __forceinline__ int clamp_len(const int* len, int b, int rows) {
 //   * Output: the unit's normalised O and its log2-domain log-sum-exp per
 //     column (O = 0, lse = -inf for a column that saw none of its rows).
 constexpr int kPrivCH = kDecodeChunk;  // keys per chunk
-constexpr int kPrivStages = 2;
+// Chunk buffers per CTA.  One for up to 16 query columns: each chunk is
+// copied once the previous one is done, and the copies of one CTA overlap
+// the compute of the others (about six CTAs fit per SM this way; two buffers
+// per CTA leave room for three and measured 9 % slower on the serving step).
+// Two for 24-32 columns, whose registers already limit an SM to three CTAs.
+template <int QN>
+constexpr int kPrivStagesFor = QN >= 3 ? 2 : 1;
 
 template <int D, int QN>
 struct PrivSmem {
+  static constexpr int kPrivStages = kPrivStagesFor<QN>;
   static constexpr int kHalf = kPrivCH * 128;          // 64 dims x CH rows (bf16)
   static constexpr int kTile = (D / 64) * kHalf;       // one K or V chunk
   static constexpr int kStage = 2 * kTile;             // K then V
@@ -74,7 +81,7 @@ struct PrivSmem {
   static constexpr int kPStride = kPrivCH + 8;         // padded row: conflict-free B loads
   static constexpr int kCS = kP + 8 * QN * kPStride * 2;  // float2 [D/2]: a new key's angles
   static constexpr int kRed = kCS + (D / 2) * 8;       // f32 [2][4 warps][8*QN]
-  static constexpr int kBar = kRed + 2 * 4 * 8 * QN * 4;  // full[kPrivStages], abort word
+  static constexpr int kBar = kRed + 2 * 4 * 8 * QN * 4;  // full[stages], abort word
   static constexpr int kBytes = kBar + kPrivStages * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -115,6 +122,7 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
     const __grid_constant__ CUtensorMap mKs, const __grid_constant__ CUtensorMap mVs,
     DecodeLaunch a, const RopeFreqs f, float scale_log2) {
   using L = PrivSmem<D, QN>;
+  constexpr int kPrivStages = L::kPrivStages;
   constexpr int CH = kPrivCH;
   constexpr int HALF = D / 2;
   static_assert(CH == 64, "four warps own 16 keys each");
