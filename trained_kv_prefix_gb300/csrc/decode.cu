@@ -120,6 +120,7 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t base, int row, int dc) {
 template <int D, int QN, int kG>
 __global__ void __launch_bounds__(128) decode_private_kernel(
     const __grid_constant__ CUtensorMap mKs, const __grid_constant__ CUtensorMap mVs,
+    const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mVt,
     DecodeLaunch a, const RopeFreqs f, float scale_log2) {
   using L = PrivSmem<D, QN>;
   constexpr int kPrivStages = L::kPrivStages;
@@ -188,18 +189,34 @@ __global__ void __launch_bounds__(128) decode_private_kernel(
   }
 
   // Stage chunk c into ring slot (c - c0) % kPrivStages (thread 0): the K and
-  // V rows of the chunk by TMA, 64 rows per box (rows past the cache's end
-  // read as zero; rows past the unit's end are whatever the cache holds).
+  // V rows of the chunk by TMA, one 64-row box per 64-dim half, or for the
+  // unit's last, partial chunk 16-row boxes up to its last row (rows past the
+  // cache's end read as zero; rows past the unit's end are whatever the
+  // cache holds).  A 16-row box lands where the 64-row box would put those
+  // rows: the 128-byte swizzle repeats every 8 rows.
   auto stage = [&](int c) {
     if (tid != 0) return;
     const int sl = (c - c0) % kPrivStages;
     uint8_t* sK = smem + sl * L::kStage;
-    mbar_arrive_expect_tx(&full[sl], L::kStage);
     const int row = k_lo + c * CH;
+    const int kn_c = min(CH, nk - c * CH);
+    if (kn_c == CH) {
+      mbar_arrive_expect_tx(&full[sl], L::kStage);
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-      tma_load_4d(sK + h * L::kHalf, &mKs, &full[sl], h * 64, g, row, b);
-      tma_load_4d(sK + L::kTile + h * L::kHalf, &mVs, &full[sl], h * 64, g, row, b);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(sK + h * L::kHalf, &mKs, &full[sl], h * 64, g, row, b);
+        tma_load_4d(sK + L::kTile + h * L::kHalf, &mVs, &full[sl], h * 64, g, row, b);
+      }
+    } else {
+      const int nb = (kn_c + 15) / 16;
+      mbar_arrive_expect_tx(&full[sl], nb * 16 * 128 * (D / 64) * 2);
+      for (int q = 0; q < nb; ++q)
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_4d(sK + h * L::kHalf + q * 2048, &mKt, &full[sl], h * 64, g, row + 16 * q, b);
+          tma_load_4d(sK + L::kTile + h * L::kHalf + q * 2048, &mVt, &full[sl], h * 64, g,
+                      row + 16 * q, b);
+        }
     }
   };
   for (int c = c0; c < c0 + kPrivStages && c < nc; ++c) stage(c);
@@ -486,16 +503,20 @@ cudaError_t launch_private_dq(const DecodeLaunch& a, const RopeFreqs& f, bool de
   using L = PrivSmem<D, QN>;
   cudaError_t e = set_smem_once<decode_private_kernel<D, QN, kG>>(L::kAlloc);
   if (e != cudaSuccess) return e;
-  // private caches [B, rows, Hkv, d] as (d, Hkv, rows, B), a (64, 1, CH, 1) box
-  CUtensorMap mKs, mVs;
+  // private caches [B, rows, Hkv, d] as (d, Hkv, rows, B), (64, 1, CH, 1)
+  // boxes, and (64, 1, 16, 1) boxes for the tails
+  CUtensorMap mKs, mVs, mKt, mVt;
   const uint64_t e2 = 2;
   const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hkv),
                             static_cast<uint64_t>(a.rows), static_cast<uint64_t>(a.B)};
   const uint64_t str[3] = {D * e2, static_cast<uint64_t>(a.Hkv) * D * e2,
                            static_cast<uint64_t>(a.rows) * a.Hkv * D * e2};
   const uint32_t box[4] = {64, 1, static_cast<uint32_t>(kPrivCH), 1};
+  const uint32_t box16[4] = {64, 1, 16, 1};
   if (!make_bf16_map4(&mKs, a.k_cache, dims, str, box) ||
-      !make_bf16_map4(&mVs, a.v_cache, dims, str, box))
+      !make_bf16_map4(&mVs, a.v_cache, dims, str, box) ||
+      !make_bf16_map4(&mKt, a.k_cache, dims, str, box16) ||
+      !make_bf16_map4(&mVt, a.v_cache, dims, str, box16))
     return cudaErrorInvalidValue;
   DecodeLaunch pa = a;
   pa.status = device_status_ptr();
@@ -510,7 +531,7 @@ cudaError_t launch_private_dq(const DecodeLaunch& a, const RopeFreqs& f, bool de
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, QN, kG>, mKs, mVs, pa, f,
+  return cudaLaunchKernelEx(&cfg, decode_private_kernel<D, QN, kG>, mKs, mVs, mKt, mVt, pa, f,
                             scale_log2);
 }
 
