@@ -553,19 +553,30 @@ __global__ void decode_merge_kernel(DecodeLaunch a) {
   const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = a.B * QC, r = vb * G + hh;
   const int Lb = clamp_len(a.len, b, a.rows - a.span + 1);
-  const int S = a.n_cart_splits;
-  // private units from the first one inside the sliding window (u_lo)
-  const int lo0 = a.window > 0 ? Lb - a.window + 1 : 0;
-  const int u_lo = lo0 > 0 ? lo0 / kDecodeUnit : 0;
+  // parts in the sliding window: cartridge splits s_lo .. n_cart_splits - 1
+  // (a split wholly before the row's window may not have been written: the
+  // cartridge pass skips splits no row of its CTA sees), then private units
+  // u_lo .. the last
+  int s_lo = 0, u_lo = 0;
+  if (a.window > 0) {
+    const int lo_c = a.p + Lb + t - a.window + 1;  // first visible key position
+    if (lo_c >= a.p)
+      s_lo = a.n_cart_splits;
+    else if (lo_c > 0 && a.cart_tiles_per_split > 0)
+      s_lo = (lo_c / kTile) / a.cart_tiles_per_split;
+    const int lo0 = Lb - a.window + 1;  // (t = 0: the parts every column shares)
+    u_lo = lo0 > 0 ? lo0 / kDecodeUnit : 0;
+  }
+  const int S = a.n_cart_splits - s_lo;  // cartridge parts of this row
   const int np = S + (Lb + a.span - 1) / kDecodeUnit + 1 - u_lo;
   const long long pbase =
       (static_cast<long long>(b) * a.Hkv + g) * a.max_units * QC + t * G + hh;
   auto part_row = [&](int pt) -> const float* {
-    return pt < S ? a.cart_part + ((static_cast<long long>(pt) * a.Hkv + g) * R + r) * D
+    return pt < S ? a.cart_part + ((static_cast<long long>(s_lo + pt) * a.Hkv + g) * R + r) * D
                   : a.priv_part + (pbase + static_cast<long long>(u_lo + pt - S) * QC) * D;
   };
   auto part_lse = [&](int pt) -> float {
-    return pt < S ? __ldcg(a.cart_lse + (static_cast<long long>(pt) * a.Hkv + g) * R + r)
+    return pt < S ? __ldcg(a.cart_lse + (static_cast<long long>(s_lo + pt) * a.Hkv + g) * R + r)
                   : __ldcg(a.priv_lse + pbase + static_cast<long long>(u_lo + pt - S) * QC);
   };
   constexpr int PL = D / 32;  // dims per lane: 4 or 2

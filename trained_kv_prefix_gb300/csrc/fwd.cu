@@ -30,6 +30,7 @@
 //              publishes S_X(t+1) also certifies that PV_X(t) has finished
 //              reading P_X(t) and writing O_X.
 // TMEM (512 columns): S_A 0-127, S_B 128-255, O_A at 256, O_B at 384.
+#include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -262,6 +263,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (kDecode) {
     ct_lo = split * a.cart_tiles_per_split;
     ct_hi = min(ct_lo + a.cart_tiles_per_split, n_ct_all);
+    if (window > 0) {
+      // skip the tiles before every row's window: the earliest first key of
+      // the CTA's rows is that of a t = 0 row (conversation b's rows are
+      // (b*s + t)*G + hh), position p + len[b] - window + 1
+      __shared__ int s_lo;
+      if (threadIdx.x == 0) s_lo = INT_MAX;
+      __syncthreads();
+      const int r_lo = 2 * pair * kTile, r_hi = min(r_lo + 2 * kTile, a.n_rows);
+      const int b_lo = (r_lo / a.dec_G) / a.dec_s;
+      const int b_hi = min(((r_hi - 1) / a.dec_G) / a.dec_s, a.dec_B / a.dec_s - 1);
+      const int lmax = a.dec_rows - a.dec_s;
+      for (int bb = b_lo + static_cast<int>(threadIdx.x); bb <= b_hi; bb += blockDim.x) {
+        int len = __ldg(a.dec_len + bb);
+        len = len < 0 ? 0 : (len > lmax ? lmax : len);
+        atomicMin(&s_lo, a.p + len - window + 1);
+      }
+      __syncthreads();
+      const int lo = s_lo;
+      if (lo > 0) ct_lo = max(ct_lo, min(lo / kTile, ct_hi));  // none left: T = 0
+    }
   } else {
     const int n_real_tiles = (seq_len + kTile - 1) / kTile;
     n_rt_A = min(2 * pair + 1, n_real_tiles);
