@@ -104,6 +104,21 @@ def test_calls_validate_before_touching_the_device(lib):
         rc = lib.cart_attn_bwd_parts(ctypes.byref(g), 0, 1, al, al, al, al, al, al, al, al, al,
                                      al, al, al, al, lst, cnt, 0, al, 1 << 30, null)
         assert rc == -1
+    # packed segments: no table, a misaligned table, no tokens, more tokens
+    # than B segments of n can hold
+    gp = cartattn.geom(2, 8, 4, 2, 64, 4)
+    odd4 = ctypes.c_void_p(0x1002)
+    for total, cu in ((10, null), (10, odd4), (0, al), (17, al)):
+        rc = lib.cart_attn_fwd_packed(ctypes.byref(gp), total, cu, 0, 1, al, al, al, al, al, al,
+                                      al, al, 1 << 30, null)
+        assert rc in (-1, -2), (total, cu, rc)
+        rc = lib.cart_attn_bwd_packed(ctypes.byref(gp), total, cu, 0, 1, al, al, al, al, al, al,
+                                      al, al, al, al, al, al, al, None, 0, 0, al, 1 << 30, null)
+        assert rc in (-1, -2), (total, cu, rc)
+    assert cartattn.fwd_packed_workspace_size(gp, 0, 0, 1) == 0
+    assert cartattn.fwd_packed_workspace_size(gp, 16, 0, 1) > 0
+    assert cartattn.bwd_packed_workspace_size(gp, 16, 0, 1) > cartattn.fwd_packed_workspace_size(
+        gp, 16, 0, 1)
     # a negative sliding window
     gw = cartattn.geom(1, 8, 4, 2, 64, 4, window=-1)
     rc = lib.cart_attn_fwd(ctypes.byref(gw), 0, 1, al, al, al, al, al, al, al, al, 1 << 30, null)

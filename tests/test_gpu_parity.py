@@ -137,6 +137,27 @@ def test_packed_parity(case):
     gh.check_grads(got, ref, s.frozen_prefix)
 
 
+def test_packed_bad_table_sets_status_bit():
+    """A segment table that breaks its rules (falling, a segment longer than
+    the bound, not ending at the token count) is reported in device status
+    bit 6; the kernels clamp it, so every access stays inside the tensors."""
+    s = _shape("packed_bad", 0, 0, 4, 2, 128, 130, seed=126)
+    inp = synth.packed_inputs(s, (40, 60, 28))
+    g = gh.to_gpu({k: v for k, v in inp.items() if k != "max_seqlen"})
+    cartattn.device_status(clear=True)
+    for bad in ((0, 50, 30, 128), (0, 100, 110, 128), (0, 40, 100, 127)):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        o, lse = cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], cu, 64)
+        cartattn.cart_attn_bwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse, g["do"],
+                                      cu, 64)
+        torch.cuda.synchronize()
+        assert cartattn.device_status(clear=True) == 1 << 6, bad
+    # a good table afterwards: no bit
+    cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], g["cu"], 60)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+
+
 def test_packed_equal_segments_match_the_batch_bitwise():
     """Equal-length packed segments run the same tiles as the [B, n] batch:
     every output is bit for bit the batched call's (the ragged tails read the
