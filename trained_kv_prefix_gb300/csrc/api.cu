@@ -89,6 +89,19 @@ bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_f32_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
+                   const uint64_t (&strides)[3], const uint32_t (&box)[4]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t ss[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t bb[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dd, ss, bb, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

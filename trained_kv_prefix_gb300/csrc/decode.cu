@@ -691,6 +691,18 @@ cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_
     l.scale_log2 = a.scale * 1.4426950408889634f;
     l.out = const_cast<float*>(a.cart_part);
     l.out_f32 = true;
+    // f32 partials [S, Hkv, R, d] as (d, R, Hkv, S): 32 x 32 blocks by TMA
+    CUtensorMap mOd;
+    const int R = a.B * a.span * G;
+    const uint64_t e4 = 4;
+    const uint64_t odims[4] = {static_cast<uint64_t>(a.d), static_cast<uint64_t>(R),
+                               static_cast<uint64_t>(a.Hkv),
+                               static_cast<uint64_t>(a.n_cart_splits)};
+    const uint64_t ostr[3] = {a.d * e4, static_cast<uint64_t>(R) * a.d * e4,
+                              static_cast<uint64_t>(a.Hkv) * R * a.d * e4};
+    const uint32_t obox[4] = {32, 32, 1, 1};
+    if (!make_f32_map4(&mOd, a.cart_part, odims, ostr, obox)) return cudaErrorInvalidValue;
+    l.mO32 = &mOd;
     l.lse = const_cast<float*>(a.cart_lse);
     l.decode = true;
     l.pdl = false;

@@ -50,6 +50,7 @@ struct FwdParams {
   int decode;
   int rotate_q;
   int tma_out;          // training bf16 output: warps store their rows with mO32
+  int tma_dec;          // decode f32 partials: warps store 32 x 32 blocks with mO32
   const float2* table;  // rotate_q: cos/sin rows for positions p .. p + n_rows - 1
   uint32_t* status;
   // decode mode: raw query rows r = b*G + hh, rotated here at p + len[b]
@@ -735,6 +736,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
         }
         __syncwarp();
+        if (kDecode && a.tma_dec) {
+          // the staged 32 x 32 f32 block is the 128-byte-swizzled layout of
+          // the partials map's box: one bulk store (rows past R are clipped)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&mO32, stg, blk * 32, row0, head, split);
+            bulk_commit_group();
+            bulk_wait_read_all();  // the slice is staged again for the next block
+          }
+          __syncwarp();
+          continue;
+        }
         for (int st = 0; st < gpr; ++st) {
           const int gi = st * 32 + lane;
           const int r = gi / gpr, k = gi % gpr;
@@ -755,6 +769,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         __syncwarp();
       }
+      if (kDecode && a.tma_dec && lane == 0) bulk_wait_all();  // writes done before exit
       }
       if (row_ok) {
         const float lse2 = m + __log2f(l);
@@ -801,6 +816,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   p.decode = a.decode ? 1 : 0;
   p.rotate_q = a.rotate_q ? 1 : 0;
   p.tma_out = (!a.decode && !a.out_f32 && a.mO32) ? 1 : 0;
+  p.tma_dec = (a.decode && a.mO32) ? 1 : 0;
   p.table = a.table;
   p.status = device_status_ptr();
   if (a.decode) {
@@ -832,7 +848,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
-                            p.tma_out ? *a.mO32 : *a.mQ, p);
+                            (p.tma_out || p.tma_dec) ? *a.mO32 : *a.mQ, p);
 }
 
 }  // namespace

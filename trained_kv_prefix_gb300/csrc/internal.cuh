@@ -134,6 +134,9 @@ __device__ __forceinline__ long long lse_index(const int* cu, int total, int n, 
 // first, strides in bytes for dims 1..3 (api.cu).
 bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
                     const uint64_t (&strides)[3], const uint32_t (&box)[4]);
+// The same for f32 data (api.cu).
+bool make_f32_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
+                   const uint64_t (&strides)[3], const uint32_t (&box)[4]);
 
 // ----------------------------------------------------------------- misc ----
 // f32 -> bf16 / f32 row copy into a strided destination, for one or two
@@ -180,7 +183,8 @@ struct FwdLaunch {
   const CUtensorMap* mK;   // 4D (d, Hkv, n, B) rotated real keys
   const CUtensorMap* mV;   // 4D (d, Hkv, n, B)
   const CUtensorMap* mO32; // training, bf16 output: 4D (d, Hq, n, B) over o, 64x1x32x1 box
-                           // (each warp stores its 32 rows by TMA); else null
+                           // (each warp stores its 32 rows by TMA); decode: f32
+                           // (d, R, Hkv, S) over the partials, 32x32x1x1 box; or null
   int d;
   int n_rows;              // query rows per query block (n, or B*G for decode)
   int n_qblocks;           // query blocks: B for training, 1 for decode

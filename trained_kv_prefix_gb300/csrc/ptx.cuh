@@ -207,6 +207,11 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until this thread's committed bulk stores have read their
+// shared-memory sources (the global writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA, tcgen05.mma) after this fence.
