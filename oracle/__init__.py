@@ -182,7 +182,7 @@ def _segments(cu_seqlens, total):
 
 
 def fwd_packed(q, k, v, kc, vc, cu_seqlens, *, p=None, frozen_prefix=1, scale=None,
-               theta=1.0e6, window=0):
+               theta=1.0e6, window=0, heads=None):
     """Packed segments (Cartridges guide, "Deliberate divergences from the
     reference", packing bullet; "Batched self-study (measured)", packed
     training step): the group's sequences lie back to back along ONE token
@@ -190,7 +190,8 @@ def fwd_packed(q, k, v, kc, vc, cu_seqlens, *, p=None, frozen_prefix=1, scale=No
     ``cu_seqlens[s] .. cu_seqlens[s+1] - 1``.  RoPE restarts per segment
     (its token i sits at position p + i) and attention runs per segment
     behind the one shared cartridge, so each segment is exactly a
-    single-sequence call of ``fwd``.  Returns ``(o [T, Hq, d], lse [Hq, T])``."""
+    single-sequence call of ``fwd``.  Returns ``(o [T, Hq, d], lse [Hq, T])``
+    (``heads`` restricts the computed heads as in ``fwd``)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     T, Hq, d = q.shape
     o = np.zeros((T, Hq, d))
@@ -199,14 +200,15 @@ def fwd_packed(q, k, v, kc, vc, cu_seqlens, *, p=None, frozen_prefix=1, scale=No
         if b == a:
             continue
         o_s, lse_s = fwd(q[None, a:b], k[None, a:b], v[None, a:b], kc, vc, p=p,
-                         frozen_prefix=frozen_prefix, scale=scale, theta=theta, window=window)
+                         frozen_prefix=frozen_prefix, scale=scale, theta=theta, window=window,
+                         heads=heads)
         o[a:b] = o_s[0]
         lse[:, a:b] = lse_s[0]
     return o, lse
 
 
 def bwd_packed(q, k, v, kc, vc, dout, cu_seqlens, *, p=None, frozen_prefix=1, scale=None,
-               theta=1.0e6, frozen_rows=(), window=0):
+               theta=1.0e6, frozen_rows=(), window=0, kv_heads=None):
     """Gradients of ``sum(dout * o)`` for packed segments (layouts of
     ``fwd_packed``): each segment's dq/dk/dv are those of its own
     single-sequence problem, and the cartridge gradient is their sum over
@@ -222,7 +224,7 @@ def bwd_packed(q, k, v, kc, vc, dout, cu_seqlens, *, p=None, frozen_prefix=1, sc
             continue
         g = bwd(q[None, a:b], k[None, a:b], v[None, a:b], kc, vc, dout[None, a:b], p=p,
                 frozen_prefix=frozen_prefix, scale=scale, theta=theta, frozen_rows=frozen_rows,
-                window=window)
+                window=window, kv_heads=kv_heads)
         dq[a:b], dk[a:b], dv[a:b] = g[0][0], g[1][0], g[2][0]
         dkc += g[3]
         dvc += g[4]

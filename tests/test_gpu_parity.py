@@ -430,6 +430,76 @@ def test_selfstudy_workload_one_group():
                             dkc=(slice(None), slice(0, 1)), dvc=(slice(None), slice(0, 1))))
 
 
+def test_selfstudy_window_one_group():
+    """The self-study workload under a 1024-key window (early queries see
+    half of the cartridge, late ones none of it): kv-head group 0 against the
+    oracle, cartridge gradient included."""
+    s = synth.SELFSTUDY
+    window = 1024
+    inp = synth.train_inputs(s)
+    got = gh.run_train_gpu(s, inp, window=window)
+    G = s.Hq // s.Hkv
+    ref = gh.oracle_train(s, inp, heads=(0, G), kv_heads=(0, 1), window=window)
+    gh.check_fwd(got, ref, sl=(slice(None), slice(None), slice(0, G)),
+                 lse_sl=(slice(None), slice(0, G)))
+    gh.check_grads(got, ref, s.frozen_prefix,
+                   sls=dict(dq=(slice(None), slice(None), slice(0, G)),
+                            dk=(slice(None), slice(None), slice(0, 1)),
+                            dv=(slice(None), slice(None), slice(0, 1)),
+                            dkc=(slice(None), slice(0, 1)), dvc=(slice(None), slice(0, 1))))
+    # rows before the first query's window: exactly zero
+    assert (got["dkc"][:s.p - window + 1] == 0).all()
+
+
+def test_packed_selfstudy_one_group():
+    """Eight packed conversations of up to 1024 tokens with the self-study
+    heads and cartridge: kv-head group 0 against the oracle."""
+    s = synth.SELFSTUDY
+    lens = synth.packed_lengths(s.n, 8, seed=7)
+    inp = synth.packed_inputs(s, lens)
+    g = gh.to_gpu({k: v for k, v in inp.items() if k != "max_seqlen"})
+    n = inp["max_seqlen"]
+    o, lse = cartattn.cart_attn_fwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], g["cu"], n)
+    grads = cartattn.cart_attn_bwd_packed(g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse,
+                                          g["do"], g["cu"], n)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    got = {k: synth.f64(v) for k, v in zip(("o", "lse", "dq", "dk", "dv", "dkc", "dvc"),
+                                           (o, lse, *grads))}
+    a = {k: synth.f64(v) for k, v in inp.items() if k not in ("cu", "max_seqlen")}
+    cu = inp["cu"].numpy()
+    G = s.Hq // s.Hkv
+    ref = dict(zip(("o", "lse"), oracle.fwd_packed(a["q"], a["k"], a["v"], a["kc"], a["vc"], cu,
+                                                   heads=(0, G))))
+    ref.update(zip(("dq", "dk", "dv", "dkc", "dvc"),
+                   oracle.bwd_packed(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["do"], cu,
+                                     kv_heads=(0, 1))))
+    gh.check_fwd(got, ref, sl=(slice(None), slice(0, G)), lse_sl=(slice(0, G),))
+    gh.check_grads(got, ref, s.frozen_prefix,
+                   sls=dict(dq=(slice(None), slice(0, G)), dk=(slice(None), slice(0, 1)),
+                            dv=(slice(None), slice(0, 1)), dkc=(slice(None), slice(0, 1)),
+                            dvc=(slice(None), slice(0, 1))))
+
+
+def test_decode_serving_workload_windowed():
+    """The serving workload with a 512-key window: most conversations see
+    only the last cartridge tiles (the cartridge pass skips the rest)."""
+    s = synth.DECODE
+    inp = synth.decode_inputs(s)
+    g = {k: v.cuda() for k, v in inp.items()}
+    o = cartattn.cart_attn_decode_span(g["q"][:, None], g["k_new"][:, None], g["v_new"][:, None],
+                                       g["kc"], g["vc"], g["k_cache"], g["v_cache"], g["lens"],
+                                       theta=s.theta, window=512)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    a = {k: synth.f64(v) for k, v in inp.items() if k != "lens"}
+    o_ref, _, _ = oracle.decode(a["q"], a["k_new"], a["v_new"], a["kc"], a["vc"], a["k_cache"],
+                                a["v_cache"], inp["lens"].numpy(), theta=s.theta, window=512)
+    o = synth.f64(o[:, 0])
+    assert gh.max_abs(o, o_ref) <= gh.FWD_MAXABS, gh.max_abs(o, o_ref)
+    assert gh.rel_l2(o, o_ref) <= gh.FWD_RELL2, gh.rel_l2(o, o_ref)
+
+
 def test_longctx_workload_sampled():
     """B=1, Hq=64, Hkv=8, d=128, p=8192, n=4096.  Forward rows and the last
     query tile's gradients of kv group 3 against the oracle; the keys of the
