@@ -518,21 +518,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(&bars[kQReady0 + x]);
       } else if (kDecode) {
         // row i = (b*s + t)*G + hh of this kv head: query t of conversation
-        // b's span at position p + len[b] + t
-        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
+        // b's span at position p + len[b] + t.  The length, the position and
+        // the angles of the first 32 pairs come before the Q tile lands.
         const int vb = i / a.dec_G;
-        if (ok && vb < a.dec_B) {
+        const bool live = vb < a.dec_B;
+        int pos = 0;
+        float2 c0[32];
+        if (live) {
           int len = __ldg(a.dec_len + vb / a.dec_s);
           const int lmax = a.dec_rows - a.dec_s;
           len = len < 0 ? 0 : (len > lmax ? lmax : len);
-          const int pos = a.p + len + vb % a.dec_s;
+          pos = a.p + len + vb % a.dec_s;
           if (window > 0) key_lo_dec = pos - window + 1;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) c0[q] = rope_cs_turns_fast(a.turns[q], pos);
+        }
+        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && live) {
           rotate_q_row<D>(smem + L::kQ + x * L::kTileBytes, static_cast<uint32_t>(row),
                           [&](int j0, float2* c) {
 #pragma unroll
                             for (int q = 0; q < 32; ++q)
-                              c[q] = rope_cs_turns_fast(a.turns[j0 + q], pos);
+                              c[q] = j0 == 0 ? c0[q] : rope_cs_turns_fast(a.turns[j0 + q], pos);
                           });
         }
         fence_proxy_async_smem();
