@@ -153,7 +153,10 @@ static_assert(kDkdvBars * 8 + 16 + 4 * kDkdvQSlots <= 256, "dK/dV barrier area")
 // The steps of a key tile in order: a cartridge tile sees every (sequence,
 // head of the group, 128-row query tile), sequence-major; real tile rt of a
 // sequence sees the heads of the group and query tiles rt.. (the causal
-// diagonal and after).  The query tile runs fastest, then the head.
+// diagonal and after).  Under a sliding window only the first qcap query
+// tiles of a sequence can reach the key tile.  The query tile runs fastest,
+// then the head.  (Packed and / or windowed instances; the fixed layout
+// without a window maps a step to its tile in closed form.)
 struct DkdvCursor {
   int b, hh, qt;
   int nq;         // query tiles of sequence b that see the key tile
