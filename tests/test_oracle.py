@@ -554,3 +554,24 @@ def test_windowed_decode_span_is_rows_of_windowed_forward(window):
         of, _ = oracle.fwd(qs, kraw[None, b, :L + span], vraw[None, b, :L + span], kc, vc,
                            rows=(L, L + span), window=window)
         np.testing.assert_allclose(o[b], of[0, L:], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [1, 5, 9])
+def test_packed_window_matches_block_diagonal_windowed_attention(window):
+    """Packed segments under a sliding window: one SDPA over the packed
+    tokens with the block-diagonal mask intersected with the window (key
+    position > query position - W)."""
+    cu, Hq, Hkv, d, p = (0, 5, 5, 12, 13, 20), 4, 2, 16, 6
+    T = cu[-1]
+    P = _problem(100 + window, 1, T, Hq, Hkv, d, p)
+    q, k, v, do = P["q"][0], P["k"][0], P["v"][0], P["do"][0]
+    o, lse = oracle.fwd_packed(q, k, v, P["kc"], P["vc"], cu, window=window)
+    o_t, lse_t = tf.packed_attention(_t(q), _t(k), _t(v), _t(P["kc"]), _t(P["vc"]), cu,
+                                     window=window)
+    np.testing.assert_allclose(o, o_t.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_t.numpy(), rtol=0, atol=1e-12)
+    g = oracle.bwd_packed(q, k, v, P["kc"], P["vc"], do, cu, window=window)
+    g_t = tf.packed_grads(_t(q), _t(k), _t(v), _t(P["kc"]), _t(P["vc"]), _t(do), cu,
+                          window=window)
+    for a, b in zip(g, g_t):
+        np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-11)

@@ -86,7 +86,7 @@ def cartridge_grads(q, k, v, kc, vc, dout, *, frozen_prefix=1, theta=1.0e6, scal
     return q.grad, k.grad, v.grad, dkc, dvc
 
 
-def packed_attention(q, k, v, kc, vc, cu_seqlens, *, theta=1.0e6, scale=None):
+def packed_attention(q, k, v, kc, vc, cu_seqlens, *, theta=1.0e6, scale=None, window=0):
     """Packed segments as ONE attention over the packed token axis: q
     ``[T, Hq, d]``, k/v ``[T, Hkv, d]``, keys = the p cartridge rows then all
     T tokens.  The mask is block diagonal over the segments: token i of
@@ -113,6 +113,9 @@ def packed_attention(q, k, v, kc, vc, cu_seqlens, *, theta=1.0e6, scale=None):
     same = seg[:, None] == seg[None, :]
     causal = local[None, :] <= local[:, None]
     mask = torch.cat([torch.ones(T, p, dtype=torch.bool), same & causal], dim=1)  # [T, p + T]
+    if window > 0:  # positions: cartridge row j at j, token i of a segment at p + i
+        kpos = torch.cat([torch.arange(p), pos])
+        mask = mask & (pos[:, None] - kpos[None, :] < window)
     o = F.scaled_dot_product_attention(qh, K, V, attn_mask=mask, scale=scale)
     logits = torch.matmul(qh, K.transpose(-1, -2)) * scale
     lse = torch.logsumexp(logits.masked_fill(~mask, float("-inf")), dim=-1)
@@ -120,7 +123,7 @@ def packed_attention(q, k, v, kc, vc, cu_seqlens, *, theta=1.0e6, scale=None):
 
 
 def packed_grads(q, k, v, kc, vc, dout, cu_seqlens, *, frozen_prefix=1, theta=1.0e6,
-                 scale=None):
+                 scale=None, window=0):
     """Autograd gradients of sum(dout * o) through ``packed_attention``, the
     sink rows held constant (gradient reported as exactly 0)."""
     q = q.clone().requires_grad_(True)
@@ -130,7 +133,7 @@ def packed_grads(q, k, v, kc, vc, dout, cu_seqlens, *, frozen_prefix=1, theta=1.
     vt = vc[frozen_prefix:].clone().requires_grad_(True)
     o, _ = packed_attention(q, k, v, torch.cat([kc[:frozen_prefix], kt]),
                             torch.cat([vc[:frozen_prefix], vt]), cu_seqlens, theta=theta,
-                            scale=scale)
+                            scale=scale, window=window)
     (o * dout).sum().backward()
     dkc = torch.zeros_like(kc)
     dvc = torch.zeros_like(vc)
