@@ -22,6 +22,11 @@
 //  dq_kernel    one CTA per 128-row query tile: S = Q K^T, dP = dO V^T,
 //               dS = P (dP - D) -> TMEM, dQ += dS K over 128-key steps;
 //               epilogue rotates back by R(p+i)^T.
+// Both kernels have a second instance (kGeneral) for packed segments and /
+// or a sliding window: sequences located through the segment table, key
+// tiles limited to the query tiles' windows and query tiles to the key
+// tiles' windows, per-row / per-key window bounds in the masks, and exact
+// zeros for cartridge tiles no query reaches.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

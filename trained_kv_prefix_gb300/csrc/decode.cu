@@ -22,6 +22,10 @@
 //   merge     combines the cartridge and private parts of every
 //             (conversation, span position, query head) with their
 //             log-sum-exps into o.
+// With a sliding window the cartridge pass starts at the earliest window of
+// its conversations, the private pass skips units and chunks before a
+// conversation's window, and the merge reads only the parts inside its
+// row's window.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

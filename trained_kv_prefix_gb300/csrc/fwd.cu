@@ -30,6 +30,17 @@
 //              publishes S_X(t+1) also certifies that PV_X(t) has finished
 //              reading P_X(t) and writing O_X.
 // TMEM (512 columns): S_A 0-127, S_B 128-255, O_A at 256, O_B at 384.
+//
+// Variants (one kernel instance each, see FwdMode):
+//   packed segments  a sequence's tiles start at its first packed row and
+//                    its own length bounds the tiles, the causal mask and
+//                    the stores (a store that would cross into the next
+//                    segment goes row by row);
+//   sliding window   a CTA starts at the first key tile its tile A's first
+//                    row can see, and each row masks the keys before its
+//                    window (a row that has seen no visible key yet keeps
+//                    P = 0); in decode mode the CTA starts at the earliest
+//                    window among its conversations.
 #include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>
