@@ -178,7 +178,8 @@ def cart_attn_fwd(q, k, v, kc, vc, *, frozen_prefix=1, scale=None, theta=1.0e6, 
                   workspace=None, stream=None, window=0):
     """Training forward.  q ``[B, n, Hq, d]``, k/v ``[B, n, Hkv, d]`` (not
     rotated), kc/vc ``[p, Hkv, d]`` (bf16 shadow or f32 leaves).  Returns
-    ``(o, lse)`` with o like q and lse ``[B, Hq, n]`` f32."""
+    ``(o, lse)`` with o like q and lse ``[B, Hq, n]`` f32.  ``window`` > 0:
+    sliding window in keys over the concatenated sequence (see ``geom``)."""
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
     p = kc.shape[0]
@@ -201,7 +202,8 @@ def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None,
                   workspace=None, stream=None, frozen_rows=None, window=0):
     """Backward.  Returns ``(dq, dk, dv, dkc, dvc)``; dkc/dvc are f32
     ``[p, Hkv, d]`` summed over the batch, rows < frozen_prefix and the rows
-    listed in ``frozen_rows`` (a composed cartridge's part sinks) exactly 0."""
+    listed in ``frozen_rows`` (a composed cartridge's part sinks) exactly 0.
+    ``window`` must match the forward's."""
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
     p = kc.shape[0]
@@ -348,7 +350,8 @@ def cart_attn_decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, sc
     """Span verify: ``span`` new tokens per conversation in one step.  q
     ``[B, span, Hq, d]``, k_new/v_new ``[B, span, Hkv, d]`` (bf16, not
     rotated); the caches receive the span's rows lens[b] .. lens[b]+span-1.
-    Returns o ``[B, span, Hq, d]`` bf16."""
+    Returns o ``[B, span, Hq, d]`` bf16.  ``window`` > 0: token t sees the
+    keys at positions p + lens[b] + t - window + 1 .. p + lens[b] + t."""
     B, span, Hq, d = q.shape
     Hkv = k_new.shape[2]
     p = kc.shape[0]
