@@ -575,3 +575,28 @@ def test_packed_window_matches_block_diagonal_windowed_attention(window):
                           window=window)
     for a, b in zip(g, g_t):
         np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-11)
+
+
+def test_window_pin_catches_an_off_by_one():
+    """Sensitivity of the window pin: a window one key wider (a plausible
+    mistake in the reading of 'the W most recent keys') is caught."""
+    B, n, Hq, Hkv, d, p, W = 1, 7, 4, 2, 8, 9, 5
+    P = _problem(110, B, n, Hq, Hkv, d, p)
+    o_wrong, _ = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], window=W + 1)
+    o_t, _ = tf.cartridge_attention(_t(P["q"]), _t(P["k"]), _t(P["v"]), _t(P["kc"]),
+                                    _t(P["vc"]), window=W)
+    assert np.abs(o_wrong - o_t.numpy()).max() > 1e-3
+
+
+def test_packed_pin_catches_unrestarted_positions():
+    """Sensitivity of the packed pin: running the packed tokens as one
+    sequence (positions not restarted, no segment mask) is caught."""
+    cu, Hq, Hkv, d, p = (0, 5, 12), 4, 2, 16, 6
+    T = cu[-1]
+    P = _problem(111, 1, T, Hq, Hkv, d, p)
+    o_wrong, _ = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"])
+    o_t, _ = tf.packed_attention(_t(P["q"][0]), _t(P["k"][0]), _t(P["v"][0]), _t(P["kc"]),
+                                 _t(P["vc"]), cu)
+    assert np.abs(o_wrong[0, cu[1]:] - o_t.numpy()[cu[1]:]).max() > 1e-3
+    # ... while the first segment, which starts the sequence, agrees
+    np.testing.assert_allclose(o_wrong[0, :cu[1]], o_t.numpy()[:cu[1]], rtol=0, atol=1e-12)
