@@ -600,3 +600,30 @@ def test_packed_pin_catches_unrestarted_positions():
     assert np.abs(o_wrong[0, cu[1]:] - o_t.numpy()[cu[1]:]).max() > 1e-3
     # ... while the first segment, which starts the sequence, agrees
     np.testing.assert_allclose(o_wrong[0, :cu[1]], o_t.numpy()[:cu[1]], rtol=0, atol=1e-12)
+
+
+def test_span_pin_catches_a_shared_position():
+    """Sensitivity of the span pin: placing every span token at p + len
+    (not p + len + t) and letting it see only rows 0 .. len is caught."""
+    B, Hq, Hkv, d, p, span = 1, 4, 2, 16, 9, 3
+    lens = np.array([4], dtype=np.int32)
+    rows = 8
+    rng = np.random.default_rng(112)
+    kc = rng.standard_normal((p, Hkv, d)) * 0.5
+    vc = rng.standard_normal((p, Hkv, d)) * 0.5
+    kraw = rng.standard_normal((B, rows, Hkv, d)) * 0.5
+    vraw = rng.standard_normal((B, rows, Hkv, d)) * 0.5
+    q = rng.standard_normal((B, span, Hq, d)) * 0.5
+    k_cache = np.zeros((B, rows, Hkv, d))
+    v_cache = np.zeros((B, rows, Hkv, d))
+    L = int(lens[0])
+    k_cache[0, :L] = oracle.rope(kraw[0, :L], p)
+    v_cache[0, :L] = vraw[0, :L]
+    qs = np.zeros((1, L + span, Hq, d))
+    qs[0, L:] = q[0]
+    of, _ = oracle.fwd(qs, kraw[None, 0, :L + span], vraw[None, 0, :L + span], kc, vc,
+                       rows=(L, L + span))
+    for t in range(1, span):
+        o_wrong, _, _ = oracle.decode(q[:, t], kraw[:, L + t], vraw[:, L + t], kc, vc, k_cache,
+                                      v_cache, lens)
+        assert np.abs(o_wrong[0] - of[0, L + t]).max() > 1e-3
