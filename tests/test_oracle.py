@@ -627,3 +627,24 @@ def test_span_pin_catches_a_shared_position():
         o_wrong, _, _ = oracle.decode(q[:, t], kraw[:, L + t], vraw[:, L + t], kc, vc, k_cache,
                                       v_cache, lens)
         assert np.abs(o_wrong[0] - of[0, L + t]).max() > 1e-3
+
+
+@pytest.mark.parametrize("name", ["causal_p3", "window4_p3"])
+def test_golden_fixtures(name):
+    """The oracle still reproduces its stored records (written by
+    tests/golden/make_golden.py from the oracle alone)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name + ".json")
+    c = json.load(open(path))
+    g = c["geometry"]
+    P = {k: np.asarray(v, dtype=np.float64) for k, v in c["inputs"].items()}
+    o, lse = oracle.fwd(P["q"], P["k"], P["v"], P["kc"], P["vc"],
+                        frozen_prefix=g["frozen_prefix"], theta=g["theta"], window=g["window"])
+    got = dict(o=o, lse=lse)
+    got.update(zip(("dq", "dk", "dv", "dkc", "dvc"),
+                   oracle.bwd(P["q"], P["k"], P["v"], P["kc"], P["vc"], P["do"],
+                              frozen_prefix=g["frozen_prefix"], theta=g["theta"],
+                              window=g["window"])))
+    for k, v in c["outputs"].items():
+        np.testing.assert_allclose(got[k], np.asarray(v), rtol=0, atol=1e-12, err_msg=k)
