@@ -294,6 +294,16 @@ CART_API const char* cart_status_string(int status);
  * any bit is set, or CART_ERR_CUDA. */
 CART_API int cart_device_status(unsigned* bits_out, int clear);
 
+/* cart_release -- destroys the current device's helper stream and events
+ * (created by the first cart_attn_bwd on that device; see the conventions
+ * above) after waiting for the work queued on that stream.  The next
+ * backward call creates them again.  Call it with no library call in
+ * flight on the device from another host thread.  The library holds no
+ * other per-device state besides the static scratch array of
+ * cart_attn_decode_noalloc, which lives as long as the loaded library.
+ * Returns CART_OK or CART_ERR_CUDA (no usable current device).            */
+CART_API int cart_release(void);
+
 /* ------------------------------------------------------------------------
  * Launch tracing (off by default).  cart_trace_enable(1) clears the trace
  * and starts recording: every later kernel launch of the library is

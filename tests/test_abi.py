@@ -137,6 +137,13 @@ def test_calls_validate_before_touching_the_device(lib):
         assert rc == -1, (span, rows)
 
 
+def test_release_without_a_device_is_a_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.cart_release() == -5
+
+
 def test_no_gpu_here_means_a_cuda_or_device_error(lib):
     """With valid arguments but no usable sm_103 device the call fails loudly
     instead of computing anything elsewhere."""

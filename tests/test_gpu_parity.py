@@ -235,6 +235,18 @@ def test_packed_window_parity():
     gh.check_grads(got, ref, 1)
 
 
+def test_release_then_backward_again():
+    """cart_release drops the helper stream; the next backward recreates it
+    and gives the same bits."""
+    s = _shape("release", 1, 140, 4, 2, 128, 130, seed=127)
+    inp = synth.train_inputs(s)
+    a = gh.run_train_gpu(s, inp)
+    cartattn.release()
+    b = gh.run_train_gpu(s, inp)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
 def test_backward_is_deterministic():
     s = _shape("det", 2, 200, 8, 2, 128, 300, seed=111)
     inp = synth.train_inputs(s)

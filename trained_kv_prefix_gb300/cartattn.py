@@ -91,6 +91,8 @@ def lib():
             L.cart_status_string.restype = ctypes.c_char_p
             L.cart_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
             L.cart_trace_enable.argtypes = [i]
+            L.cart_release.argtypes = []
+            L.cart_release.restype = ctypes.c_int
             L.cart_trace_count.argtypes = []
             L.cart_trace_get.argtypes = [i, ctypes.c_char_p, i, ctypes.POINTER(ctypes.c_float)]
             for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd", "cart_attn_bwd_parts",
@@ -110,7 +112,7 @@ EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd
            "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc",
            "cart_attn_decode_span_workspace_size", "cart_attn_decode_span",
            "cart_attn_fwd_packed_workspace_size", "cart_attn_fwd_packed",
-           "cart_attn_bwd_packed_workspace_size", "cart_attn_bwd_packed")
+           "cart_attn_bwd_packed_workspace_size", "cart_attn_bwd_packed", "cart_release")
 
 
 def _check(fn: str, rc: int):
@@ -370,6 +372,11 @@ def cart_attn_decode_span(q, k_new, v_new, kc, vc, k_cache, v_cache, lens, *, sc
                                      _ptr(ws), ws.numel(), _stream(stream, q.device))
     _check("cart_attn_decode_span", rc)
     return o
+
+
+def release() -> None:
+    """Destroy this device's helper stream and events (recreated on use)."""
+    _check("cart_release", lib().cart_release())
 
 
 def device_status(clear: bool = True) -> int:

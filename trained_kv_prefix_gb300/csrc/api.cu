@@ -115,18 +115,27 @@ struct SideStream {
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 
+SideStream g_side[64];  // per device, created on first use
+std::mutex g_side_mu;
+
+// Destroys what a SideStream holds (callers hold g_side_mu).
+void destroy_side(SideStream& x) {
+  if (x.fork) cudaEventDestroy(x.fork);
+  if (x.join) cudaEventDestroy(x.join);
+  if (x.s) cudaStreamDestroy(x.s);
+  x = SideStream{};
+}
+
 SideStream* side_stream() {
-  static SideStream ss[64];
-  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(mu);
-  SideStream& x = ss[dev];
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream& x = g_side[dev];
   if (!x.s) {
-    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
-      x.s = nullptr;
+      destroy_side(x);
       return nullptr;
     }
   }
@@ -355,6 +364,16 @@ const char* cart_status_string(int s) {
     case CART_ERR_TIMEOUT: return "a kernel gave up waiting";
     default: return "unknown status";
   }
+}
+
+int cart_release(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CART_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream& x = g_side[dev];
+  if (x.s && cudaStreamSynchronize(x.s) != cudaSuccess) return CART_ERR_CUDA;
+  destroy_side(x);
+  return CART_OK;
 }
 
 int cart_device_status(unsigned* bits_out, int clear) {
