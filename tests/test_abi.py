@@ -155,3 +155,50 @@ def test_no_gpu_here_means_a_cuda_or_device_error(lib):
     ws = cartattn.fwd_workspace_size(g, 0, 1)
     rc = lib.cart_attn_fwd(ctypes.byref(g), 0, 1, al, al, al, al, al, al, al, al, ws, None)
     assert rc in (-5, -6)
+
+
+def test_header_is_plain_c99():
+    """The boundary header compiles as C99 (no C++ in the signatures)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-fsyntax-only", "-x", "c", os.path.join(ROOT, "include", "cartattn.h")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_plain_c_host_links_and_calls(lib, tmp_path):
+    """A plain C program links only libcartattn.so and calls the ABI: the
+    status strings and a workspace size (no device needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "host.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "cartattn.h"
+int main(void) {
+  cart_geom g = {2, 256, 8, 2, 128, 64, 1, 0.0883883f, 1.0e6, 0};
+  size_t ws = cart_attn_fwd_workspace_size(&g, CART_BF16, CART_F32);
+  g.window = -1;
+  size_t bad = cart_attn_fwd_workspace_size(&g, CART_BF16, CART_F32);
+  printf("%s|%s|%d|%d\n", cart_status_string(CART_OK), cart_status_string(CART_ERR_WORKSPACE),
+         ws > 0, bad == 0);
+  return 0;
+}
+""")
+    so = cbuild.LIB
+    exe = tmp_path / "host"
+    r = subprocess.run([gcc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                        str(exe), so, "-Wl,-rpath," + os.path.dirname(so)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "ok|workspace too small|1|1"
