@@ -95,3 +95,49 @@ def check_grads(got, ref, frozen, names=("dq", "dk", "dv", "dkc", "dvc"), sls=No
             continue
         assert not np.isnan(y).any(), nme
         assert rel_l2(x, y) <= GRAD_RELL2, (nme, rel_l2(x, y))
+
+
+def oracle_group_parallel(s: synth.TrainShape, inp: dict, g: int, *, chunk_rows: int = 128,
+                          workers: int | None = None):
+    """fp64 oracle for every output of kv-head group ``g`` (its G query heads,
+    every query row), the cartridge gradient of that group included.
+
+    The group is an independent problem with Hq = G and Hkv = 1 (query head h
+    reads kv head h // G), so its inputs are sliced out and the loss
+    sum(dout * o) is split into query-row ranges run on host threads: o, lse
+    and dq of a row come from the range holding it, and the key, value and
+    cartridge gradients are the sums of the ranges' contributions (the loss
+    is a sum over query rows).  The oracle's C code runs without the GIL.
+    Returns arrays shaped like the full problem's outputs restricted to the
+    group (heads g*G .. g*G + G - 1, kv head g)."""
+    import concurrent.futures as cf
+    import os
+
+    G = s.Hq // s.Hkv
+    hs = slice(g * G, (g + 1) * G)
+    a = {k: synth.f64(v) for k, v in inp.items()}
+    q, do = np.ascontiguousarray(a["q"][:, :, hs]), np.ascontiguousarray(a["do"][:, :, hs])
+    k, v = np.ascontiguousarray(a["k"][:, :, g:g + 1]), np.ascontiguousarray(a["v"][:, :, g:g + 1])
+    kc, vc = np.ascontiguousarray(a["kc"][:, g:g + 1]), np.ascontiguousarray(a["vc"][:, g:g + 1])
+    ranges = [(lo, min(lo + chunk_rows, s.n)) for lo in range(0, s.n, chunk_rows)]
+
+    def one(rg):
+        o, lse = oracle.fwd(q, k, v, kc, vc, frozen_prefix=s.frozen_prefix, theta=s.theta,
+                            rows=rg)
+        grads = oracle.bwd(q, k, v, kc, vc, do, frozen_prefix=s.frozen_prefix, theta=s.theta,
+                           rows=rg)
+        return rg, o, lse, grads
+
+    ref = dict(o=np.empty(q.shape), lse=np.empty((s.B, G, s.n)), dq=np.empty(q.shape),
+               dk=np.zeros(k.shape), dv=np.zeros(v.shape), dkc=np.zeros(kc.shape),
+               dvc=np.zeros(vc.shape))
+    with cf.ThreadPoolExecutor(max_workers=workers or os.cpu_count()) as ex:
+        for (lo, hi), o, lse, (dq, dk, dv, dkc, dvc) in ex.map(one, ranges):
+            ref["o"][:, lo:hi] = o[:, lo:hi]
+            ref["lse"][:, :, lo:hi] = lse[:, :, lo:hi]
+            ref["dq"][:, lo:hi] = dq[:, lo:hi]
+            ref["dk"] += dk
+            ref["dv"] += dv
+            ref["dkc"] += dkc
+            ref["dvc"] += dvc
+    return ref

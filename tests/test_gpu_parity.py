@@ -335,6 +335,50 @@ def test_decode_parity_small(s):
     _check_decode(s, inp, o, kc, vc)
 
 
+# Edge cases of the single-token step: kv-head counts 1 to 8, d = 64, p = 0
+# (no cartridge pass), lengths at and around the 256-row unit and 128-row
+# tile edges, one conversation over many units, and NaN in every cache row
+# past a conversation's length (rows a unit or tile reads beyond the length
+# must never reach a product).
+EDGE_DECODE = [
+    (_decode_case("e_hkv8_nan", 5, 32, 8, 128, 200, 800, lens=(0, 15, 16, 17, 700)), True),
+    (_decode_case("e_hkv1_g8_d64", 4, 8, 1, 64, 100, 400, lens=(127, 128, 0, 300)), True),
+    (_decode_case("e_hkv4_g2", 7, 8, 4, 128, 129, 300, lens=(1, 2, 3, 299, 7, 8, 9)), False),
+    (_decode_case("e_hkv2_p0_tiny", 3, 8, 2, 128, 0, 600, lens=(0, 0, 0)), True),
+    (_decode_case("e_long", 2, 32, 8, 128, 4096, 8000, lens=(8000, 3)), False),
+]
+
+
+def _nan_tails(inp):
+    """Private cache rows past each conversation's new row set to NaN."""
+    out = dict(inp)
+    for name in ("k_cache", "v_cache"):
+        t = inp[name].clone()
+        for b, L in enumerate(inp["lens"].tolist()):
+            t[b, L + 1:] = float("nan")
+        out[name] = t
+    return out
+
+
+@pytest.mark.parametrize("case", EDGE_DECODE, ids=[c[0].name for c in EDGE_DECODE])
+def test_decode_edge_parity(case):
+    s, nan_tail = case
+    inp = synth.decode_inputs(s)
+    if nan_tail:
+        inp = _nan_tails(inp)
+    o, kc, vc = _run_decode(s, inp)
+    assert not np.isnan(o).any()
+    _check_decode(s, inp, o, kc, vc)
+
+
+def test_decode_many_small_conversations():
+    """12000 conversations of 1-5 rows each behind a 64-row cartridge."""
+    s = _decode_case("e_many", 12000, 8, 2, 64, 64, 4, seed=201)
+    inp = synth.decode_inputs(s)
+    o, kc, vc = _run_decode(s, inp)
+    _check_decode(s, inp, o, kc, vc)
+
+
 SPAN_CASES = [
     # (case, span): G*span query columns from 4 to 32 (one to four groups of
     # 8); lengths at 0, at the last slot that fits the span, and spans that
@@ -512,25 +556,23 @@ def test_decode_serving_workload_windowed():
     assert gh.rel_l2(o, o_ref) <= gh.FWD_RELL2, gh.rel_l2(o, o_ref)
 
 
-def test_longctx_workload_sampled():
-    """B=1, Hq=64, Hkv=8, d=128, p=8192, n=4096.  Forward rows and the last
-    query tile's gradients of kv group 3 against the oracle; the keys of the
-    last real tile are seen only by that tile's queries, so their dK/dV are
-    exact there.  Cartridge gradients via properties that hold at any size."""
+def test_longctx_workload_one_group():
+    """B=1, Hq=64, Hkv=8, d=128, p=8192, n=4096: every output of kv-head
+    group 3 (query heads 24-31, all 4096 query rows) against the oracle, the
+    p = 8192 cartridge gradient of that group included; then properties that
+    hold for every group."""
     s = synth.LONGCTX
     inp = synth.train_inputs(s)
     got = gh.run_train_gpu(s, inp)
     G = s.Hq // s.Hkv
     g0 = 3
-    lo, hi = s.n - 128, s.n
-    ref = gh.oracle_train(s, inp, heads=(g0 * G, g0 * G + G), rows=(lo, hi),
-                          kv_heads=(g0, g0 + 1), bwd_rows=(lo, hi))
+    ref = gh.oracle_group_parallel(s, inp, g0)
     hs = slice(g0 * G, g0 * G + G)
-    gh.check_fwd(got, ref, sl=(slice(None), slice(lo, hi), hs), lse_sl=(slice(None), hs, slice(lo, hi)))
-    gh.check_grads(got, ref, s.frozen_prefix, names=("dq", "dk", "dv"),
-                   sls=dict(dq=(slice(None), slice(lo, hi), hs),
-                            dk=(slice(None), slice(lo, hi), slice(g0, g0 + 1)),
-                            dv=(slice(None), slice(lo, hi), slice(g0, g0 + 1))))
+    grp = {"o": got["o"][:, :, hs], "lse": got["lse"][:, hs], "dq": got["dq"][:, :, hs],
+           "dk": got["dk"][:, :, g0:g0 + 1], "dv": got["dv"][:, :, g0:g0 + 1],
+           "dkc": got["dkc"][:, g0:g0 + 1], "dvc": got["dvc"][:, g0:g0 + 1]}
+    gh.check_fwd(grp, ref)
+    gh.check_grads(grp, ref, s.frozen_prefix)
     # frozen sink row exactly zero; the other rows do not depend on the freeze
     assert (got["dkc"][0] == 0).all() and (got["dvc"][0] == 0).all()
     unfrozen = gh.run_train_gpu(s, inp, frozen_prefix=0)

@@ -302,6 +302,31 @@ def test_bwd_row_partition_sums_to_full():
         np.testing.assert_allclose(parts[0][t] + parts[1][t], full[t], rtol=0, atol=1e-13)
 
 
+def test_group_parallel_helper_equals_one_oracle_call():
+    """The row-split, group-sliced oracle helper the long-context GPU test
+    uses gives the outputs of one full oracle call restricted to the group."""
+    from tests import gpu_helpers as gh
+    s = synth.TrainShape("grp", B=2, n=37, Hq=8, Hkv=2, d=16, p=11, frozen_prefix=1,
+                         dtype="f32", cart_dtype="f32", seed=44, qkv_std=0.5, do_std=1.0)
+    inp = synth.train_inputs(s)
+    a = {k: synth.f64(v) for k, v in inp.items()}
+    o, lse = oracle.fwd(a["q"], a["k"], a["v"], a["kc"], a["vc"], theta=s.theta)
+    dq, dk, dv, dkc, dvc = oracle.bwd(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["do"],
+                                      theta=s.theta)
+    G = s.Hq // s.Hkv
+    for g in range(s.Hkv):
+        ref = gh.oracle_group_parallel(s, inp, g, chunk_rows=8, workers=3)
+        hs = slice(g * G, (g + 1) * G)
+        np.testing.assert_array_equal(ref["o"], o[:, :, hs])
+        np.testing.assert_array_equal(ref["lse"], lse[:, hs])
+        np.testing.assert_array_equal(ref["dq"], dq[:, :, hs])
+        for name, full in (("dk", dk), ("dv", dv)):
+            np.testing.assert_allclose(ref[name], full[:, :, g:g + 1], rtol=0, atol=1e-12)
+        for name, full in (("dkc", dkc), ("dvc", dvc)):
+            np.testing.assert_allclose(ref[name], full[:, g:g + 1], rtol=0, atol=1e-12)
+        assert (ref["dkc"][0] == 0).all() and (ref["dvc"][0] == 0).all()
+
+
 # -------------------------------------------------------------- decode ----
 def test_decode_is_last_row_of_forward():
     """Decoding behind the cartridge equals the training-time forward of the
