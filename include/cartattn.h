@@ -22,7 +22,13 @@
  *     validate their arguments synchronously on the host, then enqueue work
  *     asynchronously on `stream`; nothing is written when validation fails.
  *   - RoPE is the rotate-half form: element j pairs with j + d/2 at angle
- *     position * theta^(-2j/d); angles are reduced in fp64 on the device.
+ *     position * theta^(-2j/d).  The training entry points form each angle
+ *     in fp64 and reduce it modulo 2*pi in fp64 before an f32 sine/cosine.
+ *     The decode entry points reduce in f32: the frequency in turns is held
+ *     as an f32 (hi, lo) pair, position * hi is split exactly into its
+ *     rounded value and the fma remainder, whole turns are dropped and the
+ *     remaining angle goes to the hardware sine/cosine (absolute error
+ *     about 5e-7); decode positions must stay below 2^24.
  *   - Return value: CART_OK (0) or a negative cart_status.
  *   - The library holds no per-call state.  It caches, per process, the
  *     CUDA driver entry point used to build TMA descriptors and, per device,
