@@ -17,10 +17,15 @@ namespace cart {
 __device__ uint32_t g_device_status;
 
 uint32_t* device_status_ptr() {
-  // One address per device; looked up with that device current.
+  // One address per device, looked up once with that device current.  The
+  // address belongs to the library's module in the device's current context:
+  // after cudaDeviceReset (a new context) the cached address is stale, so a
+  // process that resets a device must not call the library on it again.
+  static std::mutex mu;
   static uint32_t* cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
   if (!cache[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
@@ -46,19 +51,86 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Tensor-map encoding through a small per-process cache.  A map depends only
+// on its arguments (type, base address, sizes, strides, box), so an entry
+// can be reused by any later call with the same arguments; caching takes the
+// driver's encode (microseconds each, several per decode step) off the
+// host's launch path.  Entries are replaced round robin.
+struct MapKey {
+  int dtype, rank;
+  const void* base;
+  uint64_t dims[5], strides[4];
+  uint32_t box[5];
+  bool operator==(const MapKey& o) const {
+    return dtype == o.dtype && rank == o.rank && base == o.base &&
+           std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+           std::memcmp(strides, o.strides, sizeof strides) == 0 &&
+           std::memcmp(box, o.box, sizeof box) == 0;
+  }
+};
+constexpr int kMapCacheSize = 64;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCacheSize];
+  CUtensorMap map[kMapCacheSize];
+  bool used[kMapCacheSize] = {};
+  int next = 0;
+};
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
+bool encode_cached(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
+                   const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+  MapKey k{};
+  k.dtype = static_cast<int>(dtype);
+  k.rank = rank;
+  k.base = base;
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) k.strides[i] = strides[i];
+  MapCache& c = map_cache();
+  {
+    std::lock_guard<std::mutex> lk(c.mu);
+    for (int i = 0; i < kMapCacheSize; ++i)
+      if (c.used[i] && c.key[i] == k) {
+        *m = c.map[i];
+        return true;
+      }
+  }
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dd[5], ss[4];
+  cuuint32_t bb[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    dd[i] = dims[i];
+    bb[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) ss[i] = strides[i];
+  if (fn(m, dtype, rank, const_cast<void*>(base), dd, ss, bb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(c.mu);
+  c.key[c.next] = k;
+  c.map[c.next] = *m;
+  c.used[c.next] = true;
+  c.next = (c.next + 1) % kMapCacheSize;
+  return true;
+}
+
 // 4D bf16 map with a 64 x 1 x rows x 1 box, 128-byte swizzle.  dims innermost
 // first; strides in bytes for dims 1..3.
 bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
               uint64_t d3, uint64_t s1, uint64_t s2, uint64_t s3, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[4] = {d0, d1, d2, d3};
-  cuuint64_t strides[3] = {s1, s2, s3};
-  cuuint32_t box[4] = {64, 1, box_rows, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[4] = {d0, d1, d2, d3};
+  const uint64_t strides[3] = {s1, s2, s3};
+  const uint32_t box[4] = {64, 1, box_rows, 1};
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box);
 }
 
 // [blocks, rows, H, d] bf16 tensor as (d, H, rows, blocks).
@@ -78,28 +150,12 @@ bool make_bf16_rows_map(CUtensorMap* m, const void* base, int blocks, int rows, 
 
 bool make_bf16_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
                     const uint64_t (&strides)[3], const uint32_t (&box)[4]) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dd[4] = {dims[0], dims[1], dims[2], dims[3]};
-  cuuint64_t ss[3] = {strides[0], strides[1], strides[2]};
-  cuuint32_t bb[4] = {box[0], box[1], box[2], box[3]};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dd, ss, bb, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box);
 }
 
 bool make_f32_map4(CUtensorMap* m, const void* base, const uint64_t (&dims)[4],
                    const uint64_t (&strides)[3], const uint32_t (&box)[4]) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dd[4] = {dims[0], dims[1], dims[2], dims[3]};
-  cuuint64_t ss[3] = {strides[0], strides[1], strides[2]};
-  cuuint32_t bb[4] = {box[0], box[1], box[2], box[3]};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dd, ss, bb, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box);
 }
 
 namespace {
@@ -633,14 +689,11 @@ int cart_attn_bwd_packed(const cart_geom* g, int total, const int* cu_seqlens, c
 }
 
 // ------------------------------------------------------------------ decode --
-namespace {
+}  // extern "C"
 
-struct DecodeWs {
-  size_t cart_part = 0, cart_lse = 0, priv_part = 0, priv_lse = 0, total = 0;
-  int splits = 0, tiles_per_split = 0, max_units = 0;
-};
+namespace cart {
 
-DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows, int span = 1) {
+DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows, int span) {
   DecodeWs w;
   const int n_ct = (p + 127) / 128;
   const int R = B * span * (Hq / Hkv);
@@ -669,7 +722,7 @@ DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows, int span = 1)
 }
 
 int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta, int rows,
-                 int span = 1) {
+                 int span) {
   if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || p < 0 || rows < 1)
     return CART_ERR_GEOMETRY;
   const int G = Hq / Hkv;
@@ -686,7 +739,46 @@ int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta
   if (static_cast<long long>(p) + rows >= (1ll << 24)) return CART_ERR_GEOMETRY;
   return CART_OK;
 }
-}  // namespace
+
+int run_decode(int B, int span, int window, int Hq, int Hkv, int d, int p, float scale,
+               double rope_theta, const void* q, const void* k_new, const void* v_new,
+               const void* kc, const void* vc, void* k_cache, void* v_cache, int cache_rows,
+               const int* priv_len, void* o, void* workspace, const DecodeWs& w,
+               cudaStream_t stream) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeLaunch a{};
+  a.span = span;
+  a.window = window;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.p = p;
+  a.rows = cache_rows;
+  a.scale = scale;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.kc = static_cast<const __nv_bfloat16*>(kc);
+  a.vc = static_cast<const __nv_bfloat16*>(vc);
+  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  a.len = priv_len;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.n_cart_splits = w.splits;
+  a.cart_tiles_per_split = w.tiles_per_split;
+  a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
+  a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
+  a.max_units = w.max_units;
+  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
+  a.priv_lse = reinterpret_cast<float*>(ws + w.priv_lse);
+  return launch_decode(a, make_rope_freqs(d, rope_theta), stream) == cudaSuccess ? CART_OK
+                                                                                   : CART_ERR_CUDA;
+}
+
+}  // namespace cart
+
+extern "C" {
 
 size_t cart_attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int p, int cache_rows) {
   return cart_attn_decode_span_workspace_size(B, 1, Hq, Hkv, d, p, cache_rows);
@@ -725,35 +817,9 @@ int cart_attn_decode_span(int B, int span, int window, int Hq, int Hkv, int d, i
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DecodeLaunch a{};
-  a.span = span;
-  a.window = window;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.d = d;
-  a.p = p;
-  a.rows = cache_rows;
-  a.scale = scale;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  a.kc = static_cast<const __nv_bfloat16*>(kc);
-  a.vc = static_cast<const __nv_bfloat16*>(vc);
-  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-  a.len = priv_len;
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.n_cart_splits = w.splits;
-  a.cart_tiles_per_split = w.tiles_per_split;
-  a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
-  a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
-  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
-  a.priv_lse = reinterpret_cast<float*>(ws + w.priv_lse);
-  a.max_units = w.max_units;
-  CART_CUDA(launch_decode(a, make_rope_freqs(d, rope_theta), static_cast<cudaStream_t>(stream)));
-  return CART_OK;
+  return run_decode(B, span, window, Hq, Hkv, d, p, scale, rope_theta, q, k_new, v_new, kc, vc,
+                    k_cache, v_cache, cache_rows, priv_len, o, workspace, w,
+                    static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -23,7 +23,6 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -34,42 +33,11 @@ static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[CART_DEC
 namespace cart {
 namespace {
 
-struct NoallocLayout {
-  size_t cart_part = 0, cart_lse = 0, priv_part = 0, priv_lse = 0, total = 0;
-  int splits = 0, tiles_per_split = 0, max_units = 0;
-};
-
-size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-NoallocLayout layout(int B, int Hq, int Hkv, int d, int p, int rows) {
-  NoallocLayout w;
-  const int n_ct = (p + 127) / 128;
-  const int R = B * (Hq / Hkv);
-  const int qpairs = ((R + 127) / 128 + 1) / 2;  // the cartridge pass takes two row tiles per CTA
-  if (n_ct > 0) {
-    const long long units = static_cast<long long>(n_ct) * Hkv * qpairs;
-    int per = static_cast<int>((units + kDecodeCartCtas - 1) / kDecodeCartCtas);
-    if (per < 1) per = 1;
-    w.tiles_per_split = per;
-    w.splits = (n_ct + per - 1) / per;
-  }
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t o = off;
-    off += up256(bytes);
-    return o;
-  };
-  w.max_units = (rows + kDecodeUnit - 1) / kDecodeUnit;
-  w.cart_part = take(static_cast<size_t>(w.splits) * Hkv * R * d * 4);
-  w.cart_lse = take(static_cast<size_t>(w.splits) * Hkv * R * 4);
-  w.priv_part = take(static_cast<size_t>(B) * Hq * w.max_units * d * 4);
-  w.priv_lse = take(static_cast<size_t>(B) * Hq * w.max_units * 4);
-  w.total = off;
-  return w;
-}
-
 // Device address of the scratch array for the current device, looked up once
-// per device with that device current.
+// per device with that device current.  The address belongs to the library's
+// module in the device's current context: after cudaDeviceReset (a new
+// context) it is stale, so a process that resets a device must not call this
+// entry point on that device again.
 std::mutex g_mu;
 void* g_addr[64] = {};
 
@@ -101,25 +69,18 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
                                                  const void* kc, const void* vc, void* k_cache,
                                                  void* v_cache, int cache_rows,
                                                  const int* priv_len, void* o, void* stream) {
-  // ---- the same argument rules as cart_attn_decode
-  if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || p < 0 || cache_rows < 1)
-    return CART_ERR_GEOMETRY;
-  const int G = Hq / Hkv;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return CART_ERR_GEOMETRY;
-  if (d != 64 && d != 128) return CART_ERR_GEOMETRY;
-  if (!std::isfinite(scale) || !(scale > 0.f) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
-    return CART_ERR_GEOMETRY;
-  if ((static_cast<long long>(B) * G + 127) / 128 > 65535) return CART_ERR_GEOMETRY;
-  if (cache_rows > 32768) return CART_ERR_GEOMETRY;
-  if (static_cast<long long>(p) + cache_rows >= (1ll << 24)) return CART_ERR_GEOMETRY;
+  // ---- the problem must fit the static scratch: checked first, so that a
+  // problem too large for it is refused before anything else is looked at
+  int rc = check_decode(B, Hq, Hkv, d, p, scale, rope_theta, cache_rows);
+  if (rc) return rc;
+  const DecodeWs w = decode_ws(B, Hq, Hkv, d, p, cache_rows);
+  if (w.total > static_cast<size_t>(CART_DECODE_NOALLOC_SCRATCH_BYTES)) return CART_ERR_WORKSPACE;
+  // ---- the same pointer rules as cart_attn_decode
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, o};
   for (const void* ptr : ptrs)
     if (!ptr || !al16(ptr)) return CART_ERR_POINTER;
   if (!priv_len || (reinterpret_cast<uintptr_t>(priv_len) & 3u)) return CART_ERR_POINTER;
   if (p > 0 && (!kc || !vc || !al16(kc) || !al16(vc))) return CART_ERR_POINTER;
-  // ---- the problem must fit the static scratch
-  const NoallocLayout w = layout(B, Hq, Hkv, d, p, cache_rows);
-  if (w.total > static_cast<size_t>(CART_DECODE_NOALLOC_SCRATCH_BYTES)) return CART_ERR_WORKSPACE;
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -127,35 +88,9 @@ extern "C" CART_API int cart_attn_decode_noalloc(int B, int Hq, int Hkv, int d, 
     return CART_ERR_CUDA;
   if (major != 10 || minor != 3) return CART_ERR_DEVICE;
   void* base = nullptr;
-  int rc = scratch_address(&base);
+  rc = scratch_address(&base);
   if (rc) return rc;
-  uint8_t* ws = static_cast<uint8_t*>(base);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  DecodeLaunch a{};
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.d = d;
-  a.p = p;
-  a.rows = cache_rows;
-  a.scale = scale;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  a.kc = static_cast<const __nv_bfloat16*>(kc);
-  a.vc = static_cast<const __nv_bfloat16*>(vc);
-  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
-  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-  a.len = priv_len;
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.n_cart_splits = w.splits;
-  a.cart_tiles_per_split = w.tiles_per_split;
-  a.cart_part = reinterpret_cast<float*>(ws + w.cart_part);
-  a.cart_lse = reinterpret_cast<float*>(ws + w.cart_lse);
-  a.priv_part = reinterpret_cast<float*>(ws + w.priv_part);
-  a.priv_lse = reinterpret_cast<float*>(ws + w.priv_lse);
-  a.max_units = w.max_units;
-  if (launch_decode(a, make_rope_freqs(d, rope_theta), st) != cudaSuccess) return CART_ERR_CUDA;
-  return CART_OK;
+  // the same decode step as cart_attn_decode, its workspace being the array
+  return run_decode(B, 1, 0, Hq, Hkv, d, p, scale, rope_theta, q, k_new, v_new, kc, vc, k_cache,
+                    v_cache, cache_rows, priv_len, o, base, w, static_cast<cudaStream_t>(stream));
 }

@@ -293,4 +293,22 @@ constexpr int kDecodeMaxColumns = 32;  // G * span: query columns of the private
 constexpr int kDecodeCartCtas = 48;
 cudaError_t launch_decode(const DecodeLaunch& a, const RopeFreqs& f, cudaStream_t st);
 
+// Decode workspace layout (api.cu): byte offsets of each part inside the
+// caller's workspace (or the static scratch of the allocation-free entry).
+struct DecodeWs {
+  size_t cart_part = 0, cart_lse = 0, priv_part = 0, priv_lse = 0, total = 0;
+  int splits = 0, tiles_per_split = 0, max_units = 0;
+};
+DecodeWs decode_ws(int B, int Hq, int Hkv, int d, int p, int rows, int span = 1);
+// Host-side argument rules shared by every decode entry point (a cart_status).
+int check_decode(int B, int Hq, int Hkv, int d, int p, float scale, double theta, int rows,
+                 int span = 1);
+// Carves the workspace and enqueues the decode step (arguments already
+// checked); returns a cart_status.
+int run_decode(int B, int span, int window, int Hq, int Hkv, int d, int p, float scale,
+               double rope_theta, const void* q, const void* k_new, const void* v_new,
+               const void* kc, const void* vc, void* k_cache, void* v_cache, int cache_rows,
+               const int* priv_len, void* o, void* workspace, const DecodeWs& w,
+               cudaStream_t stream);
+
 }  // namespace cart
