@@ -16,8 +16,10 @@ training part for B=1, Hq=64, p=8192, n=4096.
 `value` is the training fwd+bwd throughput in algorithmic TFLOP/s (4*d FLOPs
 per visible (query, key) pair forward, 2.5x that backward), summed over
 ranks; the decode throughput (algorithmic HBM GB/s, the shared cartridge
-counted once) is reported under "decode".  L2 is flushed (256 MiB write)
-between timed steps, outside the timed events.
+counted once) is reported under "decode".  L2 is flushed between timed steps,
+outside the timed events: a 256 MiB write, then a 256 MiB read of another
+buffer, so that no dirty line of the flush is written back inside a timed
+kernel (decode.dirty_l2 reports the decode after the write alone).
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of the same workload.
@@ -52,6 +54,14 @@ def parse_args():
     ap.add_argument("--workload", choices=("selfstudy", "longctx"), default="selfstudy")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--workload-steps", type=int, default=10,
+                    help="timed steps of the other training workloads (long-context fwd+bwd, "
+                         "equivalence-gate fwd; 0: skip)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="write profiles/dram_traffic.json from an ncu CSV of DRAM bytes and exit")
+    ap.add_argument("--traffic-steps", type=int, default=1,
+                    help="whole bench steps the --record-traffic capture covers")
+    ap.add_argument("--traffic-command", default="", help="the command that made the capture")
     ap.add_argument("--ext-steps", type=int, default=20,
                     help="timed steps of the packed-training and span-decode lines (0: skip)")
     return ap.parse_args()
@@ -82,21 +92,77 @@ def kernel_src_sha(name: str) -> str:
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """Per-launch DRAM bytes from the committed ncu summary, when it was taken
-    on the current source of that kernel (else None)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
+def ncu_key(name: str):
+    """The bench's kernel key of an ncu kernel name (demangled); the decode
+    step's kernels (the cartridge pass is fwd_kernel in decode mode, template
+    mode 2) all count under "decode"."""
+    m = re.search(r"(\w+_kernel)<([^>]*)>", name)
+    if not m:
         return None
-    sha = kernel_src_sha(kernel)
-    pat = re.compile(r"^\|\s*" + re.escape(kernel) + r"\s*\|\s*" + re.escape(workload) +
-                     r"\s*\|\s*(\d+)\s*\|\s*([0-9a-f]+)\s*\|")
-    with open(path) as f:
-        for line in f:
-            m = pat.match(line.strip())
-            if m and m.group(2) == sha:
-                return int(m.group(1))
-    return None
+    base, targs = m.group(1), [t.strip() for t in m.group(2).split(",")]
+    if base == "fwd_kernel":
+        return "decode" if len(targs) > 1 and targs[1] == "2" else "fwd"
+    return {"dkdv_kernel": "bwd_dkdv", "dq_kernel": "bwd_dq",
+            "decode_private_kernel": "decode", "decode_merge_kernel": "decode"}.get(base)
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` on `workload`, from the data file that
+    `--record-traffic` writes from an ncu capture, when it was taken on the
+    current source of that kernel (else None)."""
+    try:
+        with open(TRAFFIC_JSON) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get("kernels", {}).get(f"{kernel}@{workload}")
+    if not ent or ent.get("src_sha") != kernel_src_sha(kernel):
+        return None
+    return int(ent["bytes"])
+
+
+def record_traffic(csv_path: str, steps: int, workloads: dict, command: str):
+    """Parse an ncu --csv capture of dram__bytes_read.sum and
+    dram__bytes_write.sum covering `steps` whole bench steps and write the
+    per-step DRAM bytes of each bench kernel (summed over its launches in a
+    step) into profiles/dram_traffic.json, with the hash of the sources they
+    were taken on.  `workloads` maps a kernel key to its workload name."""
+    import csv
+    with open(csv_path, newline="") as f:
+        rows = [r for r in csv.reader(f) if r]
+    hdr = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
+    cols = rows[hdr]
+    ki, mi, vi = cols.index("Kernel Name"), cols.index("Metric Name"), cols.index("Metric Value")
+    ui = cols.index("Metric Unit") if "Metric Unit" in cols else None
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024, "MB": 1 << 20,
+             "GB": 1 << 30}
+    tot = {}
+    for r in rows[hdr + 1:]:
+        if len(r) <= max(ki, mi, vi) or not r[mi].startswith("dram__bytes_"):
+            continue
+        key = ncu_key(r[ki])
+        if key is None:
+            continue
+        unit = r[ui] if ui is not None else "byte"
+        tot[key] = tot.get(key, 0.0) + float(r[vi].replace(",", "")) * scale.get(unit, 1)
+    try:
+        with open(TRAFFIC_JSON) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    rec["what"] = ("DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of each bench "
+                   "kernel per step (the decode entry sums the kernels of one decode step), "
+                   "from one ncu capture; bench.py uses an entry while src_sha matches")
+    kern = rec.setdefault("kernels", {})
+    for key, b in tot.items():
+        kern[f"{key}@{workloads.get(key, '')}"] = {
+            "bytes": int(round(b / max(1, steps))), "src_sha": kernel_src_sha(key),
+            "command": command}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(rec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return rec
 
 
 # ----------------------------------------------------------------- clocks ----
@@ -156,6 +222,29 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r["sm"] for r in load),
                 "sm_max_mhz": max(r["smax"] for r in rows), "samples": len(rows),
                 "samples_under_load": len(load), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- L2 flush ----
+class L2Flush:
+    """Between timed steps no input may sit in L2 (129 MB on GB300).  Calling
+    the object writes a 256 MiB buffer (the flush) and then reads a second
+    256 MiB buffer, so that L2 holds clean lines of that buffer: the dirty
+    lines the write leaves behind are written back here, outside the timed
+    region, instead of inside the next timed kernel (where they would cost
+    HBM write bandwidth that belongs to the flush, not to the kernel).
+    `dirty()` is the write alone, for comparison."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.clean_buf = torch.ones(32 << 20, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+        self.sink = self.clean_buf.sum()
+
+    def dirty(self):
+        self.buf.zero_()
 
 
 # ------------------------------------------------------------- accounting ----
@@ -288,12 +377,12 @@ def measure_extensions(args, ts, ds, dev, rank, peaks, flush):
 
     def timed(fn, steps):
         for _ in range(3):
-            flush.zero_()
+            flush()
             fn()
         torch.cuda.synchronize(dev)
         tot = 0.0
         for _ in range(steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -356,16 +445,100 @@ def measure_extensions(args, ts, ds, dev, rank, peaks, flush):
     return out
 
 
-def workload_name(ts):
-    return (f"{ts.name}-train B={ts.B} Hq={ts.Hq} Hkv={ts.Hkv} d={ts.d} p={ts.p} "
-            f"(row 0 frozen) n={ts.n} bf16/f32-leaves + serving-decode B=64 Hq=32 Hkv=8 d=128 "
-            f"p=4096 L~U{{0..1024}}")
+def measure_train_workload(ts, dev, rank, peaks, flush, steps, bwd=True):
+    """One more training workload timed alone: `steps` passes of the
+    cartridge write + forward (+ backward), CUDA events on the launch stream
+    around each pass, L2 flushed outside the events.  Work = 4d FLOPs per
+    visible (query, key) pair forward and 2.5x that backward.  Per-kernel
+    figures come from the library's launch trace over the same passes."""
+    import torch
+    from trained_kv_prefix_gb300 import cartattn, synth
+
+    stream = torch.cuda.current_stream(dev)
+    tin = {k: v.to(dev) for k, v in synth.train_inputs(ts, seed=ts.seed + 1000 * rank).items()}
+    kcb = torch.empty(tin["kc"].shape, dtype=torch.bfloat16, device=dev)
+    vcb = torch.empty_like(kcb)
+    o = torch.empty_like(tin["q"])
+    lse = torch.empty((ts.B, ts.Hq, ts.n), dtype=torch.float32, device=dev)
+    g = cartattn.geom(ts.B, ts.n, ts.Hq, ts.Hkv, ts.d, ts.p, ts.frozen_prefix, None, ts.theta)
+    ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+    grads = None
+    if bwd:
+        grads = dict(dq=torch.empty_like(tin["q"]), dk=torch.empty_like(tin["k"]),
+                     dv=torch.empty_like(tin["v"]),
+                     dkc=torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev),
+                     dvc=torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev))
+        ws_b = torch.empty(cartattn.bwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+
+    def step():
+        cartattn.cart_write_to_cache(tin["kc"], tin["vc"], kcb, vcb)
+        cartattn.cart_attn_fwd(tin["q"], tin["k"], tin["v"], kcb, vcb,
+                               frozen_prefix=ts.frozen_prefix, theta=ts.theta, o=o, lse=lse,
+                               workspace=ws_f)
+        if bwd:
+            cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], kcb, vcb, o, lse, tin["do"],
+                                   frozen_prefix=ts.frozen_prefix, theta=ts.theta,
+                                   workspace=ws_b, **grads)
+
+    for _ in range(3):
+        flush()
+        step()
+    torch.cuda.synchronize(dev)
+    cartattn.trace_read(True)  # drop older records
+    cartattn.trace_enable(True)
+    tot = 0.0
+    for _ in range(steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    cartattn.trace_enable(False)
+    trace = cartattn.trace_read(True)
+    assert cartattn.device_status() == 0
+    ms = tot / steps
+    flops = ts.fwd_flops() + (ts.bwd_flops() if bwd else 0.0)
+    tf = flops / (ms * 1e-3) / 1e12
+    per = {}
+    for name, t in trace:
+        e = per.setdefault(name, [0, 0.0])
+        e[0] += 1
+        e[1] += t
+    kernels = {}
+    for name, (cnt, t) in per.items():
+        ent = {"launches": cnt, "avg_us": round(t / cnt * 1e3, 2)}
+        amt, unit = kernel_work(name, ts, None, None)
+        if amt is not None and unit == "flop":
+            ach = amt / (t / cnt * 1e-3) / 1e12
+            ent.update(achieved=ach, unit="TFLOP/s", frac=ach / peaks["bf16_tflops"])
+        kernels[name] = ent
+    return {"metric": ("fwd+bwd" if bwd else "fwd") + " TFLOP/s", "value": tf, "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "ms_per_step": ms, "steps": steps,
+            "flops_per_step": flops,
+            "config": {"workload": workload_name(ts, decode=False), "B": ts.B, "n": ts.n,
+                       "Hq": ts.Hq, "Hkv": ts.Hkv, "d": ts.d, "cartridge_rows": ts.p,
+                       "pairs_per_head": ts.pairs_per_head()},
+            "kernels": kernels}
+
+
+def workload_name(ts, decode=True):
+    name = (f"{ts.name}-train B={ts.B} Hq={ts.Hq} Hkv={ts.Hkv} d={ts.d} p={ts.p} "
+            f"(row 0 frozen) n={ts.n} bf16/f32-leaves")
+    return name + (" + serving-decode B=64 Hq=32 Hkv=8 d=128 p=4096 L~U{0..1024}" if decode else "")
 
 
 # ------------------------------------------------------------------ ours ----
 def main():
     args = parse_args()
     from trained_kv_prefix_gb300 import synth
+    if args.record_traffic:
+        ts = synth.SELFSTUDY if args.workload == "selfstudy" else synth.LONGCTX
+        wl = {"fwd": ts.name, "bwd_dkdv": ts.name, "bwd_dq": ts.name, "decode": synth.DECODE.name}
+        rec = record_traffic(args.record_traffic, args.traffic_steps, wl, args.traffic_command)
+        print(json.dumps(rec, indent=1))
+        return
     ts = synth.SELFSTUDY if args.workload == "selfstudy" else synth.LONGCTX
     if args.impl == "reference":
         reference_arm(args, ts)
@@ -405,7 +578,7 @@ def main():
     ws_b = torch.empty(cartattn.bwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
     ws_d = torch.empty(cartattn.decode_workspace_size(ds.B, ds.Hq, ds.Hkv, ds.d, ds.p,
                                                       ds.cache_rows), dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def train_part():
@@ -423,7 +596,7 @@ def main():
                                   o=od, workspace=ws_d)
 
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
+        flush()
         train_part()
         decode_part()
     torch.cuda.synchronize(dev)
@@ -438,7 +611,7 @@ def main():
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         for i in range(K):
-            flush.zero_()
+            flush()
             evs[i][0].record(stream)
             train_part()
             evs[i][1].record(stream)
@@ -460,6 +633,22 @@ def main():
     value = world * flops_step * K / (train_ms * 1e-3) / 1e12
     dbytes = decode_bytes(ds, lens)
     dec_gbs = world * dbytes * K / (dec_ms * 1e-3) / 1e9
+
+    # the decode step after a write-only flush (its dirty lines are written
+    # back while the decode reads), for comparison with the headline
+    dirty_ms = 0.0
+    for _ in range(K):
+        flush.dirty()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        decode_part()
+        d1.record(stream)
+        d1.synchronize()
+        dirty_ms += d0.elapsed_time(d1)
+    dirty_ms = cdist.max_over_ranks([dirty_ms], dev)[0]
+    dec_dirty = {"value": world * dbytes * K / (dirty_ms * 1e-3) / 1e9, "unit": "GB/s",
+                 "ms_per_step": dirty_ms / K,
+                 "l2": "256 MiB write between steps, no clean read after it"}
 
     # ---- per-kernel device times from the trace (events on the launch stream)
     per = {}
@@ -565,14 +754,14 @@ def main():
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(args.e2e_steps):
-            flush.zero_()
+            flush()
             dec_e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         dflush = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         dflush[0].record(stream)
         for _ in range(args.e2e_steps):
-            flush.zero_()
+            flush()
         dflush[1].record(stream)
         torch.cuda.synchronize(dev)
         d_ms = max(e0.elapsed_time(e1) - dflush[0].elapsed_time(dflush[1]), 1e-6)
@@ -582,6 +771,16 @@ def main():
                    "d2h_bytes_per_step": od_h.numel() * od_h.element_size()}
 
     ext = measure_extensions(args, ts, ds, dev, rank, peaks, flush) if args.ext_steps > 0 else None
+    more = None
+    if args.workload_steps > 0:
+        other = synth.LONGCTX if ts is synth.SELFSTUDY else synth.SELFSTUDY
+        more = {f"{other.name}_train": measure_train_workload(other, dev, rank, peaks, flush,
+                                                              args.workload_steps),
+                "equiv_fwd": measure_train_workload(synth.EQUIV, dev, rank, peaks, flush,
+                                                    max(args.workload_steps, 20), bwd=False)}
+        more["equiv_fwd"]["config"]["values"] = (
+            "random inputs of the equivalence gate's shapes (the forward's work does not "
+            "depend on the values)")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -596,15 +795,20 @@ def main():
             "config": {"workload": workload_name(ts), "global_batch": ts.B * world,
                        "seq_len": ts.n, "cartridge_rows": ts.p,
                        "decode_conversations": ds.B * world, "parallelism": f"dp{world}",
-                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "l2": ("flushed between timed steps, outside the events: a 256 MiB "
+                              "write, then a 256 MiB read of a second buffer (the write's "
+                              "dirty lines go back to HBM before the timed kernels); "
+                              "decode.dirty_l2 times the decode after the write alone"),
                        "train_ms_per_step": train_ms / K, "decode_ms_per_step": dec_ms / K,
                        "wall_s": round(wall, 3)},
             "roofline": roofline_for(dominant),
             "decode": {"metric": "decode HBM GB/s (shared cartridge counted once)",
                        "value": dec_gbs, "unit": "GB/s", "bytes_per_step": dbytes,
                        "frac": dec_gbs / world / peaks["hbm_gbs"],
-                       "roofline": roofline_for(dec_dom) if dec_dom else None, "e2e": dec_e2e},
+                       "roofline": roofline_for(dec_dom) if dec_dom else None, "e2e": dec_e2e,
+                       "dirty_l2": dec_dirty},
             "extensions": ext,
+            "workloads": more,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,
             "clocks": clk.summary(), "kernels": kernels, "device_status": status,
         }
