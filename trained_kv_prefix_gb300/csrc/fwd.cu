@@ -79,6 +79,14 @@ struct FwdParams {
 
 constexpr int kFwdThreads = 320;
 
+#ifdef CART_TEST_HOOKS
+// Test-hook build only: while nonzero, the MMA warp of the first CTA
+// withholds its commit to tile B's O-done barrier, whose one waiter is tile
+// B's epilogue: that bounded wait runs out, the CTA unwinds through its
+// abort path and the status word gets the epilogue bit alone.
+__device__ int g_test_skip_arrival;
+#endif
+
 template <int D>
 struct FwdSmem {
   static constexpr int kTileBytes = kTile * D * 2;  // one 128-row Q, K or V tile (bf16)
@@ -491,7 +499,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, t);
-          if (t == T_B - 1) umma_commit_w(&bars[kODone1]);
+#ifdef CART_TEST_HOOKS
+          if (t == T_B - 1 && !(blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+                                *reinterpret_cast<volatile int*>(&g_test_skip_arrival)))
+#else
+          if (t == T_B - 1)
+#endif
+            umma_commit_w(&bars[kODone1]);
           if (t + 1 < T_B) issue_qk(1, t + 1);
         }
         umma_commit_w(&bars[kVEmpty0 + s]);
@@ -883,3 +897,12 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
 }
 
 }  // namespace cart
+
+#ifdef CART_TEST_HOOKS
+// Test-hook build only: sets the flag above (0 or 1) on the current device.
+extern "C" CART_API int cart_test_skip_arrival(int on) {
+  return cudaMemcpyToSymbol(cart::g_test_skip_arrival, &on, sizeof on) == cudaSuccess
+             ? CART_OK
+             : CART_ERR_CUDA;
+}
+#endif
