@@ -22,13 +22,14 @@
  *     validate their arguments synchronously on the host, then enqueue work
  *     asynchronously on `stream`; nothing is written when validation fails.
  *   - RoPE is the rotate-half form: element j pairs with j + d/2 at angle
- *     position * theta^(-2j/d).  The training entry points form each angle
- *     in fp64 and reduce it modulo 2*pi in fp64 before an f32 sine/cosine.
- *     The decode entry points reduce in f32: the frequency in turns is held
- *     as an f32 (hi, lo) pair, position * hi is split exactly into its
- *     rounded value and the fma remainder, whole turns are dropped and the
- *     remaining angle goes to the hardware sine/cosine (absolute error
- *     about 5e-7); decode positions must stay below 2^24.
+ *     position * theta^(-2j/d).  Angles are reduced in f32: the frequency
+ *     in turns is held as an f32 (hi, lo) pair, position * hi is split
+ *     exactly into its rounded value and the fma remainder, and whole turns
+ *     are dropped; positions must stay below 2^24.  Training with bf16
+ *     inputs evaluates the remaining fraction with sincospif (absolute
+ *     error about 2e-7), decode with the hardware sine/cosine (about 5e-7).
+ *     Training with f32 inputs forms each angle in fp64 and reduces it
+ *     modulo 2*pi in fp64 before an f32 sine/cosine.
  *   - Return value: CART_OK (0) or a negative cart_status.
  *   - The library holds no per-call state.  It caches, per process, the
  *     CUDA driver entry point used to build TMA descriptors and, per device,
@@ -142,6 +143,31 @@ CART_API int cart_attn_bwd(const cart_geom* g, cart_dtype in_dtype, cart_dtype c
                   const void* o, const float* lse, const void* dout, void* dq, void* dk,
                   void* dv, float* dkc, float* dvc, int accumulate, void* workspace,
                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * cart_attn_bwd_reuse -- cart_attn_bwd that takes the rotated queries and
+ * keys, the RoPE table and the bf16 copies from the workspace of the
+ * forward call that produced o and lse, instead of recomputing them.
+ * (Cartridges guide, "Semantics": the backward of the same attention.)
+ *   fwd_workspace [fwd_workspace_bytes]: the workspace passed to that
+ *        cart_attn_fwd (same geometry, dtypes and inputs), read only; it
+ *        must not have been reused since.  At least
+ *        cart_attn_fwd_workspace_size() bytes, 16-byte aligned.
+ *   workspace: cart_attn_bwd_reuse_workspace_size() bytes (the backward's
+ *        own per-row vectors only).
+ *   Everything else, outputs included, is as in cart_attn_bwd; the results
+ *   are bit-identical to cart_attn_bwd on the same inputs.  The contents of
+ *   fwd_workspace are not checked: a stale one gives wrong gradients.
+ *   Returns CART_ERR_WORKSPACE for a missing or short workspace.         */
+CART_API size_t cart_attn_bwd_reuse_workspace_size(const cart_geom* g, cart_dtype in_dtype,
+                                                   cart_dtype cart_dtype);
+CART_API int cart_attn_bwd_reuse(const cart_geom* g, cart_dtype in_dtype, cart_dtype cart_dtype,
+                                 const void* q, const void* k, const void* v, const void* kc,
+                                 const void* vc, const void* o, const float* lse,
+                                 const void* dout, void* dq, void* dk, void* dv, float* dkc,
+                                 float* dvc, int accumulate, const void* fwd_workspace,
+                                 size_t fwd_workspace_bytes, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * cart_attn_bwd_parts -- cart_attn_bwd for a cartridge composed of several

@@ -1,8 +1,10 @@
 // fwd.cu -- tcgen05 forward of cartridge attention (sm_103a).
 //
-// One CTA owns two 128-row query tiles, A and B, that see the same keys:
+// A work item is two 128-row query tiles, A and B, that see the same keys:
 // consecutive row tiles of one (sequence, head) in training, the two halves
-// of a kv head's stacked decode rows in decode mode.  Both walk the key tiles
+// of a kv head's stacked decode rows in decode mode.  Training CTAs are
+// persistent (one per SM) and take items heaviest first from a counter;
+// a decode CTA runs one item.  Both tiles of an item walk the key tiles
 // of concat(cartridge rows, real tokens) -- first every cartridge tile (all
 // visible), then the real-token tiles up to their diagonal (end-aligned
 // causal mask: real key j is visible from query i iff j <= i; Cartridges
@@ -17,13 +19,15 @@
 //              row, so row maxima and sums need no exchange.  O is rescaled
 //              in TMEM only when the running maximum grows by more than 2^8
 //              (lazy rescaling, log2 domain).  P (bf16 pairs) goes back into
-//              TMEM over the first 64 columns of the tile's S.
-//              With rotate_q the group first applies RoPE to its Q tile in
-//              shared memory (real-token queries at positions p + i); in
-//              decode mode it rotates the raw queries of row (b, hh) at
-//              p + len[b].
-//   warp 8     TMA producer: both Q tiles once, then K and V tiles into two
-//              separate 2-stage rings.
+//              TMEM over the first 64 columns of the tile's S.  Training
+//              queries arrive rotated (the prep kernel applies RoPE); in
+//              decode mode the group rotates the raw queries of row (b, hh)
+//              at p + len[b] in shared memory.  The epilogue stages O in a
+//              4 KB slice per warp of its own.
+//   warp 8     TMA producer: takes the next item, then both Q tiles of the
+//              item (once the previous item's S MMAs have read Q), then K
+//              and V tiles into two separate 2-stage rings that run on
+//              across items.
 //   warp 9     MMA issuer (one thread).  Per key tile t:
 //                PV_A(t), S_A(t+1) = Q_A K(t+1)^T, PV_B(t), S_B(t+1).
 //              One CTA's MMAs run in issue order, so the commit that
@@ -59,11 +63,13 @@ struct FwdParams {
   float* lse;
   int out_f32;
   int decode;
-  int rotate_q;
   int tma_out;          // training bf16 output: warps store their rows with mO32
   int tma_dec;          // decode f32 partials: warps store 32 x 32 blocks with mO32
-  const float2* table;  // rotate_q: cos/sin rows for positions p .. p + n_rows - 1
   uint32_t* status;
+  // training: work items and the counter CTAs take them from (zeroed by the
+  // prep kernel that runs before the forward)
+  int n_items;
+  int* sched;
   // decode mode: raw query rows r = b*G + hh, rotated here at p + len[b]
   const int* dec_len;
   int dec_B, dec_G, dec_rows;
@@ -93,15 +99,23 @@ struct FwdSmem {
   static constexpr int kQ = 0;                      // Q_A, Q_B
   static constexpr int kK = kQ + 2 * kTileBytes;    // K ring, 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;    // V ring, 2 stages
-  static constexpr int kBar = kV + 2 * kTileBytes;
-  static constexpr int kBytes = kBar + 256;         // barriers + TMEM slot
+  static constexpr int kStage = kV + 2 * kTileBytes;  // output staging, 4 KB per softmax warp
+  static constexpr int kBar = kStage + 8 * 4096;   // barriers, TMEM slot
+  static constexpr int kItems = kBar + 256;         // two item slots
+  static constexpr int kBytes = kItems + 128;
   static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-B alignment
 };
 
 enum FwdBar {
   kQFull = 0,  // TMA: both Q tiles landed
-  kQReady0,    // softmax group x: its Q tile is final (rotated if asked); 128 arrivals
+  kQReady0,    // decode, softmax group x: its Q tile is rotated; 128 arrivals
   kQReady1,
+  kQEmpty0,    // the item's last S MMA of tile x has read Q_x (MMA commit)
+  kQEmpty1,
+  kItemFull0,  // the producer published the next item in slot s
+  kItemFull1,
+  kItemEmpty0, // the MMA warp and the 8 softmax warps have read slot s
+  kItemEmpty1,
   kKFull0,
   kKFull1,
   kKEmpty0,
@@ -119,7 +133,7 @@ enum FwdBar {
   kDrain,
   kNumBars
 };
-static_assert(kNumBars * 8 + 4 <= 256, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
 // RoPE of one Q row held in a 128-byte-swizzled tile, in place.
 // cs(j0, c) fills c[0..31] with the (cos, sin) of pairs j0..j0+31.
@@ -168,71 +182,95 @@ __device__ __forceinline__ void rotate_q_row(uint8_t* sQ, uint32_t row, CS cs) {
   }
 }
 
-// Training-forward Q rotation by table rows, one warp per 32 rows of a
-// 128-row tile: the warp takes one row at a time and lane l holds RoPE pairs
-// [l*PPL, (l + 1)*PPL), so each table row is read coalesced (one thread per
-// row would gather a table row per lane) and each row's pair halves are
-// 128-byte shared-memory segments.  Same arithmetic as rope_pair on the
-// table's (cos, sin): the bits equal those of the prep kernel's rotation.
-template <int D>
-struct RopeRowsCoop {
-  static constexpr int PPL = D / 64;  // pairs per lane
-  float2 cs[32][PPL];
-  // (cos, sin) of rows i0 .. i0 + 31 (rows at or past n_rows are skipped)
-  __device__ __forceinline__ void load(const float2* table, int i0, int n_rows, int lane) {
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      if (i0 + r < n_rows) {
-        const float2* t = table + static_cast<long long>(i0 + r) * (D / 2) + lane * PPL;
-        if (PPL == 2) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(t));
-          cs[r][0] = make_float2(v.x, v.y);
-          cs[r][PPL - 1] = make_float2(v.z, v.w);
-        } else {
-          cs[r][0] = __ldg(t);
-        }
-      }
-    }
-  }
-  // rotate tile rows r0 .. r0 + 31 in place (SW128 layout, 64-column chunks
-  // 16 KB apart)
-  __device__ __forceinline__ void apply(uint8_t* sQ, int r0, int i0, int n_rows, int lane) const {
-    const uint32_t base = smem_u32(sQ);
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      if (i0 + r >= n_rows) break;
-      const uint32_t row = static_cast<uint32_t>(r0 + r);
-      if (PPL == 2) {
-        // elements 2l, 2l+1 (chunk 0) and 64+2l, 64+2l+1 (chunk 1)
-        const uint32_t o = sw128_offset(row, static_cast<uint32_t>(lane) >> 2) + (lane & 3) * 4;
-        const float2 a = bf16x2_to_float2(lds_u32(base + o));
-        const float2 b = bf16x2_to_float2(lds_u32(base + 16384u + o));
-        float y0a, y1a, y0b, y1b;
-        rope_pair(a.x, b.x, cs[r][0], y0a, y1a);
-        rope_pair(a.y, b.y, cs[r][PPL - 1], y0b, y1b);
-        sts_u32(base + o, pack_bf16x2(y0a, y0b));
-        sts_u32(base + 16384u + o, pack_bf16x2(y1a, y1b));
-      } else {
-        // element l (16-byte chunk l/8) and l + 32 (chunk 4 + l/8)
-        const uint32_t oa = sw128_offset(row, static_cast<uint32_t>(lane) >> 3) + (lane & 7) * 2;
-        const uint32_t ob = sw128_offset(row, 4u + (static_cast<uint32_t>(lane) >> 3)) + (lane & 7) * 2;
-        const float xa = __uint_as_float(static_cast<uint32_t>(lds_u16(base + oa)) << 16);
-        const float xb = __uint_as_float(static_cast<uint32_t>(lds_u16(base + ob)) << 16);
-        float y0, y1;
-        rope_pair(xa, xb, cs[r][0], y0, y1);
-        const uint32_t pk = pack_bf16x2(y0, y1);
-        sts_u16(base + oa, static_cast<uint16_t>(pk & 0xFFFFu));
-        sts_u16(base + ob, static_cast<uint16_t>(pk >> 16));
-      }
-    }
-  }
-};
-
 enum FwdMode { kFwdTrain = 0, kFwdGeneral = 1, kFwdDecode = 2 };
 
-// kMode: kFwdTrain (training, fixed [B, n] layout, no window), kFwdGeneral
-// (training with packed segments and / or a sliding window) or kFwdDecode
+// One work item: two query tiles A and B that see the same keys, and the key
+// tiles they walk -- cartridge tiles [ct_lo, ct_lo + n_ct), then real tiles
+// from rt_lo up to each tile's diagonal.  T_x tiles for tile x (0: no work).
+struct FwdItem {
+  int head, qb, pair, kvh, split;
+  int seq_len;  // rows of the query block (decode: the stacked rows)
+  SeqRows sq;   // training: where the query block's rows sit
+  int n_ct, ct_lo, rt_lo, T_A, T_B, T;
+  bool hasB;
+};
+
+// An item as the producer publishes it in a shared-memory slot (w < 0: no
+// more items).  The other roles read each field where they use it (volatile
+// loads), so that no item field stays in registers across the softmax loop.
+struct ItemSlot {
+  int w, head, qb, pair, split, seq_len, row0, blk, g0, n_ct, ct_lo, rt_lo, T_A, T_B, T, pad;
+};
+static_assert(sizeof(ItemSlot) == 64, "item slot");
+__device__ __forceinline__ int vld(const int& f) {
+  return *reinterpret_cast<const volatile int*>(&f);
+}
+
+// Tile counts of a pair of query tiles under the causal mask and the window.
+__device__ __forceinline__ void item_tiles(const FwdParams& a, FwdItem& I, int window,
+                                           bool decode) {
+  const int n_qtiles = decode ? a.n_qtiles : (I.seq_len + kTile - 1) / kTile;
+  I.T_A = I.T_B = I.T = I.n_ct = 0;
+  I.rt_lo = 0;
+  I.hasB = false;
+  if (2 * I.pair >= n_qtiles) return;  // a packed segment shorter than the longest
+  I.hasB = 2 * I.pair + 1 < n_qtiles;
+  const int n_ct_all = (a.p + kTile - 1) / kTile;
+  int ct_hi = n_ct_all, n_rt_A = 0, n_rt_B = 0;
+  if (decode) {
+    ct_hi = min((I.split + 1) * a.cart_tiles_per_split, n_ct_all);
+  } else {
+    I.ct_lo = 0;
+    n_rt_A = min(2 * I.pair + 1, n_qtiles);
+    n_rt_B = I.hasB ? min(2 * I.pair + 2, n_qtiles) : 0;
+    if (window > 0) {
+      // the first key any row of tile A sees: position p + q0A - window + 1
+      const int lo = a.p + 2 * I.pair * kTile - window + 1;
+      if (lo > 0) {
+        I.ct_lo = min(lo / kTile, n_ct_all);
+        I.rt_lo = lo > a.p ? (lo - a.p) / kTile : 0;
+      }
+    }
+  }
+  I.n_ct = max(ct_hi - I.ct_lo, 0);
+  I.T_A = I.n_ct + n_rt_A - I.rt_lo;
+  I.T_B = I.hasB ? I.n_ct + n_rt_B - I.rt_lo : 0;
+  I.T = max(I.T_A, I.T_B);
+}
+
+// Training work item w: items are numbered heaviest first (the pair index
+// falls as w grows; every pair of a sequence sees all cartridge tiles and
+// the later pairs more real tiles), so CTAs that take the next free item
+// form a longest-first schedule.
+__device__ __forceinline__ FwdItem train_item(const FwdParams& a, int w, const int* cu,
+                                              int window) {
+  FwdItem I;
+  const int hb = a.Hq_map * a.n_qblocks;
+  I.pair = a.n_pairs - 1 - w / hb;
+  const int rem = w % hb;
+  I.head = rem % a.Hq_map;
+  I.qb = rem / a.Hq_map;
+  I.kvh = I.head / a.G;
+  I.split = 0;
+  I.sq = seq_rows(cu, a.total, a.n_rows, I.qb);
+  I.seq_len = I.sq.len;
+  item_tiles(a, I, window, false);
+  return I;
+}
+
+// kMode: kFwdTrain (training, fixed [B, n] layout, no window, bf16 output),
+// kFwdGeneral (training with packed segments, a sliding window or an f32
+// output) or kFwdDecode
 // (the decode cartridge pass); each mode compiles only its own code.
+//
+// Training CTAs are persistent (one per SM): the producer lane takes the
+// next item from a counter that the prep kernel zeroed, publishes it in a
+// two-slot ring, and every role walks the same item sequence with barrier
+// phases that carry across items.  TMEM is allocated once.  Q of the next
+// item is loaded as soon as the last S MMA of the current one has read its
+// Q tile, and the output is staged in a region of its own, so that the next
+// item's first products overlap the current item's last softmax and its
+// epilogue.  A decode CTA runs its one item (blockIdx) the same way.
 template <int D, int kMode>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
@@ -245,44 +283,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kNumBars * 8);
+  ItemSlot* items = reinterpret_cast<ItemSlot*>(smem + L::kItems);
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // packed training layout: the segment table (a constant null otherwise)
   constexpr bool kDecode = kMode == kFwdDecode;
+  // packed training layout: the segment table (a constant null otherwise)
   const int* const cu = kMode == kFwdGeneral ? a.cu : nullptr;
   const int window = kMode == kFwdTrain ? 0 : a.window;
 
-  // ---- work item (training: heaviest pairs first) ----
-  int head, qb, pair, kvh, split;
-  // tokens of the query block's sequence (decode: the n_rows stacked rows);
-  // its place on the token axis is looked up again where it is used
-  int seq_len = a.n_rows;
-  if (!kDecode) {
-    const int hb = a.Hq_map * a.n_qblocks;
-    pair = a.n_pairs - 1 - static_cast<int>(blockIdx.x) / hb;
-    const int rem = static_cast<int>(blockIdx.x) % hb;
-    head = rem % a.Hq_map;
-    qb = rem / a.Hq_map;
-    kvh = head / a.G;
-    split = 0;
-    seq_len = seq_rows(cu, a.total, a.n_rows, qb).len;
-  } else {
-    head = blockIdx.x;
-    qb = 0;
-    pair = blockIdx.y;
-    kvh = head;
-    split = blockIdx.z;
-  }
-  const int n_qtiles = kDecode ? a.n_qtiles : (seq_len + kTile - 1) / kTile;
-  if (2 * pair >= n_qtiles) return;  // a packed segment shorter than the longest
-  const bool hasB = 2 * pair + 1 < n_qtiles;
-  const int n_ct_all = (a.p + kTile - 1) / kTile;
-  // key tiles: cartridge tiles [ct_lo, ct_hi), then real tiles [rt_lo, n_rt_x)
-  int ct_lo = 0, ct_hi = n_ct_all, rt_lo = 0, n_rt_A = 0, n_rt_B = 0;
+  // ---- decode: this CTA's one item (its window bound needs the block) ----
+  FwdItem dec{};
   if (kDecode) {
-    ct_lo = split * a.cart_tiles_per_split;
-    ct_hi = min(ct_lo + a.cart_tiles_per_split, n_ct_all);
+    dec.head = blockIdx.x;
+    dec.qb = 0;
+    dec.pair = blockIdx.y;
+    dec.kvh = dec.head;
+    dec.split = blockIdx.z;
+    dec.seq_len = a.n_rows;
+    dec.sq = SeqRows{0, 0, 0, a.n_rows};
+    const int n_ct_all = (a.p + kTile - 1) / kTile;
+    dec.ct_lo = dec.split * a.cart_tiles_per_split;
     if (window > 0) {
       // skip the tiles before every row's window: the earliest first key of
       // the CTA's rows is that of a t = 0 row (conversation b's rows are
@@ -290,7 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __shared__ int s_lo;
       if (threadIdx.x == 0) s_lo = INT_MAX;
       __syncthreads();
-      const int r_lo = 2 * pair * kTile, r_hi = min(r_lo + 2 * kTile, a.n_rows);
+      const int r_lo = 2 * dec.pair * kTile, r_hi = min(r_lo + 2 * kTile, a.n_rows);
       const int b_lo = (r_lo / a.dec_G) / a.dec_s;
       const int b_hi = min(((r_hi - 1) / a.dec_G) / a.dec_s, a.dec_B / a.dec_s - 1);
       const int lmax = a.dec_rows - a.dec_s;
@@ -301,34 +322,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       __syncthreads();
       const int lo = s_lo;
-      if (lo > 0) ct_lo = max(ct_lo, min(lo / kTile, ct_hi));  // none left: T = 0
+      const int ct_hi = min(dec.ct_lo + a.cart_tiles_per_split, n_ct_all);
+      if (lo > 0) dec.ct_lo = max(dec.ct_lo, min(lo / kTile, ct_hi));  // none left: T = 0
     }
-  } else {
-    const int n_real_tiles = (seq_len + kTile - 1) / kTile;
-    n_rt_A = min(2 * pair + 1, n_real_tiles);
-    n_rt_B = hasB ? min(2 * pair + 2, n_real_tiles) : 0;
-    if (window > 0) {
-      // the first key any row of tile A sees: position p + q0A - window + 1
-      const int lo = a.p + 2 * pair * kTile - window + 1;
-      if (lo > 0) {
-        ct_lo = min(lo / kTile, n_ct_all);
-        rt_lo = lo > a.p ? (lo - a.p) / kTile : 0;
-      }
-    }
+    item_tiles(a, dec, window, true);
   }
-  const int n_ct = max(ct_hi - ct_lo, 0);
-  const int T_A = n_ct + n_rt_A - rt_lo;
-  const int T_B = hasB ? n_ct + n_rt_B - rt_lo : 0;
-  const int T = max(T_A, T_B);
 
   if (threadIdx.x == 0) {
-    // decode mode: let the dependent private pass start right away (one of
-    // its CTAs waits for this grid before that grid completes)
+    // decode mode: let the dependent private pass start right away (it waits
+    // for this grid before it reads what this grid writes)
     if (kDecode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kQReady0 + s], 128);
+      mbar_init(&bars[kQEmpty0 + s], 1);
       mbar_init(&bars[kKFull0 + s], 1);
       mbar_init(&bars[kKEmpty0 + s], 1);
       mbar_init(&bars[kVFull0 + s], 1);
@@ -336,6 +344,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars[kSFull0 + s], 1);
       mbar_init(&bars[kPFull0 + s], 128);
       mbar_init(&bars[kODone0 + s], 1);
+      mbar_init(&bars[kItemFull0 + s], 1);
+      mbar_init(&bars[kItemEmpty0 + s], 9);  // the MMA warp and the 8 softmax warps
     }
     mbar_init(&bars[kDrain], 1);
     fence_mbar_init();
@@ -352,66 +362,115 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0 && T > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mKc);
       tma_prefetch_desc(&mVc);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
-      const int q0A = 2 * pair * kTile;
-      const SeqRows sq = seq_rows(cu, a.total, a.n_rows, qb);  // training only
-      mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        // tile B of a lone last tile reads rows past the end: zero fill
-        if (kDecode) {  // (d, G, Hkv, B) map, 128/G conversations per box
-          tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, 0, kvh,
-                      q0A / a.dec_G);
-          tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, 0,
-                      kvh, (q0A + kTile) / a.dec_G);
-        } else {
-          tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, head, sq.row0 + q0A,
-                      sq.blk);
-          tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64, head,
-                      sq.row0 + q0A + kTile, sq.blk);
-        }
-      }
+      // the next item: decode has one; training takes the counter's next
+      auto fetch = [&](int k) -> int {
+        if (kDecode) return k == 0 ? 0 : -1;
+        const int w = atomicAdd(a.sched, 1);
+        return w < a.n_items ? w : -1;
+      };
+      int g = 0;           // K / V tiles issued, over all items
+      int nq = 0;          // Q loads issued (items with work)
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
-        const int s = t & 1;
-        const bool cart = t < n_ct;
-        const int row0 = cart ? (ct_lo + t) * kTile : sq.row0 + (rt_lo + t - n_ct) * kTile;
-        const CUtensorMap* mk = cart ? &mKc : &mK;
-        const CUtensorMap* mv = cart ? &mVc : &mV;
-        const int blk = cart ? 0 : sq.blk;
-        if (t >= 2) {
-          ok = mbar_wait(&bars[kKEmpty0 + s], ((t >> 1) - 1) & 1, abort_s, a.status,
+      int w = fetch(0);
+      for (int it = 0; ok; ++it) {
+        const int sl = it & 1;
+        if (it >= 2) {
+          ok = mbar_wait(&bars[kItemEmpty0 + sl], ((it >> 1) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
-        uint8_t* sK = smem + L::kK + s * L::kTileBytes;
-        mbar_arrive_expect_tx(&bars[kKFull0 + s], L::kTileBytes);
+        FwdItem I{};
+        if (w >= 0) I = kDecode ? dec : train_item(a, w, cu, window);
+        ItemSlot& o = items[sl];
+        o.w = w;
+        o.head = I.head;
+        o.qb = I.qb;
+        o.pair = I.pair;
+        o.split = I.split;
+        o.seq_len = I.seq_len;
+        o.row0 = I.sq.row0;
+        o.blk = I.sq.blk;
+        o.g0 = I.sq.g0;
+        o.n_ct = I.n_ct;
+        o.ct_lo = I.ct_lo;
+        o.rt_lo = I.rt_lo;
+        o.T_A = I.T_A;
+        o.T_B = I.T_B;
+        o.T = I.T;
+        mbar_arrive(&bars[kItemFull0 + sl]);  // (release: the slot is visible to the waiters)
+        if (w < 0) break;
+        const int w_next = fetch(it + 1);
+        if (I.T > 0) {
+          // Q of this item once every S MMA of the previous one has read Q
+          if (nq >= 1) {
+            ok = mbar_wait(&bars[kQEmpty0], (nq - 1) & 1, abort_s, a.status, kDevErrTimeoutTma) &&
+                 mbar_wait(&bars[kQEmpty1], (nq - 1) & 1, abort_s, a.status, kDevErrTimeoutTma);
+            if (!ok) break;
+          }
+          const int q0A = 2 * I.pair * kTile;
+          mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(sK + h * 16384, mk, &bars[kKFull0 + s], h * 64, kvh, row0, blk);
-        k_issued = t + 1;
-        if (t >= 2) {
-          ok = mbar_wait(&bars[kVEmpty0 + s], ((t >> 1) - 1) & 1, abort_s, a.status,
-                         kDevErrTimeoutTma);
-          if (!ok) break;
+          for (int h = 0; h < D / 64; ++h) {
+            // tile B of a lone last tile reads rows past the end: zero fill
+            if (kDecode) {  // (d, G, Hkv, B) map, 128/G conversations per box
+              tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, 0, I.kvh,
+                          q0A / a.dec_G);
+              tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64,
+                          0, I.kvh, (q0A + kTile) / a.dec_G);
+            } else {
+              tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, I.head,
+                          I.sq.row0 + q0A, I.sq.blk);
+              tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64,
+                          I.head, I.sq.row0 + q0A + kTile, I.sq.blk);
+            }
+          }
+          ++nq;
+          for (int t = 0; t < I.T && ok; ++t, ++g) {
+            const int s = g & 1;
+            const bool cart = t < I.n_ct;
+            const int row0 =
+                cart ? (I.ct_lo + t) * kTile : I.sq.row0 + (I.rt_lo + t - I.n_ct) * kTile;
+            const CUtensorMap* mk = cart ? &mKc : &mK;
+            const CUtensorMap* mv = cart ? &mVc : &mV;
+            const int blk = cart ? 0 : I.sq.blk;
+            if (g >= 2) {
+              ok = mbar_wait(&bars[kKEmpty0 + s], ((g >> 1) - 1) & 1, abort_s, a.status,
+                             kDevErrTimeoutTma);
+              if (!ok) break;
+            }
+            uint8_t* sK = smem + L::kK + s * L::kTileBytes;
+            mbar_arrive_expect_tx(&bars[kKFull0 + s], L::kTileBytes);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_4d(sK + h * 16384, mk, &bars[kKFull0 + s], h * 64, I.kvh, row0, blk);
+            k_issued = g + 1;
+            if (g >= 2) {
+              ok = mbar_wait(&bars[kVEmpty0 + s], ((g >> 1) - 1) & 1, abort_s, a.status,
+                             kDevErrTimeoutTma);
+              if (!ok) break;
+            }
+            uint8_t* sV = smem + L::kV + s * L::kTileBytes;
+            mbar_arrive_expect_tx(&bars[kVFull0 + s], L::kTileBytes);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_4d(sV + h * 16384, mv, &bars[kVFull0 + s], h * 64, I.kvh, row0, blk);
+            v_issued = g + 1;
+          }
         }
-        uint8_t* sV = smem + L::kV + s * L::kTileBytes;
-        mbar_arrive_expect_tx(&bars[kVFull0 + s], L::kTileBytes);
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(sV + h * 16384, mv, &bars[kVFull0 + s], h * 64, kvh, row0, blk);
-        v_issued = t + 1;
+        w = w_next;
       }
       if (!ok) {
-        // Give the copies already in flight a bounded chance to land before
-        // the CTA releases its shared memory.
-        mbar_wait(&bars[kQFull], 0, 0u, nullptr, 0);
+        // Give the copies still in flight (the last Q load, the last two K
+        // and V tiles) a bounded chance to land before the CTA releases its
+        // shared memory.
+        if (nq > 0) mbar_wait(&bars[kQFull], (nq - 1) & 1, 0u, nullptr, 0);
         for (int t = max(k_issued - 2, 0); t < k_issued; ++t)
           mbar_wait(&bars[kKFull0 + (t & 1)], (t >> 1) & 1, 0u, nullptr, 0);
         for (int t = max(v_issued - 2, 0); t < v_issued; ++t)
@@ -423,125 +482,158 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ----------------------------------------------------------------- MMA --
     // The whole warp runs this loop (warp-uniform descriptors); one elected
     // lane issues each MMA and commit.
-    if (T > 0) {
-      auto wait = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu,
-                          mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
-      };
-      const uint32_t idS = idesc_bf16(128, 128, false, false);
-      const uint32_t idPV = idesc_bf16(128, D, false, true);
-      // Base descriptors, computed once; each MMA adds an offset.
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + L::kQ), 16u, 1024u);
-      const uint64_t dQ1 = desc_add(dQ0, L::kTileBytes);
-      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);
-      const uint64_t dK1 = desc_add(dK0, L::kTileBytes);
-      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + L::kV), 16384u, 1024u);
-      const uint64_t dV1 = desc_add(dV0, L::kTileBytes);
-      // S_x = Q_x K(t)^T (K-major operands; K step k of 16 at byte offset
-      // (k/4)*16384 + (k%4)*32 within the two 64-wide blocks)
-      auto issue_qk = [&](int x, int t) {
-        const uint64_t dq = x ? dQ1 : dQ0;
-        const uint64_t dk = (t & 1) ? dK1 : dK0;
-        const uint32_t ts = tmem + x * 128;
-        umma_bf16_ss_w(ts, dq, dk, idS, 0u);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu,
+                        mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
+    };
+    const uint32_t idS = idesc_bf16(128, 128, false, false);
+    const uint32_t idPV = idesc_bf16(128, D, false, true);
+    // Base descriptors, computed once; each MMA adds an offset.
+    const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + L::kQ), 16u, 1024u);
+    const uint64_t dQ1 = desc_add(dQ0, L::kTileBytes);
+    const uint64_t dK0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);
+    const uint64_t dK1 = desc_add(dK0, L::kTileBytes);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(smem + L::kV), 16384u, 1024u);
+    const uint64_t dV1 = desc_add(dV0, L::kTileBytes);
+    // S_x = Q_x K^T from ring slot s (K-major operands; K step k of 16 at
+    // byte offset (k/4)*16384 + (k%4)*32 within the two 64-wide blocks)
+    auto issue_qk = [&](int x, int s) {
+      const uint64_t dq = x ? dQ1 : dQ0;
+      const uint64_t dk = s ? dK1 : dK0;
+      const uint32_t ts = tmem + x * 128;
+      umma_bf16_ss_w(ts, dq, dk, idS, 0u);
 #pragma unroll
-        for (int k = 1; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss_w(ts, desc_add(dq, off), desc_add(dk, off), idS, 1u);
-        }
-        umma_commit_w(&bars[kSFull0 + x]);
-      };
-      // O_x += P_x V(t): P from TMEM (K step k of 16 keys = 8 packed columns
-      // at 8k), V MN-major (16 rows = 2048 B per K step).
-      auto issue_pv = [&](int x, int t) {
-        const uint64_t dv = (t & 1) ? dV1 : dV0;
-        const uint32_t tp = tmem + x * 128;
-        const uint32_t to = tmem + 256 + x * 128;
-        umma_bf16_ts_w(to, tp, dv, idPV, t > 0 ? 1u : 0u);
+      for (int k = 1; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        umma_bf16_ss_w(ts, desc_add(dq, off), desc_add(dk, off), idS, 1u);
+      }
+      umma_commit_w(&bars[kSFull0 + x]);
+    };
+    // O_x (+)= P_x V from ring slot s: P from TMEM (K step k of 16 keys = 8
+    // packed columns at 8k), V MN-major (16 rows = 2048 B per K step).
+    auto issue_pv = [&](int x, int s, bool acc) {
+      const uint64_t dv = s ? dV1 : dV0;
+      const uint32_t tp = tmem + x * 128;
+      const uint32_t to = tmem + 256 + x * 128;
+      umma_bf16_ts_w(to, tp, dv, idPV, acc ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < kTile / 16; ++k)
-          umma_bf16_ts_w(to, tp + k * 8, desc_add(dv, k * 2048), idPV, 1u);
-      };
-      bool ok = wait(&bars[kQReady0], 0) &&
-                wait(&bars[kKFull0], 0);
+      for (int k = 1; k < kTile / 16; ++k)
+        umma_bf16_ts_w(to, tp + k * 8, desc_add(dv, k * 2048), idPV, 1u);
+    };
+    int g = 0;             // K / V tiles consumed, over all items
+    int nq = 0;            // Q loads consumed
+    int nP0 = 0, nP1 = 0;  // P tiles of A / B consumed, over all items
+    bool ok = true;
+    for (int it = 0; ok && (!kDecode || it < 1); ++it) {
+      ok = wait(&bars[kItemFull0 + (it & 1)], (it >> 1) & 1);
+      if (!ok) break;
+      const ItemSlot& sI = items[it & 1];
+      const int w = vld(sI.w);
+      const int TA = vld(sI.T_A), TB = vld(sI.T_B), T = vld(sI.T);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + (it & 1)]);  // read all it needs
+      if (w < 0) break;
+      if (T == 0) continue;
+      ok = kDecode ? wait(&bars[kQReady0], 0) : wait(&bars[kQFull], nq & 1);
+      ok = ok && wait(&bars[kKFull0 + (g & 1)], (g >> 1) & 1);
       if (ok) {
         tc_fence_after();
-        issue_qk(0, 0);
+        issue_qk(0, g & 1);
+        if (TA == 1) umma_commit_w(&bars[kQEmpty0]);
       }
-      if (ok && hasB) {
-        ok = wait(&bars[kQReady1], 0);
+      if (ok && TB > 0) {
+        if (kDecode) ok = wait(&bars[kQReady1], 0);
         if (ok) {
           tc_fence_after();
-          issue_qk(1, 0);
+          issue_qk(1, g & 1);
+          if (TB == 1) umma_commit_w(&bars[kQEmpty1]);
         }
       }
-      if (ok) umma_commit_w(&bars[kKEmpty0]);
+      if (ok && TB == 0) umma_commit_w(&bars[kQEmpty1]);  // no MMA reads Q_B
+      if (ok) umma_commit_w(&bars[kKEmpty0 + (g & 1)]);
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t & 1;
-        ok = wait(&bars[kVFull0 + s], (t >> 1) & 1);
+        const int gt = g + t, s = gt & 1;
+        ok = wait(&bars[kVFull0 + s], (gt >> 1) & 1);
         if (!ok) break;
         const bool next = t + 1 < T;
-        if (t < T_A) {
-          ok = wait(&bars[kPFull0], t & 1);
+        if (t < TA) {
+          ok = wait(&bars[kPFull0], (nP0 + t) & 1);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, t);
-          if (t == T_A - 1) umma_commit_w(&bars[kODone0]);
+          issue_pv(0, s, t > 0);
+          if (t == TA - 1) umma_commit_w(&bars[kODone0]);
         }
         if (next) {
-          ok = wait(&bars[kKFull0 + (s ^ 1)], ((t + 1) >> 1) & 1);
+          ok = wait(&bars[kKFull0 + (s ^ 1)], ((gt + 1) >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          if (t + 1 < T_A) issue_qk(0, t + 1);
+          if (t + 1 < TA) {
+            issue_qk(0, s ^ 1);
+            if (t + 1 == TA - 1) umma_commit_w(&bars[kQEmpty0]);
+          }
         }
-        if (t < T_B) {
-          ok = wait(&bars[kPFull1], t & 1);
+        if (t < TB) {
+          ok = wait(&bars[kPFull1], (nP1 + t) & 1);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(1, t);
+          issue_pv(1, s, t > 0);
 #ifdef CART_TEST_HOOKS
-          if (t == T_B - 1 && !(blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
-                                *reinterpret_cast<volatile int*>(&g_test_skip_arrival)))
+          if (t == TB - 1 && !(blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+                               *reinterpret_cast<volatile int*>(&g_test_skip_arrival)))
 #else
-          if (t == T_B - 1)
+          if (t == TB - 1)
 #endif
             umma_commit_w(&bars[kODone1]);
-          if (t + 1 < T_B) issue_qk(1, t + 1);
+          if (t + 1 < TB) {
+            issue_qk(1, s ^ 1);
+            if (t + 1 == TB - 1) umma_commit_w(&bars[kQEmpty1]);
+          }
         }
         umma_commit_w(&bars[kVEmpty0 + s]);
         if (next) umma_commit_w(&bars[kKEmpty0 + (s ^ 1)]);
       }
-      // Drain: every MMA issued above completes before the CTA tears down.
-      umma_commit_w(&bars[kDrain]);
-      mbar_wait(&bars[kDrain], 0, 0u, nullptr, 0);
+      g += T;
+      ++nq;
+      nP0 += TA;
+      nP1 += TB;
     }
+    // Drain: every MMA issued above completes before the CTA tears down.
+    umma_commit_w(&bars[kDrain]);
+    mbar_wait(&bars[kDrain], 0, 0u, nullptr, 0);
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax --
     const int x = warp >> 2;  // 0: tile A, 1: tile B
-    const int Tx = x ? T_B : T_A;
     const int row = threadIdx.x & 127;  // == TMEM lane
-    const int i = (2 * pair + x) * kTile + row;  // query row within its block
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + x * 128 + lane_off;
     const uint32_t tO = tmem + 256 + x * 128 + lane_off;
-    float m = -INFINITY, l = 0.f;
-    bool ok = Tx > 0;
-    // decode: position of the row's first visible key (window > 0)
-    int key_lo_dec = 0;
-    if (ok) {
-      if (a.rotate_q) {
-        // this warp's 32 rows: table rows fetched while the Q tile lands
-        const int r0 = (warp & 3) * 32;
-        const int i0 = (2 * pair + x) * kTile + r0;
-        RopeRowsCoop<D> rr;
-        rr.load(a.table, i0, seq_len, lane);
-        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) rr.apply(smem + L::kQ + x * L::kTileBytes, r0, i0, seq_len, lane);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[kQReady0 + x]);
-      } else if (kDecode) {
+    // this warp's output staging slice (32 rows x 128 bytes)
+    uint8_t* const stg = smem + L::kStage + warp * 4096;
+    int nS = 0;  // S tiles of this tile x consumed, over all items
+    int nO = 0;  // items of tile x finished
+    bool ok = true;
+    // (a decode CTA has one item: the loop ends without reading the end mark)
+    for (int it = 0; ok && (!kDecode || it < 1); ++it) {
+      ok = mbar_wait(&bars[kItemFull0 + (it & 1)], (it >> 1) & 1, abort_s, a.status,
+                     kDevErrTimeoutSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // the slot is released once the item's epilogue is done with it
+      const ItemSlot& sI = items[it & 1];
+      if (vld(sI.w) < 0) break;
+      const int Tx = x ? vld(sI.T_B) : vld(sI.T_A);
+      if (Tx == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + (it & 1)]);
+        continue;
+      }
+      const int i = (2 * vld(sI.pair) + x) * kTile + row;  // query row within its block
+      const int seq_len = vld(sI.seq_len);
+      float m = -INFINITY, l = 0.f;
+      // decode: position of the row's first visible key (window > 0)
+      int key_lo_dec = 0;
+      if (kDecode) {
         // row i = (b*s + t)*G + hh of this kv head: query t of conversation
         // b's span at position p + len[b] + t.  The length, the position and
         // the angles of the first 32 pairs come before the Q tile lands.
@@ -570,249 +662,245 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[kQReady0 + x]);
-      } else {
-        // the MMA thread waits on kQReady only: forward the TMA completion
-        ok = mbar_wait(&bars[kQFull], 0, abort_s, a.status, kDevErrTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        mbar_arrive(&bars[kQReady0 + x]);
+        if (!ok) break;
       }
-    }
-    const int i_cap = min(i, seq_len - 1);  // decode: no real keys, unused
-    for (int t = 0; t < Tx && ok; ++t) {
-      ok = mbar_wait(&bars[kSFull0 + x], t & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
-      ok = __all_sync(0xffffffffu, ok);
+      const int i_cap = min(i, seq_len - 1);  // decode: no real keys, unused
+      // the item's key tiles (kept in registers for the tile loop)
+      const int n_ct = vld(sI.n_ct), ct_lo = vld(sI.ct_lo), rt_lo = vld(sI.rt_lo);
+      for (int t = 0; t < Tx && ok; ++t) {
+        ok = mbar_wait(&bars[kSFull0 + x], (nS + t) & 1, abort_s, a.status,
+                       kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[4][32];
+        tmem_ld32(tS, r[0]);
+        tmem_ld32(tS + 32, r[1]);
+        tmem_ld32(tS + 64, r[2]);
+        tmem_ld32(tS + 96, r[3]);
+        tmem_ld_wait();
+        tmem_reg_fence(r[0]);
+        tmem_reg_fence(r[1]);
+        tmem_reg_fence(r[2]);
+        tmem_reg_fence(r[3]);
+        // number of visible keys of this tile (leading columns)
+        // and the first one (sliding window); key positions of this tile
+        // start at kpos0
+        const int kpos0 =
+            t < n_ct ? (ct_lo + t) * kTile : a.p + (rt_lo + t - n_ct) * kTile;
+        int valid = t < n_ct ? a.p - kpos0 : i_cap - (kpos0 - a.p) + 1;
+        valid = max(0, min(valid, kTile));
+        int first = 0;
+        if (window > 0) {
+          const int key_lo = kDecode ? key_lo_dec : a.p + i - window + 1;
+          first = max(0, min(key_lo - kpos0, kTile));
+        }
+        if (__any_sync(0xffffffffu, valid < kTile || first > 0)) {
+#pragma unroll
+          for (int c = 0; c < kTile; ++c)
+            if (c >= valid || c < first) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        }
+        // row maximum of the raw scores (scale_log2 > 0), 4 independent
+        // chains of three-input maxima
+        float mx[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v = fmax3(__uint_as_float(r[q][0]), __uint_as_float(r[q][1]),
+                          __uint_as_float(r[q][2]));
+#pragma unroll
+          for (int c = 3; c < 31; c += 2)
+            v = fmax3(v, __uint_as_float(r[q][c]), __uint_as_float(r[q][c + 1]));
+          mx[q] = fmaxf(v, __uint_as_float(r[q][31]));
+        }
+        const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+        // Lazy rescaling: keep the stale max unless the new one exceeds it
+        // by more than 8 (P values then stay below 2^8, safe in bf16 / f32).
+        float alpha = 1.f;
+        bool rescale = false;
+        if (rmax > m + 8.f) {
+          alpha = exp2_approx(m - rmax);  // exp2(-inf) = 0 on the first tile
+          m = rmax;
+          rescale = t > 0;
+        }
+        // P = 2^(S * scale * log2(e) - m), two keys per packed two-lane op
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        // (a row that has seen no visible key yet keeps m = -inf: P = 0)
+        const float mr = (kMode != kFwdTrain && m == -INFINITY) ? 0.f : m;
+        const float2 nm2 = make_float2(-mr, -mr);
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float2 x0 = __ffma2_rn(u2f2(r[q][2 * c], r[q][2 * c + 1]), sc2, nm2);
+            const float2 p01 = make_float2(exp2_approx(x0.x), exp2_approx(x0.y));
+            rs[c & 3] = __fadd2_rn(rs[c & 3], p01);
+            pk[c] = pack_bf16x2(p01.x, p01.y);
+          }
+          // keys 32q .. 32q + 31 -> packed columns 16q .. 16q + 15 (S of
+          // the whole row is already in registers)
+          tmem_st16(tS + 16 * q, pk);
+        }
+        const float2 rs01 = __fadd2_rn(rs[0], rs[1]), rs23 = __fadd2_rn(rs[2], rs[3]);
+        l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
+        if (__any_sync(0xffffffffu, rescale)) {
+          // PV(t-1) has completed: the commit that published S(t) follows it.
+#pragma unroll
+          for (int blk = 0; blk < D / 32; ++blk) {
+            uint32_t o[32];
+            tmem_ld32(tO + blk * 32, o);
+            tmem_ld_wait();
+            tmem_reg_fence(o);
+            const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 v = __fmul2_rn(u2f2(o[c], o[c + 1]), al2);
+              o[c] = __float_as_uint(v.x);
+              o[c + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + blk * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kPFull0 + x]);
+      }
+      nS += Tx;
+      // ---------------------------------------------------------- epilogue --
+      if (ok) {
+        ok = mbar_wait(&bars[kODone0 + x], nO & 1, abort_s, a.status, kDevErrTimeoutEpilogue);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      ++nO;
       if (!ok) break;
       tc_fence_after();
-      uint32_t r[4][32];
-      tmem_ld32(tS, r[0]);
-      tmem_ld32(tS + 32, r[1]);
-      tmem_ld32(tS + 64, r[2]);
-      tmem_ld32(tS + 96, r[3]);
-      tmem_ld_wait();
-      tmem_reg_fence(r[0]);
-      tmem_reg_fence(r[1]);
-      tmem_reg_fence(r[2]);
-      tmem_reg_fence(r[3]);
-      // number of visible keys of this tile (leading columns)
-      // and the first one (sliding window); key positions of this tile start
-      // at kpos0
-      const int kpos0 = t < n_ct ? (ct_lo + t) * kTile : a.p + (rt_lo + t - n_ct) * kTile;
-      int valid = t < n_ct ? a.p - kpos0 : i_cap - (kpos0 - a.p) + 1;
-      valid = max(0, min(valid, kTile));
-      int first = 0;
-      if (window > 0) {
-        const int key_lo = kDecode ? key_lo_dec : a.p + i - window + 1;
-        first = max(0, min(key_lo - kpos0, kTile));
-      }
-      if (__any_sync(0xffffffffu, valid < kTile || first > 0)) {
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c >= valid || c < first) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-      }
-      // row maximum of the raw scores (scale_log2 > 0), 4 independent chains
-      // of three-input maxima
-      float mx[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v = fmax3(__uint_as_float(r[q][0]), __uint_as_float(r[q][1]),
-                        __uint_as_float(r[q][2]));
-#pragma unroll
-        for (int c = 3; c < 31; c += 2)
-          v = fmax3(v, __uint_as_float(r[q][c]), __uint_as_float(r[q][c + 1]));
-        mx[q] = fmaxf(v, __uint_as_float(r[q][31]));
-      }
-      const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-      // Lazy rescaling: keep the stale max unless the new one exceeds it by
-      // more than 8 (P values then stay below 2^8, safe in bf16 / f32).
-      float alpha = 1.f;
-      bool rescale = false;
-      if (rmax > m + 8.f) {
-        alpha = exp2_approx(m - rmax);  // exp2(-inf) = 0 on the first tile
-        m = rmax;
-        rescale = t > 0;
-      }
-      // P = 2^(S * scale * log2(e) - m), two keys per packed two-lane op
-      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-      // (a row that has seen no visible key yet keeps m = -inf: P = 0)
-      const float mr = (kMode != kFwdTrain && m == -INFINITY) ? 0.f : m;
-      const float2 nm2 = make_float2(-mr, -mr);
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int q = 0; q < 4; q += 2) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float2 x0 = __ffma2_rn(u2f2(r[q][2 * c], r[q][2 * c + 1]), sc2, nm2);
-          const float2 x1 = __ffma2_rn(u2f2(r[q + 1][2 * c], r[q + 1][2 * c + 1]), sc2, nm2);
-          const float2 p01 = make_float2(exp2_approx(x0.x), exp2_approx(x0.y));
-          const float2 p23 = make_float2(exp2_approx(x1.x), exp2_approx(x1.y));
-          rs[(c & 1) * 2] = __fadd2_rn(rs[(c & 1) * 2], p01);
-          rs[(c & 1) * 2 + 1] = __fadd2_rn(rs[(c & 1) * 2 + 1], p23);
-          pk[c] = pack_bf16x2(p01.x, p01.y);
-          pk[16 + c] = pack_bf16x2(p23.x, p23.y);
-        }
-        // keys 32q .. 32q + 63 -> packed columns 16q .. 16q + 31
-        tmem_st32(tS + 16 * q, pk);
-      }
-      const float2 rs01 = __fadd2_rn(rs[0], rs[1]), rs23 = __fadd2_rn(rs[2], rs[3]);
-      l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
-      if (__any_sync(0xffffffffu, rescale)) {
-        // PV(t-1) has completed: the commit that published S(t) follows it.
-#pragma unroll
-        for (int blk = 0; blk < D / 32; ++blk) {
-          uint32_t o[32];
-          tmem_ld32(tO + blk * 32, o);
-          tmem_ld_wait();
-          tmem_reg_fence(o);
-          const float2 al2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 v = __fmul2_rn(u2f2(o[c], o[c + 1]), al2);
-            o[c] = __float_as_uint(v.x);
-            o[c + 1] = __float_as_uint(v.y);
-          }
-          tmem_st32(tO + blk * 32, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[kPFull0 + x]);
-    }
-    // ------------------------------------------------------------ epilogue --
-    if (ok) {
-      ok = mbar_wait(&bars[kODone0 + x], 0, abort_s, a.status, kDevErrTimeoutEpilogue);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
+      // (once this thread has read O from TMEM, the next item's first PV may
+      // overwrite it: its P-ready arrival for that item comes later)
       // a decode split may hold none of a windowed row's keys: O = 0
       const float inv_l = (kMode == kFwdTrain || l > 0.f) ? 1.f / l : 0.f;
       const bool row_ok = i < seq_len;
       const bool f32 = kDecode || a.out_f32;
-      const SeqRows sq = kDecode ? SeqRows{0, 0, 0, a.n_rows}
-                                  : seq_rows(cu, a.total, a.n_rows, qb);
+      const int head = vld(sI.head), split = vld(sI.split);
+      const SeqRows sq = {vld(sI.row0), vld(sI.blk), vld(sI.g0), seq_len};
+      const int wr0 = (2 * vld(sI.pair) + x) * kTile + (warp & 3) * 32;
       // a packed segment's last rows: a TMA store of the warp's 32 rows would
       // run into the next segment, so those warps store row by row
-      const int wr0 = (2 * pair + x) * kTile + (warp & 3) * 32;
-      const bool use_tma = a.tma_out && (!cu || wr0 + 32 <= sq.len ||
-                                         sq.row0 + sq.len == a.total);
+      // (the fixed-layout training instance always has a bf16 output map)
+      const bool use_tma =
+          kMode == kFwdTrain ||
+          (a.tma_out && (!cu || wr0 + 32 <= sq.len || sq.row0 + sq.len == a.total));
       if (use_tma) {
-        // bf16 output by TMA: every thread writes its row into its tile's Q
-        // buffer (every MMA that read Q_x is done) in the 128-byte-swizzled
-        // layout of the output map's box, then lane 0 stores the warp's 32
-        // rows (rows past n are clipped by the map).
-        uint8_t* sO = smem + L::kQ + x * L::kTileBytes;
-        const uint32_t base = smem_u32(sO);
+        // bf16 output by TMA, 64 columns at a time: every thread writes its
+        // row into the warp's slice in the 128-byte-swizzled layout of the
+        // output map's 64 x 32 box, then lane 0 stores the box (rows past n
+        // are clipped by the map) and waits until the slice has been read.
+        const uint32_t base = smem_u32(stg);
+        // every column block of O in flight at once, one wait
         uint32_t ob[D / 32][32];
 #pragma unroll
         for (int blk = 0; blk < D / 32; ++blk) tmem_ld32(tO + blk * 32, ob[blk]);
         tmem_ld_wait();
 #pragma unroll
-        for (int blk = 0; blk < D / 32; ++blk) {
-          tmem_reg_fence(ob[blk]);
-          // columns 32*blk.. = 64-wide block blk/2, 16-byte chunks 4*(blk%2)..
+        for (int blk = 0; blk < D / 32; ++blk) tmem_reg_fence(ob[blk]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t* o = ob[blk] + 8 * k;
-            sts_u4(base + (blk >> 1) * 16384 + sw128_offset(row, 4 * (blk & 1) + k),
+        for (int h = 0; h < D / 64; ++h) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t* o = ob[2 * h + (k >> 2)] + 8 * (k & 3);
+            sts_u4(base + sw128_offset(static_cast<uint32_t>(lane), static_cast<uint32_t>(k)),
                    make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l),
                               pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l),
                               pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l),
                               pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l)));
           }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int h = 0; h < D / 64; ++h)
-            tma_store_4d(&mO32, sO + h * 16384 + (warp & 3) * 4096, h * 64, head, sq.row0 + wr0,
-                         sq.blk);
-          bulk_commit_group();
-          bulk_wait_all();
-        }
-        __syncwarp();
-      } else {
-      // Each warp turns its 32 rows x 32 columns at a time around through a
-      // 4 KB slice of its tile's Q buffer (every MMA that read Q_x is done),
-      // so that global stores cover whole 32-byte sectors: 16-byte granule
-      // k of staged row r sits at r*128 + (k ^ (r & 7))*16.
-      uint8_t* stg = smem + L::kQ + x * L::kTileBytes + (warp & 3) * 4096;
-      const int gpr = f32 ? 8 : 4;  // 16-byte granules per row and 32 columns
-      const int row0 = (2 * pair + x) * kTile + (warp & 3) * 32;
-      // every column block of O in flight at once, one wait
-      uint32_t ob[D / 32][32];
-#pragma unroll
-      for (int blk = 0; blk < D / 32; ++blk) tmem_ld32(tO + blk * 32, ob[blk]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int blk = 0; blk < D / 32; ++blk) tmem_reg_fence(ob[blk]);
-#pragma unroll
-      for (int blk = 0; blk < D / 32; ++blk) {
-        const uint32_t* o = ob[blk];
-        uint8_t* my = stg + lane * 128;
-        if (f32) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4*>(my + ((k ^ (lane & 7)) << 4)) =
-                make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                            __uint_as_float(o[4 * k + 2]) * inv_l,
-                            __uint_as_float(o[4 * k + 3]) * inv_l);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(my + ((k ^ (lane & 7)) << 4)) = make_uint4(
-                pack_bf16x2(__uint_as_float(o[8 * k]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
-        }
-        __syncwarp();
-        if (kDecode && a.tma_dec) {
-          // the staged 32 x 32 f32 block is the 128-byte-swizzled layout of
-          // the partials map's box: one bulk store (rows past R are clipped)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_4d(&mO32, stg, blk * 32, row0, head, split);
+            tma_store_4d(&mO32, stg, h * 64, head, sq.row0 + wr0, sq.blk);
             bulk_commit_group();
-            bulk_wait_read_all();  // the slice is staged again for the next block
+            bulk_wait_read_all();
           }
           __syncwarp();
-          continue;
         }
-        for (int st = 0; st < gpr; ++st) {
-          const int gi = st * 32 + lane;
-          const int r = gi / gpr, k = gi % gpr;
-          const int grow = row0 + r;
-          if (grow < sq.len) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
-            long long off;  // element offset of the row
-            if (kDecode)
-              off = ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + grow) * D;
-            else
-              off = ((static_cast<long long>(sq.g0) + grow) * a.Hq_map + head) * D;
-            if (f32)
-              *reinterpret_cast<uint4*>(static_cast<float*>(a.out) + off + blk * 32 + k * 4) = v;
-            else
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off + blk * 32 + k * 8) =
-                  v;
+      } else {
+        // Each warp turns its 32 rows x 32 columns at a time around through
+        // its slice, so that global stores cover whole 32-byte sectors:
+        // 16-byte granule k of staged row r sits at r*128 + (k ^ (r & 7))*16.
+        // O is read one 32-column block at a time (few registers live).
+        const int gpr = f32 ? 8 : 4;  // 16-byte granules per row and 32 columns
+#pragma unroll 1
+        for (int blk = 0; blk < D / 32; ++blk) {
+          uint32_t o[32];
+          tmem_ld32(tO + blk * 32, o);
+          tmem_ld_wait();
+          tmem_reg_fence(o);
+          uint8_t* my = stg + lane * 128;
+          if (f32) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(my + ((k ^ (lane & 7)) << 4)) = make_float4(
+                  __uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                  __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<uint4*>(my + ((k ^ (lane & 7)) << 4)) = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[8 * k]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
           }
+          __syncwarp();
+          if (kDecode && a.tma_dec) {
+            // the staged 32 x 32 f32 block is the 128-byte-swizzled layout
+            // of the partials map's box: one bulk store (rows past R are
+            // clipped)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_4d(&mO32, stg, blk * 32, wr0, head, split);
+              bulk_commit_group();
+              bulk_wait_read_all();  // the slice is staged again for the next block
+            }
+            __syncwarp();
+            continue;
+          }
+          for (int st = 0; st < gpr; ++st) {
+            const int gi = st * 32 + lane;
+            const int r = gi / gpr, k = gi % gpr;
+            const int grow = wr0 + r;
+            if (grow < sq.len) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((k ^ (r & 7)) << 4));
+              long long off;  // element offset of the row
+              if (kDecode)
+                off = ((static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + grow) * D;
+              else
+                off = ((static_cast<long long>(sq.g0) + grow) * a.Hq_map + head) * D;
+              if (f32)
+                *reinterpret_cast<uint4*>(static_cast<float*>(a.out) + off + blk * 32 + k * 4) = v;
+              else
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off + blk * 32 +
+                                          k * 8) = v;
+            }
+          }
+          __syncwarp();
         }
-        __syncwarp();
-      }
-      if (kDecode && a.tma_dec && lane == 0) bulk_wait_all();  // writes done before exit
       }
       if (row_ok) {
         const float lse2 = m + __log2f(l);
         if (kDecode)
           a.lse[(static_cast<long long>(split) * a.Hq_map + head) * a.n_rows + i] = lse2;
         else
-          a.lse[lse_index(cu, a.total, a.n_rows, a.Hq_map, qb, head, sq, i)] =
+          a.lse[lse_index(cu, a.total, a.n_rows, a.Hq_map, vld(sI.qb), head, sq, i)] =
               lse2 * 0.69314718055994531f;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + (it & 1)]);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's stores are done before exit
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -825,7 +913,8 @@ template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdSmem<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  const bool general = !a.decode && (a.cu || a.window > 0);
+  // kFwdTrain: fixed layout, no window, bf16 output stored by TMA
+  const bool general = !a.decode && (a.cu || a.window > 0 || a.out_f32 || !a.mO32);
   auto* kern = a.decode ? fwd_kernel<D, kFwdDecode>
                         : (general ? fwd_kernel<D, kFwdGeneral> : fwd_kernel<D, kFwdTrain>);
   cudaError_t e = a.decode ? set_smem_once<fwd_kernel<D, kFwdDecode>>(L::kAlloc)
@@ -847,11 +936,11 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   p.lse = a.lse;
   p.out_f32 = a.out_f32 ? 1 : 0;
   p.decode = a.decode ? 1 : 0;
-  p.rotate_q = a.rotate_q ? 1 : 0;
   p.tma_out = (!a.decode && !a.out_f32 && a.mO32) ? 1 : 0;
   p.tma_dec = (a.decode && a.mO32) ? 1 : 0;
-  p.table = a.table;
   p.status = device_status_ptr();
+  p.n_items = p.n_pairs * a.Hq_map * a.n_qblocks;
+  p.sched = a.sched;
   if (a.decode) {
     p.dec_len = a.dec_len;
     p.dec_B = a.dec_B;
@@ -865,10 +954,14 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   }
   p.window = a.window;
   dim3 grid;
-  if (!a.decode)
-    grid = dim3(static_cast<unsigned>(p.n_pairs) * a.Hq_map * a.n_qblocks, 1, 1);
-  else
+  if (!a.decode) {
+    // persistent: one CTA per SM, none idle from the start
+    const int nsm = sm_count();
+    if (nsm < 1) return cudaErrorInvalidValue;
+    grid = dim3(static_cast<unsigned>(p.n_items < nsm ? p.n_items : nsm), 1, 1);
+  } else {
     grid = dim3(a.Hq_map, p.n_pairs, a.n_splits);
+  }
   TraceScope tr(a.decode ? nullptr : "fwd", st);  // decode: traced as one step
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -887,7 +980,7 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
-  if (a.rotate_q && (a.decode || !a.table)) return cudaErrorInvalidValue;
+  if (!a.decode && !a.sched) return cudaErrorInvalidValue;
   if (a.decode && (!a.dec_len || !a.freqs || a.dec_G < 1 || kTile % a.dec_G != 0 ||
                    a.dec_s < 1 || a.dec_B % a.dec_s != 0))
     return cudaErrorInvalidValue;

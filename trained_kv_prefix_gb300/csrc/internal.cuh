@@ -145,21 +145,28 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
                                   int p, int row_elems, long long row_stride, int dst_row0,
                                   bool dst_bf16, cudaStream_t st);
 
-// bf16 training inputs, one launch: RoPE table rows for positions p..p+n-1,
-// K rotated into kr, Q into qr (if qr), and with o given the backward's
+// bf16 training inputs, one launch: RoPE table rows for positions p..p+n-1
+// (if table), K rotated into kr (if kr), Q into qr (if qr), and with o given
+// the backward's
 // [B, Hq, npad] vectors -D = -rowsum(dO * O) and -lse * log2(e), stored
 // negated (padding rows 0 and -inf).
 // cu / total: the packed layout (see SeqRows; cu == nullptr: fixed); the
 // packed table is checked here (status bit kDevErrSegments).
+// sched (may be null): the forward's work-item counter, set to 0.
 cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
                               const __nv_bfloat16* dout, const float* lse, float* nDvec,
-                              float* nlse2, int npad, const int* cu, int total, cudaStream_t st);
-
-// cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2].
-cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
+                              float* nlse2, int npad, const int* cu, int total, int* sched,
                               cudaStream_t st);
+
+// cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2]; sets
+// *sched to 0 when sched is given (as launch_train_prep).
+cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
+                              int* sched, cudaStream_t st);
+
+// Multiprocessors of the current device (cached per device; 0 on error).
+int sm_count();
 
 // Rotate rows of x [B, n, H, d] (bf16 or f32) at positions pos0 + i using the
 // table (row i of the table = position pos0 + i) and write bf16 to out (same
@@ -199,9 +206,7 @@ struct FwdLaunch {
   bool out_f32;
   float* lse;              // training: [B, Hq, n]; decode: [S, Hkv, R]
   bool decode;
-  bool rotate_q;           // training: mQ holds unrotated bf16 queries; the kernel
-                           // applies RoPE in shared memory using `table`
-  const float2* table;     // rope table for positions p .. p+n-1 (rotate_q)
+  int* sched;              // training: the work-item counter, zero at launch
   // decode mode: mQ maps the raw queries [B, Hkv, G, d] as (d, G, Hkv, B)
   // with a (64, G, 1, 128/G) box, so that a 128-row tile is rows b*G + hh;
   // the kernel rotates row (b, hh) at position p + len[b] in shared memory.

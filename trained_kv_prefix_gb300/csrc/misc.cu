@@ -82,7 +82,8 @@ __device__ __forceinline__ float2 rope_table_entry(double pos, double inv_freq) 
 }
 
 __global__ void rope_table_kernel(float2* __restrict__ table, int pos0, int npos, int half,
-                                  const RopeFreqs f) {
+                                  const RopeFreqs f, int* sched) {
+  if (sched && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   const long long total = static_cast<long long>(npos) * half;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -202,8 +203,9 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     const RopeFreqs f, int p, int B, int n, int Hq, int Hkv, int d,
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, float* __restrict__ nDvec, float* __restrict__ nlse2, int npad,
-    int ppc, const int* __restrict__ cu_arg, int ntok, uint32_t* status) {
+    int ppc, const int* __restrict__ cu_arg, int ntok, int* sched, uint32_t* status) {
   const int* const cu = kPacked ? cu_arg : nullptr;
+  if (sched && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   __shared__ float2 cs[kPrepPos][kMaxHeadDim / 2];
   const int half = d / 2, chunks = half / 8;
   if (cu && blockIdx.x == 0) {
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     const int pl = t / half, j = t % half;
     const float2 v = rope_cs_turns(f.turns[j], p + i0 + pl);
     cs[pl][j] = v;
-    table[static_cast<long long>(i0 + pl) * half + j] = v;
+    if (table) table[static_cast<long long>(i0 + pl) * half + j] = v;
   }
   __syncthreads();
   // rotations: task = ((pos, b), head, chunk)
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
       rotate_chunk8(x + row * d + jc * 8, y + row * d + jc * 8, &cs[pl][jc * 8], half);
     }
   };
-  rotate_all(k, kr, Hkv);
+  if (kr) rotate_all(k, kr, Hkv);
   if (qr) rotate_all(q, qr, Hq);
   if (!o) return;
   // -D and -lse2: 8 lanes per (b, i, h) row, 4 rows per warp (uniform trip count)
@@ -412,7 +414,8 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
                               const __nv_bfloat16* dout, const float* lse, float* nDvec,
-                              float* nlse2, int npad, const int* cu, int total, cudaStream_t st) {
+                              float* nlse2, int npad, const int* cu, int total, int* sched,
+                              cudaStream_t st) {
   const int span = o ? max(n, npad) : n;
   // positions per CTA: enough CTAs for about eight per SM, at most kPrepPos
   const int ppc = max(1, min(kPrepPos, (span + 152 * 8 - 1) / (152 * 8)));
@@ -421,16 +424,16 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
   TraceScope tr(o ? "bwd_prep" : "fwd_prep", st);
   auto* kern = cu ? train_prep_kernel<true> : train_prep_kernel<false>;
   kern<<<grid, kThreads, 0, st>>>(q, k, qr, kr, table, f, p, B, n, Hq, Hkv, d, o, dout, lse, nDvec,
-                                  nlse2, npad, ppc, cu, total, device_status_ptr());
+                                  nlse2, npad, ppc, cu, total, sched, device_status_ptr());
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
-                              cudaStream_t st) {
-  if (npos <= 0) return cudaSuccess;
-  const long long work = static_cast<long long>(npos) * (d / 2);
+                              int* sched, cudaStream_t st) {
+  if (npos <= 0 && !sched) return cudaSuccess;
+  const long long work = static_cast<long long>(npos > 0 ? npos : 0) * (d / 2);
   TraceScope tr("rope_table", st);
-  rope_table_kernel<<<grid_for(work), kThreads, 0, st>>>(table, pos0, npos, d / 2, f);
+  rope_table_kernel<<<grid_for(work), kThreads, 0, st>>>(table, pos0, npos, d / 2, f, sched);
   return cudaGetLastError();
 }
 
