@@ -468,7 +468,8 @@ def measure_train_workload(ts, dev, rank, peaks, flush, steps, bwd=True):
                      dv=torch.empty_like(tin["v"]),
                      dkc=torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev),
                      dvc=torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev))
-        ws_b = torch.empty(cartattn.bwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(cartattn.bwd_reuse_workspace_size(g, 0, 0), dtype=torch.uint8,
+                           device=dev)
 
     def step():
         cartattn.cart_write_to_cache(tin["kc"], tin["vc"], kcb, vcb)
@@ -478,7 +479,7 @@ def measure_train_workload(ts, dev, rank, peaks, flush, steps, bwd=True):
         if bwd:
             cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], kcb, vcb, o, lse, tin["do"],
                                    frozen_prefix=ts.frozen_prefix, theta=ts.theta,
-                                   workspace=ws_b, **grads)
+                                   workspace=ws_b, fwd_workspace=ws_f, **grads)
 
     for _ in range(3):
         flush()
@@ -575,7 +576,7 @@ def main():
     od = torch.empty_like(din["q"])
     g = cartattn.geom(ts.B, ts.n, ts.Hq, ts.Hkv, ts.d, ts.p, ts.frozen_prefix, None, ts.theta)
     ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(cartattn.bwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(cartattn.bwd_reuse_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
     ws_d = torch.empty(cartattn.decode_workspace_size(ds.B, ds.Hq, ds.Hkv, ds.d, ds.p,
                                                       ds.cache_rows), dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
@@ -587,7 +588,7 @@ def main():
                                theta=ts.theta, o=o, lse=lse, workspace=ws_f)
         cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], kcb, vcb, o, lse, tin["do"],
                                frozen_prefix=ts.frozen_prefix, theta=ts.theta, dq=dq, dk=dk, dv=dv,
-                               dkc=dkc, dvc=dvc, workspace=ws_b)
+                               dkc=dkc, dvc=dvc, workspace=ws_b, fwd_workspace=ws_f)
         cdist.allreduce_cartridge_grads(dkc, dvc)
 
     def decode_part():
@@ -722,7 +723,8 @@ def main():
                                    workspace=ws_f)
             cartattn.cart_attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], kcb, vcb, o, lse,
                                    dev_in["do"], frozen_prefix=ts.frozen_prefix, theta=ts.theta,
-                                   dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc, workspace=ws_b)
+                                   dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc, workspace=ws_b,
+                                   fwd_workspace=ws_f)
             cdist.allreduce_cartridge_grads(dkc, dvc)
             for k2, t in (("dq", dq), ("dk", dk), ("dv", dv), ("dkc", dkc), ("dvc", dvc)):
                 outs_h[k2].copy_(t, non_blocking=True)

@@ -211,6 +211,44 @@ def test_window_wider_than_the_sequence_is_bitwise_no_window():
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
 
 
+REUSE_CASES = [
+    # (name, B, n, Hq, Hkv, d, p, dtype, cart dtype, window)
+    ("reuse_bf16", 2, 300, 8, 2, 128, 200, "bf16", "f32", 0),
+    ("reuse_bf16_cartbf16", 1, 257, 4, 1, 64, 129, "bf16", "bf16", 0),
+    ("reuse_f32", 1, 130, 4, 2, 64, 64, "f32", "f32", 0),
+    ("reuse_window", 2, 200, 8, 2, 128, 150, "bf16", "f32", 96),
+]
+
+
+@pytest.mark.parametrize("case", REUSE_CASES, ids=[c[0] for c in REUSE_CASES])
+def test_bwd_reusing_the_forward_workspace_is_bitwise_bwd(case):
+    """cart_attn_bwd_reuse reads the forward's rotated Q / K, table and bf16
+    copies: its gradients equal cart_attn_bwd's bit for bit, and the oracle's
+    at the gradient tolerance."""
+    name, B, n, Hq, Hkv, d, p, dt, cdt, window = case
+    s = synth.TrainShape(name, B=B, n=n, Hq=Hq, Hkv=Hkv, d=d, p=p, dtype=dt, cart_dtype=cdt,
+                         seed=151, qkv_std=0.5, do_std=1.0)
+    inp = synth.train_inputs(s)
+    g = gh.to_gpu(inp)
+    geom = cartattn.geom(B, n, Hq, Hkv, d, p, s.frozen_prefix, None, s.theta, window)
+    ws_f = torch.empty(cartattn.fwd_workspace_size(geom, cartattn._dt(g["q"]),
+                                                   cartattn._dt(g["kc"])),
+                       dtype=torch.uint8, device="cuda")
+    o, lse = cartattn.cart_attn_fwd(g["q"], g["k"], g["v"], g["kc"], g["vc"], theta=s.theta,
+                                    window=window, workspace=ws_f)
+    plain = cartattn.cart_attn_bwd(g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse, g["do"],
+                                   theta=s.theta, window=window)
+    reuse = cartattn.cart_attn_bwd(g["q"], g["k"], g["v"], g["kc"], g["vc"], o, lse, g["do"],
+                                   theta=s.theta, window=window, fwd_workspace=ws_f)
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    for nme, x, y in zip(("dq", "dk", "dv", "dkc", "dvc"), plain, reuse):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), nme
+    got = {k: synth.f64(v) for k, v in zip(("dq", "dk", "dv", "dkc", "dvc"), reuse)}
+    ref = gh.oracle_train(s, inp, window=window)
+    gh.check_grads(got, ref, s.frozen_prefix)
+
+
 def test_packed_window_parity():
     s = _shape("packed_win", 0, 0, 8, 2, 128, 300, seed=136)
     lens, window = (130, 1, 0, 257, 64), 180

@@ -70,6 +70,10 @@ def lib():
             L.cart_attn_bwd_parts.argtypes = [G, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                               vp, vp, vp, ctypes.POINTER(ctypes.c_int), i, i, vp,
                                               sz, vp]
+            L.cart_attn_bwd_reuse_workspace_size.argtypes = [G, i, i]
+            L.cart_attn_bwd_reuse_workspace_size.restype = sz
+            L.cart_attn_bwd_reuse.argtypes = [G, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, vp, i, vp, sz, vp, sz, vp]
             L.cart_attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
             L.cart_attn_decode_workspace_size.restype = sz
             L.cart_attn_decode.argtypes = [i, i, i, i, i, f, d, vp, vp, vp, vp, vp, vp, vp, i, vp,
@@ -96,6 +100,7 @@ def lib():
             L.cart_trace_count.argtypes = []
             L.cart_trace_get.argtypes = [i, ctypes.c_char_p, i, ctypes.POINTER(ctypes.c_float)]
             for name in ("cart_write_to_cache", "cart_attn_fwd", "cart_attn_bwd", "cart_attn_bwd_parts",
+                         "cart_attn_bwd_reuse",
                          "cart_attn_fwd_packed", "cart_attn_bwd_packed",
                          "cart_attn_decode", "cart_attn_decode_span", "cart_device_status",
                          "cart_trace_enable",
@@ -107,6 +112,7 @@ def lib():
 
 EXPORTS = ("cart_write_to_cache", "cart_attn_fwd_workspace_size", "cart_attn_fwd",
            "cart_attn_bwd_workspace_size", "cart_attn_bwd", "cart_attn_bwd_parts",
+           "cart_attn_bwd_reuse_workspace_size", "cart_attn_bwd_reuse",
            "cart_attn_decode_workspace_size",
            "cart_attn_decode", "cart_status_string", "cart_device_status", "cart_trace_enable",
            "cart_trace_count", "cart_trace_get", "cart_attn_decode_noalloc",
@@ -201,11 +207,15 @@ def cart_attn_fwd(q, k, v, kc, vc, *, frozen_prefix=1, scale=None, theta=1.0e6, 
 
 def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None, theta=1.0e6,
                   accumulate=False, dq=None, dk=None, dv=None, dkc=None, dvc=None,
-                  workspace=None, stream=None, frozen_rows=None, window=0):
+                  workspace=None, stream=None, frozen_rows=None, window=0,
+                  fwd_workspace=None):
     """Backward.  Returns ``(dq, dk, dv, dkc, dvc)``; dkc/dvc are f32
     ``[p, Hkv, d]`` summed over the batch, rows < frozen_prefix and the rows
     listed in ``frozen_rows`` (a composed cartridge's part sinks) exactly 0.
-    ``window`` must match the forward's."""
+    ``window`` must match the forward's.  ``fwd_workspace``: the workspace
+    the forward of these inputs used (cart_attn_bwd_reuse: its rotated
+    queries and keys are read instead of recomputed); not with
+    ``frozen_rows``."""
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
     p = kc.shape[0]
@@ -220,6 +230,19 @@ def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None,
     if dvc is None:
         dvc = (torch.zeros if accumulate else torch.empty)((max(p, 1), Hkv, d),
                                                            dtype=torch.float32, device=q.device)
+    if fwd_workspace is not None:
+        if frozen_rows is not None:
+            raise ValueError("fwd_workspace does not combine with frozen_rows")
+        ws = _workspace(int(lib().cart_attn_bwd_reuse_workspace_size(ctypes.byref(g), dt, cd)),
+                        q.device, workspace)
+        rc = lib().cart_attn_bwd_reuse(ctypes.byref(g), dt, cd, _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(kc), _ptr(vc), _ptr(o), _ptr(lse), _ptr(dout),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkc), _ptr(dvc),
+                                       1 if accumulate else 0, _ptr(fwd_workspace),
+                                       fwd_workspace.numel(), _ptr(ws), ws.numel(),
+                                       _stream(stream, q.device))
+        _check("cart_attn_bwd_reuse", rc)
+        return dq, dk, dv, dkc[:p], dvc[:p]
     ws = _workspace(bwd_workspace_size(g, dt, cd), q.device, workspace)
     if frozen_rows is None:
         rc = lib().cart_attn_bwd(ctypes.byref(g), dt, cd, _ptr(q), _ptr(k), _ptr(v), _ptr(kc),
@@ -237,6 +260,10 @@ def cart_attn_bwd(q, k, v, kc, vc, o, lse, dout, *, frozen_prefix=1, scale=None,
                                        _stream(stream, q.device))
         _check("cart_attn_bwd_parts", rc)
     return dq, dk, dv, dkc[:p], dvc[:p]
+
+
+def bwd_reuse_workspace_size(g: _Geom, in_dtype: int, cart_dtype: int) -> int:
+    return int(lib().cart_attn_bwd_reuse_workspace_size(ctypes.byref(g), in_dtype, cart_dtype))
 
 
 def fwd_packed_workspace_size(g: _Geom, total: int, in_dtype: int, cart_dtype: int) -> int:

@@ -34,6 +34,18 @@ uint32_t* device_status_ptr() {
   return cache[dev];
 }
 
+int sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cache[dev] &&
+      cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    cache[dev] = 0;
+  return cache[dev];
+}
+
 namespace {
 
 // ------------------------------------------------------------ utilities ----
@@ -230,7 +242,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Workspace carving shared by the size query and the call.
 struct TrainWs {
   size_t table = 0, qr = 0, kr = 0, vb = 0, kcb = 0, vcb = 0, dob = 0, dvec = 0, nlse2 = 0,
-         total = 0;
+         sched = SIZE_MAX, total = 0;
   int npad = 0;
 };
 
@@ -245,8 +257,11 @@ long long token_rows(const cart_geom* g, const Packing& pk) {
   return pk.cu ? pk.total : static_cast<long long>(g->B) * g->n;
 }
 
+// reuse (backward only): the forward's workspace supplies the table, the
+// rotated Q / K and the bf16 copies, so this workspace holds only the
+// backward's own parts.
 TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd,
-                 const Packing& pk = Packing()) {
+                 const Packing& pk = Packing(), bool reuse = false) {
   TrainWs w;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -258,12 +273,15 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd,
   const size_t rows_q = static_cast<size_t>(token_rows(g, pk)) * g->Hq * g->d;
   const size_t rows_k = static_cast<size_t>(token_rows(g, pk)) * g->Hkv * g->d;
   const size_t cart = static_cast<size_t>(g->p) * g->Hkv * g->d;
-  w.table = take(static_cast<size_t>(g->n) * (g->d / 2) * sizeof(float2));
-  w.qr = take(rows_q * e16);
-  w.kr = take(rows_k * e16);
-  w.vb = (in == CART_F32) ? take(rows_k * e16) : SIZE_MAX;
-  w.kcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
-  w.vcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
+  if (!reuse) {
+    w.table = take(static_cast<size_t>(g->n) * (g->d / 2) * sizeof(float2));
+    w.qr = take(rows_q * e16);
+    w.kr = take(rows_k * e16);
+    w.vb = (in == CART_F32) ? take(rows_k * e16) : SIZE_MAX;
+    w.kcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
+    w.vcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
+  }
+  if (!bwd) w.sched = take(sizeof(int));  // the forward's work-item counter
   if (bwd) {
     w.dob = (in == CART_F32) ? take(rows_q * e16) : SIZE_MAX;
     w.npad = (g->n + 127) / 128 * 128;
@@ -292,8 +310,7 @@ bool make_tokens_map(CUtensorMap* m, const void* base, const cart_geom* g, const
 struct TrainPrep {
   const float2* table;
   RopeFreqs freqs;
-  bool q_in_kernel;
-  const void* qr;  // rotated bf16 queries, or q itself when q_in_kernel
+  const void* qr;  // rotated bf16 queries
   const void* kr;
   const void* vb;
   const void* kcb;
@@ -312,29 +329,64 @@ struct PrepVec {
   int npad = 0;
 };
 
-// With q_in_kernel (bf16 queries only) Q is left unrotated: mQ maps q itself
-// and the forward kernel rotates each tile in shared memory.  bf16 inputs
-// take one fused launch (table, K, Q, backward vectors); f32 inputs take the
-// generic kernels and the caller computes the vectors.
+// The TMA maps over the prepared tensors.
+int prep_maps(const cart_geom* g, const Packing& pk, TrainPrep* out) {
+  bool ok = make_tokens_map(&out->mQ, out->qr, g, pk, g->Hq, 128) &&
+            make_tokens_map(&out->mK, out->kr, g, pk, g->Hkv, 128) &&
+            make_tokens_map(&out->mV, out->vb, g, pk, g->Hkv, 128);
+  if (g->p > 0)
+    ok = ok && make_rows_map(&out->mKc, out->kcb, 1, g->p, g->Hkv, g->d, 128) &&
+         make_rows_map(&out->mVc, out->vcb, 1, g->p, g->Hkv, g->d, 128);
+  else  // never loaded when there are no cartridge tiles
+    ok = ok && make_rows_map(&out->mKc, out->kr, 1, 1, g->Hkv, g->d, 128) &&
+         make_rows_map(&out->mVc, out->kr, 1, 1, g->Hkv, g->d, 128);
+  return ok ? CART_OK : CART_ERR_CUDA;
+}
+
+// bf16 inputs take one fused launch (table, rotated K and Q, backward
+// vectors); f32 inputs take the generic kernels and the caller computes the
+// vectors.  The forward's workspace also has its work-item counter zeroed
+// here (the first kernel of the call).
+// With fwd_ws (the backward reusing a forward's workspace) nothing is
+// recomputed: the table, the rotated Q / K and the bf16 copies are read from
+// the forward's workspace (its layout: train_ws(..., bwd = false)), and only
+// the backward's vectors are computed (bf16 inputs; f32 callers compute them).
 int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, const void* k,
                const void* v, const void* kc, const void* vc, uint8_t* ws, const TrainWs& w,
-               cudaStream_t st, TrainPrep* out, bool q_in_kernel, const PrepVec& vec,
-               const Packing& pk) {
+               cudaStream_t st, TrainPrep* out, const PrepVec& vec, const Packing& pk,
+               const uint8_t* fwd_ws = nullptr) {
   const bool f32 = in == CART_F32;
-  if (f32) q_in_kernel = false;
+  const RopeFreqs freqs = make_rope_freqs(g->d, g->rope_theta);
+  if (fwd_ws) {
+    const TrainWs wf = train_ws(g, in, cd, false, pk);
+    if (!f32 && vec.o)
+      CART_CUDA(launch_train_prep(
+          static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), nullptr,
+          nullptr, nullptr, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
+          static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
+          vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, nullptr, st));
+    const bool cart_f32 = cd == CART_F32 && g->p > 0;
+    out->table = reinterpret_cast<const float2*>(fwd_ws + wf.table);
+    out->freqs = freqs;
+    out->qr = fwd_ws + wf.qr;
+    out->kr = fwd_ws + wf.kr;
+    out->vb = f32 ? static_cast<const void*>(fwd_ws + wf.vb) : v;
+    out->kcb = cart_f32 ? static_cast<const void*>(fwd_ws + wf.kcb) : kc;
+    out->vcb = cart_f32 ? static_cast<const void*>(fwd_ws + wf.vcb) : vc;
+    return prep_maps(g, pk, out);
+  }
+  int* sched = w.sched == SIZE_MAX ? nullptr : reinterpret_cast<int*>(ws + w.sched);
   float2* table = reinterpret_cast<float2*>(ws + w.table);
   __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(ws + w.qr);
   __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(ws + w.kr);
-  const RopeFreqs freqs = make_rope_freqs(g->d, g->rope_theta);
   if (!f32) {
     CART_CUDA(launch_train_prep(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-        q_in_kernel ? nullptr : qr, kr, table, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
+        qr, kr, table, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
         static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
-        vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, st));
-    if (q_in_kernel) qr = static_cast<__nv_bfloat16*>(const_cast<void*>(q));
+        vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, sched, st));
   } else {
-    CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, freqs, st));
+    CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, freqs, sched, st));
     CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, pk.cu, pk.total,
                                st));
     CART_CUDA(launch_rope_rows(k, f32, kr, table, g->B, g->n, g->Hkv, g->d, true, pk.cu, pk.total,
@@ -360,22 +412,12 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
   }
   out->table = table;
   out->freqs = freqs;
-  out->q_in_kernel = q_in_kernel;
   out->qr = qr;
   out->kr = kr;
   out->vb = vb;
   out->kcb = kcb;
   out->vcb = vcb;
-  bool ok = make_tokens_map(&out->mQ, qr, g, pk, g->Hq, 128) &&
-            make_tokens_map(&out->mK, kr, g, pk, g->Hkv, 128) &&
-            make_tokens_map(&out->mV, vb, g, pk, g->Hkv, 128);
-  if (g->p > 0)
-    ok = ok && make_rows_map(&out->mKc, kcb, 1, g->p, g->Hkv, g->d, 128) &&
-         make_rows_map(&out->mVc, vcb, 1, g->p, g->Hkv, g->d, 128);
-  else  // never loaded when there are no cartridge tiles
-    ok = ok && make_rows_map(&out->mKc, kr, 1, 1, g->Hkv, g->d, 128) &&
-         make_rows_map(&out->mVc, kr, 1, 1, g->Hkv, g->d, 128);
-  return ok ? CART_OK : CART_ERR_CUDA;
+  return prep_maps(g, pk, out);
 }
 
 // Packed layout: at least one token, no more than B segments of n tokens
@@ -477,7 +519,7 @@ static int fwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TrainPrep tp;
   rc = train_prep(g, in, cd, q, k, v, kc, vc, static_cast<uint8_t*>(workspace), w, st, &tp,
-                  /*q_in_kernel=*/true, PrepVec(), pk);
+                  PrepVec(), pk);
   if (rc) return rc;
   FwdLaunch l{};
   l.mQ = &tp.mQ;
@@ -499,8 +541,7 @@ static int fwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   l.out_f32 = in == CART_F32;
   l.lse = lse;
   l.decode = false;
-  l.rotate_q = tp.q_in_kernel;
-  l.table = tp.table;
+  l.sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + w.sched);
   l.cu = pk.cu;
   l.total = pk.total;
   l.window = g->window;
@@ -554,7 +595,8 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
                     const void* q, const void* k, const void* v, const void* kc, const void* vc,
                     const void* o, const float* lse, const void* dout, void* dq, void* dk,
                     void* dv, float* dkc, float* dvc, const int* frozen_rows, int n_frozen,
-                    int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
+                    int accumulate, void* workspace, size_t workspace_bytes, void* stream,
+                    const void* fwd_ws = nullptr, size_t fwd_ws_bytes = 0) {
   int rc = train_common_checks(g, in, cd, q, k, v, kc, vc, pk);
   if (rc) return rc;
   if (n_frozen < 0 || n_frozen > CART_MAX_FROZEN_ROWS || (n_frozen > 0 && !frozen_rows))
@@ -566,8 +608,10 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
     return CART_ERR_POINTER;
   if (g->p > 0 && (!dkc || !dvc || !aligned16(dkc) || !aligned16(dvc))) return CART_ERR_POINTER;
   if (accumulate != 0 && accumulate != 1) return CART_ERR_GEOMETRY;
-  const TrainWs w = train_ws(g, in, cd, true, pk);
+  const TrainWs w = train_ws(g, in, cd, true, pk, fwd_ws != nullptr);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return CART_ERR_WORKSPACE;
+  if (fwd_ws && (fwd_ws_bytes < train_ws(g, in, cd, false, pk).total || !aligned16(fwd_ws)))
+    return CART_ERR_WORKSPACE;
   rc = check_device();
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -585,7 +629,8 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
     vec.nlse2 = nlse2;
     vec.npad = w.npad;
   }
-  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp, false, vec, pk);
+  rc = train_prep(g, in, cd, q, k, v, kc, vc, ws, w, st, &tp, vec, pk,
+                  static_cast<const uint8_t*>(fwd_ws));
   if (rc) return rc;
   const void* dob = dout;
   if (f32) {
@@ -654,6 +699,23 @@ int cart_attn_bwd(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* 
                   int accumulate, void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(g, Packing(), in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
                   nullptr, 0, accumulate, workspace, workspace_bytes, stream);
+}
+
+size_t cart_attn_bwd_reuse_workspace_size(const cart_geom* g, cart_dtype in, cart_dtype cd) {
+  if (check_geom(g) || !dtype_ok(in) || !dtype_ok(cd)) return 0;
+  return train_ws(g, in, cd, true, Packing(), true).total;
+}
+
+int cart_attn_bwd_reuse(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
+                        const void* k, const void* v, const void* kc, const void* vc,
+                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                        void* dv, float* dkc, float* dvc, int accumulate,
+                        const void* fwd_workspace, size_t fwd_workspace_bytes, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!fwd_workspace) return CART_ERR_WORKSPACE;
+  return bwd_impl(g, Packing(), in, cd, q, k, v, kc, vc, o, lse, dout, dq, dk, dv, dkc, dvc,
+                  nullptr, 0, accumulate, workspace, workspace_bytes, stream, fwd_workspace,
+                  fwd_workspace_bytes);
 }
 
 int cart_attn_bwd_parts(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q,
