@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--traffic-command", default="", help="the command that made the capture")
     ap.add_argument("--ext-steps", type=int, default=20,
                     help="timed steps of the packed-training and span-decode lines (0: skip)")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="run --steps untimed steps of the headline step (training step + "
+                         "decode step) after --warmup ones and exit: the command ncu captures")
     return ap.parse_args()
 
 
@@ -595,6 +598,18 @@ def main():
         cartattn.cart_attn_decode(din["q"], din["k_new"], din["v_new"], din["kc"], din["vc"],
                                   din["k_cache"], din["v_cache"], din["lens"], theta=ds.theta,
                                   o=od, workspace=ws_d)
+
+    if args.profile_only:
+        # exactly warmup + steps headline steps of the library's kernels
+        for _ in range(args.warmup + args.steps):
+            flush()
+            train_part()
+            decode_part()
+        torch.cuda.synchronize(dev)
+        assert cartattn.device_status() == 0
+        if rank == 0:
+            print(json.dumps({"profile_only": True, "steps": args.steps, "warmup": args.warmup}))
+        return
 
     for _ in range(max(args.warmup, 3)):
         flush()
