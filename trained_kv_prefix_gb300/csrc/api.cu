@@ -281,7 +281,7 @@ TrainWs train_ws(const cart_geom* g, cart_dtype in, cart_dtype cd, bool bwd,
     w.kcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
     w.vcb = (cd == CART_F32 && g->p > 0) ? take(cart * e16) : SIZE_MAX;
   }
-  if (!bwd) w.sched = take(sizeof(int));  // the forward's work-item counter
+  w.sched = take(sizeof(int));  // the forward's / the dQ kernel's work-item counter
   if (bwd) {
     w.dob = (in == CART_F32) ? take(rows_q * e16) : SIZE_MAX;
     w.npad = (g->n + 127) / 128 * 128;
@@ -345,8 +345,8 @@ int prep_maps(const cart_geom* g, const Packing& pk, TrainPrep* out) {
 
 // bf16 inputs take one fused launch (table, rotated K and Q, backward
 // vectors); f32 inputs take the generic kernels and the caller computes the
-// vectors.  The forward's workspace also has its work-item counter zeroed
-// here (the first kernel of the call).
+// vectors.  The workspace's work-item counter (of the persistent forward or
+// dQ kernel that follows) is zeroed here, by the first launch of the call.
 // With fwd_ws (the backward reusing a forward's workspace) nothing is
 // recomputed: the table, the rotated Q / K and the bf16 copies are read from
 // the forward's workspace (its layout: train_ws(..., bwd = false)), and only
@@ -357,6 +357,9 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
                const uint8_t* fwd_ws = nullptr) {
   const bool f32 = in == CART_F32;
   const RopeFreqs freqs = make_rope_freqs(g->d, g->rope_theta);
+  // the work-item counter of the kernel that follows (zeroed by the first
+  // launch of this prep)
+  int* sched = w.sched == SIZE_MAX ? nullptr : reinterpret_cast<int*>(ws + w.sched);
   if (fwd_ws) {
     const TrainWs wf = train_ws(g, in, cd, false, pk);
     if (!f32 && vec.o)
@@ -364,7 +367,9 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
           static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), nullptr,
           nullptr, nullptr, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
           static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
-          vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, nullptr, st));
+          vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, sched, st));
+    else if (sched)
+      CART_CUDA(cudaMemsetAsync(sched, 0, sizeof(int), st));
     const bool cart_f32 = cd == CART_F32 && g->p > 0;
     out->table = reinterpret_cast<const float2*>(fwd_ws + wf.table);
     out->freqs = freqs;
@@ -375,7 +380,6 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
     out->vcb = cart_f32 ? static_cast<const void*>(fwd_ws + wf.vcb) : vc;
     return prep_maps(g, pk, out);
   }
-  int* sched = w.sched == SIZE_MAX ? nullptr : reinterpret_cast<int*>(ws + w.sched);
   float2* table = reinterpret_cast<float2*>(ws + w.table);
   __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(ws + w.qr);
   __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(ws + w.kr);
@@ -641,9 +645,8 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
     CART_CUDA(launch_bwd_vec(o, dout, f32, lse, nDvec, nlse2, g->B, g->n, w.npad, g->Hq, g->d,
                              pk.cu, pk.total, st));
   }
-  CUtensorMap mdO, mdQ;
+  CUtensorMap mdO;
   if (!make_tokens_map(&mdO, dob, g, pk, g->Hq, 128)) return CART_ERR_CUDA;
-  if (!f32 && !make_tokens_map(&mdQ, dq, g, pk, g->Hq, 128)) return CART_ERR_CUDA;
   BwdLaunch l{};
   l.mQ = &tp.mQ;
   l.mdO = &mdO;
@@ -651,7 +654,6 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   l.mVc = &tp.mVc;
   l.mK = &tp.mK;
   l.mV = &tp.mV;
-  l.mdQ = f32 ? nullptr : &mdQ;
   l.B = g->B;
   l.n = g->n;
   l.Hq = g->Hq;
@@ -677,6 +679,7 @@ static int bwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   l.cu = pk.cu;
   l.total = pk.total;
   l.window = g->window;
+  l.sched = reinterpret_cast<int*>(ws + w.sched);
   SideStream* side = side_stream();
   if (!side) {
     CART_CUDA(launch_bwd(l, st, st));

@@ -19,9 +19,9 @@
 //               P^T, dS^T (bf16, shared memory), dV += P^T dO, dK += dS^T Q.
 //               Epilogue: cartridge rows (f32, frozen rows = 0) or
 //               real rows (dK rotated back by R(p+j)^T).
-//  dq_kernel    one CTA per 128-row query tile: S = Q K^T, dP = dO V^T,
-//               dS = P (dP - D) -> TMEM, dQ += dS K over 128-key steps;
-//               epilogue rotates back by R(p+i)^T.
+//  dq_kernel    persistent, one 128-row query tile per work item: S = Q K^T,
+//               dP = dO V^T, dS = P (dP - D) -> TMEM, dQ += dS K over
+//               128-key steps; epilogue rotates back by R(p+i)^T.
 // Both kernels have a second instance (kGeneral) for packed segments and /
 // or a sliding window: sequences located through the segment table, key
 // tiles limited to the query tiles' windows and query tiles to the key
@@ -56,7 +56,10 @@ struct BwdParams {
   int accumulate;
   const float2* table;
   uint32_t* status;
-  int tma_dq;  // bf16 dQ stored by TMA through mdQ
+  // dQ: work items (query tiles of every head and sequence) and the counter
+  // CTAs take them from (zeroed by the prep launch before the backward)
+  int n_items;
+  int* sched;
   // RoPE angle of pair c at position x, in turns: x * (turns[c].x + turns[c].y)
   float2 turns[kMaxHeadDim / 2];
   // cartridge rows frozen besides those < frozen_prefix (composed parts' sinks)
@@ -681,18 +684,28 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 }
 
 // ================================================================ dQ ======
-// One CTA per 128-row query tile (heaviest tiles first), Q and dO resident in
-// shared memory.  Keys stream in 128-row steps (every MMA has N = 128).
-// TMEM: S double buffered at x*128 (x = step & 1), dP at 256, dQ at 384.
-// Both warpgroups work on every step, warpgroup w on keys [64w, 64w + 64)
-// (thread = query row = TMEM lane).  A warpgroup reads its S and dP columns,
-// releases dP at once (so dP of the next step can be computed while it
-// works), then overwrites the first 32 of its 64 S columns with
-// dS = P (dP - D) packed as bf16 pairs; dQ += dS K reads dS from TMEM as its
-// A operand (K step k of 16 keys at column (k/4)*64 + (k%4)*8), K entering
-// as an MN-major operand.  MMA order per step t:
+// Persistent: one CTA per SM takes work items -- 128-row query tiles of one
+// (head, sequence), heaviest first -- from a counter that the prep launch
+// zeroes; the producer publishes each item in a two-slot shared-memory ring.
+// Q and dO of an item are resident in shared memory; the next item's Q loads
+// once the current item's last S MMA has read Q, its dO once the last dP MMA
+// has read dO.  Keys stream in 128-row steps (every MMA has N = 128).
+// TMEM: S double buffered at x*128 (x = step & 1, steps counted over all
+// items), dP at 256, dQ at 384.  Both warpgroups work on every step,
+// warpgroup w on keys [64w, 64w + 64) (thread = query row = TMEM lane).  A
+// warpgroup reads its S and dP columns, releases dP at once (so dP of the
+// next step can be computed while it works), then overwrites the first 32 of
+// its 64 S columns with dS = P (dP - D) packed as bf16 pairs; dQ += dS K
+// reads dS from TMEM as its A operand (K step k of 16 keys at column
+// (k/4)*64 + (k%4)*8), K entering as an MN-major operand.  MMA order per
+// step t:
 //   S(t+1), dP(t+1) [after dP(t) is released], dQ(t) [after dS(t)].
-// K has a 3-stage ring (read by S and dQ), V a 2-stage ring (read by dP).
+// K has a 3-stage ring (read by S and dQ), V a 2-stage ring (read by dP);
+// both run on across items.  The epilogue rotates dQ back and stores each
+// thread's row straight from registers (no staging, so the next item's Q and
+// dO are not held up); the next item's first dQ MMA, which overwrites the
+// accumulator, follows that item's first dS, which the softmax warps write
+// only after their epilogue has read dQ out.
 // Threads: warps 0-7 the two warpgroups, warp 8 TMA, warp 9 MMA.
 constexpr int kDqThreads = 320;
 constexpr int kDqKStages = 3;
@@ -705,13 +718,17 @@ struct DqSmem {
   static constexpr int kdO = kQ + kTileBytes;
   static constexpr int kK = kdO + kTileBytes;                 // K ring
   static constexpr int kV = kK + kDqKStages * kTileBytes;     // V ring
-  static constexpr int kBar = kV + kDqVStages * kTileBytes;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kBar = kV + kDqVStages * kTileBytes;   // barriers, TMEM slot, abort word
+  static constexpr int kItems = kBar + 256;                   // two item slots
+  static constexpr int kBytes = kItems + 128;
   static constexpr int kAlloc = kBytes;  // dynamic shared memory starts 1024-aligned
 };
 
 enum DqBar {
-  kQdFull = 0,
+  kQFull = 0,
+  kQEmpty,                           // the item's last S MMA has read Q
+  kdOFull,
+  kdOEmpty,                          // the item's last dP MMA has read dO
   kKFull0,
   kKEmpty0 = kKFull0 + kDqKStages,
   kVFull0 = kKEmpty0 + kDqKStages,
@@ -720,20 +737,65 @@ enum DqBar {
   kDpFull = kSdFull0 + 2,            // dP computed
   kDpFree,                           // both groups read dP (256 arrivals)
   kDsdFull0,                         // dS of buffer x written (256 arrivals)
-  kDqDone = kDsdFull0 + 2,
+  kDqDone = kDsdFull0 + 2,           // the item's last dQ MMA has completed
   kDqDrain,
-  kDqStaged,                         // both groups staged their dQ columns (256 arrivals)
-  kDqBars
+  kDqItemFull0,                      // the producer published the next item in slot s
+  kDqItemEmpty0 = kDqItemFull0 + 2,  // the MMA warp and the 8 softmax warps are done with slot s
+  kDqBars = kDqItemEmpty0 + 2
 };
-static_assert(kDqBars * 8 + 16 <= 256, "dQ barrier area");
-static_assert(kDqBars * 8 + 4 <= 256, "dq barrier area");
+static_assert(kDqBars * 8 + 8 <= 256, "dQ barrier area");
+
+// One dQ work item: query tile qt of (head h, sequence b) and its key tiles
+// -- cartridge tiles [ct_lo, ct_lo + n_ct), then real tiles [rt_lo, rt_hi).
+struct DqItem {
+  int h, b, q0, kvh, seq_len, n_ct, ct_lo, rt_lo, T;
+  SeqRows sr;
+};
+
+// As published in a shared-memory slot (w < 0: no more items); the roles
+// read each field where they use it.
+struct DqSlot {
+  int w, h, b, q0, seq_len, row0, blk, g0, n_ct, ct_lo, rt_lo, T, pad[4];
+};
+static_assert(sizeof(DqSlot) == 64, "dQ item slot");
+
+// Item w: tiles are numbered heaviest first (the query tile index falls as w
+// grows: later tiles see more real keys).
+__device__ __forceinline__ DqItem dq_item(const BwdParams& a, int w, const int* cu, int window) {
+  DqItem I;
+  const int hb = a.Hq * a.B;
+  const int z = w / hb, rem = w % hb;
+  I.h = rem % a.Hq;
+  I.b = rem / a.Hq;
+  const int qt = a.n_qtiles - 1 - z;
+  I.sr = seq_rows(cu, a.total, a.n, I.b);
+  I.seq_len = cu ? I.sr.len : a.n;
+  I.kvh = I.h / a.G;
+  I.q0 = qt * kTile;
+  I.n_ct = I.ct_lo = I.rt_lo = I.T = 0;
+  if (I.q0 >= I.seq_len) return I;  // a segment shorter than the longest
+  const int n_ct_all = (a.p + kTile - 1) / kTile;
+  const int last_q = min(I.q0 + kTile, I.seq_len) - 1;  // last real query of the tile
+  const int rt_hi = last_q / kTile + 1;                  // real key steps up to the diagonal
+  if (window > 0) {
+    // the first key any row of the tile sees: position p + q0 - window + 1
+    const int lo = a.p + I.q0 - window + 1;
+    if (lo > 0) {
+      I.ct_lo = min(lo / kTile, n_ct_all);
+      I.rt_lo = lo > a.p ? (lo - a.p) / kTile : 0;
+    }
+  }
+  I.n_ct = n_ct_all - I.ct_lo;
+  I.T = I.n_ct + rt_hi - I.rt_lo;
+  return I;
+}
 
 template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
               const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
               const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
-              const __grid_constant__ CUtensorMap mdQ, const BwdParams a) {
+              const BwdParams a) {
   using L = DqSmem<D>;
   constexpr int SK = kDqKStages, SV = kDqVStages;
   extern __shared__ __align__(1024) uint8_t dq_smem[];
@@ -744,36 +806,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + kDqBars * 8);
-  int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDqBars * 8 + 8);
+  int* abort_flag = reinterpret_cast<int*>(smem + L::kBar + kDqBars * 8 + 4);
+  DqSlot* items = reinterpret_cast<DqSlot*>(smem + L::kItems);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int* const cu = kGeneral ? a.cu : nullptr;  // packed segment table
   const int window = kGeneral ? a.window : 0;
 
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);
-  const int seq_len = cu ? seq_rows(cu, a.total, a.n, b).len : a.n;
-  if (kGeneral && qt * kTile >= seq_len) return;  // a segment shorter than the longest
-  const int kvh = h / a.G;
-  const int q0 = qt * kTile;
-  // key tiles: cartridge tiles [ct_lo, n_ct_all), real tiles [rt_lo, rt_hi)
-  const int n_ct_all = (a.p + kTile - 1) / kTile;
-  const int last_q = min(q0 + kTile, seq_len) - 1;      // last real query of the tile
-  const int rt_hi = last_q / kTile + 1;                  // real key steps up to the diagonal
-  int ct_lo = 0, rt_lo = 0;
-  if (window > 0) {
-    // the first key any row of the tile sees: position p + q0 - window + 1
-    const int lo = a.p + q0 - window + 1;
-    if (lo > 0) {
-      ct_lo = min(lo / kTile, n_ct_all);
-      rt_lo = lo > a.p ? (lo - a.p) / kTile : 0;
-    }
-  }
-  const int n_ct = n_ct_all - ct_lo;
-  const int T = n_ct + rt_hi - rt_lo;
-
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(&bars[kQdFull], 1);
+    mbar_init(&bars[kQFull], 1);
+    mbar_init(&bars[kQEmpty], 1);
+    mbar_init(&bars[kdOFull], 1);
+    mbar_init(&bars[kdOEmpty], 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(&bars[kKFull0 + s], 1);
       mbar_init(&bars[kKEmpty0 + s], 1);
@@ -785,12 +829,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kSdFull0 + x], 1);
       mbar_init(&bars[kDsdFull0 + x], 256);
+      mbar_init(&bars[kDqItemFull0 + x], 1);
+      mbar_init(&bars[kDqItemEmpty0 + x], 9);  // the MMA warp and the 8 softmax warps
     }
     mbar_init(&bars[kDpFull], 1);
     mbar_init(&bars[kDpFree], 256);
     mbar_init(&bars[kDqDone], 1);
     mbar_init(&bars[kDqDrain], 1);
-    mbar_init(&bars[kDqStaged], 256);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -807,50 +852,112 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint8_t* sdO = smem + L::kdO;
 
   if (warp == 8) {
-    if (lane == 0 && T > 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
       tma_prefetch_desc(&mQ);
       tma_prefetch_desc(&mdO);
-      const SeqRows sr = seq_rows(cu, a.total, a.n, b);
-      mbar_arrive_expect_tx(&bars[kQdFull], 2 * L::kTileBytes);
-#pragma unroll
-      for (int hc = 0; hc < D / 64; ++hc) {
-        tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQdFull], hc * 64, h, sr.row0 + q0, sr.blk);
-        tma_load_4d(sdO + hc * 16384, &mdO, &bars[kQdFull], hc * 64, h, sr.row0 + q0, sr.blk);
-      }
+      tma_prefetch_desc(&mKc);
+      tma_prefetch_desc(&mVc);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      auto fetch = [&]() -> int {
+        const int w = atomicAdd(a.sched, 1);
+        return w < a.n_items ? w : -1;
+      };
+      int g = 0;   // K / V tiles issued, over all items
+      int nq = 0;  // Q / dO loads issued (items with work)
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
-        const bool cart = t < n_ct;
-        const int row0 = cart ? (ct_lo + t) * kTile : sr.row0 + (rt_lo + t - n_ct) * kTile;
-        const int blk = cart ? 0 : sr.blk;
-        const int sk = t % SK, sv = t % SV;
-        if (t >= SK) {
-          ok = mbar_wait(&bars[kKEmpty0 + sk], ((t / SK) - 1) & 1, abort_s, a.status,
+      int w = fetch();
+      for (int it = 0; ok; ++it) {
+        const int sl = it & 1;
+        if (it >= 2) {
+          ok = mbar_wait(&bars[kDqItemEmpty0 + sl], ((it >> 1) - 1) & 1, abort_s, a.status,
                          kDevErrTimeoutTma);
           if (!ok) break;
         }
-        uint8_t* sK = smem + L::kK + sk * L::kTileBytes;
-        mbar_arrive_expect_tx(&bars[kKFull0 + sk], L::kTileBytes);
+        DqItem I{};
+        if (w >= 0) I = dq_item(a, w, cu, window);
+        DqSlot& o = items[sl];
+        o.w = w;
+        o.h = I.h;
+        o.b = I.b;
+        o.q0 = I.q0;
+        o.seq_len = I.seq_len;
+        o.row0 = I.sr.row0;
+        o.blk = I.sr.blk;
+        o.g0 = I.sr.g0;
+        o.n_ct = I.n_ct;
+        o.ct_lo = I.ct_lo;
+        o.rt_lo = I.rt_lo;
+        o.T = I.T;
+        mbar_arrive(&bars[kDqItemFull0 + sl]);  // (release: the slot is visible to the waiters)
+        if (w < 0) break;
+        const int w_next = fetch();
+        if (I.T > 0) {
+          // Q and dO of this item once the previous item's last S / dP MMA
+          // has read them
+          if (nq >= 1) {
+            ok = mbar_wait(&bars[kQEmpty], (nq - 1) & 1, abort_s, a.status, kDevErrTimeoutTma);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&bars[kQFull], L::kTileBytes);
 #pragma unroll
-        for (int hc = 0; hc < D / 64; ++hc)
-          tma_load_4d(sK + hc * 16384, cart ? &mKc : &mK, &bars[kKFull0 + sk], hc * 64, kvh, row0,
-                      blk);
-        k_issued = t + 1;
-        if (t >= SV) {
-          ok = mbar_wait(&bars[kVEmpty0 + sv], ((t / SV) - 1) & 1, abort_s, a.status,
-                         kDevErrTimeoutTma);
-          if (!ok) break;
+          for (int hc = 0; hc < D / 64; ++hc)
+            tma_load_4d(sQ + hc * 16384, &mQ, &bars[kQFull], hc * 64, I.h, I.sr.row0 + I.q0,
+                        I.sr.blk);
+          if (nq >= 1) {
+            ok = mbar_wait(&bars[kdOEmpty], (nq - 1) & 1, abort_s, a.status, kDevErrTimeoutTma);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&bars[kdOFull], L::kTileBytes);
+#pragma unroll
+          for (int hc = 0; hc < D / 64; ++hc)
+            tma_load_4d(sdO + hc * 16384, &mdO, &bars[kdOFull], hc * 64, I.h, I.sr.row0 + I.q0,
+                        I.sr.blk);
+          ++nq;
+          for (int t = 0; t < I.T && ok; ++t, ++g) {
+            const bool cart = t < I.n_ct;
+            const int row0 =
+                cart ? (I.ct_lo + t) * kTile : I.sr.row0 + (I.rt_lo + t - I.n_ct) * kTile;
+            const int blk = cart ? 0 : I.sr.blk;
+            const int sk = g % SK, sv = g % SV;
+            if (g >= SK) {
+              ok = mbar_wait(&bars[kKEmpty0 + sk], ((g / SK) - 1) & 1, abort_s, a.status,
+                             kDevErrTimeoutTma);
+              if (!ok) break;
+            }
+            uint8_t* sK = smem + L::kK + sk * L::kTileBytes;
+            mbar_arrive_expect_tx(&bars[kKFull0 + sk], L::kTileBytes);
+#pragma unroll
+            for (int hc = 0; hc < D / 64; ++hc)
+              tma_load_4d(sK + hc * 16384, cart ? &mKc : &mK, &bars[kKFull0 + sk], hc * 64, I.kvh,
+                          row0, blk);
+            k_issued = g + 1;
+            if (g >= SV) {
+              ok = mbar_wait(&bars[kVEmpty0 + sv], ((g / SV) - 1) & 1, abort_s, a.status,
+                             kDevErrTimeoutTma);
+              if (!ok) break;
+            }
+            uint8_t* sV = smem + L::kV + sv * L::kTileBytes;
+            mbar_arrive_expect_tx(&bars[kVFull0 + sv], L::kTileBytes);
+#pragma unroll
+            for (int hc = 0; hc < D / 64; ++hc)
+              tma_load_4d(sV + hc * 16384, cart ? &mVc : &mV, &bars[kVFull0 + sv], hc * 64, I.kvh,
+                          row0, blk);
+            v_issued = g + 1;
+          }
         }
-        uint8_t* sV = smem + L::kV + sv * L::kTileBytes;
-        mbar_arrive_expect_tx(&bars[kVFull0 + sv], L::kTileBytes);
-#pragma unroll
-        for (int hc = 0; hc < D / 64; ++hc)
-          tma_load_4d(sV + hc * 16384, cart ? &mVc : &mV, &bars[kVFull0 + sv], hc * 64, kvh, row0,
-                      blk);
-        v_issued = t + 1;
+        w = w_next;
       }
       if (!ok) {
-        mbar_wait(&bars[kQdFull], 0, 0u, nullptr, 0);
+        // Give the copies still in flight (the last Q and dO loads, the last
+        // K and V tiles) a bounded chance to land before the CTA releases
+        // its shared memory.
+        if (nq > 0) {
+          mbar_wait(&bars[kQFull], (nq - 1) & 1, 0u, nullptr, 0);
+          mbar_wait(&bars[kdOFull], (nq - 1) & 1, 0u, nullptr, 0);
+        }
         for (int t = max(k_issued - SK, 0); t < k_issued; ++t)
           mbar_wait(&bars[kKFull0 + t % SK], (t / SK) & 1, 0u, nullptr, 0);
         for (int t = max(v_issued - SV, 0); t < v_issued; ++t)
@@ -862,64 +969,81 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     // ----------------------------------------------------------------- MMA --
     // The whole warp runs this loop (warp-uniform descriptors); one elected
     // lane issues each MMA and commit.
-    if (T > 0) {
-      auto wait = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu,
-                          mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
-      };
-      const uint32_t idS = idesc_bf16(128, 128, false, false);
-      const uint32_t idDQ = idesc_bf16(128, D, false, true);
-      const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
-      const uint64_t dOd = sdesc_sw128(smem_u32(sdO), 16u, 1024u);
-      const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);      // K-major
-      const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kK), 16384u, 1024u);   // MN-major
-      const uint64_t dVk0 = sdesc_sw128(smem_u32(smem + L::kV), 16u, 1024u);
-      // C (f32, TMEM) = A (128 rows) * B^T (128 rows), both K-major over d
-      auto issue_nt = [&](uint32_t c, uint64_t da, uint64_t db) {
-        umma_bf16_ss_w(c, da, db, idS, 0u);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu,
+                        mbar_wait(bar, parity, abort_s, a.status, kDevErrTimeoutMma));
+    };
+    const uint32_t idS = idesc_bf16(128, 128, false, false);
+    const uint32_t idDQ = idesc_bf16(128, D, false, true);
+    const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16u, 1024u);
+    const uint64_t dOd = sdesc_sw128(smem_u32(sdO), 16u, 1024u);
+    const uint64_t dKk0 = sdesc_sw128(smem_u32(smem + L::kK), 16u, 1024u);      // K-major
+    const uint64_t dKm0 = sdesc_sw128(smem_u32(smem + L::kK), 16384u, 1024u);   // MN-major
+    const uint64_t dVk0 = sdesc_sw128(smem_u32(smem + L::kV), 16u, 1024u);
+    // C (f32, TMEM) = A (128 rows) * B^T (128 rows), both K-major over d
+    auto issue_nt = [&](uint32_t c, uint64_t da, uint64_t db) {
+      umma_bf16_ss_w(c, da, db, idS, 0u);
 #pragma unroll
-        for (int k = 1; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          umma_bf16_ss_w(c, desc_add(da, off), desc_add(db, off), idS, 1u);
-        }
-      };
-      bool ok = wait(&bars[kQdFull], 0) &&
-                wait(&bars[kKFull0], 0);
+      for (int k = 1; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        umma_bf16_ss_w(c, desc_add(da, off), desc_add(db, off), idS, 1u);
+      }
+    };
+    int g = 0;   // K / V tiles consumed, over all items
+    int gs = 0;  // steps, over all items (S buffer, dP and dS phases)
+    int nq = 0;  // Q / dO loads consumed
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      ok = wait(&bars[kDqItemFull0 + (it & 1)], (it >> 1) & 1);
+      if (!ok) break;
+      const DqSlot& sI = items[it & 1];
+      const int w = vld(sI.w), T = vld(sI.T);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kDqItemEmpty0 + (it & 1)]);  // read all it needs
+      if (w < 0) break;
+      if (T == 0) continue;
+      // first step: S into buffer gs & 1, dP once dP of the previous step
+      // (the previous item's last) has been read
+      ok = wait(&bars[kQFull], nq & 1) && wait(&bars[kKFull0 + g % SK], (g / SK) & 1);
       if (ok) {
         tc_fence_after();
-        issue_nt(tS0, dQd, dKk0);
-        umma_commit_w(&bars[kSdFull0]);
-        ok = wait(&bars[kVFull0], 0);
+        issue_nt(tS0 + (gs & 1) * 128, dQd, desc_add(dKk0, (g % SK) * L::kTileBytes));
+        umma_commit_w(&bars[kSdFull0 + (gs & 1)]);
+        if (T == 1) umma_commit_w(&bars[kQEmpty]);
+        ok = wait(&bars[kdOFull], nq & 1) && (gs == 0 || wait(&bars[kDpFree], (gs - 1) & 1)) &&
+             wait(&bars[kVFull0 + g % SV], (g / SV) & 1);
       }
       if (ok) {
         tc_fence_after();
-        issue_nt(tDP, dOd, dVk0);
+        issue_nt(tDP, dOd, desc_add(dVk0, (g % SV) * L::kTileBytes));
         umma_commit_w(&bars[kDpFull]);
-        umma_commit_w(&bars[kVEmpty0]);
+        umma_commit_w(&bars[kVEmpty0 + g % SV]);
+        if (T == 1) umma_commit_w(&bars[kdOEmpty]);
       }
       for (int t = 0; t < T && ok; ++t) {
-        const int x = t & 1;
+        const int G = gs + t, x = G & 1;
         if (t + 1 < T) {
-          const int sk = (t + 1) % SK, sv = (t + 1) % SV;
-          ok = wait(&bars[kKFull0 + sk], ((t + 1) / SK) & 1);
+          const int gk = g + t + 1, sk = gk % SK, sv = gk % SV;
+          ok = wait(&bars[kKFull0 + sk], (gk / SK) & 1);
           if (!ok) break;
           tc_fence_after();
-          // buffer x^1 last held dS(t-1), read by dQ(t-1) issued earlier
+          // buffer x^1 last held dS(G-1), read by dQ(G-1) issued earlier
           // (one CTA's MMAs run in issue order)
           issue_nt(tS0 + (x ^ 1) * 128, dQd, desc_add(dKk0, sk * L::kTileBytes));
           umma_commit_w(&bars[kSdFull0 + (x ^ 1)]);
-          ok = wait(&bars[kDpFree], t & 1) &&
-               wait(&bars[kVFull0 + sv], ((t + 1) / SV) & 1);
+          if (t + 1 == T - 1) umma_commit_w(&bars[kQEmpty]);
+          ok = wait(&bars[kDpFree], G & 1) && wait(&bars[kVFull0 + sv], (gk / SV) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_nt(tDP, dOd, desc_add(dVk0, sv * L::kTileBytes));
           umma_commit_w(&bars[kDpFull]);
           umma_commit_w(&bars[kVEmpty0 + sv]);
+          if (t + 1 == T - 1) umma_commit_w(&bars[kdOEmpty]);
         }
-        ok = wait(&bars[kDsdFull0 + x], (t >> 1) & 1);
+        ok = wait(&bars[kDsdFull0 + x], (G >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
-        const int sk = t % SK;
+        const int sk = (g + t) % SK;
         const uint64_t dkm = desc_add(dKm0, sk * L::kTileBytes);
         const uint32_t ds = tS0 + x * 128;
         umma_bf16_ts_w(tDQ, ds, dkm, idDQ, t > 0 ? 1u : 0u);
@@ -929,84 +1053,112 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         umma_commit_w(&bars[kKEmpty0 + sk]);
       }
       if (ok) umma_commit_w(&bars[kDqDone]);
-      umma_commit_w(&bars[kDqDrain]);
-      mbar_wait(&bars[kDqDrain], 0, 0u, nullptr, 0);
+      g += T;
+      gs += T;
+      ++nq;
     }
+    // Drain: every MMA issued above completes before the CTA tears down.
+    umma_commit_w(&bars[kDqDrain]);
+    mbar_wait(&bars[kDqDrain], 0, 0u, nullptr, 0);
     __syncwarp();
   } else {
+    // ------------------------------------------------------------ dS / dQ --
     const int wg = warp >> 2;
     const int row = threadIdx.x & 127;
-    const int i = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // padded vectors: rows past n read -lse2 = -inf (P = 0) and -D = 0
-    const long long vidx = (static_cast<long long>(b) * a.Hq + h) * a.npad + i;
-    const float nl = __ldg(a.nlse2 + vidx), nd = __ldg(a.nDvec + vidx);
     const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-    const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
-    const int i_cap = min(i, seq_len - 1);
-    bool ok = T > 0;
-    for (int t = 0; t < T && ok; ++t) {
-      const int x = t & 1;
-      ok = mbar_wait(&bars[kSdFull0 + x], (t >> 1) & 1, abort_s, a.status, kDevErrTimeoutSoftmax) &&
-           mbar_wait(&bars[kDpFull], t & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
+    int gs = 0;  // steps, over all items
+    int nd = 0;  // items finished
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      ok = mbar_wait(&bars[kDqItemFull0 + (it & 1)], (it >> 1) & 1, abort_s, a.status,
+                     kDevErrTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      // visible keys of this group's 64 (leading columns)
-      // (key positions of this group's 64 columns start at kpos0)
-      const int kpos0 =
-          (t < n_ct ? (ct_lo + t) * kTile : a.p + (rt_lo + t - n_ct) * kTile) + wg * 64;
-      int valid = t < n_ct ? a.p - kpos0 : i_cap - (kpos0 - a.p) + 1;
-      valid = max(0, min(valid, 64));
-      // ... and the first one under the window
-      const int first = window > 0 ? max(0, min(a.p + i - window + 1 - kpos0, 64)) : 0;
-      const uint32_t ts = tS0 + x * 128 + wg * 64 + lane_off;
-      const uint32_t tdp = tDP + wg * 64 + lane_off;
-      uint32_t sa[32], sb[32], da[32], db[32];
-      tmem_ld32(ts, sa);
-      tmem_ld32(ts + 32, sb);
-      tmem_ld32(tdp, da);
-      tmem_ld32(tdp + 32, db);
-      tmem_ld_wait();
-      tmem_reg_fence(sa);
-      tmem_reg_fence(sb);
-      tmem_reg_fence(da);
-      tmem_reg_fence(db);
-      tc_fence_before();
-      mbar_arrive(&bars[kDpFree]);
-      uint32_t pk[32];
-      auto compute = [&](auto masked) {
+      // the slot is released once the item's epilogue is done with it
+      const DqSlot& sI = items[it & 1];
+      if (vld(sI.w) < 0) break;
+      const int T = vld(sI.T);
+      if (T == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kDqItemEmpty0 + (it & 1)]);
+        continue;
+      }
+      const int h = vld(sI.h), b = vld(sI.b);
+      const int i = vld(sI.q0) + row;
+      const int seq_len = vld(sI.seq_len);
+      const int n_ct = vld(sI.n_ct), ct_lo = vld(sI.ct_lo), rt_lo = vld(sI.rt_lo);
+      // padded vectors: rows past n read -lse2 = -inf (P = 0) and -D = 0
+      const long long vidx = (static_cast<long long>(b) * a.Hq + h) * a.npad + i;
+      const float nl = __ldg(a.nlse2 + vidx), ndv = __ldg(a.nDvec + vidx);
+      const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(ndv, ndv);
+      const int i_cap = min(i, seq_len - 1);
+      for (int t = 0; t < T && ok; ++t) {
+        const int G = gs + t, x = G & 1;
+        ok = mbar_wait(&bars[kSdFull0 + x], (G >> 1) & 1, abort_s, a.status,
+                       kDevErrTimeoutSoftmax) &&
+             mbar_wait(&bars[kDpFull], G & 1, abort_s, a.status, kDevErrTimeoutSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        // visible keys of this group's 64 (leading columns)
+        // (key positions of this group's 64 columns start at kpos0)
+        const int kpos0 =
+            (t < n_ct ? (ct_lo + t) * kTile : a.p + (rt_lo + t - n_ct) * kTile) + wg * 64;
+        int valid = t < n_ct ? a.p - kpos0 : i_cap - (kpos0 - a.p) + 1;
+        valid = max(0, min(valid, 64));
+        // ... and the first one under the window
+        const int first = window > 0 ? max(0, min(a.p + i - window + 1 - kpos0, 64)) : 0;
+        const uint32_t ts = tS0 + x * 128 + wg * 64 + lane_off;
+        const uint32_t tdp = tDP + wg * 64 + lane_off;
+        uint32_t sa[32], sb[32], da[32], db[32];
+        tmem_ld32(ts, sa);
+        tmem_ld32(ts + 32, sb);
+        tmem_ld32(tdp, da);
+        tmem_ld32(tdp + 32, db);
+        tmem_ld_wait();
+        tmem_reg_fence(sa);
+        tmem_reg_fence(sb);
+        tmem_reg_fence(da);
+        tmem_reg_fence(db);
+        tc_fence_before();
+        mbar_arrive(&bars[kDpFree]);
+        uint32_t pk[32];
+        auto compute = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          // two keys per packed two-lane op: P = 2^(S*scale*log2(e) - lse2),
-          // dS = P * (dP - D)
-          const float2 sv = c < 32 ? u2f2(sa[c], sa[c + 1]) : u2f2(sb[c - 32], sb[c - 31]);
-          const float2 dv = c < 32 ? u2f2(da[c], da[c + 1]) : u2f2(db[c - 32], db[c - 31]);
-          const float2 x = __ffma2_rn(sv, sc2, nl2);
-          float2 pe = make_float2(exp2_approx(x.x), exp2_approx(x.y));
-          if (decltype(masked)::value) {
-            pe.x = (c < valid && c >= first) ? pe.x : 0.f;
-            pe.y = (c + 1 < valid && c + 1 >= first) ? pe.y : 0.f;
+          for (int c = 0; c < 64; c += 2) {
+            // two keys per packed two-lane op: P = 2^(S*scale*log2(e) - lse2),
+            // dS = P * (dP - D)
+            const float2 sv = c < 32 ? u2f2(sa[c], sa[c + 1]) : u2f2(sb[c - 32], sb[c - 31]);
+            const float2 dv = c < 32 ? u2f2(da[c], da[c + 1]) : u2f2(db[c - 32], db[c - 31]);
+            const float2 xe = __ffma2_rn(sv, sc2, nl2);
+            float2 pe = make_float2(exp2_approx(xe.x), exp2_approx(xe.y));
+            if (decltype(masked)::value) {
+              pe.x = (c < valid && c >= first) ? pe.x : 0.f;
+              pe.y = (c + 1 < valid && c + 1 >= first) ? pe.y : 0.f;
+            }
+            const float2 ds = __fmul2_rn(pe, __fadd2_rn(dv, nd2));
+            pk[c / 2] = pack_bf16x2(ds.x, ds.y);
           }
-          const float2 ds = __fmul2_rn(pe, __fadd2_rn(dv, nd2));
-          pk[c / 2] = pack_bf16x2(ds.x, ds.y);
-        }
-      };
-      if (__any_sync(0xffffffffu, valid < 64 || first > 0))
-        compute(std::true_type{});
-      else
-        compute(std::false_type{});
-      // dS over the first 32 of this group's S columns (already read)
-      tmem_st32(ts, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[kDsdFull0 + x]);
-    }
-    if (ok) {
-      ok = mbar_wait(&bars[kDqDone], 0, abort_s, a.status, kDevErrTimeoutEpilogue);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
+        };
+        if (__any_sync(0xffffffffu, valid < 64 || first > 0))
+          compute(std::true_type{});
+        else
+          compute(std::false_type{});
+        // dS over the first 32 of this group's S columns (already read)
+        tmem_st32(ts, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kDsdFull0 + x]);
+      }
+      gs += T;
+      // ---------------------------------------------------------- epilogue --
+      if (ok) {
+        ok = mbar_wait(&bars[kDqDone], nd & 1, abort_s, a.status, kDevErrTimeoutEpilogue);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      ++nd;
+      if (!ok) break;
       tc_fence_after();
       // warpgroup wg finishes the rotation pairs j in [wg*D/4, wg*D/4 + D/4)
       // and their partners j + D/2
@@ -1038,44 +1190,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           lo[e] = x0 * cs.x + x1 * cs.y;
           hi[e] = x1 * cs.x - x0 * cs.y;
         }
-      }
-      const SeqRows sr = seq_rows(cu, a.total, a.n, b);
-      // a packed segment's last tile: a TMA store would run into the next
-      // segment, so its rows are stored one by one
-      if (a.tma_dq && (!cu || q0 + kTile <= seq_len || sr.row0 + seq_len == a.total)) {
-        // Stage the row's columns in the (spent) Q tile, in the swizzled
-        // layout of the dQ map's 128-row box, then one thread stores the
-        // tile; rows past n are clipped by the map.
-        const uint32_t base = smem_u32(sQ);
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const float* v = part ? hi : lo;
-          const int col0 = (part ? D / 2 : 0) + wg * Q;
-#pragma unroll
-          for (int k = 0; k < Q / 8; ++k) {
-            const int col = col0 + 8 * k;
-            sts_u4(base + (col >> 6) * 16384 + sw128_offset(row, (col & 63) >> 3),
-                   make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                              pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
-                              pack_bf16x2(v[8 * k + 6], v[8 * k + 7])));
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[kDqStaged]);
-        if (threadIdx.x == 0) {
-          if (mbar_wait(&bars[kDqStaged], 0, abort_s, a.status, kDevErrTimeoutEpilogue)) {
-#pragma unroll
-            for (int hc = 0; hc < D / 64; ++hc)
-              tma_store_4d(&mdQ, sQ + hc * 16384, hc * 64, h, sr.row0 + q0, sr.blk);
-            bulk_commit_group();
-            bulk_wait_all();
-          }
-        }
-      } else if (i < seq_len) {
-        const long long off = ((static_cast<long long>(sr.g0) + i) * a.Hq + h) * D;
+        // this thread's row, straight from registers (whole 16-byte pieces)
+        const long long off = ((static_cast<long long>(vld(sI.g0)) + i) * a.Hq + h) * D;
         store_row_out(a.dq, off + wg * Q, lo, Q, a.out_f32 != 0);
         store_row_out(a.dq, off + D / 2 + wg * Q, hi, Q, a.out_f32 != 0);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kDqItemEmpty0 + (it & 1)]);
     }
   }
 
@@ -1137,10 +1258,14 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   TraceScope tr("bwd_dq", st_dq);
-  p.tma_dq = (!l.out_f32 && l.mdQ) ? 1 : 0;
+  // persistent: one CTA per SM, none idle from the start
+  p.n_items = p.Hq * p.B * p.n_qtiles;
+  p.sched = l.sched;
+  const int nsm = sm_count();
+  if (nsm < 1 || !l.sched) return cudaErrorInvalidValue;
   auto* kern_dq = general ? dq_kernel<D, true> : dq_kernel<D, false>;
-  kern_dq<<<dim3(p.Hq, p.B, p.n_qtiles), kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
-      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p.tma_dq ? *l.mdQ : *l.mQ, p);
+  kern_dq<<<p.n_items < nsm ? p.n_items : nsm, kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
+      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
   return cudaGetLastError();
 }
 

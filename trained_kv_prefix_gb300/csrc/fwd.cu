@@ -202,9 +202,6 @@ struct ItemSlot {
   int w, head, qb, pair, split, seq_len, row0, blk, g0, n_ct, ct_lo, rt_lo, T_A, T_B, T, pad;
 };
 static_assert(sizeof(ItemSlot) == 64, "item slot");
-__device__ __forceinline__ int vld(const int& f) {
-  return *reinterpret_cast<const volatile int*>(&f);
-}
 
 // Tile counts of a pair of query tiles under the causal mask and the window.
 __device__ __forceinline__ void item_tiles(const FwdParams& a, FwdItem& I, int window,

@@ -234,7 +234,6 @@ struct BwdLaunch {
   const CUtensorMap* mVc;
   const CUtensorMap* mK;    // 4D (d, Hkv, n, B) rotated real keys
   const CUtensorMap* mV;
-  const CUtensorMap* mdQ;   // bf16 output: 4D (d, Hq, n, B) over dq, 128-row box; else null
   int B, n, Hq, Hkv, d, p, frozen_prefix;
   int n_frozen;                            // cartridge rows also frozen (parts' sinks)
   int frozen_rows[CART_MAX_FROZEN_ROWS];
@@ -256,6 +255,7 @@ struct BwdLaunch {
   const int* cu = nullptr;
   int total = 0;
   int window = 0;           // sliding window in keys (0: none)
+  int* sched = nullptr;     // the dQ kernel's work-item counter, zero at launch
 };
 // dK/dV kernel on st_dkdv, dQ kernel on st_dq (the two are independent).
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st_dkdv, cudaStream_t st_dq);

@@ -31,6 +31,12 @@ constexpr uint64_t kWaitLimitNs = 20000000ull;    // 20 ms
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 #endif
 
+// A volatile read of a shared-memory word another role wrote (a field of a
+// published work item, read where it is used rather than kept in registers).
+__device__ __forceinline__ int vld(const int& f) {
+  return *reinterpret_cast<const volatile int*>(&f);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
