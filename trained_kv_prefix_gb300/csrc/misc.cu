@@ -219,13 +219,15 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
   }
   const int i0 = blockIdx.x * ppc;
   const int np = max(0, min(ppc, n - i0));  // real positions in this block
-  for (int t = threadIdx.x; t < np * half; t += blockDim.x) {
-    const int pl = t / half, j = t % half;
-    const float2 v = rope_cs_turns(f.turns[j], p + i0 + pl);
-    cs[pl][j] = v;
-    if (table) table[static_cast<long long>(i0 + pl) * half + j] = v;
+  if (table || kr || qr) {  // (the backward vectors alone need no angles)
+    for (int t = threadIdx.x; t < np * half; t += blockDim.x) {
+      const int pl = t / half, j = t % half;
+      const float2 v = rope_cs_turns(f.turns[j], p + i0 + pl);
+      cs[pl][j] = v;
+      if (table) table[static_cast<long long>(i0 + pl) * half + j] = v;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // rotations: task = ((pos, b), head, chunk)
   auto rotate_all = [&](const __nv_bfloat16* x, __nv_bfloat16* y, int H) {
     const int tasks = np * B * H * chunks;
