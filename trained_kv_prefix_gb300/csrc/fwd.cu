@@ -45,7 +45,15 @@
 //                    window (a row that has seen no visible key yet keeps
 //                    P = 0); in decode mode the CTA starts at the earliest
 //                    window among its conversations.
+#include <algorithm>
 #include <climits>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -255,6 +263,21 @@ __device__ __forceinline__ FwdItem train_item(const FwdParams& a, int w, const i
   return I;
 }
 
+// A static schedule of training work items over the persistent CTAs: CTA c
+// takes items[off[c] .. off[c+1]) in that order (n == 0: no plan, CTAs take
+// items from the counter instead).  Only the fixed-layout instance carries
+// the full arrays, as a kernel parameter.
+constexpr int kPlanCtas = 160;
+constexpr int kPlanItems = 4096;
+template <int N>
+struct FwdPlan {
+  int n;
+  uint16_t off[kPlanCtas + 1];
+  uint16_t items[N];
+};
+template <int kMode>
+using PlanOf = FwdPlan<kMode == kFwdTrain ? kPlanItems : 1>;
+
 // kMode: kFwdTrain (training, fixed [B, n] layout, no window, bf16 output),
 // kFwdGeneral (training with packed segments, a sliding window or an f32
 // output) or kFwdDecode
@@ -273,7 +296,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKc,
                const __grid_constant__ CUtensorMap mVc, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mO32,
-               const FwdParams a) {
+               const FwdParams a, const __grid_constant__ PlanOf<kMode> plan) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -366,8 +389,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
       // the next item: decode has one; training takes the counter's next
+      // the next item: decode has one; training follows its static plan
+      // if it has one, else takes the counter's next
       auto fetch = [&](int k) -> int {
         if (kDecode) return k == 0 ? 0 : -1;
+        if (kMode == kFwdTrain && plan.n > 0) {
+          const int o = plan.off[blockIdx.x] + k;
+          return o < plan.off[blockIdx.x + 1] ? static_cast<int>(plan.items[o]) : -1;
+        }
         const int w = atomicAdd(a.sched, 1);
         return w < a.n_items ? w : -1;
       };
@@ -906,18 +935,133 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
+// A static schedule for `grid` persistent CTAs and the fixed-layout items
+// (numbering of train_item): each item costs its tiles (one unit = one
+// 128-key tile for one query tile) plus kItemCost for its start and end.
+// Longest-processing-time first onto the least loaded CTA, then moves and
+// swaps that lower the most loaded CTA's total while any does -- a tighter
+// fit than taking items in order from a counter when every CTA gets only a
+// few items.  Cached per geometry (its host cost is milliseconds).
+const std::vector<uint16_t>& fwd_plan(int n_pairs, int hb, int n_ct, int n_qtiles, int grid,
+                                      std::vector<uint16_t>* off_out) {
+  constexpr double kItemCost = 2.5;
+  struct Plan {
+    std::vector<uint16_t> items, off;
+  };
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int>, Plan> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(n_pairs, hb, n_ct, n_qtiles, grid);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    const int n = n_pairs * hb;
+    std::vector<double> cost(n);
+    for (int w = 0; w < n; ++w) {
+      const int pr = n_pairs - 1 - w / hb;
+      const bool hasB = 2 * pr + 1 < n_qtiles;
+      const int rA = std::min(2 * pr + 1, n_qtiles);
+      const int rB = hasB ? std::min(2 * pr + 2, n_qtiles) : 0;
+      cost[w] = (hasB ? 2 : 1) * n_ct + rA + rB + kItemCost;
+    }
+    std::vector<std::vector<int>> per(grid);
+    std::vector<double> load(grid, 0.0);
+    {
+      std::vector<int> order(n);
+      for (int w = 0; w < n; ++w) order[w] = w;
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int x, int y) { return cost[x] > cost[y]; });
+      using Slot = std::pair<double, int>;
+      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> q;
+      for (int c = 0; c < grid; ++c) q.push({0.0, c});
+      for (int w : order) {
+        const Slot sl = q.top();
+        q.pop();
+        per[sl.second].push_back(w);
+        load[sl.second] += cost[w];
+        q.push({load[sl.second], sl.second});
+      }
+    }
+    for (int iter = 0; iter < 100000; ++iter) {
+      const int cm = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
+      double best = load[cm];
+      int bj = -1, ba = -1, bb = -1;  // move per[cm][ba] to CTA bj (bb < 0) or swap with per[bj][bb]
+      for (int j = 0; j < grid; ++j) {
+        if (j == cm) continue;
+        for (int ia = 0; ia < static_cast<int>(per[cm].size()); ++ia) {
+          const double ca = cost[per[cm][ia]];
+          const double mv = std::max(load[cm] - ca, load[j] + ca);
+          if (mv < best - 1e-9) {
+            best = mv;
+            bj = j;
+            ba = ia;
+            bb = -1;
+          }
+          for (int ib = 0; ib < static_cast<int>(per[j].size()); ++ib) {
+            const double d = ca - cost[per[j][ib]];
+            if (d <= 1e-9) continue;
+            const double sw = std::max(load[cm] - d, load[j] + d);
+            if (sw < best - 1e-9) {
+              best = sw;
+              bj = j;
+              ba = ia;
+              bb = ib;
+            }
+          }
+        }
+      }
+      if (bj < 0) break;
+      const int wa = per[cm][ba];
+      per[cm].erase(per[cm].begin() + ba);
+      per[bj].push_back(wa);
+      load[cm] -= cost[wa];
+      load[bj] += cost[wa];
+      if (bb >= 0) {
+        const int wb = per[bj][bb];
+        per[bj].erase(per[bj].begin() + bb);
+        per[cm].push_back(wb);
+        load[bj] -= cost[wb];
+        load[cm] += cost[wb];
+      }
+    }
+    Plan pl;
+    pl.off.push_back(0);
+    for (int c = 0; c < grid; ++c) {
+      std::sort(per[c].begin(), per[c].end(), [&](int x, int y) { return cost[x] > cost[y]; });
+      for (int w : per[c]) pl.items.push_back(static_cast<uint16_t>(w));
+      pl.off.push_back(static_cast<uint16_t>(pl.items.size()));
+    }
+    it = cache.emplace(key, std::move(pl)).first;
+  }
+  *off_out = it->second.off;
+  return it->second.items;
+}
+
+template <int D, int kMode>
+cudaError_t launch_fwd_mode(const FwdLaunch& a, const FwdParams& p, dim3 grid,
+                            const PlanOf<kMode>& plan, cudaStream_t st) {
+  using L = FwdSmem<D>;
+  cudaError_t e = set_smem_once<fwd_kernel<D, kMode>>(L::kAlloc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kFwdThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fwd_kernel<D, kMode>, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
+                            (p.tma_out || p.tma_dec) ? *a.mO32 : *a.mQ, p, plan);
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdSmem<D>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
   // kFwdTrain: fixed layout, no window, bf16 output stored by TMA
   const bool general = !a.decode && (a.cu || a.window > 0 || a.out_f32 || !a.mO32);
-  auto* kern = a.decode ? fwd_kernel<D, kFwdDecode>
-                        : (general ? fwd_kernel<D, kFwdGeneral> : fwd_kernel<D, kFwdTrain>);
-  cudaError_t e = a.decode ? set_smem_once<fwd_kernel<D, kFwdDecode>>(L::kAlloc)
-                           : (general ? set_smem_once<fwd_kernel<D, kFwdGeneral>>(L::kAlloc)
-                                      : set_smem_once<fwd_kernel<D, kFwdTrain>>(L::kAlloc));
-  if (e != cudaSuccess) return e;
   FwdParams p{};
   p.n_rows = a.n_rows;
   p.Hq_map = a.Hq_map;
@@ -950,28 +1094,31 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
     p.total = a.total;
   }
   p.window = a.window;
-  dim3 grid;
-  if (!a.decode) {
-    // persistent: one CTA per SM, none idle from the start
-    const int nsm = sm_count();
-    if (nsm < 1) return cudaErrorInvalidValue;
-    grid = dim3(static_cast<unsigned>(p.n_items < nsm ? p.n_items : nsm), 1, 1);
-  } else {
-    grid = dim3(a.Hq_map, p.n_pairs, a.n_splits);
+  if (a.decode) {
+    PlanOf<kFwdDecode> none{};
+    return launch_fwd_mode<D, kFwdDecode>(a, p, dim3(a.Hq_map, p.n_pairs, a.n_splits), none, st);
   }
-  TraceScope tr(a.decode ? nullptr : "fwd", st);  // decode: traced as one step
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kFwdThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::kAlloc;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, *a.mQ, *a.mKc, *a.mVc, *a.mK, *a.mV,
-                            (p.tma_out || p.tma_dec) ? *a.mO32 : *a.mQ, p);
+  // persistent: one CTA per SM, none idle from the start
+  const int nsm = sm_count();
+  if (nsm < 1) return cudaErrorInvalidValue;
+  const int g = p.n_items < nsm ? p.n_items : nsm;
+  TraceScope tr("fwd", st);
+  if (general) {
+    PlanOf<kFwdGeneral> none{};
+    return launch_fwd_mode<D, kFwdGeneral>(a, p, dim3(g, 1, 1), none, st);
+  }
+  static thread_local PlanOf<kFwdTrain> plan;
+  plan.n = 0;
+  if (p.n_items <= kPlanItems && g <= kPlanCtas) {
+    std::vector<uint16_t> off;
+    const std::vector<uint16_t>& items =
+        fwd_plan(p.n_pairs, a.Hq_map * a.n_qblocks, (a.p + kTile - 1) / kTile, p.n_qtiles, g,
+                 &off);
+    plan.n = static_cast<int>(items.size());
+    std::memcpy(plan.off, off.data(), off.size() * sizeof(uint16_t));
+    std::memcpy(plan.items, items.data(), items.size() * sizeof(uint16_t));
+  }
+  return launch_fwd_mode<D, kFwdTrain>(a, p, dim3(g, 1, 1), plan, st);
 }
 
 }  // namespace
