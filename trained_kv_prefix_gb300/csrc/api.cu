@@ -7,8 +7,10 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <queue>
 
 #include "internal.cuh"
 
@@ -44,6 +46,75 @@ int sm_count() {
       cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     cache[dev] = 0;
   return cache[dev];
+}
+
+void build_work_plan(const std::vector<double>& cost, int grid, std::vector<uint16_t>* items,
+                     std::vector<uint16_t>* off) {
+  const int n = static_cast<int>(cost.size());
+  std::vector<std::vector<int>> per(grid);
+  std::vector<double> load(grid, 0.0);
+  std::vector<int> order(n);
+  for (int w = 0; w < n; ++w) order[w] = w;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> q;
+  for (int c = 0; c < grid; ++c) q.push({0.0, c});
+  for (int w : order) {
+    const Slot sl = q.top();
+    q.pop();
+    per[sl.second].push_back(w);
+    load[sl.second] += cost[w];
+    q.push({load[sl.second], sl.second});
+  }
+  for (int iter = 0; iter < 100000; ++iter) {
+    const int cm = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
+    double best = load[cm];
+    int bj = -1, ba = -1, bb = -1;  // move per[cm][ba] to CTA bj (bb < 0) or swap with per[bj][bb]
+    for (int j = 0; j < grid; ++j) {
+      if (j == cm) continue;
+      for (int ia = 0; ia < static_cast<int>(per[cm].size()); ++ia) {
+        const double ca = cost[per[cm][ia]];
+        const double mv = std::max(load[cm] - ca, load[j] + ca);
+        if (mv < best - 1e-9) {
+          best = mv;
+          bj = j;
+          ba = ia;
+          bb = -1;
+        }
+        for (int ib = 0; ib < static_cast<int>(per[j].size()); ++ib) {
+          const double d = ca - cost[per[j][ib]];
+          if (d <= 1e-9) continue;
+          const double sw = std::max(load[cm] - d, load[j] + d);
+          if (sw < best - 1e-9) {
+            best = sw;
+            bj = j;
+            ba = ia;
+            bb = ib;
+          }
+        }
+      }
+    }
+    if (bj < 0) break;
+    const int wa = per[cm][ba];
+    per[cm].erase(per[cm].begin() + ba);
+    per[bj].push_back(wa);
+    load[cm] -= cost[wa];
+    load[bj] += cost[wa];
+    if (bb >= 0) {
+      const int wb = per[bj][bb];
+      per[bj].erase(per[bj].begin() + bb);
+      per[cm].push_back(wb);
+      load[bj] -= cost[wb];
+      load[cm] += cost[wb];
+    }
+  }
+  items->clear();
+  off->assign(1, 0);
+  for (int c = 0; c < grid; ++c) {
+    std::sort(per[c].begin(), per[c].end(), [&](int x, int y) { return cost[x] > cost[y]; });
+    for (int w : per[c]) items->push_back(static_cast<uint16_t>(w));
+    off->push_back(static_cast<uint16_t>(items->size()));
+  }
 }
 
 namespace {

@@ -31,7 +31,12 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <type_traits>
+#include <vector>
 
 #include "internal.cuh"
 #include "ptx.cuh"
@@ -790,12 +795,17 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& a, int w, const int* 
   return I;
 }
 
+// The fixed-layout instance takes a static schedule of its items (WorkPlan);
+// the packed / windowed one takes items from the counter.
+template <bool kGeneral>
+using DqPlanOf = WorkPlan<kGeneral ? 1 : kPlanItems>;
+
 template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kDqThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
               const __grid_constant__ CUtensorMap mKc, const __grid_constant__ CUtensorMap mVc,
               const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
-              const BwdParams a) {
+              const BwdParams a, const __grid_constant__ DqPlanOf<kGeneral> plan) {
   using L = DqSmem<D>;
   constexpr int SK = kDqKStages, SV = kDqVStages;
   extern __shared__ __align__(1024) uint8_t dq_smem[];
@@ -860,7 +870,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tma_prefetch_desc(&mVc);
       tma_prefetch_desc(&mK);
       tma_prefetch_desc(&mV);
-      auto fetch = [&]() -> int {
+      // the next item: the static plan's if there is one, else the counter's
+      auto fetch = [&](int k) -> int {
+        if (!kGeneral && plan.n > 0) {
+          const int o = plan.off[blockIdx.x] + k;
+          return o < plan.off[blockIdx.x + 1] ? static_cast<int>(plan.items[o]) : -1;
+        }
         const int w = atomicAdd(a.sched, 1);
         return w < a.n_items ? w : -1;
       };
@@ -868,7 +883,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       int nq = 0;  // Q / dO loads issued (items with work)
       int k_issued = 0, v_issued = 0;
       bool ok = true;
-      int w = fetch();
+      int w = fetch(0);
       for (int it = 0; ok; ++it) {
         const int sl = it & 1;
         if (it >= 2) {
@@ -893,7 +908,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         o.T = I.T;
         mbar_arrive(&bars[kDqItemFull0 + sl]);  // (release: the slot is visible to the waiters)
         if (w < 0) break;
-        const int w_next = fetch();
+        const int w_next = fetch(it + 1);
         if (I.T > 0) {
           // Q and dO of this item once the previous item's last S / dP MMA
           // has read them
@@ -1206,6 +1221,35 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
+// The static schedule of the fixed-layout dQ items (numbering of dq_item):
+// an item costs its key steps plus 2 for its start and end.  Cached per
+// geometry.
+const std::vector<uint16_t>& dq_plan(const BwdParams& p, int grid, std::vector<uint16_t>* off_out) {
+  constexpr double kItemCost = 2.0;
+  struct Plan {
+    std::vector<uint16_t> items, off;
+  };
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int>, Plan> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(p.Hq * p.B, p.n_qtiles, p.n_ct, p.n, grid);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    const int hb = p.Hq * p.B, n = hb * p.n_qtiles;
+    std::vector<double> cost(n);
+    for (int w = 0; w < n; ++w) {
+      const int qt = p.n_qtiles - 1 - w / hb;
+      const int last_q = std::min(qt * kTile + kTile, p.n) - 1;
+      cost[w] = p.n_ct + last_q / kTile + 1 + kItemCost;
+    }
+    Plan pl;
+    build_work_plan(cost, grid, &pl.items, &pl.off);
+    it = cache.emplace(key, std::move(pl)).first;
+  }
+  *off_out = it->second.off;
+  return it->second.items;
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t st_dq) {
   static_assert(DkdvSmem<D>::kAlloc <= 232448, "dkdv shared memory budget");
@@ -1263,9 +1307,24 @@ cudaError_t launch_bwd_d(const BwdLaunch& l, cudaStream_t st_dkdv, cudaStream_t 
   p.sched = l.sched;
   const int nsm = sm_count();
   if (nsm < 1 || !l.sched) return cudaErrorInvalidValue;
-  auto* kern_dq = general ? dq_kernel<D, true> : dq_kernel<D, false>;
-  kern_dq<<<p.n_items < nsm ? p.n_items : nsm, kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
-      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p);
+  const int grid = p.n_items < nsm ? p.n_items : nsm;
+  if (general) {
+    DqPlanOf<true> none{};
+    dq_kernel<D, true><<<grid, kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
+        *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p, none);
+    return cudaGetLastError();
+  }
+  static thread_local DqPlanOf<false> plan;
+  plan.n = 0;
+  if (p.n_items <= kPlanItems && grid <= kPlanCtas) {
+    std::vector<uint16_t> off;
+    const std::vector<uint16_t>& items = dq_plan(p, grid, &off);
+    plan.n = static_cast<int>(items.size());
+    std::memcpy(plan.off, off.data(), off.size() * sizeof(uint16_t));
+    std::memcpy(plan.items, items.data(), items.size() * sizeof(uint16_t));
+  }
+  dq_kernel<D, false><<<grid, kDqThreads, DqSmem<D>::kAlloc, st_dq>>>(
+      *l.mQ, *l.mdO, *l.mKc, *l.mVc, *l.mK, *l.mV, p, plan);
   return cudaGetLastError();
 }
 

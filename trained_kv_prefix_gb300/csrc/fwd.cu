@@ -263,20 +263,9 @@ __device__ __forceinline__ FwdItem train_item(const FwdParams& a, int w, const i
   return I;
 }
 
-// A static schedule of training work items over the persistent CTAs: CTA c
-// takes items[off[c] .. off[c+1]) in that order (n == 0: no plan, CTAs take
-// items from the counter instead).  Only the fixed-layout instance carries
-// the full arrays, as a kernel parameter.
-constexpr int kPlanCtas = 160;
-constexpr int kPlanItems = 4096;
-template <int N>
-struct FwdPlan {
-  int n;
-  uint16_t off[kPlanCtas + 1];
-  uint16_t items[N];
-};
+// Only the fixed-layout instance carries a full static schedule (WorkPlan).
 template <int kMode>
-using PlanOf = FwdPlan<kMode == kFwdTrain ? kPlanItems : 1>;
+using PlanOf = WorkPlan<kMode == kFwdTrain ? kPlanItems : 1>;
 
 // kMode: kFwdTrain (training, fixed [B, n] layout, no window, bf16 output),
 // kFwdGeneral (training with packed segments, a sliding window or an f32
@@ -935,13 +924,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-// A static schedule for `grid` persistent CTAs and the fixed-layout items
-// (numbering of train_item): each item costs its tiles (one unit = one
-// 128-key tile for one query tile) plus kItemCost for its start and end.
-// Longest-processing-time first onto the least loaded CTA, then moves and
-// swaps that lower the most loaded CTA's total while any does -- a tighter
-// fit than taking items in order from a counter when every CTA gets only a
-// few items.  Cached per geometry (its host cost is milliseconds).
+// The static schedule for `grid` persistent CTAs and the fixed-layout items
+// (numbering of train_item): an item costs its tiles (one unit = one 128-key
+// tile for one query tile) plus 2.5 for its start and end.  Cached per
+// geometry (its host cost is milliseconds).
 const std::vector<uint16_t>& fwd_plan(int n_pairs, int hb, int n_ct, int n_qtiles, int grid,
                                       std::vector<uint16_t>* off_out) {
   constexpr double kItemCost = 2.5;
@@ -963,73 +949,8 @@ const std::vector<uint16_t>& fwd_plan(int n_pairs, int hb, int n_ct, int n_qtile
       const int rB = hasB ? std::min(2 * pr + 2, n_qtiles) : 0;
       cost[w] = (hasB ? 2 : 1) * n_ct + rA + rB + kItemCost;
     }
-    std::vector<std::vector<int>> per(grid);
-    std::vector<double> load(grid, 0.0);
-    {
-      std::vector<int> order(n);
-      for (int w = 0; w < n; ++w) order[w] = w;
-      std::stable_sort(order.begin(), order.end(),
-                       [&](int x, int y) { return cost[x] > cost[y]; });
-      using Slot = std::pair<double, int>;
-      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> q;
-      for (int c = 0; c < grid; ++c) q.push({0.0, c});
-      for (int w : order) {
-        const Slot sl = q.top();
-        q.pop();
-        per[sl.second].push_back(w);
-        load[sl.second] += cost[w];
-        q.push({load[sl.second], sl.second});
-      }
-    }
-    for (int iter = 0; iter < 100000; ++iter) {
-      const int cm = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
-      double best = load[cm];
-      int bj = -1, ba = -1, bb = -1;  // move per[cm][ba] to CTA bj (bb < 0) or swap with per[bj][bb]
-      for (int j = 0; j < grid; ++j) {
-        if (j == cm) continue;
-        for (int ia = 0; ia < static_cast<int>(per[cm].size()); ++ia) {
-          const double ca = cost[per[cm][ia]];
-          const double mv = std::max(load[cm] - ca, load[j] + ca);
-          if (mv < best - 1e-9) {
-            best = mv;
-            bj = j;
-            ba = ia;
-            bb = -1;
-          }
-          for (int ib = 0; ib < static_cast<int>(per[j].size()); ++ib) {
-            const double d = ca - cost[per[j][ib]];
-            if (d <= 1e-9) continue;
-            const double sw = std::max(load[cm] - d, load[j] + d);
-            if (sw < best - 1e-9) {
-              best = sw;
-              bj = j;
-              ba = ia;
-              bb = ib;
-            }
-          }
-        }
-      }
-      if (bj < 0) break;
-      const int wa = per[cm][ba];
-      per[cm].erase(per[cm].begin() + ba);
-      per[bj].push_back(wa);
-      load[cm] -= cost[wa];
-      load[bj] += cost[wa];
-      if (bb >= 0) {
-        const int wb = per[bj][bb];
-        per[bj].erase(per[bj].begin() + bb);
-        per[cm].push_back(wb);
-        load[bj] -= cost[wb];
-        load[cm] += cost[wb];
-      }
-    }
     Plan pl;
-    pl.off.push_back(0);
-    for (int c = 0; c < grid; ++c) {
-      std::sort(per[c].begin(), per[c].end(), [&](int x, int y) { return cost[x] > cost[y]; });
-      for (int w : per[c]) pl.items.push_back(static_cast<uint16_t>(w));
-      pl.off.push_back(static_cast<uint16_t>(pl.items.size()));
-    }
+    build_work_plan(cost, grid, &pl.items, &pl.off);
     it = cache.emplace(key, std::move(pl)).first;
   }
   *off_out = it->second.off;

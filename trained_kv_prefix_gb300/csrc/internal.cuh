@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 #include "../../include/cartattn.h"
 
@@ -167,6 +168,25 @@ cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const Ro
 
 // Multiprocessors of the current device (cached per device; 0 on error).
 int sm_count();
+
+// A static schedule of work items over persistent CTAs, passed as a kernel
+// parameter: CTA c takes items[off[c] .. off[c+1]) in that order (n == 0: no
+// plan; the CTAs take items from a counter instead).
+constexpr int kPlanCtas = 160;
+constexpr int kPlanItems = 4096;
+template <int N>
+struct WorkPlan {
+  int n;
+  uint16_t off[kPlanCtas + 1];
+  uint16_t items[N];
+};
+// Host: items 0..cost.size()-1 onto `grid` CTAs -- longest processing time
+// first onto the least loaded CTA, then moves and swaps that lower the most
+// loaded CTA's total while any does (a tighter fit than taking items in
+// order from a counter when every CTA gets only a few).  Each CTA's items
+// come heaviest first.  cost.size() <= kPlanItems, grid <= kPlanCtas.
+void build_work_plan(const std::vector<double>& cost, int grid, std::vector<uint16_t>* items,
+                     std::vector<uint16_t>* off);
 
 // Rotate rows of x [B, n, H, d] (bf16 or f32) at positions pos0 + i using the
 // table (row i of the table = position pos0 + i) and write bf16 to out (same
