@@ -265,16 +265,26 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
       sr = seq_rows(cu, ntok, n, b);
       live = !kPacked || i0 + pl < sr.len;
     }
+    float lv = 0.f;
     if (live) {
+      // every load of the row in flight at once (d is 64 or 128: one or two
+      // 16-byte pieces of o and of dO per lane), the lse with them
       const long long row = (static_cast<long long>(sr.g0) + i0 + pl) * Hq + h;
-      for (int c = lane8 * 8; c < d; c += 64) {
-        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + row * d + c));
-        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + row * d + c));
-        const uint32_t po[4] = {ov.x, ov.y, ov.z, ov.w};
-        const uint32_t pg[4] = {gv.x, gv.y, gv.z, gv.w};
+      const uint4* po = reinterpret_cast<const uint4*>(o + row * d + lane8 * 8);
+      const uint4* pg = reinterpret_cast<const uint4*>(dout + row * d + lane8 * 8);
+      if (lane8 == 0) lv = __ldg(lse + lse_index(cu, ntok, n, Hq, b, h, sr, i0 + pl));
+      uint4 ov[2], gv[2];
+      ov[0] = __ldg(po);
+      gv[0] = __ldg(pg);
+      ov[1] = d > 64 ? __ldg(po + 8) : make_uint4(0u, 0u, 0u, 0u);
+      gv[1] = d > 64 ? __ldg(pg + 8) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t a4[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+        const uint32_t g4[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 fo = bf16x2_to_float2(po[e]), fg = bf16x2_to_float2(pg[e]);
+          const float2 fo = bf16x2_to_float2(a4[e]), fg = bf16x2_to_float2(g4[e]);
           acc += fo.x * fg.x + fo.y * fg.y;
         }
       }
@@ -285,9 +295,7 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     if (lane8 == 0 && rr < rows) {
       const long long bh = static_cast<long long>(b) * Hq + h;
       nDvec[bh * npad + i0 + pl] = live ? -acc : 0.f;
-      nlse2[bh * npad + i0 + pl] =
-          live ? __ldg(lse + lse_index(cu, ntok, n, Hq, b, h, sr, i0 + pl)) * -1.4426950408889634f
-               : -INFINITY;
+      nlse2[bh * npad + i0 + pl] = live ? lv * -1.4426950408889634f : -INFINITY;
     }
   }
   // padding rows of this block's positions
