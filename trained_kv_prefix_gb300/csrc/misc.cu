@@ -25,9 +25,12 @@ int grid_for(long long work, int per_block = kThreads) {
 }
 
 // ---------------------------------------------------------- cache write ----
-// One thread converts 8 consecutive values of one cartridge row; the second
-// tensor (src1 -> dst1, may be absent) continues the index range of the
-// first, so K and V go in one launch.
+// One thread converts kCacheBatch runs of 8 consecutive values of a
+// cartridge row, one grid stride apart, with all their loads issued before
+// any store; the second tensor (src1 -> dst1, may be absent) continues the
+// index range of the first, so K and V go in one launch.
+constexpr int kCacheBatch = 4;
+
 __global__ void write_to_cache_kernel(const float* __restrict__ src0, void* __restrict__ dst0,
                                       const float* __restrict__ src1, void* __restrict__ dst1,
                                       int p, int row_elems, long long row_stride, int dst_row0,
@@ -35,29 +38,43 @@ __global__ void write_to_cache_kernel(const float* __restrict__ src0, void* __re
   const int vec_per_row = row_elems / 8;
   const long long per = static_cast<long long>(p) * vec_per_row;
   const long long total = src1 ? 2 * per : per;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t0 < total;
-       t0 += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const bool second = t0 >= per;
-    const long long t = second ? t0 - per : t0;
-    const float* src = second ? src1 : src0;
-    void* dst = second ? dst1 : dst0;
-    const int r = static_cast<int>(t / vec_per_row);
-    const int c = static_cast<int>(t % vec_per_row) * 8;
-    const float4* s =
-        reinterpret_cast<const float4*>(src + static_cast<long long>(r) * row_elems + c);
-    const float4 a = __ldg(s), b = __ldg(s + 1);
-    const long long off = static_cast<long long>(dst_row0 + r) * row_stride + c;
-    if (dst_bf16) {
-      uint4 o;
-      o.x = pack_bf16x2(a.x, a.y);
-      o.y = pack_bf16x2(a.z, a.w);
-      o.z = pack_bf16x2(b.x, b.y);
-      o.w = pack_bf16x2(b.z, b.w);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + off) = o;
-    } else {
-      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dst) + off);
-      d[0] = a;
-      d[1] = b;
+       t0 += stride * kCacheBatch) {
+    float4 a[kCacheBatch], b[kCacheBatch];
+#pragma unroll
+    for (int u = 0; u < kCacheBatch; ++u) {
+      const long long t1 = t0 + u * stride;
+      if (t1 < total) {
+        const bool second = t1 >= per;
+        const long long t = second ? t1 - per : t1;
+        const float4* s = reinterpret_cast<const float4*>((second ? src1 : src0) + t * 8);
+        a[u] = __ldg(s);
+        b[u] = __ldg(s + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCacheBatch; ++u) {
+      const long long t1 = t0 + u * stride;
+      if (t1 >= total) break;
+      const bool second = t1 >= per;
+      const long long t = second ? t1 - per : t1;
+      void* dst = second ? dst1 : dst0;
+      const int r = static_cast<int>(t / vec_per_row);
+      const int c = static_cast<int>(t % vec_per_row) * 8;
+      const long long off = static_cast<long long>(dst_row0 + r) * row_stride + c;
+      if (dst_bf16) {
+        uint4 o;
+        o.x = pack_bf16x2(a[u].x, a[u].y);
+        o.y = pack_bf16x2(a[u].z, a[u].w);
+        o.z = pack_bf16x2(b[u].x, b[u].y);
+        o.w = pack_bf16x2(b[u].z, b[u].w);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + off) = o;
+      } else {
+        float4* d = reinterpret_cast<float4*>(static_cast<float*>(dst) + off);
+        d[0] = a[u];
+        d[1] = b[u];
+      }
     }
   }
 }
@@ -415,7 +432,7 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
   if (!src0) return cudaSuccess;
   const long long work = static_cast<long long>(p) * (row_elems / 8) * (src1 ? 2 : 1);
   TraceScope tr("write_to_cache", st);
-  write_to_cache_kernel<<<grid_for(work), kThreads, 0, st>>>(
+  write_to_cache_kernel<<<grid_for((work + kCacheBatch - 1) / kCacheBatch), kThreads, 0, st>>>(
       src0, dst0, src1, src1 ? dst1 : nullptr, p, row_elems, row_stride, dst_row0, dst_bf16 ? 1 : 0);
   return cudaGetLastError();
 }
