@@ -616,6 +616,7 @@ static int fwd_impl(const cart_geom* g, const Packing& pk, cart_dtype in, cart_d
   l.out_f32 = in == CART_F32;
   l.lse = lse;
   l.decode = false;
+  l.pdl = true;  // the kernel waits for the prep launch before it reads anything
   l.sched = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + w.sched);
   l.cu = pk.cu;
   l.total = pk.total;

@@ -368,6 +368,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t abort_s = smem_u32(&abort_flag);
+  // (training launches are programmatic dependents of the prep kernel: the
+  // set-up above overlaps its end; no global access before this)
+  pdl_wait();
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer --
@@ -481,6 +484,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         w = w_next;
       }
+      // training: every load of this CTA is issued; the next launch on the
+      // stream (which waits for this grid before it touches memory) may
+      // start setting up
+      if (!kDecode) pdl_release();
       if (!ok) {
         // Give the copies still in flight (the last Q load, the last two K
         // and V tiles) a bounded chance to land before the CTA releases its

@@ -32,6 +32,26 @@ cudaError_t set_smem_once(int bytes) {
   return e;
 }
 
+// Launches kern<<<grid, block, smem, st>>>(args...) as the programmatic
+// dependent of the previous kernel on st: it may start while that kernel
+// still runs, and calls pdl_wait() (ptx.cuh) in every thread before it
+// touches global memory, so the stream order of memory effects is kept.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Device status word (bits from ptx.cuh); one per device.
 uint32_t* device_status_ptr();
 

@@ -35,6 +35,8 @@ __global__ void write_to_cache_kernel(const float* __restrict__ src0, void* __re
                                       const float* __restrict__ src1, void* __restrict__ dst1,
                                       int p, int row_elems, long long row_stride, int dst_row0,
                                       int dst_bf16) {
+  pdl_wait();
+  pdl_release();
   const int vec_per_row = row_elems / 8;
   const long long per = static_cast<long long>(p) * vec_per_row;
   const long long total = src1 ? 2 * per : per;
@@ -222,6 +224,8 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     const float* __restrict__ lse, float* __restrict__ nDvec, float* __restrict__ nlse2, int npad,
     int ppc, const int* __restrict__ cu_arg, int ntok, int* sched, uint32_t* status) {
   const int* const cu = kPacked ? cu_arg : nullptr;
+  pdl_wait();
+  pdl_release();
   if (sched && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   __shared__ float2 cs[kPrepPos][kMaxHeadDim / 2];
   const int half = d / 2, chunks = half / 8;
@@ -432,9 +436,10 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
   if (!src0) return cudaSuccess;
   const long long work = static_cast<long long>(p) * (row_elems / 8) * (src1 ? 2 : 1);
   TraceScope tr("write_to_cache", st);
-  write_to_cache_kernel<<<grid_for((work + kCacheBatch - 1) / kCacheBatch), kThreads, 0, st>>>(
-      src0, dst0, src1, src1 ? dst1 : nullptr, p, row_elems, row_stride, dst_row0, dst_bf16 ? 1 : 0);
-  return cudaGetLastError();
+  return launch_dependent(write_to_cache_kernel,
+                          dim3(grid_for((work + kCacheBatch - 1) / kCacheBatch)), dim3(kThreads), 0,
+                          st, src0, dst0, src1, src1 ? dst1 : nullptr, p, row_elems, row_stride,
+                          dst_row0, dst_bf16 ? 1 : 0);
 }
 
 cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
@@ -450,9 +455,9 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(o ? "bwd_prep" : "fwd_prep", st);
   auto* kern = cu ? train_prep_kernel<true> : train_prep_kernel<false>;
-  kern<<<grid, kThreads, 0, st>>>(q, k, qr, kr, table, f, p, B, n, Hq, Hkv, d, o, dout, lse, nDvec,
-                                  nlse2, npad, ppc, cu, total, sched, device_status_ptr());
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), 0, st, q, k, qr, kr, table, f, p, B, n,
+                          Hq, Hkv, d, o, dout, lse, nDvec, nlse2, npad, ppc, cu, total, sched,
+                          device_status_ptr());
 }
 
 cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,

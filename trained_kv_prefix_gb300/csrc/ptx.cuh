@@ -53,6 +53,18 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched as the programmatic
+// dependent of the previous kernel on its stream may start before that
+// kernel ends; pdl_wait() returns once it (and so, transitively, all earlier
+// work on the stream) has completed with its writes visible, and is a no-op
+// for a plain launch.  Every thread of such a kernel calls it before its
+// first global-memory access.  pdl_release() lets this grid's own dependent
+// launch (it still waits for this grid before touching memory).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
