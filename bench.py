@@ -2,9 +2,11 @@
 """Benchmark of the cartridge-attention hot path on GB300.
 
 One step = one pass over every step of the path on synthetic data:
-  a1  cartridge write: f32 leaf rows -> bf16 shadow        (cart_write_to_cache)
+  a1  cartridge write: f32 leaf rows -> bf16 shadow        (cart_attn_fwd given
+      the f32 leaves: its prep launch writes the shadow into the workspace)
   a2-a4  training forward (RoPE at p+i, end-aligned mask)  (cart_attn_fwd)
-  a5-a8  training backward into the cartridge rows          (cart_attn_bwd)
+  a5-a8  training backward into the cartridge rows          (cart_attn_bwd, reading
+      the forward's workspace)
          [N > 1: all-reduce(SUM) of the cartridge gradients]
   a9  one decode step of 64 conversations behind a shared cartridge
                                                             (cart_attn_decode)
@@ -461,28 +463,28 @@ def measure_train_workload(ts, dev, rank, peaks, flush, steps, bwd=True):
 
     stream = torch.cuda.current_stream(dev)
     tin = {k: v.to(dev) for k, v in synth.train_inputs(ts, seed=ts.seed + 1000 * rank).items()}
-    kcb = torch.empty(tin["kc"].shape, dtype=torch.bfloat16, device=dev)
-    vcb = torch.empty_like(kcb)
     o = torch.empty_like(tin["q"])
     lse = torch.empty((ts.B, ts.Hq, ts.n), dtype=torch.float32, device=dev)
     g = cartattn.geom(ts.B, ts.n, ts.Hq, ts.Hkv, ts.d, ts.p, ts.frozen_prefix, None, ts.theta)
-    ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+    # f32 cartridge leaves: the forward's prep launch writes their bf16 shadow
+    ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, cartattn.CART_F32), dtype=torch.uint8,
+                       device=dev)
     grads = None
     if bwd:
         grads = dict(dq=torch.empty_like(tin["q"]), dk=torch.empty_like(tin["k"]),
                      dv=torch.empty_like(tin["v"]),
                      dkc=torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev),
                      dvc=torch.empty((ts.p, ts.Hkv, ts.d), dtype=torch.float32, device=dev))
-        ws_b = torch.empty(cartattn.bwd_reuse_workspace_size(g, 0, 0), dtype=torch.uint8,
-                           device=dev)
+        ws_b = torch.empty(cartattn.bwd_reuse_workspace_size(g, 0, cartattn.CART_F32),
+                           dtype=torch.uint8, device=dev)
 
     def step():
-        cartattn.cart_write_to_cache(tin["kc"], tin["vc"], kcb, vcb)
-        cartattn.cart_attn_fwd(tin["q"], tin["k"], tin["v"], kcb, vcb,
+        cartattn.cart_attn_fwd(tin["q"], tin["k"], tin["v"], tin["kc"], tin["vc"],
                                frozen_prefix=ts.frozen_prefix, theta=ts.theta, o=o, lse=lse,
                                workspace=ws_f)
         if bwd:
-            cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], kcb, vcb, o, lse, tin["do"],
+            cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], tin["kc"], tin["vc"], o, lse,
+                                   tin["do"],
                                    frozen_prefix=ts.frozen_prefix, theta=ts.theta,
                                    workspace=ws_b, fwd_workspace=ws_f, **grads)
 
@@ -575,8 +577,6 @@ def main():
     tin = {k: v.to(dev) for k, v in synth.train_inputs(ts, seed=ts.seed + 1000 * rank).items()}
     din = {k: v.to(dev) for k, v in synth.decode_inputs(ds, seed=ds.seed + 1000 * rank).items()}
     lens = din["lens"].cpu().numpy()
-    kcb = torch.empty(tin["kc"].shape, dtype=torch.bfloat16, device=dev)
-    vcb = torch.empty_like(kcb)
     o = torch.empty_like(tin["q"])
     lse = torch.empty((ts.B, ts.Hq, ts.n), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(tin["q"]), torch.empty_like(tin["k"]), torch.empty_like(tin["v"])
@@ -584,18 +584,22 @@ def main():
     dvc = torch.empty_like(dkc)
     od = torch.empty_like(din["q"])
     g = cartattn.geom(ts.B, ts.n, ts.Hq, ts.Hkv, ts.d, ts.p, ts.frozen_prefix, None, ts.theta)
-    ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(cartattn.bwd_reuse_workspace_size(g, 0, 0), dtype=torch.uint8, device=dev)
+    # f32 cartridge leaves: the forward's prep launch writes their bf16 shadow
+    # into ws_f, where the backward reads it
+    ws_f = torch.empty(cartattn.fwd_workspace_size(g, 0, cartattn.CART_F32), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(cartattn.bwd_reuse_workspace_size(g, 0, cartattn.CART_F32),
+                       dtype=torch.uint8, device=dev)
     ws_d = torch.empty(cartattn.decode_workspace_size(ds.B, ds.Hq, ds.Hkv, ds.d, ds.p,
                                                       ds.cache_rows), dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def train_part():
-        cartattn.cart_write_to_cache(tin["kc"], tin["vc"], kcb, vcb)
-        cartattn.cart_attn_fwd(tin["q"], tin["k"], tin["v"], kcb, vcb, frozen_prefix=ts.frozen_prefix,
-                               theta=ts.theta, o=o, lse=lse, workspace=ws_f)
-        cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], kcb, vcb, o, lse, tin["do"],
+        cartattn.cart_attn_fwd(tin["q"], tin["k"], tin["v"], tin["kc"], tin["vc"],
+                               frozen_prefix=ts.frozen_prefix, theta=ts.theta, o=o, lse=lse,
+                               workspace=ws_f)
+        cartattn.cart_attn_bwd(tin["q"], tin["k"], tin["v"], tin["kc"], tin["vc"], o, lse, tin["do"],
                                frozen_prefix=ts.frozen_prefix, theta=ts.theta, dq=dq, dk=dk, dv=dv,
                                dkc=dkc, dvc=dvc, workspace=ws_b, fwd_workspace=ws_f)
         cdist.allreduce_cartridge_grads(dkc, dvc)
@@ -751,11 +755,11 @@ def main():
         def e2e_step():
             for k2, v in host.items():
                 dev_in[k2].copy_(v, non_blocking=True)
-            cartattn.cart_write_to_cache(dev_in["kc"], dev_in["vc"], kcb, vcb)
-            cartattn.cart_attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], kcb, vcb,
-                                   frozen_prefix=ts.frozen_prefix, theta=ts.theta, o=o, lse=lse,
-                                   workspace=ws_f)
-            cartattn.cart_attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], kcb, vcb, o, lse,
+            cartattn.cart_attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["kc"],
+                                   dev_in["vc"], frozen_prefix=ts.frozen_prefix, theta=ts.theta,
+                                   o=o, lse=lse, workspace=ws_f)
+            cartattn.cart_attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["kc"],
+                                   dev_in["vc"], o, lse,
                                    dev_in["do"], frozen_prefix=ts.frozen_prefix, theta=ts.theta,
                                    dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc, workspace=ws_b,
                                    fwd_workspace=ws_f)

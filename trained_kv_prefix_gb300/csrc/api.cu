@@ -454,12 +454,22 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
   float2* table = reinterpret_cast<float2*>(ws + w.table);
   __nv_bfloat16* qr = reinterpret_cast<__nv_bfloat16*>(ws + w.qr);
   __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(ws + w.kr);
+  const bool cart_f32 = cd == CART_F32 && g->p > 0;
   if (!f32) {
+    // f32 cartridge leaves: their bf16 copies come from the same launch
+    CartCast cast;
+    if (cart_f32) {
+      cast.kc = static_cast<const float*>(kc);
+      cast.vc = static_cast<const float*>(vc);
+      cast.kcb = reinterpret_cast<__nv_bfloat16*>(ws + w.kcb);
+      cast.vcb = reinterpret_cast<__nv_bfloat16*>(ws + w.vcb);
+      cast.elems = static_cast<long long>(g->p) * g->Hkv * g->d;
+    }
     CART_CUDA(launch_train_prep(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         qr, kr, table, freqs, g->p, g->B, g->n, g->Hq, g->Hkv, g->d,
         static_cast<const __nv_bfloat16*>(vec.o), static_cast<const __nv_bfloat16*>(vec.dout),
-        vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, sched, st));
+        vec.lse, vec.nDvec, vec.nlse2, vec.npad, pk.cu, pk.total, sched, st, cast));
   } else {
     CART_CUDA(launch_rope_table(table, g->p, g->n, g->d, freqs, sched, st));
     CART_CUDA(launch_rope_rows(q, f32, qr, table, g->B, g->n, g->Hq, g->d, true, pk.cu, pk.total,
@@ -476,12 +486,15 @@ int train_prep(const cart_geom* g, cart_dtype in, cart_dtype cd, const void* q, 
   }
   const void* kcb = kc;
   const void* vcb = vc;
-  if (cd == CART_F32 && g->p > 0) {
+  if (cart_f32) {
     __nv_bfloat16* tk = reinterpret_cast<__nv_bfloat16*>(ws + w.kcb);
     __nv_bfloat16* tv = reinterpret_cast<__nv_bfloat16*>(ws + w.vcb);
-    const int row = g->Hkv * g->d;
-    CART_CUDA(launch_write_to_cache(static_cast<const float*>(kc), tk, static_cast<const float*>(vc),
-                                    tv, g->p, row, row, 0, true, st));
+    if (f32) {  // (bf16 inputs: made by the prep launch above)
+      const int row = g->Hkv * g->d;
+      CART_CUDA(launch_write_to_cache(static_cast<const float*>(kc), tk,
+                                      static_cast<const float*>(vc), tv, g->p, row, row, 0, true,
+                                      st));
+    }
     kcb = tk;
     vcb = tv;
   }

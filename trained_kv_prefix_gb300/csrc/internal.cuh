@@ -174,12 +174,21 @@ cudaError_t launch_write_to_cache(const float* src0, void* dst0, const float* sr
 // cu / total: the packed layout (see SeqRows; cu == nullptr: fixed); the
 // packed table is checked here (status bit kDevErrSegments).
 // sched (may be null): the forward's work-item counter, set to 0.
+// bf16 copies of f32 cartridge leaves, made by the same prep launch:
+// kcb/vcb[e] = bf16(kc/vc[e]) for e < elems (a multiple of 8); kc null: none.
+struct CartCast {
+  const float* kc = nullptr;
+  const float* vc = nullptr;
+  __nv_bfloat16* kcb = nullptr;
+  __nv_bfloat16* vcb = nullptr;
+  long long elems = 0;
+};
 cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __nv_bfloat16* qr,
                               __nv_bfloat16* kr, float2* table, const RopeFreqs& f, int p, int B,
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
                               const __nv_bfloat16* dout, const float* lse, float* nDvec,
                               float* nlse2, int npad, const int* cu, int total, int* sched,
-                              cudaStream_t st);
+                              cudaStream_t st, const CartCast& cast = CartCast());
 
 // cos/sin table for positions [pos0, pos0 + npos): float2 [npos, d/2]; sets
 // *sched to 0 when sched is given (as launch_train_prep).

@@ -184,6 +184,7 @@ __global__ void rope_rows_kernel(const void* __restrict__ xv, __nv_bfloat16* __r
 //     rope_cs_turns; positions must stay below 2^24);
 //   * K rotated at p + i for every (sequence, kv head), and Q for every
 //     (sequence, head) when qr is given (the forward rotates Q itself);
+//   * the bf16 copies of f32 cartridge leaves when cast.kc is given;
 //   * with o given (backward): the negated row vectors -D = -rowsum(dO * O)
 //     and -lse * log2(e) in [B, Hq, npad] (stored negated so that the
 //     backward kernels add them with packed two-lane arithmetic), padding
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
     const RopeFreqs f, int p, int B, int n, int Hq, int Hkv, int d,
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, float* __restrict__ nDvec, float* __restrict__ nlse2, int npad,
-    int ppc, const int* __restrict__ cu_arg, int ntok, int* sched, uint32_t* status) {
+    int ppc, const int* __restrict__ cu_arg, int ntok, int* sched, uint32_t* status,
+    const CartCast cast) {
   const int* const cu = kPacked ? cu_arg : nullptr;
   pdl_wait();
   pdl_release();
@@ -266,6 +268,21 @@ __global__ void __launch_bounds__(kThreads) train_prep_kernel(
   };
   if (kr) rotate_all(k, kr, Hkv);
   if (qr) rotate_all(q, qr, Hq);
+  if (cast.kc) {
+    // the cartridge leaves' bf16 copies: eight values per thread and step
+    // over the whole grid, K's then V's
+    const long long per = cast.elems / 8, all = 2 * per;
+    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < all;
+         t += static_cast<long long>(gridDim.x) * blockDim.x) {
+      const bool second = t >= per;
+      const long long u = second ? t - per : t;
+      const float4* src = reinterpret_cast<const float4*>((second ? cast.vc : cast.kc) + u * 8);
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      *reinterpret_cast<uint4*>((second ? cast.vcb : cast.kcb) + u * 8) =
+          make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                     pack_bf16x2(b.z, b.w));
+    }
+  }
   if (!o) return;
   // -D and -lse2: 8 lanes per (b, i, h) row, 4 rows per warp (uniform trip count)
   const int lane8 = threadIdx.x & 7;
@@ -447,7 +464,7 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
                               int n, int Hq, int Hkv, int d, const __nv_bfloat16* o,
                               const __nv_bfloat16* dout, const float* lse, float* nDvec,
                               float* nlse2, int npad, const int* cu, int total, int* sched,
-                              cudaStream_t st) {
+                              cudaStream_t st, const CartCast& cast) {
   const int span = o ? max(n, npad) : n;
   // positions per CTA: enough CTAs for about eight per SM, at most kPrepPos
   const int ppc = max(1, min(kPrepPos, (span + 152 * 8 - 1) / (152 * 8)));
@@ -457,7 +474,7 @@ cudaError_t launch_train_prep(const __nv_bfloat16* q, const __nv_bfloat16* k, __
   auto* kern = cu ? train_prep_kernel<true> : train_prep_kernel<false>;
   return launch_dependent(kern, dim3(grid), dim3(kThreads), 0, st, q, k, qr, kr, table, f, p, B, n,
                           Hq, Hkv, d, o, dout, lse, nDvec, nlse2, npad, ppc, cu, total, sched,
-                          device_status_ptr());
+                          device_status_ptr(), cast);
 }
 
 cudaError_t launch_rope_table(float2* table, int pos0, int npos, int d, const RopeFreqs& f,
