@@ -77,6 +77,10 @@ struct FwdParams {
   // training: work items and the counter CTAs take them from (zeroed by the
   // prep kernel that runs before the forward)
   int n_items;
+  // fixed-layout training with an even group size: an item's tile B is the
+  // same query tile of the next head (same kv head, same keys) instead of
+  // the next query tile of the same head
+  int cross;
   int* sched;
   // decode mode: raw query rows r = b*G + hh, rotated here at p + len[b]
   const int* dec_len;
@@ -197,6 +201,7 @@ enum FwdMode { kFwdTrain = 0, kFwdGeneral = 1, kFwdDecode = 2 };
 // from rt_lo up to each tile's diagonal.  T_x tiles for tile x (0: no work).
 struct FwdItem {
   int head, qb, pair, kvh, split;
+  int xh;       // tile B: the same rows of head + 1 (pair = their query tile)
   int seq_len;  // rows of the query block (decode: the stacked rows)
   SeqRows sq;   // training: where the query block's rows sit
   int n_ct, ct_lo, rt_lo, T_A, T_B, T;
@@ -207,7 +212,7 @@ struct FwdItem {
 // more items).  The other roles read each field where they use it (volatile
 // loads), so that no item field stays in registers across the softmax loop.
 struct ItemSlot {
-  int w, head, qb, pair, split, seq_len, row0, blk, g0, n_ct, ct_lo, rt_lo, T_A, T_B, T, pad;
+  int w, head, qb, pair, split, seq_len, row0, blk, g0, n_ct, ct_lo, rt_lo, T_A, T_B, T, xh;
 };
 static_assert(sizeof(ItemSlot) == 64, "item slot");
 
@@ -218,6 +223,13 @@ __device__ __forceinline__ void item_tiles(const FwdParams& a, FwdItem& I, int w
   I.T_A = I.T_B = I.T = I.n_ct = 0;
   I.rt_lo = 0;
   I.hasB = false;
+  if (I.xh) {  // two heads, query tile I.pair: the same keys for both
+    I.n_ct = (a.p + kTile - 1) / kTile;
+    I.ct_lo = 0;
+    I.hasB = true;
+    I.T_A = I.T_B = I.T = I.n_ct + min(I.pair + 1, n_qtiles);
+    return;
+  }
   if (2 * I.pair >= n_qtiles) return;  // a packed segment shorter than the longest
   I.hasB = 2 * I.pair + 1 < n_qtiles;
   const int n_ct_all = (a.p + kTile - 1) / kTile;
@@ -248,13 +260,22 @@ __device__ __forceinline__ void item_tiles(const FwdParams& a, FwdItem& I, int w
 // the later pairs more real tiles), so CTAs that take the next free item
 // form a longest-first schedule.
 __device__ __forceinline__ FwdItem train_item(const FwdParams& a, int w, const int* cu,
-                                              int window) {
+                                              int window, bool may_cross) {
   FwdItem I;
-  const int hb = a.Hq_map * a.n_qblocks;
-  I.pair = a.n_pairs - 1 - w / hb;
-  const int rem = w % hb;
-  I.head = rem % a.Hq_map;
-  I.qb = rem / a.Hq_map;
+  I.xh = may_cross && a.cross;
+  if (a.cross) {  // (query tile, sequence, head pair), query tile falling
+    const int hb = (a.Hq_map / 2) * a.n_qblocks;
+    I.pair = a.n_qtiles - 1 - w / hb;
+    const int rem = w % hb;
+    I.head = 2 * (rem % (a.Hq_map / 2));
+    I.qb = rem / (a.Hq_map / 2);
+  } else {
+    const int hb = a.Hq_map * a.n_qblocks;
+    I.pair = a.n_pairs - 1 - w / hb;
+    const int rem = w % hb;
+    I.head = rem % a.Hq_map;
+    I.qb = rem / a.Hq_map;
+  }
   I.kvh = I.head / a.G;
   I.split = 0;
   I.sq = seq_rows(cu, a.total, a.n_rows, I.qb);
@@ -405,7 +426,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!ok) break;
         }
         FwdItem I{};
-        if (w >= 0) I = kDecode ? dec : train_item(a, w, cu, window);
+        if (w >= 0) I = kDecode ? dec : train_item(a, w, cu, window, kMode == kFwdTrain);
         ItemSlot& o = items[sl];
         o.w = w;
         o.head = I.head;
@@ -422,6 +443,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         o.T_A = I.T_A;
         o.T_B = I.T_B;
         o.T = I.T;
+        o.xh = I.xh;
         mbar_arrive(&bars[kItemFull0 + sl]);  // (release: the slot is visible to the waiters)
         if (w < 0) break;
         const int w_next = fetch(it + 1);
@@ -432,7 +454,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                  mbar_wait(&bars[kQEmpty1], (nq - 1) & 1, abort_s, a.status, kDevErrTimeoutTma);
             if (!ok) break;
           }
-          const int q0A = 2 * I.pair * kTile;
+          // tile B: the next 128 rows, or (cross) the same rows of head + 1
+          const int q0A = (I.xh ? I.pair : 2 * I.pair) * kTile;
+          const int q0B = I.xh ? q0A : q0A + kTile;
           mbar_arrive_expect_tx(&bars[kQFull], 2 * L::kTileBytes);
 #pragma unroll
           for (int h = 0; h < D / 64; ++h) {
@@ -446,7 +470,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tma_load_4d(smem + L::kQ + h * 16384, &mQ, &bars[kQFull], h * 64, I.head,
                           I.sq.row0 + q0A, I.sq.blk);
               tma_load_4d(smem + L::kQ + L::kTileBytes + h * 16384, &mQ, &bars[kQFull], h * 64,
-                          I.head, I.sq.row0 + q0A + kTile, I.sq.blk);
+                          I.head + I.xh, I.sq.row0 + q0B, I.sq.blk);
             }
           }
           ++nq;
@@ -650,7 +674,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + (it & 1)]);
         continue;
       }
-      const int i = (2 * vld(sI.pair) + x) * kTile + row;  // query row within its block
+      // query row within its block (cross items: the pair's tile, head + x)
+      const int i = ((kMode == kFwdTrain && vld(sI.xh)) ? vld(sI.pair) : 2 * vld(sI.pair) + x) *
+                        kTile + row;
       const int seq_len = vld(sI.seq_len);
       float m = -INFINITY, l = 0.f;
       // decode: position of the row's first visible key (window > 0)
@@ -804,9 +830,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float inv_l = (kMode == kFwdTrain || l > 0.f) ? 1.f / l : 0.f;
       const bool row_ok = i < seq_len;
       const bool f32 = kDecode || a.out_f32;
-      const int head = vld(sI.head), split = vld(sI.split);
+      const int head =
+          vld(sI.head) + ((kMode == kFwdTrain && vld(sI.xh)) ? x : 0), split = vld(sI.split);
       const SeqRows sq = {vld(sI.row0), vld(sI.blk), vld(sI.g0), seq_len};
-      const int wr0 = (2 * vld(sI.pair) + x) * kTile + (warp & 3) * 32;
+      const int wr0 =
+          ((kMode == kFwdTrain && vld(sI.xh)) ? vld(sI.pair) : 2 * vld(sI.pair) + x) * kTile +
+          (warp & 3) * 32;
       // a packed segment's last rows: a TMA store of the warp's 32 rows would
       // run into the next segment, so those warps store row by row
       // (the fixed-layout training instance always has a bf16 output map)
@@ -936,20 +965,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // tile for one query tile) plus 2.5 for its start and end.  Cached per
 // geometry (its host cost is milliseconds).
 const std::vector<uint16_t>& fwd_plan(int n_pairs, int hb, int n_ct, int n_qtiles, int grid,
-                                      std::vector<uint16_t>* off_out) {
+                                      bool cross, std::vector<uint16_t>* off_out) {
   constexpr double kItemCost = 2.5;
   struct Plan {
     std::vector<uint16_t> items, off;
   };
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int, int>, Plan> cache;
+  static std::map<std::tuple<int, int, int, int, int, bool>, Plan> cache;
   std::lock_guard<std::mutex> lk(mu);
-  const auto key = std::make_tuple(n_pairs, hb, n_ct, n_qtiles, grid);
+  const auto key = std::make_tuple(n_pairs, hb, n_ct, n_qtiles, grid, cross);
   auto it = cache.find(key);
   if (it == cache.end()) {
-    const int n = n_pairs * hb;
+    // cross items: hb counts (sequence, head pair) and an item's two tiles
+    // are query tile t of both heads
+    const int n = (cross ? n_qtiles : n_pairs) * hb;
     std::vector<double> cost(n);
     for (int w = 0; w < n; ++w) {
+      if (cross) {
+        const int t = n_qtiles - 1 - w / hb;
+        cost[w] = 2 * (n_ct + t + 1) + kItemCost;
+        continue;
+      }
       const int pr = n_pairs - 1 - w / hb;
       const bool hasB = 2 * pr + 1 < n_qtiles;
       const int rA = std::min(2 * pr + 1, n_qtiles);
@@ -1008,7 +1044,10 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   p.tma_out = (!a.decode && !a.out_f32 && a.mO32) ? 1 : 0;
   p.tma_dec = (a.decode && a.mO32) ? 1 : 0;
   p.status = device_status_ptr();
-  p.n_items = p.n_pairs * a.Hq_map * a.n_qblocks;
+  // fixed-layout training with an even group size pairs heads, not tiles
+  p.cross = (!a.decode && !general && a.G % 2 == 0) ? 1 : 0;
+  p.n_items = p.cross ? p.n_qtiles * (a.Hq_map / 2) * a.n_qblocks
+                      : p.n_pairs * a.Hq_map * a.n_qblocks;
   p.sched = a.sched;
   if (a.decode) {
     p.dec_len = a.dec_len;
@@ -1040,8 +1079,8 @@ cudaError_t launch_fwd_d(const FwdLaunch& a, cudaStream_t st) {
   if (p.n_items <= kPlanItems && g <= kPlanCtas) {
     std::vector<uint16_t> off;
     const std::vector<uint16_t>& items =
-        fwd_plan(p.n_pairs, a.Hq_map * a.n_qblocks, (a.p + kTile - 1) / kTile, p.n_qtiles, g,
-                 &off);
+        fwd_plan(p.n_pairs, (p.cross ? a.Hq_map / 2 : a.Hq_map) * a.n_qblocks,
+                 (a.p + kTile - 1) / kTile, p.n_qtiles, g, p.cross != 0, &off);
     plan.n = static_cast<int>(items.size());
     std::memcpy(plan.off, off.data(), off.size() * sizeof(uint16_t));
     std::memcpy(plan.items, items.data(), items.size() * sizeof(uint16_t));
