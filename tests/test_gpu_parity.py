@@ -30,6 +30,9 @@ SMALL = [
     _shape("bf16_cart", 2, 160, 4, 1, 128, 200, cart="bf16", seed=107),
     _shape("f32_d128", 1, 150, 4, 2, 128, 140, dtype="f32", seed=108),
     _shape("frozen3", 1, 100, 4, 2, 64, 40, frozen=3, seed=109),
+    # an odd group (3 heads per kv head): the forward pairs query tiles of
+    # one head instead of one tile of two heads; ragged n, 3 query tiles
+    _shape("g3_odd_tiles", 2, 300, 6, 2, 128, 140, seed=113),
 ]
 
 
