@@ -743,7 +743,6 @@ def main():
     if args.e2e_steps > 0:
         host = {k: v.cpu().pin_memory() for k, v in synth.train_inputs(
             ts, seed=ts.seed + 1000 * rank).items()}
-        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         outs_h = {"dq": torch.empty_like(dq, device="cpu").pin_memory(),
                   "dk": torch.empty_like(dk, device="cpu").pin_memory(),
                   "dv": torch.empty_like(dv, device="cpu").pin_memory(),
@@ -751,35 +750,65 @@ def main():
                   "dvc": torch.empty_like(dvc, device="cpu").pin_memory()}
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+        # A pipelined trainer: inputs and gradients are double-buffered on the
+        # device; step i's host-to-device copy runs on a copy stream while
+        # step i-1's kernels run, and step i's gradients go back to the host
+        # on another stream while step i+1's kernels run.  Events keep each
+        # buffer's reuse in order.  Every step still copies all its inputs in
+        # and all its gradients out inside the timed region.
+        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+        dev_out = [{k: torch.empty_like(t) for k, t in (("dq", dq), ("dk", dk), ("dv", dv),
+                                                          ("dkc", dkc), ("dvc", dvc))}
+                   for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = {n: [torch.cuda.Event() for _ in range(2)]
+              for n in ("in_ready", "in_free", "out_ready", "out_free")}
 
-        def e2e_step():
-            for k2, v in host.items():
-                dev_in[k2].copy_(v, non_blocking=True)
-            cartattn.cart_attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["kc"],
-                                   dev_in["vc"], frozen_prefix=ts.frozen_prefix, theta=ts.theta,
+        def e2e_step(i):
+            b = i % 2
+            x, y = dev_in[b], dev_out[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev["in_free"][b])  # step i-2's kernels are done with x
+                for k2, v in host.items():
+                    x[k2].copy_(v, non_blocking=True)
+                ev["in_ready"][b].record(s_in)
+            stream.wait_event(ev["in_ready"][b])
+            if i >= 2:
+                stream.wait_event(ev["out_free"][b])  # step i-2's gradients have left y
+            cartattn.cart_attn_fwd(x["q"], x["k"], x["v"], x["kc"], x["vc"],
+                                   frozen_prefix=ts.frozen_prefix, theta=ts.theta,
                                    o=o, lse=lse, workspace=ws_f)
-            cartattn.cart_attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["kc"],
-                                   dev_in["vc"], o, lse,
-                                   dev_in["do"], frozen_prefix=ts.frozen_prefix, theta=ts.theta,
-                                   dq=dq, dk=dk, dv=dv, dkc=dkc, dvc=dvc, workspace=ws_b,
-                                   fwd_workspace=ws_f)
-            cdist.allreduce_cartridge_grads(dkc, dvc)
-            for k2, t in (("dq", dq), ("dk", dk), ("dv", dv), ("dkc", dkc), ("dvc", dvc)):
-                outs_h[k2].copy_(t, non_blocking=True)
+            cartattn.cart_attn_bwd(x["q"], x["k"], x["v"], x["kc"], x["vc"], o, lse, x["do"],
+                                   frozen_prefix=ts.frozen_prefix, theta=ts.theta,
+                                   dq=y["dq"], dk=y["dk"], dv=y["dv"], dkc=y["dkc"],
+                                   dvc=y["dvc"], workspace=ws_b, fwd_workspace=ws_f)
+            cdist.allreduce_cartridge_grads(y["dkc"], y["dvc"])
+            ev["in_free"][b].record(stream)
+            ev["out_ready"][b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["out_ready"][b])
+                for k2, t in y.items():
+                    outs_h[k2].copy_(t, non_blocking=True)
+                ev["out_free"][b].record(s_out)
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         cdist.barrier(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_in)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        e1.record(s_out)
         torch.cuda.synchronize(dev)
         e_ms = cdist.max_over_ranks([e0.elapsed_time(e1)], dev)[0]
         e2e = {"value": world * flops_step * args.e2e_steps / (e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / args.e2e_steps}
+               "ms_per_step": e_ms / args.e2e_steps,
+               "pipelined": "inputs and gradients double-buffered: step i's host-to-device "
+                            "copy overlaps step i-1's kernels, its device-to-host copy step "
+                            "i+1's; events from the first input copy to the last gradient copy"}
         # decode end to end: the new token's q/k/v and lengths in, o out
         dhost = {k: din[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "lens")}
         od_h = torch.empty_like(od, device="cpu").pin_memory()
