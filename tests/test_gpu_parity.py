@@ -297,6 +297,75 @@ def test_backward_is_deterministic():
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
 
 
+def test_chained_launches_keep_stream_order_over_reused_memory():
+    """The cache write, the preps and the forward are launched as
+    programmatic dependents of the launch before them.  Memory that a
+    caching allocator hands out again on the same stream must still see
+    plain stream order: (1) the cache write reads f32 leaves from a buffer
+    freed right after the call, and the forward's workspace is then carved
+    from that memory (the prep writes it); (2) the forward reads V from a
+    buffer freed right after the call, and the backward's workspace is then
+    carved from it (the forward lets the backward's prep launch once its
+    loads are issued).  Both must give the fresh-buffer results bit for bit."""
+    s = _shape("reused_mem", 2, 256, 8, 2, 128, 300, seed=114)
+    g = gh.to_gpu(synth.train_inputs(s))
+    geom = cartattn.geom(s.B, s.n, s.Hq, s.Hkv, s.d, s.p, s.frozen_prefix, None, s.theta)
+    wf = cartattn.fwd_workspace_size(geom, cartattn.CART_BF16, cartattn.CART_BF16)
+    wb = cartattn.bwd_reuse_workspace_size(geom, cartattn.CART_BF16, cartattn.CART_BF16)
+    kcb = torch.empty(g["kc"].shape, dtype=torch.bfloat16, device="cuda")
+    vcb = torch.empty_like(kcb)
+    cartattn.cart_write_to_cache(g["kc"], g["vc"], kcb, vcb)
+    ws_f = torch.empty(wf, dtype=torch.uint8, device="cuda")
+    o_ref, lse_ref = cartattn.cart_attn_fwd(g["q"], g["k"], g["v"], kcb, vcb, theta=s.theta,
+                                            workspace=ws_f)
+    grads_ref = cartattn.cart_attn_bwd(g["q"], g["k"], g["v"], kcb, vcb, o_ref, lse_ref, g["do"],
+                                       theta=s.theta, fwd_workspace=ws_f,
+                                       workspace=torch.empty(wb, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    del ws_f
+    nkc = g["kc"].numel()
+    assert 2 * nkc * 4 <= wf
+    nbv = max(wb, g["v"].numel() * 2)  # (a workspace may be larger than needed)
+    reused = [0, 0]
+    for _ in range(4):
+        # (1) the leaves' f32 copies at the start of a block the size of the
+        # forward's workspace, freed once the cache write is enqueued
+        blk = torch.empty(wf, dtype=torch.uint8, device="cuda")
+        leaves = blk[: 2 * nkc * 4].view(torch.float32)
+        leaves[:nkc].copy_(g["kc"].reshape(-1))
+        leaves[nkc:].copy_(g["vc"].reshape(-1))
+        kcb2, vcb2 = torch.empty_like(kcb), torch.empty_like(vcb)
+        cartattn.cart_write_to_cache(leaves[:nkc].view(g["kc"].shape),
+                                     leaves[nkc:].view(g["vc"].shape), kcb2, vcb2)
+        addr = blk.data_ptr()
+        del leaves, blk
+        ws_f = torch.empty(wf, dtype=torch.uint8, device="cuda")
+        reused[0] += ws_f.data_ptr() == addr
+        # (2) V copied into a block, freed once the forward is enqueued; the
+        # backward's workspace is a block of the same size
+        blk = torch.empty(nbv, dtype=torch.uint8, device="cuda")
+        v_tmp = blk[: g["v"].numel() * 2].view(torch.bfloat16).view(g["v"].shape)
+        v_tmp.copy_(g["v"])
+        o, lse = cartattn.cart_attn_fwd(g["q"], g["k"], v_tmp, kcb2, vcb2, theta=s.theta,
+                                        workspace=ws_f)
+        addr = blk.data_ptr()
+        del v_tmp, blk
+        ws_b = torch.empty(nbv, dtype=torch.uint8, device="cuda")
+        reused[1] += ws_b.data_ptr() == addr
+        grads = cartattn.cart_attn_bwd(g["q"], g["k"], g["v"], kcb2, vcb2, o, lse, g["do"],
+                                       theta=s.theta, fwd_workspace=ws_f, workspace=ws_b)
+        torch.cuda.synchronize()
+        assert cartattn.device_status(clear=True) == 0
+        assert torch.equal(kcb2.view(torch.uint8), kcb.view(torch.uint8))
+        assert torch.equal(o.view(torch.uint8), o_ref.view(torch.uint8))
+        assert torch.equal(lse, lse_ref)
+        for nme, x, y in zip(("dq", "dk", "dv", "dkc", "dvc"), grads, grads_ref):
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), nme
+        del ws_f, ws_b
+    # the allocator did hand the freed blocks out again (else nothing was tested)
+    assert reused[0] > 0 and reused[1] > 0, reused
+
+
 def test_cache_write_bitwise():
     rng = np.random.default_rng(7)
     p, Hkv, d = 300, 4, 128
