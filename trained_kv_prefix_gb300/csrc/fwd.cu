@@ -1,10 +1,12 @@
 // fwd.cu -- tcgen05 forward of cartridge attention (sm_103a).
 //
-// A work item is two 128-row query tiles, A and B, that see the same keys:
-// consecutive row tiles of one (sequence, head) in training, the two halves
-// of a kv head's stacked decode rows in decode mode.  Training CTAs are
-// persistent (one per SM) and take items heaviest first from a counter;
-// a decode CTA runs one item.  Both tiles of an item walk the key tiles
+// A work item is two 128-row query tiles, A and B, that stream the same
+// keys: in fixed-layout training with an even group size, the same query
+// tile of two heads of one kv group (both see exactly the same key tiles);
+// otherwise in training, consecutive row tiles of one (sequence, head); in
+// decode mode, the two halves of a kv head's stacked decode rows.  Training
+// CTAs are persistent (one per SM) and follow a static plan (fixed layout)
+// or take items heaviest first from a counter; a decode CTA runs one item.  Both tiles of an item walk the key tiles
 // of concat(cartridge rows, real tokens) -- first every cartridge tile (all
 // visible), then the real-token tiles up to their diagonal (end-aligned
 // causal mask: real key j is visible from query i iff j <= i; Cartridges
@@ -255,10 +257,11 @@ __device__ __forceinline__ void item_tiles(const FwdParams& a, FwdItem& I, int w
   I.T = max(I.T_A, I.T_B);
 }
 
-// Training work item w: items are numbered heaviest first (the pair index
-// falls as w grows; every pair of a sequence sees all cartridge tiles and
-// the later pairs more real tiles), so CTAs that take the next free item
-// form a longest-first schedule.
+// Training work item w: items are numbered heaviest first (the query tile,
+// or pair of tiles, falls as w grows; every item of a sequence sees all
+// cartridge tiles and the later ones more real tiles), so CTAs that take the
+// next free item form a longest-first schedule.  Cross items (may_cross and
+// a.cross): (query tile, sequence, head pair); else (pair, sequence, head).
 __device__ __forceinline__ FwdItem train_item(const FwdParams& a, int w, const int* cu,
                                               int window, bool may_cross) {
   FwdItem I;

@@ -271,8 +271,9 @@ struct FwdLaunch {
   int total = 0;
   int window = 0;          // sliding window in keys (0: none)
 };
-// Two 128-row query tiles per CTA (training: consecutive row tiles of one
-// (sequence, head); decode: rows 0-127 / 128-255 of a kv head's stacked rows).
+// Two 128-row query tiles per work item (training: one query tile of two
+// heads of a kv group, or consecutive row tiles of one (sequence, head);
+// decode: rows 0-127 / 128-255 of a kv head's stacked rows).
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 
 // ------------------------------------------------------------ backward ----
