@@ -297,6 +297,35 @@ def test_backward_is_deterministic():
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_f32_leaves_equal_cache_write_then_bf16_path(d):
+    """Given f32 cartridge leaves, the forward's prep launch writes their
+    bf16 copy itself.  That copy must be the bytes cart_write_to_cache
+    writes (round to nearest even, pinned bit for bit elsewhere): the
+    forward and the backward that reads the forward's workspace must then
+    equal the bf16-cartridge path fed by cart_write_to_cache, bit for bit."""
+    s = _shape(f"leaves_d{d}", 2, 200, 8, 2, d, 333, seed=115)
+    g = gh.to_gpu(synth.train_inputs(s))
+    assert g["kc"].dtype == torch.float32
+    geom = cartattn.geom(s.B, s.n, s.Hq, s.Hkv, s.d, s.p, s.frozen_prefix, None, s.theta)
+    kcb = torch.empty(g["kc"].shape, dtype=torch.bfloat16, device="cuda")
+    vcb = torch.empty_like(kcb)
+    cartattn.cart_write_to_cache(g["kc"], g["vc"], kcb, vcb)
+    runs = []
+    for kc, vc, cd in ((g["kc"], g["vc"], cartattn.CART_F32), (kcb, vcb, cartattn.CART_BF16)):
+        ws = torch.empty(cartattn.fwd_workspace_size(geom, cartattn.CART_BF16, cd),
+                         dtype=torch.uint8, device="cuda")
+        o, lse = cartattn.cart_attn_fwd(g["q"], g["k"], g["v"], kc, vc, theta=s.theta,
+                                        workspace=ws)
+        grads = cartattn.cart_attn_bwd(g["q"], g["k"], g["v"], kc, vc, o, lse, g["do"],
+                                       theta=s.theta, fwd_workspace=ws)
+        runs.append((o, lse) + tuple(grads))
+    torch.cuda.synchronize()
+    assert cartattn.device_status(clear=True) == 0
+    for nme, x, y in zip(("o", "lse", "dq", "dk", "dv", "dkc", "dvc"), *runs):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), nme
+
+
 def test_chained_launches_keep_stream_order_over_reused_memory():
     """The cache write, the preps and the forward are launched as
     programmatic dependents of the launch before them.  Memory that a
